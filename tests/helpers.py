@@ -1,0 +1,108 @@
+"""Shared test utilities: the error metrics and an fp64 dense restatement of the layer.
+
+The dense restatement is deliberately different from the oracle's per-token
+loops: it evaluates every expert on every token with ``torch.einsum`` in
+float64 and masks the result with the dense gate matrix G[t, e] (zero off the
+selected k).  It is the brute-force check the oracle is pinned against; it
+calls nothing in ``oracle/``.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+# Pass bar of the CUDA path against the oracle, per output tensor.
+MAX_REL_TOL = 2e-2
+MEAN_REL_TOL = 1e-2
+
+
+def bf16_to_f64(a: np.ndarray) -> np.ndarray:
+    return (np.asarray(a, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def rel_errors(got, ref) -> tuple[float, float]:
+    """(max_rel, mean_rel) of ``got`` against ``ref``.
+
+    max_rel  = max_i |g_i - r_i| / max(|r_i|, rms(r))   (floor at rms keeps near-zero
+               entries from dominating)
+    mean_rel = sum |g - r| / sum |r|
+    """
+    g = np.asarray(got, dtype=np.float64).ravel()
+    r = np.asarray(ref, dtype=np.float64).ravel()
+    if r.size == 0:
+        return 0.0, 0.0
+    d = np.abs(g - r)
+    if not np.all(np.isfinite(d)):
+        return float("inf"), float("inf")
+    rms = float(np.sqrt(np.mean(r * r)))
+    s = float(np.sum(np.abs(r)))
+    if s == 0.0:
+        m = float(d.max())
+        return m, m
+    denom = np.maximum(np.abs(r), rms)
+    return float(np.max(d / denom)), float(np.sum(d) / s)
+
+
+def rel_errors_per_expert(got, ref) -> tuple[float, float]:
+    """Metrics for weight gradients [E, ...]: max_rel uses each expert's own rms as the floor.
+
+    Expert gradients differ in scale by the square root of their row counts
+    (strongly so under skewed routing), so one tensor-wide rms floor would
+    judge a heavy expert's near-zero entries against a light expert's scale.
+    mean_rel stays tensor-wide.
+    """
+    g = np.asarray(got, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    mx = max((rel_errors(g[e], r[e])[0] for e in range(r.shape[0])), default=0.0)
+    return mx, rel_errors(g, r)[1]
+
+
+def assert_close(got, ref, name, max_rel=MAX_REL_TOL, mean_rel=MEAN_REL_TOL, per_expert=False):
+    mx, mn = (rel_errors_per_expert if per_expert else rel_errors)(got, ref)
+    assert mx <= max_rel and mn <= mean_rel, f"{name}: max_rel={mx:.3e} (tol {max_rel}) mean_rel={mn:.3e} (tol {mean_rel})"
+    return mx, mn
+
+
+def topk_bruteforce(logits: np.ndarray, k: int) -> np.ndarray:
+    """Selected experts per token: full sort by (logit descending, id ascending)."""
+    T, E = logits.shape
+    out = np.empty((T, k), np.int32)
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-float(logits[t, e]), e))
+        out[t] = order[:k]
+    return out
+
+
+def dense_layer_fp64(x_bits, wgu_bits, wd_bits, logits, sel, requires_grad=False):
+    """fp64 dense evaluation of the routed SwiGLU layer.
+
+    Y[t, c] = sum_e G[t, e] * sum_n silu(g[t,e,n]) * u[t,e,n] * Wd[e, c, n]
+    with g = x Wgu[e, :I]^T, u = x Wgu[e, I:]^T and G = softmax over the
+    selected logits (zero elsewhere).  Returns (Y, leaves) with leaves the
+    tensors gradients can be taken against (x, wgu, wd, logits).
+    """
+    x = torch.tensor(bf16_to_f64(x_bits), requires_grad=requires_grad)
+    wgu = torch.tensor(bf16_to_f64(wgu_bits), requires_grad=requires_grad)
+    wd = torch.tensor(bf16_to_f64(wd_bits), requires_grad=requires_grad)
+    lg = torch.tensor(np.asarray(logits, dtype=np.float64), requires_grad=requires_grad)
+    T, E = lg.shape
+    I = wgu.shape[1] // 2
+    mask = torch.zeros((T, E), dtype=torch.bool)
+    mask[torch.arange(T)[:, None], torch.tensor(sel, dtype=torch.long)] = True
+    G = torch.softmax(lg.masked_fill(~mask, float("-inf")), dim=1)
+    gu = torch.einsum("th,enh->ten", x, wgu)
+    a = torch.nn.functional.silu(gu[..., :I]) * gu[..., I:]
+    o = torch.einsum("ten,ecn->tec", a, wd)
+    Y = torch.einsum("te,tec->tc", G, o)
+    return Y, dict(x=x, wgu=wgu, wd=wd, logits=lg, G=G)
+
+
+def dense_swiglu_mlp_fp64(x_bits, wgu_e_bits, wd_e_bits):
+    """One dense SwiGLU MLP, down(silu(gate x) * up x), in fp64 (Liger's SwiGLU MLP form)."""
+    x = torch.tensor(bf16_to_f64(x_bits))
+    wgu = torch.tensor(bf16_to_f64(wgu_e_bits))
+    wd = torch.tensor(bf16_to_f64(wd_e_bits))
+    I = wgu.shape[0] // 2
+    gate = x @ wgu[:I].T
+    up = x @ wgu[I:].T
+    return (torch.nn.functional.silu(gate) * up) @ wd.T

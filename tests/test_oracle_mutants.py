@@ -1,0 +1,81 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in a temporary copy of the oracle source (never
+in the real one), compiles it on the CPU, and runs the pin battery of
+test_oracle_route / _dispatch / _layer against it: at least one pin must fail.
+"""
+import os
+import shutil
+
+import pytest
+
+import oracle
+from tests import test_oracle_dispatch as P_D
+from tests import test_oracle_layer as P_L
+from tests import test_oracle_route as P_R
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.cpp")
+
+MUTANTS = {
+    "tie_break_reversed": ("return ia < ib;", "return ia > ib;"),
+    "nan_ranked_first": ("if (na != nb) return nb;", "if (na != nb) return na;"),
+    "softmax_drops_first_term": ("for (int j = 0; j < k; ++j) {\n      ex[j] = std::exp(l[order[j]] - m);\n      s += ex[j];",
+                                 "for (int j = 0; j < k; ++j) {\n      ex[j] = std::exp(l[order[j]] - m);\n      if (j) s += ex[j];"),
+    "dispatch_not_stable": ("for (long long s = 0; s < R; ++s) {\n    int e = ids[s];",
+                            "for (long long s = R - 1; s >= 0; --s) {\n    int e = ids[s];"),
+    "gate_up_rows_swapped": ("const uint16_t* wg = wgu_e + static_cast<size_t>(n) * H;\n    const uint16_t* wu = wgu_e + static_cast<size_t>(I + n) * H;",
+                             "const uint16_t* wu = wgu_e + static_cast<size_t>(n) * H;\n    const uint16_t* wg = wgu_e + static_cast<size_t>(I + n) * H;"),
+    "silu_sign": ("inline float silu(float a) { return a / (1.0f + std::exp(-a)); }",
+                  "inline float silu(float a) { return a / (1.0f + std::exp(a)); }"),
+    "down_transposed": ("for (int n = 0; n < I; ++n) a += hq[n] * bf16_to_float(wr[n]);",
+                        "for (int n = 0; n < I; ++n) a += hq[n] * bf16_to_float(wd_e[static_cast<size_t>(n) * H + c]);"),
+    "combine_weight_dropped": ("acc[c] += round_to_bf16(wj * o[c]);", "acc[c] += round_to_bf16(o[c]);"),
+    "grouped_weight_dropped": ("float_to_bf16(w_perm[r] * o[c]);", "float_to_bf16(o[c]);"),
+    "swiglu_grad_sign": ("dg[n] = ((dh * u[n]) * s) * (1.0f + g[n] * (1.0f - s));",
+                         "dg[n] = ((dh * u[n]) * s) * (1.0f - g[n] * (1.0f - s));"),
+    "dx_up_term_dropped": ("          acc[h] += du[n] * bf16_to_float(wu[h]);\n", ""),
+    "router_grad_sign": ("dl[ids[static_cast<size_t>(t) * k + j]] = wj * (gam[j] - S);",
+                         "dl[ids[static_cast<size_t>(t) * k + j]] = wj * (gam[j] + S);"),
+    "router_grad_unweighted_gamma": ("for (int j = 0; j < k; ++j) S += w[static_cast<size_t>(t) * k + j] * gam[j];",
+                                     "for (int j = 0; j < k; ++j) S += gam[j];"),
+    "dwd_weight_dropped": ("float wdy = wj * bf16_to_float(dyr[c]);", "float wdy = bf16_to_float(dyr[c]);"),
+    "dwgu_wrong_input_row": ("float xv = bf16_to_float(xr[h]);\n            rg[h]",
+                             "float xv = bf16_to_float(dyr[h]);\n            rg[h]"),
+    "dhu_reads_gate_weights": ("const uint16_t* wr = wd_e + static_cast<size_t>(c) * I;\n    for (int n = 0; n < I; ++n) dHu[n]",
+                               "const uint16_t* wr = wd_e + static_cast<size_t>(c) * I + 1;\n    for (int n = 0; n < I - 1; ++n) dHu[n]"),
+}
+
+
+def _battery():
+    """Every pin that can be run as a plain call, on the current oracle build."""
+    P_R.test_ids_match_bruteforce_sort(50, 37, 5, True)
+    P_R.test_weights_are_renormalised_softmax(40, 64, 6)
+    P_R.test_nan_logits_rank_last_and_ids_distinct()
+    P_R.test_closed_form_worked_example()
+    P_D.test_matches_stable_argsort(300, 37, 5, 0.3)
+    for wl in (P_L.TINY, P_L.RAGGED, P_L.ZIPF):
+        P_L.test_forward_matches_fp64_dense(wl)
+        P_L.test_forward_is_dispatch_grouped_combine(wl)
+        P_L.test_backward_matches_fp64_autograd(wl)
+    P_L.test_router_gradient_by_central_differences()
+    P_L.test_weight_gradient_by_central_differences()
+    P_L.test_identity_expert_roundtrip()
+    P_L.test_closed_form_worked_example()
+
+
+def test_battery_passes_on_the_real_oracle():
+    _battery()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    before, after = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(before) == 1, f"mutation anchor for {name} not found exactly once"
+    path = tmp_path / "mutant.cpp"
+    path.write_text(src.replace(before, after))
+    lib = oracle.open_library(oracle.compile_source(str(path), str(tmp_path / "libmutant.so")))
+    with oracle.using(lib):
+        with pytest.raises((AssertionError, ValueError)):
+            _battery()
+    shutil.rmtree(tmp_path, ignore_errors=True)
