@@ -1,0 +1,211 @@
+/*
+ * liger_moe.h -- C ABI of the routed Mixture-of-Experts layer on one GPU
+ * (forward and backward), hand-written CUDA for sm_103a (GB300).
+ *
+ * The layer, per token t with router logits l[t, 0..E-1] and input x[t, :]:
+ *   route     ids[t, 0..k-1] = the k largest logits (ties -> smaller id),
+ *             w[t, j] = softmax of the k selected logits
+ *   dispatch  slots s = t*k + j sorted stably by expert -> expert-major rows
+ *   experts   per row r of expert e:  g = x W_gu[e, :I]^T,  u = x W_gu[e, I:]^T,
+ *             h = bf16(silu(g) * u),   y = bf16(w * (h W_d[e]^T))
+ *   combine   Y[t] = bf16(sum_j y[row of slot (t, j)])
+ *   backward  dX, dW_gate_up, dW_down and d_logits of L = <dY, Y>.
+ * Sources: LightMoE README ("MoE inference": dispatch, gate/up projection,
+ * gated activation, down projection, routing-weight application,
+ * deterministic combine; "MoE training": MoEDispatch outputs, input-, weight-
+ * and router-gradient kernels; "Grouped GEMM": expert-major rows, m_indptr
+ * int32 [E+1], empty experts valid; "Limits": K aligned to 64), LigerCute
+ * README ("LigerMoE design": forward sorts routed tokens, final local combine
+ * applies router weights; backward recomputes activations, computes dX and
+ * dW, reduces routed dX to tokens) and the LigerCute PR summary (a flat
+ * extern "C" boundary with no torch types; BF16).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers, row-major and contiguous.
+ *     bf16 tensors are passed as void* (IEEE bfloat16 bit patterns).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *     Every call only enqueues work on `stream`: it never synchronises, never
+ *     allocates device memory and never frees anything.
+ *   - The caller owns every buffer.  Outputs are overwritten, never
+ *     accumulated into.  Buffers of one call must not overlap unless stated.
+ *   - bf16 buffers must be 16-byte aligned; H and I must be multiples of 64.
+ *   - Limits: 1 <= E <= 1024; 1 <= k <= min(E, 32); T >= 0;
+ *     T*k, E*2I and E*H below 2^31.  T = 0 is valid and launches nothing.
+ *   - Entry points that take `workspace` report its size: called with
+ *     workspace == NULL they store the required byte count in
+ *     *workspace_bytes, validate the other arguments and launch nothing.
+ *     Otherwise *workspace_bytes is the size of the caller's buffer (256-byte
+ *     aligned device memory) and must be at least the reported size.
+ *   - Argument errors are reported before anything is launched.  Errors the
+ *     device finds (an expert id outside [0, E), a row index outside [0, R),
+ *     an internal pipeline wait that ran past its time limit) set a flag that
+ *     liger_moe_device_error() returns; outputs of that call are unspecified.
+ *   - Only devices of compute capability 10.3 (sm_103) are supported.
+ */
+#ifndef LIGER_MOE_H_
+#define LIGER_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+typedef enum {
+  LIGER_MOE_OK = 0,
+  LIGER_MOE_ERR_INVALID_ARG = -1,        /* null pointer, k > E, negative size, ... */
+  LIGER_MOE_ERR_MISALIGNED = -2,         /* H or I not a multiple of 64, pointer not 16-byte aligned */
+  LIGER_MOE_ERR_CAPACITY = -3,           /* workspace too small, or a size above a stated limit */
+  LIGER_MOE_ERR_UNSUPPORTED_DEVICE = -4, /* current device is not sm_103 */
+  LIGER_MOE_ERR_LAUNCH = -5,             /* a CUDA call failed (see liger_moe_last_cuda_error) */
+  LIGER_MOE_ERR_DEVICE = -6              /* returned by liger_moe_device_error when a flag is set */
+} liger_moe_status;
+
+/* Bits of the device error flag. */
+#define LIGER_MOE_DEVERR_BAD_EXPERT_ID 0x1 /* topk_ids entry outside [0, E) */
+#define LIGER_MOE_DEVERR_BAD_ROW 0x2       /* row / slot index outside [0, T*k) */
+#define LIGER_MOE_DEVERR_BAD_INDPTR 0x4    /* m_indptr not 0 = m[0] <= ... <= m[E] = R */
+#define LIGER_MOE_DEVERR_WAIT_TIMEOUT 0x8  /* a pipeline wait inside a GEMM kernel gave up */
+
+/*
+ * Router: top-k experts and renormalised gate weights per token.
+ * LightMoE README, "MoE inference" (top_k_ids int32, distinct per token;
+ * top_k_weights float32) and "MoE training" (differentiable_probs).
+ *   logits    [T, E] float32, input.
+ *   topk_ids  [T, k] int32, output: experts by descending logit; equal logits
+ *             -> smaller id first; NaN ranks below every number (by id).
+ *             -0.0 and +0.0 are equal.
+ *   topk_w    [T, k] float32, output: w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0)
+ *             over the selected k (softmax over E, top-k, renormalised).
+ * No workspace.  Bit-exact ids for a given logits tensor.
+ */
+int liger_moe_route_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
+                         void* stream);
+
+/*
+ * Dispatch: deterministic expert-major order of the R = T*k routed slots
+ * (slot s = t*k + j).  Rows of expert e are m_indptr[e] .. m_indptr[e+1]-1,
+ * in slot order (a stable counting sort: histogram, prefix scan, stable
+ * scatter).  LightMoE README, "MoE training" (gather_indices, m_indptr,
+ * routing_weights, inverse_slots) and "Grouped GEMM"; LigerCute README,
+ * "Forward pass" (routed tokens are sorted and copied before the expert loop).
+ *   topk_ids     [T, k] int32, input, entries in [0, E).
+ *   topk_w       [T, k] float32, input; may be NULL when w_perm is NULL.
+ *   x            [T, H] bf16, input; may be NULL when x_perm is NULL.
+ *   counts       [E] int32, output: rows per expert.
+ *   m_indptr     [E+1] int32, output: exclusive prefix sum of counts.
+ *   row_to_slot  [R] int32, output: slot of each row.
+ *   slot_to_row  [R] int32, output: row of each slot (the inverse).
+ *   w_perm       [R] float32, output or NULL: topk_w of each row's slot.
+ *   x_perm       [R, H] bf16, output or NULL: x[row_to_slot[r] / k].
+ * Workspace: per-chunk expert histograms (a few hundred KB at R = 82k, E = 512).
+ * Integer outputs are bit-exact and independent of the launch.
+ */
+int liger_moe_dispatch(const int32_t* topk_ids, const float* topk_w, const void* x, int T, int H, int E,
+                       int k, int32_t* counts, int32_t* m_indptr, int32_t* row_to_slot,
+                       int32_t* slot_to_row, float* w_perm, void* x_perm, void* workspace,
+                       size_t* workspace_bytes, void* stream);
+
+/*
+ * Grouped SwiGLU expert MLP on expert-major rows, with the routing weight
+ * applied to the down projection.  LightMoE README, "Grouped GEMM"
+ * (out = a[rows_e] @ b[e]^T, b laid out [num_experts, N, K]) and "MoE
+ * inference" (gate/up projection, gated activation, down projection,
+ * routing-weight application); LigerCute README, "Forward pass".
+ *   x_perm     [R, H] bf16, input (rows in expert-major order).
+ *   m_indptr   [E+1] int32, input, as produced by liger_moe_dispatch.
+ *   w_gate_up  [E, 2I, H] bf16: rows [0, I) gate, rows [I, 2I) up.
+ *   w_down     [E, H, I] bf16.
+ *   w_perm     [R] float32: routing weight of each row.
+ *   h_perm     [R, I] bf16, output: h = bf16(silu(g) * u)  (saved for backward).
+ *   gu_perm    [R, 2I] float32, output or NULL: [g | u], the fp32 accumulators
+ *              (saved for backward; when NULL the backward recomputes them).
+ *   y_perm     [R, H] bf16, output: bf16(w_perm[r] * (h W_d[e]^T)).
+ * fp32 accumulation on the tensor cores.  Workspace: the tile schedule
+ * (4*(E+1) bytes, rounded up).
+ */
+int liger_moe_grouped_swiglu_fwd(const void* x_perm, const int32_t* m_indptr, const void* w_gate_up,
+                                 const void* w_down, const float* w_perm, int R, int H, int I, int E,
+                                 void* h_perm, float* gu_perm, void* y_perm, void* workspace,
+                                 size_t* workspace_bytes, void* stream);
+
+/*
+ * Combine: routed rows back to token order.  LigerCute README, "Forward
+ * pass" (final local combine); LightMoE README, "Highlights" (deterministic
+ * combine).
+ *   y_perm       [R, H] bf16, input (already weighted).
+ *   slot_to_row  [R] int32, input.
+ *   y            [T, H] bf16, output: bf16( sum_{j=0..k-1} y_perm[slot_to_row[t*k+j]] ),
+ *                float sum in j order (deterministic).
+ * No workspace.
+ */
+int liger_moe_combine(const void* y_perm, const int32_t* slot_to_row, int T, int H, int k, void* y,
+                      void* stream);
+
+/*
+ * Backward of the whole layer for L = <dY, Y>.  LigerCute README, "Backward
+ * pass" (expert-output gradients, recomputed activations, input and weight
+ * gradients, routed dX reduced back to tokens); LightMoE README, "MoE
+ * training" (deterministic input-, weight- and router-gradient kernels).
+ * Inputs are the forward's saved state:
+ *   dy [T, H] bf16; x_perm [R, H] bf16; h_perm [R, I] bf16;
+ *   gu_perm [R, 2I] float32 or NULL (then g, u are recomputed from x_perm);
+ *   topk_ids, topk_w [T, k]; m_indptr [E+1]; row_to_slot, slot_to_row [R];
+ *   w_perm [R]; w_gate_up [E, 2I, H]; w_down [E, H, I].
+ * Outputs (overwritten):
+ *   dx          [T, H] bf16      sum over the token's k rows of dgu W_gu[e]
+ *   dw_gate_up  [E, 2I, H] bf16  sum over expert rows of dgu^T x (zero for empty experts)
+ *   dw_down     [E, H, I] bf16   sum over expert rows of (w dY)^T h
+ *   d_logits    [T, E] float32   w_j (gamma_j - sum_i w_i gamma_i) at the selected
+ *                                experts, gamma_j = <dY, expert-j output>; 0 elsewhere
+ * Weight gradients are summed in a fixed order (no atomics): results are
+ * identical from run to run.  The upstream gradient enters the expert GEMMs
+ * unscaled; the routing weight is applied in fp32 to the dH accumulator, and
+ * bf16(w * h) is the second operand of dW_down.  Workspace: about
+ * R*(2H + 3I)*2 bytes, plus R*2I*4 more when gu_perm is NULL.
+ */
+int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const void* h_perm, const float* gu_perm,
+                        const int32_t* topk_ids, const float* topk_w, const int32_t* m_indptr,
+                        const int32_t* row_to_slot, const int32_t* slot_to_row, const float* w_perm,
+                        const void* w_gate_up, const void* w_down, int T, int H, int I, int E, int k,
+                        void* dx, void* dw_gate_up, void* dw_down, float* d_logits, void* workspace,
+                        size_t* workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then returns LIGER_MOE_OK and *flags = 0 when no
+ * device error was recorded on the current device since the last call, or
+ * LIGER_MOE_ERR_DEVICE with *flags = the LIGER_MOE_DEVERR_* bits.  The flag
+ * is cleared.  Returns LIGER_MOE_ERR_LAUNCH if the synchronisation failed.
+ */
+int liger_moe_device_error(void* stream, int* flags);
+
+/*
+ * Kernel trace (diagnostics; off by default).  While enabled, every kernel
+ * this library launches is bracketed by two CUDA events recorded on the
+ * launch stream, giving its device-side duration without a profiler.
+ *   liger_moe_trace_enable(on)   turns tracing on or off and clears the log
+ *   liger_moe_trace_count()      number of launches logged
+ *   liger_moe_trace_get(i, ...)  kernel name (static string) and duration in ms
+ *                                of launch i; waits for that launch to finish
+ * Host-side cost: two cudaEventRecord calls per launch while enabled.
+ */
+int liger_moe_trace_enable(int on);
+int liger_moe_trace_count(void);
+int liger_moe_trace_get(int i, const char** name, float* ms);
+
+/* Text of the last CUDA error seen by this library in this thread ("" if none). */
+const char* liger_moe_last_cuda_error(void);
+
+/* Name of a liger_moe_status value. */
+const char* liger_moe_status_string(int status);
+
+/* ABI version (major * 100 + minor). */
+int liger_moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIGER_MOE_H_ */

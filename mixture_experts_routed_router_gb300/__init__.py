@@ -1,0 +1,284 @@
+"""Routed Mixture-of-Experts layer (forward + backward) on one GB300: Python binding.
+
+Every computation runs in ``libliger_moe.so`` (hand-written CUDA for sm_103a,
+see ``include/liger_moe.h``).  This module only checks tensor dtypes, shapes
+and devices, allocates outputs with PyTorch when the caller does not pass
+them, and calls the C entry points of the same names on the current CUDA
+stream.  There is no fallback: without the library, or without an sm_103
+device, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = ["route_topk", "dispatch", "grouped_swiglu_fwd", "combine", "bwd_dx_dw", "device_error",
+           "workspace_bytes", "trace_enable", "trace_records", "LigerMoEError", "library_path", "load_library"]
+
+_lock = threading.Lock()
+_lib = None
+
+OK = 0
+STATUS = {0: "OK", -1: "INVALID_ARG", -2: "MISALIGNED", -3: "CAPACITY", -4: "UNSUPPORTED_DEVICE", -5: "LAUNCH",
+          -6: "DEVICE"}
+DEVERR = {0x1: "BAD_EXPERT_ID", 0x2: "BAD_ROW", 0x4: "BAD_INDPTR", 0x8: "WAIT_TIMEOUT"}
+
+
+class LigerMoEError(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}{(' (' + detail + ')') if detail else ''}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = True):
+    """Loads libliger_moe.so (building it with nvcc first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build() if build_if_missing else _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libliger_moe.so not found at {path}")
+        lib = ctypes.CDLL(path)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)
+        lib.liger_moe_route_topk.argtypes = [P, I, I, I, P, P, P]
+        lib.liger_moe_dispatch.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, P, S, P]
+        lib.liger_moe_grouped_swiglu_fwd.argtypes = [P, P, P, P, P, I, I, I, I, P, P, P, P, S, P]
+        lib.liger_moe_combine.argtypes = [P, P, I, I, I, P, P]
+        lib.liger_moe_bwd_dx_dw.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, P, S, P]
+        lib.liger_moe_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
+        lib.liger_moe_trace_enable.argtypes = [I]
+        lib.liger_moe_trace_get.argtypes = [I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)]
+        lib.liger_moe_last_cuda_error.restype = ctypes.c_char_p
+        lib.liger_moe_status_string.restype = ctypes.c_char_p
+        lib.liger_moe_status_string.argtypes = [I]
+        for f in (lib.liger_moe_route_topk, lib.liger_moe_dispatch, lib.liger_moe_grouped_swiglu_fwd,
+                  lib.liger_moe_combine, lib.liger_moe_bwd_dx_dw, lib.liger_moe_device_error,
+                  lib.liger_moe_abi_version, lib.liger_moe_trace_enable, lib.liger_moe_trace_count,
+                  lib.liger_moe_trace_get):
+            f.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, rc: int):
+    if rc != OK:
+        lib = load_library()
+        raise LigerMoEError(fn, rc, lib.liger_moe_last_cuda_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+def _out(t, name, dtype, shape, device):
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    return _need(t, name, dtype, shape)
+
+
+def _workspace(ws, nbytes, device):
+    if ws is None:
+        return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    _need(ws, "workspace", torch.uint8)
+    if ws.numel() < nbytes:
+        raise ValueError(f"workspace has {ws.numel()} bytes, {nbytes} needed")
+    return ws
+
+
+def route_topk(logits, k, *, topk_ids=None, topk_w=None, stream=None):
+    """(topk_ids int32 [T,k], topk_w float32 [T,k]) from logits float32 [T,E]."""
+    lib = load_library()
+    _need(logits, "logits", torch.float32)
+    T, E = logits.shape
+    topk_ids = _out(topk_ids, "topk_ids", torch.int32, (T, k), logits.device)
+    topk_w = _out(topk_w, "topk_w", torch.float32, (T, k), logits.device)
+    _check("liger_moe_route_topk", lib.liger_moe_route_topk(_ptr(logits), T, E, k, _ptr(topk_ids), _ptr(topk_w),
+                                                            _stream(stream)))
+    return topk_ids, topk_w
+
+
+def workspace_bytes(fn: str, **kw) -> int:
+    """Workspace size an entry point needs (query call: nothing is launched)."""
+    lib = load_library()
+    n = ctypes.c_size_t(0)
+    d = ctypes.c_void_p(256)  # stand-in pointers: a query validates arguments but never dereferences them
+    if fn == "dispatch":
+        T, E, k = kw["T"], kw["E"], kw["k"]
+        rc = lib.liger_moe_dispatch(d, None, None, T, 0, E, k, d, d, d, d, None, None, None, ctypes.byref(n), None)
+    elif fn == "grouped_swiglu_fwd":
+        R, H, I, E = kw["R"], kw["H"], kw["I"], kw["E"]
+        p = None if R == 0 else ctypes.c_void_p(256)
+        rc = lib.liger_moe_grouped_swiglu_fwd(p, ctypes.c_void_p(256), p, p, p, R, H, I, E, p, None, p, None,
+                                              ctypes.byref(n), None)
+    elif fn == "bwd_dx_dw":
+        T, H, I, E, k = kw["T"], kw["H"], kw["I"], kw["E"], kw["k"]
+        p = ctypes.c_void_p(256)
+        q = None if T * k == 0 else p
+        gu = p if kw.get("saved_gu", True) else None
+        rc = lib.liger_moe_bwd_dx_dw(q, q, q, gu, q, q, p, q, q, q, p, p, T, H, I, E, k, q, p, p, q, None,
+                                     ctypes.byref(n), None)
+    else:
+        raise ValueError(fn)
+    _check(f"workspace query ({fn})", rc)
+    return n.value
+
+
+def dispatch(topk_ids, topk_w, x, num_experts, *, out=None, workspace=None, stream=None):
+    """Deterministic expert-major dispatch.
+
+    Returns dict(counts, m_indptr, row_to_slot, slot_to_row, w_perm, x_perm); w_perm / x_perm
+    are None when topk_w / x is None.
+    """
+    lib = load_library()
+    _need(topk_ids, "topk_ids", torch.int32)
+    T, k = topk_ids.shape
+    R, E, dev = T * k, num_experts, topk_ids.device
+    H = 0 if x is None else x.shape[1]
+    if topk_w is not None:
+        _need(topk_w, "topk_w", torch.float32, (T, k))
+    if x is not None:
+        _need(x, "x", torch.bfloat16, (T, H))
+    out = dict(out or {})
+    o = dict(counts=_out(out.get("counts"), "counts", torch.int32, (E,), dev),
+             m_indptr=_out(out.get("m_indptr"), "m_indptr", torch.int32, (E + 1,), dev),
+             row_to_slot=_out(out.get("row_to_slot"), "row_to_slot", torch.int32, (R,), dev),
+             slot_to_row=_out(out.get("slot_to_row"), "slot_to_row", torch.int32, (R,), dev),
+             w_perm=None if topk_w is None else _out(out.get("w_perm"), "w_perm", torch.float32, (R,), dev),
+             x_perm=None if x is None else _out(out.get("x_perm"), "x_perm", torch.bfloat16, (R, H), dev))
+    ws = _workspace(workspace, workspace_bytes("dispatch", T=T, H=H, E=E, k=k), dev)
+    n = ctypes.c_size_t(ws.numel())
+    _check("liger_moe_dispatch", lib.liger_moe_dispatch(
+        _ptr(topk_ids), _ptr(topk_w), _ptr(x), T, H, E, k, _ptr(o["counts"]), _ptr(o["m_indptr"]),
+        _ptr(o["row_to_slot"]), _ptr(o["slot_to_row"]), _ptr(o["w_perm"]), _ptr(o["x_perm"]), _ptr(ws),
+        ctypes.byref(n), _stream(stream)))
+    return o
+
+
+def grouped_swiglu_fwd(x_perm, m_indptr, w_gate_up, w_down, w_perm, *, save_gu=True, out=None, workspace=None,
+                       stream=None):
+    """Grouped SwiGLU expert MLP: returns (h_perm [R,I] bf16, gu_perm [R,2I] fp32 or None, y_perm [R,H] bf16)."""
+    lib = load_library()
+    _need(x_perm, "x_perm", torch.bfloat16)
+    R, H = x_perm.shape
+    _need(w_gate_up, "w_gate_up", torch.bfloat16)
+    E, two_i, _ = w_gate_up.shape
+    I = two_i // 2
+    _need(w_gate_up, "w_gate_up", torch.bfloat16, (E, 2 * I, H))
+    _need(w_down, "w_down", torch.bfloat16, (E, H, I))
+    _need(m_indptr, "m_indptr", torch.int32, (E + 1,))
+    _need(w_perm, "w_perm", torch.float32, (R,))
+    dev = x_perm.device
+    out = dict(out or {})
+    h = _out(out.get("h_perm"), "h_perm", torch.bfloat16, (R, I), dev)
+    gu = _out(out.get("gu_perm"), "gu_perm", torch.float32, (R, 2 * I), dev) if save_gu else None
+    y = _out(out.get("y_perm"), "y_perm", torch.bfloat16, (R, H), dev)
+    ws = _workspace(workspace, workspace_bytes("grouped_swiglu_fwd", R=R, H=H, I=I, E=E), dev)
+    n = ctypes.c_size_t(ws.numel())
+    _check("liger_moe_grouped_swiglu_fwd", lib.liger_moe_grouped_swiglu_fwd(
+        _ptr(x_perm), _ptr(m_indptr), _ptr(w_gate_up), _ptr(w_down), _ptr(w_perm), R, H, I, E, _ptr(h), _ptr(gu),
+        _ptr(y), _ptr(ws), ctypes.byref(n), _stream(stream)))
+    return h, gu, y
+
+
+def combine(y_perm, slot_to_row, T, k, *, out=None, stream=None):
+    """Y [T,H] = bf16(sum_j y_perm[slot_to_row[t*k+j]])."""
+    lib = load_library()
+    _need(y_perm, "y_perm", torch.bfloat16)
+    H = y_perm.shape[1]
+    _need(slot_to_row, "slot_to_row", torch.int32, (T * k,))
+    y = _out(out, "y", torch.bfloat16, (T, H), y_perm.device)
+    _check("liger_moe_combine", lib.liger_moe_combine(_ptr(y_perm), _ptr(slot_to_row), T, H, k, _ptr(y),
+                                                      _stream(stream)))
+    return y
+
+
+def bwd_dx_dw(dy, x_perm, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_slot, slot_to_row, w_perm, w_gate_up,
+              w_down, *, out=None, workspace=None, stream=None):
+    """Backward of the layer: returns (dx [T,H], dw_gate_up [E,2I,H], dw_down [E,H,I], d_logits [T,E])."""
+    lib = load_library()
+    _need(dy, "dy", torch.bfloat16)
+    T, H = dy.shape
+    _need(topk_ids, "topk_ids", torch.int32)
+    k = topk_ids.shape[1]
+    E, two_i, _ = w_gate_up.shape
+    I = two_i // 2
+    R = T * k
+    for t, n, dt, sh in ((x_perm, "x_perm", torch.bfloat16, (R, H)), (h_perm, "h_perm", torch.bfloat16, (R, I)),
+                         (topk_w, "topk_w", torch.float32, (T, k)), (m_indptr, "m_indptr", torch.int32, (E + 1,)),
+                         (row_to_slot, "row_to_slot", torch.int32, (R,)),
+                         (slot_to_row, "slot_to_row", torch.int32, (R,)), (w_perm, "w_perm", torch.float32, (R,)),
+                         (w_gate_up, "w_gate_up", torch.bfloat16, (E, 2 * I, H)),
+                         (w_down, "w_down", torch.bfloat16, (E, H, I))):
+        _need(t, n, dt, sh)
+    if gu_perm is not None:
+        _need(gu_perm, "gu_perm", torch.float32, (R, 2 * I))
+    dev = dy.device
+    out = dict(out or {})
+    dx = _out(out.get("dx"), "dx", torch.bfloat16, (T, H), dev)
+    dwgu = _out(out.get("dw_gate_up"), "dw_gate_up", torch.bfloat16, (E, 2 * I, H), dev)
+    dwd = _out(out.get("dw_down"), "dw_down", torch.bfloat16, (E, H, I), dev)
+    dl = _out(out.get("d_logits"), "d_logits", torch.float32, (T, E), dev)
+    ws = _workspace(workspace, workspace_bytes("bwd_dx_dw", T=T, H=H, I=I, E=E, k=k, saved_gu=gu_perm is not None),
+                    dev)
+    n = ctypes.c_size_t(ws.numel())
+    _check("liger_moe_bwd_dx_dw", lib.liger_moe_bwd_dx_dw(
+        _ptr(dy), _ptr(x_perm), _ptr(h_perm), _ptr(gu_perm), _ptr(topk_ids), _ptr(topk_w), _ptr(m_indptr),
+        _ptr(row_to_slot), _ptr(slot_to_row), _ptr(w_perm), _ptr(w_gate_up), _ptr(w_down), T, H, I, E, k, _ptr(dx),
+        _ptr(dwgu), _ptr(dwd), _ptr(dl), _ptr(ws), ctypes.byref(n), _stream(stream)))
+    return dx, dwgu, dwd, dl
+
+
+def device_error(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error bits (0 = none)."""
+    lib = load_library()
+    flags = ctypes.c_int(0)
+    rc = lib.liger_moe_device_error(_stream(stream), ctypes.byref(flags))
+    if rc not in (OK, -6):
+        _check("liger_moe_device_error", rc)
+    return flags.value
+
+
+def trace_enable(on: bool = True) -> None:
+    """Turns the library's per-kernel CUDA-event trace on or off (clears the log)."""
+    _check("liger_moe_trace_enable", load_library().liger_moe_trace_enable(1 if on else 0))
+
+
+def trace_records() -> list[tuple[str, float]]:
+    """(kernel name, device milliseconds) of every launch logged since trace_enable(True)."""
+    lib = load_library()
+    out = []
+    name = ctypes.c_char_p()
+    ms = ctypes.c_float()
+    for i in range(lib.liger_moe_trace_count()):
+        _check("liger_moe_trace_get", lib.liger_moe_trace_get(i, ctypes.byref(name), ctypes.byref(ms)))
+        out.append((name.value.decode(), float(ms.value)))
+    return out

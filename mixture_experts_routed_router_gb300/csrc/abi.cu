@@ -1,0 +1,405 @@
+// The C ABI of the routed MoE layer (see include/liger_moe.h): argument
+// validation, workspace layout and the launch sequence of each entry point.
+// No entry point allocates, frees or synchronises (except
+// liger_moe_device_error, whose job is to synchronise and read the flag).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+
+#define LIGER_MOE_API extern "C" __attribute__((visibility("default")))
+
+namespace lmoe {
+
+namespace {
+thread_local char g_last_error[256] = "";
+__device__ int g_device_error = 0;  // device-side error word, one per device
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+DeviceInfo g_dev_cache[kMaxDevices];
+bool g_dev_known[kMaxDevices] = {};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr long long kIndexLimit = 2147483647LL;  // int32 row / slot indices and TMA coordinates
+
+// Shape checks shared by the expert entry points.
+int check_shapes(long long R, int H, int I, int E) {
+  if (R < 0 || E < 1 || H < 1 || I < 1) return LIGER_MOE_ERR_INVALID_ARG;
+  if (E > kMaxExperts) return LIGER_MOE_ERR_CAPACITY;
+  if (H % 64 != 0 || I % 64 != 0) return LIGER_MOE_ERR_MISALIGNED;
+  if (R > kIndexLimit || 2LL * I * E > kIndexLimit || 1LL * H * E > kIndexLimit) return LIGER_MOE_ERR_CAPACITY;
+  return LIGER_MOE_OK;
+}
+
+int check_topk(long long T, int E, int k) {
+  if (T < 0 || E < 1 || k < 1 || k > E) return LIGER_MOE_ERR_INVALID_ARG;
+  if (E > kMaxExperts || k > kMaxTopK) return LIGER_MOE_ERR_CAPACITY;
+  if (T * k > kIndexLimit) return LIGER_MOE_ERR_CAPACITY;
+  return LIGER_MOE_OK;
+}
+
+template <class T>
+T* carve(uint8_t*& cursor, size_t bytes) {
+  T* p = reinterpret_cast<T*>(cursor);
+  cursor += align_up(bytes, 256);
+  return p;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- kernel trace
+namespace {
+struct TraceRecord {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+std::atomic<int> g_trace_on{0};
+std::mutex g_trace_mu;
+std::vector<TraceRecord> g_trace;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t trace_event() {
+  // caller holds g_trace_mu
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+}  // namespace
+
+KernelScope::KernelScope(const char* name, cudaStream_t s) : name_(name), stream_(s) {
+  if (!g_trace_on.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  start_ = trace_event();
+  if (start_ != nullptr) cudaEventRecord(start_, stream_);
+}
+
+KernelScope::~KernelScope() {
+  if (start_ == nullptr) return;
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  cudaEvent_t stop = trace_event();
+  if (stop == nullptr) {
+    g_event_pool.push_back(start_);
+    return;
+  }
+  cudaEventRecord(stop, stream_);
+  g_trace.push_back(TraceRecord{name_, start_, stop});
+}
+
+void set_cuda_error(cudaError_t e, const char* where) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, cudaGetErrorString(e));
+}
+
+int check_launch(const char* where) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_cuda_error(e, where);
+    return LIGER_MOE_ERR_LAUNCH;
+  }
+  return LIGER_MOE_OK;
+}
+
+int current_device(DeviceInfo* info) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_cuda_error(e, "cudaGetDevice");
+    return LIGER_MOE_ERR_UNSUPPORTED_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (dev >= 0 && dev < kMaxDevices && g_dev_known[dev]) {
+    *info = g_dev_cache[dev];
+    return LIGER_MOE_OK;
+  }
+  int major = 0, minor = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (major != 10 || minor != 3) return LIGER_MOE_ERR_UNSUPPORTED_DEVICE;
+  void* flag = nullptr;
+  e = cudaGetSymbolAddress(&flag, g_device_error);
+  if (e != cudaSuccess) {
+    set_cuda_error(e, "cudaGetSymbolAddress(device error flag)");
+    return LIGER_MOE_ERR_LAUNCH;
+  }
+  DeviceInfo d{dev, sms, static_cast<int*>(flag)};
+  if (dev >= 0 && dev < kMaxDevices) {
+    g_dev_cache[dev] = d;
+    g_dev_known[dev] = true;
+  }
+  *info = d;
+  return LIGER_MOE_OK;
+}
+
+namespace {
+
+size_t bwd_workspace_bytes(long long R, int H, int I, int E, bool recompute_gu) {
+  size_t b = schedule_bytes(E);
+  b += align_up(static_cast<size_t>(R) * H * 2, 256);                 // dy_perm
+  b += align_up(static_cast<size_t>(R) * 2 * I * 2, 256);             // dgu
+  b += align_up(static_cast<size_t>(R) * H * 2, 256);                 // dx_perm
+  b += align_up(static_cast<size_t>(R) * I * 2, 256);                 // hw_perm
+  b += align_up(static_cast<size_t>(R) * gdot_tiles(I) * 4, 256);     // gdot
+  if (recompute_gu) b += align_up(static_cast<size_t>(R) * 2 * I * 4, 256);
+  return b;
+}
+
+}  // namespace
+}  // namespace lmoe
+
+using namespace lmoe;
+
+LIGER_MOE_API int liger_moe_abi_version(void) { return 100; }
+
+LIGER_MOE_API const char* liger_moe_last_cuda_error(void) { return g_last_error; }
+
+LIGER_MOE_API const char* liger_moe_status_string(int status) {
+  switch (status) {
+    case LIGER_MOE_OK: return "LIGER_MOE_OK";
+    case LIGER_MOE_ERR_INVALID_ARG: return "LIGER_MOE_ERR_INVALID_ARG";
+    case LIGER_MOE_ERR_MISALIGNED: return "LIGER_MOE_ERR_MISALIGNED";
+    case LIGER_MOE_ERR_CAPACITY: return "LIGER_MOE_ERR_CAPACITY";
+    case LIGER_MOE_ERR_UNSUPPORTED_DEVICE: return "LIGER_MOE_ERR_UNSUPPORTED_DEVICE";
+    case LIGER_MOE_ERR_LAUNCH: return "LIGER_MOE_ERR_LAUNCH";
+    case LIGER_MOE_ERR_DEVICE: return "LIGER_MOE_ERR_DEVICE";
+    default: return "unknown liger_moe status";
+  }
+}
+
+LIGER_MOE_API int liger_moe_route_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
+                                       void* stream) {
+  if (int rc = check_topk(T, E, k)) return rc;
+  if (T > 0 && (logits == nullptr || topk_ids == nullptr || topk_w == nullptr)) return LIGER_MOE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  if (T == 0) return LIGER_MOE_OK;
+  return launch_route_topk(logits, T, E, k, topk_ids, topk_w, static_cast<cudaStream_t>(stream));
+}
+
+LIGER_MOE_API int liger_moe_dispatch(const int32_t* topk_ids, const float* topk_w, const void* x, int T, int H, int E,
+                                     int k, int32_t* counts, int32_t* m_indptr, int32_t* row_to_slot,
+                                     int32_t* slot_to_row, float* w_perm, void* x_perm, void* workspace,
+                                     size_t* workspace_bytes, void* stream) {
+  if (int rc = check_topk(T, E, k)) return rc;
+  const long long R = static_cast<long long>(T) * k;
+  if (workspace_bytes == nullptr || counts == nullptr || m_indptr == nullptr) return LIGER_MOE_ERR_INVALID_ARG;
+  if (R > 0 && (topk_ids == nullptr || row_to_slot == nullptr || slot_to_row == nullptr))
+    return LIGER_MOE_ERR_INVALID_ARG;
+  if (w_perm != nullptr && R > 0 && topk_w == nullptr) return LIGER_MOE_ERR_INVALID_ARG;
+  if (x_perm != nullptr && R > 0) {
+    if (x == nullptr) return LIGER_MOE_ERR_INVALID_ARG;
+    if (H < 64 || H % 64 != 0 || !aligned16(x) || !aligned16(x_perm)) return LIGER_MOE_ERR_MISALIGNED;
+  }
+  const size_t need = dispatch_workspace_bytes(R, E);
+  if (workspace == nullptr) {
+    *workspace_bytes = need;
+    return LIGER_MOE_OK;
+  }
+  if (*workspace_bytes < need) return LIGER_MOE_ERR_CAPACITY;
+  if (!aligned16(workspace)) return LIGER_MOE_ERR_MISALIGNED;
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  return launch_dispatch(topk_ids, topk_w, static_cast<const uint16_t*>(x), T, H, E, k, counts, m_indptr, row_to_slot,
+                         slot_to_row, w_perm, static_cast<uint16_t*>(x_perm), workspace, dev,
+                         static_cast<cudaStream_t>(stream));
+}
+
+LIGER_MOE_API int liger_moe_grouped_swiglu_fwd(const void* x_perm, const int32_t* m_indptr, const void* w_gate_up,
+                                               const void* w_down, const float* w_perm, int R, int H, int I, int E,
+                                               void* h_perm, float* gu_perm, void* y_perm, void* workspace,
+                                               size_t* workspace_bytes, void* stream) {
+  if (int rc = check_shapes(R, H, I, E)) return rc;
+  if (workspace_bytes == nullptr || m_indptr == nullptr) return LIGER_MOE_ERR_INVALID_ARG;
+  if (R > 0 && (x_perm == nullptr || w_gate_up == nullptr || w_down == nullptr || w_perm == nullptr ||
+                h_perm == nullptr || y_perm == nullptr))
+    return LIGER_MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(h_perm) ||
+      !aligned16(gu_perm) || !aligned16(y_perm))
+    return LIGER_MOE_ERR_MISALIGNED;
+  const size_t need = schedule_bytes(E);
+  if (workspace == nullptr) {
+    *workspace_bytes = need;
+    return LIGER_MOE_OK;
+  }
+  if (*workspace_bytes < need) return LIGER_MOE_ERR_CAPACITY;
+  if (!aligned16(workspace)) return LIGER_MOE_ERR_MISALIGNED;
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  if (R == 0) return LIGER_MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* tile_prefix = static_cast<int32_t*>(workspace);
+  if (int rc = launch_tile_schedule(m_indptr, E, R, tile_prefix, dev, s)) return rc;
+  FwdGemmArgs a{static_cast<const uint16_t*>(x_perm),
+                m_indptr,
+                tile_prefix,
+                static_cast<const uint16_t*>(w_gate_up),
+                static_cast<const uint16_t*>(w_down),
+                w_perm,
+                R,
+                H,
+                I,
+                E,
+                static_cast<uint16_t*>(h_perm),
+                gu_perm,
+                static_cast<uint16_t*>(y_perm)};
+  if (int rc = launch_gate_up(a, dev, s)) return rc;
+  return launch_down(a, dev, s);
+}
+
+LIGER_MOE_API int liger_moe_combine(const void* y_perm, const int32_t* slot_to_row, int T, int H, int k, void* y,
+                                    void* stream) {
+  if (T < 0 || k < 1 || H < 1) return LIGER_MOE_ERR_INVALID_ARG;
+  if (k > kMaxTopK || static_cast<long long>(T) * k > kIndexLimit) return LIGER_MOE_ERR_CAPACITY;
+  if (H % 64 != 0) return LIGER_MOE_ERR_MISALIGNED;
+  if (T > 0 && (y_perm == nullptr || slot_to_row == nullptr || y == nullptr)) return LIGER_MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(y)) return LIGER_MOE_ERR_MISALIGNED;
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  return launch_combine(static_cast<const uint16_t*>(y_perm), slot_to_row, T, H, k, static_cast<uint16_t*>(y), dev,
+                        static_cast<cudaStream_t>(stream));
+}
+
+LIGER_MOE_API int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const void* h_perm, const float* gu_perm,
+                                      const int32_t* topk_ids, const float* topk_w, const int32_t* m_indptr,
+                                      const int32_t* row_to_slot, const int32_t* slot_to_row, const float* w_perm,
+                                      const void* w_gate_up, const void* w_down, int T, int H, int I, int E, int k,
+                                      void* dx, void* dw_gate_up, void* dw_down, float* d_logits, void* workspace,
+                                      size_t* workspace_bytes, void* stream) {
+  if (int rc = check_topk(T, E, k)) return rc;
+  const long long R = static_cast<long long>(T) * k;
+  if (int rc = check_shapes(R, H, I, E)) return rc;
+  if (workspace_bytes == nullptr || m_indptr == nullptr || w_gate_up == nullptr || w_down == nullptr ||
+      dw_gate_up == nullptr || dw_down == nullptr)
+    return LIGER_MOE_ERR_INVALID_ARG;
+  if (R > 0 && (dy == nullptr || x_perm == nullptr || h_perm == nullptr || topk_ids == nullptr ||
+                topk_w == nullptr || row_to_slot == nullptr || slot_to_row == nullptr || w_perm == nullptr ||
+                dx == nullptr || d_logits == nullptr))
+    return LIGER_MOE_ERR_INVALID_ARG;
+  if (!aligned16(dy) || !aligned16(x_perm) || !aligned16(h_perm) || !aligned16(gu_perm) || !aligned16(w_gate_up) ||
+      !aligned16(w_down) || !aligned16(dx) || !aligned16(dw_gate_up) || !aligned16(dw_down))
+    return LIGER_MOE_ERR_MISALIGNED;
+  const bool recompute = (gu_perm == nullptr);
+  const size_t need = bwd_workspace_bytes(R, H, I, E, recompute);
+  if (workspace == nullptr) {
+    *workspace_bytes = need;
+    return LIGER_MOE_OK;
+  }
+  if (*workspace_bytes < need) return LIGER_MOE_ERR_CAPACITY;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LIGER_MOE_ERR_MISALIGNED;
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  uint8_t* cur = static_cast<uint8_t*>(workspace);
+  int32_t* tile_prefix = carve<int32_t>(cur, schedule_bytes(E));
+  uint16_t* dy_perm = carve<uint16_t>(cur, static_cast<size_t>(R) * H * 2);
+  uint16_t* dgu = carve<uint16_t>(cur, static_cast<size_t>(R) * 2 * I * 2);
+  uint16_t* dx_perm = carve<uint16_t>(cur, static_cast<size_t>(R) * H * 2);
+  uint16_t* hw_perm = carve<uint16_t>(cur, static_cast<size_t>(R) * I * 2);
+  float* gdot = carve<float>(cur, static_cast<size_t>(R) * gdot_tiles(I) * 4);
+  float* gu_ws = recompute ? carve<float>(cur, static_cast<size_t>(R) * 2 * I * 4) : nullptr;
+
+  BwdGemmArgs a{};
+  a.m_indptr = m_indptr;
+  a.tile_prefix = tile_prefix;
+  a.w_gate_up = static_cast<const uint16_t*>(w_gate_up);
+  a.w_down = static_cast<const uint16_t*>(w_down);
+  a.x_perm = static_cast<const uint16_t*>(x_perm);
+  a.h_perm = static_cast<const uint16_t*>(h_perm);
+  a.gu = recompute ? gu_ws : gu_perm;
+  a.dy_perm = dy_perm;
+  a.w_perm = w_perm;
+  a.hw_perm = hw_perm;
+  a.dgu = dgu;
+  a.dx_perm = dx_perm;
+  a.gdot = gdot;
+  a.dw_gate_up = static_cast<uint16_t*>(dw_gate_up);
+  a.dw_down = static_cast<uint16_t*>(dw_down);
+  a.R = R;
+  a.H = H;
+  a.I = I;
+  a.E = E;
+
+  if (R > 0) {
+    if (int rc = launch_tile_schedule(m_indptr, E, R, tile_prefix, dev, s)) return rc;
+    // dy_perm[r] = dY[token of r]
+    if (int rc = launch_gather_rows(static_cast<const uint16_t*>(dy), row_to_slot, nullptr, R, H, k, dy_perm, dev, s))
+      return rc;
+    if (recompute) {
+      FwdGemmArgs f{a.x_perm, m_indptr, tile_prefix, a.w_gate_up, a.w_down, w_perm, R, H, I, E, nullptr, gu_ws,
+                    nullptr};
+      if (int rc = launch_gate_up(f, dev, s)) return rc;
+    }
+    if (int rc = launch_bwd_dh(a, dev, s)) return rc;
+    if (int rc = launch_bwd_dx(a, dev, s)) return rc;
+    if (int rc = launch_combine(dx_perm, slot_to_row, T, H, k, static_cast<uint16_t*>(dx), dev, s)) return rc;
+  }
+  if (int rc = launch_bwd_dw(a, dev, s)) return rc;
+  if (R > 0)
+    return launch_router_grad(gdot, gdot_tiles(I), topk_ids, topk_w, slot_to_row, T, E, k, d_logits, dev, s);
+  return LIGER_MOE_OK;
+}
+
+LIGER_MOE_API int liger_moe_trace_enable(int on) {
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  for (const TraceRecord& r : g_trace) {
+    g_event_pool.push_back(r.start);
+    g_event_pool.push_back(r.stop);
+  }
+  g_trace.clear();
+  g_trace_on.store(on ? 1 : 0);
+  return LIGER_MOE_OK;
+}
+
+LIGER_MOE_API int liger_moe_trace_count(void) {
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  return static_cast<int>(g_trace.size());
+}
+
+LIGER_MOE_API int liger_moe_trace_get(int i, const char** name, float* ms) {
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  if (i < 0 || i >= static_cast<int>(g_trace.size()) || name == nullptr || ms == nullptr)
+    return LIGER_MOE_ERR_INVALID_ARG;
+  const TraceRecord& r = g_trace[i];
+  *name = r.name;
+  cudaError_t e = cudaEventSynchronize(r.stop);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(ms, r.start, r.stop);
+  if (e != cudaSuccess) {
+    set_cuda_error(e, "trace event");
+    return LIGER_MOE_ERR_LAUNCH;
+  }
+  return LIGER_MOE_OK;
+}
+
+LIGER_MOE_API int liger_moe_device_error(void* stream, int* flags) {
+  if (flags == nullptr) return LIGER_MOE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    set_cuda_error(e, "cudaStreamSynchronize");
+    return LIGER_MOE_ERR_LAUNCH;
+  }
+  int v = 0;
+  e = cudaMemcpy(&v, dev.err_flag, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && v != 0) e = cudaMemset(dev.err_flag, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    set_cuda_error(e, "reading the device error flag");
+    return LIGER_MOE_ERR_LAUNCH;
+  }
+  *flags = v;
+  return v ? LIGER_MOE_ERR_DEVICE : LIGER_MOE_OK;
+}

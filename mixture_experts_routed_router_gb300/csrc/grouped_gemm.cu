@@ -1,0 +1,743 @@
+// Grouped GEMMs of the routed MoE layer on the 5th-generation tensor cores.
+//
+// One persistent, warp-specialised kernel template serves every contraction
+// of the layer (LightMoE README, "Grouped GEMM": expert-major rows, m_indptr,
+// b laid out [num_experts, N, K]; LigerCute README, "LigerMoE design":
+// persistent warp-specialised TMA / MMA pipeline):
+//   warp 0      TMA producer: one elected lane streams A and B tiles into a
+//               4-stage shared-memory ring (128-byte swizzle), mbarrier-tracked
+//   warp 1      MMA issuer: allocates 512 TMEM columns, one elected lane issues
+//               tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32) and commits
+//               stage releases and accumulator-ready events to mbarriers
+//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (each warp owns one
+//               32-lane TMEM quadrant = 32 rows), fused math, bf16 stores
+// The two 128x256 fp32 accumulators in TMEM are double-buffered, so the
+// epilogue of tile i overlaps the MMAs of tile i+1.
+//
+// Two schedules:
+//   RowsM  rows of an expert are the GEMM's M (forward gate/up and down,
+//          backward dH and dX): tiles (expert, 128-row block, N block), K fixed.
+//          The per-expert M-tile prefix is built on the device from m_indptr.
+//   RowsK  rows of an expert are the GEMM's K (weight gradients): tiles
+//          (expert, M block, N block), K = rows of that expert, walked in row
+//          order by one CTA (deterministic, no split-K atomics).  The last
+//          K block's rows that belong to the next expert are zeroed in shared
+//          memory before the MMA reads them.
+// Epilogues: SwiGLU (h = silu(g)*u, optional [g|u] store), ScaleRows
+// (y = w_r * acc), DH (dgu = SwiGLU backward, per-row partial <dh, h> for the
+// router gradient), Store (plain bf16).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace lmoe {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64 (MN) x 64 (K) box of an MN-major operand
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 2 * BN;
+constexpr int kBarrierBytes = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + kBarrierBytes;
+
+enum class Sched : int { RowsM = 0, RowsK = 1 };
+enum class Epi : int { SwiGLU = 0, ScaleRows = 1, DH = 2, Store = 3 };
+
+struct Params {
+  const int32_t* m_indptr;     // [E+1]
+  const int32_t* tile_prefix;  // RowsM: [E+1] M-tile prefix
+  int E;
+  int n_tiles;            // tiles along N
+  int m_tiles;            // RowsK: M tiles per expert
+  int num_kb;             // RowsM: K / BK
+  int b_rows_per_expert;  // rows of B's tensor map per expert
+  int b_split;            // SwiGLU: row offset of the up half of W_gu (= I)
+  int M_out;              // RowsK: output rows per expert
+  int N_out;              // valid output columns
+  int I;
+  uint16_t* out;
+  long long ld_out;
+  long long out_expert_stride;
+  uint16_t* out2;         // DH: dgu [R, 2I]
+  float* gu_out;          // SwiGLU: [g|u] fp32 [R, 2I] (nullable)
+  const float* row_scale; // ScaleRows, DH: w_perm
+  const float* gu_in;     // DH: [g|u] fp32 [R, 2I]
+  const uint16_t* h_in;   // DH: h [R, I]
+  uint16_t* hw_out;       // DH: bf16(w * h) [R, I]
+  float* gdot;            // DH: [R, n_tiles] partial <dh, h>
+  int* err;
+};
+
+struct Tile {
+  int e;
+  int m0;        // RowsM: first global row of the tile; RowsK: first output row inside the expert
+  int rows;      // RowsM: valid rows in the tile; RowsK: rows of the expert (K extent)
+  int nt;        // N tile
+  int row0;      // RowsK: first global row of the expert
+  int kb_count;  // K blocks
+};
+
+template <Sched S>
+__device__ __forceinline__ Tile decode_tile(int t, const Params& p) {
+  Tile tl;
+  if constexpr (S == Sched::RowsM) {
+    const int mt = t / p.n_tiles;
+    tl.nt = t - mt * p.n_tiles;
+    int lo = 0, hi = p.E;  // tile_prefix[lo] <= mt < tile_prefix[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.tile_prefix + mid) <= mt)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    tl.e = lo;
+    const int end = __ldg(p.m_indptr + lo + 1);
+    tl.m0 = __ldg(p.m_indptr + lo) + (mt - __ldg(p.tile_prefix + lo)) * BM;
+    tl.rows = min(BM, end - tl.m0);
+    tl.row0 = 0;
+    tl.kb_count = p.num_kb;
+  } else {
+    const int per_e = p.m_tiles * p.n_tiles;
+    tl.e = t / per_e;
+    const int r = t - tl.e * per_e;
+    const int mt = r / p.n_tiles;
+    tl.nt = r - mt * p.n_tiles;
+    tl.m0 = mt * BM;
+    tl.row0 = __ldg(p.m_indptr + tl.e);
+    tl.rows = __ldg(p.m_indptr + tl.e + 1) - tl.row0;
+    tl.kb_count = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
+  }
+  return tl;
+}
+
+__device__ __forceinline__ void raise_abort(int* err, volatile int* abort_flag) {
+  if (!*abort_flag) {
+    atomicOr(err, LIGER_MOE_DEVERR_WAIT_TIMEOUT);
+    *abort_flag = 1;
+  }
+}
+
+__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
+
+__device__ __forceinline__ void store16_bf16(uint16_t* dst, const float (&v)[16]) {
+  uint4 a, b;
+  a.x = pack_bf16x2(v[0], v[1]);
+  a.y = pack_bf16x2(v[2], v[3]);
+  a.z = pack_bf16x2(v[4], v[5]);
+  a.w = pack_bf16x2(v[6], v[7]);
+  b.x = pack_bf16x2(v[8], v[9]);
+  b.y = pack_bf16x2(v[10], v[11]);
+  b.z = pack_bf16x2(v[12], v[13]);
+  b.w = pack_bf16x2(v[14], v[15]);
+  reinterpret_cast<uint4*>(dst)[0] = a;
+  reinterpret_cast<uint4*>(dst)[1] = b;
+}
+
+__device__ __forceinline__ void store16_f32(float* dst, const float (&v)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
+__device__ __forceinline__ void load16_f32(const float* src, float (&v)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 q = __ldg(reinterpret_cast<const float4*>(src) + i);
+    v[4 * i] = q.x;
+    v[4 * i + 1] = q.y;
+    v[4 * i + 2] = q.z;
+    v[4 * i + 3] = q.w;
+  }
+}
+
+__device__ __forceinline__ void load16_bf16(const uint16_t* src, float (&v)[16]) {
+  const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
+  const uint4 b = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = bf16_lo(w[i]);
+    v[2 * i + 1] = bf16_hi(w[i]);
+  }
+}
+
+// Epilogue of one tile for one thread (= one accumulator row).
+template <Sched S, Epi EP>
+__device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, int row_local, const Params& p) {
+  if constexpr (EP == Epi::SwiGLU) {
+    // accumulator columns [0, BN/2) = g, [BN/2, BN) = u for output columns nt*BN/2 + c
+    const bool ok = row_local < tl.rows;
+    const long long r = tl.m0 + row_local;
+    const int j0 = tl.nt * (BN / 2);
+#pragma unroll 1
+    for (int c = 0; c < BN / 2; c += 16) {
+      float g[16], u[16];
+      tmem_ld16(t_row + c, g);
+      tmem_ld16(t_row + BN / 2 + c, u);
+      tmem_ld_wait();
+      const int col = j0 + c;
+      if (ok && col < p.I) {
+        if (p.out != nullptr) {
+          float h[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) h[i] = silu_f(g[i]) * u[i];
+          store16_bf16(p.out + r * p.ld_out + col, h);
+        }
+        if (p.gu_out != nullptr) {
+          store16_f32(p.gu_out + r * (2LL * p.I) + col, g);
+          store16_f32(p.gu_out + r * (2LL * p.I) + p.I + col, u);
+        }
+      }
+    }
+  } else if constexpr (EP == Epi::ScaleRows) {
+    const bool ok = row_local < tl.rows;
+    const long long r = tl.m0 + row_local;
+    const float sc = ok ? __ldg(p.row_scale + r) : 0.f;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 16) {
+      float v[16];
+      tmem_ld16(t_row + c, v);
+      tmem_ld_wait();
+      const int col = tl.nt * BN + c;
+      if (ok && col < p.N_out) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] *= sc;
+        store16_bf16(p.out + r * p.ld_out + col, v);
+      }
+    }
+  } else if constexpr (EP == Epi::DH) {
+    // acc = dHu = dY[token] W_d[e] for this row; dh = w_r * dHu in fp32.  g, u (fp32) and h
+    // come from the saved forward state.  Writes dgu = [dg | du] (bf16), hw = bf16(w_r * h)
+    // (the dW_down operand) and the partial router-gradient dot <dh, h> of this N tile.
+    const bool ok = row_local < tl.rows;
+    const long long r = tl.m0 + row_local;
+    const long long two_i = 2LL * p.I;
+    const float wr = ok ? __ldg(p.row_scale + r) : 0.f;
+    float part = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 16) {
+      float dh[16];
+      tmem_ld16(t_row + c, dh);
+      tmem_ld_wait();
+      const int n = tl.nt * BN + c;
+      if (ok && n < p.I) {
+        float g[16], u[16], h[16], dg[16], du[16];
+        load16_f32(p.gu_in + r * two_i + n, g);
+        load16_f32(p.gu_in + r * two_i + p.I + n, u);
+        load16_bf16(p.h_in + r * p.I + n, h);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float d = wr * dh[i];
+          part += d * h[i];
+          const float sg = 1.0f / (1.0f + expf(-g[i]));
+          dg[i] = d * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
+          du[i] = d * g[i] * sg;
+          h[i] *= wr;
+        }
+        store16_bf16(p.out2 + r * two_i + n, dg);
+        store16_bf16(p.out2 + r * two_i + p.I + n, du);
+        store16_bf16(p.hw_out + r * p.I + n, h);
+      }
+    }
+    if (ok) p.gdot[r * p.n_tiles + tl.nt] = part;
+  } else {  // Store
+    long long row;
+    bool ok;
+    if constexpr (S == Sched::RowsM) {
+      ok = row_local < tl.rows;
+      row = tl.m0 + row_local;
+    } else {
+      ok = tl.m0 + row_local < p.M_out;
+      row = static_cast<long long>(tl.e) * (p.out_expert_stride / p.ld_out) + tl.m0 + row_local;
+    }
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 16) {
+      float v[16];
+      tmem_ld16(t_row + c, v);
+      tmem_ld_wait();
+      const int col = tl.nt * BN + c;
+      if (ok && col < p.N_out) store16_bf16(p.out + row * p.ld_out + col, v);
+    }
+  }
+}
+
+// RowsK tile of an expert with no rows: the gradient block is exactly zero.
+__device__ __forceinline__ void store_zero_tile(const Tile& tl, int row_local, const Params& p) {
+  if (tl.m0 + row_local >= p.M_out) return;
+  const long long row = static_cast<long long>(tl.e) * (p.out_expert_stride / p.ld_out) + tl.m0 + row_local;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (int c = 0; c < BN; c += 8) {
+    const int col = tl.nt * BN + c;
+    if (col < p.N_out) *reinterpret_cast<uint4*>(p.out + row * p.ld_out + col) = z;
+  }
+}
+
+// Zeroes K rows [valid, BK) of every 64-wide MN box of an MN-major stage
+// (A: 2 boxes, B: 4 boxes, each 64 rows of 128 B).  Whole 128-byte rows are
+// cleared, so the swizzle inside a row does not matter.
+__device__ __forceinline__ void zero_tail_rows(uint8_t* stage_ptr, int valid, int lane) {
+  const int nz = BK - valid;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  const int per_box = nz * 8;  // uint4 per box
+  for (int box = 0; box < 6; ++box) {
+    uint4* dst = reinterpret_cast<uint4*>(stage_ptr + box * MN_BOX_BYTES + valid * 128);
+    for (int i = lane; i < per_box; i += 32) dst[i] = z;
+  }
+}
+
+template <Sched S, Epi EP, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (sbase - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + STAGES);
+  const uint32_t tfull0 = smem_u32(bars + 2 * STAGES);
+  const uint32_t tempty0 = smem_u32(bars + 2 * STAGES + 2);
+  const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  int total;
+  if constexpr (S == Sched::RowsM)
+    total = __ldg(p.tile_prefix + p.E) * p.n_tiles;
+  else
+    total = p.E * p.m_tiles * p.n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool failed = false;
+      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
+        const Tile tl = decode_tile<S>(t, p);
+        for (int kb = 0; kb < tl.kb_count; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
+            raise_abort(p.err, abort_flag);
+            failed = true;
+            break;
+          }
+          const uint32_t sa = sbase + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          if constexpr (!A_MN) {
+            tma_load_2d(sa, &tmA, fb, kb * BK, tl.m0);
+          } else {
+#pragma unroll
+            for (int i = 0; i < BM / 64; ++i) tma_load_2d(sa + i * MN_BOX_BYTES, &tmA, fb, tl.m0 + 64 * i, tl.row0 + kb * BK);
+          }
+          if constexpr (!B_MN) {
+            if constexpr (EP == Epi::SwiGLU) {
+              const int r = tl.e * p.b_rows_per_expert + tl.nt * (BN / 2);
+              tma_load_2d(sb, &tmB, fb, kb * BK, r);
+              tma_load_2d(sb + B_BYTES / 2, &tmB, fb, kb * BK, r + p.b_split);
+            } else {
+              tma_load_2d(sb, &tmB, fb, kb * BK, tl.e * p.b_rows_per_expert + tl.nt * BN);
+            }
+          } else {
+            const int krow = (S == Sched::RowsM) ? tl.e * p.b_rows_per_expert + kb * BK : tl.row0 + kb * BK;
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * MN_BOX_BYTES, &tmB, fb, tl.nt * BN + 64 * i, krow);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (failed) {
+        // let loads already in flight land before the CTA's shared memory goes away
+        for (int i = 0; i < 200; ++i) __nanosleep(1000);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool failed = false;
+    for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
+      const Tile tl = decode_tile<S>(t, p);
+      if (tl.kb_count == 0) continue;
+      // every lane waits (so every lane acquires the phase); the outcome is made warp-uniform
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag))) {
+        raise_abort(p.err, abort_flag);
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      for (int kb = 0; kb < tl.kb_count; ++kb) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * stage, phase, abort_flag))) {
+          raise_abort(p.err, abort_flag);
+          failed = true;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t sa = sbase + stage * STAGE_BYTES;
+        const uint32_t sb = sa + A_BYTES;
+        if constexpr (S == Sched::RowsK) {
+          const int valid = tl.rows - kb * BK;
+          if (valid < BK) {
+            zero_tail_rows(base_ptr + stage * STAGE_BYTES, valid, lane);
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? smem_desc_sw128(sa + kk * 2048, MN_BOX_BYTES, 1024)
+                                     : smem_desc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(sb + kk * 2048, MN_BOX_BYTES, 1024)
+                                     : smem_desc_sw128(sb + kk * 32, 16, 1024);
+            umma_bf16_f32(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty0 + 8 * stage);
+        }
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (failed) break;
+      if (lane == 0) umma_commit(tfull0 + 8 * acc);
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    // every MMA issued by this CTA has completed before TMEM is released
+    if (lane == 0) {
+      umma_commit(drain);
+      const int never = 0;
+      mbar_wait(drain, 0, &never);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int sub = warp & 3;  // TMEM lane quadrant this warp may access
+    const int row_local = sub * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile tl = decode_tile<S>(t, p);
+      if (tl.kb_count == 0) {
+        if constexpr (S == Sched::RowsK) store_zero_tile(tl, row_local, p);
+        continue;
+      }
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag))) {
+        raise_abort(p.err, abort_flag);
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      epilogue_tile<S, EP>(t_row, tl, row_local, p);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ============================================================================
+// Tile schedule: tile_prefix[e] = sum_{e' < e} ceil(rows_e' / BM), tile_prefix[E]
+// = total.  m_indptr is validated (0 = m[0] <= ... <= m[E] = R); if it is not,
+// the schedule is empty and the device error flag is set.
+// ============================================================================
+__global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __restrict__ m_indptr, int E,
+                                                             long long R, int32_t* __restrict__ tile_prefix,
+                                                             int* err) {
+  __shared__ int s_warp[32];
+  __shared__ int s_bad;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_bad = (m_indptr[0] != 0 || static_cast<long long>(m_indptr[E]) != R) ? 1 : 0;
+  __syncthreads();
+  int tiles = 0;
+  if (tid < E) {
+    const int a = m_indptr[tid], b = m_indptr[tid + 1];
+    if (b < a) atomicOr(&s_bad, 1);
+    tiles = (b > a) ? (b - a + BM - 1) / BM : 0;
+  }
+  int incl = tiles;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, m);
+    if (lane >= m) incl += o;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int x = s_warp[lane];
+    int xi = x;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const int o = __shfl_up_sync(0xFFFFFFFFu, xi, m);
+      if (lane >= m) xi += o;
+    }
+    s_warp[lane] = xi - x;
+  }
+  __syncthreads();
+  const bool bad = s_bad != 0;
+  if (tid < E) tile_prefix[tid] = bad ? 0 : s_warp[warp] + incl - tiles;
+  if (tid == E - 1) tile_prefix[E] = bad ? 0 : s_warp[warp] + incl;
+  if (bad && tid == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_INDPTR);
+}
+
+// ============================================================================
+// Host side
+// ============================================================================
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [outer, inner] -> 2D tensor map with a {box_inner, box_outer}
+// box, 128-byte swizzle, zero fill outside the matrix.
+int make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+              uint32_t box_outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return LIGER_MOE_ERR_LAUNCH;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? LIGER_MOE_OK : LIGER_MOE_ERR_LAUNCH;
+}
+
+template <Sched S, Epi EP, bool A_MN, bool B_MN>
+int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, int grid, cudaStream_t s,
+                const char* name) {
+  auto kern = grouped_gemm_kernel<S, EP, A_MN, B_MN>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) {
+    set_cuda_error(attr_err, name);
+    return LIGER_MOE_ERR_LAUNCH;
+  }
+  if (grid < 1) return LIGER_MOE_OK;
+  {
+    KernelScope trace(name, s);
+    kern<<<grid, kThreads, SMEM_BYTES, s>>>(ta, tb, p);
+  }
+  return check_launch(name);
+}
+
+Params base_params(const int32_t* m_indptr, const int32_t* tile_prefix, int E, int* err) {
+  Params p{};
+  p.m_indptr = m_indptr;
+  p.tile_prefix = tile_prefix;
+  p.E = E;
+  p.err = err;
+  return p;
+}
+
+int rows_m_grid(long long R, int E, int n_tiles, const DeviceInfo& dev) {
+  const long long max_tiles = ((R + BM - 1) / BM + E) * n_tiles;
+  return static_cast<int>(max_tiles < dev.sm_count ? max_tiles : dev.sm_count);
+}
+
+int rows_k_grid(long long tiles, const DeviceInfo& dev) {
+  return static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
+}
+
+int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+}  // namespace
+
+size_t schedule_bytes(int E) { return align_up(sizeof(int32_t) * (E + 1), 256); }
+
+int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, int32_t* tile_prefix, const DeviceInfo& dev,
+                         cudaStream_t s) {
+  {
+    KernelScope trace("tile_schedule", s);
+    tile_schedule_kernel<<<1, 1024, 0, s>>>(m_indptr, E, R, tile_prefix, dev.err_flag);
+  }
+  return check_launch("tile_schedule");
+}
+
+int gdot_tiles(int I) { return cdiv(I, BN); }
+
+int launch_gate_up(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
+  if (a.R == 0) return LIGER_MOE_OK;
+  CUtensorMap ta, tb;
+  if (make_tmap(&ta, a.x_perm, a.H, a.R, BK, BM) ||
+      make_tmap(&tb, a.w_gate_up, a.H, 2ULL * a.I * a.E, BK, BN / 2))
+    return LIGER_MOE_ERR_LAUNCH;
+  Params p = base_params(a.m_indptr, a.tile_prefix, a.E, dev.err_flag);
+  p.n_tiles = cdiv(a.I, BN / 2);
+  p.num_kb = a.H / BK;
+  p.b_rows_per_expert = 2 * a.I;
+  p.b_split = a.I;
+  p.N_out = a.I;
+  p.I = a.I;
+  p.out = a.h_perm;
+  p.ld_out = a.I;
+  p.gu_out = a.gu_perm;
+  return launch_gemm<Sched::RowsM, Epi::SwiGLU, false, false>(ta, tb, p, rows_m_grid(a.R, a.E, p.n_tiles, dev), s,
+                                                               "gemm_gate_up_swiglu");
+}
+
+int launch_down(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
+  if (a.R == 0) return LIGER_MOE_OK;
+  CUtensorMap ta, tb;
+  if (make_tmap(&ta, a.h_perm, a.I, a.R, BK, BM) || make_tmap(&tb, a.w_down, a.I, 1ULL * a.H * a.E, BK, BN))
+    return LIGER_MOE_ERR_LAUNCH;
+  Params p = base_params(a.m_indptr, a.tile_prefix, a.E, dev.err_flag);
+  p.n_tiles = cdiv(a.H, BN);
+  p.num_kb = a.I / BK;
+  p.b_rows_per_expert = a.H;
+  p.N_out = a.H;
+  p.I = a.I;
+  p.out = a.y_perm;
+  p.ld_out = a.H;
+  p.row_scale = a.w_perm;
+  return launch_gemm<Sched::RowsM, Epi::ScaleRows, false, false>(ta, tb, p, rows_m_grid(a.R, a.E, p.n_tiles, dev),
+                                                                  s, "gemm_down_scale");
+}
+
+int launch_bwd_dh(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
+  if (a.R == 0) return LIGER_MOE_OK;
+  CUtensorMap ta, tb;
+  if (make_tmap(&ta, a.dy_perm, a.H, a.R, BK, BM) || make_tmap(&tb, a.w_down, a.I, 1ULL * a.H * a.E, 64, BK))
+    return LIGER_MOE_ERR_LAUNCH;
+  Params p = base_params(a.m_indptr, a.tile_prefix, a.E, dev.err_flag);
+  p.n_tiles = cdiv(a.I, BN);
+  p.num_kb = a.H / BK;
+  p.b_rows_per_expert = a.H;
+  p.N_out = a.I;
+  p.I = a.I;
+  p.out2 = a.dgu;
+  p.gu_in = a.gu;
+  p.h_in = a.h_perm;
+  p.hw_out = a.hw_perm;
+  p.row_scale = a.w_perm;
+  p.gdot = a.gdot;
+  return launch_gemm<Sched::RowsM, Epi::DH, false, true>(ta, tb, p, rows_m_grid(a.R, a.E, p.n_tiles, dev), s,
+                                                          "gemm_bwd_dh");
+}
+
+int launch_bwd_dx(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
+  if (a.R == 0) return LIGER_MOE_OK;
+  CUtensorMap ta, tb;
+  if (make_tmap(&ta, a.dgu, 2ULL * a.I, a.R, BK, BM) ||
+      make_tmap(&tb, a.w_gate_up, a.H, 2ULL * a.I * a.E, 64, BK))
+    return LIGER_MOE_ERR_LAUNCH;
+  Params p = base_params(a.m_indptr, a.tile_prefix, a.E, dev.err_flag);
+  p.n_tiles = cdiv(a.H, BN);
+  p.num_kb = 2 * a.I / BK;
+  p.b_rows_per_expert = 2 * a.I;
+  p.N_out = a.H;
+  p.I = a.I;
+  p.out = a.dx_perm;
+  p.ld_out = a.H;
+  return launch_gemm<Sched::RowsM, Epi::Store, false, true>(ta, tb, p, rows_m_grid(a.R, a.E, p.n_tiles, dev), s,
+                                                             "gemm_bwd_dx");
+}
+
+int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
+  // dW_gu[e] = dgu_e^T x_e  ([2I, H]),  dW_d[e] = dY_e^T (w h)_e  ([H, I]); K = rows of e.
+  // With no rows at all (R = 0) every expert's gradient is zero: the kernel still
+  // runs to write the zeros, over 1-row dummy tensor maps that it never reads.
+  CUtensorMap ta, tb;
+  const uint64_t rows = a.R > 0 ? static_cast<uint64_t>(a.R) : 1;
+  Params p = base_params(a.m_indptr, nullptr, a.E, dev.err_flag);
+  if (make_tmap(&ta, a.R > 0 ? a.dgu : a.dw_gate_up, 2ULL * a.I, rows, 64, BK) ||
+      make_tmap(&tb, a.R > 0 ? a.x_perm : a.dw_gate_up, a.H, rows, 64, BK))
+    return LIGER_MOE_ERR_LAUNCH;
+  p.m_tiles = cdiv(2LL * a.I, BM);
+  p.n_tiles = cdiv(a.H, BN);
+  p.M_out = 2 * a.I;
+  p.N_out = a.H;
+  p.out = a.dw_gate_up;
+  p.ld_out = a.H;
+  p.out_expert_stride = 2LL * a.I * a.H;
+  int rc = launch_gemm<Sched::RowsK, Epi::Store, true, true>(
+      ta, tb, p, rows_k_grid(static_cast<long long>(a.E) * p.m_tiles * p.n_tiles, dev), s, "gemm_bwd_dw_gate_up");
+  if (rc) return rc;
+  if (make_tmap(&ta, a.R > 0 ? a.dy_perm : a.dw_down, a.H, rows, 64, BK) ||
+      make_tmap(&tb, a.R > 0 ? a.hw_perm : a.dw_down, a.I, rows, 64, BK))
+    return LIGER_MOE_ERR_LAUNCH;
+  p.m_tiles = cdiv(a.H, BM);
+  p.n_tiles = cdiv(a.I, BN);
+  p.M_out = a.H;
+  p.N_out = a.I;
+  p.out = a.dw_down;
+  p.ld_out = a.I;
+  p.out_expert_stride = 1LL * a.H * a.I;
+  return launch_gemm<Sched::RowsK, Epi::Store, true, true>(
+      ta, tb, p, rows_k_grid(static_cast<long long>(a.E) * p.m_tiles * p.n_tiles, dev), s, "gemm_bwd_dw_down");
+}
+
+}  // namespace lmoe

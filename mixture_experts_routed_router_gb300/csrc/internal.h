@@ -1,0 +1,117 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/liger_moe.h"
+
+namespace lmoe {
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+
+// Records a CUDA error message for liger_moe_last_cuda_error().
+void set_cuda_error(cudaError_t e, const char* where);
+// Returns LIGER_MOE_OK or LIGER_MOE_ERR_LAUNCH (recording the error).
+int check_launch(const char* where);
+
+// Per-device state: SM count and the device error flag's address.
+struct DeviceInfo {
+  int device;
+  int sm_count;
+  int* err_flag;  // device address of the library's error word for this device
+};
+// Fills `info` for the current device; returns a liger_moe_status.
+int current_device(DeviceInfo* info);
+
+// ---- launchers (each enqueues on `s`; return a liger_moe_status)
+int launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s);
+
+// Dispatch workspace bytes for R slots and E experts.
+size_t dispatch_workspace_bytes(long long R, int E);
+int launch_dispatch(const int32_t* ids, const float* w, const uint16_t* x, int T, int H, int E, int k,
+                    int32_t* counts, int32_t* m_indptr, int32_t* row_to_slot, int32_t* slot_to_row, float* w_perm,
+                    uint16_t* x_perm, void* workspace, const DeviceInfo& dev, cudaStream_t s);
+
+// dst[r, :] = src[row_to_slot[r] / k, :] (times scale[r] in fp32 when scale != NULL).
+int launch_gather_rows(const uint16_t* src, const int32_t* row_to_slot, const float* scale, long long R, int H,
+                       int k, uint16_t* dst, const DeviceInfo& dev, cudaStream_t s);
+
+// y[t, :] = bf16(sum_j y_perm[slot_to_row[t*k+j], :]).
+int launch_combine(const uint16_t* y_perm, const int32_t* slot_to_row, int T, int H, int k, uint16_t* y,
+                   const DeviceInfo& dev, cudaStream_t s);
+
+// d_logits from the per-row router-gradient partials (see grouped_gemm.cu).
+int launch_router_grad(const float* gdot, int gdot_tiles, const int32_t* ids, const float* w,
+                       const int32_t* slot_to_row, int T, int E, int k, float* d_logits, const DeviceInfo& dev,
+                       cudaStream_t s);
+
+// ---- grouped GEMMs (grouped_gemm.cu)
+// Tile schedule: tile_prefix[e] = sum over e' < e of ceil(rows_e' / 128); [E] = total.
+size_t schedule_bytes(int E);
+int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, int32_t* tile_prefix, const DeviceInfo& dev,
+                         cudaStream_t s);
+
+struct FwdGemmArgs {
+  const uint16_t* x_perm;
+  const int32_t* m_indptr;
+  const int32_t* tile_prefix;
+  const uint16_t* w_gate_up;
+  const uint16_t* w_down;
+  const float* w_perm;
+  long long R;
+  int H, I, E;
+  uint16_t* h_perm;  // nullable (then only gu is stored)
+  float* gu_perm;     // [R, 2I] fp32, nullable
+  uint16_t* y_perm;
+};
+// gate/up GEMM + SwiGLU epilogue (h_perm may be NULL: only gu is stored).
+int launch_gate_up(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s);
+// down GEMM + routing-weight epilogue.
+int launch_down(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s);
+
+struct BwdGemmArgs {
+  const int32_t* m_indptr;
+  const int32_t* tile_prefix;
+  const uint16_t* w_gate_up;
+  const uint16_t* w_down;
+  const uint16_t* x_perm;
+  const uint16_t* h_perm;
+  const float* gu;       // [R, 2I] fp32 [g | u] (saved or recomputed)
+  const uint16_t* dy_perm;  // [R, H] dY[token of row]
+  const float* w_perm;   // [R]
+  uint16_t* hw_perm;     // [R, I] bf16(w_perm * h)
+  uint16_t* dgu;         // [R, 2I]
+  uint16_t* dx_perm;     // [R, H]
+  float* gdot;           // [R, ceil(I / 256)]
+  uint16_t* dw_gate_up;  // [E, 2I, H]
+  uint16_t* dw_down;     // [E, H, I]
+  long long R;
+  int H, I, E;
+};
+int gdot_tiles(int I);
+int launch_bwd_dh(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s);
+int launch_bwd_dx(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s);
+int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s);
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Kernel trace (off by default): while enabled, each launch made inside a
+// KernelScope is bracketed by two CUDA events recorded on its stream.
+class KernelScope {
+ public:
+  KernelScope(const char* name, cudaStream_t s);
+  ~KernelScope();
+  KernelScope(const KernelScope&) = delete;
+  KernelScope& operator=(const KernelScope&) = delete;
+
+ private:
+  const char* name_;
+  cudaStream_t stream_;
+  cudaEvent_t start_ = nullptr;
+};
+
+}  // namespace lmoe

@@ -1,0 +1,454 @@
+// Bandwidth-bound kernels of the routed MoE layer: router top-k, the
+// deterministic expert-major dispatch, row gathers, the combine back to token
+// order, and the router-logit gradient.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace lmoe {
+namespace {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+// ============================================================================
+// Router: top-k + renormalised softmax.  LightMoE README, "MoE inference"
+// (top_k_ids distinct per token, top_k_weights float32) and "MoE training"
+// (differentiable_probs).  One warp per token; lane i holds experts
+// i, i+32, ... as 64-bit keys
+//    key = (order-preserving bits of the logit) << 32 | (0xFFFFFFFF - id)
+// so the warp-wide maximum is the largest logit, ties to the smallest id.
+// NaN maps to the lowest order value; -0.0 is treated as +0.0.  A selected
+// expert's key is set to 0, below every valid key.
+// ============================================================================
+__device__ __forceinline__ uint64_t route_key(float v, int e) {
+  uint32_t u = __float_as_uint(v);
+  uint32_t ord;
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) {
+    ord = 0u;
+  } else {
+    if (u == 0x80000000u) u = 0u;
+    ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  }
+  return (static_cast<uint64_t>(ord) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(e));
+}
+
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
+  uint32_t lo = __shfl_xor_sync(kFull, static_cast<uint32_t>(v), m);
+  uint32_t hi = __shfl_xor_sync(kFull, static_cast<uint32_t>(v >> 32), m);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                         int32_t* __restrict__ ids, float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (t >= T) return;
+  const float* row = logits + t * E;
+  uint64_t key[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = i * 32 + lane;
+    key[i] = (e < E) ? route_key(__ldg(row + e), e) : 0ull;
+  }
+  float my_val = 0.f, top = 0.f;
+  int my_id = 0;
+  for (int j = 0; j < k; ++j) {
+    uint64_t best = key[0];
+#pragma unroll
+    for (int i = 1; i < EPL; ++i) best = key[i] > best ? key[i] : best;
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+      const uint64_t o = shfl_xor_u64(best, m);
+      best = o > best ? o : best;
+    }
+    const int id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best));
+    // clear the winner's key in place (compare against the key itself so the
+    // array stays in registers)
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) key[i] = (key[i] == best) ? 0ull : key[i];
+    const float v = __ldg(row + id);
+    if (j == 0) top = v;
+    if (lane == j) {
+      my_val = v;
+      my_id = id;
+    }
+  }
+  // w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0), sum in j order.
+  const float ex = (lane < k) ? expf(my_val - top) : 0.f;
+  float s = 0.f;
+  for (int j = 0; j < k; ++j) s += __shfl_sync(kFull, ex, j);
+  if (lane < k) {
+    ids[t * k + lane] = my_id;
+    w[t * k + lane] = ex / s;
+  }
+}
+
+// ============================================================================
+// Dispatch.  LightMoE README, "MoE training" / "Grouped GEMM"; LigerCute
+// README, "Forward pass".  The R = T*k slots are cut into units of kUnit
+// consecutive slots.
+//   1. hist:    per unit, a histogram of its expert ids  -> hist[e][unit]
+//   2. scan:    per expert, exclusive scan over units     -> base[e][unit], counts[e]
+//   3. scatter: per unit, walking its slots in order, the row of slot s is
+//               m_indptr[e] + base[e][unit] + (earlier slots of e in this unit)
+// The rank inside a 32-slot group comes from __match_any_sync; groups are
+// walked in order, so rows of one expert follow slot order (stable).
+// ============================================================================
+constexpr int kUnit = 256;
+constexpr int kWarpsPerBlock = 8;
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) dispatch_hist_kernel(const int32_t* __restrict__ ids,
+                                                                           long long R, int E, int nunits,
+                                                                           int32_t* __restrict__ hist, int* err) {
+  extern __shared__ int s_hist[];
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = blockIdx.x * kWarpsPerBlock + wib;
+  int* h = s_hist + wib * E;
+  for (int e = lane; e < E; e += 32) h[e] = 0;
+  __syncwarp();
+  if (unit >= nunits) return;
+  const long long s0 = static_cast<long long>(unit) * kUnit;
+  int bad = 0;
+  for (int i = lane; i < kUnit; i += 32) {
+    const long long s = s0 + i;
+    if (s < R) {
+      const int e = __ldg(ids + s);
+      if (static_cast<unsigned>(e) < static_cast<unsigned>(E))
+        atomicAdd(&h[e], 1);
+      else
+        bad = 1;
+    }
+  }
+  if (__any_sync(kFull, bad) && lane == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_EXPERT_ID);
+  __syncwarp();
+  for (int e = lane; e < E; e += 32) hist[static_cast<size_t>(e) * nunits + unit] = h[e];
+}
+
+// One warp per expert: exclusive scan of hist[e][*] in place, counts[e] = total.
+__global__ void __launch_bounds__(256) dispatch_scan_kernel(int32_t* __restrict__ hist, int nunits, int E,
+                                                            int32_t* __restrict__ counts) {
+  const int lane = threadIdx.x & 31;
+  const int e = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (e >= E) return;
+  int32_t* row = hist + static_cast<size_t>(e) * nunits;
+  int run = 0;
+  for (int u0 = 0; u0 < nunits; u0 += 32) {
+    const int u = u0 + lane;
+    const int v = (u < nunits) ? row[u] : 0;
+    int incl = v;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const int o = __shfl_up_sync(kFull, incl, m);
+      if (lane >= m) incl += o;
+    }
+    if (u < nunits) row[u] = run + incl - v;
+    run += __shfl_sync(kFull, incl, 31);
+  }
+  if (lane == 0) counts[e] = run;
+}
+
+// Exclusive scan of counts[0..E) into s_off[0..E] by one block (E <= 1024).
+__device__ void block_exclusive_scan(const int32_t* __restrict__ counts, int E, int* s_off, int* s_warp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  for (int base = 0; base < E; base += blockDim.x) {
+    const int carry = (base == 0) ? 0 : s_off[base];  // total of the earlier passes
+    const int e = base + tid;
+    const int v = (e < E) ? counts[e] : 0;
+    int incl = v;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const int o = __shfl_up_sync(kFull, incl, m);
+      if (lane >= m) incl += o;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int x = (lane < nwarps) ? s_warp[lane] : 0;
+      int xi = x;
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const int o = __shfl_up_sync(kFull, xi, m);
+        if (lane >= m) xi += o;
+      }
+      if (lane < nwarps) s_warp[lane] = xi - x;
+    }
+    __syncthreads();
+    if (e < E) s_off[e] = carry + s_warp[warp] + incl - v;
+    if (tid == blockDim.x - 1) s_off[min(base + static_cast<int>(blockDim.x), E)] = carry + s_warp[warp] + incl;
+    __syncthreads();
+  }
+  if (E == 0 && tid == 0) s_off[0] = 0;
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) dispatch_scatter_kernel(
+    const int32_t* __restrict__ ids, const float* __restrict__ w, long long R, int E, int nunits,
+    const int32_t* __restrict__ base, const int32_t* __restrict__ counts, int32_t* __restrict__ m_indptr,
+    int32_t* __restrict__ row_to_slot, int32_t* __restrict__ slot_to_row, float* __restrict__ w_perm) {
+  extern __shared__ int smem[];
+  int* s_off = smem;                       // [E + 1]
+  int* s_warp = s_off + (E + 1);           // [32]
+  int* s_cnt = s_warp + 32;                // [kWarpsPerBlock][E]
+  block_exclusive_scan(counts, E, s_off, s_warp);
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) m_indptr[e] = s_off[e];
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = blockIdx.x * kWarpsPerBlock + wib;
+  if (unit >= nunits) return;
+  int* cnt = s_cnt + wib * E;
+  for (int e = lane; e < E; e += 32) cnt[e] = s_off[e] + __ldg(base + static_cast<size_t>(e) * nunits + unit);
+  __syncwarp();
+  const long long s0 = static_cast<long long>(unit) * kUnit;
+  for (int g = 0; g < kUnit; g += 32) {
+    const long long s = s0 + g + lane;
+    int e = (s < R) ? __ldg(ids + s) : -1;
+    const bool ok = static_cast<unsigned>(e) < static_cast<unsigned>(E);
+    if (!ok) e = E + lane;  // unique per lane: never matches a real expert
+    const unsigned peers = __match_any_sync(kFull, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int leader = __ffs(peers) - 1;
+    int pos = 0;
+    if (ok) pos = cnt[e];
+    __syncwarp();
+    if (ok && lane == leader) cnt[e] = pos + __popc(peers);
+    __syncwarp();
+    if (ok) {
+      const int r = pos + rank;
+      slot_to_row[s] = r;
+      row_to_slot[r] = static_cast<int32_t>(s);
+      if (w_perm) w_perm[r] = __ldg(w + s);
+    }
+  }
+}
+
+// ============================================================================
+// Row gather: dst[r] = src[row_to_slot[r] / k] (optionally scaled by scale[r]
+// in fp32 and rounded to bf16).  One warp per row, 16-byte vectors.
+// ============================================================================
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ src,
+                                                          const int32_t* __restrict__ row_to_slot,
+                                                          const float* __restrict__ scale, long long R, int H, int k,
+                                                          uint16_t* __restrict__ dst, int* err) {
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const int chunks = H >> 3;
+  for (long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < R; r += nwarps) {
+    const int s = __ldg(row_to_slot + r);
+    if (static_cast<unsigned long long>(s) >= static_cast<unsigned long long>(R)) {
+      if (lane == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_ROW);
+      continue;
+    }
+    const uint4* a = reinterpret_cast<const uint4*>(src + static_cast<size_t>(s / k) * H);
+    uint4* b = reinterpret_cast<uint4*>(dst + static_cast<size_t>(r) * H);
+    if (scale == nullptr) {
+#pragma unroll 4
+      for (int c = lane; c < chunks; c += 32) b[c] = __ldg(a + c);
+    } else {
+      const float f = __ldg(scale + r);
+#pragma unroll 4
+      for (int c = lane; c < chunks; c += 32) {
+        uint4 v = __ldg(a + c);
+        v.x = pack_bf16x2(f * bf16_lo(v.x), f * bf16_hi(v.x));
+        v.y = pack_bf16x2(f * bf16_lo(v.y), f * bf16_hi(v.y));
+        v.z = pack_bf16x2(f * bf16_lo(v.z), f * bf16_hi(v.z));
+        v.w = pack_bf16x2(f * bf16_lo(v.w), f * bf16_hi(v.w));
+        b[c] = v;
+      }
+    }
+  }
+}
+
+// ============================================================================
+// Combine.  LigerCute README, "Forward pass" (final local combine);
+// LightMoE README, "Highlights" (deterministic combine).
+//   y[t, :] = bf16( sum_{j=0..k-1} y_perm[slot_to_row[t*k + j], :] )  (fp32, j ascending)
+// One warp per token; lane j fetches the row index of slot j once.
+// ============================================================================
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y_perm,
+                                                      const int32_t* __restrict__ slot_to_row, int T, int H, int k,
+                                                      long long R, uint16_t* __restrict__ y, int* err) {
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const int chunks = H >> 3;
+  for (long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+    int my_row = (lane < k) ? __ldg(slot_to_row + t * k + lane) : 0;
+    const bool bad = static_cast<unsigned long long>(my_row) >= static_cast<unsigned long long>(R);
+    if (__any_sync(kFull, bad)) {
+      if (lane == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_ROW);
+      continue;
+    }
+    for (int c = lane; c < chunks; c += 32) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const int r = __shfl_sync(kFull, my_row, j);
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(y_perm + static_cast<size_t>(r) * H) + c);
+        acc[0] += bf16_lo(v.x);
+        acc[1] += bf16_hi(v.x);
+        acc[2] += bf16_lo(v.y);
+        acc[3] += bf16_hi(v.y);
+        acc[4] += bf16_lo(v.z);
+        acc[5] += bf16_hi(v.z);
+        acc[6] += bf16_lo(v.w);
+        acc[7] += bf16_hi(v.w);
+      }
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * H)[c] = o;
+    }
+  }
+}
+
+// ============================================================================
+// Router-logit gradient.  LightMoE README, "MoE training" (router-gradient
+// kernel, differentiable_probs).  With gamma'_j = w_j * <dY, o_j> (computed
+// per row by the dH GEMM epilogue as partial sums over its column tiles):
+//   d_logits[t, ids_j] = gamma'_j - w_j * sum_i gamma'_i,  0 elsewhere,
+// which equals w_j (gamma_j - sum_i w_i gamma_i).  One warp per token.
+// ============================================================================
+__global__ void __launch_bounds__(256) router_grad_kernel(const float* __restrict__ gdot, int ntiles,
+                                                          const int32_t* __restrict__ ids,
+                                                          const float* __restrict__ w,
+                                                          const int32_t* __restrict__ slot_to_row, int T, int E,
+                                                          int k, long long R, float* __restrict__ d_logits,
+                                                          int* err) {
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+    float* out = d_logits + t * E;
+    for (int e = lane; e < E; e += 32) out[e] = 0.f;
+    float gp = 0.f, wj = 0.f;
+    int id = 0;
+    bool bad = false;
+    if (lane < k) {
+      const int r = __ldg(slot_to_row + t * k + lane);
+      id = __ldg(ids + t * k + lane);
+      wj = __ldg(w + t * k + lane);
+      bad = static_cast<unsigned long long>(r) >= static_cast<unsigned long long>(R) ||
+            static_cast<unsigned>(id) >= static_cast<unsigned>(E);
+      if (!bad)
+        for (int q = 0; q < ntiles; ++q) gp += __ldg(gdot + static_cast<size_t>(r) * ntiles + q);
+    }
+    if (__any_sync(kFull, bad)) {
+      if (lane == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_ROW);
+      continue;
+    }
+    float S = 0.f;
+    for (int j = 0; j < k; ++j) S += __shfl_sync(kFull, gp, j);
+    __syncwarp();
+    if (lane < k) out[id] = gp - wj * S;
+  }
+}
+
+int grid_for_warps(long long nwarps_needed, int warps_per_block, const DeviceInfo& dev, int waves = 16) {
+  long long blocks = (nwarps_needed + warps_per_block - 1) / warps_per_block;
+  const long long cap = static_cast<long long>(dev.sm_count) * waves;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return static_cast<int>(blocks);
+}
+
+}  // namespace
+
+int launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s) {
+  if (T == 0) return LIGER_MOE_OK;
+  const int blocks = static_cast<int>((static_cast<long long>(T) * 32 + 255) / 256);
+  const int epl = (E + 31) / 32;
+  KernelScope trace("route_topk", s);
+  if (epl <= 1)
+    route_topk_kernel<1><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+  else if (epl <= 2)
+    route_topk_kernel<2><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+  else if (epl <= 4)
+    route_topk_kernel<4><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+  else if (epl <= 8)
+    route_topk_kernel<8><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+  else if (epl <= 16)
+    route_topk_kernel<16><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+  else
+    route_topk_kernel<32><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+  return check_launch("route_topk");
+}
+
+size_t dispatch_workspace_bytes(long long R, int E) {
+  const long long nunits = (R + kUnit - 1) / kUnit;
+  return align_up(static_cast<size_t>(nunits) * E * sizeof(int32_t), 256) + 256;
+}
+
+int launch_dispatch(const int32_t* ids, const float* w, const uint16_t* x, int T, int H, int E, int k,
+                    int32_t* counts, int32_t* m_indptr, int32_t* row_to_slot, int32_t* slot_to_row, float* w_perm,
+                    uint16_t* x_perm, void* workspace, const DeviceInfo& dev, cudaStream_t s) {
+  const long long R = static_cast<long long>(T) * k;
+  const int nunits = static_cast<int>((R + kUnit - 1) / kUnit);
+  int32_t* hist = static_cast<int32_t*>(workspace);
+  const int blocks = (nunits + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  if (nunits > 0) {
+    {
+      KernelScope trace("dispatch_hist", s);
+      dispatch_hist_kernel<<<blocks, kWarpsPerBlock * 32, kWarpsPerBlock * E * sizeof(int), s>>>(
+          ids, R, E, nunits, hist, dev.err_flag);
+    }
+    if (int rc = check_launch("dispatch_hist")) return rc;
+    {
+      KernelScope trace("dispatch_scan", s);
+      dispatch_scan_kernel<<<(E * 32 + 255) / 256, 256, 0, s>>>(hist, nunits, E, counts);
+    }
+    if (int rc = check_launch("dispatch_scan")) return rc;
+  } else {
+    cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
+  }
+  const size_t smem = (E + 1 + 32 + kWarpsPerBlock * E) * sizeof(int);
+  {
+    KernelScope trace("dispatch_scatter", s);
+    dispatch_scatter_kernel<<<blocks > 0 ? blocks : 1, kWarpsPerBlock * 32, smem, s>>>(
+        ids, w, R, E, nunits, hist, counts, m_indptr, row_to_slot, slot_to_row, w_perm);
+  }
+  if (int rc = check_launch("dispatch_scatter")) return rc;
+  if (x_perm != nullptr && R > 0) return launch_gather_rows(x, row_to_slot, nullptr, R, H, k, x_perm, dev, s);
+  return LIGER_MOE_OK;
+}
+
+int launch_gather_rows(const uint16_t* src, const int32_t* row_to_slot, const float* scale, long long R, int H,
+                       int k, uint16_t* dst, const DeviceInfo& dev, cudaStream_t s) {
+  if (R == 0) return LIGER_MOE_OK;
+  {
+    KernelScope trace(scale == nullptr ? "gather_rows" : "gather_rows_scaled", s);
+    gather_rows_kernel<<<grid_for_warps(R, 8, dev), 256, 0, s>>>(src, row_to_slot, scale, R, H, k, dst,
+                                                                 dev.err_flag);
+  }
+  return check_launch("gather_rows");
+}
+
+int launch_combine(const uint16_t* y_perm, const int32_t* slot_to_row, int T, int H, int k, uint16_t* y,
+                   const DeviceInfo& dev, cudaStream_t s) {
+  if (T == 0) return LIGER_MOE_OK;
+  {
+    KernelScope trace("combine", s);
+    combine_kernel<<<grid_for_warps(T, 8, dev), 256, 0, s>>>(y_perm, slot_to_row, T, H, k,
+                                                             static_cast<long long>(T) * k, y, dev.err_flag);
+  }
+  return check_launch("combine");
+}
+
+int launch_router_grad(const float* gdot, int gdot_tiles_, const int32_t* ids, const float* w,
+                       const int32_t* slot_to_row, int T, int E, int k, float* d_logits, const DeviceInfo& dev,
+                       cudaStream_t s) {
+  if (T == 0) return LIGER_MOE_OK;
+  {
+    KernelScope trace("router_grad", s);
+    router_grad_kernel<<<grid_for_warps(T, 8, dev), 256, 0, s>>>(gdot, gdot_tiles_, ids, w, slot_to_row, T, E, k,
+                                                                 static_cast<long long>(T) * k, d_logits,
+                                                                 dev.err_flag);
+  }
+  return check_launch("router_grad");
+}
+
+}  // namespace lmoe

@@ -1,0 +1,116 @@
+"""Host-side checks of the C ABI (no GPU needed): symbols, argument validation, workspace queries."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+import mixture_experts_routed_router_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "liger_moe.h")
+
+OK, INVALID, MISALIGNED, CAPACITY, UNSUPPORTED = 0, -1, -2, -3, -4
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(liger_moe_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return moe.load_library()
+
+
+def test_header_declares_the_five_entry_points():
+    names = declared_functions()
+    for f in ("liger_moe_route_topk", "liger_moe_dispatch", "liger_moe_grouped_swiglu_fwd", "liger_moe_combine",
+              "liger_moe_bwd_dx_dw"):
+        assert f in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in liger_moe.h but not exported"
+
+
+def test_only_liger_symbols_are_exported():
+    out = subprocess.run(["nm", "-D", "--defined-only", moe.library_path()], capture_output=True, text=True,
+                         check=True).stdout
+    syms = [l.split()[-1] for l in out.splitlines() if l.strip() and l.split()[-2] in ("T", "W", "D", "B")]
+    assert syms and all(s.startswith("liger_moe_") or s.startswith("_") for s in syms), syms
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    src = tmp_path / "use.c"
+    src.write_text('#include "liger_moe.h"\nint main(void){return liger_moe_abi_version() > 0 ? 0 : 1;}\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-c", "-I", os.path.dirname(HEADER), str(src), "-o",
+                    str(tmp_path / "use.o")], check=True)
+
+
+def test_status_strings(lib):
+    assert lib.liger_moe_status_string(0) == b"LIGER_MOE_OK"
+    assert lib.liger_moe_status_string(-3) == b"LIGER_MOE_ERR_CAPACITY"
+    assert lib.liger_moe_abi_version() >= 100
+
+
+D = ctypes.c_void_p(256)  # never dereferenced: every call below is rejected or is a size query
+
+
+def test_route_argument_errors(lib):
+    f = lib.liger_moe_route_topk
+    assert f(D, -1, 8, 2, D, D, None) == INVALID
+    assert f(D, 4, 8, 9, D, D, None) == INVALID      # k > E
+    assert f(D, 4, 8, 0, D, D, None) == INVALID      # k < 1
+    assert f(D, 4, 2048, 2, D, D, None) == CAPACITY  # E above the limit
+    assert f(D, 4, 64, 33, D, D, None) == CAPACITY   # k above the limit
+    assert f(None, 4, 8, 2, D, D, None) == INVALID
+    assert f(D, 2 ** 30, 64, 8, D, D, None) == CAPACITY  # T*k beyond int32
+
+
+def test_dispatch_validation_and_query(lib):
+    n = ctypes.c_size_t(0)
+    f = lib.liger_moe_dispatch
+    assert f(D, None, None, 8192, 0, 256, 8, D, D, D, D, None, None, None, ctypes.byref(n), None) == OK
+    assert n.value >= 256 * (8192 * 8 // 256) * 4
+    assert f(D, None, D, 16, 100, 8, 2, D, D, D, D, None, D, None, ctypes.byref(n), None) == MISALIGNED
+    assert f(D, None, None, 16, 0, 8, 2, D, D, D, D, D, None, None, ctypes.byref(n), None) == INVALID  # w_perm w/o w
+    small = ctypes.c_size_t(8)
+    assert f(D, None, None, 8192, 0, 256, 8, D, D, D, D, None, None, D, ctypes.byref(small), None) == CAPACITY
+
+
+def test_grouped_validation_and_query(lib):
+    n = ctypes.c_size_t(0)
+    f = lib.liger_moe_grouped_swiglu_fwd
+    assert f(D, D, D, D, D, 1024, 256, 128, 8, D, None, D, None, ctypes.byref(n), None) == OK
+    assert n.value >= 4 * 9
+    assert f(D, D, D, D, D, 1024, 256, 96, 8, D, None, D, None, ctypes.byref(n), None) == MISALIGNED
+    assert f(D, D, D, D, D, 1024, 200, 128, 8, D, None, D, None, ctypes.byref(n), None) == MISALIGNED
+    assert f(ctypes.c_void_p(258), D, D, D, D, 1024, 256, 128, 8, D, None, D, None, ctypes.byref(n), None) == MISALIGNED
+    assert f(D, D, D, D, D, 1024, 256, 128, 0, D, None, D, None, ctypes.byref(n), None) == INVALID
+    assert f(D, D, None, D, D, 1024, 256, 128, 8, D, None, D, None, ctypes.byref(n), None) == INVALID
+
+
+def test_bwd_workspace_grows_when_recomputing(lib):
+    a = moe.workspace_bytes("bwd_dx_dw", T=256, H=256, I=128, E=8, k=2, saved_gu=True)
+    b = moe.workspace_bytes("bwd_dx_dw", T=256, H=256, I=128, E=8, k=2, saved_gu=False)
+    R = 512
+    assert a >= R * (256 * 2 * 2 + 2 * 128 * 2) and b >= a + R * 2 * 128 * 2
+
+
+def test_combine_argument_errors(lib):
+    f = lib.liger_moe_combine
+    assert f(D, D, 4, 100, 2, D, None) == MISALIGNED
+    assert f(D, D, -1, 128, 2, D, None) == INVALID
+    assert f(D, D, 4, 128, 33, D, None) == CAPACITY
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
+def test_calls_fail_loudly_without_a_device(lib):
+    # valid arguments, no sm_103 device: the library refuses instead of computing anything
+    assert lib.liger_moe_route_topk(D, 4, 8, 2, D, D, None) == UNSUPPORTED
+    with pytest.raises(RuntimeError):  # LigerMoEError or torch's "no CUDA" error: never a silent result
+        moe.device_error()
