@@ -109,6 +109,28 @@ int liger_moe_dispatch(const int32_t* topk_ids, const float* topk_w, const void*
                        size_t* workspace_bytes, void* stream);
 
 /*
+ * liger_moe_dispatch_noalloc: liger_moe_dispatch for callers that cannot
+ * allocate device memory (a static memory plan with no room for a workspace,
+ * a plug-in limited to the tensors it is handed, host code that must not
+ * allocate mid-step).  It has no counterpart in the pages; it exists for such
+ * callers.  Same arguments, outputs and results as liger_moe_dispatch, minus
+ * the workspace: its scratch is a fixed 1 MiB array inside this library,
+ * present in the memory of every GPU that loads the library until the
+ * process exits.  It allocates nothing and frees nothing.
+ *   Limit: ceil(T*k / 256) * E * 4 + 512 <= 1 MiB (e.g. T*k <= 131072 at E = 512);
+ *   larger sizes return LIGER_MOE_ERR_CAPACITY before anything is launched.
+ *   The first call on each device looks up the array's device address; make
+ *   that first call before any stream capture.
+ *   All calls on a device share the array: calls that overlap on the GPU
+ *   (e.g. on two streams with no ordering between them) race and give wrong
+ *   results.  The array keeps the last call's contents; nothing in it needs
+ *   to start at zero.
+ */
+int liger_moe_dispatch_noalloc(const int32_t* topk_ids, const float* topk_w, const void* x, int T, int H, int E,
+                               int k, int32_t* counts, int32_t* m_indptr, int32_t* row_to_slot,
+                               int32_t* slot_to_row, float* w_perm, void* x_perm, void* stream);
+
+/*
  * Grouped SwiGLU expert MLP on expert-major rows, with the routing weight
  * applied to the down projection.  LightMoE README, "Grouped GEMM"
  * (out = a[rows_e] @ b[e]^T, b laid out [num_experts, N, K]) and "MoE
