@@ -202,7 +202,7 @@ def run_reference(args, rank, world):
     import oracle
     import synthetic
 
-    wl = synthetic.WORKLOADS[args.workload]
+    wl = synthetic.workload(args.workload)
     inp = synthetic.make_inputs(wl, seed=args.seed)
     ids, w = oracle.route_topk(inp["logits"], wl.k)
     total_steps = args.warmup + args.steps
@@ -249,7 +249,7 @@ def run_ours(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    wl = synthetic.WORKLOADS[args.workload]
+    wl = synthetic.workload(args.workload)
     T, H, I, E, k, R = wl.T, wl.H, wl.I, wl.E, wl.k, wl.R
     inp = synthetic.make_inputs(wl, seed=args.seed)
 

@@ -184,9 +184,11 @@ int liger_moe_combine(const void* y_perm, const int32_t* slot_to_row, int T, int
  *                                experts, gamma_j = <dY, expert-j output>; 0 elsewhere
  * Weight gradients are summed in a fixed order (no atomics): results are
  * identical from run to run.  The upstream gradient enters the expert GEMMs
- * unscaled; the routing weight is applied in fp32 to the dH accumulator, and
- * bf16(w * h) is the second operand of dW_down.  Workspace: about
- * R*(2H + 3I)*2 bytes, plus R*2I*4 more when gu_perm is NULL.
+ * unscaled; the routing weight is applied in fp32 to the dH accumulator.  The
+ * weight-gradient GEMMs take their non-input operand (dgu for dW_gate_up,
+ * w * h for dW_down) as two bf16 parts, hi + lo, so that operand carries
+ * about 16 significant bits.  Limit: T*k < 2^30.  Workspace: about
+ * R*(2H + 6I)*2 bytes, plus R*2I*4 more when gu_perm is NULL.
  */
 int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const void* h_perm, const float* gu_perm,
                         const int32_t* topk_ids, const float* topk_w, const int32_t* m_indptr,

@@ -148,9 +148,9 @@ namespace {
 size_t bwd_workspace_bytes(long long R, int H, int I, int E, bool recompute_gu) {
   size_t b = schedule_bytes(E);
   b += align_up(static_cast<size_t>(R) * H * 2, 256);                 // dy_perm
-  b += align_up(static_cast<size_t>(R) * 2 * I * 2, 256);             // dgu
+  b += align_up(static_cast<size_t>(R) * 2 * I * 2 * 2, 256);         // dgu (hi, lo)
   b += align_up(static_cast<size_t>(R) * H * 2, 256);                 // dx_perm
-  b += align_up(static_cast<size_t>(R) * I * 2, 256);                 // hw_perm
+  b += align_up(static_cast<size_t>(R) * I * 2 * 2, 256);             // hw_perm (hi, lo)
   b += align_up(static_cast<size_t>(R) * gdot_tiles(I) * 4, 256);     // gdot
   if (recompute_gu) b += align_up(static_cast<size_t>(R) * 2 * I * 4, 256);
   return b;
@@ -280,6 +280,7 @@ LIGER_MOE_API int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const 
   if (int rc = check_topk(T, E, k)) return rc;
   const long long R = static_cast<long long>(T) * k;
   if (int rc = check_shapes(R, H, I, E)) return rc;
+  if (2 * R > kIndexLimit) return LIGER_MOE_ERR_CAPACITY;  // the dW_down operand has 2R rows
   if (workspace_bytes == nullptr || m_indptr == nullptr || w_gate_up == nullptr || w_down == nullptr ||
       dw_gate_up == nullptr || dw_down == nullptr)
     return LIGER_MOE_ERR_INVALID_ARG;
@@ -305,9 +306,9 @@ LIGER_MOE_API int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const 
   uint8_t* cur = static_cast<uint8_t*>(workspace);
   int32_t* tile_prefix = carve<int32_t>(cur, schedule_bytes(E));
   uint16_t* dy_perm = carve<uint16_t>(cur, static_cast<size_t>(R) * H * 2);
-  uint16_t* dgu = carve<uint16_t>(cur, static_cast<size_t>(R) * 2 * I * 2);
+  uint16_t* dgu = carve<uint16_t>(cur, static_cast<size_t>(R) * 2 * I * 2 * 2);
   uint16_t* dx_perm = carve<uint16_t>(cur, static_cast<size_t>(R) * H * 2);
-  uint16_t* hw_perm = carve<uint16_t>(cur, static_cast<size_t>(R) * I * 2);
+  uint16_t* hw_perm = carve<uint16_t>(cur, static_cast<size_t>(R) * I * 2 * 2);
   float* gdot = carve<float>(cur, static_cast<size_t>(R) * gdot_tiles(I) * 4);
   float* gu_ws = recompute ? carve<float>(cur, static_cast<size_t>(R) * 2 * I * 4) : nullptr;
 

@@ -44,9 +44,16 @@ constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64 (MN) x 64 (K) box of an MN-major operand
 constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
 constexpr uint32_t kTmemCols = 2 * BN;
+// Epilogue staging: per epilogue warp two 32-row x 128-byte boxes (128-byte swizzle) that
+// feed TMA bulk stores, so output rows leave the SM as whole lines.
+constexpr int STG_BYTES = 32 * 128;
+constexpr int STG_PER_WARP = 2;
+constexpr int STG_OFFSET = STAGES * STAGE_BYTES;
+constexpr int BAR_OFFSET = STG_OFFSET + kEpiWarps * STG_PER_WARP * STG_BYTES;
 constexpr int kBarrierBytes = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + kBarrierBytes;
+constexpr int SMEM_BYTES = BAR_OFFSET + kBarrierBytes + 1024;
 
 enum class Sched : int { RowsM = 0, RowsK = 1 };
 enum class Epi : int { SwiGLU = 0, ScaleRows = 1, DH = 2, Store = 3 };
@@ -61,6 +68,11 @@ struct Params {
   int b_rows_per_expert;  // rows of B's tensor map per expert
   int b_split;            // SwiGLU: row offset of the up half of W_gu (= I)
   int M_out;              // RowsK: output rows per expert
+  int k_halves;           // RowsK: 2 = the K loop runs twice over the expert's rows; the second
+                          //        pass reads A rows + a_split_rows and B rows + b_split_rows
+                          //        (an operand stored as bf16 hi and lo parts)
+  int a_split_rows;       // RowsK: row offset of A's second part
+  int b_split_rows;       // RowsK: row offset of B's second part
   int N_out;              // valid output columns
   int I;
   uint16_t* out;
@@ -73,6 +85,7 @@ struct Params {
   const uint16_t* h_in;   // DH: h [R, I]
   uint16_t* hw_out;       // DH: bf16(w * h) [R, I]
   float* gdot;            // DH: [R, n_tiles] partial <dh, h>
+  long long R;            // DH: rows (offset of the lo half of hw_out)
   int* err;
 };
 
@@ -83,6 +96,7 @@ struct Tile {
   int nt;        // N tile
   int row0;      // RowsK: first global row of the expert
   int kb_count;  // K blocks
+  int kb_half;   // RowsK: K blocks per pass over the expert's rows
 };
 
 template <Sched S>
@@ -105,6 +119,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p) {
     tl.rows = min(BM, end - tl.m0);
     tl.row0 = 0;
     tl.kb_count = p.num_kb;
+    tl.kb_half = p.num_kb;
   } else {
     const int per_e = p.m_tiles * p.n_tiles;
     tl.e = t / per_e;
@@ -114,7 +129,8 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p) {
     tl.m0 = mt * BM;
     tl.row0 = __ldg(p.m_indptr + tl.e);
     tl.rows = __ldg(p.m_indptr + tl.e + 1) - tl.row0;
-    tl.kb_count = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
+    tl.kb_half = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
+    tl.kb_count = tl.kb_half * p.k_halves;
   }
   return tl;
 }
@@ -170,114 +186,242 @@ __device__ __forceinline__ void load16_bf16(const uint16_t* src, float (&v)[16])
   }
 }
 
-// Epilogue of one tile for one thread (= one accumulator row).
+// ---------------------------------------------------------------- epilogue output path
+// An epilogue warp owns 32 accumulator rows.  Each output box is 32 rows x 128 bytes
+// (64 bf16 or 32 fp32 columns): every lane writes its row into a swizzled staging buffer,
+// then lane 0 issues one TMA store.  Where only part of the warp's 32 rows belong to the
+// tile (the last tile of an expert), the valid rows are stored directly instead.
+enum class Rows : int { Full = 0, Partial = 1, None = 2 };
+
+struct Stager {
+  uint32_t base;  // this warp's staging buffers (shared address, 1024-aligned)
+  int idx;        // buffer to fill next
+};
+
+template <int RANK>
+__device__ __forceinline__ void emit_box(const CUtensorMap* tm, Stager& st, int lane, const uint32_t (&w)[32], int x,
+                                         int y, int z) {
+  if (lane == 0) bulk_wait_group_read<STG_PER_WARP - 1>();  // the buffer's previous store has read it
+  __syncwarp();
+  const uint32_t row = st.base + st.idx * STG_BYTES + lane * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    st_shared_v4(row + ((c ^ (lane & 7)) << 4), make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]));
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if constexpr (RANK == 3)
+      tma_store_3d(tm, st.base + st.idx * STG_BYTES, x, y, z);
+    else
+      tma_store_2d(tm, st.base + st.idx * STG_BYTES, x, y);
+    bulk_commit_group();
+  }
+  st.idx = (st.idx + 1) % STG_PER_WARP;
+}
+
+// One 128-byte output row segment: a TMA box for full slices, direct stores otherwise.
+__device__ __forceinline__ void emit_row(Rows mode, bool row_ok, const CUtensorMap* tm, Stager& st, int lane,
+                                         const uint32_t (&w)[32], int x, int y, void* direct) {
+  if (mode == Rows::Full) {
+    emit_box<2>(tm, st, lane, w, x, y, 0);
+  } else if (row_ok) {
+    uint4* d = reinterpret_cast<uint4*>(direct);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) d[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  }
+}
+
+template <Sched S>
+__device__ __forceinline__ Rows slice_mode(const Tile& tl, int sub) {
+  if constexpr (S == Sched::RowsK) return Rows::Full;  // 3D output maps clip the M tail
+  const int n = tl.rows - sub * 32;
+  return n >= 32 ? Rows::Full : (n > 0 ? Rows::Partial : Rows::None);
+}
+
+// Epilogue of one tile for one warp (each lane = one accumulator row).
 template <Sched S, Epi EP>
-__device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, int row_local, const Params& p) {
+__device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, int sub, int lane, const Params& p,
+                                              const CUtensorMap* tmC0, const CUtensorMap* tmC1, Stager& st) {
+  const int row_local = sub * 32 + lane;
+  const Rows mode = slice_mode<S>(tl, sub);
+  if (mode == Rows::None) return;
+  const bool row_ok = (S == Sched::RowsK) ? true : row_local < tl.rows;
   if constexpr (EP == Epi::SwiGLU) {
     // accumulator columns [0, BN/2) = g, [BN/2, BN) = u for output columns nt*BN/2 + c
-    const bool ok = row_local < tl.rows;
     const long long r = tl.m0 + row_local;
+    const int y = tl.m0 + sub * 32;
     const int j0 = tl.nt * (BN / 2);
 #pragma unroll 1
-    for (int c = 0; c < BN / 2; c += 16) {
-      float g[16], u[16];
-      tmem_ld16(t_row + c, g);
-      tmem_ld16(t_row + BN / 2 + c, u);
-      tmem_ld_wait();
-      const int col = j0 + c;
-      if (ok && col < p.I) {
-        if (p.out != nullptr) {
-          float h[16];
+    for (int q = 0; q < 2; ++q) {
+      const int col = j0 + q * 64;
+      if (col >= p.I) break;
+      uint32_t hw[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) h[i] = silu_f(g[i]) * u[i];
-          store16_bf16(p.out + r * p.ld_out + col, h);
-        }
+      for (int half = 0; half < 2; ++half) {
+        float g[32], u[32];
+        tmem_ld32(t_row + q * 64 + half * 32, g);
+        tmem_ld32(t_row + BN / 2 + q * 64 + half * 32, u);
+        tmem_ld_wait();
         if (p.gu_out != nullptr) {
-          store16_f32(p.gu_out + r * (2LL * p.I) + col, g);
-          store16_f32(p.gu_out + r * (2LL * p.I) + p.I + col, u);
-        }
-      }
-    }
-  } else if constexpr (EP == Epi::ScaleRows) {
-    const bool ok = row_local < tl.rows;
-    const long long r = tl.m0 + row_local;
-    const float sc = ok ? __ldg(p.row_scale + r) : 0.f;
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
-      float v[16];
-      tmem_ld16(t_row + c, v);
-      tmem_ld_wait();
-      const int col = tl.nt * BN + c;
-      if (ok && col < p.N_out) {
+          uint32_t gw[32], uw[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] *= sc;
-        store16_bf16(p.out + r * p.ld_out + col, v);
+          for (int i = 0; i < 32; ++i) {
+            gw[i] = __float_as_uint(g[i]);
+            uw[i] = __float_as_uint(u[i]);
+          }
+          const int xg = col + half * 32;
+          emit_row(mode, row_ok, tmC1, st, lane, gw, xg, y, p.gu_out + r * (2LL * p.I) + xg);
+          emit_row(mode, row_ok, tmC1, st, lane, uw, p.I + xg, y, p.gu_out + r * (2LL * p.I) + p.I + xg);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          hw[half * 16 + i] = pack_bf16x2(silu_f(g[2 * i]) * u[2 * i], silu_f(g[2 * i + 1]) * u[2 * i + 1]);
       }
+      if (p.out != nullptr) emit_row(mode, row_ok, tmC0, st, lane, hw, col, y, p.out + r * p.ld_out + col);
     }
   } else if constexpr (EP == Epi::DH) {
     // acc = dHu = dY[token] W_d[e] for this row; dh = w_r * dHu in fp32.  g, u (fp32) and h
-    // come from the saved forward state.  Writes dgu = [dg | du] (bf16), hw = bf16(w_r * h)
-    // (the dW_down operand) and the partial router-gradient dot <dh, h> of this N tile.
-    const bool ok = row_local < tl.rows;
+    // come from the saved forward state.  Every bf16 operand of the weight-gradient GEMMs is
+    // written as two bf16 parts, hi = bf16(v) in rows [0, R) and lo = bf16(v - hi) in rows
+    // [R, 2R), so that hi + lo carries v to about 2^-17 relative:
+    //   dgu = [dg | du]  ([2R, 2I]; the dX GEMM reads only the hi rows)
+    //   hw  = w_r * h    ([2R, I], the dW_down operand)
+    // plus the partial router-gradient dot <dh, h> of this N tile.
+    // Outputs leave through 32-row x 16-column boxes (32-byte swizzle), six per 16 columns.
     const long long r = tl.m0 + row_local;
     const long long two_i = 2LL * p.I;
-    const float wr = ok ? __ldg(p.row_scale + r) : 0.f;
+    const int y = tl.m0 + sub * 32;
+    const float wr = row_ok ? __ldg(p.row_scale + r) : 0.f;
     float part = 0.f;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 16) {
+      const int n = tl.nt * BN + c;
+      if (n >= p.I) break;
       float dh[16];
       tmem_ld16(t_row + c, dh);
       tmem_ld_wait();
-      const int n = tl.nt * BN + c;
-      if (ok && n < p.I) {
-        float g[16], u[16], h[16], dg[16], du[16];
+      uint32_t o[6][8];  // dg hi, dg lo, du hi, du lo, hw hi, hw lo (8 bf16 pairs each)
+      if (row_ok) {
+        float g[16], u[16], h[16];
         load16_f32(p.gu_in + r * two_i + n, g);
         load16_f32(p.gu_in + r * two_i + p.I + n, u);
         load16_bf16(p.h_in + r * p.I + n, h);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float d = wr * dh[i];
-          part += d * h[i];
-          const float sg = 1.0f / (1.0f + expf(-g[i]));
-          dg[i] = d * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
-          du[i] = d * g[i] * sg;
-          h[i] *= wr;
+        for (int i = 0; i < 16; i += 2) {
+          float v[3][2];
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int q = i + e2;
+            const float d = wr * dh[q];
+            part += d * h[q];
+            const float sg = 1.0f / (1.0f + expf(-g[q]));
+            v[0][e2] = d * u[q] * sg * (1.0f + g[q] * (1.0f - sg));
+            v[1][e2] = d * g[q] * sg;
+            v[2][e2] = wr * h[q];
+          }
+#pragma unroll
+          for (int f = 0; f < 3; ++f) {
+            const uint32_t hi = pack_bf16x2(v[f][0], v[f][1]);
+            o[2 * f][i / 2] = hi;
+            o[2 * f + 1][i / 2] = pack_bf16x2(v[f][0] - bf16_lo(hi), v[f][1] - bf16_hi(hi));
+          }
         }
-        store16_bf16(p.out2 + r * two_i + n, dg);
-        store16_bf16(p.out2 + r * two_i + p.I + n, du);
-        store16_bf16(p.hw_out + r * p.I + n, h);
+      } else {
+#pragma unroll
+        for (int f = 0; f < 6; ++f)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o[f][i] = 0u;
+      }
+      if (mode == Rows::Full) {
+        if (lane == 0) bulk_wait_group_read<0>();  // previous boxes have been read
+        __syncwarp();
+#pragma unroll
+        for (int f = 0; f < 6; ++f) {
+          // box f at st.base + f*1 KB: row = lane (32 bytes), 32-byte swizzle (chunk ^= (row >> 2) & 1)
+          const uint32_t row_addr = st.base + f * 1024 + lane * 32;
+          const uint32_t sw = (lane >> 2) & 1;
+          st_shared_v4(row_addr + ((0 ^ sw) << 4), make_uint4(o[f][0], o[f][1], o[f][2], o[f][3]));
+          st_shared_v4(row_addr + ((1 ^ sw) << 4), make_uint4(o[f][4], o[f][5], o[f][6], o[f][7]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int yl = y + static_cast<int>(p.R);
+          tma_store_2d(tmC0, st.base + 0 * 1024, n, y);
+          tma_store_2d(tmC0, st.base + 1 * 1024, n, yl);
+          tma_store_2d(tmC0, st.base + 2 * 1024, p.I + n, y);
+          tma_store_2d(tmC0, st.base + 3 * 1024, p.I + n, yl);
+          tma_store_2d(tmC1, st.base + 4 * 1024, n, y);
+          tma_store_2d(tmC1, st.base + 5 * 1024, n, yl);
+          bulk_commit_group();
+        }
+      } else if (row_ok) {
+        uint16_t* dst[6] = {p.out2 + r * two_i + n, p.out2 + (p.R + r) * two_i + n, p.out2 + r * two_i + p.I + n,
+                            p.out2 + (p.R + r) * two_i + p.I + n, p.hw_out + r * p.I + n,
+                            p.hw_out + (p.R + r) * p.I + n};
+#pragma unroll
+        for (int f = 0; f < 6; ++f) {
+          reinterpret_cast<uint4*>(dst[f])[0] = make_uint4(o[f][0], o[f][1], o[f][2], o[f][3]);
+          reinterpret_cast<uint4*>(dst[f])[1] = make_uint4(o[f][4], o[f][5], o[f][6], o[f][7]);
+        }
       }
     }
-    if (ok) p.gdot[r * p.n_tiles + tl.nt] = part;
-  } else {  // Store
-    long long row;
-    bool ok;
-    if constexpr (S == Sched::RowsM) {
-      ok = row_local < tl.rows;
-      row = tl.m0 + row_local;
-    } else {
-      ok = tl.m0 + row_local < p.M_out;
-      row = static_cast<long long>(tl.e) * (p.out_expert_stride / p.ld_out) + tl.m0 + row_local;
-    }
+    if (row_ok) p.gdot[r * p.n_tiles + tl.nt] = part;
+  } else {  // ScaleRows, Store
+    float sc = 1.f;
+    if constexpr (EP == Epi::ScaleRows) sc = row_ok ? __ldg(p.row_scale + tl.m0 + row_local) : 0.f;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
-      float v[16];
-      tmem_ld16(t_row + c, v);
+    for (int q = 0; q < BN / 64; ++q) {
+      const int col = tl.nt * BN + q * 64;
+      if (col >= p.N_out) break;
+      float a[32], b[32];
+      tmem_ld32(t_row + q * 64, a);
+      tmem_ld32(t_row + q * 64 + 32, b);
       tmem_ld_wait();
-      const int col = tl.nt * BN + c;
-      if (ok && col < p.N_out) store16_bf16(p.out + row * p.ld_out + col, v);
+      uint32_t w[32];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        w[i] = pack_bf16x2(sc * a[2 * i], sc * a[2 * i + 1]);
+        w[16 + i] = pack_bf16x2(sc * b[2 * i], sc * b[2 * i + 1]);
+      }
+      if constexpr (S == Sched::RowsK) {
+        emit_box<3>(tmC0, st, lane, w, col, tl.m0 + sub * 32, tl.e);
+      } else {
+        const long long r = tl.m0 + row_local;
+        emit_row(mode, row_ok, tmC0, st, lane, w, col, tl.m0 + sub * 32, p.out + r * p.ld_out + col);
+      }
     }
   }
 }
 
 // RowsK tile of an expert with no rows: the gradient block is exactly zero.
-__device__ __forceinline__ void store_zero_tile(const Tile& tl, int row_local, const Params& p) {
-  if (tl.m0 + row_local >= p.M_out) return;
-  const long long row = static_cast<long long>(tl.e) * (p.out_expert_stride / p.ld_out) + tl.m0 + row_local;
-  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-  for (int c = 0; c < BN; c += 8) {
-    const int col = tl.nt * BN + c;
-    if (col < p.N_out) *reinterpret_cast<uint4*>(p.out + row * p.ld_out + col) = z;
+__device__ __forceinline__ void store_zero_tile(const Tile& tl, int sub, int lane, const Params& p,
+                                                const CUtensorMap* tmC0, Stager& st) {
+  uint32_t w[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) w[i] = 0u;
+  for (int q = 0; q < BN / 64; ++q) {
+    const int col = tl.nt * BN + q * 64;
+    if (col >= p.N_out) break;
+    emit_box<3>(tmC0, st, lane, w, col, tl.m0 + sub * 32, tl.e);
+  }
+}
+
+// DH epilogue operands of one tile row (fp32 g and u, bf16 h) are pulled into L2 ahead of
+// time, one tile early, so the epilogue's loads do not wait on DRAM.
+template <Sched S, Epi EP>
+__device__ __forceinline__ void prefetch_epilogue_operands(int t, int total, int row_local, const Params& p) {
+  if constexpr (EP == Epi::DH) {
+    if (t >= total) return;
+    const Tile tl = decode_tile<S>(t, p);
+    if (row_local >= tl.rows) return;
+    const long long r = tl.m0 + row_local;
+    const int n0 = tl.nt * BN;
+    const int ncols = min(BN, p.I - n0);
+    if (ncols <= 0) return;
+    prefetch_l2_bulk(p.gu_in + r * 2LL * p.I + n0, ncols * 4);
+    prefetch_l2_bulk(p.gu_in + r * 2LL * p.I + p.I + n0, ncols * 4);
+    prefetch_l2_bulk(p.h_in + r * p.I + n0, ncols * 2);
   }
 }
 
@@ -297,12 +441,13 @@ __device__ __forceinline__ void zero_tail_rows(uint8_t* stage_ptr, int valid, in
 template <Sched S, Epi EP, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
                         const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (sbase - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + STAGES * STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + BAR_OFFSET);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -330,6 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC0);
+    tma_prefetch_desc(&tmC1);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -364,11 +511,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sb = sa + A_BYTES;
           const uint32_t fb = full0 + 8 * stage;
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const int kr = kb % tl.kb_half;  // K block within the pass over the expert's rows
           if constexpr (!A_MN) {
             tma_load_2d(sa, &tmA, fb, kb * BK, tl.m0);
           } else {
 #pragma unroll
-            for (int i = 0; i < BM / 64; ++i) tma_load_2d(sa + i * MN_BOX_BYTES, &tmA, fb, tl.m0 + 64 * i, tl.row0 + kb * BK);
+            for (int i = 0; i < BM / 64; ++i)
+              tma_load_2d(sa + i * MN_BOX_BYTES, &tmA, fb, tl.m0 + 64 * i,
+                          tl.row0 + kr * BK + (kb >= tl.kb_half ? p.a_split_rows : 0));
           }
           if constexpr (!B_MN) {
             if constexpr (EP == Epi::SwiGLU) {
@@ -379,7 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d(sb, &tmB, fb, kb * BK, tl.e * p.b_rows_per_expert + tl.nt * BN);
             }
           } else {
-            const int krow = (S == Sched::RowsM) ? tl.e * p.b_rows_per_expert + kb * BK : tl.row0 + kb * BK;
+            const int krow = (S == Sched::RowsM) ? tl.e * p.b_rows_per_expert + kb * BK
+                                                 : tl.row0 + kr * BK + (kb >= tl.kb_half ? p.b_split_rows : 0);
 #pragma unroll
             for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * MN_BOX_BYTES, &tmB, fb, tl.nt * BN + 64 * i, krow);
           }
@@ -422,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sa = sbase + stage * STAGE_BYTES;
         const uint32_t sb = sa + A_BYTES;
         if constexpr (S == Sched::RowsK) {
-          const int valid = tl.rows - kb * BK;
+          const int valid = tl.rows - (kb % tl.kb_half) * BK;
           if (valid < BK) {
             zero_tail_rows(base_ptr + stage * STAGE_BYTES, valid, lane);
             fence_proxy_async_smem();
@@ -463,12 +614,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int sub = warp & 3;  // TMEM lane quadrant this warp may access
     const int row_local = sub * 32 + lane;
+    Stager st{sbase + STG_OFFSET + static_cast<uint32_t>((warp - 2) * STG_PER_WARP * STG_BYTES), 0};
     int acc = 0;
     uint32_t acc_phase = 0;
+    prefetch_epilogue_operands<S, EP>(blockIdx.x, total, row_local, p);
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode_tile<S>(t, p);
+      prefetch_epilogue_operands<S, EP>(t + gridDim.x, total, row_local, p);
       if (tl.kb_count == 0) {
-        if constexpr (S == Sched::RowsK) store_zero_tile(tl, row_local, p);
+        if constexpr (S == Sched::RowsK) store_zero_tile(tl, sub, lane, p, &tmC0, st);
         continue;
       }
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag))) {
@@ -477,13 +631,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epilogue_tile<S, EP>(t_row, tl, row_local, p);
+      epilogue_tile<S, EP>(t_row, tl, sub, lane, p, &tmC0, &tmC1, st);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    // outputs are in global memory (and the staging buffers free) before the CTA exits
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
   }
 
   tc_fence_before_sync();
@@ -557,25 +714,60 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major bf16 matrix [outer, inner] -> 2D tensor map with a {box_inner, box_outer}
-// box, 128-byte swizzle, zero fill outside the matrix.
-int make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer) {
+// Row-major tensor (dims[0] innermost) -> tensor map with the given box, 128-byte swizzle,
+// zero fill outside the tensor on loads, clipping outside it on stores.
+int make_tmap_nd(CUtensorMap* m, const void* ptr, CUtensorMapDataType dtype, int elem_bytes, int rank,
+                 const uint64_t* dims, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return LIGER_MOE_ERR_LAUNCH;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t es[2] = {1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  cuuint64_t d[3], strides[2];
+  cuuint32_t b[3], es[3] = {1, 1, 1};
+  uint64_t stride = static_cast<uint64_t>(elem_bytes);
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    if (i > 0) strides[i - 1] = stride;
+    stride *= dims[i];
+  }
+  const CUresult r = enc(m, dtype, rank, const_cast<void*>(ptr), d, strides, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? LIGER_MOE_OK : LIGER_MOE_ERR_LAUNCH;
 }
 
+// bf16 matrix [outer, inner] with a {box_inner, box_outer} box.
+int make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+              uint32_t box_outer) {
+  const uint64_t dims[2] = {inner, outer};
+  const uint32_t box[2] = {box_inner, box_outer};
+  return make_tmap_nd(m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, dims, box);
+}
+
+// Output maps: one epilogue box is 32 rows x 128 bytes.
+int make_out_bf16(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows) {
+  return make_tmap(m, ptr, cols, rows, 64, 32);
+}
+int make_out_f32(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows) {
+  const uint64_t dims[2] = {cols, rows};
+  const uint32_t box[2] = {32, 32};
+  return make_tmap_nd(m, ptr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2, dims, box);
+}
+// 32-row x 16-column bf16 boxes with a 32-byte swizzle (the dH epilogue's outputs).
+int make_out_bf16_narrow(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows) {
+  const uint64_t dims[2] = {cols, rows};
+  const uint32_t box[2] = {16, 32};
+  return make_tmap_nd(m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, dims, box, CU_TENSOR_MAP_SWIZZLE_32B);
+}
+// [E, rows, cols] bf16 weight gradient: the 3D map clips each expert's block at its own row count.
+int make_out_bf16_3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t experts) {
+  const uint64_t dims[3] = {cols, rows, experts};
+  const uint32_t box[3] = {64, 32, 1};
+  return make_tmap_nd(m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3, dims, box);
+}
+
 template <Sched S, Epi EP, bool A_MN, bool B_MN>
-int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, int grid, cudaStream_t s,
-                const char* name) {
+int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc0, const CUtensorMap& tc1,
+                const Params& p, int grid, cudaStream_t s, const char* name) {
   auto kern = grouped_gemm_kernel<S, EP, A_MN, B_MN>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -589,7 +781,7 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, i
   if (grid < 1) return LIGER_MOE_OK;
   {
     KernelScope trace(name, s);
-    kern<<<grid, kThreads, SMEM_BYTES, s>>>(ta, tb, p);
+    kern<<<grid, kThreads, SMEM_BYTES, s>>>(ta, tb, tc0, tc1, p);
   }
   return check_launch(name);
 }
@@ -645,7 +837,14 @@ int launch_gate_up(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) 
   p.out = a.h_perm;
   p.ld_out = a.I;
   p.gu_out = a.gu_perm;
-  return launch_gemm<Sched::RowsM, Epi::SwiGLU, false, false>(ta, tb, p, rows_m_grid(a.R, a.E, p.n_tiles, dev), s,
+  CUtensorMap tc0, tc1;  // h (bf16) and [g|u] (fp32); an absent output reuses the other's map
+  if (a.h_perm != nullptr && make_out_bf16(&tc0, a.h_perm, a.I, a.R)) return LIGER_MOE_ERR_LAUNCH;
+  if (a.gu_perm != nullptr && make_out_f32(&tc1, a.gu_perm, 2ULL * a.I, a.R)) return LIGER_MOE_ERR_LAUNCH;
+  if (a.h_perm == nullptr) tc0 = tc1;
+  if (a.gu_perm == nullptr) tc1 = tc0;
+  if (a.h_perm == nullptr && a.gu_perm == nullptr) return LIGER_MOE_OK;
+  return launch_gemm<Sched::RowsM, Epi::SwiGLU, false, false>(ta, tb, tc0, tc1, p,
+                                                               rows_m_grid(a.R, a.E, p.n_tiles, dev), s,
                                                                "gemm_gate_up_swiglu");
 }
 
@@ -663,8 +862,11 @@ int launch_down(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.out = a.y_perm;
   p.ld_out = a.H;
   p.row_scale = a.w_perm;
-  return launch_gemm<Sched::RowsM, Epi::ScaleRows, false, false>(ta, tb, p, rows_m_grid(a.R, a.E, p.n_tiles, dev),
-                                                                  s, "gemm_down_scale");
+  CUtensorMap tc0;
+  if (make_out_bf16(&tc0, a.y_perm, a.H, a.R)) return LIGER_MOE_ERR_LAUNCH;
+  return launch_gemm<Sched::RowsM, Epi::ScaleRows, false, false>(ta, tb, tc0, tc0, p,
+                                                                  rows_m_grid(a.R, a.E, p.n_tiles, dev), s,
+                                                                  "gemm_down_scale");
 }
 
 int launch_bwd_dh(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
@@ -684,8 +886,12 @@ int launch_bwd_dh(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.hw_out = a.hw_perm;
   p.row_scale = a.w_perm;
   p.gdot = a.gdot;
-  return launch_gemm<Sched::RowsM, Epi::DH, false, true>(ta, tb, p, rows_m_grid(a.R, a.E, p.n_tiles, dev), s,
-                                                          "gemm_bwd_dh");
+  p.R = a.R;
+  CUtensorMap tc0, tc1;  // dgu [2R, 2I] and hw [2R, I]: hi rows then lo rows
+  if (make_out_bf16_narrow(&tc0, a.dgu, 2ULL * a.I, 2ULL * a.R) || make_out_bf16_narrow(&tc1, a.hw_perm, a.I, 2ULL * a.R))
+    return LIGER_MOE_ERR_LAUNCH;
+  return launch_gemm<Sched::RowsM, Epi::DH, false, true>(ta, tb, tc0, tc1, p, rows_m_grid(a.R, a.E, p.n_tiles, dev),
+                                                          s, "gemm_bwd_dh");
 }
 
 int launch_bwd_dx(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
@@ -702,8 +908,10 @@ int launch_bwd_dx(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.I = a.I;
   p.out = a.dx_perm;
   p.ld_out = a.H;
-  return launch_gemm<Sched::RowsM, Epi::Store, false, true>(ta, tb, p, rows_m_grid(a.R, a.E, p.n_tiles, dev), s,
-                                                             "gemm_bwd_dx");
+  CUtensorMap tc0;
+  if (make_out_bf16(&tc0, a.dx_perm, a.H, a.R)) return LIGER_MOE_ERR_LAUNCH;
+  return launch_gemm<Sched::RowsM, Epi::Store, false, true>(ta, tb, tc0, tc0, p,
+                                                             rows_m_grid(a.R, a.E, p.n_tiles, dev), s, "gemm_bwd_dx");
 }
 
 int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
@@ -713,31 +921,45 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   CUtensorMap ta, tb;
   const uint64_t rows = a.R > 0 ? static_cast<uint64_t>(a.R) : 1;
   Params p = base_params(a.m_indptr, nullptr, a.E, dev.err_flag);
-  if (make_tmap(&ta, a.R > 0 ? a.dgu : a.dw_gate_up, 2ULL * a.I, rows, 64, BK) ||
+  // dW_gu[e] = dgu_hi_e^T x_e + dgu_lo_e^T x_e: the K loop walks the expert's rows twice,
+  // the second time with A in the lo half of dgu ([2R, 2I]).
+  if (make_tmap(&ta, a.R > 0 ? a.dgu : a.dw_gate_up, 2ULL * a.I, 2 * rows, 64, BK) ||
       make_tmap(&tb, a.R > 0 ? a.x_perm : a.dw_gate_up, a.H, rows, 64, BK))
     return LIGER_MOE_ERR_LAUNCH;
   p.m_tiles = cdiv(2LL * a.I, BM);
   p.n_tiles = cdiv(a.H, BN);
+  p.k_halves = 2;
+  p.a_split_rows = static_cast<int>(a.R);
+  p.b_split_rows = 0;
   p.M_out = 2 * a.I;
   p.N_out = a.H;
   p.out = a.dw_gate_up;
   p.ld_out = a.H;
   p.out_expert_stride = 2LL * a.I * a.H;
+  CUtensorMap tc0;
+  if (make_out_bf16_3d(&tc0, a.dw_gate_up, a.H, 2ULL * a.I, a.E)) return LIGER_MOE_ERR_LAUNCH;
   int rc = launch_gemm<Sched::RowsK, Epi::Store, true, true>(
-      ta, tb, p, rows_k_grid(static_cast<long long>(a.E) * p.m_tiles * p.n_tiles, dev), s, "gemm_bwd_dw_gate_up");
+      ta, tb, tc0, tc0, p, rows_k_grid(static_cast<long long>(a.E) * p.m_tiles * p.n_tiles, dev), s,
+      "gemm_bwd_dw_gate_up");
   if (rc) return rc;
+  // dW_d[e] = dY_e^T hw_hi_e + dY_e^T hw_lo_e: the second pass reads B in the lo half of hw ([2R, I]).
   if (make_tmap(&ta, a.R > 0 ? a.dy_perm : a.dw_down, a.H, rows, 64, BK) ||
-      make_tmap(&tb, a.R > 0 ? a.hw_perm : a.dw_down, a.I, rows, 64, BK))
+      make_tmap(&tb, a.R > 0 ? a.hw_perm : a.dw_down, a.I, 2 * rows, 64, BK))
     return LIGER_MOE_ERR_LAUNCH;
   p.m_tiles = cdiv(a.H, BM);
   p.n_tiles = cdiv(a.I, BN);
+  p.k_halves = 2;
+  p.a_split_rows = 0;
+  p.b_split_rows = static_cast<int>(a.R);
   p.M_out = a.H;
   p.N_out = a.I;
   p.out = a.dw_down;
   p.ld_out = a.I;
   p.out_expert_stride = 1LL * a.H * a.I;
+  if (make_out_bf16_3d(&tc0, a.dw_down, a.I, a.H, a.E)) return LIGER_MOE_ERR_LAUNCH;
   return launch_gemm<Sched::RowsK, Epi::Store, true, true>(
-      ta, tb, p, rows_k_grid(static_cast<long long>(a.E) * p.m_tiles * p.n_tiles, dev), s, "gemm_bwd_dw_down");
+      ta, tb, tc0, tc0, p, rows_k_grid(static_cast<long long>(a.E) * p.m_tiles * p.n_tiles, dev), s,
+      "gemm_bwd_dw_down");
 }
 
 }  // namespace lmoe

@@ -83,8 +83,8 @@ struct BwdGemmArgs {
   const float* gu;       // [R, 2I] fp32 [g | u] (saved or recomputed)
   const uint16_t* dy_perm;  // [R, H] dY[token of row]
   const float* w_perm;   // [R]
-  uint16_t* hw_perm;     // [R, I] bf16(w_perm * h)
-  uint16_t* dgu;         // [R, 2I]
+  uint16_t* hw_perm;     // [2R, I]: rows [0,R) bf16(w h), rows [R,2R) bf16(w h - hi)
+  uint16_t* dgu;         // [2R, 2I]: rows [0,R) bf16(dgu), rows [R,2R) bf16(dgu - hi)
   uint16_t* dx_perm;     // [R, H]
   float* gdot;           // [R, ceil(I / 256)]
   uint16_t* dw_gate_up;  // [E, 2I, H]

@@ -71,6 +71,19 @@ WORKLOADS = {
 }
 
 
+def workload(name: str) -> Workload:
+    """A named workload, or one spelled out as <label>_T<T>_H<H>_I<I>_E<E>_k<k>[_zipf<s>]."""
+    if name in WORKLOADS:
+        return WORKLOADS[name]
+    import re
+
+    m = re.fullmatch(r"[A-Za-z0-9]+_T(\d+)_H(\d+)_I(\d+)_E(\d+)_k(\d+)(?:_zipf([0-9.]+))?", name)
+    if not m:
+        raise KeyError(f"unknown workload {name!r}")
+    T, H, I, E, k = (int(v) for v in m.groups()[:5])
+    return Workload(name, T, H, I, E, k, zipf_s=float(m.group(6)) if m.group(6) else None)
+
+
 def build(force: bool = False) -> str:
     """Compile gen.c into libsynth.so beside it (gcc, no vendor code)."""
     if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
