@@ -142,8 +142,10 @@ int liger_moe_dispatch_noalloc(const int32_t* topk_ids, const float* topk_w, con
  *   w_down     [E, H, I] bf16.
  *   w_perm     [R] float32: routing weight of each row.
  *   h_perm     [R, I] bf16, output: h = bf16(silu(g) * u)  (saved for backward).
- *   gu_perm    [R, 2I] float32, output or NULL: [g | u], the fp32 accumulators
- *              (saved for backward; when NULL the backward recomputes them).
+ *   gu_perm    [R, 2I] float32, output or NULL: the SwiGLU derivative factors
+ *              [dh/dg | dh/du] = [u s (1 + g (1 - s)) | g s], s = sigmoid(g), from
+ *              the fp32 accumulators g, u (saved for backward; when NULL the
+ *              backward recomputes them).
  *   y_perm     [R, H] bf16, output: bf16(w_perm[r] * (h W_d[e]^T)).
  * fp32 accumulation on the tensor cores.  Workspace: the tile schedule
  * (4*(E+1) bytes, rounded up).
@@ -173,7 +175,7 @@ int liger_moe_combine(const void* y_perm, const int32_t* slot_to_row, int T, int
  * training" (deterministic input-, weight- and router-gradient kernels).
  * Inputs are the forward's saved state:
  *   dy [T, H] bf16; x_perm [R, H] bf16; h_perm [R, I] bf16;
- *   gu_perm [R, 2I] float32 or NULL (then g, u are recomputed from x_perm);
+ *   gu_perm [R, 2I] float32 derivative factors or NULL (then recomputed from x_perm);
  *   topk_ids, topk_w [T, k]; m_indptr [E+1]; row_to_slot, slot_to_row [R];
  *   w_perm [R]; w_gate_up [E, 2I, H]; w_down [E, H, I].
  * Outputs (overwritten):

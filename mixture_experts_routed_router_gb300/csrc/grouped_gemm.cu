@@ -23,9 +23,9 @@
 //          order by one CTA (deterministic, no split-K atomics).  The last
 //          K block's rows that belong to the next expert are zeroed in shared
 //          memory before the MMA reads them.
-// Epilogues: SwiGLU (h = silu(g)*u, optional [g|u] store), ScaleRows
-// (y = w_r * acc), DH (dgu = SwiGLU backward, per-row partial <dh, h> for the
-// router gradient), Store (plain bf16).
+// Epilogues: SwiGLU (h = silu(g)*u, optional fp32 derivative factors), ScaleRows
+// (y = w_r * acc), DH (SwiGLU backward from the saved factors, hi/lo operands for
+// the weight gradients, per-row partial <dh, h> for the router gradient), Store.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -38,7 +38,7 @@
 namespace lmoe {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -50,13 +50,27 @@ constexpr uint32_t kTmemCols = 2 * BN;
 // feed TMA bulk stores, so output rows leave the SM as whole lines.
 constexpr int STG_BYTES = 32 * 128;
 constexpr int STG_PER_WARP = 2;
-constexpr int STG_OFFSET = STAGES * STAGE_BYTES;
-constexpr int BAR_OFFSET = STG_OFFSET + kEpiWarps * STG_PER_WARP * STG_BYTES;
 constexpr int kBarrierBytes = 256;
-constexpr int SMEM_BYTES = BAR_OFFSET + kBarrierBytes + 1024;
+constexpr int kDhBoxBytes = 32 * 32;            // dH epilogue: 32 rows x 16 bf16 columns
+constexpr int kDhSetBytes = 6 * kDhBoxBytes;    // six output boxes per 16 columns
+
+// Shared memory of one CTA: operand stages | epilogue staging | barriers.  The dH kernel
+// keeps 3 operand stages (its MMAs are a small part of its time) to double-buffer its six
+// narrow staging boxes; the others keep 4 stages and two 4 KB staging boxes per warp.
+template <int kDh>
+struct Layout {
+  static constexpr int kStages = kDh ? 3 : 4;
+  static constexpr int kStgWarpBytes = kDh ? 2 * kDhSetBytes : STG_PER_WARP * STG_BYTES;
+  static constexpr int kStgOffset = kStages * STAGE_BYTES;
+  static constexpr int kBarOffset = kStgOffset + kEpiWarps * kStgWarpBytes;
+  static constexpr int kSmemBytes = kBarOffset + kBarrierBytes + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
 
 enum class Sched : int { RowsM = 0, RowsK = 1 };
 enum class Epi : int { SwiGLU = 0, ScaleRows = 1, DH = 2, Store = 3 };
+template <Epi EP>
+using LayoutOf = Layout<EP == Epi::DH ? 1 : 0>;
 
 struct Params {
   const int32_t* m_indptr;     // [E+1]
@@ -78,10 +92,10 @@ struct Params {
   uint16_t* out;
   long long ld_out;
   long long out_expert_stride;
-  uint16_t* out2;         // DH: dgu [R, 2I]
-  float* gu_out;          // SwiGLU: [g|u] fp32 [R, 2I] (nullable)
+  uint16_t* out2;         // DH: dgu [2R, 2I] (hi rows, then lo rows)
+  float* gu_out;          // SwiGLU: derivative factors [a | b] fp32 [R, 2I] (nullable)
   const float* row_scale; // ScaleRows, DH: w_perm
-  const float* gu_in;     // DH: [g|u] fp32 [R, 2I]
+  const float* gu_in;     // DH: derivative factors [a | b] fp32 [R, 2I]
   const uint16_t* h_in;   // DH: h [R, I]
   uint16_t* hw_out;       // DH: bf16(w * h) [R, I]
   float* gdot;            // DH: [R, n_tiles] partial <dh, h>
@@ -141,8 +155,6 @@ __device__ __forceinline__ void raise_abort(int* err, volatile int* abort_flag) 
     *abort_flag = 1;
   }
 }
-
-__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
 
 __device__ __forceinline__ void store16_bf16(uint16_t* dst, const float (&v)[16]) {
   uint4 a, b;
@@ -262,84 +274,88 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
         tmem_ld32(t_row + q * 64 + half * 32, g);
         tmem_ld32(t_row + BN / 2 + q * 64 + half * 32, u);
         tmem_ld_wait();
-        if (p.gu_out != nullptr) {
-          uint32_t gw[32], uw[32];
+        // h = silu(g) u with silu(g) = g s, s = 1 / (1 + exp(-g)); the backward's derivative
+        // factors dh/dg = u s (1 + g (1 - s)) and dh/du = silu(g) are saved in fp32.
+        uint32_t aw[32], bw[32];
+        float hv[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            gw[i] = __float_as_uint(g[i]);
-            uw[i] = __float_as_uint(u[i]);
-          }
+        for (int i = 0; i < 32; ++i) {
+          const float sg = 1.0f / (1.0f + expf(-g[i]));
+          const float sl = g[i] * sg;
+          hv[i] = sl * u[i];
+          aw[i] = __float_as_uint(u[i] * sg * (1.0f + g[i] * (1.0f - sg)));
+          bw[i] = __float_as_uint(sl);
+        }
+        if (p.gu_out != nullptr) {
           const int xg = col + half * 32;
-          emit_row(mode, row_ok, tmC1, st, lane, gw, xg, y, p.gu_out + r * (2LL * p.I) + xg);
-          emit_row(mode, row_ok, tmC1, st, lane, uw, p.I + xg, y, p.gu_out + r * (2LL * p.I) + p.I + xg);
+          emit_row(mode, row_ok, tmC1, st, lane, aw, xg, y, p.gu_out + r * (2LL * p.I) + xg);
+          emit_row(mode, row_ok, tmC1, st, lane, bw, p.I + xg, y, p.gu_out + r * (2LL * p.I) + p.I + xg);
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          hw[half * 16 + i] = pack_bf16x2(silu_f(g[2 * i]) * u[2 * i], silu_f(g[2 * i + 1]) * u[2 * i + 1]);
+        for (int i = 0; i < 16; ++i) hw[half * 16 + i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
       }
       if (p.out != nullptr) emit_row(mode, row_ok, tmC0, st, lane, hw, col, y, p.out + r * p.ld_out + col);
     }
   } else if constexpr (EP == Epi::DH) {
-    // acc = dHu = dY[token] W_d[e] for this row; dh = w_r * dHu in fp32.  g, u (fp32) and h
-    // come from the saved forward state.  Every bf16 operand of the weight-gradient GEMMs is
-    // written as two bf16 parts, hi = bf16(v) in rows [0, R) and lo = bf16(v - hi) in rows
-    // [R, 2R), so that hi + lo carries v to about 2^-17 relative:
-    //   dgu = [dg | du]  ([2R, 2I]; the dX GEMM reads only the hi rows)
-    //   hw  = w_r * h    ([2R, I], the dW_down operand)
-    // plus the partial router-gradient dot <dh, h> of this N tile.
-    // Outputs leave through 32-row x 16-column boxes (32-byte swizzle), six per 16 columns.
+    // acc = dHu = dY[token] W_d[e] for this row; d = w_r * dHu in fp32.  The saved forward
+    // state gives the SwiGLU derivative factors a = dh/dg, b = dh/du (fp32) and h (bf16):
+    //   dg = d a,  du = d b,  <d, h> (router-gradient partial),  w_r h (the dW_down operand).
+    // Every bf16 operand of the weight-gradient GEMMs is written as two bf16 parts,
+    // hi = bf16(v) in rows [0, R) and lo = bf16(v - hi) in rows [R, 2R), so that hi + lo
+    // carries v to about 2^-17 relative:  dgu = [dg | du] ([2R, 2I]; the dX GEMM reads only
+    // the hi rows) and hw = w_r h ([2R, I]).  Outputs leave through 32-row x 16-column boxes
+    // (32-byte swizzle), six per 16 columns, double-buffered; the loads of the next 16
+    // columns are issued before the current ones are processed.
     const long long r = tl.m0 + row_local;
     const long long two_i = 2LL * p.I;
     const int y = tl.m0 + sub * 32;
+    const int n0 = tl.nt * BN;
+    const int ncols = min(BN, p.I - n0);  // a positive multiple of 64
     const float wr = row_ok ? __ldg(p.row_scale + r) : 0.f;
+    const float* arow = p.gu_in + r * two_i;
+    const uint16_t* hrow = p.h_in + r * p.I;
     float part = 0.f;
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
-      const int n = tl.nt * BN + c;
-      if (n >= p.I) break;
+    int set = 0;
+    auto load_ops = [&](int n, float (&a)[16], float (&b)[16], float (&h)[16]) {
+      if (row_ok) {
+        load16_f32(arow + n, a);
+        load16_f32(arow + p.I + n, b);
+        load16_bf16(hrow + n, h);
+      }
+    };
+    auto process = [&](int c, const float (&a)[16], const float (&b)[16], const float (&h)[16]) {
       float dh[16];
       tmem_ld16(t_row + c, dh);
       tmem_ld_wait();
       uint32_t o[6][8];  // dg hi, dg lo, du hi, du lo, hw hi, hw lo (8 bf16 pairs each)
-      if (row_ok) {
-        float g[16], u[16], h[16];
-        load16_f32(p.gu_in + r * two_i + n, g);
-        load16_f32(p.gu_in + r * two_i + p.I + n, u);
-        load16_bf16(p.h_in + r * p.I + n, h);
 #pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-          float v[3][2];
+      for (int i = 0; i < 16; i += 2) {
+        float v[3][2];
 #pragma unroll
-          for (int e2 = 0; e2 < 2; ++e2) {
-            const int q = i + e2;
-            const float d = wr * dh[q];
-            part += d * h[q];
-            const float sg = 1.0f / (1.0f + expf(-g[q]));
-            v[0][e2] = d * u[q] * sg * (1.0f + g[q] * (1.0f - sg));
-            v[1][e2] = d * g[q] * sg;
-            v[2][e2] = wr * h[q];
-          }
-#pragma unroll
-          for (int f = 0; f < 3; ++f) {
-            const uint32_t hi = pack_bf16x2(v[f][0], v[f][1]);
-            o[2 * f][i / 2] = hi;
-            o[2 * f + 1][i / 2] = pack_bf16x2(v[f][0] - bf16_lo(hi), v[f][1] - bf16_hi(hi));
-          }
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int q = i + e2;
+          const float d = wr * dh[q];
+          part += d * h[q];
+          v[0][e2] = d * a[q];
+          v[1][e2] = d * b[q];
+          v[2][e2] = wr * h[q];
         }
-      } else {
 #pragma unroll
-        for (int f = 0; f < 6; ++f)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) o[f][i] = 0u;
+        for (int f = 0; f < 3; ++f) {
+          const uint32_t hi = pack_bf16x2(v[f][0], v[f][1]);
+          o[2 * f][i / 2] = hi;
+          o[2 * f + 1][i / 2] = pack_bf16x2(v[f][0] - bf16_lo(hi), v[f][1] - bf16_hi(hi));
+        }
       }
+      const int n = n0 + c;
       if (mode == Rows::Full) {
-        if (lane == 0) bulk_wait_group_read<0>();  // previous boxes have been read
+        if (lane == 0) bulk_wait_group_read<1>();  // the set about to be reused has been read
         __syncwarp();
+        const uint32_t base = st.base + set * kDhSetBytes;
+        const uint32_t sw = (lane >> 2) & 1;  // 32-byte swizzle: chunk ^= (row >> 2) & 1
 #pragma unroll
         for (int f = 0; f < 6; ++f) {
-          // box f at st.base + f*1 KB: row = lane (32 bytes), 32-byte swizzle (chunk ^= (row >> 2) & 1)
-          const uint32_t row_addr = st.base + f * 1024 + lane * 32;
-          const uint32_t sw = (lane >> 2) & 1;
+          const uint32_t row_addr = base + f * kDhBoxBytes + lane * 32;
           st_shared_v4(row_addr + ((0 ^ sw) << 4), make_uint4(o[f][0], o[f][1], o[f][2], o[f][3]));
           st_shared_v4(row_addr + ((1 ^ sw) << 4), make_uint4(o[f][4], o[f][5], o[f][6], o[f][7]));
         }
@@ -347,14 +363,15 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
         __syncwarp();
         if (lane == 0) {
           const int yl = y + static_cast<int>(p.R);
-          tma_store_2d(tmC0, st.base + 0 * 1024, n, y);
-          tma_store_2d(tmC0, st.base + 1 * 1024, n, yl);
-          tma_store_2d(tmC0, st.base + 2 * 1024, p.I + n, y);
-          tma_store_2d(tmC0, st.base + 3 * 1024, p.I + n, yl);
-          tma_store_2d(tmC1, st.base + 4 * 1024, n, y);
-          tma_store_2d(tmC1, st.base + 5 * 1024, n, yl);
+          tma_store_2d(tmC0, base + 0 * kDhBoxBytes, n, y);
+          tma_store_2d(tmC0, base + 1 * kDhBoxBytes, n, yl);
+          tma_store_2d(tmC0, base + 2 * kDhBoxBytes, p.I + n, y);
+          tma_store_2d(tmC0, base + 3 * kDhBoxBytes, p.I + n, yl);
+          tma_store_2d(tmC1, base + 4 * kDhBoxBytes, n, y);
+          tma_store_2d(tmC1, base + 5 * kDhBoxBytes, n, yl);
           bulk_commit_group();
         }
+        set ^= 1;
       } else if (row_ok) {
         uint16_t* dst[6] = {p.out2 + r * two_i + n, p.out2 + (p.R + r) * two_i + n, p.out2 + r * two_i + p.I + n,
                             p.out2 + (p.R + r) * two_i + p.I + n, p.hw_out + r * p.I + n,
@@ -365,6 +382,15 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
           reinterpret_cast<uint4*>(dst[f])[1] = make_uint4(o[f][4], o[f][5], o[f][6], o[f][7]);
         }
       }
+    };
+    float a0[16], b0[16], h0[16], a1[16], b1[16], h1[16];
+    load_ops(n0, a0, b0, h0);
+#pragma unroll 1
+    for (int c = 0; c < ncols; c += 32) {
+      load_ops(n0 + c + 16, a1, b1, h1);
+      process(c, a0, b0, h0);
+      if (c + 32 < ncols) load_ops(n0 + c + 32, a0, b0, h0);
+      process(c + 16, a1, b1, h1);
     }
     if (row_ok) p.gdot[r * p.n_tiles + tl.nt] = part;
   } else {  // ScaleRows, Store
@@ -443,11 +469,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
                         const Params p) {
+  using L = LayoutOf<EP>;
+  constexpr int STAGES = L::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (sbase - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + BAR_OFFSET);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + L::kBarOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -614,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int sub = warp & 3;  // TMEM lane quadrant this warp may access
     const int row_local = sub * 32 + lane;
-    Stager st{sbase + STG_OFFSET + static_cast<uint32_t>((warp - 2) * STG_PER_WARP * STG_BYTES), 0};
+    Stager st{sbase + L::kStgOffset + static_cast<uint32_t>((warp - 2) * L::kStgWarpBytes), 0};
     int acc = 0;
     uint32_t acc_phase = 0;
     prefetch_epilogue_operands<S, EP>(blockIdx.x, total, row_local, p);
@@ -772,7 +800,7 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LayoutOf<EP>::kSmemBytes);
   });
   if (attr_err != cudaSuccess) {
     set_cuda_error(attr_err, name);
@@ -781,7 +809,7 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
   if (grid < 1) return LIGER_MOE_OK;
   {
     KernelScope trace(name, s);
-    kern<<<grid, kThreads, SMEM_BYTES, s>>>(ta, tb, tc0, tc1, p);
+    kern<<<grid, kThreads, LayoutOf<EP>::kSmemBytes, s>>>(ta, tb, tc0, tc1, p);
   }
   return check_launch(name);
 }

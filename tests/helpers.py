@@ -106,3 +106,15 @@ def dense_swiglu_mlp_fp64(x_bits, wgu_e_bits, wd_e_bits):
     gate = x @ wgu[:I].T
     up = x @ wgu[I:].T
     return (torch.nn.functional.silu(gate) * up) @ wd.T
+
+
+def swiglu_factors(gu_f32: np.ndarray) -> np.ndarray:
+    """SwiGLU derivative factors [dh/dg | dh/du] of h = silu(g) u from [g | u] (float32 out).
+
+    dh/dg = u s (1 + g (1 - s)), dh/du = silu(g) = g s, with s = 1 / (1 + exp(-g)).
+    """
+    gu = np.asarray(gu_f32, dtype=np.float64)
+    I = gu.shape[1] // 2
+    g, u = gu[:, :I], gu[:, I:]
+    s = 1.0 / (1.0 + np.exp(-g))
+    return np.concatenate([u * s * (1.0 + g * (1.0 - s)), g * s], axis=1).astype(np.float32)

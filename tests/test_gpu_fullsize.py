@@ -24,7 +24,7 @@ import mixture_experts_routed_router_gb300 as moe
 import oracle
 import synthetic
 from tests.gpu_util import to_dev, to_host
-from tests.helpers import MAX_REL_TOL, MEAN_REL_TOL, assert_close, bf16_to_f64, rel_errors
+from tests.helpers import MAX_REL_TOL, MEAN_REL_TOL, assert_close, bf16_to_f64, rel_errors, swiglu_factors
 
 pytestmark = pytest.mark.gpu
 
@@ -160,7 +160,7 @@ def test_full_size_backward_isolated(name):
     rh, rgu, _ = oracle.grouped_swiglu_rows(xp, ref["m_indptr"], inp["wgu"], inp["wd"], w_perm_ref, rows)
     ridx = torch.from_numpy(rows).long().cuda()
     h[ridx] = to_dev(rh)
-    gu[ridx] = torch.from_numpy(rgu).cuda()
+    gu[ridx] = torch.from_numpy(swiglu_factors(rgu)).cuda()
     w_perm = to_dev(w_perm_ref)
     dx, dwgu, dwd, dl = moe.bwd_dx_dw(dy, d["x_perm"], h, gu, ids, to_dev(rw), d["m_indptr"], d["row_to_slot"],
                                       d["slot_to_row"], w_perm, wgu, wd)
