@@ -41,7 +41,7 @@ namespace {
 constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+
 constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64 (MN) x 64 (K) box of an MN-major operand
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
@@ -54,23 +54,30 @@ constexpr int kBarrierBytes = 256;
 constexpr int kDhBoxBytes = 32 * 32;            // dH epilogue: 32 rows x 16 bf16 columns
 constexpr int kDhSetBytes = 6 * kDhBoxBytes;    // six output boxes per 16 columns
 
-// Shared memory of one CTA: operand stages | epilogue staging | barriers.  The dH kernel
-// keeps 3 operand stages (its MMAs are a small part of its time) to double-buffer its six
-// narrow staging boxes; the others keep 4 stages and two 4 KB staging boxes per warp.
-template <int kDh>
+// Shared memory of one CTA: operand stages | epilogue staging | barriers.
+//   SPLIT = 0: one A and one B tile per stage (48 KB), 4 stages;
+//   SPLIT = 1: A as two bf16 parts (hi, lo) + B (64 KB), 3 stages: two MMAs per K step share B;
+//   SPLIT = 2: A + B as two parts (80 KB), 2 stages: two MMAs per K step share A.
+// The dH kernel keeps 3 operand stages (its MMAs are a small part of its time) to
+// double-buffer its six narrow staging boxes; the others have two 4 KB boxes per warp.
+template <int kDh, int SPLIT>
 struct Layout {
-  static constexpr int kStages = kDh ? 3 : 4;
+  static constexpr int kABytes = A_BYTES * (SPLIT == 1 ? 2 : 1);
+  static constexpr int kBBytes = B_BYTES * (SPLIT == 2 ? 2 : 1);
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = kDh ? 3 : (SPLIT == 0 ? 4 : (SPLIT == 1 ? 3 : 2));
   static constexpr int kStgWarpBytes = kDh ? 2 * kDhSetBytes : STG_PER_WARP * STG_BYTES;
-  static constexpr int kStgOffset = kStages * STAGE_BYTES;
+  static constexpr int kStgOffset = kStages * kStageBytes;
   static constexpr int kBarOffset = kStgOffset + kEpiWarps * kStgWarpBytes;
   static constexpr int kSmemBytes = kBarOffset + kBarrierBytes + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
 };
 
 enum class Sched : int { RowsM = 0, RowsK = 1 };
 enum class Epi : int { SwiGLU = 0, ScaleRows = 1, DH = 2, Store = 3 };
-template <Epi EP>
-using LayoutOf = Layout<EP == Epi::DH ? 1 : 0>;
+template <Epi EP, int SPLIT>
+using LayoutOf = Layout<EP == Epi::DH ? 1 : 0, SPLIT>;
 
 struct Params {
   const int32_t* m_indptr;     // [E+1]
@@ -82,11 +89,8 @@ struct Params {
   int b_rows_per_expert;  // rows of B's tensor map per expert
   int b_split;            // SwiGLU: row offset of the up half of W_gu (= I)
   int M_out;              // RowsK: output rows per expert
-  int k_halves;           // RowsK: 2 = the K loop runs twice over the expert's rows; the second
-                          //        pass reads A rows + a_split_rows and B rows + b_split_rows
-                          //        (an operand stored as bf16 hi and lo parts)
-  int a_split_rows;       // RowsK: row offset of A's second part
-  int b_split_rows;       // RowsK: row offset of B's second part
+  int a_split_rows;       // RowsK, SPLIT = 1: row offset of A's lo part (A stored as bf16 hi, lo)
+  int b_split_rows;       // RowsK, SPLIT = 2: row offset of B's lo part
   int N_out;              // valid output columns
   int I;
   uint16_t* out;
@@ -110,7 +114,6 @@ struct Tile {
   int nt;        // N tile
   int row0;      // RowsK: first global row of the expert
   int kb_count;  // K blocks
-  int kb_half;   // RowsK: K blocks per pass over the expert's rows
 };
 
 template <Sched S>
@@ -133,7 +136,6 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p) {
     tl.rows = min(BM, end - tl.m0);
     tl.row0 = 0;
     tl.kb_count = p.num_kb;
-    tl.kb_half = p.num_kb;
   } else {
     const int per_e = p.m_tiles * p.n_tiles;
     tl.e = t / per_e;
@@ -143,8 +145,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p) {
     tl.m0 = mt * BM;
     tl.row0 = __ldg(p.m_indptr + tl.e);
     tl.rows = __ldg(p.m_indptr + tl.e + 1) - tl.row0;
-    tl.kb_half = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
-    tl.kb_count = tl.kb_half * p.k_halves;
+    tl.kb_count = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
   }
   return tl;
 }
@@ -452,25 +453,28 @@ __device__ __forceinline__ void prefetch_epilogue_operands(int t, int total, int
 }
 
 // Zeroes K rows [valid, BK) of every 64-wide MN box of an MN-major stage
-// (A: 2 boxes, B: 4 boxes, each 64 rows of 128 B).  Whole 128-byte rows are
-// cleared, so the swizzle inside a row does not matter.
+// (A: 2 boxes per part, B: 4 boxes per part, each 64 rows of 128 B).  Whole
+// 128-byte rows are cleared, so the swizzle inside a row does not matter.
+template <int kBoxes>
 __device__ __forceinline__ void zero_tail_rows(uint8_t* stage_ptr, int valid, int lane) {
   const int nz = BK - valid;
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
   const int per_box = nz * 8;  // uint4 per box
-  for (int box = 0; box < 6; ++box) {
+  for (int box = 0; box < kBoxes; ++box) {
     uint4* dst = reinterpret_cast<uint4*>(stage_ptr + box * MN_BOX_BYTES + valid * 128);
     for (int i = lane; i < per_box; i += 32) dst[i] = z;
   }
 }
 
-template <Sched S, Epi EP, bool A_MN, bool B_MN>
+template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
                         const Params p) {
-  using L = LayoutOf<EP>;
+  using L = LayoutOf<EP, SPLIT>;
   constexpr int STAGES = L::kStages;
+  constexpr int STAGE_BYTES = L::kStageBytes;
+  static_assert(SPLIT == 0 || (S == Sched::RowsK && A_MN && B_MN), "hi/lo operands only in the dW GEMMs");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -536,17 +540,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t sa = sbase + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t sb = sa + L::kABytes;
           const uint32_t fb = full0 + 8 * stage;
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          const int kr = kb % tl.kb_half;  // K block within the pass over the expert's rows
           if constexpr (!A_MN) {
             tma_load_2d(sa, &tmA, fb, kb * BK, tl.m0);
           } else {
 #pragma unroll
-            for (int i = 0; i < BM / 64; ++i)
-              tma_load_2d(sa + i * MN_BOX_BYTES, &tmA, fb, tl.m0 + 64 * i,
-                          tl.row0 + kr * BK + (kb >= tl.kb_half ? p.a_split_rows : 0));
+            for (int part = 0; part < (SPLIT == 1 ? 2 : 1); ++part)
+#pragma unroll
+              for (int i = 0; i < BM / 64; ++i)
+                tma_load_2d(sa + part * A_BYTES + i * MN_BOX_BYTES, &tmA, fb, tl.m0 + 64 * i,
+                            tl.row0 + kb * BK + part * p.a_split_rows);
           }
           if constexpr (!B_MN) {
             if constexpr (EP == Epi::SwiGLU) {
@@ -557,10 +562,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d(sb, &tmB, fb, kb * BK, tl.e * p.b_rows_per_expert + tl.nt * BN);
             }
           } else {
-            const int krow = (S == Sched::RowsM) ? tl.e * p.b_rows_per_expert + kb * BK
-                                                 : tl.row0 + kr * BK + (kb >= tl.kb_half ? p.b_split_rows : 0);
+            const int krow = (S == Sched::RowsM) ? tl.e * p.b_rows_per_expert + kb * BK : tl.row0 + kb * BK;
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * MN_BOX_BYTES, &tmB, fb, tl.nt * BN + 64 * i, krow);
+            for (int part = 0; part < (SPLIT == 2 ? 2 : 1); ++part)
+#pragma unroll
+              for (int i = 0; i < BN / 64; ++i)
+                tma_load_2d(sb + part * B_BYTES + i * MN_BOX_BYTES, &tmB, fb, tl.nt * BN + 64 * i,
+                            krow + part * p.b_split_rows);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -599,11 +607,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t sa = sbase + stage * STAGE_BYTES;
-        const uint32_t sb = sa + A_BYTES;
+        const uint32_t sb = sa + L::kABytes;
         if constexpr (S == Sched::RowsK) {
-          const int valid = tl.rows - (kb % tl.kb_half) * BK;
+          const int valid = tl.rows - kb * BK;
           if (valid < BK) {
-            zero_tail_rows(base_ptr + stage * STAGE_BYTES, valid, lane);
+            zero_tail_rows<STAGE_BYTES / MN_BOX_BYTES>(base_ptr + stage * STAGE_BYTES, valid, lane);
             fence_proxy_async_smem();
           }
           __syncwarp();
@@ -616,6 +624,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = B_MN ? smem_desc_sw128(sb + kk * 2048, MN_BOX_BYTES, 1024)
                                      : smem_desc_sw128(sb + kk * 32, 16, 1024);
             umma_bf16_f32(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            if constexpr (SPLIT == 1)  // lo part of A against the same B
+              umma_bf16_f32(d_tmem, smem_desc_sw128(sa + A_BYTES + kk * 2048, MN_BOX_BYTES, 1024), bd, idesc, 1u);
+            if constexpr (SPLIT == 2)  // the same A against the lo part of B
+              umma_bf16_f32(d_tmem, ad, smem_desc_sw128(sb + B_BYTES + kk * 2048, MN_BOX_BYTES, 1024), idesc, 1u);
           }
           umma_commit(empty0 + 8 * stage);
         }
@@ -793,14 +805,14 @@ int make_out_bf16_3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t ro
   return make_tmap_nd(m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3, dims, box);
 }
 
-template <Sched S, Epi EP, bool A_MN, bool B_MN>
+template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT = 0>
 int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc0, const CUtensorMap& tc1,
                 const Params& p, int grid, cudaStream_t s, const char* name) {
-  auto kern = grouped_gemm_kernel<S, EP, A_MN, B_MN>;
+  auto kern = grouped_gemm_kernel<S, EP, A_MN, B_MN, SPLIT>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LayoutOf<EP>::kSmemBytes);
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LayoutOf<EP, SPLIT>::kSmemBytes);
   });
   if (attr_err != cudaSuccess) {
     set_cuda_error(attr_err, name);
@@ -809,7 +821,7 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
   if (grid < 1) return LIGER_MOE_OK;
   {
     KernelScope trace(name, s);
-    kern<<<grid, kThreads, LayoutOf<EP>::kSmemBytes, s>>>(ta, tb, tc0, tc1, p);
+    kern<<<grid, kThreads, LayoutOf<EP, SPLIT>::kSmemBytes, s>>>(ta, tb, tc0, tc1, p);
   }
   return check_launch(name);
 }
@@ -949,14 +961,13 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   CUtensorMap ta, tb;
   const uint64_t rows = a.R > 0 ? static_cast<uint64_t>(a.R) : 1;
   Params p = base_params(a.m_indptr, nullptr, a.E, dev.err_flag);
-  // dW_gu[e] = dgu_hi_e^T x_e + dgu_lo_e^T x_e: the K loop walks the expert's rows twice,
-  // the second time with A in the lo half of dgu ([2R, 2I]).
+  // dW_gu[e] = dgu_hi_e^T x_e + dgu_lo_e^T x_e: each stage holds both parts of A (rows r and
+  // R + r of dgu [2R, 2I]) and one B tile; two MMAs per K step.
   if (make_tmap(&ta, a.R > 0 ? a.dgu : a.dw_gate_up, 2ULL * a.I, 2 * rows, 64, BK) ||
       make_tmap(&tb, a.R > 0 ? a.x_perm : a.dw_gate_up, a.H, rows, 64, BK))
     return LIGER_MOE_ERR_LAUNCH;
   p.m_tiles = cdiv(2LL * a.I, BM);
   p.n_tiles = cdiv(a.H, BN);
-  p.k_halves = 2;
   p.a_split_rows = static_cast<int>(a.R);
   p.b_split_rows = 0;
   p.M_out = 2 * a.I;
@@ -966,17 +977,17 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.out_expert_stride = 2LL * a.I * a.H;
   CUtensorMap tc0;
   if (make_out_bf16_3d(&tc0, a.dw_gate_up, a.H, 2ULL * a.I, a.E)) return LIGER_MOE_ERR_LAUNCH;
-  int rc = launch_gemm<Sched::RowsK, Epi::Store, true, true>(
+  int rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1>(
       ta, tb, tc0, tc0, p, rows_k_grid(static_cast<long long>(a.E) * p.m_tiles * p.n_tiles, dev), s,
       "gemm_bwd_dw_gate_up");
   if (rc) return rc;
-  // dW_d[e] = dY_e^T hw_hi_e + dY_e^T hw_lo_e: the second pass reads B in the lo half of hw ([2R, I]).
+  // dW_d[e] = dY_e^T hw_hi_e + dY_e^T hw_lo_e: each stage holds one A tile and both parts of B
+  // (rows r and R + r of hw [2R, I]); two MMAs per K step.
   if (make_tmap(&ta, a.R > 0 ? a.dy_perm : a.dw_down, a.H, rows, 64, BK) ||
       make_tmap(&tb, a.R > 0 ? a.hw_perm : a.dw_down, a.I, 2 * rows, 64, BK))
     return LIGER_MOE_ERR_LAUNCH;
   p.m_tiles = cdiv(a.H, BM);
   p.n_tiles = cdiv(a.I, BN);
-  p.k_halves = 2;
   p.a_split_rows = 0;
   p.b_split_rows = static_cast<int>(a.R);
   p.M_out = a.H;
@@ -985,7 +996,7 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.ld_out = a.I;
   p.out_expert_stride = 1LL * a.H * a.I;
   if (make_out_bf16_3d(&tc0, a.dw_down, a.I, a.H, a.E)) return LIGER_MOE_ERR_LAUNCH;
-  return launch_gemm<Sched::RowsK, Epi::Store, true, true>(
+  return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2>(
       ta, tb, tc0, tc0, p, rows_k_grid(static_cast<long long>(a.E) * p.m_tiles * p.n_tiles, dev), s,
       "gemm_bwd_dw_down");
 }
