@@ -43,13 +43,13 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 
 constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64 (MN) x 64 (K) box of an MN-major operand
-constexpr int kThreads = 192;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, each owning half of the tile's columns
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 2 * BN;
-// Epilogue staging: per epilogue warp two 32-row x 128-byte boxes (128-byte swizzle) that
-// feed TMA bulk stores, so output rows leave the SM as whole lines.
+// Epilogue staging: per epilogue warp one 32-row x 128-byte box (128-byte swizzle) that
+// feeds TMA bulk stores, so output rows leave the SM as whole lines.
 constexpr int STG_BYTES = 32 * 128;
-constexpr int STG_PER_WARP = 2;
+constexpr int STG_PER_WARP = 1;
 constexpr int kBarrierBytes = 256;
 constexpr int kDhBoxBytes = 32 * 32;            // dH epilogue: 32 rows x 16 bf16 columns
 constexpr int kDhSetBytes = 6 * kDhBoxBytes;    // six output boxes per 16 columns
@@ -58,15 +58,15 @@ constexpr int kDhSetBytes = 6 * kDhBoxBytes;    // six output boxes per 16 colum
 //   SPLIT = 0: one A and one B tile per stage (48 KB), 4 stages;
 //   SPLIT = 1: A as two bf16 parts (hi, lo) + B (64 KB), 3 stages: two MMAs per K step share B;
 //   SPLIT = 2: A + B as two parts (80 KB), 2 stages: two MMAs per K step share A.
-// The dH kernel keeps 3 operand stages (its MMAs are a small part of its time) to
-// double-buffer its six narrow staging boxes; the others have two 4 KB boxes per warp.
+// Epilogue staging per warp: one 4 KB box, or for the dH kernel one set of six 1 KB boxes
+// (3 operand stages there: its MMAs are a small part of its time).
 template <int kDh, int SPLIT>
 struct Layout {
   static constexpr int kABytes = A_BYTES * (SPLIT == 1 ? 2 : 1);
   static constexpr int kBBytes = B_BYTES * (SPLIT == 2 ? 2 : 1);
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = kDh ? 3 : (SPLIT == 0 ? 4 : (SPLIT == 1 ? 3 : 2));
-  static constexpr int kStgWarpBytes = kDh ? 2 * kDhSetBytes : STG_PER_WARP * STG_BYTES;
+  static constexpr int kStgWarpBytes = kDh ? kDhSetBytes : STG_PER_WARP * STG_BYTES;
   static constexpr int kStgOffset = kStages * kStageBytes;
   static constexpr int kBarOffset = kStgOffset + kEpiWarps * kStgWarpBytes;
   static constexpr int kSmemBytes = kBarOffset + kBarrierBytes + 1024;
@@ -102,7 +102,7 @@ struct Params {
   const float* gu_in;     // DH: derivative factors [a | b] fp32 [R, 2I]
   const uint16_t* h_in;   // DH: h [R, I]
   uint16_t* hw_out;       // DH: bf16(w * h) [R, I]
-  float* gdot;            // DH: [R, n_tiles] partial <dh, h>
+  float* gdot;            // DH: [R, 2 n_tiles] partial <dh, h> (per N tile and column half)
   long long R;            // DH: rows (offset of the lo half of hw_out)
   int* err;
 };
@@ -251,21 +251,24 @@ __device__ __forceinline__ Rows slice_mode(const Tile& tl, int sub) {
   return n >= 32 ? Rows::Full : (n > 0 ? Rows::Partial : Rows::None);
 }
 
-// Epilogue of one tile for one warp (each lane = one accumulator row).
+// Epilogue of one tile for one warp: each lane is one accumulator row; the warp covers the
+// rows of TMEM quadrant `sub` and the tile's output columns of half `colhalf`.
 template <Sched S, Epi EP>
-__device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, int sub, int lane, const Params& p,
-                                              const CUtensorMap* tmC0, const CUtensorMap* tmC1, Stager& st) {
+__device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, int sub, int colhalf, int lane,
+                                              const Params& p, const CUtensorMap* tmC0, const CUtensorMap* tmC1,
+                                              Stager& st) {
   const int row_local = sub * 32 + lane;
   const Rows mode = slice_mode<S>(tl, sub);
-  if (mode == Rows::None) return;
   const bool row_ok = (S == Sched::RowsK) ? true : row_local < tl.rows;
   if constexpr (EP == Epi::SwiGLU) {
-    // accumulator columns [0, BN/2) = g, [BN/2, BN) = u for output columns nt*BN/2 + c
+    if (mode == Rows::None) return;
+    // accumulator columns [0, BN/2) = g, [BN/2, BN) = u for output columns nt*BN/2 + c;
+    // this warp's output columns: [64 colhalf, 64 colhalf + 64)
     const long long r = tl.m0 + row_local;
     const int y = tl.m0 + sub * 32;
     const int j0 = tl.nt * (BN / 2);
 #pragma unroll 1
-    for (int q = 0; q < 2; ++q) {
+    for (int q = colhalf; q < colhalf + 1; ++q) {
       const int col = j0 + q * 64;
       if (col >= p.I) break;
       uint32_t hw[32];
@@ -307,16 +310,18 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
     // the hi rows) and hw = w_r h ([2R, I]).  Outputs leave through 32-row x 16-column boxes
     // (32-byte swizzle), six per 16 columns, double-buffered; the loads of the next 16
     // columns are issued before the current ones are processed.
+    // This warp's columns: [n0 + c_lo, n0 + c_hi), half of the tile's N columns.
     const long long r = tl.m0 + row_local;
     const long long two_i = 2LL * p.I;
     const int y = tl.m0 + sub * 32;
     const int n0 = tl.nt * BN;
     const int ncols = min(BN, p.I - n0);  // a positive multiple of 64
+    const int c_lo = colhalf * (BN / 2);
+    const int c_hi = min(c_lo + BN / 2, ncols);
     const float wr = row_ok ? __ldg(p.row_scale + r) : 0.f;
     const float* arow = p.gu_in + r * two_i;
     const uint16_t* hrow = p.h_in + r * p.I;
     float part = 0.f;
-    int set = 0;
     auto load_ops = [&](int n, float (&a)[16], float (&b)[16], float (&h)[16]) {
       if (row_ok) {
         load16_f32(arow + n, a);
@@ -350,9 +355,9 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
       }
       const int n = n0 + c;
       if (mode == Rows::Full) {
-        if (lane == 0) bulk_wait_group_read<1>();  // the set about to be reused has been read
+        if (lane == 0) bulk_wait_group_read<0>();  // the boxes' previous stores have read them
         __syncwarp();
-        const uint32_t base = st.base + set * kDhSetBytes;
+        const uint32_t base = st.base;
         const uint32_t sw = (lane >> 2) & 1;  // 32-byte swizzle: chunk ^= (row >> 2) & 1
 #pragma unroll
         for (int f = 0; f < 6; ++f) {
@@ -372,7 +377,6 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
           tma_store_2d(tmC1, base + 5 * kDhBoxBytes, n, yl);
           bulk_commit_group();
         }
-        set ^= 1;
       } else if (row_ok) {
         uint16_t* dst[6] = {p.out2 + r * two_i + n, p.out2 + (p.R + r) * two_i + n, p.out2 + r * two_i + p.I + n,
                             p.out2 + (p.R + r) * two_i + p.I + n, p.hw_out + r * p.I + n,
@@ -384,21 +388,24 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
         }
       }
     };
-    float a0[16], b0[16], h0[16], a1[16], b1[16], h1[16];
-    load_ops(n0, a0, b0, h0);
+    if (mode != Rows::None) {
+      float a0[16], b0[16], h0[16], a1[16], b1[16], h1[16];
+      if (c_lo < c_hi) load_ops(n0 + c_lo, a0, b0, h0);
 #pragma unroll 1
-    for (int c = 0; c < ncols; c += 32) {
-      load_ops(n0 + c + 16, a1, b1, h1);
-      process(c, a0, b0, h0);
-      if (c + 32 < ncols) load_ops(n0 + c + 32, a0, b0, h0);
-      process(c + 16, a1, b1, h1);
+      for (int c = c_lo; c < c_hi; c += 32) {
+        load_ops(n0 + c + 16, a1, b1, h1);
+        process(c, a0, b0, h0);
+        if (c + 32 < c_hi) load_ops(n0 + c + 32, a0, b0, h0);
+        process(c + 16, a1, b1, h1);
+      }
     }
-    if (row_ok) p.gdot[r * p.n_tiles + tl.nt] = part;
-  } else {  // ScaleRows, Store
+    if (row_ok) p.gdot[r * (2LL * p.n_tiles) + 2 * tl.nt + colhalf] = part;
+  } else {  // ScaleRows, Store: this warp's columns [128 colhalf, 128 colhalf + 128)
+    if (mode == Rows::None) return;
     float sc = 1.f;
     if constexpr (EP == Epi::ScaleRows) sc = row_ok ? __ldg(p.row_scale + tl.m0 + row_local) : 0.f;
 #pragma unroll 1
-    for (int q = 0; q < BN / 64; ++q) {
+    for (int q = 2 * colhalf; q < 2 * colhalf + 2; ++q) {
       const int col = tl.nt * BN + q * 64;
       if (col >= p.N_out) break;
       float a[32], b[32];
@@ -422,12 +429,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
 }
 
 // RowsK tile of an expert with no rows: the gradient block is exactly zero.
-__device__ __forceinline__ void store_zero_tile(const Tile& tl, int sub, int lane, const Params& p,
+__device__ __forceinline__ void store_zero_tile(const Tile& tl, int sub, int colhalf, int lane, const Params& p,
                                                 const CUtensorMap* tmC0, Stager& st) {
   uint32_t w[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) w[i] = 0u;
-  for (int q = 0; q < BN / 64; ++q) {
+  for (int q = 2 * colhalf; q < 2 * colhalf + 2; ++q) {
     const int col = tl.nt * BN + q * 64;
     if (col >= p.N_out) break;
     emit_box<3>(tmC0, st, lane, w, col, tl.m0 + sub * 32, tl.e);
@@ -437,14 +444,15 @@ __device__ __forceinline__ void store_zero_tile(const Tile& tl, int sub, int lan
 // DH epilogue operands of one tile row (fp32 g and u, bf16 h) are pulled into L2 ahead of
 // time, one tile early, so the epilogue's loads do not wait on DRAM.
 template <Sched S, Epi EP>
-__device__ __forceinline__ void prefetch_epilogue_operands(int t, int total, int row_local, const Params& p) {
+__device__ __forceinline__ void prefetch_epilogue_operands(int t, int total, int row_local, int colhalf,
+                                                           const Params& p) {
   if constexpr (EP == Epi::DH) {
     if (t >= total) return;
     const Tile tl = decode_tile<S>(t, p);
     if (row_local >= tl.rows) return;
     const long long r = tl.m0 + row_local;
-    const int n0 = tl.nt * BN;
-    const int ncols = min(BN, p.I - n0);
+    const int n0 = tl.nt * BN + colhalf * (BN / 2);
+    const int ncols = min(BN / 2, p.I - n0);
     if (ncols <= 0) return;
     prefetch_l2_bulk(p.gu_in + r * 2LL * p.I + n0, ncols * 4);
     prefetch_l2_bulk(p.gu_in + r * 2LL * p.I + p.I + n0, ncols * 4);
@@ -498,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 4);
+      mbar_init(tempty0 + 8 * a, kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -652,17 +660,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int sub = warp & 3;  // TMEM lane quadrant this warp may access
+    const int ew = warp - 2;
+    const int sub = warp & 3;      // TMEM lane quadrant this warp may access
+    const int colhalf = ew >> 2;   // which half of the tile's columns
     const int row_local = sub * 32 + lane;
-    Stager st{sbase + L::kStgOffset + static_cast<uint32_t>((warp - 2) * L::kStgWarpBytes), 0};
+    Stager st{sbase + L::kStgOffset + static_cast<uint32_t>(ew * L::kStgWarpBytes), 0};
     int acc = 0;
     uint32_t acc_phase = 0;
-    prefetch_epilogue_operands<S, EP>(blockIdx.x, total, row_local, p);
+    prefetch_epilogue_operands<S, EP>(blockIdx.x, total, row_local, colhalf, p);
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode_tile<S>(t, p);
-      prefetch_epilogue_operands<S, EP>(t + gridDim.x, total, row_local, p);
+      prefetch_epilogue_operands<S, EP>(t + gridDim.x, total, row_local, colhalf, p);
       if (tl.kb_count == 0) {
-        if constexpr (S == Sched::RowsK) store_zero_tile(tl, sub, lane, p, &tmC0, st);
+        if constexpr (S == Sched::RowsK) store_zero_tile(tl, sub, colhalf, lane, p, &tmC0, st);
         continue;
       }
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag))) {
@@ -671,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epilogue_tile<S, EP>(t_row, tl, sub, lane, p, &tmC0, &tmC1, st);
+      epilogue_tile<S, EP>(t_row, tl, sub, colhalf, lane, p, &tmC0, &tmC1, st);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
@@ -859,7 +869,7 @@ int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, int32_t* t
   return check_launch("tile_schedule");
 }
 
-int gdot_tiles(int I) { return cdiv(I, BN); }
+int gdot_tiles(int I) { return 2 * cdiv(I, BN); }
 
 int launch_gate_up(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   if (a.R == 0) return LIGER_MOE_OK;
