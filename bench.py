@@ -178,19 +178,21 @@ def size_oracle_sample(wl, inp, ids, w, seconds: float):
     """Tokens / experts for a sample of about `seconds` of oracle work (one calibration call)."""
     import numpy as np
 
+    import oracle
+
+    n_cal = min(wl.T, 2 * oracle.default_threads())  # enough tokens to engage every thread
     t0 = time.perf_counter()
-    oracle_sample(wl, inp, ids, w, 2, [])
-    per_tok = max((time.perf_counter() - t0) / 2.0, 1e-6)
+    oracle_sample(wl, inp, ids, w, n_cal, [])
+    per_tok = max((time.perf_counter() - t0) / n_cal, 1e-6)
     n_tok = int(max(1, min(wl.T, seconds * 0.7 / per_tok)))
+    # dW runs one expert per thread: up to `threads` mid-size experts whose largest row count
+    # keeps one thread's share near 30 % of the budget (a row costs about 1.5 token-rows of work)
+    threads = oracle.default_threads()
+    per_row_single = per_tok * threads / wl.k * 1.5
     counts = np.bincount(ids.ravel(), minlength=wl.E)
-    order = np.argsort(counts, kind="stable")
-    budget_rows = max(1.0, seconds * 0.3 / per_tok * wl.k / 2.0)
-    experts, rows = [], 0
-    for e in order[::-1][len(order) // 2:]:  # mid-size experts first
-        if rows + counts[e] > budget_rows and experts:
-            break
-        experts.append(int(e))
-        rows += int(counts[e])
+    order = [int(e) for e in np.argsort(counts, kind="stable") if counts[e] > 0]
+    mid = order[len(order) // 2:] + order[: len(order) // 2][::-1]
+    experts = [e for e in mid if counts[e] * per_row_single <= 0.3 * seconds][:threads]
     return n_tok, experts
 
 
@@ -451,12 +453,22 @@ def run_ours(args, rank, world, local_rank):
 
 
 def load_traffic(workload: str, kernel: str):
-    """DRAM bytes per launch of `kernel` from a committed ncu summary, if one matches."""
+    """DRAM bytes per launch of `kernel` from a committed ncu capture, if one matches.
+
+    None when there is no capture for this workload and kernel, or when the GEMM source
+    has changed since the counters were taken (the capture records its hash).
+    """
+    import hashlib
+
     path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "mixture_experts_routed_router_gb300", "csrc", "grouped_gemm.cu")
     try:
         with open(path) as f:
-            t = json.load(f)
-        return t[workload][kernel]["dram_bytes_per_launch"]
+            entry = json.load(f)[workload][kernel]
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != entry.get("kernel_source_sha256"):
+                return None
+        return entry["dram_bytes_per_launch"]
     except (OSError, KeyError, ValueError, TypeError):
         return None
 
