@@ -215,7 +215,9 @@ int liger_moe_device_error(void* stream, int* flags);
  *   liger_moe_trace_count()      number of launches logged
  *   liger_moe_trace_get(i, ...)  kernel name (static string) and duration in ms
  *                                of launch i; waits for that launch to finish
- * Host-side cost: two cudaEventRecord calls per launch while enabled.
+ * Host-side cost: two event records per launch while enabled.  The records
+ * are "external", so a trace taken while the stream is captured into a CUDA
+ * graph times every replay of the captured launches (the last replay wins).
  */
 int liger_moe_trace_enable(int on);
 int liger_moe_trace_count(void);

@@ -83,7 +83,8 @@ KernelScope::KernelScope(const char* name, cudaStream_t s) : name_(name), stream
   if (!g_trace_on.load(std::memory_order_relaxed)) return;
   std::lock_guard<std::mutex> lock(g_trace_mu);
   start_ = trace_event();
-  if (start_ != nullptr) cudaEventRecord(start_, stream_);
+  // "external" records stay real event records when the stream is being captured into a graph
+  if (start_ != nullptr) cudaEventRecordWithFlags(start_, stream_, cudaEventRecordExternal);
 }
 
 KernelScope::~KernelScope() {
@@ -94,7 +95,7 @@ KernelScope::~KernelScope() {
     g_event_pool.push_back(start_);
     return;
   }
-  cudaEventRecord(stop, stream_);
+  cudaEventRecordWithFlags(stop, stream_, cudaEventRecordExternal);
   g_trace.push_back(TraceRecord{name_, start_, stop});
 }
 

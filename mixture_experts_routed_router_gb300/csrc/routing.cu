@@ -244,19 +244,24 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
     }
     const uint4* a = reinterpret_cast<const uint4*>(src + static_cast<size_t>(s / k) * H);
     uint4* b = reinterpret_cast<uint4*>(dst + static_cast<size_t>(r) * H);
-    if (scale == nullptr) {
-#pragma unroll 4
-      for (int c = lane; c < chunks; c += 32) b[c] = __ldg(a + c);
-    } else {
-      const float f = __ldg(scale + r);
-#pragma unroll 4
-      for (int c = lane; c < chunks; c += 32) {
-        uint4 v = __ldg(a + c);
-        v.x = pack_bf16x2(f * bf16_lo(v.x), f * bf16_hi(v.x));
-        v.y = pack_bf16x2(f * bf16_lo(v.y), f * bf16_hi(v.y));
-        v.z = pack_bf16x2(f * bf16_lo(v.z), f * bf16_hi(v.z));
-        v.w = pack_bf16x2(f * bf16_lo(v.w), f * bf16_hi(v.w));
-        b[c] = v;
+    const float f = (scale == nullptr) ? 1.f : __ldg(scale + r);
+    // up to 8 chunks per lane in flight: all loads of a group are issued before its stores
+    for (int c0 = lane; c0 < chunks; c0 += 32 * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (c0 + 32 * j < chunks) v[j] = __ldg(a + c0 + 32 * j);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (c0 + 32 * j >= chunks) break;
+        uint4 o = v[j];
+        if (scale != nullptr) {
+          o.x = pack_bf16x2(f * bf16_lo(o.x), f * bf16_hi(o.x));
+          o.y = pack_bf16x2(f * bf16_lo(o.y), f * bf16_hi(o.y));
+          o.z = pack_bf16x2(f * bf16_lo(o.z), f * bf16_hi(o.z));
+          o.w = pack_bf16x2(f * bf16_lo(o.w), f * bf16_hi(o.w));
+        }
+        b[c0 + 32 * j] = o;
       }
     }
   }
