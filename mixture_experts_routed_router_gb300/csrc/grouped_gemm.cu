@@ -460,12 +460,12 @@ __device__ __forceinline__ void prefetch_epilogue_operands(int t, int total, int
   }
 }
 
-// Zeroes K rows [valid, BK) of every 64-wide MN box of an MN-major stage
+// Zeroes K rows [valid, end) of every 64-wide MN box of an MN-major stage
 // (A: 2 boxes per part, B: 4 boxes per part, each 64 rows of 128 B).  Whole
 // 128-byte rows are cleared, so the swizzle inside a row does not matter.
 template <int kBoxes>
-__device__ __forceinline__ void zero_tail_rows(uint8_t* stage_ptr, int valid, int lane) {
-  const int nz = BK - valid;
+__device__ __forceinline__ void zero_tail_rows(uint8_t* stage_ptr, int valid, int end, int lane) {
+  const int nz = end - valid;
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
   const int per_box = nz * 8;  // uint4 per box
   for (int box = 0; box < kBoxes; ++box) {
@@ -616,17 +616,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t sa = sbase + stage * STAGE_BYTES;
         const uint32_t sb = sa + L::kABytes;
+        // K steps of 16 rows to issue: all of them, except in a weight-gradient tile's last
+        // block, which ends at the 16-row step holding the expert's last row; the rows of that
+        // step past the expert are zeroed first (they belong to the next expert).
+        int ksteps = BK / 16;
         if constexpr (S == Sched::RowsK) {
           const int valid = tl.rows - kb * BK;
           if (valid < BK) {
-            zero_tail_rows<STAGE_BYTES / MN_BOX_BYTES>(base_ptr + stage * STAGE_BYTES, valid, lane);
-            fence_proxy_async_smem();
+            ksteps = (valid + 15) / 16;
+            if (valid < ksteps * 16) {
+              zero_tail_rows<STAGE_BYTES / MN_BOX_BYTES>(base_ptr + stage * STAGE_BYTES, valid, ksteps * 16, lane);
+              fence_proxy_async_smem();
+            }
           }
           __syncwarp();
         }
         if (lane == 0) {
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
+            if (kk >= ksteps) break;
             const uint64_t ad = A_MN ? smem_desc_sw128(sa + kk * 2048, MN_BOX_BYTES, 1024)
                                      : smem_desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc_sw128(sb + kk * 2048, MN_BOX_BYTES, 1024)
