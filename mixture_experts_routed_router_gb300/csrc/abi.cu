@@ -66,6 +66,16 @@ std::mutex g_trace_mu;
 std::vector<TraceRecord> g_trace;
 std::vector<cudaEvent_t> g_event_pool;
 
+// Records `e` on `s`; inside a stream capture the record becomes an external event node, so
+// the event still marks the time when the captured graph is replayed.
+void trace_record(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &st) == cudaSuccess && st == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
+}
+
 cudaEvent_t trace_event() {
   // caller holds g_trace_mu
   if (!g_event_pool.empty()) {
@@ -83,8 +93,7 @@ KernelScope::KernelScope(const char* name, cudaStream_t s) : name_(name), stream
   if (!g_trace_on.load(std::memory_order_relaxed)) return;
   std::lock_guard<std::mutex> lock(g_trace_mu);
   start_ = trace_event();
-  // "external" records stay real event records when the stream is being captured into a graph
-  if (start_ != nullptr) cudaEventRecordWithFlags(start_, stream_, cudaEventRecordExternal);
+  if (start_ != nullptr) trace_record(start_, stream_);
 }
 
 KernelScope::~KernelScope() {
@@ -95,7 +104,7 @@ KernelScope::~KernelScope() {
     g_event_pool.push_back(start_);
     return;
   }
-  cudaEventRecordWithFlags(stop, stream_, cudaEventRecordExternal);
+  trace_record(stop, stream_);
   g_trace.push_back(TraceRecord{name_, start_, stop});
 }
 
