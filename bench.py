@@ -53,6 +53,9 @@ def parse_args():
     ap.add_argument("--no-graph", action="store_true", help="launch the timed steps one by one instead of "
                     "replaying them as one captured CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work of the oracle baseline sample")
+    ap.add_argument("--inputs", choices=["x_perm", "gather"], default="x_perm",
+                    help="expert GEMM inputs: expert-major copies (x_perm, dy_perm) read as dense tiles, or the "
+                    "memory-lean path that gathers x and dY rows by token inside the GEMMs")
     return ap.parse_args()
 
 
@@ -269,30 +272,43 @@ def run_ours(args, rank, world, local_rank):
     e = lambda *s, dt=bf: torch.empty(s, dtype=dt, device=dev)
     ids, w = e(T, k, dt=i32), e(T, k, dt=f32)
     dbuf = dict(counts=e(E, dt=i32), m_indptr=e(E + 1, dt=i32), row_to_slot=e(R, dt=i32), slot_to_row=e(R, dt=i32),
-                w_perm=e(R, dt=f32), x_perm=e(R, H))
+                w_perm=e(R, dt=f32))
+    gather = args.inputs == "gather"
+    if not gather:
+        dbuf["x_perm"] = e(R, H)
     fbuf = dict(h_perm=e(R, I), gu_perm=e(R, 2 * I, dt=f32), y_perm=e(R, H))
     Y = e(T, H)
     bbuf = dict(dx=e(T, H), dw_gate_up=e(E, 2 * I, H), dw_down=e(E, H, I), d_logits=e(T, E, dt=f32))
     ws_d = e(moe.workspace_bytes("dispatch", T=T, E=E, k=k), dt=torch.uint8)
     ws_f = e(moe.workspace_bytes("grouped_swiglu_fwd", R=R, H=H, I=I, E=E), dt=torch.uint8)
-    ws_b = e(moe.workspace_bytes("bwd_dx_dw", T=T, H=H, I=I, E=E, k=k, saved_gu=True), dt=torch.uint8)
+    ws_b = e(moe.workspace_bytes("bwd_dx_dw", T=T, H=H, I=I, E=E, k=k, saved_gu=True, gather=gather), dt=torch.uint8)
 
+    # --inputs x_perm (default): the dispatch writes the expert-major copy x_perm (and the backward
+    # its dy_perm), which the GEMMs read as dense TMA tiles.  --inputs gather: the layer on
+    # token-major x and dY, the expert GEMMs copying their rows by token, so no expert-major copy
+    # exists (less memory, slower).
     def forward(lg, xx, y_out=None):
         moe.route_topk(lg, k, topk_ids=ids, topk_w=w)
-        moe.dispatch(ids, w, xx, E, out=dbuf, workspace=ws_d)
-        moe.grouped_swiglu_fwd(dbuf["x_perm"], dbuf["m_indptr"], wgu, wd, dbuf["w_perm"], out=fbuf, workspace=ws_f)
+        moe.dispatch(ids, w, None if gather else xx, E, out=dbuf, workspace=ws_d)
+        if gather:
+            moe.grouped_swiglu_fwd_gather(xx, dbuf["row_to_slot"], k, dbuf["m_indptr"], wgu, wd, dbuf["w_perm"],
+                                          out=fbuf, workspace=ws_f)
+        else:
+            moe.grouped_swiglu_fwd(dbuf["x_perm"], dbuf["m_indptr"], wgu, wd, dbuf["w_perm"], out=fbuf,
+                                   workspace=ws_f)
         moe.combine(fbuf["y_perm"], dbuf["slot_to_row"], T, k, out=Y if y_out is None else y_out)
 
-    def backward(dyy, dx_out=None, dl_out=None):
+    def backward(dyy, xx, dx_out=None, dl_out=None):
         out = dict(bbuf)
         if dx_out is not None:
             out.update(dx=dx_out, d_logits=dl_out)
-        moe.bwd_dx_dw(dyy, dbuf["x_perm"], fbuf["h_perm"], fbuf["gu_perm"], ids, w, dbuf["m_indptr"],
-                      dbuf["row_to_slot"], dbuf["slot_to_row"], dbuf["w_perm"], wgu, wd, out=out, workspace=ws_b)
+        bwd = moe.bwd_dx_dw_gather if gather else moe.bwd_dx_dw
+        bwd(dyy, xx if gather else dbuf["x_perm"], fbuf["h_perm"], fbuf["gu_perm"], ids, w, dbuf["m_indptr"],
+            dbuf["row_to_slot"], dbuf["slot_to_row"], dbuf["w_perm"], wgu, wd, out=out, workspace=ws_b)
 
     def step():
         forward(logits, x)
-        backward(dy)
+        backward(dy, x)
 
     def barrier():
         if dist is not None:
@@ -467,7 +483,7 @@ def run_ours(args, rank, world, local_rank):
                 lg, xx, dyy = d_in[b_]
                 Yb, dxb, dlb = d_out[b_]
                 forward(lg, xx, y_out=Yb)
-                backward(dyy, dx_out=dxb, dl_out=dlb)
+                backward(dyy, xx, dx_out=dxb, dl_out=dlb)
                 computed[b_].record(cur)
                 copy_s.wait_event(computed[b_])
                 with torch.cuda.stream(copy_s):
@@ -535,6 +551,7 @@ def run_ours(args, rank, world, local_rank):
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict(wl.as_dict(), **{"pass": "forward+backward", "parallelism": f"replicas x{world}",
+                                           "expert_inputs": args.inputs,
                                            "l2": f"inputs larger than L2: {(wgu.numel() + wd.numel()) * 2 / 1e9:.2f} GB "
                                                  f"of weights + activations streamed per step (L2 129 MB)"}),
             "tokens_per_s": round(tokens_per_s, 1),

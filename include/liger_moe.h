@@ -156,6 +156,25 @@ int liger_moe_grouped_swiglu_fwd(const void* x_perm, const int32_t* m_indptr, co
                                  size_t* workspace_bytes, void* stream);
 
 /*
+ * The same expert MLP on token-major input: row r's input is x[row_to_slot[r] / k],
+ * copied row by row by the gate/up GEMM's loader straight from x, so no
+ * expert-major copy of x is written or read (memory-lean; on GB300 the loader's
+ * row copies make this GEMM several times slower than the x_perm entry point).
+ * LightMoE README, "MoE inference" (the layer is called with token-major x and
+ * the routing ids, and copies rows in expert order itself).  Outputs are
+ * identical to liger_moe_dispatch's x_perm followed by
+ * liger_moe_grouped_swiglu_fwd.
+ *   x            [T, H] bf16, input.
+ *   row_to_slot  [R] int32, input (R = T*k), as produced by liger_moe_dispatch;
+ *                a value outside [0, R) sets LIGER_MOE_DEVERR_BAD_ROW and reads token 0.
+ * Other arguments, outputs and the workspace as liger_moe_grouped_swiglu_fwd.
+ */
+int liger_moe_grouped_swiglu_fwd_gather(const void* x, const int32_t* row_to_slot, int T, int k,
+                                        const int32_t* m_indptr, const void* w_gate_up, const void* w_down,
+                                        const float* w_perm, int H, int I, int E, void* h_perm, float* gu_perm,
+                                        void* y_perm, void* workspace, size_t* workspace_bytes, void* stream);
+
+/*
  * Combine: routed rows back to token order.  LigerCute README, "Forward
  * pass" (final local combine); LightMoE README, "Highlights" (deterministic
  * combine).
@@ -186,11 +205,12 @@ int liger_moe_combine(const void* y_perm, const int32_t* slot_to_row, int T, int
  *                                experts, gamma_j = <dY, expert-j output>; 0 elsewhere
  * Weight gradients are summed in a fixed order (no atomics): results are
  * identical from run to run.  The upstream gradient enters the expert GEMMs
- * unscaled; the routing weight is applied in fp32 to the dH accumulator.  The
- * weight-gradient GEMMs take their non-input operand (dgu for dW_gate_up,
- * w * h for dW_down) as two bf16 parts, hi + lo, so that operand carries
- * about 16 significant bits.  Limit: T*k < 2^30.  Workspace: about
- * R*(2H + 6I)*2 bytes, plus R*2I*4 more when gu_perm is NULL.
+ * unscaled (copied to expert-major order in the workspace); the routing
+ * weight is applied in fp32 to the dH accumulator.  The weight-gradient GEMMs
+ * take their non-input operand (dgu for dW_gate_up, w * h for dW_down) as two
+ * bf16 parts, hi + lo, so that operand carries about 16 significant bits.
+ * Limit: T*k < 2^30.  Workspace: about R*(2H + 6I)*2 bytes, plus R*2I*4 more
+ * when gu_perm is NULL.
  */
 int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const void* h_perm, const float* gu_perm,
                         const int32_t* topk_ids, const float* topk_w, const int32_t* m_indptr,
@@ -198,6 +218,23 @@ int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const void* h_perm, 
                         const void* w_gate_up, const void* w_down, int T, int H, int I, int E, int k,
                         void* dx, void* dw_gate_up, void* dw_down, float* d_logits, void* workspace,
                         size_t* workspace_bytes, void* stream);
+
+/*
+ * The same backward on token-major input: x [T, H] bf16 replaces x_perm.  The
+ * dH, dW_gate_up and dW_down GEMMs copy the rows of x and dy they need by token
+ * (row_to_slot[r] / k) straight from x and dy, so no expert-major copy of
+ * either exists (memory-lean, slower, as for the gathered forward).  LightMoE
+ * README, "MoE inference" and "MoE training"; LigerCute README, "Backward
+ * pass".  Every other argument, output and limit as liger_moe_bwd_dx_dw; the
+ * outputs are identical.  Workspace: about R*(H + 6I)*2 bytes, plus R*2I*4
+ * more when gu_perm is NULL.
+ */
+int liger_moe_bwd_dx_dw_gather(const void* dy, const void* x, const void* h_perm, const float* gu_perm,
+                               const int32_t* topk_ids, const float* topk_w, const int32_t* m_indptr,
+                               const int32_t* row_to_slot, const int32_t* slot_to_row, const float* w_perm,
+                               const void* w_gate_up, const void* w_down, int T, int H, int I, int E, int k,
+                               void* dx, void* dw_gate_up, void* dw_down, float* d_logits, void* workspace,
+                               size_t* workspace_bytes, void* stream);
 
 /*
  * Synchronises `stream`, then returns LIGER_MOE_OK and *flags = 0 when no

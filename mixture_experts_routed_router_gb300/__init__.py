@@ -17,8 +17,9 @@ import torch
 
 from . import build as _build
 
-__all__ = ["route_topk", "dispatch", "grouped_swiglu_fwd", "combine", "bwd_dx_dw", "device_error",
-           "workspace_bytes", "trace_enable", "trace_records", "LigerMoEError", "library_path", "load_library"]
+__all__ = ["route_topk", "dispatch", "grouped_swiglu_fwd", "grouped_swiglu_fwd_gather", "combine", "bwd_dx_dw",
+           "bwd_dx_dw_gather", "device_error", "workspace_bytes", "trace_enable", "trace_records", "LigerMoEError",
+           "library_path", "load_library"]
 
 _lock = threading.Lock()
 _lib = None
@@ -55,6 +56,8 @@ def load_library(build_if_missing: bool = True):
         lib.liger_moe_grouped_swiglu_fwd.argtypes = [P, P, P, P, P, I, I, I, I, P, P, P, P, S, P]
         lib.liger_moe_combine.argtypes = [P, P, I, I, I, P, P]
         lib.liger_moe_bwd_dx_dw.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, P, S, P]
+        lib.liger_moe_grouped_swiglu_fwd_gather.argtypes = [P, P, I, I, P, P, P, P, I, I, I, P, P, P, P, S, P]
+        lib.liger_moe_bwd_dx_dw_gather.argtypes = lib.liger_moe_bwd_dx_dw.argtypes
         lib.liger_moe_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
         lib.liger_moe_trace_enable.argtypes = [I]
         lib.liger_moe_trace_get.argtypes = [I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)]
@@ -62,7 +65,8 @@ def load_library(build_if_missing: bool = True):
         lib.liger_moe_status_string.restype = ctypes.c_char_p
         lib.liger_moe_status_string.argtypes = [I]
         for f in (lib.liger_moe_route_topk, lib.liger_moe_dispatch, lib.liger_moe_grouped_swiglu_fwd,
-                  lib.liger_moe_combine, lib.liger_moe_bwd_dx_dw, lib.liger_moe_device_error,
+                  lib.liger_moe_grouped_swiglu_fwd_gather, lib.liger_moe_combine, lib.liger_moe_bwd_dx_dw,
+                  lib.liger_moe_bwd_dx_dw_gather, lib.liger_moe_device_error,
                   lib.liger_moe_abi_version, lib.liger_moe_trace_enable, lib.liger_moe_trace_count,
                   lib.liger_moe_trace_get):
             f.restype = ctypes.c_int
@@ -144,8 +148,8 @@ def workspace_bytes(fn: str, **kw) -> int:
         p = ctypes.c_void_p(256)
         q = None if T * k == 0 else p
         gu = p if kw.get("saved_gu", True) else None
-        rc = lib.liger_moe_bwd_dx_dw(q, q, q, gu, q, q, p, q, q, q, p, p, T, H, I, E, k, q, p, p, q, None,
-                                     ctypes.byref(n), None)
+        f = lib.liger_moe_bwd_dx_dw_gather if kw.get("gather", False) else lib.liger_moe_bwd_dx_dw
+        rc = f(q, q, q, gu, q, q, p, q, q, q, p, p, T, H, I, E, k, q, p, p, q, None, ctypes.byref(n), None)
     else:
         raise ValueError(fn)
     _check(f"workspace query ({fn})", rc)
@@ -183,12 +187,7 @@ def dispatch(topk_ids, topk_w, x, num_experts, *, out=None, workspace=None, stre
     return o
 
 
-def grouped_swiglu_fwd(x_perm, m_indptr, w_gate_up, w_down, w_perm, *, save_gu=True, out=None, workspace=None,
-                       stream=None):
-    """Grouped SwiGLU expert MLP: returns (h_perm [R,I] bf16, gu_perm [R,2I] fp32 or None, y_perm [R,H] bf16)."""
-    lib = load_library()
-    _need(x_perm, "x_perm", torch.bfloat16)
-    R, H = x_perm.shape
+def _fwd_args(R, H, w_gate_up, w_down, m_indptr, w_perm, save_gu, out, workspace, dev):
     _need(w_gate_up, "w_gate_up", torch.bfloat16)
     E, two_i, _ = w_gate_up.shape
     I = two_i // 2
@@ -196,16 +195,44 @@ def grouped_swiglu_fwd(x_perm, m_indptr, w_gate_up, w_down, w_perm, *, save_gu=T
     _need(w_down, "w_down", torch.bfloat16, (E, H, I))
     _need(m_indptr, "m_indptr", torch.int32, (E + 1,))
     _need(w_perm, "w_perm", torch.float32, (R,))
-    dev = x_perm.device
     out = dict(out or {})
     h = _out(out.get("h_perm"), "h_perm", torch.bfloat16, (R, I), dev)
     gu = _out(out.get("gu_perm"), "gu_perm", torch.float32, (R, 2 * I), dev) if save_gu else None
     y = _out(out.get("y_perm"), "y_perm", torch.bfloat16, (R, H), dev)
     ws = _workspace(workspace, workspace_bytes("grouped_swiglu_fwd", R=R, H=H, I=I, E=E), dev)
+    return E, I, h, gu, y, ws
+
+
+def grouped_swiglu_fwd(x_perm, m_indptr, w_gate_up, w_down, w_perm, *, save_gu=True, out=None, workspace=None,
+                       stream=None):
+    """Grouped SwiGLU expert MLP: returns (h_perm [R,I] bf16, gu_perm [R,2I] fp32 or None, y_perm [R,H] bf16)."""
+    lib = load_library()
+    _need(x_perm, "x_perm", torch.bfloat16)
+    R, H = x_perm.shape
+    E, I, h, gu, y, ws = _fwd_args(R, H, w_gate_up, w_down, m_indptr, w_perm, save_gu, out, workspace, x_perm.device)
     n = ctypes.c_size_t(ws.numel())
     _check("liger_moe_grouped_swiglu_fwd", lib.liger_moe_grouped_swiglu_fwd(
         _ptr(x_perm), _ptr(m_indptr), _ptr(w_gate_up), _ptr(w_down), _ptr(w_perm), R, H, I, E, _ptr(h), _ptr(gu),
         _ptr(y), _ptr(ws), ctypes.byref(n), _stream(stream)))
+    return h, gu, y
+
+
+def grouped_swiglu_fwd_gather(x, row_to_slot, k, m_indptr, w_gate_up, w_down, w_perm, *, save_gu=True, out=None,
+                              workspace=None, stream=None):
+    """The expert MLP on token-major x [T,H]: row r reads x[row_to_slot[r] // k] (no x_perm).
+
+    Returns (h_perm, gu_perm or None, y_perm) as grouped_swiglu_fwd.
+    """
+    lib = load_library()
+    _need(x, "x", torch.bfloat16)
+    T, H = x.shape
+    R = T * k
+    _need(row_to_slot, "row_to_slot", torch.int32, (R,))
+    E, I, h, gu, y, ws = _fwd_args(R, H, w_gate_up, w_down, m_indptr, w_perm, save_gu, out, workspace, x.device)
+    n = ctypes.c_size_t(ws.numel())
+    _check("liger_moe_grouped_swiglu_fwd_gather", lib.liger_moe_grouped_swiglu_fwd_gather(
+        _ptr(x), _ptr(row_to_slot), T, k, _ptr(m_indptr), _ptr(w_gate_up), _ptr(w_down), _ptr(w_perm), H, I, E,
+        _ptr(h), _ptr(gu), _ptr(y), _ptr(ws), ctypes.byref(n), _stream(stream)))
     return h, gu, y
 
 
@@ -221,9 +248,8 @@ def combine(y_perm, slot_to_row, T, k, *, out=None, stream=None):
     return y
 
 
-def bwd_dx_dw(dy, x_perm, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_slot, slot_to_row, w_perm, w_gate_up,
-              w_down, *, out=None, workspace=None, stream=None):
-    """Backward of the layer: returns (dx [T,H], dw_gate_up [E,2I,H], dw_down [E,H,I], d_logits [T,E])."""
+def _bwd(fn, dy, x_src, x_name, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_slot, slot_to_row, w_perm,
+         w_gate_up, w_down, out, workspace, stream):
     lib = load_library()
     _need(dy, "dy", torch.bfloat16)
     T, H = dy.shape
@@ -232,7 +258,8 @@ def bwd_dx_dw(dy, x_perm, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_sl
     E, two_i, _ = w_gate_up.shape
     I = two_i // 2
     R = T * k
-    for t, n, dt, sh in ((x_perm, "x_perm", torch.bfloat16, (R, H)), (h_perm, "h_perm", torch.bfloat16, (R, I)),
+    x_shape = (T, H) if x_name == "x" else (R, H)
+    for t, n, dt, sh in ((x_src, x_name, torch.bfloat16, x_shape), (h_perm, "h_perm", torch.bfloat16, (R, I)),
                          (topk_w, "topk_w", torch.float32, (T, k)), (m_indptr, "m_indptr", torch.int32, (E + 1,)),
                          (row_to_slot, "row_to_slot", torch.int32, (R,)),
                          (slot_to_row, "slot_to_row", torch.int32, (R,)), (w_perm, "w_perm", torch.float32, (R,)),
@@ -247,14 +274,28 @@ def bwd_dx_dw(dy, x_perm, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_sl
     dwgu = _out(out.get("dw_gate_up"), "dw_gate_up", torch.bfloat16, (E, 2 * I, H), dev)
     dwd = _out(out.get("dw_down"), "dw_down", torch.bfloat16, (E, H, I), dev)
     dl = _out(out.get("d_logits"), "d_logits", torch.float32, (T, E), dev)
-    ws = _workspace(workspace, workspace_bytes("bwd_dx_dw", T=T, H=H, I=I, E=E, k=k, saved_gu=gu_perm is not None),
-                    dev)
+    ws = _workspace(workspace, workspace_bytes("bwd_dx_dw", T=T, H=H, I=I, E=E, k=k, saved_gu=gu_perm is not None,
+                                               gather=x_name == "x"), dev)
     n = ctypes.c_size_t(ws.numel())
-    _check("liger_moe_bwd_dx_dw", lib.liger_moe_bwd_dx_dw(
-        _ptr(dy), _ptr(x_perm), _ptr(h_perm), _ptr(gu_perm), _ptr(topk_ids), _ptr(topk_w), _ptr(m_indptr),
+    _check(fn, getattr(lib, fn)(
+        _ptr(dy), _ptr(x_src), _ptr(h_perm), _ptr(gu_perm), _ptr(topk_ids), _ptr(topk_w), _ptr(m_indptr),
         _ptr(row_to_slot), _ptr(slot_to_row), _ptr(w_perm), _ptr(w_gate_up), _ptr(w_down), T, H, I, E, k, _ptr(dx),
         _ptr(dwgu), _ptr(dwd), _ptr(dl), _ptr(ws), ctypes.byref(n), _stream(stream)))
     return dx, dwgu, dwd, dl
+
+
+def bwd_dx_dw(dy, x_perm, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_slot, slot_to_row, w_perm, w_gate_up,
+              w_down, *, out=None, workspace=None, stream=None):
+    """Backward of the layer: returns (dx [T,H], dw_gate_up [E,2I,H], dw_down [E,H,I], d_logits [T,E])."""
+    return _bwd("liger_moe_bwd_dx_dw", dy, x_perm, "x_perm", h_perm, gu_perm, topk_ids, topk_w, m_indptr,
+                row_to_slot, slot_to_row, w_perm, w_gate_up, w_down, out, workspace, stream)
+
+
+def bwd_dx_dw_gather(dy, x, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_slot, slot_to_row, w_perm,
+                     w_gate_up, w_down, *, out=None, workspace=None, stream=None):
+    """The backward on token-major x [T,H] (no x_perm); same outputs as bwd_dx_dw."""
+    return _bwd("liger_moe_bwd_dx_dw_gather", dy, x, "x", h_perm, gu_perm, topk_ids, topk_w, m_indptr,
+                row_to_slot, slot_to_row, w_perm, w_gate_up, w_down, out, workspace, stream)
 
 
 def device_error(stream=None) -> int:

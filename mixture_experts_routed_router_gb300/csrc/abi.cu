@@ -155,9 +155,9 @@ int current_device(DeviceInfo* info) {
 
 namespace {
 
-size_t bwd_workspace_bytes(long long R, int H, int I, int E, bool recompute_gu) {
+size_t bwd_workspace_bytes(long long R, int H, int I, int E, bool recompute_gu, bool gather) {
   size_t b = schedule_bytes(E);
-  b += align_up(static_cast<size_t>(R) * H * 2, 256);                 // dy_perm
+  if (!gather) b += align_up(static_cast<size_t>(R) * H * 2, 256);  // dy_perm
   b += align_up(static_cast<size_t>(R) * 2 * I * 2 * 2, 256);         // dgu (hi, lo)
   b += align_up(static_cast<size_t>(R) * H * 2, 256);                 // dx_perm
   b += align_up(static_cast<size_t>(R) * I * 2 * 2, 256);             // hw_perm (hi, lo)
@@ -226,16 +226,22 @@ LIGER_MOE_API int liger_moe_dispatch(const int32_t* topk_ids, const float* topk_
                          static_cast<cudaStream_t>(stream));
 }
 
-LIGER_MOE_API int liger_moe_grouped_swiglu_fwd(const void* x_perm, const int32_t* m_indptr, const void* w_gate_up,
-                                               const void* w_down, const float* w_perm, int R, int H, int I, int E,
-                                               void* h_perm, float* gu_perm, void* y_perm, void* workspace,
-                                               size_t* workspace_bytes, void* stream) {
+namespace {
+
+// Forward expert MLP.  A rows come from x_perm [R, H] or, when x != NULL, are gathered from
+// x [T, H] by token (row_to_slot[r] / k).
+int grouped_swiglu_fwd_impl(const void* x_perm, const void* x, const int32_t* row_to_slot, int T, int k,
+                            const int32_t* m_indptr, const void* w_gate_up, const void* w_down, const float* w_perm,
+                            long long R, int H, int I, int E, void* h_perm, float* gu_perm, void* y_perm,
+                            void* workspace, size_t* workspace_bytes, void* stream) {
   if (int rc = check_shapes(R, H, I, E)) return rc;
   if (workspace_bytes == nullptr || m_indptr == nullptr) return LIGER_MOE_ERR_INVALID_ARG;
-  if (R > 0 && (x_perm == nullptr || w_gate_up == nullptr || w_down == nullptr || w_perm == nullptr ||
+  const void* a_src = x != nullptr ? x : x_perm;
+  if (R > 0 && (a_src == nullptr || w_gate_up == nullptr || w_down == nullptr || w_perm == nullptr ||
                 h_perm == nullptr || y_perm == nullptr))
     return LIGER_MOE_ERR_INVALID_ARG;
-  if (!aligned16(x_perm) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(h_perm) ||
+  if (R > 0 && x != nullptr && row_to_slot == nullptr) return LIGER_MOE_ERR_INVALID_ARG;
+  if (!aligned16(a_src) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(h_perm) ||
       !aligned16(gu_perm) || !aligned16(y_perm))
     return LIGER_MOE_ERR_MISALIGNED;
   const size_t need = schedule_bytes(E);
@@ -251,21 +257,49 @@ LIGER_MOE_API int liger_moe_grouped_swiglu_fwd(const void* x_perm, const int32_t
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* tile_prefix = static_cast<int32_t*>(workspace);
   if (int rc = launch_tile_schedule(m_indptr, E, R, tile_prefix, dev, s)) return rc;
-  FwdGemmArgs a{static_cast<const uint16_t*>(x_perm),
-                m_indptr,
-                tile_prefix,
-                static_cast<const uint16_t*>(w_gate_up),
-                static_cast<const uint16_t*>(w_down),
-                w_perm,
-                R,
-                H,
-                I,
-                E,
-                static_cast<uint16_t*>(h_perm),
-                gu_perm,
-                static_cast<uint16_t*>(y_perm)};
+  FwdGemmArgs a{};
+  a.x_perm = static_cast<const uint16_t*>(x_perm);
+  a.x = static_cast<const uint16_t*>(x);
+  a.row_to_slot = row_to_slot;
+  a.T = T;
+  a.k = k;
+  a.m_indptr = m_indptr;
+  a.tile_prefix = tile_prefix;
+  a.w_gate_up = static_cast<const uint16_t*>(w_gate_up);
+  a.w_down = static_cast<const uint16_t*>(w_down);
+  a.w_perm = w_perm;
+  a.R = R;
+  a.H = H;
+  a.I = I;
+  a.E = E;
+  a.h_perm = static_cast<uint16_t*>(h_perm);
+  a.gu_perm = gu_perm;
+  a.y_perm = static_cast<uint16_t*>(y_perm);
   if (int rc = launch_gate_up(a, dev, s)) return rc;
   return launch_down(a, dev, s);
+}
+
+}  // namespace
+
+LIGER_MOE_API int liger_moe_grouped_swiglu_fwd(const void* x_perm, const int32_t* m_indptr, const void* w_gate_up,
+                                               const void* w_down, const float* w_perm, int R, int H, int I, int E,
+                                               void* h_perm, float* gu_perm, void* y_perm, void* workspace,
+                                               size_t* workspace_bytes, void* stream) {
+  return grouped_swiglu_fwd_impl(x_perm, nullptr, nullptr, 0, 1, m_indptr, w_gate_up, w_down, w_perm, R, H, I, E,
+                                 h_perm, gu_perm, y_perm, workspace, workspace_bytes, stream);
+}
+
+LIGER_MOE_API int liger_moe_grouped_swiglu_fwd_gather(const void* x, const int32_t* row_to_slot, int T, int k,
+                                                      const int32_t* m_indptr, const void* w_gate_up,
+                                                      const void* w_down, const float* w_perm, int H, int I, int E,
+                                                      void* h_perm, float* gu_perm, void* y_perm, void* workspace,
+                                                      size_t* workspace_bytes, void* stream) {
+  if (T < 0 || k < 1) return LIGER_MOE_ERR_INVALID_ARG;
+  if (k > kMaxTopK) return LIGER_MOE_ERR_CAPACITY;
+  const long long R = static_cast<long long>(T) * k;
+  if (R > 0 && x == nullptr) return LIGER_MOE_ERR_INVALID_ARG;
+  return grouped_swiglu_fwd_impl(nullptr, R > 0 ? x : nullptr, row_to_slot, T, k, m_indptr, w_gate_up, w_down,
+                                 w_perm, R, H, I, E, h_perm, gu_perm, y_perm, workspace, workspace_bytes, stream);
 }
 
 LIGER_MOE_API int liger_moe_combine(const void* y_perm, const int32_t* slot_to_row, int T, int H, int k, void* y,
@@ -281,12 +315,16 @@ LIGER_MOE_API int liger_moe_combine(const void* y_perm, const int32_t* slot_to_r
                         static_cast<cudaStream_t>(stream));
 }
 
-LIGER_MOE_API int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const void* h_perm, const float* gu_perm,
-                                      const int32_t* topk_ids, const float* topk_w, const int32_t* m_indptr,
-                                      const int32_t* row_to_slot, const int32_t* slot_to_row, const float* w_perm,
-                                      const void* w_gate_up, const void* w_down, int T, int H, int I, int E, int k,
-                                      void* dx, void* dw_gate_up, void* dw_down, float* d_logits, void* workspace,
-                                      size_t* workspace_bytes, void* stream) {
+namespace {
+
+// Backward of the layer.  With x_perm: dY is copied to expert-major order (dy_perm, in the
+// workspace) and both are read as dense tiles.  With x (x_perm NULL): x and dY rows are
+// gathered by token inside the GEMMs and no expert-major copy is made.
+int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void* h_perm, const float* gu_perm,
+                   const int32_t* topk_ids, const float* topk_w, const int32_t* m_indptr, const int32_t* row_to_slot,
+                   const int32_t* slot_to_row, const float* w_perm, const void* w_gate_up, const void* w_down, int T,
+                   int H, int I, int E, int k, void* dx, void* dw_gate_up, void* dw_down, float* d_logits,
+                   void* workspace, size_t* workspace_bytes, void* stream) {
   if (int rc = check_topk(T, E, k)) return rc;
   const long long R = static_cast<long long>(T) * k;
   if (int rc = check_shapes(R, H, I, E)) return rc;
@@ -294,15 +332,17 @@ LIGER_MOE_API int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const 
   if (workspace_bytes == nullptr || m_indptr == nullptr || w_gate_up == nullptr || w_down == nullptr ||
       dw_gate_up == nullptr || dw_down == nullptr)
     return LIGER_MOE_ERR_INVALID_ARG;
-  if (R > 0 && (dy == nullptr || x_perm == nullptr || h_perm == nullptr || topk_ids == nullptr ||
+  const void* x_src = x != nullptr ? x : x_perm;
+  if (R > 0 && (dy == nullptr || x_src == nullptr || h_perm == nullptr || topk_ids == nullptr ||
                 topk_w == nullptr || row_to_slot == nullptr || slot_to_row == nullptr || w_perm == nullptr ||
                 dx == nullptr || d_logits == nullptr))
     return LIGER_MOE_ERR_INVALID_ARG;
-  if (!aligned16(dy) || !aligned16(x_perm) || !aligned16(h_perm) || !aligned16(gu_perm) || !aligned16(w_gate_up) ||
+  if (!aligned16(dy) || !aligned16(x_src) || !aligned16(h_perm) || !aligned16(gu_perm) || !aligned16(w_gate_up) ||
       !aligned16(w_down) || !aligned16(dx) || !aligned16(dw_gate_up) || !aligned16(dw_down))
     return LIGER_MOE_ERR_MISALIGNED;
   const bool recompute = (gu_perm == nullptr);
-  const size_t need = bwd_workspace_bytes(R, H, I, E, recompute);
+  const bool gather = (x != nullptr);  // token-major inputs: x and dY rows gathered inside the GEMMs
+  const size_t need = bwd_workspace_bytes(R, H, I, E, recompute, gather);
   if (workspace == nullptr) {
     *workspace_bytes = need;
     return LIGER_MOE_OK;
@@ -315,7 +355,7 @@ LIGER_MOE_API int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const 
 
   uint8_t* cur = static_cast<uint8_t*>(workspace);
   int32_t* tile_prefix = carve<int32_t>(cur, schedule_bytes(E));
-  uint16_t* dy_perm = carve<uint16_t>(cur, static_cast<size_t>(R) * H * 2);
+  uint16_t* dy_perm = gather ? nullptr : carve<uint16_t>(cur, static_cast<size_t>(R) * H * 2);
   uint16_t* dgu = carve<uint16_t>(cur, static_cast<size_t>(R) * 2 * I * 2 * 2);
   uint16_t* dx_perm = carve<uint16_t>(cur, static_cast<size_t>(R) * H * 2);
   uint16_t* hw_perm = carve<uint16_t>(cur, static_cast<size_t>(R) * I * 2 * 2);
@@ -328,9 +368,14 @@ LIGER_MOE_API int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const 
   a.w_gate_up = static_cast<const uint16_t*>(w_gate_up);
   a.w_down = static_cast<const uint16_t*>(w_down);
   a.x_perm = static_cast<const uint16_t*>(x_perm);
+  a.x = static_cast<const uint16_t*>(x);
+  a.dy = static_cast<const uint16_t*>(dy);
+  a.dy_perm = dy_perm;
+  a.row_to_slot = row_to_slot;
+  a.T = T;
+  a.k = k;
   a.h_perm = static_cast<const uint16_t*>(h_perm);
   a.gu = recompute ? gu_ws : gu_perm;
-  a.dy_perm = dy_perm;
   a.w_perm = w_perm;
   a.hw_perm = hw_perm;
   a.dgu = dgu;
@@ -345,12 +390,27 @@ LIGER_MOE_API int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const 
 
   if (R > 0) {
     if (int rc = launch_tile_schedule(m_indptr, E, R, tile_prefix, dev, s)) return rc;
-    // dy_perm[r] = dY[token of r]
-    if (int rc = launch_gather_rows(static_cast<const uint16_t*>(dy), row_to_slot, nullptr, R, H, k, dy_perm, dev, s))
-      return rc;
+    if (!gather) {  // dy_perm[r] = dY[token of r]: the dH and dW_down GEMMs read it as dense tiles
+      if (int rc = launch_gather_rows(static_cast<const uint16_t*>(dy), row_to_slot, nullptr, R, H, k, dy_perm, dev, s))
+        return rc;
+    }
     if (recompute) {
-      FwdGemmArgs f{a.x_perm, m_indptr, tile_prefix, a.w_gate_up, a.w_down, w_perm, R, H, I, E, nullptr, gu_ws,
-                    nullptr};
+      FwdGemmArgs f{};
+      f.x_perm = a.x_perm;
+      f.x = a.x;
+      f.row_to_slot = row_to_slot;
+      f.T = T;
+      f.k = k;
+      f.m_indptr = m_indptr;
+      f.tile_prefix = tile_prefix;
+      f.w_gate_up = a.w_gate_up;
+      f.w_down = a.w_down;
+      f.w_perm = w_perm;
+      f.R = R;
+      f.H = H;
+      f.I = I;
+      f.E = E;
+      f.gu_perm = gu_ws;
       if (int rc = launch_gate_up(f, dev, s)) return rc;
     }
     if (int rc = launch_bwd_dh(a, dev, s)) return rc;
@@ -361,6 +421,32 @@ LIGER_MOE_API int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const 
   if (R > 0)
     return launch_router_grad(gdot, gdot_tiles(I), topk_ids, topk_w, slot_to_row, T, E, k, d_logits, dev, s);
   return LIGER_MOE_OK;
+}
+
+}  // namespace
+
+LIGER_MOE_API int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const void* h_perm, const float* gu_perm,
+                                      const int32_t* topk_ids, const float* topk_w, const int32_t* m_indptr,
+                                      const int32_t* row_to_slot, const int32_t* slot_to_row, const float* w_perm,
+                                      const void* w_gate_up, const void* w_down, int T, int H, int I, int E, int k,
+                                      void* dx, void* dw_gate_up, void* dw_down, float* d_logits, void* workspace,
+                                      size_t* workspace_bytes, void* stream) {
+  return bwd_dx_dw_impl(dy, x_perm, nullptr, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_slot, slot_to_row,
+                        w_perm, w_gate_up, w_down, T, H, I, E, k, dx, dw_gate_up, dw_down, d_logits, workspace,
+                        workspace_bytes, stream);
+}
+
+LIGER_MOE_API int liger_moe_bwd_dx_dw_gather(const void* dy, const void* x, const void* h_perm, const float* gu_perm,
+                                             const int32_t* topk_ids, const float* topk_w, const int32_t* m_indptr,
+                                             const int32_t* row_to_slot, const int32_t* slot_to_row,
+                                             const float* w_perm, const void* w_gate_up, const void* w_down, int T,
+                                             int H, int I, int E, int k, void* dx, void* dw_gate_up, void* dw_down,
+                                             float* d_logits, void* workspace, size_t* workspace_bytes,
+                                             void* stream) {
+  if (static_cast<long long>(T) * k > 0 && x == nullptr) return LIGER_MOE_ERR_INVALID_ARG;
+  return bwd_dx_dw_impl(dy, nullptr, x, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_slot, slot_to_row, w_perm,
+                        w_gate_up, w_down, T, H, I, E, k, dx, dw_gate_up, dw_down, d_logits, workspace,
+                        workspace_bytes, stream);
 }
 
 LIGER_MOE_API int liger_moe_trace_enable(int on) {

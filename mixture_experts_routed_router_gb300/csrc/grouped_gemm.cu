@@ -5,7 +5,11 @@
 // b laid out [num_experts, N, K]; LigerCute README, "LigerMoE design":
 // persistent warp-specialised TMA / MMA pipeline):
 //   warp 0      TMA producer: one elected lane streams A and B tiles into a
-//               4-stage shared-memory ring (128-byte swizzle), mbarrier-tracked
+//               shared-memory ring of 2-4 stages (128-byte swizzle), mbarrier-tracked.
+//               In the memory-lean variant an operand whose rows are token rows picked
+//               by the routing (x or dY in expert-major order) is instead gathered by
+//               the whole warp with TMA gather4 (four rows per copy) straight from the
+//               token-major tensor, so no permuted copy of it is ever written.
 //   warp 1      MMA issuer: allocates 512 TMEM columns, one elected lane issues
 //               tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32) and commits
 //               stage releases and accumulator-ready events to mbarriers
@@ -103,7 +107,9 @@ struct Params {
   const uint16_t* h_in;   // DH: h [R, I]
   uint16_t* hw_out;       // DH: bf16(w * h) [R, I]
   float* gdot;            // DH: [R, 2 n_tiles] partial <dh, h> (per N tile and column half)
-  long long R;            // DH: rows (offset of the lo half of hw_out)
+  long long R;            // routed rows (DH: offset of the lo half of hw_out)
+  const int32_t* row_slot;  // gathered operand: row_to_slot [R]; token of row r = row_slot[r] / topk
+  int topk;
   int* err;
 };
 
@@ -155,26 +161,6 @@ __device__ __forceinline__ void raise_abort(int* err, volatile int* abort_flag) 
     atomicOr(err, LIGER_MOE_DEVERR_WAIT_TIMEOUT);
     *abort_flag = 1;
   }
-}
-
-__device__ __forceinline__ void store16_bf16(uint16_t* dst, const float (&v)[16]) {
-  uint4 a, b;
-  a.x = pack_bf16x2(v[0], v[1]);
-  a.y = pack_bf16x2(v[2], v[3]);
-  a.z = pack_bf16x2(v[4], v[5]);
-  a.w = pack_bf16x2(v[6], v[7]);
-  b.x = pack_bf16x2(v[8], v[9]);
-  b.y = pack_bf16x2(v[10], v[11]);
-  b.z = pack_bf16x2(v[12], v[13]);
-  b.w = pack_bf16x2(v[14], v[15]);
-  reinterpret_cast<uint4*>(dst)[0] = a;
-  reinterpret_cast<uint4*>(dst)[1] = b;
-}
-
-__device__ __forceinline__ void store16_f32(float* dst, const float (&v)[16]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
 __device__ __forceinline__ void load16_f32(const float* src, float (&v)[16]) {
@@ -474,7 +460,79 @@ __device__ __forceinline__ void zero_tail_rows(uint8_t* stage_ptr, int valid, in
   }
 }
 
-template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT>
+// Operand sources.  Gather::None: both operands through tiled TMA boxes.  Gather::A / B: that
+// operand's rows are token rows of a token-major [T, cols] bf16 matrix, fetched with TMA
+// gather4 through a tensor map whose box is one row high; RowsM gathers a K-major A (rows =
+// M), RowsK an MN-major operand (rows = K).
+enum class Gather : int { None = 0, A = 1, B = 2 };
+
+// Tiled loads of one stage for the operands that are not gathered (lane 0 of the producer).
+template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT, bool kLoadA, bool kLoadB>
+__device__ __forceinline__ void load_stage_tiled(const CUtensorMap* tmA, const CUtensorMap* tmB, const Params& p,
+                                                 const Tile& tl, int kb, uint32_t sa, uint32_t sb, uint32_t fb) {
+  if constexpr (kLoadA) {
+    if constexpr (!A_MN) {
+      tma_load_2d(sa, tmA, fb, kb * BK, tl.m0);
+    } else {
+#pragma unroll
+      for (int part = 0; part < (SPLIT == 1 ? 2 : 1); ++part)
+#pragma unroll
+        for (int i = 0; i < BM / 64; ++i)
+          tma_load_2d(sa + part * A_BYTES + i * MN_BOX_BYTES, tmA, fb, tl.m0 + 64 * i,
+                      tl.row0 + kb * BK + part * p.a_split_rows);
+    }
+  }
+  if constexpr (kLoadB) {
+    if constexpr (!B_MN) {
+      if constexpr (EP == Epi::SwiGLU) {
+        const int r = tl.e * p.b_rows_per_expert + tl.nt * (BN / 2);
+        tma_load_2d(sb, tmB, fb, kb * BK, r);
+        tma_load_2d(sb + B_BYTES / 2, tmB, fb, kb * BK, r + p.b_split);
+      } else {
+        tma_load_2d(sb, tmB, fb, kb * BK, tl.e * p.b_rows_per_expert + tl.nt * BN);
+      }
+    } else {
+      const int krow = (S == Sched::RowsM) ? tl.e * p.b_rows_per_expert + kb * BK : tl.row0 + kb * BK;
+#pragma unroll
+      for (int part = 0; part < (SPLIT == 2 ? 2 : 1); ++part)
+#pragma unroll
+        for (int i = 0; i < BN / 64; ++i)
+          tma_load_2d(sb + part * B_BYTES + i * MN_BOX_BYTES, tmB, fb, tl.nt * BN + 64 * i,
+                      krow + part * p.b_split_rows);
+    }
+  }
+}
+
+// Tokens of the four rows a producer lane gathers for (tile, K block): RowsM, rows 4 lane ..
+// 4 lane + 3 of the tile; RowsK, rows 4 (lane & 15) .. + 3 of the K block.  Rows outside the
+// tile or expert take token 0 (their products are discarded, or their shared-memory rows are
+// zeroed before the MMA); a slot outside [0, R) raises BAD_ROW and also reads token 0.
+template <Sched S>
+__device__ __forceinline__ void gather_tokens(const Tile& tl, int kb, int lane, const Params& p, int (&tk)[4]) {
+  int first;
+  long long base;
+  if constexpr (S == Sched::RowsM) {
+    first = 4 * lane;
+    base = tl.m0;
+  } else {
+    first = kb * BK + 4 * (lane & 15);
+    base = tl.row0;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    int tok = 0;
+    if (first + j < tl.rows) {
+      const int slot = __ldg(p.row_slot + base + first + j);
+      if (slot >= 0 && slot < p.R)
+        tok = slot / p.topk;
+      else
+        atomicOr(p.err, LIGER_MOE_DEVERR_BAD_ROW);
+    }
+    tk[j] = tok;
+  }
+}
+
+template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT, Gather G>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
@@ -483,6 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int STAGES = L::kStages;
   constexpr int STAGE_BYTES = L::kStageBytes;
   static_assert(SPLIT == 0 || (S == Sched::RowsK && A_MN && B_MN), "hi/lo operands only in the dW GEMMs");
+  static_assert(G == Gather::None || (S == Sched::RowsM ? (G == Gather::A && !A_MN)
+                                                         : (G == Gather::A ? (A_MN && SPLIT != 1)
+                                                                           : (B_MN && SPLIT != 2))),
+                "RowsM gathers a K-major A; RowsK gathers an MN-major operand held as one part");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -535,57 +597,96 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if constexpr (G == Gather::None) {
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        bool failed = false;
+        for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
+          const Tile tl = decode_tile<S>(t, p);
+          for (int kb = 0; kb < tl.kb_count; ++kb) {
+            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
+              raise_abort(p.err, abort_flag);
+              failed = true;
+              break;
+            }
+            const uint32_t sa = sbase + stage * STAGE_BYTES;
+            const uint32_t fb = full0 + 8 * stage;
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            load_stage_tiled<S, EP, A_MN, B_MN, SPLIT, true, true>(&tmA, &tmB, p, tl, kb, sa, sa + L::kABytes, fb);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        if (failed) {
+          // let loads already in flight land before the CTA's shared memory goes away
+          for (int i = 0; i < 200; ++i) __nanosleep(1000);
+        }
+      }
+    } else {
+      // The whole warp: lane 0 arms the stage's barrier and loads the tiled operand, then every
+      // lane gathers four rows per 64-column box.  The tokens of the next (tile, K block) are read
+      // before the stage wait, so their latency overlaps it.
+      constexpr bool kGA = (G == Gather::A);
+      const CUtensorMap* tmG = kGA ? &tmA : &tmB;
       int stage = 0;
       uint32_t phase = 0;
       bool failed = false;
-      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
-        const Tile tl = decode_tile<S>(t, p);
-        for (int kb = 0; kb < tl.kb_count; ++kb) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
-            raise_abort(p.err, abort_flag);
-            failed = true;
-            break;
-          }
-          const uint32_t sa = sbase + stage * STAGE_BYTES;
-          const uint32_t sb = sa + L::kABytes;
-          const uint32_t fb = full0 + 8 * stage;
+      int t = blockIdx.x, kb = 0;
+      Tile tl{};
+      auto seek = [&](int from) {  // first tile at or after `from` (stride gridDim.x) with K blocks
+        for (t = from; t < total; t += gridDim.x) {
+          tl = decode_tile<S>(t, p);
+          if (tl.kb_count > 0) return;
+        }
+      };
+      seek(blockIdx.x);
+      int tok[4] = {0, 0, 0, 0};
+      if (t < total) gather_tokens<S>(tl, kb, lane, p, tok);
+      while (t < total) {
+        const Tile ct = tl;
+        const int ckb = kb;
+        const int c0 = tok[0], c1 = tok[1], c2 = tok[2], c3 = tok[3];
+        if (++kb == tl.kb_count) {
+          kb = 0;
+          seek(t + gridDim.x);
+        }
+        if (t < total && (S == Sched::RowsK || kb == 0)) gather_tokens<S>(tl, kb, lane, p, tok);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag))) {
+          if (lane == 0) raise_abort(p.err, abort_flag);
+          failed = true;
+          break;
+        }
+        const uint32_t sa = sbase + stage * STAGE_BYTES;
+        const uint32_t sb = sa + L::kABytes;
+        const uint32_t fb = full0 + 8 * stage;
+        if (lane == 0) {
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          if constexpr (!A_MN) {
-            tma_load_2d(sa, &tmA, fb, kb * BK, tl.m0);
-          } else {
+          load_stage_tiled<S, EP, A_MN, B_MN, SPLIT, !kGA, kGA>(&tmA, &tmB, p, ct, ckb, sa, sb, fb);
+        }
+        __syncwarp();
+        if constexpr (S == Sched::RowsM) {
+          // K-major A: four consecutive tile rows, one K block wide (4 x 128 bytes)
+          tma_gather4(sa + lane * 512, tmG, fb, ckb * BK, c0, c1, c2, c3);
+        } else {
+          // MN-major: four K rows of each 64-column box; half of the boxes per half-warp
+          constexpr int kBoxes = (kGA ? BM : BN) / 64;
+          const uint32_t dst = (kGA ? sa : sb) + (lane & 15) * 512;
+          const int col0 = kGA ? ct.m0 : ct.nt * BN;
 #pragma unroll
-            for (int part = 0; part < (SPLIT == 1 ? 2 : 1); ++part)
-#pragma unroll
-              for (int i = 0; i < BM / 64; ++i)
-                tma_load_2d(sa + part * A_BYTES + i * MN_BOX_BYTES, &tmA, fb, tl.m0 + 64 * i,
-                            tl.row0 + kb * BK + part * p.a_split_rows);
-          }
-          if constexpr (!B_MN) {
-            if constexpr (EP == Epi::SwiGLU) {
-              const int r = tl.e * p.b_rows_per_expert + tl.nt * (BN / 2);
-              tma_load_2d(sb, &tmB, fb, kb * BK, r);
-              tma_load_2d(sb + B_BYTES / 2, &tmB, fb, kb * BK, r + p.b_split);
-            } else {
-              tma_load_2d(sb, &tmB, fb, kb * BK, tl.e * p.b_rows_per_expert + tl.nt * BN);
-            }
-          } else {
-            const int krow = (S == Sched::RowsM) ? tl.e * p.b_rows_per_expert + kb * BK : tl.row0 + kb * BK;
-#pragma unroll
-            for (int part = 0; part < (SPLIT == 2 ? 2 : 1); ++part)
-#pragma unroll
-              for (int i = 0; i < BN / 64; ++i)
-                tma_load_2d(sb + part * B_BYTES + i * MN_BOX_BYTES, &tmB, fb, tl.nt * BN + 64 * i,
-                            krow + part * p.b_split_rows);
-          }
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+          for (int i = 0; i < kBoxes / 2; ++i) {
+            const int box = (lane >> 4) * (kBoxes / 2) + i;
+            tma_gather4(dst + box * MN_BOX_BYTES, tmG, fb, col0 + 64 * box, c0, c1, c2, c3);
           }
         }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-      if (failed) {
-        // let loads already in flight land before the CTA's shared memory goes away
+      if (failed && lane == 0) {
         for (int i = 0; i < 200; ++i) __nanosleep(1000);
       }
     }
@@ -823,10 +924,10 @@ int make_out_bf16_3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t ro
   return make_tmap_nd(m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3, dims, box);
 }
 
-template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT = 0>
+template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT = 0, Gather G = Gather::None>
 int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc0, const CUtensorMap& tc1,
                 const Params& p, int grid, cudaStream_t s, const char* name) {
-  auto kern = grouped_gemm_kernel<S, EP, A_MN, B_MN, SPLIT>;
+  auto kern = grouped_gemm_kernel<S, EP, A_MN, B_MN, SPLIT, G>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -851,6 +952,18 @@ Params base_params(const int32_t* m_indptr, const int32_t* tile_prefix, int E, i
   p.E = E;
   p.err = err;
   return p;
+}
+
+// Token-major bf16 matrix [rows, cols] as a gather source: box 64 columns x 1 row.
+int make_gather_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows) {
+  return make_tmap(m, ptr, cols, rows, 64, 1);
+}
+
+// Gathered operand: row r of the GEMM is row row_to_slot[r] / k of the source matrix.
+void set_gather(Params& p, const int32_t* row_to_slot, long long R, int k) {
+  p.row_slot = row_to_slot;
+  p.R = R;
+  p.topk = k;
 }
 
 int rows_m_grid(long long R, int E, int n_tiles, const DeviceInfo& dev) {
@@ -881,11 +994,13 @@ int gdot_tiles(int I) { return 2 * cdiv(I, BN); }
 
 int launch_gate_up(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   if (a.R == 0) return LIGER_MOE_OK;
+  const bool gather = a.x != nullptr;  // A rows gathered from x [T, H]; else read from x_perm [R, H]
   CUtensorMap ta, tb;
-  if (make_tmap(&ta, a.x_perm, a.H, a.R, BK, BM) ||
+  if ((gather ? make_gather_map(&ta, a.x, a.H, a.T) : make_tmap(&ta, a.x_perm, a.H, a.R, BK, BM)) ||
       make_tmap(&tb, a.w_gate_up, a.H, 2ULL * a.I * a.E, BK, BN / 2))
     return LIGER_MOE_ERR_LAUNCH;
   Params p = base_params(a.m_indptr, a.tile_prefix, a.E, dev.err_flag);
+  if (gather) set_gather(p, a.row_to_slot, a.R, a.k);
   p.n_tiles = cdiv(a.I, BN / 2);
   p.num_kb = a.H / BK;
   p.b_rows_per_expert = 2 * a.I;
@@ -901,9 +1016,11 @@ int launch_gate_up(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) 
   if (a.h_perm == nullptr) tc0 = tc1;
   if (a.gu_perm == nullptr) tc1 = tc0;
   if (a.h_perm == nullptr && a.gu_perm == nullptr) return LIGER_MOE_OK;
-  return launch_gemm<Sched::RowsM, Epi::SwiGLU, false, false>(ta, tb, tc0, tc1, p,
-                                                               rows_m_grid(a.R, a.E, p.n_tiles, dev), s,
-                                                               "gemm_gate_up_swiglu");
+  const int grid = rows_m_grid(a.R, a.E, p.n_tiles, dev);
+  if (gather)
+    return launch_gemm<Sched::RowsM, Epi::SwiGLU, false, false, 0, Gather::A>(ta, tb, tc0, tc1, p, grid, s,
+                                                                              "gemm_gate_up_swiglu");
+  return launch_gemm<Sched::RowsM, Epi::SwiGLU, false, false>(ta, tb, tc0, tc1, p, grid, s, "gemm_gate_up_swiglu");
 }
 
 int launch_down(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
@@ -929,10 +1046,16 @@ int launch_down(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
 
 int launch_bwd_dh(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   if (a.R == 0) return LIGER_MOE_OK;
+  // A: dY rows of the routed rows, from dy_perm [R, H] as dense tiles, or gathered by token from
+  // dY [T, H] when dy_perm is NULL
+  const bool gather = a.dy_perm == nullptr;
   CUtensorMap ta, tb;
-  if (make_tmap(&ta, a.dy_perm, a.H, a.R, BK, BM) || make_tmap(&tb, a.w_down, a.I, 1ULL * a.H * a.E, 64, BK))
+  if ((gather ? make_gather_map(&ta, a.dy, a.H, a.T) : make_tmap(&ta, a.dy_perm, a.H, a.R, BK, BM)) ||
+      make_tmap(&tb, a.w_down, a.I, 1ULL * a.H * a.E, 64, BK))
     return LIGER_MOE_ERR_LAUNCH;
   Params p = base_params(a.m_indptr, a.tile_prefix, a.E, dev.err_flag);
+  if (gather) set_gather(p, a.row_to_slot, a.R, a.k);
+  p.R = a.R;  // row offset of the lo halves of dgu and hw
   p.n_tiles = cdiv(a.I, BN);
   p.num_kb = a.H / BK;
   p.b_rows_per_expert = a.H;
@@ -944,12 +1067,14 @@ int launch_bwd_dh(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.hw_out = a.hw_perm;
   p.row_scale = a.w_perm;
   p.gdot = a.gdot;
-  p.R = a.R;
   CUtensorMap tc0, tc1;  // dgu [2R, 2I] and hw [2R, I]: hi rows then lo rows
   if (make_out_bf16_narrow(&tc0, a.dgu, 2ULL * a.I, 2ULL * a.R) || make_out_bf16_narrow(&tc1, a.hw_perm, a.I, 2ULL * a.R))
     return LIGER_MOE_ERR_LAUNCH;
-  return launch_gemm<Sched::RowsM, Epi::DH, false, true>(ta, tb, tc0, tc1, p, rows_m_grid(a.R, a.E, p.n_tiles, dev),
-                                                          s, "gemm_bwd_dh");
+  const int grid = rows_m_grid(a.R, a.E, p.n_tiles, dev);
+  if (gather)
+    return launch_gemm<Sched::RowsM, Epi::DH, false, true, 0, Gather::A>(ta, tb, tc0, tc1, p, grid, s,
+                                                                        "gemm_bwd_dh");
+  return launch_gemm<Sched::RowsM, Epi::DH, false, true>(ta, tb, tc0, tc1, p, grid, s, "gemm_bwd_dh");
 }
 
 int launch_bwd_dx(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
@@ -974,16 +1099,25 @@ int launch_bwd_dx(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
 
 int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   // dW_gu[e] = dgu_e^T x_e  ([2I, H]),  dW_d[e] = dY_e^T (w h)_e  ([H, I]); K = rows of e.
-  // With no rows at all (R = 0) every expert's gradient is zero: the kernel still
-  // runs to write the zeros, over 1-row dummy tensor maps that it never reads.
-  CUtensorMap ta, tb;
-  const uint64_t rows = a.R > 0 ? static_cast<uint64_t>(a.R) : 1;
+  // The token-row operands x_e and dY_e are read as dense tiles of x_perm / dy_perm [R, H], or
+  // gathered by token from x / dY [T, H] where those copies are absent.  With no rows at all
+  // (R = 0) every expert's gradient is zero: the kernel still runs to write the zeros, over
+  // 1-row dummy tensor maps that it never reads.
+  CUtensorMap ta, tb, tc0;
+  const bool empty = a.R == 0;
+  const uint64_t rows = empty ? 1 : static_cast<uint64_t>(a.R);
   Params p = base_params(a.m_indptr, nullptr, a.E, dev.err_flag);
+  const bool gather_x = a.x != nullptr || empty;
   // dW_gu[e] = dgu_hi_e^T x_e + dgu_lo_e^T x_e: each stage holds both parts of A (rows r and
   // R + r of dgu [2R, 2I]) and one B tile; two MMAs per K step.
-  if (make_tmap(&ta, a.R > 0 ? a.dgu : a.dw_gate_up, 2ULL * a.I, 2 * rows, 64, BK) ||
-      make_tmap(&tb, a.R > 0 ? a.x_perm : a.dw_gate_up, a.H, rows, 64, BK))
+  if (make_tmap(&ta, empty ? a.dw_gate_up : a.dgu, 2ULL * a.I, 2 * rows, 64, BK)) return LIGER_MOE_ERR_LAUNCH;
+  if (gather_x) {
+    set_gather(p, a.row_to_slot, a.R, a.k);
+    if (empty ? make_gather_map(&tb, a.dw_gate_up, a.H, 1) : make_gather_map(&tb, a.x, a.H, a.T))
+      return LIGER_MOE_ERR_LAUNCH;
+  } else if (make_tmap(&tb, a.x_perm, a.H, rows, 64, BK)) {
     return LIGER_MOE_ERR_LAUNCH;
+  }
   p.m_tiles = cdiv(2LL * a.I, BM);
   p.n_tiles = cdiv(a.H, BN);
   p.a_split_rows = static_cast<int>(a.R);
@@ -993,17 +1127,25 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.out = a.dw_gate_up;
   p.ld_out = a.H;
   p.out_expert_stride = 2LL * a.I * a.H;
-  CUtensorMap tc0;
   if (make_out_bf16_3d(&tc0, a.dw_gate_up, a.H, 2ULL * a.I, a.E)) return LIGER_MOE_ERR_LAUNCH;
-  int rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1>(
-      ta, tb, tc0, tc0, p, rows_k_grid(static_cast<long long>(a.E) * p.m_tiles * p.n_tiles, dev), s,
-      "gemm_bwd_dw_gate_up");
+  const int grid_gu = rows_k_grid(static_cast<long long>(a.E) * p.m_tiles * p.n_tiles, dev);
+  int rc = gather_x
+               ? launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::B>(ta, tb, tc0, tc0, p, grid_gu, s,
+                                                                                 "gemm_bwd_dw_gate_up")
+               : launch_gemm<Sched::RowsK, Epi::Store, true, true, 1>(ta, tb, tc0, tc0, p, grid_gu, s,
+                                                                      "gemm_bwd_dw_gate_up");
   if (rc) return rc;
-  // dW_d[e] = dY_e^T hw_hi_e + dY_e^T hw_lo_e: each stage holds one A tile and both parts of B
-  // (rows r and R + r of hw [2R, I]); two MMAs per K step.
-  if (make_tmap(&ta, a.R > 0 ? a.dy_perm : a.dw_down, a.H, rows, 64, BK) ||
-      make_tmap(&tb, a.R > 0 ? a.hw_perm : a.dw_down, a.I, 2 * rows, 64, BK))
+  // dW_d[e] = dY_e^T hw_hi_e + dY_e^T hw_lo_e: each stage holds one A tile (dY rows gathered by
+  // token) and both parts of B (rows r and R + r of hw [2R, I]); two MMAs per K step.
+  const bool gather_dy = a.dy_perm == nullptr || empty;
+  if (make_tmap(&tb, empty ? a.dw_down : a.hw_perm, a.I, 2 * rows, 64, BK)) return LIGER_MOE_ERR_LAUNCH;
+  if (gather_dy) {
+    set_gather(p, a.row_to_slot, a.R, a.k);
+    if (empty ? make_gather_map(&ta, a.dw_down, a.H, 1) : make_gather_map(&ta, a.dy, a.H, a.T))
+      return LIGER_MOE_ERR_LAUNCH;
+  } else if (make_tmap(&ta, a.dy_perm, a.H, rows, 64, BK)) {
     return LIGER_MOE_ERR_LAUNCH;
+  }
   p.m_tiles = cdiv(a.H, BM);
   p.n_tiles = cdiv(a.I, BN);
   p.a_split_rows = 0;
@@ -1014,9 +1156,11 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.ld_out = a.I;
   p.out_expert_stride = 1LL * a.H * a.I;
   if (make_out_bf16_3d(&tc0, a.dw_down, a.I, a.H, a.E)) return LIGER_MOE_ERR_LAUNCH;
-  return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2>(
-      ta, tb, tc0, tc0, p, rows_k_grid(static_cast<long long>(a.E) * p.m_tiles * p.n_tiles, dev), s,
-      "gemm_bwd_dw_down");
+  const int grid_d = rows_k_grid(static_cast<long long>(a.E) * p.m_tiles * p.n_tiles, dev);
+  if (gather_dy)
+    return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::A>(ta, tb, tc0, tc0, p, grid_d, s,
+                                                                           "gemm_bwd_dw_down");
+  return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2>(ta, tb, tc0, tc0, p, grid_d, s, "gemm_bwd_dw_down");
 }
 
 }  // namespace lmoe

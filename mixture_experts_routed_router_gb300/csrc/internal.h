@@ -56,7 +56,10 @@ int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, int32_t* t
                          cudaStream_t s);
 
 struct FwdGemmArgs {
-  const uint16_t* x_perm;
+  const uint16_t* x_perm;       // [R, H]; used when x is NULL
+  const uint16_t* x;            // [T, H] or NULL: A rows gathered by token (row_to_slot / k)
+  const int32_t* row_to_slot;   // [R] (gather only)
+  int T, k;                     // (gather only)
   const int32_t* m_indptr;
   const int32_t* tile_prefix;
   const uint16_t* w_gate_up;
@@ -78,10 +81,14 @@ struct BwdGemmArgs {
   const int32_t* tile_prefix;
   const uint16_t* w_gate_up;
   const uint16_t* w_down;
-  const uint16_t* x_perm;
+  const uint16_t* x_perm;   // [R, H]; used when x is NULL
+  const uint16_t* x;        // [T, H] or NULL: dW_gate_up's B rows gathered by token
+  const uint16_t* dy;       // [T, H]: rows gathered by token when dy_perm is NULL
+  const uint16_t* dy_perm;  // [R, H] dY[token of row] (read as dense tiles), or NULL
+  const int32_t* row_to_slot;  // [R]; token of row r = row_to_slot[r] / k
+  int T, k;
   const uint16_t* h_perm;
-  const float* gu;       // [R, 2I] fp32 [g | u] (saved or recomputed)
-  const uint16_t* dy_perm;  // [R, H] dY[token of row]
+  const float* gu;       // [R, 2I] fp32 [dh/dg | dh/du] (saved or recomputed)
   const float* w_perm;   // [R]
   uint16_t* hw_perm;     // [2R, I]: rows [0,R) bf16(w h), rows [R,2R) bf16(w h - hi)
   uint16_t* dgu;         // [2R, 2I]: rows [0,R) bf16(dgu), rows [R,2R) bf16(dgu - hi)

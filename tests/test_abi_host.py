@@ -25,10 +25,10 @@ def lib():
     return moe.load_library()
 
 
-def test_header_declares_the_five_entry_points():
+def test_header_declares_the_entry_points():
     names = declared_functions()
     for f in ("liger_moe_route_topk", "liger_moe_dispatch", "liger_moe_grouped_swiglu_fwd", "liger_moe_combine",
-              "liger_moe_bwd_dx_dw"):
+              "liger_moe_bwd_dx_dw", "liger_moe_grouped_swiglu_fwd_gather", "liger_moe_bwd_dx_dw_gather"):
         assert f in names
 
 
@@ -97,8 +97,40 @@ def test_grouped_validation_and_query(lib):
 def test_bwd_workspace_grows_when_recomputing(lib):
     a = moe.workspace_bytes("bwd_dx_dw", T=256, H=256, I=128, E=8, k=2, saved_gu=True)
     b = moe.workspace_bytes("bwd_dx_dw", T=256, H=256, I=128, E=8, k=2, saved_gu=False)
-    R = 512
-    assert a >= R * (256 * 2 * 2 + 2 * 128 * 2) and b >= a + R * 2 * 128 * 2
+    R, H, I = 512, 256, 128
+    # dy_perm [R,H] + dx_perm [R,H] + dgu hi/lo [2R,2I] + w*h hi/lo [2R,I] (bf16)
+    assert a >= R * (4 * H + 12 * I)
+    assert b >= a + R * 2 * I * 4
+    # token-major entry point: dY rows are gathered inside the GEMMs, so no dy_perm
+    g = moe.workspace_bytes("bwd_dx_dw", T=256, H=256, I=128, E=8, k=2, saved_gu=True, gather=True)
+    assert g >= R * (2 * H + 12 * I) and a - g >= R * H * 2
+
+
+def test_gather_entry_points_validate_like_their_x_perm_twins(lib):
+    n = ctypes.c_size_t(0)
+    f = lib.liger_moe_grouped_swiglu_fwd_gather
+    # (x, row_to_slot, T, k, m_indptr, w_gate_up, w_down, w_perm, H, I, E, h, gu, y, ws, ws_bytes, stream)
+    assert f(D, D, 512, 2, D, D, D, D, 256, 128, 8, D, None, D, None, ctypes.byref(n), None) == OK
+    q = n.value
+    assert lib.liger_moe_grouped_swiglu_fwd(D, D, D, D, D, 1024, 256, 128, 8, D, None, D, None, ctypes.byref(n),
+                                            None) == OK
+    assert n.value == q
+    assert f(None, D, 512, 2, D, D, D, D, 256, 128, 8, D, None, D, None, ctypes.byref(n), None) == INVALID
+    assert f(D, None, 512, 2, D, D, D, D, 256, 128, 8, D, None, D, None, ctypes.byref(n), None) == INVALID
+    assert f(D, D, 512, 0, D, D, D, D, 256, 128, 8, D, None, D, None, ctypes.byref(n), None) == INVALID
+    assert f(D, D, 512, 2, D, D, D, D, 200, 128, 8, D, None, D, None, ctypes.byref(n), None) == MISALIGNED
+    assert f(ctypes.c_void_p(258), D, 512, 2, D, D, D, D, 256, 128, 8, D, None, D, None, ctypes.byref(n),
+             None) == MISALIGNED
+    g = lib.liger_moe_bwd_dx_dw_gather
+    args = [D, D, D, D, D, D, D, D, D, D, D, D, 256, 256, 128, 8, 2, D, D, D, D, None, ctypes.byref(n), None]
+    assert g(*args) == OK
+    assert n.value == moe.workspace_bytes("bwd_dx_dw", T=256, H=256, I=128, E=8, k=2, saved_gu=True, gather=True)
+    bad = list(args)
+    bad[1] = None  # x
+    assert g(*bad) == INVALID
+    bad = list(args)
+    bad[16] = 9  # k > E
+    assert g(*bad) == INVALID
 
 
 def test_combine_argument_errors(lib):

@@ -1,4 +1,5 @@
-"""Full-size parity on every workload shape, in the launch configuration the benchmark uses.
+"""Full-size parity on every workload shape, in the launch configuration the benchmark uses
+(dispatch writes x_perm; the expert GEMMs read expert-major tiles).
 
 Routing ids, counts, m_indptr and both permutations are compared whole and must
 be bit-exact.  Float outputs are compared on samples the oracle computes one by
@@ -102,11 +103,10 @@ def test_full_size_sampled_parity(name):
     toks = np.sort(rng.choice(T, size=min(N_TOKENS, T), replace=False)).astype(np.int32)
     rows = np.sort(rng.choice(R, size=min(64, R), replace=False)).astype(np.int32)
 
-    # expert MLP rows (h, y) on the GPU's dispatched inputs
-    xp = to_host(d["x_perm"][torch.from_numpy(rows).long().cuda()])
+    # expert MLP rows (h, y): each row's input is its token's x (the dispatch above is bit-exact)
     sub_indptr = ref["m_indptr"]
     full_xperm = np.zeros((R, H), np.uint16)  # only the sampled rows are read by the oracle
-    full_xperm[rows] = xp
+    full_xperm[rows] = inp["x"][ref["row_to_slot"][rows] // k]
     rh, _, ry = oracle.grouped_swiglu_rows(full_xperm, sub_indptr, inp["wgu"], inp["wd"], to_host(d["w_perm"]), rows)
     ridx = torch.from_numpy(rows).long().cuda()
     assert_close(bf16_to_f64(to_host(h[ridx])), bf16_to_f64(rh), f"{name} h rows")
@@ -173,3 +173,26 @@ def test_full_size_backward_isolated(name):
     eidx = torch.from_numpy(exps).long().cuda()
     assert_close(bf16_to_f64(to_host(dwgu[eidx])), bf16_to_f64(rdwgu), f"{name} dW_gate_up (isolated)", per_expert=True)
     assert_close(bf16_to_f64(to_host(dwd[eidx])), bf16_to_f64(rdwd), f"{name} dW_down (isolated)", per_expert=True)
+
+
+def test_full_size_gathered_and_dispatched_inputs_agree_bitwise():
+    """On the benchmark's workload, the x_perm entry points give the same bits as the gathered ones."""
+    wl = synthetic.WORKLOADS["fwd_T8192_H2048_I512_E256_k8"]
+    inp = synthetic.make_inputs(wl, seed=0)
+    k, E = wl.k, wl.E
+    logits, x, dy = to_dev(inp["logits"]), to_dev(inp["x"]), to_dev(inp["dy"])
+    wgu, wd = to_dev(inp["wgu"]), to_dev(inp["wd"])
+    ids, w = moe.route_topk(logits, k)
+    d = moe.dispatch(ids, w, x, E)
+    ga = moe.grouped_swiglu_fwd_gather(x, d["row_to_slot"], k, d["m_indptr"], wgu, wd, d["w_perm"])
+    pa = moe.grouped_swiglu_fwd(d["x_perm"], d["m_indptr"], wgu, wd, d["w_perm"])
+    for u, v, name in zip(ga, pa, ("h", "gu", "y_perm")):
+        assert torch.equal(u, v), name
+    h, gu, _ = ga
+    del pa
+    common = (h, gu, ids, w, d["m_indptr"], d["row_to_slot"], d["slot_to_row"], d["w_perm"], wgu, wd)
+    gb = moe.bwd_dx_dw_gather(dy, x, *common)
+    pb = moe.bwd_dx_dw(dy, d["x_perm"], *common)
+    for u, v, name in zip(gb, pb, ("dX", "dW_gate_up", "dW_down", "d_logits")):
+        assert torch.equal(u, v), name
+    assert moe.device_error() == 0

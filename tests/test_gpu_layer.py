@@ -25,20 +25,38 @@ CASES = [
 ]
 
 
-def _run_forward(wl, inp, save_gu=True):
+MODES = ["x_perm", "gather"]  # expert inputs from the dispatched copy, or gathered by token inside the GEMMs
+
+
+def _run_forward(wl, inp, save_gu=True, mode="x_perm"):
     ids, w = moe.route_topk(to_dev(inp["logits"]), wl.k)
     x = to_dev(inp["x"])
-    d = moe.dispatch(ids, w, x, wl.E)
     wgu, wd = to_dev(inp["wgu"]), to_dev(inp["wd"])
-    h, gu, y_perm = moe.grouped_swiglu_fwd(d["x_perm"], d["m_indptr"], wgu, wd, d["w_perm"], save_gu=save_gu)
+    if mode == "gather":
+        d = moe.dispatch(ids, w, None, wl.E)
+        h, gu, y_perm = moe.grouped_swiglu_fwd_gather(x, d["row_to_slot"], wl.k, d["m_indptr"], wgu, wd, d["w_perm"],
+                                                      save_gu=save_gu)
+    else:
+        d = moe.dispatch(ids, w, x, wl.E)
+        h, gu, y_perm = moe.grouped_swiglu_fwd(d["x_perm"], d["m_indptr"], wgu, wd, d["w_perm"], save_gu=save_gu)
     Y = moe.combine(y_perm, d["slot_to_row"], wl.T, wl.k)
-    return dict(ids=ids, w=w, x=x, d=d, wgu=wgu, wd=wd, h=h, gu=gu, y_perm=y_perm, Y=Y)
+    return dict(ids=ids, w=w, x=x, d=d, wgu=wgu, wd=wd, h=h, gu=gu, y_perm=y_perm, Y=Y, mode=mode)
+
+
+def _run_backward(g, dy, **kw):
+    d = g["d"]
+    if g["mode"] == "gather":
+        return moe.bwd_dx_dw_gather(dy, g["x"], g["h"], g["gu"], g["ids"], g["w"], d["m_indptr"], d["row_to_slot"],
+                                    d["slot_to_row"], d["w_perm"], g["wgu"], g["wd"], **kw)
+    return moe.bwd_dx_dw(dy, d["x_perm"], g["h"], g["gu"], g["ids"], g["w"], d["m_indptr"], d["row_to_slot"],
+                         d["slot_to_row"], d["w_perm"], g["wgu"], g["wd"], **kw)
 
 
 @pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
-def test_forward_parity(wl):
+@pytest.mark.parametrize("mode", MODES)
+def test_forward_parity(wl, mode):
     inp = synthetic.make_inputs(wl)
-    g = _run_forward(wl, inp)
+    g = _run_forward(wl, inp, mode=mode)
     assert moe.device_error() == 0
     ids, w = oracle.route_topk(inp["logits"], wl.k)
     np.testing.assert_array_equal(to_host(g["ids"]), ids)
@@ -80,13 +98,11 @@ def test_identity_expert_roundtrip_on_gpu():
 
 @pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
 @pytest.mark.parametrize("save_gu", [True, False], ids=["saved_gu", "recomputed_gu"])
-def test_backward_parity(wl, save_gu):
+@pytest.mark.parametrize("mode", MODES)
+def test_backward_parity(wl, save_gu, mode):
     inp = synthetic.make_inputs(wl)
-    g = _run_forward(wl, inp, save_gu=save_gu)
-    dy = to_dev(inp["dy"])
-    d = g["d"]
-    dx, dwgu, dwd, dl = moe.bwd_dx_dw(dy, d["x_perm"], g["h"], g["gu"], g["ids"], g["w"], d["m_indptr"],
-                                      d["row_to_slot"], d["slot_to_row"], d["w_perm"], g["wgu"], g["wd"])
+    g = _run_forward(wl, inp, save_gu=save_gu, mode=mode)
+    dx, dwgu, dwd, dl = _run_backward(g, to_dev(inp["dy"]))
     assert moe.device_error() == 0
     ids, w = oracle.route_topk(inp["logits"], wl.k)
     rdx, rdl = oracle.backward_tokens(inp["x"], inp["dy"], inp["wgu"], inp["wd"], ids, w)
@@ -99,6 +115,20 @@ def test_backward_parity(wl, save_gu):
     assert_close(bf16_to_f64(to_host(dwd)), bf16_to_f64(rdwd), "dW_down", per_expert=True)
     empty = np.nonzero(np.bincount(ids.ravel(), minlength=wl.E) == 0)[0]
     assert np.all(to_host(dwgu)[empty] == 0) and np.all(to_host(dwd)[empty] == 0)
+
+
+@pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
+def test_gathered_inputs_match_the_dispatched_copy_bitwise(wl):
+    """Gathering rows by token inside the GEMMs feeds the tensor cores the same bytes as x_perm."""
+    inp = synthetic.make_inputs(wl)
+    a = _run_forward(wl, inp, mode="x_perm")
+    b = _run_forward(wl, inp, mode="gather")
+    for key in ("h", "gu", "y_perm", "Y"):
+        assert torch.equal(a[key], b[key]), key
+    dy = to_dev(inp["dy"])
+    for u, v, name in zip(_run_backward(a, dy), _run_backward(b, dy), ("dX", "dW_gate_up", "dW_down", "d_logits")):
+        assert torch.equal(u, v), name
+    assert moe.device_error() == 0
 
 
 def test_backward_is_deterministic():
@@ -114,21 +144,39 @@ def test_backward_is_deterministic():
         assert torch.equal(u, v)
 
 
-def test_zero_tokens_gives_zero_weight_gradients():
+@pytest.mark.parametrize("mode", MODES)
+def test_zero_tokens_gives_zero_weight_gradients(mode):
     wl = W("zero_T0_H128_I64_E4_k2", 0, 128, 64, 4, 2)
     E, H, I = wl.E, wl.H, wl.I
     z = lambda *s, dt=torch.bfloat16: torch.empty(s, dtype=dt, device="cuda")
-    d = moe.dispatch(z(0, 2, dt=torch.int32), z(0, 2, dt=torch.float32), z(0, H), E)
+    x = z(0, H)
+    d = moe.dispatch(z(0, 2, dt=torch.int32), z(0, 2, dt=torch.float32), x, E)
     wgu = torch.randn(E, 2 * I, H, device="cuda").to(torch.bfloat16)
     wd = torch.randn(E, H, I, device="cuda").to(torch.bfloat16)
-    h, gu, y = moe.grouped_swiglu_fwd(d["x_perm"], d["m_indptr"], wgu, wd, d["w_perm"])
+    if mode == "gather":
+        h, gu, y = moe.grouped_swiglu_fwd_gather(x, d["row_to_slot"], 2, d["m_indptr"], wgu, wd, d["w_perm"])
+    else:
+        h, gu, y = moe.grouped_swiglu_fwd(d["x_perm"], d["m_indptr"], wgu, wd, d["w_perm"])
     out = dict(dw_gate_up=torch.full((E, 2 * I, H), 7.0, device="cuda").to(torch.bfloat16),
                dw_down=torch.full((E, H, I), 7.0, device="cuda").to(torch.bfloat16))
-    dx, dwgu, dwd, dl = moe.bwd_dx_dw(z(0, H), d["x_perm"], h, gu, z(0, 2, dt=torch.int32),
-                                      z(0, 2, dt=torch.float32), d["m_indptr"], d["row_to_slot"], d["slot_to_row"],
-                                      d["w_perm"], wgu, wd, out=out)
+    bwd = moe.bwd_dx_dw_gather if mode == "gather" else moe.bwd_dx_dw
+    dx, dwgu, dwd, dl = bwd(z(0, H), x if mode == "gather" else d["x_perm"], h, gu, z(0, 2, dt=torch.int32),
+                            z(0, 2, dt=torch.float32), d["m_indptr"], d["row_to_slot"], d["slot_to_row"],
+                            d["w_perm"], wgu, wd, out=out)
     assert moe.device_error() == 0
     assert torch.count_nonzero(dwgu) == 0 and torch.count_nonzero(dwd) == 0
+
+
+def test_bad_row_to_slot_is_flagged_not_faulted():
+    wl = CASES[0]
+    inp = synthetic.make_inputs(wl)
+    g = _run_forward(wl, inp, mode="gather")
+    assert moe.device_error() == 0
+    bad = g["d"]["row_to_slot"].clone()
+    bad[5] = wl.R + 7
+    bad[9] = -3
+    moe.grouped_swiglu_fwd_gather(g["x"], bad, wl.k, g["d"]["m_indptr"], g["wgu"], g["wd"], g["d"]["w_perm"])
+    assert moe.device_error() & 0x2
 
 
 def test_bad_indptr_is_flagged_not_faulted():
