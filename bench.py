@@ -566,22 +566,29 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
+def kernel_source_hash() -> str:
+    """sha256 over the GEMM kernel's sources (the kernel file and its inline-PTX header)."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in ("grouped_gemm.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "mixture_experts_routed_router_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def load_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of `kernel` from a committed ncu capture, if one matches.
 
     None when there is no capture for this workload and kernel, or when the GEMM source
     has changed since the counters were taken (the capture records its hash).
     """
-    import hashlib
-
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "mixture_experts_routed_router_gb300", "csrc", "grouped_gemm.cu")
     try:
         with open(path) as f:
             entry = json.load(f)[workload][kernel]
-        with open(src, "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != entry.get("kernel_source_sha256"):
-                return None
+        if kernel_source_hash() != entry.get("kernel_source_sha256"):
+            return None
         return entry["dram_bytes_per_launch"]
     except (OSError, KeyError, ValueError, TypeError):
         return None

@@ -155,12 +155,16 @@ int current_device(DeviceInfo* info) {
 
 namespace {
 
+// Rows of each half of the padded weight-gradient operands: every expert's rows rounded up to 16.
+long long padded_rows(long long R, int E) { return R + 15LL * E; }
+
 size_t bwd_workspace_bytes(long long R, int H, int I, int E, bool recompute_gu, bool gather) {
-  size_t b = schedule_bytes(E);
+  const long long Rp = padded_rows(R, E);
+  size_t b = 2 * schedule_bytes(E);                                   // tile prefix, padded row prefix
   if (!gather) b += align_up(static_cast<size_t>(R) * H * 2, 256);  // dy_perm
-  b += align_up(static_cast<size_t>(R) * 2 * I * 2 * 2, 256);         // dgu (hi, lo)
+  b += align_up(static_cast<size_t>(Rp) * 2 * I * 2 * 2, 256);        // dgu (hi, lo), padded rows
   b += align_up(static_cast<size_t>(R) * H * 2, 256);                 // dx_perm
-  b += align_up(static_cast<size_t>(R) * I * 2 * 2, 256);             // hw_perm (hi, lo)
+  b += align_up(static_cast<size_t>(Rp) * I * 2 * 2, 256);            // hw_perm (hi, lo), padded rows
   b += align_up(static_cast<size_t>(R) * gdot_tiles(I) * 4, 256);     // gdot
   if (recompute_gu) b += align_up(static_cast<size_t>(R) * 2 * I * 4, 256);
   return b;
@@ -256,7 +260,7 @@ int grouped_swiglu_fwd_impl(const void* x_perm, const void* x, const int32_t* ro
   if (R == 0) return LIGER_MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* tile_prefix = static_cast<int32_t*>(workspace);
-  if (int rc = launch_tile_schedule(m_indptr, E, R, tile_prefix, dev, s)) return rc;
+  if (int rc = launch_tile_schedule(m_indptr, E, R, tile_prefix, nullptr, dev, s)) return rc;
   FwdGemmArgs a{};
   a.x_perm = static_cast<const uint16_t*>(x_perm);
   a.x = static_cast<const uint16_t*>(x);
@@ -328,7 +332,7 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
   if (int rc = check_topk(T, E, k)) return rc;
   const long long R = static_cast<long long>(T) * k;
   if (int rc = check_shapes(R, H, I, E)) return rc;
-  if (2 * R > kIndexLimit) return LIGER_MOE_ERR_CAPACITY;  // the dW_down operand has 2R rows
+  if (2 * padded_rows(R, E) > kIndexLimit) return LIGER_MOE_ERR_CAPACITY;  // the padded dW operands' rows
   if (workspace_bytes == nullptr || m_indptr == nullptr || w_gate_up == nullptr || w_down == nullptr ||
       dw_gate_up == nullptr || dw_down == nullptr)
     return LIGER_MOE_ERR_INVALID_ARG;
@@ -354,11 +358,13 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   uint8_t* cur = static_cast<uint8_t*>(workspace);
+  const long long Rp = padded_rows(R, E);
   int32_t* tile_prefix = carve<int32_t>(cur, schedule_bytes(E));
+  int32_t* pad_indptr = carve<int32_t>(cur, schedule_bytes(E));
   uint16_t* dy_perm = gather ? nullptr : carve<uint16_t>(cur, static_cast<size_t>(R) * H * 2);
-  uint16_t* dgu = carve<uint16_t>(cur, static_cast<size_t>(R) * 2 * I * 2 * 2);
+  uint16_t* dgu = carve<uint16_t>(cur, static_cast<size_t>(Rp) * 2 * I * 2 * 2);
   uint16_t* dx_perm = carve<uint16_t>(cur, static_cast<size_t>(R) * H * 2);
-  uint16_t* hw_perm = carve<uint16_t>(cur, static_cast<size_t>(R) * I * 2 * 2);
+  uint16_t* hw_perm = carve<uint16_t>(cur, static_cast<size_t>(Rp) * I * 2 * 2);
   float* gdot = carve<float>(cur, static_cast<size_t>(R) * gdot_tiles(I) * 4);
   float* gu_ws = recompute ? carve<float>(cur, static_cast<size_t>(R) * 2 * I * 4) : nullptr;
 
@@ -377,6 +383,8 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
   a.h_perm = static_cast<const uint16_t*>(h_perm);
   a.gu = recompute ? gu_ws : gu_perm;
   a.w_perm = w_perm;
+  a.pad_indptr = pad_indptr;
+  a.R_pad = Rp;
   a.hw_perm = hw_perm;
   a.dgu = dgu;
   a.dx_perm = dx_perm;
@@ -389,7 +397,7 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
   a.E = E;
 
   if (R > 0) {
-    if (int rc = launch_tile_schedule(m_indptr, E, R, tile_prefix, dev, s)) return rc;
+    if (int rc = launch_tile_schedule(m_indptr, E, R, tile_prefix, pad_indptr, dev, s)) return rc;
     if (!gather) {  // dy_perm[r] = dY[token of r]: the dH and dW_down GEMMs read it as dense tiles
       if (int rc = launch_gather_rows(static_cast<const uint16_t*>(dy), row_to_slot, nullptr, R, H, k, dy_perm, dev, s))
         return rc;

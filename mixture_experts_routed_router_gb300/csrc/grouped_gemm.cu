@@ -107,7 +107,14 @@ struct Params {
   const uint16_t* h_in;   // DH: h [R, I]
   uint16_t* hw_out;       // DH: bf16(w * h) [R, I]
   float* gdot;            // DH: [R, 2 n_tiles] partial <dh, h> (per N tile and column half)
-  long long R;            // routed rows (DH: offset of the lo half of hw_out)
+  long long R;            // routed rows
+  // Row-padded operands of the weight-gradient GEMMs: the dH epilogue writes dgu and w h with
+  // each expert's rows starting at pad_indptr[e] (exclusive scan of the row counts rounded up
+  // to 16) and zero rows up to the next multiple of 16, so a weight-gradient K step never reads
+  // another expert's rows in that operand.  lo_rows: row offset of the lo halves.
+  const int32_t* pad_indptr;  // [E+1] or NULL (no padding)
+  long long lo_rows;
+  int pad_a, pad_b;           // A / B rows are padded rows (RowsM: A only)
   const int32_t* row_slot;  // gathered operand: row_to_slot [R]; token of row r = row_slot[r] / topk
   int topk;
   int* err;
@@ -119,6 +126,8 @@ struct Tile {
   int rows;      // RowsM: valid rows in the tile; RowsK: rows of the expert (K extent)
   int nt;        // N tile
   int row0;      // RowsK: first global row of the expert
+  int am0;       // RowsM: first row of the tile in the padded row space (= m0 without padding)
+  int prow0;     // RowsK: first padded row of the expert (= row0 without padding)
   int kb_count;  // K blocks
 };
 
@@ -138,19 +147,26 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p) {
     }
     tl.e = lo;
     const int end = __ldg(p.m_indptr + lo + 1);
-    tl.m0 = __ldg(p.m_indptr + lo) + (mt - __ldg(p.tile_prefix + lo)) * BM;
+    const int start = __ldg(p.m_indptr + lo);
+    tl.m0 = start + (mt - __ldg(p.tile_prefix + lo)) * BM;
     tl.rows = min(BM, end - tl.m0);
     tl.row0 = 0;
+    tl.am0 = p.pad_indptr != nullptr ? __ldg(p.pad_indptr + lo) + (tl.m0 - start) : tl.m0;
+    tl.prow0 = 0;
     tl.kb_count = p.num_kb;
   } else {
+    // M blocks fastest: consecutive tiles (the CTAs of a cluster) share the expert and the N
+    // block, so they read the same B tile
     const int per_e = p.m_tiles * p.n_tiles;
     tl.e = t / per_e;
     const int r = t - tl.e * per_e;
-    const int mt = r / p.n_tiles;
-    tl.nt = r - mt * p.n_tiles;
+    tl.nt = r / p.m_tiles;
+    const int mt = r - tl.nt * p.m_tiles;
     tl.m0 = mt * BM;
     tl.row0 = __ldg(p.m_indptr + tl.e);
     tl.rows = __ldg(p.m_indptr + tl.e + 1) - tl.row0;
+    tl.am0 = tl.m0;
+    tl.prow0 = p.pad_indptr != nullptr ? __ldg(p.pad_indptr + tl.e) : tl.row0;
     tl.kb_count = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
   }
   return tl;
@@ -297,9 +313,14 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
     // (32-byte swizzle), six per 16 columns, double-buffered; the loads of the next 16
     // columns are issued before the current ones are processed.
     // This warp's columns: [n0 + c_lo, n0 + c_hi), half of the tile's N columns.
+    // Input rows are routed rows r; outputs go to padded rows ro (their expert's padded range).
+    // In an expert's last tile the lanes past its rows, up to the next multiple of 16, write
+    // zero rows (all inside the slice that holds the expert's last row, since 16 divides 32).
     const long long r = tl.m0 + row_local;
+    const long long ro = tl.am0 + row_local;
+    const bool pad_row = !row_ok && row_local < ((tl.rows + 15) & ~15);
     const long long two_i = 2LL * p.I;
-    const int y = tl.m0 + sub * 32;
+    const int y = tl.am0 + sub * 32;
     const int n0 = tl.nt * BN;
     const int ncols = min(BN, p.I - n0);  // a positive multiple of 64
     const int c_lo = colhalf * (BN / 2);
@@ -354,7 +375,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          const int yl = y + static_cast<int>(p.R);
+          const int yl = y + static_cast<int>(p.lo_rows);
           tma_store_2d(tmC0, base + 0 * kDhBoxBytes, n, y);
           tma_store_2d(tmC0, base + 1 * kDhBoxBytes, n, yl);
           tma_store_2d(tmC0, base + 2 * kDhBoxBytes, p.I + n, y);
@@ -363,10 +384,16 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
           tma_store_2d(tmC1, base + 5 * kDhBoxBytes, n, yl);
           bulk_commit_group();
         }
-      } else if (row_ok) {
-        uint16_t* dst[6] = {p.out2 + r * two_i + n, p.out2 + (p.R + r) * two_i + n, p.out2 + r * two_i + p.I + n,
-                            p.out2 + (p.R + r) * two_i + p.I + n, p.hw_out + r * p.I + n,
-                            p.hw_out + (p.R + r) * p.I + n};
+      } else if (row_ok || pad_row) {
+        if (pad_row) {
+#pragma unroll
+          for (int f = 0; f < 6; ++f)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) o[f][q] = 0u;
+        }
+        const long long rl = p.lo_rows + ro;
+        uint16_t* dst[6] = {p.out2 + ro * two_i + n, p.out2 + rl * two_i + n, p.out2 + ro * two_i + p.I + n,
+                            p.out2 + rl * two_i + p.I + n, p.hw_out + ro * p.I + n, p.hw_out + rl * p.I + n};
 #pragma unroll
         for (int f = 0; f < 6; ++f) {
           reinterpret_cast<uint4*>(dst[f])[0] = make_uint4(o[f][0], o[f][1], o[f][2], o[f][3]);
@@ -446,20 +473,6 @@ __device__ __forceinline__ void prefetch_epilogue_operands(int t, int total, int
   }
 }
 
-// Zeroes K rows [valid, end) of every 64-wide MN box of an MN-major stage
-// (A: 2 boxes per part, B: 4 boxes per part, each 64 rows of 128 B).  Whole
-// 128-byte rows are cleared, so the swizzle inside a row does not matter.
-template <int kBoxes>
-__device__ __forceinline__ void zero_tail_rows(uint8_t* stage_ptr, int valid, int end, int lane) {
-  const int nz = end - valid;
-  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-  const int per_box = nz * 8;  // uint4 per box
-  for (int box = 0; box < kBoxes; ++box) {
-    uint4* dst = reinterpret_cast<uint4*>(stage_ptr + box * MN_BOX_BYTES + valid * 128);
-    for (int i = lane; i < per_box; i += 32) dst[i] = z;
-  }
-}
-
 // Operand sources.  Gather::None: both operands through tiled TMA boxes.  Gather::A / B: that
 // operand's rows are token rows of a token-major [T, cols] bf16 matrix, fetched with TMA
 // gather4 through a tensor map whose box is one row high; RowsM gathers a K-major A (rows =
@@ -467,19 +480,32 @@ __device__ __forceinline__ void zero_tail_rows(uint8_t* stage_ptr, int valid, in
 enum class Gather : int { None = 0, A = 1, B = 2 };
 
 // Tiled loads of one stage for the operands that are not gathered (lane 0 of the producer).
-template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT, bool kLoadA, bool kLoadB>
+// In a cluster of CL > 1 CTAs one operand is shared: RowsM tiles of a cluster have the same
+// M block (A shared; each CTA loads BM / CL of its rows, tensor map box BM / CL rows high),
+// RowsK tiles the same expert and N block (B shared; each CTA loads every CL-th 64-column
+// box); the shared part is multicast to every CTA of the cluster, at the same offsets.
+template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT, bool kLoadA, bool kLoadB, int CL = 1>
 __device__ __forceinline__ void load_stage_tiled(const CUtensorMap* tmA, const CUtensorMap* tmB, const Params& p,
-                                                 const Tile& tl, int kb, uint32_t sa, uint32_t sb, uint32_t fb) {
+                                                 const Tile& tl, int kb, uint32_t sa, uint32_t sb, uint32_t fb,
+                                                 uint32_t rank = 0) {
+  constexpr uint16_t kMask = static_cast<uint16_t>((1u << CL) - 1u);
   if constexpr (kLoadA) {
-    if constexpr (!A_MN) {
-      tma_load_2d(sa, tmA, fb, kb * BK, tl.m0);
+    if constexpr (!A_MN) {  // RowsM: the tile's rows, in the padded row space when A is a padded operand
+      const int arow = p.pad_a ? tl.am0 : tl.m0;
+      if constexpr (S == Sched::RowsM && CL > 1) {
+        constexpr int kRows = BM / CL;
+        tma_load_2d_mc(sa + rank * kRows * 128, tmA, fb, kb * BK, arow + static_cast<int>(rank) * kRows, kMask);
+      } else {
+        tma_load_2d(sa, tmA, fb, kb * BK, arow);
+      }
     } else {
+      const int krow = (p.pad_a ? tl.prow0 : tl.row0) + kb * BK;
 #pragma unroll
       for (int part = 0; part < (SPLIT == 1 ? 2 : 1); ++part)
 #pragma unroll
         for (int i = 0; i < BM / 64; ++i)
           tma_load_2d(sa + part * A_BYTES + i * MN_BOX_BYTES, tmA, fb, tl.m0 + 64 * i,
-                      tl.row0 + kb * BK + part * p.a_split_rows);
+                      krow + part * p.a_split_rows);
     }
   }
   if constexpr (kLoadB) {
@@ -492,13 +518,20 @@ __device__ __forceinline__ void load_stage_tiled(const CUtensorMap* tmA, const C
         tma_load_2d(sb, tmB, fb, kb * BK, tl.e * p.b_rows_per_expert + tl.nt * BN);
       }
     } else {
-      const int krow = (S == Sched::RowsM) ? tl.e * p.b_rows_per_expert + kb * BK : tl.row0 + kb * BK;
+      const int krow = (S == Sched::RowsM) ? tl.e * p.b_rows_per_expert + kb * BK
+                                           : (p.pad_b ? tl.prow0 : tl.row0) + kb * BK;
 #pragma unroll
       for (int part = 0; part < (SPLIT == 2 ? 2 : 1); ++part)
 #pragma unroll
-        for (int i = 0; i < BN / 64; ++i)
-          tma_load_2d(sb + part * B_BYTES + i * MN_BOX_BYTES, tmB, fb, tl.nt * BN + 64 * i,
-                      krow + part * p.b_split_rows);
+        for (int i = 0; i < BN / 64; ++i) {
+          const uint32_t dst = sb + part * B_BYTES + i * MN_BOX_BYTES;
+          if constexpr (S == Sched::RowsK && CL > 1) {
+            if (i % CL == static_cast<int>(rank))
+              tma_load_2d_mc(dst, tmB, fb, tl.nt * BN + 64 * i, krow + part * p.b_split_rows, kMask);
+          } else {
+            tma_load_2d(dst, tmB, fb, tl.nt * BN + 64 * i, krow + part * p.b_split_rows);
+          }
+        }
     }
   }
 }
@@ -532,7 +565,11 @@ __device__ __forceinline__ void gather_tokens(const Tile& tl, int kb, int lane, 
   }
 }
 
-template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT, Gather G>
+// CL: CTAs per cluster (1, 2 or 4) sharing one operand by multicast (load_stage_tiled); the
+// tile count must be a multiple of CL, so that the CTAs of a cluster walk the same number of
+// tiles and K blocks in lockstep.  A stage is refilled only after every CTA of the cluster has
+// consumed it (each MMA warp's commit arrives on the empty barrier of all of them).
+template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT, Gather G, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
@@ -540,6 +577,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = LayoutOf<EP, SPLIT>;
   constexpr int STAGES = L::kStages;
   constexpr int STAGE_BYTES = L::kStageBytes;
+  constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CL) - 1u);
+  static_assert(CL == 1 || G == Gather::None, "clusters share tiled operands only");
+  static_assert(CL == 1 || (S == Sched::RowsM ? !A_MN : B_MN), "shared operand: K-major A (RowsM), MN-major B (RowsK)");
+  const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
   static_assert(SPLIT == 0 || (S == Sched::RowsK && A_MN && B_MN), "hi/lo operands only in the dW GEMMs");
   static_assert(G == Gather::None || (S == Sched::RowsM ? (G == Gather::A && !A_MN)
                                                          : (G == Gather::A ? (A_MN && SPLIT != 1)
@@ -564,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, CL);  // one release per CTA of the cluster
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -585,7 +626,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (CL > 1)
+    cluster_sync();  // every CTA's barriers exist before any multicast load or release reaches them
+  else
+    __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
@@ -613,7 +657,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sa = sbase + stage * STAGE_BYTES;
             const uint32_t fb = full0 + 8 * stage;
             mbar_arrive_expect_tx(fb, STAGE_BYTES);
-            load_stage_tiled<S, EP, A_MN, B_MN, SPLIT, true, true>(&tmA, &tmB, p, tl, kb, sa, sa + L::kABytes, fb);
+            load_stage_tiled<S, EP, A_MN, B_MN, SPLIT, true, true, CL>(&tmA, &tmB, p, tl, kb, sa, sa + L::kABytes, fb,
+                                                                      rank);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        if constexpr (CL > 1) {
+          // every CTA of the cluster has released the last fill of each stage: no release from a
+          // peer is still on its way to this CTA's barriers when it exits
+          for (int i = 0; i < STAGES && !failed; ++i) {
+            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
+              raise_abort(p.err, abort_flag);
+              failed = true;
+            }
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -718,19 +777,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sa = sbase + stage * STAGE_BYTES;
         const uint32_t sb = sa + L::kABytes;
         // K steps of 16 rows to issue: all of them, except in a weight-gradient tile's last
-        // block, which ends at the 16-row step holding the expert's last row; the rows of that
-        // step past the expert are zeroed first (they belong to the next expert).
+        // block, which ends at the 16-row step holding the expert's last row.  That step's rows
+        // past the expert are zero in the padded operand (dgu for dW_gate_up, w h for dW_down),
+        // so the other operand's rows there (the next expert's) add nothing.
         int ksteps = BK / 16;
         if constexpr (S == Sched::RowsK) {
           const int valid = tl.rows - kb * BK;
-          if (valid < BK) {
-            ksteps = (valid + 15) / 16;
-            if (valid < ksteps * 16) {
-              zero_tail_rows<STAGE_BYTES / MN_BOX_BYTES>(base_ptr + stage * STAGE_BYTES, valid, ksteps * 16, lane);
-              fence_proxy_async_smem();
-            }
-          }
-          __syncwarp();
+          if (valid < BK) ksteps = (valid + 15) / 16;
         }
         if (lane == 0) {
 #pragma unroll
@@ -746,7 +799,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (SPLIT == 2)  // the same A against the lo part of B
               umma_bf16_f32(d_tmem, ad, smem_desc_sw128(sb + B_BYTES + kk * 2048, MN_BOX_BYTES, 1024), idesc, 1u);
           }
-          umma_commit(empty0 + 8 * stage);
+          if constexpr (CL > 1)
+            umma_commit_mc(empty0 + 8 * stage, kClusterMask);
+          else
+            umma_commit(empty0 + 8 * stage);
         }
         __syncwarp();
         if (++stage == STAGES) {
@@ -810,24 +866,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ============================================================================
 // Tile schedule: tile_prefix[e] = sum_{e' < e} ceil(rows_e' / BM), tile_prefix[E]
-// = total.  m_indptr is validated (0 = m[0] <= ... <= m[E] = R); if it is not,
-// the schedule is empty and the device error flag is set.
+// = total; and, when pad_indptr != NULL, pad_indptr[e] = sum_{e' < e} of rows_e' rounded up
+// to 16 (the padded row space of the weight-gradient operands).  m_indptr is validated
+// (0 = m[0] <= ... <= m[E] = R); if it is not, the schedule is empty and the device error
+// flag is set.
 // ============================================================================
-__global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __restrict__ m_indptr, int E,
-                                                             long long R, int32_t* __restrict__ tile_prefix,
-                                                             int* err) {
-  __shared__ int s_warp[32];
-  __shared__ int s_bad;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) s_bad = (m_indptr[0] != 0 || static_cast<long long>(m_indptr[E]) != R) ? 1 : 0;
-  __syncthreads();
-  int tiles = 0;
-  if (tid < E) {
-    const int a = m_indptr[tid], b = m_indptr[tid + 1];
-    if (b < a) atomicOr(&s_bad, 1);
-    tiles = (b > a) ? (b - a + BM - 1) / BM : 0;
-  }
-  int incl = tiles;
+__device__ __forceinline__ int block_exclusive_scan_1024(int v, int* s_warp, int lane, int warp, int* total) {
+  int incl = v;
 #pragma unroll
   for (int m = 1; m < 32; m <<= 1) {
     const int o = __shfl_up_sync(0xFFFFFFFFu, incl, m);
@@ -844,11 +889,41 @@ __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __re
       if (lane >= m) xi += o;
     }
     s_warp[lane] = xi - x;
+    if (lane == 31) *total = xi;
   }
   __syncthreads();
+  const int excl = s_warp[warp] + incl - v;
+  __syncthreads();  // s_warp is reused by the next scan
+  return excl;
+}
+
+__global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __restrict__ m_indptr, int E,
+                                                             long long R, int32_t* __restrict__ tile_prefix,
+                                                             int32_t* __restrict__ pad_indptr, int* err) {
+  __shared__ int s_warp[32];
+  __shared__ int s_bad;
+  __shared__ int s_total[2];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_bad = (m_indptr[0] != 0 || static_cast<long long>(m_indptr[E]) != R) ? 1 : 0;
+  __syncthreads();
+  int tiles = 0, padded = 0;
+  if (tid < E) {
+    const int a = m_indptr[tid], b = m_indptr[tid + 1];
+    if (b < a) atomicOr(&s_bad, 1);
+    tiles = (b > a) ? (b - a + BM - 1) / BM : 0;
+    padded = (b > a) ? ((b - a + 15) & ~15) : 0;
+  }
+  const int t_excl = block_exclusive_scan_1024(tiles, s_warp, lane, warp, &s_total[0]);
+  const int p_excl = pad_indptr != nullptr ? block_exclusive_scan_1024(padded, s_warp, lane, warp, &s_total[1]) : 0;
   const bool bad = s_bad != 0;
-  if (tid < E) tile_prefix[tid] = bad ? 0 : s_warp[warp] + incl - tiles;
-  if (tid == E - 1) tile_prefix[E] = bad ? 0 : s_warp[warp] + incl;
+  if (tid < E) {
+    tile_prefix[tid] = bad ? 0 : t_excl;
+    if (pad_indptr != nullptr) pad_indptr[tid] = bad ? 0 : p_excl;
+  }
+  if (tid == 0) {
+    tile_prefix[E] = bad ? 0 : s_total[0];
+    if (pad_indptr != nullptr) pad_indptr[E] = bad ? 0 : s_total[1];
+  }
   if (bad && tid == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_INDPTR);
 }
 
@@ -924,23 +999,66 @@ int make_out_bf16_3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t ro
   return make_tmap_nd(m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3, dims, box);
 }
 
-template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT = 0, Gather G = Gather::None>
+// Launches one grouped GEMM.  `tiles` is the number of tiles the persistent grid walks (for
+// RowsM an upper bound: the device schedule decides); the grid is at most one CTA per SM.
+// With CL > 1 the grid is made of clusters of CL CTAs (tiles must be a multiple of CL), as
+// many as can be resident at once.
+template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT = 0, Gather G = Gather::None, int CL = 1>
 int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc0, const CUtensorMap& tc1,
-                const Params& p, int grid, cudaStream_t s, const char* name) {
-  auto kern = grouped_gemm_kernel<S, EP, A_MN, B_MN, SPLIT, G>;
+                const Params& p, long long tiles, const DeviceInfo& dev, cudaStream_t s, const char* name) {
+  auto kern = grouped_gemm_kernel<S, EP, A_MN, B_MN, SPLIT, G, CL>;
+  constexpr int kSmem = LayoutOf<EP, SPLIT>::kSmemBytes;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;
   std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LayoutOf<EP, SPLIT>::kSmemBytes);
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (attr_err == cudaSuccess && CL > 1) {
+      cudaLaunchConfig_t cfg{};
+      cudaLaunchAttribute attr{};
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = CL;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.gridDim = dim3(static_cast<unsigned>(dev.sm_count / CL * CL));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = kSmem;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+      if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
+    }
   });
   if (attr_err != cudaSuccess) {
     set_cuda_error(attr_err, name);
     return LIGER_MOE_ERR_LAUNCH;
   }
-  if (grid < 1) return LIGER_MOE_OK;
-  {
+  if (tiles < 1) return LIGER_MOE_OK;
+  if constexpr (CL == 1) {
+    const int grid = static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
     KernelScope trace(name, s);
-    kern<<<grid, kThreads, LayoutOf<EP, SPLIT>::kSmemBytes, s>>>(ta, tb, tc0, tc1, p);
+    kern<<<grid, kThreads, kSmem, s>>>(ta, tb, tc0, tc1, p);
+  } else {
+    const long long groups = tiles / CL;
+    const int clusters = static_cast<int>(groups < max_clusters ? groups : max_clusters);
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = CL;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = s;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    KernelScope trace(name, s);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc0, tc1, p);
+    if (e != cudaSuccess) {
+      set_cuda_error(e, name);
+      return LIGER_MOE_ERR_LAUNCH;
+    }
   }
   return check_launch(name);
 }
@@ -966,14 +1084,8 @@ void set_gather(Params& p, const int32_t* row_to_slot, long long R, int k) {
   p.topk = k;
 }
 
-int rows_m_grid(long long R, int E, int n_tiles, const DeviceInfo& dev) {
-  const long long max_tiles = ((R + BM - 1) / BM + E) * n_tiles;
-  return static_cast<int>(max_tiles < dev.sm_count ? max_tiles : dev.sm_count);
-}
-
-int rows_k_grid(long long tiles, const DeviceInfo& dev) {
-  return static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
-}
+// Upper bound on the RowsM tile count: sum over experts of ceil(rows_e / BM) N tiles.
+long long rows_m_tiles(long long R, int E, int n_tiles) { return ((R + BM - 1) / BM + E) * n_tiles; }
 
 int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -981,11 +1093,11 @@ int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
 size_t schedule_bytes(int E) { return align_up(sizeof(int32_t) * (E + 1), 256); }
 
-int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, int32_t* tile_prefix, const DeviceInfo& dev,
-                         cudaStream_t s) {
+int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, int32_t* tile_prefix, int32_t* pad_indptr,
+                         const DeviceInfo& dev, cudaStream_t s) {
   {
     KernelScope trace("tile_schedule", s);
-    tile_schedule_kernel<<<1, 1024, 0, s>>>(m_indptr, E, R, tile_prefix, dev.err_flag);
+    tile_schedule_kernel<<<1, 1024, 0, s>>>(m_indptr, E, R, tile_prefix, pad_indptr, dev.err_flag);
   }
   return check_launch("tile_schedule");
 }
@@ -1016,11 +1128,12 @@ int launch_gate_up(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) 
   if (a.h_perm == nullptr) tc0 = tc1;
   if (a.gu_perm == nullptr) tc1 = tc0;
   if (a.h_perm == nullptr && a.gu_perm == nullptr) return LIGER_MOE_OK;
-  const int grid = rows_m_grid(a.R, a.E, p.n_tiles, dev);
+  const long long tiles = rows_m_tiles(a.R, a.E, p.n_tiles);
   if (gather)
-    return launch_gemm<Sched::RowsM, Epi::SwiGLU, false, false, 0, Gather::A>(ta, tb, tc0, tc1, p, grid, s,
+    return launch_gemm<Sched::RowsM, Epi::SwiGLU, false, false, 0, Gather::A>(ta, tb, tc0, tc1, p, tiles, dev, s,
                                                                               "gemm_gate_up_swiglu");
-  return launch_gemm<Sched::RowsM, Epi::SwiGLU, false, false>(ta, tb, tc0, tc1, p, grid, s, "gemm_gate_up_swiglu");
+  return launch_gemm<Sched::RowsM, Epi::SwiGLU, false, false>(ta, tb, tc0, tc1, p, tiles, dev, s,
+                                                               "gemm_gate_up_swiglu");
 }
 
 int launch_down(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
@@ -1040,7 +1153,7 @@ int launch_down(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   CUtensorMap tc0;
   if (make_out_bf16(&tc0, a.y_perm, a.H, a.R)) return LIGER_MOE_ERR_LAUNCH;
   return launch_gemm<Sched::RowsM, Epi::ScaleRows, false, false>(ta, tb, tc0, tc0, p,
-                                                                  rows_m_grid(a.R, a.E, p.n_tiles, dev), s,
+                                                                  rows_m_tiles(a.R, a.E, p.n_tiles), dev, s,
                                                                   "gemm_down_scale");
 }
 
@@ -1055,7 +1168,9 @@ int launch_bwd_dh(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
     return LIGER_MOE_ERR_LAUNCH;
   Params p = base_params(a.m_indptr, a.tile_prefix, a.E, dev.err_flag);
   if (gather) set_gather(p, a.row_to_slot, a.R, a.k);
-  p.R = a.R;  // row offset of the lo halves of dgu and hw
+  p.R = a.R;
+  p.pad_indptr = a.pad_indptr;  // dgu and hw rows go to the padded row space
+  p.lo_rows = a.R_pad;          // row offset of their lo halves
   p.n_tiles = cdiv(a.I, BN);
   p.num_kb = a.H / BK;
   p.b_rows_per_expert = a.H;
@@ -1068,22 +1183,25 @@ int launch_bwd_dh(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.row_scale = a.w_perm;
   p.gdot = a.gdot;
   CUtensorMap tc0, tc1;  // dgu [2R, 2I] and hw [2R, I]: hi rows then lo rows
-  if (make_out_bf16_narrow(&tc0, a.dgu, 2ULL * a.I, 2ULL * a.R) || make_out_bf16_narrow(&tc1, a.hw_perm, a.I, 2ULL * a.R))
+  if (make_out_bf16_narrow(&tc0, a.dgu, 2ULL * a.I, 2ULL * a.R_pad) ||
+      make_out_bf16_narrow(&tc1, a.hw_perm, a.I, 2ULL * a.R_pad))
     return LIGER_MOE_ERR_LAUNCH;
-  const int grid = rows_m_grid(a.R, a.E, p.n_tiles, dev);
+  const long long tiles = rows_m_tiles(a.R, a.E, p.n_tiles);
   if (gather)
-    return launch_gemm<Sched::RowsM, Epi::DH, false, true, 0, Gather::A>(ta, tb, tc0, tc1, p, grid, s,
+    return launch_gemm<Sched::RowsM, Epi::DH, false, true, 0, Gather::A>(ta, tb, tc0, tc1, p, tiles, dev, s,
                                                                         "gemm_bwd_dh");
-  return launch_gemm<Sched::RowsM, Epi::DH, false, true>(ta, tb, tc0, tc1, p, grid, s, "gemm_bwd_dh");
+  return launch_gemm<Sched::RowsM, Epi::DH, false, true>(ta, tb, tc0, tc1, p, tiles, dev, s, "gemm_bwd_dh");
 }
 
 int launch_bwd_dx(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   if (a.R == 0) return LIGER_MOE_OK;
   CUtensorMap ta, tb;
-  if (make_tmap(&ta, a.dgu, 2ULL * a.I, a.R, BK, BM) ||
+  if (make_tmap(&ta, a.dgu, 2ULL * a.I, a.R_pad, BK, BM) ||  // hi rows of dgu, padded row space
       make_tmap(&tb, a.w_gate_up, a.H, 2ULL * a.I * a.E, 64, BK))
     return LIGER_MOE_ERR_LAUNCH;
   Params p = base_params(a.m_indptr, a.tile_prefix, a.E, dev.err_flag);
+  p.pad_indptr = a.pad_indptr;
+  p.pad_a = 1;  // A = dgu hi rows in the padded row space
   p.n_tiles = cdiv(a.H, BN);
   p.num_kb = 2 * a.I / BK;
   p.b_rows_per_expert = 2 * a.I;
@@ -1093,8 +1211,8 @@ int launch_bwd_dx(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.ld_out = a.H;
   CUtensorMap tc0;
   if (make_out_bf16(&tc0, a.dx_perm, a.H, a.R)) return LIGER_MOE_ERR_LAUNCH;
-  return launch_gemm<Sched::RowsM, Epi::Store, false, true>(ta, tb, tc0, tc0, p,
-                                                             rows_m_grid(a.R, a.E, p.n_tiles, dev), s, "gemm_bwd_dx");
+  return launch_gemm<Sched::RowsM, Epi::Store, false, true>(ta, tb, tc0, tc0, p, rows_m_tiles(a.R, a.E, p.n_tiles),
+                                                             dev, s, "gemm_bwd_dx");
 }
 
 int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
@@ -1110,7 +1228,9 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   const bool gather_x = a.x != nullptr || empty;
   // dW_gu[e] = dgu_hi_e^T x_e + dgu_lo_e^T x_e: each stage holds both parts of A (rows r and
   // R + r of dgu [2R, 2I]) and one B tile; two MMAs per K step.
-  if (make_tmap(&ta, empty ? a.dw_gate_up : a.dgu, 2ULL * a.I, 2 * rows, 64, BK)) return LIGER_MOE_ERR_LAUNCH;
+  const uint64_t prows = empty ? 1 : static_cast<uint64_t>(a.R_pad);
+  p.pad_indptr = a.pad_indptr;
+  if (make_tmap(&ta, empty ? a.dw_gate_up : a.dgu, 2ULL * a.I, 2 * prows, 64, BK)) return LIGER_MOE_ERR_LAUNCH;
   if (gather_x) {
     set_gather(p, a.row_to_slot, a.R, a.k);
     if (empty ? make_gather_map(&tb, a.dw_gate_up, a.H, 1) : make_gather_map(&tb, a.x, a.H, a.T))
@@ -1120,25 +1240,33 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   }
   p.m_tiles = cdiv(2LL * a.I, BM);
   p.n_tiles = cdiv(a.H, BN);
-  p.a_split_rows = static_cast<int>(a.R);
+  p.a_split_rows = static_cast<int>(a.R_pad);
   p.b_split_rows = 0;
+  p.pad_a = 1;  // dgu rows: padded row space (zero rows past each expert)
+  p.pad_b = 0;
   p.M_out = 2 * a.I;
   p.N_out = a.H;
   p.out = a.dw_gate_up;
   p.ld_out = a.H;
   p.out_expert_stride = 2LL * a.I * a.H;
   if (make_out_bf16_3d(&tc0, a.dw_gate_up, a.H, 2ULL * a.I, a.E)) return LIGER_MOE_ERR_LAUNCH;
-  const int grid_gu = rows_k_grid(static_cast<long long>(a.E) * p.m_tiles * p.n_tiles, dev);
-  int rc = gather_x
-               ? launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::B>(ta, tb, tc0, tc0, p, grid_gu, s,
-                                                                                 "gemm_bwd_dw_gate_up")
-               : launch_gemm<Sched::RowsK, Epi::Store, true, true, 1>(ta, tb, tc0, tc0, p, grid_gu, s,
-                                                                      "gemm_bwd_dw_gate_up");
+  // CTA pairs over neighbouring M blocks share the x tile (multicast) when the M blocks pair up
+  const long long tiles_gu = static_cast<long long>(a.E) * p.m_tiles * p.n_tiles;
+  int rc;
+  if (gather_x)
+    rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::B>(ta, tb, tc0, tc0, p, tiles_gu, dev, s,
+                                                                         "gemm_bwd_dw_gate_up");
+  else if (p.m_tiles % 2 == 0)
+    rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::None, 2>(ta, tb, tc0, tc0, p, tiles_gu, dev, s,
+                                                                               "gemm_bwd_dw_gate_up");
+  else
+    rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1>(ta, tb, tc0, tc0, p, tiles_gu, dev, s,
+                                                              "gemm_bwd_dw_gate_up");
   if (rc) return rc;
   // dW_d[e] = dY_e^T hw_hi_e + dY_e^T hw_lo_e: each stage holds one A tile (dY rows gathered by
   // token) and both parts of B (rows r and R + r of hw [2R, I]); two MMAs per K step.
   const bool gather_dy = a.dy_perm == nullptr || empty;
-  if (make_tmap(&tb, empty ? a.dw_down : a.hw_perm, a.I, 2 * rows, 64, BK)) return LIGER_MOE_ERR_LAUNCH;
+  if (make_tmap(&tb, empty ? a.dw_down : a.hw_perm, a.I, 2 * prows, 64, BK)) return LIGER_MOE_ERR_LAUNCH;
   if (gather_dy) {
     set_gather(p, a.row_to_slot, a.R, a.k);
     if (empty ? make_gather_map(&ta, a.dw_down, a.H, 1) : make_gather_map(&ta, a.dy, a.H, a.T))
@@ -1149,18 +1277,24 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.m_tiles = cdiv(a.H, BM);
   p.n_tiles = cdiv(a.I, BN);
   p.a_split_rows = 0;
-  p.b_split_rows = static_cast<int>(a.R);
+  p.b_split_rows = static_cast<int>(a.R_pad);
+  p.pad_a = 0;
+  p.pad_b = 1;  // w h rows: padded row space
   p.M_out = a.H;
   p.N_out = a.I;
   p.out = a.dw_down;
   p.ld_out = a.I;
   p.out_expert_stride = 1LL * a.H * a.I;
   if (make_out_bf16_3d(&tc0, a.dw_down, a.I, a.H, a.E)) return LIGER_MOE_ERR_LAUNCH;
-  const int grid_d = rows_k_grid(static_cast<long long>(a.E) * p.m_tiles * p.n_tiles, dev);
+  // CTA pairs over neighbouring M blocks share the two parts of the w h tile (multicast)
+  const long long tiles_d = static_cast<long long>(a.E) * p.m_tiles * p.n_tiles;
   if (gather_dy)
-    return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::A>(ta, tb, tc0, tc0, p, grid_d, s,
+    return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::A>(ta, tb, tc0, tc0, p, tiles_d, dev, s,
                                                                            "gemm_bwd_dw_down");
-  return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2>(ta, tb, tc0, tc0, p, grid_d, s, "gemm_bwd_dw_down");
+  if (p.m_tiles % 2 == 0)
+    return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::None, 2>(ta, tb, tc0, tc0, p, tiles_d, dev, s,
+                                                                                 "gemm_bwd_dw_down");
+  return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2>(ta, tb, tc0, tc0, p, tiles_d, dev, s, "gemm_bwd_dw_down");
 }
 
 }  // namespace lmoe

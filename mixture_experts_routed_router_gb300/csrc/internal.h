@@ -52,8 +52,9 @@ int launch_router_grad(const float* gdot, int gdot_tiles, const int32_t* ids, co
 // ---- grouped GEMMs (grouped_gemm.cu)
 // Tile schedule: tile_prefix[e] = sum over e' < e of ceil(rows_e' / 128); [E] = total.
 size_t schedule_bytes(int E);
-int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, int32_t* tile_prefix, const DeviceInfo& dev,
-                         cudaStream_t s);
+// With pad_indptr != NULL it also receives the padded row prefix (row counts rounded up to 16).
+int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, int32_t* tile_prefix, int32_t* pad_indptr,
+                         const DeviceInfo& dev, cudaStream_t s);
 
 struct FwdGemmArgs {
   const uint16_t* x_perm;       // [R, H]; used when x is NULL
@@ -90,8 +91,13 @@ struct BwdGemmArgs {
   const uint16_t* h_perm;
   const float* gu;       // [R, 2I] fp32 [dh/dg | dh/du] (saved or recomputed)
   const float* w_perm;   // [R]
-  uint16_t* hw_perm;     // [2R, I]: rows [0,R) bf16(w h), rows [R,2R) bf16(w h - hi)
-  uint16_t* dgu;         // [2R, 2I]: rows [0,R) bf16(dgu), rows [R,2R) bf16(dgu - hi)
+  // Weight-gradient operands in the padded row space: expert e's rows start at pad_indptr[e]
+  // and are followed by zero rows up to a multiple of 16; R_pad (>= pad_indptr[E]) is the
+  // row count of each half.
+  const int32_t* pad_indptr;  // [E+1]
+  long long R_pad;
+  uint16_t* hw_perm;     // [2 R_pad, I]: hi rows bf16(w h), then lo rows bf16(w h - hi)
+  uint16_t* dgu;         // [2 R_pad, 2I]: hi rows bf16(dgu), then lo rows bf16(dgu - hi)
   uint16_t* dx_perm;     // [R, H]
   float* gdot;           // [R, ceil(I / 256)]
   uint16_t* dw_gate_up;  // [E, 2I, H]
