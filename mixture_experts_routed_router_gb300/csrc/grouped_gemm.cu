@@ -454,8 +454,10 @@ __device__ __forceinline__ void store_zero_tile(const Tile& tl, int sub, int col
   }
 }
 
-// DH epilogue operands of one tile row (fp32 g and u, bf16 h) are pulled into L2 ahead of
-// time, one tile early, so the epilogue's loads do not wait on DRAM.
+// DH epilogue operands of one tile row (the fp32 derivative factors and bf16 h) are pulled into
+// L2 when the epilogue warp reaches the tile (before waiting for its accumulator).  One tile
+// earlier proved too early: in the epilogue-bound dH kernel a tile takes tens of microseconds,
+// and the prefetched lines were evicted before use.
 template <Sched S, Epi EP>
 __device__ __forceinline__ void prefetch_epilogue_operands(int t, int total, int row_local, int colhalf,
                                                            const Params& p) {
@@ -832,10 +834,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     Stager st{sbase + L::kStgOffset + static_cast<uint32_t>(ew * L::kStgWarpBytes), 0};
     int acc = 0;
     uint32_t acc_phase = 0;
-    prefetch_epilogue_operands<S, EP>(blockIdx.x, total, row_local, colhalf, p);
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode_tile<S>(t, p);
-      prefetch_epilogue_operands<S, EP>(t + gridDim.x, total, row_local, colhalf, p);
+      // the tile's epilogue operands (DH) start moving into L2 now, a tile's MMA time ahead of use
+      // when the MMAs lead, and at least ahead of the later column chunks when the epilogue does
+      prefetch_epilogue_operands<S, EP>(t, total, row_local, colhalf, p);
       if (tl.kb_count == 0) {
         if constexpr (S == Sched::RowsK) store_zero_tile(tl, sub, colhalf, lane, p, &tmC0, st);
         continue;
