@@ -50,11 +50,12 @@ def open_library(path: str):
     P, I = ctypes.c_void_p, ctypes.c_int
     lib.oracle_route_topk.argtypes = [P, I, I, I, P, P]
     lib.oracle_dispatch.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P]
-    lib.oracle_grouped_swiglu_rows.argtypes = [P, P, P, P, P, I, I, I, I, P, I, P, P, P, I]
+    F = ctypes.c_float
+    lib.oracle_grouped_swiglu_rows.argtypes = [P, P, P, P, P, I, I, I, I, P, I, P, P, P, I, F, I]
     lib.oracle_combine.argtypes = [P, P, I, I, I, P, I, P]
-    lib.oracle_forward_tokens.argtypes = [P, P, P, P, P, I, I, I, I, I, P, I, P, I]
-    lib.oracle_backward_tokens.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, I, P, P, I]
-    lib.oracle_backward_dw.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, I, P, P, I]
+    lib.oracle_forward_tokens.argtypes = [P, P, P, P, P, I, I, I, I, I, P, I, P, I, F, I]
+    lib.oracle_backward_tokens.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, I, P, P, I, F, I]
+    lib.oracle_backward_dw.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, I, P, P, I, F, I]
     for f in (lib.oracle_route_topk, lib.oracle_dispatch, lib.oracle_grouped_swiglu_rows,
               lib.oracle_combine, lib.oracle_forward_tokens, lib.oracle_backward_tokens,
               lib.oracle_backward_dw):
@@ -90,6 +91,17 @@ class using:
     def __exit__(self, *exc):
         _override.lib = self.prev
         return False
+
+
+# Gated activations of the expert MLP (moe_oracle.cpp, act_forward); `clamp` is the bound of
+# the bounded SwiGLU and the limit of SwiGLU-OAI, unused otherwise.
+ACTIVATIONS = {"swiglu": 0, "swiglu_bounded": 1, "swiglu_oai": 2, "geglu": 3, "reglu": 4}
+
+
+def _act(act: str) -> int:
+    if act not in ACTIVATIONS:
+        raise ValueError(f"unknown activation {act!r}")
+    return ACTIVATIONS[act]
 
 
 def default_threads() -> int:
@@ -139,8 +151,8 @@ def dispatch(ids: np.ndarray, w: np.ndarray | None, x: np.ndarray | None, E: int
     return out
 
 
-def grouped_swiglu_rows(x_perm, m_indptr, wgu, wd, w_perm, rows, threads=None):
-    """Expert MLP on chosen expert-major rows: (h bf16 [n,I], gu f32 [n,2I], y bf16 [n,H])."""
+def grouped_swiglu_rows(x_perm, m_indptr, wgu, wd, w_perm, rows, threads=None, act="swiglu", clamp=0.0):
+    """Expert MLP on chosen expert-major rows: (h bf16 [n,I], gu f32 [n,2I] = [g | u], y bf16 [n,H])."""
     x_perm = _c(x_perm, np.uint16)
     wgu = _c(wgu, np.uint16)
     wd = _c(wd, np.uint16)
@@ -156,8 +168,8 @@ def grouped_swiglu_rows(x_perm, m_indptr, wgu, wd, w_perm, rows, threads=None):
     y = np.empty((n, H), np.uint16)
     rc = _load().oracle_grouped_swiglu_rows(x_perm.ctypes.data, m_indptr.ctypes.data, wgu.ctypes.data,
                                             wd.ctypes.data, w_perm.ctypes.data, R, H, I, E, rows.ctypes.data,
-                                            n, h.ctypes.data, gu.ctypes.data, y.ctypes.data,
-                                            threads or default_threads())
+                                            n, h.ctypes.data, gu.ctypes.data, y.ctypes.data, _act(act),
+                                            float(clamp), threads or default_threads())
     _check(rc, "grouped_swiglu_rows")
     return h, gu, y
 
@@ -173,7 +185,7 @@ def combine(y_perm, slot_to_row, T, k, toks=None):
     return out
 
 
-def forward_tokens(x, wgu, wd, ids, w, toks=None, threads=None):
+def forward_tokens(x, wgu, wd, ids, w, toks=None, threads=None, act="swiglu", clamp=0.0):
     """Whole-layer output Y (bf16 [n,H]) for the listed tokens."""
     x, wgu, wd = _c(x, np.uint16), _c(wgu, np.uint16), _c(wd, np.uint16)
     ids, w = _c(ids, np.int32), _c(w, np.float32)
@@ -184,12 +196,12 @@ def forward_tokens(x, wgu, wd, ids, w, toks=None, threads=None):
     out = np.empty((toks.size, H), np.uint16)
     rc = _load().oracle_forward_tokens(x.ctypes.data, wgu.ctypes.data, wd.ctypes.data, ids.ctypes.data,
                                        w.ctypes.data, T, H, twoI // 2, E, k, toks.ctypes.data, toks.size,
-                                       out.ctypes.data, threads or default_threads())
+                                       out.ctypes.data, _act(act), float(clamp), threads or default_threads())
     _check(rc, "forward_tokens")
     return out
 
 
-def backward_tokens(x, dy, wgu, wd, ids, w, toks=None, threads=None):
+def backward_tokens(x, dy, wgu, wd, ids, w, toks=None, threads=None, act="swiglu", clamp=0.0):
     """(dX bf16 [n,H], d_logits float32 [n,E]) for the listed tokens."""
     x, dy = _c(x, np.uint16), _c(dy, np.uint16)
     wgu, wd = _c(wgu, np.uint16), _c(wd, np.uint16)
@@ -203,12 +215,12 @@ def backward_tokens(x, dy, wgu, wd, ids, w, toks=None, threads=None):
     rc = _load().oracle_backward_tokens(x.ctypes.data, dy.ctypes.data, wgu.ctypes.data, wd.ctypes.data,
                                         ids.ctypes.data, w.ctypes.data, T, H, twoI // 2, E, k,
                                         toks.ctypes.data, toks.size, dx.ctypes.data, dl.ctypes.data,
-                                        threads or default_threads())
+                                        _act(act), float(clamp), threads or default_threads())
     _check(rc, "backward_tokens")
     return dx, dl
 
 
-def backward_dw(x, dy, wgu, wd, ids, w, experts=None, threads=None):
+def backward_dw(x, dy, wgu, wd, ids, w, experts=None, threads=None, act="swiglu", clamp=0.0):
     """(dW_gu bf16 [n,2I,H], dW_d bf16 [n,H,I]) for the listed experts."""
     x, dy = _c(x, np.uint16), _c(dy, np.uint16)
     wgu, wd = _c(wgu, np.uint16), _c(wd, np.uint16)
@@ -222,7 +234,7 @@ def backward_dw(x, dy, wgu, wd, ids, w, experts=None, threads=None):
     dwd = np.empty((experts.size, H, I), np.uint16)
     rc = _load().oracle_backward_dw(x.ctypes.data, dy.ctypes.data, wgu.ctypes.data, wd.ctypes.data,
                                     ids.ctypes.data, w.ctypes.data, T, H, I, E, k, experts.ctypes.data,
-                                    experts.size, dwgu.ctypes.data, dwd.ctypes.data,
+                                    experts.size, dwgu.ctypes.data, dwd.ctypes.data, _act(act), float(clamp),
                                     threads or default_threads())
     _check(rc, "backward_dw")
     return dwgu, dwd

@@ -23,6 +23,10 @@
 //     computation on identically bf16-rounded inputs.
 //   * Liger Kernel README, "High-level APIs" (LigerSwiGLUMLP): the SwiGLU MLP
 //     down(silu(gate(x)) * up(x)).
+//   * LightMoE README, "Compatibility" and "Highlights": the gated
+//     activations bounded SwiGLU (with an activation clamp), SwiGLU-OAI and
+//     GeGLU, plus ReGLU; the pages name them without formulas, so each is
+//     written out below in its plainest published form (see act_forward).
 // Readings where the pages are silent (tie order, gate/up row order,
 // rounding points, softmax over the selected k) are spelled out at each
 // function.  Arithmetic is float (fp32) with bf16 inputs widened exactly;
@@ -64,6 +68,75 @@ inline float round_to_bf16(float f) { return bf16_to_float(float_to_bf16(f)); }
 // silu(a) = a / (1 + exp(-a))   (SwiGLU's gate activation)
 inline float silu(float a) { return a / (1.0f + std::exp(-a)); }
 
+// Gated activations h = act(g, u) of the expert MLP, and their partial derivatives.
+//   0 SwiGLU          h = silu(g) u
+//   1 bounded SwiGLU  h = silu(gc) uc,         gc = min(g, c), uc = clamp(u, -c, c)
+//   2 SwiGLU-OAI      h = gc sigmoid(a gc) (uc + 1),  a = 1.702, same clamps with c the limit
+//   3 GeGLU           h = gelu(g) u,  gelu(g) = g/2 (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3)))
+//   4 ReGLU           h = max(g, 0) u
+// A clamp passes the gradient where its input lies inside the closed interval and blocks it
+// outside.  SwiGLU keeps its own operation order (silu, then the product) everywhere below.
+constexpr int kActSwiGLU = 0, kActBounded = 1, kActOAI = 2, kActGeGLU = 3, kActReGLU = 4;
+constexpr float kOaiAlpha = 1.702f;
+constexpr float kGeluK0 = 0.7978845608028654f;  // sqrt(2 / pi)
+constexpr float kGeluK1 = 0.044715f;
+
+inline float sigmoid(float a) { return 1.0f / (1.0f + std::exp(-a)); }
+
+inline float act_forward(int act, float c, float g, float u) {
+  switch (act) {
+    case kActBounded: {
+      const float gc = std::min(g, c), uc = std::min(std::max(u, -c), c);
+      return silu(gc) * uc;
+    }
+    case kActOAI: {
+      const float gc = std::min(g, c), uc = std::min(std::max(u, -c), c);
+      return (gc * sigmoid(kOaiAlpha * gc)) * (uc + 1.0f);
+    }
+    case kActGeGLU: {
+      const float t = std::tanh(kGeluK0 * (g + kGeluK1 * g * g * g));
+      return (0.5f * g * (1.0f + t)) * u;
+    }
+    case kActReGLU:
+      return std::max(g, 0.0f) * u;
+    default:
+      return silu(g) * u;
+  }
+}
+
+// dh/dg and dh/du of act_forward (every activation other than SwiGLU).
+inline void act_partials(int act, float c, float g, float u, float* dhdg, float* dhdu) {
+  switch (act) {
+    case kActBounded: {
+      const float gc = std::min(g, c), uc = std::min(std::max(u, -c), c);
+      const float s = sigmoid(gc);
+      *dhdg = (g <= c) ? uc * s * (1.0f + gc * (1.0f - s)) : 0.0f;
+      *dhdu = (u >= -c && u <= c) ? gc * s : 0.0f;
+      return;
+    }
+    case kActOAI: {
+      const float gc = std::min(g, c), uc = std::min(std::max(u, -c), c);
+      const float s = sigmoid(kOaiAlpha * gc);
+      *dhdg = (g <= c) ? (uc + 1.0f) * s * (1.0f + kOaiAlpha * gc * (1.0f - s)) : 0.0f;
+      *dhdu = (u >= -c && u <= c) ? gc * s : 0.0f;
+      return;
+    }
+    case kActGeGLU: {
+      const float t = std::tanh(kGeluK0 * (g + kGeluK1 * g * g * g));
+      const float dgelu = 0.5f * (1.0f + t) + 0.5f * g * (1.0f - t * t) * kGeluK0 * (1.0f + 3.0f * kGeluK1 * g * g);
+      *dhdg = u * dgelu;
+      *dhdu = 0.5f * g * (1.0f + t);
+      return;
+    }
+    case kActReGLU:
+      *dhdg = (g > 0.0f) ? u : 0.0f;
+      *dhdu = std::max(g, 0.0f);
+      return;
+    default:
+      return;
+  }
+}
+
 // Runs f(i) for i in [0, n) on up to `threads` threads, each owning a
 // contiguous block of i.  Each i is computed wholly by one thread, so the
 // result does not depend on the thread count.
@@ -100,10 +173,11 @@ inline bool ranks_before(float a, int ia, float b, int ib) {
 // One expert applied to one token row (SwiGLU MLP).
 //   g[n] = sum_h x[h] * Wgu[n, h]          n < I   (rows [0, I) are the gate)
 //   u[n] = sum_h x[h] * Wgu[I + n, h]              (rows [I, 2I) are the up)
-//   hq[n] = bf16( silu(g[n]) * u[n] )               (rounded: h is stored bf16)
+//   hq[n] = bf16( act(g[n], u[n]) )                 (rounded: h is stored bf16; SwiGLU:
+//                                                   silu(g[n]) * u[n])
 // Sums in float, h ascending.
 void gate_up_row(const uint16_t* xrow, const uint16_t* wgu_e, int H, int I, float* g, float* u,
-                 float* hq) {
+                 float* hq, int act = kActSwiGLU, float clamp = 0.0f) {
   for (int n = 0; n < I; ++n) {
     const uint16_t* wg = wgu_e + static_cast<size_t>(n) * H;
     const uint16_t* wu = wgu_e + static_cast<size_t>(I + n) * H;
@@ -115,7 +189,7 @@ void gate_up_row(const uint16_t* xrow, const uint16_t* wgu_e, int H, int I, floa
     }
     g[n] = ag;
     u[n] = au;
-    hq[n] = round_to_bf16(silu(ag) * au);
+    hq[n] = round_to_bf16(act_forward(act, clamp, ag, au));
   }
 }
 
@@ -136,11 +210,12 @@ void down_row(const float* hq, const uint16_t* wd_e, int H, int I, float* o) {
 //   s      = 1 / (1 + exp(-g[n]))
 //   dg[n]  = ((dh[n] * u[n]) * s) * (1 + g[n] * (1 - s))  d/dg of silu(g)*u
 //   du[n]  = dh[n] * silu(g[n])                           d/du of silu(g)*u
+// (other activations: dg[n] = dh[n] * dh/dg, du[n] = dh[n] * dh/du from act_partials)
 // g and u are the unrounded float values (recomputed, as LigerCute's
 // backward recomputes activations: LigerCute README, "Backward pass").
 float swiglu_row_backward(const uint16_t* dyrow, const uint16_t* wd_e, int H, int I, float wj,
                           const float* g, const float* u, const float* hq, float* dHu, float* dg,
-                          float* du) {
+                          float* du, int act = kActSwiGLU, float clamp = 0.0f) {
   for (int n = 0; n < I; ++n) dHu[n] = 0.0f;
   for (int c = 0; c < H; ++c) {
     float dyc = bf16_to_float(dyrow[c]);
@@ -151,9 +226,16 @@ float swiglu_row_backward(const uint16_t* dyrow, const uint16_t* wd_e, int H, in
   for (int n = 0; n < I; ++n) gamma += dHu[n] * hq[n];
   for (int n = 0; n < I; ++n) {
     float dh = wj * dHu[n];
-    float s = 1.0f / (1.0f + std::exp(-g[n]));
-    dg[n] = ((dh * u[n]) * s) * (1.0f + g[n] * (1.0f - s));
-    du[n] = dh * silu(g[n]);
+    if (act == kActSwiGLU) {
+      float s = 1.0f / (1.0f + std::exp(-g[n]));
+      dg[n] = ((dh * u[n]) * s) * (1.0f + g[n] * (1.0f - s));
+      du[n] = dh * silu(g[n]);
+    } else {
+      float dhdg, dhdu;
+      act_partials(act, clamp, g[n], u[n], &dhdg, &dhdu);
+      dg[n] = dh * dhdg;
+      du[n] = dh * dhdu;
+    }
   }
   return gamma;
 }
@@ -254,8 +336,9 @@ int oracle_dispatch(const int32_t* ids, const float* w, const uint16_t* x, int T
 // Grouped SwiGLU expert MLP on expert-major rows, for a chosen set of rows.
 // LightMoE README, "Grouped GEMM" (out[sum M_e, N] = a[rows_e] @ b[e].T with
 // b: [num_experts, N, K]) and "MoE inference" (gate/up projection, gated
-// activation, down projection, routing-weight application).  For row r of
-// expert e (found from m_indptr):
+// activation, down projection, routing-weight application).  act / clamp
+// choose the gated activation (act_forward).  For row r of expert e (found
+// from m_indptr):
 //   g, u, hq as in gate_up_row;  o = down_row(hq)
 //   h_out[i, n]  = bf16(hq[n])                           (optional)
 //   gu_out[i, :] = [g | u] as float, 2I values            (optional)
@@ -265,8 +348,8 @@ int oracle_dispatch(const int32_t* ids, const float* w, const uint16_t* x, int T
 int oracle_grouped_swiglu_rows(const uint16_t* x_perm, const int32_t* m_indptr, const uint16_t* wgu,
                                const uint16_t* wd, const float* w_perm, int R, int H, int I, int E,
                                const int32_t* rows, int nrows, uint16_t* h_out, float* gu_out,
-                               uint16_t* y_out, int threads) {
-  if (R < 0 || H < 1 || I < 1 || E < 1 || nrows < 0) return ORACLE_BAD_ARG;
+                               uint16_t* y_out, int act, float clamp, int threads) {
+  if (R < 0 || H < 1 || I < 1 || E < 1 || nrows < 0 || act < 0 || act > kActReGLU) return ORACLE_BAD_ARG;
   for (int i = 0; i < nrows; ++i) {
     if (rows[i] < 0 || rows[i] >= R || expert_of_row(m_indptr, E, rows[i]) < 0) return ORACLE_BAD_ARG;
   }
@@ -276,7 +359,7 @@ int oracle_grouped_swiglu_rows(const uint16_t* x_perm, const int32_t* m_indptr, 
     std::vector<float> g(I), u(I), hq(I), o(H);
     const uint16_t* wgu_e = wgu + static_cast<size_t>(e) * 2 * I * H;
     const uint16_t* wd_e = wd + static_cast<size_t>(e) * H * I;
-    gate_up_row(x_perm + static_cast<size_t>(r) * H, wgu_e, H, I, g.data(), u.data(), hq.data());
+    gate_up_row(x_perm + static_cast<size_t>(r) * H, wgu_e, H, I, g.data(), u.data(), hq.data(), act, clamp);
     if (h_out)
       for (int n = 0; n < I; ++n) h_out[static_cast<size_t>(i) * I + n] = float_to_bf16(hq[n]);
     if (gu_out)
@@ -325,8 +408,8 @@ int oracle_combine(const uint16_t* y_perm, const int32_t* slot_to_row, int T, in
 // agree bit for bit (a test checks this).
 int oracle_forward_tokens(const uint16_t* x, const uint16_t* wgu, const uint16_t* wd,
                           const int32_t* ids, const float* w, int T, int H, int I, int E, int k,
-                          const int32_t* toks, int ntok, uint16_t* y_out, int threads) {
-  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || ntok < 0) return ORACLE_BAD_ARG;
+                          const int32_t* toks, int ntok, uint16_t* y_out, int act, float clamp, int threads) {
+  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || ntok < 0 || act < 0 || act > kActReGLU) return ORACLE_BAD_ARG;
   for (int i = 0; i < ntok; ++i) {
     if (toks[i] < 0 || toks[i] >= T) return ORACLE_BAD_ARG;
     for (int j = 0; j < k; ++j) {
@@ -341,7 +424,7 @@ int oracle_forward_tokens(const uint16_t* x, const uint16_t* wgu, const uint16_t
       int e = ids[static_cast<size_t>(t) * k + j];
       float wj = w[static_cast<size_t>(t) * k + j];
       gate_up_row(x + static_cast<size_t>(t) * H, wgu + static_cast<size_t>(e) * 2 * I * H, H, I, g.data(),
-                  u.data(), hq.data());
+                  u.data(), hq.data(), act, clamp);
       down_row(hq.data(), wd + static_cast<size_t>(e) * H * I, H, I, o.data());
       for (int c = 0; c < H; ++c) acc[c] += round_to_bf16(wj * o[c]);
     }
@@ -365,9 +448,9 @@ int oracle_forward_tokens(const uint16_t* x, const uint16_t* wgu, const uint16_t
 // selected k, so unselected logits get no gradient.
 int oracle_backward_tokens(const uint16_t* x, const uint16_t* dy, const uint16_t* wgu, const uint16_t* wd,
                            const int32_t* ids, const float* w, int T, int H, int I, int E, int k,
-                           const int32_t* toks, int ntok, uint16_t* dx_out, float* dlogits_out,
-                           int threads) {
-  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || ntok < 0) return ORACLE_BAD_ARG;
+                           const int32_t* toks, int ntok, uint16_t* dx_out, float* dlogits_out, int act,
+                           float clamp, int threads) {
+  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || ntok < 0 || act < 0 || act > kActReGLU) return ORACLE_BAD_ARG;
   for (int i = 0; i < ntok; ++i) {
     if (toks[i] < 0 || toks[i] >= T) return ORACLE_BAD_ARG;
     for (int j = 0; j < k; ++j) {
@@ -382,9 +465,10 @@ int oracle_backward_tokens(const uint16_t* x, const uint16_t* dy, const uint16_t
       int e = ids[static_cast<size_t>(t) * k + j];
       float wj = w[static_cast<size_t>(t) * k + j];
       const uint16_t* wgu_e = wgu + static_cast<size_t>(e) * 2 * I * H;
-      gate_up_row(x + static_cast<size_t>(t) * H, wgu_e, H, I, g.data(), u.data(), hq.data());
+      gate_up_row(x + static_cast<size_t>(t) * H, wgu_e, H, I, g.data(), u.data(), hq.data(), act, clamp);
       gam[j] = swiglu_row_backward(dy + static_cast<size_t>(t) * H, wd + static_cast<size_t>(e) * H * I, H, I,
-                                   wj, g.data(), u.data(), hq.data(), dHu.data(), dg.data(), du.data());
+                                   wj, g.data(), u.data(), hq.data(), dHu.data(), dg.data(), du.data(), act,
+                                   clamp);
       for (int n = 0; n < I; ++n) {
         const uint16_t* wg = wgu_e + static_cast<size_t>(n) * H;
         const uint16_t* wu = wgu_e + static_cast<size_t>(I + n) * H;
@@ -422,9 +506,9 @@ int oracle_backward_tokens(const uint16_t* x, const uint16_t* dy, const uint16_t
 // float sums in row order.  An expert with no rows gets exact zeros.
 int oracle_backward_dw(const uint16_t* x, const uint16_t* dy, const uint16_t* wgu, const uint16_t* wd,
                        const int32_t* ids, const float* w, int T, int H, int I, int E, int k,
-                       const int32_t* experts, int nexp, uint16_t* dwgu_out, uint16_t* dwd_out,
-                       int threads) {
-  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || nexp < 0) return ORACLE_BAD_ARG;
+                       const int32_t* experts, int nexp, uint16_t* dwgu_out, uint16_t* dwd_out, int act,
+                       float clamp, int threads) {
+  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || nexp < 0 || act < 0 || act > kActReGLU) return ORACLE_BAD_ARG;
   for (int i = 0; i < nexp; ++i)
     if (experts[i] < 0 || experts[i] >= E) return ORACLE_BAD_ARG;
   for (long long s = 0; s < static_cast<long long>(T) * k; ++s)
@@ -441,9 +525,9 @@ int oracle_backward_dw(const uint16_t* x, const uint16_t* dy, const uint16_t* wg
         float wj = w[static_cast<size_t>(t) * k + j];
         const uint16_t* xr = x + static_cast<size_t>(t) * H;
         const uint16_t* dyr = dy + static_cast<size_t>(t) * H;
-        gate_up_row(xr, wgu_e, H, I, g.data(), u.data(), hq.data());
+        gate_up_row(xr, wgu_e, H, I, g.data(), u.data(), hq.data(), act, clamp);
         swiglu_row_backward(dyr, wd_e, H, I, wj, g.data(), u.data(), hq.data(), dHu.data(), dg.data(),
-                            du.data());
+                            du.data(), act, clamp);
         for (int n = 0; n < I; ++n) {
           float* rg = agu.data() + static_cast<size_t>(n) * H;
           float* ru = agu.data() + static_cast<size_t>(I + n) * H;

@@ -73,7 +73,27 @@ def topk_bruteforce(logits: np.ndarray, k: int) -> np.ndarray:
     return out
 
 
-def dense_layer_fp64(x_bits, wgu_bits, wd_bits, logits, sel, requires_grad=False):
+def gated_act_torch(g, u, act="swiglu", clamp=0.0):
+    """The gated activations in plain torch ops (independent of the oracle's C++):
+    swiglu silu(g) u; swiglu_bounded silu(min(g, c)) clamp(u, -c, c); swiglu_oai
+    gc sigmoid(1.702 gc) (clamp(u, -c, c) + 1) with gc = min(g, c); geglu gelu_tanh(g) u;
+    reglu relu(g) u.  torch.clamp passes gradient on the closed interval."""
+    F = torch.nn.functional
+    if act == "swiglu":
+        return F.silu(g) * u
+    if act == "swiglu_bounded":
+        return F.silu(torch.clamp(g, max=clamp)) * torch.clamp(u, -clamp, clamp)
+    if act == "swiglu_oai":
+        gc = torch.clamp(g, max=clamp)
+        return gc * torch.sigmoid(1.702 * gc) * (torch.clamp(u, -clamp, clamp) + 1.0)
+    if act == "geglu":
+        return F.gelu(g, approximate="tanh") * u
+    if act == "reglu":
+        return F.relu(g) * u
+    raise ValueError(act)
+
+
+def dense_layer_fp64(x_bits, wgu_bits, wd_bits, logits, sel, requires_grad=False, act="swiglu", clamp=0.0):
     """fp64 dense evaluation of the routed SwiGLU layer.
 
     Y[t, c] = sum_e G[t, e] * sum_n silu(g[t,e,n]) * u[t,e,n] * Wd[e, c, n]
@@ -91,7 +111,7 @@ def dense_layer_fp64(x_bits, wgu_bits, wd_bits, logits, sel, requires_grad=False
     mask[torch.arange(T)[:, None], torch.tensor(sel, dtype=torch.long)] = True
     G = torch.softmax(lg.masked_fill(~mask, float("-inf")), dim=1)
     gu = torch.einsum("th,enh->ten", x, wgu)
-    a = torch.nn.functional.silu(gu[..., :I]) * gu[..., I:]
+    a = gated_act_torch(gu[..., :I], gu[..., I:], act, clamp)
     o = torch.einsum("ten,ecn->tec", a, wd)
     Y = torch.einsum("te,tec->tc", G, o)
     return Y, dict(x=x, wgu=wgu, wd=wd, logits=lg, G=G)

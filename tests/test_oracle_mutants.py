@@ -10,6 +10,7 @@ import shutil
 import pytest
 
 import oracle
+from tests import test_oracle_activations as P_A
 from tests import test_oracle_dispatch as P_D
 from tests import test_oracle_layer as P_L
 from tests import test_oracle_route as P_R
@@ -63,8 +64,32 @@ def _battery():
     P_L.test_closed_form_worked_example()
 
 
+# Mistakes in the gated-activation variants, caught by the activation pins.
+ACT_MUTANTS = {
+    "oai_alpha": ("constexpr float kOaiAlpha = 1.702f;", "constexpr float kOaiAlpha = 1.0f;"),
+    "oai_plus_one_dropped": ("return (gc * sigmoid(kOaiAlpha * gc)) * (uc + 1.0f);",
+                             "return (gc * sigmoid(kOaiAlpha * gc)) * uc;"),
+    "bounded_up_unclamped": ("return silu(gc) * uc;", "return silu(gc) * u;"),
+    "bounded_gate_grad_not_blocked": ("*dhdg = (g <= c) ? uc * s * (1.0f + gc * (1.0f - s)) : 0.0f;",
+                                      "*dhdg = uc * s * (1.0f + gc * (1.0f - s));"),
+    "gelu_cubic_term_dropped": ("constexpr float kGeluK1 = 0.044715f;", "constexpr float kGeluK1 = 0.0f;"),
+    "geglu_grad_second_term_dropped": ("const float dgelu = 0.5f * (1.0f + t) + 0.5f * g * (1.0f - t * t) * kGeluK0 * (1.0f + 3.0f * kGeluK1 * g * g);",
+                                       "const float dgelu = 0.5f * (1.0f + t);"),
+    "reglu_grad_not_gated": ("*dhdg = (g > 0.0f) ? u : 0.0f;", "*dhdg = u;"),
+}
+
+
+def _act_battery():
+    for act, clamp in P_A.VARIANTS:
+        P_A.test_forward_matches_fp64_dense(act, clamp)
+        P_A.test_backward_matches_fp64_autograd(act, clamp)
+    for case in P_A.CLOSED_FORM:
+        P_A.test_closed_form_values(*case)
+
+
 def test_battery_passes_on_the_real_oracle():
     _battery()
+    _act_battery()
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
@@ -78,4 +103,18 @@ def test_planted_mistake_is_caught(name, tmp_path):
     with oracle.using(lib):
         with pytest.raises((AssertionError, ValueError)):
             _battery()
+    shutil.rmtree(tmp_path, ignore_errors=True)
+
+
+@pytest.mark.parametrize("name", sorted(ACT_MUTANTS))
+def test_planted_activation_mistake_is_caught(name, tmp_path):
+    before, after = ACT_MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(before) == 1, f"mutation anchor for {name} not found exactly once"
+    path = tmp_path / "mutant.cpp"
+    path.write_text(src.replace(before, after))
+    lib = oracle.open_library(oracle.compile_source(str(path), str(tmp_path / "libmutant.so")))
+    with oracle.using(lib):
+        with pytest.raises((AssertionError, ValueError)):
+            _act_battery()
     shutil.rmtree(tmp_path, ignore_errors=True)
