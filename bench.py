@@ -56,7 +56,13 @@ def parse_args():
     ap.add_argument("--inputs", choices=["x_perm", "gather"], default="x_perm",
                     help="expert GEMM inputs: expert-major copies (x_perm, dy_perm) read as dense tiles, or the "
                     "memory-lean path that gathers x and dY rows by token inside the GEMMs")
-    return ap.parse_args()
+    ap.add_argument("--act", choices=["swiglu", "swiglu_bounded", "swiglu_oai", "geglu", "reglu"],
+                    default="swiglu", help="gated activation of the expert MLP (x_perm inputs only for the others)")
+    ap.add_argument("--act-clamp", type=float, default=7.0, help="clamp of swiglu_bounded / limit of swiglu_oai")
+    args = ap.parse_args()
+    if args.act != "swiglu" and args.inputs == "gather":
+        ap.error("--act other than swiglu runs on x_perm inputs")
+    return args
 
 
 def load_peaks() -> dict:
@@ -95,7 +101,7 @@ def gemm_bytes(wl, name: str, experts_used: int) -> int:
         "gemm_bwd_dx": 2 * act_x + w_gu + act_h,                  # dgu, W_gu -> dx_perm
         "gemm_bwd_dw_gate_up": 2 * act_x + act_h + E * 2 * I * H * 2,  # dgu, x_perm -> dW_gate_up (all experts)
         "gemm_bwd_dw_down": act_h + act_x + E * H * I * 2,         # dY rows, w h -> dW_down (all experts)
-    }[name]
+    }["gemm_gate_up_swiglu" if name == "gemm_gate_up_glu" else name]
 
 
 def kernel_work(wl, name: str):
@@ -103,7 +109,8 @@ def kernel_work(wl, name: str):
     T, H, I, E, k, R = wl.T, wl.H, wl.I, wl.E, wl.k, wl.R
     rhi = R * H * I
     nunits = math.ceil(R / 256)
-    gemm = {"gemm_gate_up_swiglu": 4 * rhi, "gemm_down_scale": 2 * rhi, "gemm_bwd_dh": 2 * rhi,
+    gemm = {"gemm_gate_up_swiglu": 4 * rhi, "gemm_gate_up_glu": 4 * rhi, "gemm_down_scale": 2 * rhi,
+            "gemm_bwd_dh": 2 * rhi,
             "gemm_bwd_dx": 4 * rhi, "gemm_bwd_dw_gate_up": 4 * rhi, "gemm_bwd_dw_down": 2 * rhi}
     if name in gemm:
         return "flop", gemm[name]
@@ -182,25 +189,26 @@ def gpu_index_for(local_rank: int) -> str:
 
 
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
-def oracle_sample(wl, inp, ids, w, n_tokens: int, experts) -> float:
+def oracle_sample(wl, inp, ids, w, n_tokens: int, experts, act=("swiglu", 0.0)) -> float:
     """Runs the oracle's fwd + bwd on n_tokens tokens and dW on `experts`; returns algorithmic flop."""
     import numpy as np
 
     import oracle
 
     toks = np.arange(n_tokens, dtype=np.int32)
-    oracle.forward_tokens(inp["x"], inp["wgu"], inp["wd"], ids, w, toks=toks)
-    oracle.backward_tokens(inp["x"], inp["dy"], inp["wgu"], inp["wd"], ids, w, toks=toks)
+    kw = dict(act=act[0], clamp=act[1])
+    oracle.forward_tokens(inp["x"], inp["wgu"], inp["wd"], ids, w, toks=toks, **kw)
+    oracle.backward_tokens(inp["x"], inp["dy"], inp["wgu"], inp["wd"], ids, w, toks=toks, **kw)
     flop = 12 * n_tokens * wl.k * wl.H * wl.I  # fwd (6) + dH (2) + dX (4) per routed row
     if len(experts):
         oracle.backward_dw(inp["x"], inp["dy"], inp["wgu"], inp["wd"], ids, w,
-                           experts=np.asarray(experts, dtype=np.int32))
+                           experts=np.asarray(experts, dtype=np.int32), **kw)
         rows = np.bincount(ids.ravel(), minlength=wl.E)[np.asarray(experts)].sum()
         flop += 6 * int(rows) * wl.H * wl.I
     return float(flop)
 
 
-def size_oracle_sample(wl, inp, ids, w, seconds: float):
+def size_oracle_sample(wl, inp, ids, w, seconds: float, act=("swiglu", 0.0)):
     """Tokens / experts for a sample of about `seconds` of oracle work (one calibration call)."""
     import numpy as np
 
@@ -208,7 +216,7 @@ def size_oracle_sample(wl, inp, ids, w, seconds: float):
 
     n_cal = min(wl.T, 2 * oracle.default_threads())  # enough tokens to engage every thread
     t0 = time.perf_counter()
-    oracle_sample(wl, inp, ids, w, n_cal, [])
+    oracle_sample(wl, inp, ids, w, n_cal, [], act)
     per_tok = max((time.perf_counter() - t0) / n_cal, 1e-6)
     n_tok = int(max(1, min(wl.T, seconds * 0.7 / per_tok)))
     # dW runs one expert per thread: up to `threads` mid-size experts whose largest row count
@@ -235,7 +243,7 @@ def run_reference(args, rank, world):
     ids, w = oracle.route_topk(inp["logits"], wl.k)
     total_steps = args.warmup + args.steps
     per_step = max(0.05, min(5.0, 150.0 / max(total_steps, 1)))
-    n_tok, _ = size_oracle_sample(wl, inp, ids, w, per_step)
+    n_tok, _ = size_oracle_sample(wl, inp, ids, w, per_step, (args.act, args.act_clamp))
     counts = np.bincount(ids.ravel(), minlength=wl.E)
     nonempty = [int(e) for e in np.nonzero(counts)[0]]
     flops = []
@@ -243,7 +251,7 @@ def run_reference(args, rank, world):
     for i in range(total_steps):
         experts = [nonempty[i % len(nonempty)]] if nonempty else []
         t0 = time.perf_counter()
-        f = oracle_sample(wl, inp, ids, w, n_tok, experts)
+        f = oracle_sample(wl, inp, ids, w, n_tok, experts, (args.act, args.act_clamp))
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             flops.append(f)
@@ -314,6 +322,9 @@ def run_ours(args, rank, world, local_rank):
         if gather:
             moe.grouped_swiglu_fwd_gather(xx, dbuf["row_to_slot"], k, dbuf["m_indptr"], wgu, wd, dbuf["w_perm"],
                                           out=fbuf, workspace=ws_f)
+        elif args.act != "swiglu":
+            moe.grouped_glu_fwd(dbuf["x_perm"], dbuf["m_indptr"], wgu, wd, dbuf["w_perm"], args.act, args.act_clamp,
+                                out=fbuf, workspace=ws_f)
         else:
             moe.grouped_swiglu_fwd(dbuf["x_perm"], dbuf["m_indptr"], wgu, wd, dbuf["w_perm"], out=fbuf,
                                    workspace=ws_f)
@@ -323,6 +334,7 @@ def run_ours(args, rank, world, local_rank):
         out = dict(bbuf)
         if dx_out is not None:
             out.update(dx=dx_out, d_logits=dl_out)
+        # the saved derivative factors make the backward the same for every activation
         bwd = moe.bwd_dx_dw_gather if gather else moe.bwd_dx_dw
         bwd(dyy, xx if gather else dbuf["x_perm"], fbuf["h_perm"], fbuf["gu_perm"], ids, w, dbuf["m_indptr"],
             dbuf["row_to_slot"], dbuf["slot_to_row"], dbuf["w_perm"], wgu, wd, out=out, workspace=ws_b)
@@ -574,9 +586,9 @@ def run_ours(args, rank, world, local_rank):
         import oracle
 
         ids_h, w_h = oracle.route_topk(inp["logits"], k)
-        n_tok, experts = size_oracle_sample(wl, inp, ids_h, w_h, args.cpu_seconds)
+        n_tok, experts = size_oracle_sample(wl, inp, ids_h, w_h, args.cpu_seconds, (args.act, args.act_clamp))
         t0 = time.perf_counter()
-        f = oracle_sample(wl, inp, ids_h, w_h, n_tok, experts)
+        f = oracle_sample(wl, inp, ids_h, w_h, n_tok, experts, (args.act, args.act_clamp))
         dt = time.perf_counter() - t0
         cpu = {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.default_threads(),
                "kind": "oracle",
@@ -590,7 +602,7 @@ def run_ours(args, rank, world, local_rank):
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict(wl.as_dict(), **{"pass": "forward+backward", "parallelism": f"replicas x{world}",
-                                           "expert_inputs": args.inputs,
+                                           "expert_inputs": args.inputs, "activation": args.act,
                                            "l2": f"inputs larger than L2: {(wgu.numel() + wd.numel()) * 2 / 1e9:.2f} GB "
                                                  f"of weights + activations streamed per step (L2 129 MB)"}),
             "tokens_per_s": round(tokens_per_s, 1),

@@ -63,6 +63,18 @@ typedef enum {
   LIGER_MOE_ERR_DEVICE = -6              /* returned by liger_moe_device_error when a flag is set */
 } liger_moe_status;
 
+/* Gated activations of the expert MLP, h = act(g, u) with g, u the fp32 gate and up
+ * projections.  LightMoE README, "Compatibility" and "Highlights" name the variants; their
+ * formulas are the plainest published forms.  A clamp passes the gradient on its closed
+ * interval and blocks it outside. */
+enum liger_moe_activation {
+  LIGER_MOE_ACT_SWIGLU = 0,         /* silu(g) u                                             */
+  LIGER_MOE_ACT_SWIGLU_BOUNDED = 1, /* silu(min(g, c)) clamp(u, -c, c)          (c = clamp)  */
+  LIGER_MOE_ACT_SWIGLU_OAI = 2,     /* gc sigmoid(1.702 gc) (clamp(u, -c, c) + 1), gc = min(g, c) */
+  LIGER_MOE_ACT_GEGLU = 3,          /* gelu(g) u, gelu(g) = g/2 (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))) */
+  LIGER_MOE_ACT_REGLU = 4           /* max(g, 0) u                                           */
+};
+
 /* Bits of the device error flag. */
 #define LIGER_MOE_DEVERR_BAD_EXPERT_ID 0x1 /* topk_ids entry outside [0, E) */
 #define LIGER_MOE_DEVERR_BAD_ROW 0x2       /* row / slot index outside [0, T*k) */
@@ -156,6 +168,20 @@ int liger_moe_grouped_swiglu_fwd(const void* x_perm, const int32_t* m_indptr, co
                                  size_t* workspace_bytes, void* stream);
 
 /*
+ * The expert MLP with another gated activation (enum liger_moe_activation) in place of
+ * SwiGLU; everything else as liger_moe_grouped_swiglu_fwd.  gu_perm receives that
+ * activation's derivative factors [dh/dg | dh/du], so liger_moe_bwd_dx_dw applies to the
+ * result unchanged when gu_perm is saved.
+ *   activation  LIGER_MOE_ACT_*; anything else is LIGER_MOE_ERR_INVALID_ARG.
+ *   clamp       c of the bounded SwiGLU and the limit of SwiGLU-OAI: finite and > 0 for those
+ *               two (else LIGER_MOE_ERR_INVALID_ARG); ignored by the others.
+ */
+int liger_moe_grouped_glu_fwd(const void* x_perm, const int32_t* m_indptr, const void* w_gate_up,
+                              const void* w_down, const float* w_perm, int R, int H, int I, int E,
+                              int activation, float clamp, void* h_perm, float* gu_perm, void* y_perm,
+                              void* workspace, size_t* workspace_bytes, void* stream);
+
+/*
  * The same expert MLP on token-major input: row r's input is x[row_to_slot[r] / k],
  * copied row by row by the gate/up GEMM's loader straight from x, so no
  * expert-major copy of x is written or read (memory-lean; on GB300 the loader's
@@ -218,6 +244,20 @@ int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const void* h_perm, 
                         const void* w_gate_up, const void* w_down, int T, int H, int I, int E, int k,
                         void* dx, void* dw_gate_up, void* dw_down, float* d_logits, void* workspace,
                         size_t* workspace_bytes, void* stream);
+
+/*
+ * liger_moe_bwd_dx_dw for a layer whose forward used another gated activation
+ * (liger_moe_grouped_glu_fwd): the activation and clamp matter only when gu_perm is NULL,
+ * where the derivative factors are recomputed; with saved factors the result equals
+ * liger_moe_bwd_dx_dw.  Arguments, outputs, limits and workspace otherwise as
+ * liger_moe_bwd_dx_dw; activation and clamp are checked as in liger_moe_grouped_glu_fwd.
+ */
+int liger_moe_bwd_dx_dw_glu(const void* dy, const void* x_perm, const void* h_perm, const float* gu_perm,
+                            const int32_t* topk_ids, const float* topk_w, const int32_t* m_indptr,
+                            const int32_t* row_to_slot, const int32_t* slot_to_row, const float* w_perm,
+                            const void* w_gate_up, const void* w_down, int T, int H, int I, int E, int k,
+                            int activation, float clamp, void* dx, void* dw_gate_up, void* dw_down,
+                            float* d_logits, void* workspace, size_t* workspace_bytes, void* stream);
 
 /*
  * The same backward on token-major input: x [T, H] bf16 replaces x_perm.  The

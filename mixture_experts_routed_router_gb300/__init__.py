@@ -17,9 +17,9 @@ import torch
 
 from . import build as _build
 
-__all__ = ["route_topk", "dispatch", "grouped_swiglu_fwd", "grouped_swiglu_fwd_gather", "combine", "bwd_dx_dw",
-           "bwd_dx_dw_gather", "device_error", "workspace_bytes", "trace_enable", "trace_records", "LigerMoEError",
-           "library_path", "load_library"]
+__all__ = ["route_topk", "dispatch", "grouped_swiglu_fwd", "grouped_swiglu_fwd_gather", "grouped_glu_fwd",
+           "combine", "bwd_dx_dw", "bwd_dx_dw_gather", "bwd_dx_dw_glu", "ACTIVATIONS", "device_error",
+           "workspace_bytes", "trace_enable", "trace_records", "LigerMoEError", "library_path", "load_library"]
 
 _lock = threading.Lock()
 _lib = None
@@ -28,6 +28,8 @@ OK = 0
 STATUS = {0: "OK", -1: "INVALID_ARG", -2: "MISALIGNED", -3: "CAPACITY", -4: "UNSUPPORTED_DEVICE", -5: "LAUNCH",
           -6: "DEVICE"}
 DEVERR = {0x1: "BAD_EXPERT_ID", 0x2: "BAD_ROW", 0x4: "BAD_INDPTR", 0x8: "WAIT_TIMEOUT"}
+# enum liger_moe_activation: gated activations of the expert MLP
+ACTIVATIONS = {"swiglu": 0, "swiglu_bounded": 1, "swiglu_oai": 2, "geglu": 3, "reglu": 4}
 
 
 class LigerMoEError(RuntimeError):
@@ -58,6 +60,10 @@ def load_library(build_if_missing: bool = True):
         lib.liger_moe_bwd_dx_dw.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, P, S, P]
         lib.liger_moe_grouped_swiglu_fwd_gather.argtypes = [P, P, I, I, P, P, P, P, I, I, I, P, P, P, P, S, P]
         lib.liger_moe_bwd_dx_dw_gather.argtypes = lib.liger_moe_bwd_dx_dw.argtypes
+        F = ctypes.c_float
+        lib.liger_moe_grouped_glu_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P, P, P, P, S, P]
+        lib.liger_moe_bwd_dx_dw_glu.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P,
+                                                P, S, P]
         lib.liger_moe_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
         lib.liger_moe_trace_enable.argtypes = [I]
         lib.liger_moe_trace_get.argtypes = [I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)]
@@ -66,7 +72,8 @@ def load_library(build_if_missing: bool = True):
         lib.liger_moe_status_string.argtypes = [I]
         for f in (lib.liger_moe_route_topk, lib.liger_moe_dispatch, lib.liger_moe_grouped_swiglu_fwd,
                   lib.liger_moe_grouped_swiglu_fwd_gather, lib.liger_moe_combine, lib.liger_moe_bwd_dx_dw,
-                  lib.liger_moe_bwd_dx_dw_gather, lib.liger_moe_device_error,
+                  lib.liger_moe_bwd_dx_dw_gather, lib.liger_moe_grouped_glu_fwd, lib.liger_moe_bwd_dx_dw_glu,
+                  lib.liger_moe_device_error,
                   lib.liger_moe_abi_version, lib.liger_moe_trace_enable, lib.liger_moe_trace_count,
                   lib.liger_moe_trace_get):
             f.restype = ctypes.c_int
@@ -217,6 +224,30 @@ def grouped_swiglu_fwd(x_perm, m_indptr, w_gate_up, w_down, w_perm, *, save_gu=T
     return h, gu, y
 
 
+def _act_id(activation: str) -> int:
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"unknown activation {activation!r}; one of {sorted(ACTIVATIONS)}")
+    return ACTIVATIONS[activation]
+
+
+def grouped_glu_fwd(x_perm, m_indptr, w_gate_up, w_down, w_perm, activation="swiglu", clamp=0.0, *, save_gu=True,
+                    out=None, workspace=None, stream=None):
+    """The expert MLP with a chosen gated activation (ACTIVATIONS); returns (h_perm, gu_perm, y_perm).
+
+    gu_perm holds that activation's derivative factors [dh/dg | dh/du]; clamp is the bound of
+    swiglu_bounded and the limit of swiglu_oai.
+    """
+    lib = load_library()
+    _need(x_perm, "x_perm", torch.bfloat16)
+    R, H = x_perm.shape
+    E, I, h, gu, y, ws = _fwd_args(R, H, w_gate_up, w_down, m_indptr, w_perm, save_gu, out, workspace, x_perm.device)
+    n = ctypes.c_size_t(ws.numel())
+    _check("liger_moe_grouped_glu_fwd", lib.liger_moe_grouped_glu_fwd(
+        _ptr(x_perm), _ptr(m_indptr), _ptr(w_gate_up), _ptr(w_down), _ptr(w_perm), R, H, I, E, _act_id(activation),
+        float(clamp), _ptr(h), _ptr(gu), _ptr(y), _ptr(ws), ctypes.byref(n), _stream(stream)))
+    return h, gu, y
+
+
 def grouped_swiglu_fwd_gather(x, row_to_slot, k, m_indptr, w_gate_up, w_down, w_perm, *, save_gu=True, out=None,
                               workspace=None, stream=None):
     """The expert MLP on token-major x [T,H]: row r reads x[row_to_slot[r] // k] (no x_perm).
@@ -249,7 +280,7 @@ def combine(y_perm, slot_to_row, T, k, *, out=None, stream=None):
 
 
 def _bwd(fn, dy, x_src, x_name, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_slot, slot_to_row, w_perm,
-         w_gate_up, w_down, out, workspace, stream):
+         w_gate_up, w_down, out, workspace, stream, act=None):
     lib = load_library()
     _need(dy, "dy", torch.bfloat16)
     T, H = dy.shape
@@ -277,10 +308,11 @@ def _bwd(fn, dy, x_src, x_name, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row
     ws = _workspace(workspace, workspace_bytes("bwd_dx_dw", T=T, H=H, I=I, E=E, k=k, saved_gu=gu_perm is not None,
                                                gather=x_name == "x"), dev)
     n = ctypes.c_size_t(ws.numel())
+    extra = () if act is None else (_act_id(act[0]), float(act[1]))
     _check(fn, getattr(lib, fn)(
         _ptr(dy), _ptr(x_src), _ptr(h_perm), _ptr(gu_perm), _ptr(topk_ids), _ptr(topk_w), _ptr(m_indptr),
-        _ptr(row_to_slot), _ptr(slot_to_row), _ptr(w_perm), _ptr(w_gate_up), _ptr(w_down), T, H, I, E, k, _ptr(dx),
-        _ptr(dwgu), _ptr(dwd), _ptr(dl), _ptr(ws), ctypes.byref(n), _stream(stream)))
+        _ptr(row_to_slot), _ptr(slot_to_row), _ptr(w_perm), _ptr(w_gate_up), _ptr(w_down), T, H, I, E, k, *extra,
+        _ptr(dx), _ptr(dwgu), _ptr(dwd), _ptr(dl), _ptr(ws), ctypes.byref(n), _stream(stream)))
     return dx, dwgu, dwd, dl
 
 
@@ -289,6 +321,14 @@ def bwd_dx_dw(dy, x_perm, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_sl
     """Backward of the layer: returns (dx [T,H], dw_gate_up [E,2I,H], dw_down [E,H,I], d_logits [T,E])."""
     return _bwd("liger_moe_bwd_dx_dw", dy, x_perm, "x_perm", h_perm, gu_perm, topk_ids, topk_w, m_indptr,
                 row_to_slot, slot_to_row, w_perm, w_gate_up, w_down, out, workspace, stream)
+
+
+def bwd_dx_dw_glu(dy, x_perm, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_slot, slot_to_row, w_perm,
+                  w_gate_up, w_down, activation="swiglu", clamp=0.0, *, out=None, workspace=None, stream=None):
+    """bwd_dx_dw for a forward with another gated activation (needed when gu_perm is None: the
+    derivative factors are recomputed with that activation)."""
+    return _bwd("liger_moe_bwd_dx_dw_glu", dy, x_perm, "x_perm", h_perm, gu_perm, topk_ids, topk_w, m_indptr,
+                row_to_slot, slot_to_row, w_perm, w_gate_up, w_down, out, workspace, stream, act=(activation, clamp))
 
 
 def bwd_dx_dw_gather(dy, x, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_slot, slot_to_row, w_perm,

@@ -46,6 +46,14 @@ int check_topk(long long T, int E, int k) {
   return LIGER_MOE_OK;
 }
 
+// activation id and clamp (enum liger_moe_activation)
+int check_activation(int act, float clamp) {
+  if (act < LIGER_MOE_ACT_SWIGLU || act > LIGER_MOE_ACT_REGLU) return LIGER_MOE_ERR_INVALID_ARG;
+  if ((act == LIGER_MOE_ACT_SWIGLU_BOUNDED || act == LIGER_MOE_ACT_SWIGLU_OAI) && !(clamp > 0.f && clamp < 3.0e38f))
+    return LIGER_MOE_ERR_INVALID_ARG;
+  return LIGER_MOE_OK;
+}
+
 template <class T>
 T* carve(uint8_t*& cursor, size_t bytes) {
   T* p = reinterpret_cast<T*>(cursor);
@@ -237,8 +245,10 @@ namespace {
 int grouped_swiglu_fwd_impl(const void* x_perm, const void* x, const int32_t* row_to_slot, int T, int k,
                             const int32_t* m_indptr, const void* w_gate_up, const void* w_down, const float* w_perm,
                             long long R, int H, int I, int E, void* h_perm, float* gu_perm, void* y_perm,
-                            void* workspace, size_t* workspace_bytes, void* stream) {
+                            void* workspace, size_t* workspace_bytes, void* stream, int act = LIGER_MOE_ACT_SWIGLU,
+                            float clamp = 0.f) {
   if (int rc = check_shapes(R, H, I, E)) return rc;
+  if (int rc = check_activation(act, clamp)) return rc;
   if (workspace_bytes == nullptr || m_indptr == nullptr) return LIGER_MOE_ERR_INVALID_ARG;
   const void* a_src = x != nullptr ? x : x_perm;
   if (R > 0 && (a_src == nullptr || w_gate_up == nullptr || w_down == nullptr || w_perm == nullptr ||
@@ -279,6 +289,8 @@ int grouped_swiglu_fwd_impl(const void* x_perm, const void* x, const int32_t* ro
   a.h_perm = static_cast<uint16_t*>(h_perm);
   a.gu_perm = gu_perm;
   a.y_perm = static_cast<uint16_t*>(y_perm);
+  a.act = act;
+  a.act_clamp = clamp;
   if (int rc = launch_gate_up(a, dev, s)) return rc;
   return launch_down(a, dev, s);
 }
@@ -291,6 +303,14 @@ LIGER_MOE_API int liger_moe_grouped_swiglu_fwd(const void* x_perm, const int32_t
                                                size_t* workspace_bytes, void* stream) {
   return grouped_swiglu_fwd_impl(x_perm, nullptr, nullptr, 0, 1, m_indptr, w_gate_up, w_down, w_perm, R, H, I, E,
                                  h_perm, gu_perm, y_perm, workspace, workspace_bytes, stream);
+}
+
+LIGER_MOE_API int liger_moe_grouped_glu_fwd(const void* x_perm, const int32_t* m_indptr, const void* w_gate_up,
+                                            const void* w_down, const float* w_perm, int R, int H, int I, int E,
+                                            int activation, float clamp, void* h_perm, float* gu_perm, void* y_perm,
+                                            void* workspace, size_t* workspace_bytes, void* stream) {
+  return grouped_swiglu_fwd_impl(x_perm, nullptr, nullptr, 0, 1, m_indptr, w_gate_up, w_down, w_perm, R, H, I, E,
+                                 h_perm, gu_perm, y_perm, workspace, workspace_bytes, stream, activation, clamp);
 }
 
 LIGER_MOE_API int liger_moe_grouped_swiglu_fwd_gather(const void* x, const int32_t* row_to_slot, int T, int k,
@@ -328,8 +348,10 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
                    const int32_t* topk_ids, const float* topk_w, const int32_t* m_indptr, const int32_t* row_to_slot,
                    const int32_t* slot_to_row, const float* w_perm, const void* w_gate_up, const void* w_down, int T,
                    int H, int I, int E, int k, void* dx, void* dw_gate_up, void* dw_down, float* d_logits,
-                   void* workspace, size_t* workspace_bytes, void* stream) {
+                   void* workspace, size_t* workspace_bytes, void* stream, int act = LIGER_MOE_ACT_SWIGLU,
+                   float clamp = 0.f) {
   if (int rc = check_topk(T, E, k)) return rc;
+  if (int rc = check_activation(act, clamp)) return rc;
   const long long R = static_cast<long long>(T) * k;
   if (int rc = check_shapes(R, H, I, E)) return rc;
   if (2 * padded_rows(R, E) > kIndexLimit) return LIGER_MOE_ERR_CAPACITY;  // the padded dW operands' rows
@@ -419,6 +441,8 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
       f.I = I;
       f.E = E;
       f.gu_perm = gu_ws;
+      f.act = act;
+      f.act_clamp = clamp;
       if (int rc = launch_gate_up(f, dev, s)) return rc;
     }
     if (int rc = launch_bwd_dh(a, dev, s)) return rc;
@@ -442,6 +466,18 @@ LIGER_MOE_API int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const 
   return bwd_dx_dw_impl(dy, x_perm, nullptr, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_slot, slot_to_row,
                         w_perm, w_gate_up, w_down, T, H, I, E, k, dx, dw_gate_up, dw_down, d_logits, workspace,
                         workspace_bytes, stream);
+}
+
+LIGER_MOE_API int liger_moe_bwd_dx_dw_glu(const void* dy, const void* x_perm, const void* h_perm,
+                                          const float* gu_perm, const int32_t* topk_ids, const float* topk_w,
+                                          const int32_t* m_indptr, const int32_t* row_to_slot,
+                                          const int32_t* slot_to_row, const float* w_perm, const void* w_gate_up,
+                                          const void* w_down, int T, int H, int I, int E, int k, int activation,
+                                          float clamp, void* dx, void* dw_gate_up, void* dw_down, float* d_logits,
+                                          void* workspace, size_t* workspace_bytes, void* stream) {
+  return bwd_dx_dw_impl(dy, x_perm, nullptr, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_slot, slot_to_row,
+                        w_perm, w_gate_up, w_down, T, H, I, E, k, dx, dw_gate_up, dw_down, d_logits, workspace,
+                        workspace_bytes, stream, activation, clamp);
 }
 
 LIGER_MOE_API int liger_moe_bwd_dx_dw_gather(const void* dy, const void* x, const void* h_perm, const float* gu_perm,

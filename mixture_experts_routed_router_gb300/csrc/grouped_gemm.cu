@@ -79,7 +79,10 @@ struct Layout {
 };
 
 enum class Sched : int { RowsM = 0, RowsK = 1 };
-enum class Epi : int { SwiGLU = 0, ScaleRows = 1, DH = 2, Store = 3 };
+// SwiGLU: the gate/up GEMM with SwiGLU; GLU: the same with the activation chosen at run time
+// (Params::act), kept apart so that the default SwiGLU kernel carries none of the variants' code.
+enum class Epi : int { SwiGLU = 0, ScaleRows = 1, DH = 2, Store = 3, GLU = 4 };
+constexpr bool gate_up_epi(Epi e) { return e == Epi::SwiGLU || e == Epi::GLU; }
 template <Epi EP, int SPLIT>
 using LayoutOf = Layout<EP == Epi::DH ? 1 : 0, SPLIT>;
 
@@ -102,6 +105,8 @@ struct Params {
   long long out_expert_stride;
   uint16_t* out2;         // DH: dgu [2R, 2I] (hi rows, then lo rows)
   float* gu_out;          // SwiGLU: derivative factors [a | b] fp32 [R, 2I] (nullable)
+  int act;                // SwiGLU epilogue: gated activation (LIGER_MOE_ACT_*)
+  float act_clamp;        // its clamp (bounded SwiGLU) or limit (SwiGLU-OAI)
   const float* row_scale; // ScaleRows, DH: w_perm
   const float* gu_in;     // DH: derivative factors [a | b] fp32 [R, 2I]
   const uint16_t* h_in;   // DH: h [R, I]
@@ -201,6 +206,59 @@ __device__ __forceinline__ void load16_bf16(const uint16_t* src, float (&v)[16])
   }
 }
 
+// ---------------------------------------------------------------- gated activations
+// h = act(g, u) from the fp32 gate/up accumulators, with the backward's derivative factors
+// a = dh/dg and b = dh/du (LightMoE README, "Compatibility" / "Highlights" name the variants):
+//   SwiGLU          h = silu(g) u
+//   bounded SwiGLU  h = silu(gc) uc,  gc = min(g, c), uc = clamp(u, -c, c)
+//   SwiGLU-OAI      h = gc sigmoid(1.702 gc) (uc + 1), same clamps, c the limit
+//   GeGLU           h = gelu(g) u, gelu with the tanh form
+//   ReGLU           h = max(g, 0) u
+// A clamp passes the gradient on its closed interval and blocks it outside.
+template <int ACT>
+__device__ __forceinline__ void gated_act(float g, float u, float c, float& h, float& a, float& b) {
+  if constexpr (ACT == LIGER_MOE_ACT_SWIGLU) {
+    const float sg = 1.0f / (1.0f + expf(-g));
+    const float sl = g * sg;
+    h = sl * u;
+    a = u * sg * (1.0f + g * (1.0f - sg));
+    b = sl;
+  } else if constexpr (ACT == LIGER_MOE_ACT_SWIGLU_BOUNDED || ACT == LIGER_MOE_ACT_SWIGLU_OAI) {
+    constexpr float kAlpha = ACT == LIGER_MOE_ACT_SWIGLU_OAI ? 1.702f : 1.0f;
+    const float gc = fminf(g, c), uc = fminf(fmaxf(u, -c), c);
+    const float sg = 1.0f / (1.0f + expf(-kAlpha * gc));
+    const float glu = gc * sg;
+    const float lin = ACT == LIGER_MOE_ACT_SWIGLU_OAI ? uc + 1.0f : uc;
+    h = glu * lin;
+    a = (g <= c) ? lin * sg * (1.0f + kAlpha * gc * (1.0f - sg)) : 0.0f;
+    b = (u >= -c && u <= c) ? glu : 0.0f;
+  } else if constexpr (ACT == LIGER_MOE_ACT_GEGLU) {
+    constexpr float k0 = 0.7978845608028654f, k1 = 0.044715f;  // sqrt(2/pi), cubic coefficient
+    const float t = tanhf(k0 * (g + k1 * g * g * g));
+    const float gelu = 0.5f * g * (1.0f + t);
+    h = gelu * u;
+    a = u * (0.5f * (1.0f + t) + 0.5f * g * (1.0f - t * t) * k0 * (1.0f + 3.0f * k1 * g * g));
+    b = gelu;
+  } else {  // ReGLU
+    const float r = fmaxf(g, 0.0f);
+    h = r * u;
+    a = g > 0.0f ? u : 0.0f;
+    b = r;
+  }
+}
+
+template <int ACT>
+__device__ __forceinline__ void gated_act32(const float (&g)[32], const float (&u)[32], float c, float (&hv)[32],
+                                            uint32_t (&aw)[32], uint32_t (&bw)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float a, b;
+    gated_act<ACT>(g[i], u[i], c, hv[i], a, b);
+    aw[i] = __float_as_uint(a);
+    bw[i] = __float_as_uint(b);
+  }
+}
+
 // ---------------------------------------------------------------- epilogue output path
 // An epilogue warp owns 32 accumulator rows.  Each output box is 32 rows x 128 bytes
 // (64 bf16 or 32 fp32 columns): every lane writes its row into a swizzled staging buffer,
@@ -262,7 +320,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
   const int row_local = sub * 32 + lane;
   const Rows mode = slice_mode<S>(tl, sub);
   const bool row_ok = (S == Sched::RowsK) ? true : row_local < tl.rows;
-  if constexpr (EP == Epi::SwiGLU) {
+  if constexpr (gate_up_epi(EP)) {
     if (mode == Rows::None) return;
     // accumulator columns [0, BN/2) = g, [BN/2, BN) = u for output columns nt*BN/2 + c;
     // this warp's output columns: [64 colhalf, 64 colhalf + 64)
@@ -280,17 +338,29 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
         tmem_ld32(t_row + q * 64 + half * 32, g);
         tmem_ld32(t_row + BN / 2 + q * 64 + half * 32, u);
         tmem_ld_wait();
-        // h = silu(g) u with silu(g) = g s, s = 1 / (1 + exp(-g)); the backward's derivative
-        // factors dh/dg = u s (1 + g (1 - s)) and dh/du = silu(g) are saved in fp32.
+        // h = act(g, u); the backward's derivative factors dh/dg, dh/du are saved in fp32
+        // (GLU: the activation is the same for the whole launch, so the switch is warp-uniform)
         uint32_t aw[32], bw[32];
         float hv[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float sg = 1.0f / (1.0f + expf(-g[i]));
-          const float sl = g[i] * sg;
-          hv[i] = sl * u[i];
-          aw[i] = __float_as_uint(u[i] * sg * (1.0f + g[i] * (1.0f - sg)));
-          bw[i] = __float_as_uint(sl);
+        if constexpr (EP == Epi::SwiGLU) {
+          gated_act32<LIGER_MOE_ACT_SWIGLU>(g, u, 0.f, hv, aw, bw);
+        } else {
+          switch (p.act) {
+            case LIGER_MOE_ACT_SWIGLU_BOUNDED:
+              gated_act32<LIGER_MOE_ACT_SWIGLU_BOUNDED>(g, u, p.act_clamp, hv, aw, bw);
+              break;
+            case LIGER_MOE_ACT_SWIGLU_OAI:
+              gated_act32<LIGER_MOE_ACT_SWIGLU_OAI>(g, u, p.act_clamp, hv, aw, bw);
+              break;
+            case LIGER_MOE_ACT_GEGLU:
+              gated_act32<LIGER_MOE_ACT_GEGLU>(g, u, p.act_clamp, hv, aw, bw);
+              break;
+            case LIGER_MOE_ACT_REGLU:
+              gated_act32<LIGER_MOE_ACT_REGLU>(g, u, p.act_clamp, hv, aw, bw);
+              break;
+            default:
+              gated_act32<LIGER_MOE_ACT_SWIGLU>(g, u, p.act_clamp, hv, aw, bw);
+          }
         }
         if (p.gu_out != nullptr) {
           const int xg = col + half * 32;
@@ -512,7 +582,7 @@ __device__ __forceinline__ void load_stage_tiled(const CUtensorMap* tmA, const C
   }
   if constexpr (kLoadB) {
     if constexpr (!B_MN) {
-      if constexpr (EP == Epi::SwiGLU) {
+      if constexpr (gate_up_epi(EP)) {
         const int r = tl.e * p.b_rows_per_expert + tl.nt * (BN / 2);
         tma_load_2d(sb, tmB, fb, kb * BK, r);
         tma_load_2d(sb + B_BYTES / 2, tmB, fb, kb * BK, r + p.b_split);
@@ -1125,6 +1195,8 @@ int launch_gate_up(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) 
   p.out = a.h_perm;
   p.ld_out = a.I;
   p.gu_out = a.gu_perm;
+  p.act = a.act;
+  p.act_clamp = a.act_clamp;
   CUtensorMap tc0, tc1;  // h (bf16) and [g|u] (fp32); an absent output reuses the other's map
   if (a.h_perm != nullptr && make_out_bf16(&tc0, a.h_perm, a.I, a.R)) return LIGER_MOE_ERR_LAUNCH;
   if (a.gu_perm != nullptr && make_out_f32(&tc1, a.gu_perm, 2ULL * a.I, a.R)) return LIGER_MOE_ERR_LAUNCH;
@@ -1132,6 +1204,10 @@ int launch_gate_up(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) 
   if (a.gu_perm == nullptr) tc1 = tc0;
   if (a.h_perm == nullptr && a.gu_perm == nullptr) return LIGER_MOE_OK;
   const long long tiles = rows_m_tiles(a.R, a.E, p.n_tiles);
+  if (a.act != LIGER_MOE_ACT_SWIGLU) {  // the other gated activations read x_perm
+    if (gather) return LIGER_MOE_ERR_INVALID_ARG;
+    return launch_gemm<Sched::RowsM, Epi::GLU, false, false>(ta, tb, tc0, tc1, p, tiles, dev, s, "gemm_gate_up_glu");
+  }
   if (gather)
     return launch_gemm<Sched::RowsM, Epi::SwiGLU, false, false, 0, Gather::A>(ta, tb, tc0, tc1, p, tiles, dev, s,
                                                                               "gemm_gate_up_swiglu");

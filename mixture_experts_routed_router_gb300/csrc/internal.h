@@ -71,6 +71,8 @@ struct FwdGemmArgs {
   uint16_t* h_perm;  // nullable (then only gu is stored)
   float* gu_perm;     // [R, 2I] fp32, nullable
   uint16_t* y_perm;
+  int act = LIGER_MOE_ACT_SWIGLU;  // gated activation of the gate/up epilogue
+  float act_clamp = 0.f;
 };
 // gate/up GEMM + SwiGLU epilogue (h_perm may be NULL: only gu is stored).
 int launch_gate_up(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s);

@@ -28,7 +28,8 @@ def lib():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for f in ("liger_moe_route_topk", "liger_moe_dispatch", "liger_moe_grouped_swiglu_fwd", "liger_moe_combine",
-              "liger_moe_bwd_dx_dw", "liger_moe_grouped_swiglu_fwd_gather", "liger_moe_bwd_dx_dw_gather"):
+              "liger_moe_bwd_dx_dw", "liger_moe_grouped_swiglu_fwd_gather", "liger_moe_bwd_dx_dw_gather",
+              "liger_moe_grouped_glu_fwd", "liger_moe_bwd_dx_dw_glu"):
         assert f in names
 
 
@@ -131,6 +132,46 @@ def test_gather_entry_points_validate_like_their_x_perm_twins(lib):
     bad = list(args)
     bad[16] = 9  # k > E
     assert g(*bad) == INVALID
+
+
+def test_activation_ids_match_the_header():
+    text = open(HEADER).read()
+    for name, v in moe.ACTIVATIONS.items():
+        assert re.search(rf"LIGER_MOE_ACT_{name.upper()}\s*=\s*{v}\b", text), name
+
+
+def test_glu_entry_points_validate_the_activation(lib):
+    n = ctypes.c_size_t(0)
+    f = lib.liger_moe_grouped_glu_fwd
+    F = ctypes.c_float
+
+    def fwd(act, clamp):  # (x_perm, m_indptr, w_gu, w_d, w_perm, R, H, I, E, act, clamp, h, gu, y, ws, ws_bytes, s)
+        return f(D, D, D, D, D, 1024, 256, 128, 8, act, F(clamp), D, None, D, None, ctypes.byref(n), None)
+
+    assert fwd(0, 0.0) == OK
+    q = n.value
+    assert lib.liger_moe_grouped_swiglu_fwd(D, D, D, D, D, 1024, 256, 128, 8, D, None, D, None, ctypes.byref(n),
+                                            None) == OK
+    assert n.value == q  # same workspace for every activation
+    for act, clamp in ((3, 0.0), (4, 0.0), (1, 7.0), (2, 7.0)):
+        assert fwd(act, clamp) == OK
+    # unknown ids; bounded variants need a finite positive clamp
+    for act, clamp in ((-1, 0.0), (5, 0.0), (1, 0.0), (2, -1.0), (1, float("inf")), (2, float("nan"))):
+        assert fwd(act, clamp) == INVALID, (act, clamp)
+    g = lib.liger_moe_bwd_dx_dw_glu
+    # (dy, x_perm, h, gu, ids, w, indptr, r2s, s2r, w_perm, w_gu, w_d, T, H, I, E, k, act, clamp, dx, dwgu, dwd,
+    #  d_logits, ws, ws_bytes, stream)
+    args = [D, D, D, D, D, D, D, D, D, D, D, D, 256, 256, 128, 8, 2, 3, F(0.0), D, D, D, D, None, ctypes.byref(n),
+            None]
+    assert g(*args) == OK
+    assert n.value == moe.workspace_bytes("bwd_dx_dw", T=256, H=256, I=128, E=8, k=2, saved_gu=True)
+    args[3] = None  # recompute the factors
+    assert g(*args) == OK
+    assert n.value == moe.workspace_bytes("bwd_dx_dw", T=256, H=256, I=128, E=8, k=2, saved_gu=False)
+    args[17] = 7
+    assert g(*args) == INVALID
+    args[17], args[18] = 1, F(0.0)
+    assert g(*args) == INVALID
 
 
 def test_combine_argument_errors(lib):
