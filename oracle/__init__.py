@@ -93,15 +93,22 @@ class using:
         return False
 
 
-# Gated activations of the expert MLP (moe_oracle.cpp, act_forward); `clamp` is the bound of
-# the bounded SwiGLU and the limit of SwiGLU-OAI, unused otherwise.
-ACTIVATIONS = {"swiglu": 0, "swiglu_bounded": 1, "swiglu_oai": 2, "geglu": 3, "reglu": 4}
+# Activations of the expert MLP (moe_oracle.cpp, act_forward); `clamp` is the bound of the
+# bounded SwiGLU and the limit of SwiGLU-OAI, unused otherwise.  All but relu2 are gated and take
+# wgu [E, 2I, H] (gate rows, then up rows); relu2 takes the up weight [E, I, H] in its place.
+ACTIVATIONS = {"swiglu": 0, "swiglu_bounded": 1, "swiglu_oai": 2, "geglu": 3, "reglu": 4, "relu2": 5}
 
 
 def _act(act: str) -> int:
     if act not in ACTIVATIONS:
         raise ValueError(f"unknown activation {act!r}")
     return ACTIVATIONS[act]
+
+
+def _inter(wgu, act: str) -> int:
+    """I from the first weight's rows: 2I for the gated activations, I for relu2."""
+    rows = wgu.shape[1]
+    return rows if act == "relu2" else rows // 2
 
 
 def default_threads() -> int:
@@ -152,7 +159,9 @@ def dispatch(ids: np.ndarray, w: np.ndarray | None, x: np.ndarray | None, E: int
 
 
 def grouped_swiglu_rows(x_perm, m_indptr, wgu, wd, w_perm, rows, threads=None, act="swiglu", clamp=0.0):
-    """Expert MLP on chosen expert-major rows: (h bf16 [n,I], gu f32 [n,2I] = [g | u], y bf16 [n,H])."""
+    """Expert MLP on chosen expert-major rows: (h bf16 [n,I], gu f32 [n,2I] = [g | u], y bf16 [n,H]).
+
+    relu2: gu is [n, I] (its one projection)."""
     x_perm = _c(x_perm, np.uint16)
     wgu = _c(wgu, np.uint16)
     wd = _c(wd, np.uint16)
@@ -160,11 +169,11 @@ def grouped_swiglu_rows(x_perm, m_indptr, wgu, wd, w_perm, rows, threads=None, a
     w_perm = _c(w_perm, np.float32)
     rows = _c(rows, np.int32)
     R, H = x_perm.shape
-    E, twoI, _ = wgu.shape
-    I = twoI // 2
+    E, nin, _ = wgu.shape
+    I = _inter(wgu, act)
     n = rows.size
     h = np.empty((n, I), np.uint16)
-    gu = np.empty((n, 2 * I), np.float32)
+    gu = np.empty((n, nin), np.float32)
     y = np.empty((n, H), np.uint16)
     rc = _load().oracle_grouped_swiglu_rows(x_perm.ctypes.data, m_indptr.ctypes.data, wgu.ctypes.data,
                                             wd.ctypes.data, w_perm.ctypes.data, R, H, I, E, rows.ctypes.data,
@@ -190,12 +199,12 @@ def forward_tokens(x, wgu, wd, ids, w, toks=None, threads=None, act="swiglu", cl
     x, wgu, wd = _c(x, np.uint16), _c(wgu, np.uint16), _c(wd, np.uint16)
     ids, w = _c(ids, np.int32), _c(w, np.float32)
     T, H = x.shape
-    E, twoI, _ = wgu.shape
+    E = wgu.shape[0]
     k = ids.shape[1]
     toks = np.arange(T, dtype=np.int32) if toks is None else _c(toks, np.int32)
     out = np.empty((toks.size, H), np.uint16)
     rc = _load().oracle_forward_tokens(x.ctypes.data, wgu.ctypes.data, wd.ctypes.data, ids.ctypes.data,
-                                       w.ctypes.data, T, H, twoI // 2, E, k, toks.ctypes.data, toks.size,
+                                       w.ctypes.data, T, H, _inter(wgu, act), E, k, toks.ctypes.data, toks.size,
                                        out.ctypes.data, _act(act), float(clamp), threads or default_threads())
     _check(rc, "forward_tokens")
     return out
@@ -207,13 +216,13 @@ def backward_tokens(x, dy, wgu, wd, ids, w, toks=None, threads=None, act="swiglu
     wgu, wd = _c(wgu, np.uint16), _c(wd, np.uint16)
     ids, w = _c(ids, np.int32), _c(w, np.float32)
     T, H = x.shape
-    E, twoI, _ = wgu.shape
+    E = wgu.shape[0]
     k = ids.shape[1]
     toks = np.arange(T, dtype=np.int32) if toks is None else _c(toks, np.int32)
     dx = np.empty((toks.size, H), np.uint16)
     dl = np.empty((toks.size, E), np.float32)
     rc = _load().oracle_backward_tokens(x.ctypes.data, dy.ctypes.data, wgu.ctypes.data, wd.ctypes.data,
-                                        ids.ctypes.data, w.ctypes.data, T, H, twoI // 2, E, k,
+                                        ids.ctypes.data, w.ctypes.data, T, H, _inter(wgu, act), E, k,
                                         toks.ctypes.data, toks.size, dx.ctypes.data, dl.ctypes.data,
                                         _act(act), float(clamp), threads or default_threads())
     _check(rc, "backward_tokens")
@@ -221,16 +230,16 @@ def backward_tokens(x, dy, wgu, wd, ids, w, toks=None, threads=None, act="swiglu
 
 
 def backward_dw(x, dy, wgu, wd, ids, w, experts=None, threads=None, act="swiglu", clamp=0.0):
-    """(dW_gu bf16 [n,2I,H], dW_d bf16 [n,H,I]) for the listed experts."""
+    """(dW_gu bf16 [n,2I,H] (relu2: [n,I,H]), dW_d bf16 [n,H,I]) for the listed experts."""
     x, dy = _c(x, np.uint16), _c(dy, np.uint16)
     wgu, wd = _c(wgu, np.uint16), _c(wd, np.uint16)
     ids, w = _c(ids, np.int32), _c(w, np.float32)
     T, H = x.shape
-    E, twoI, _ = wgu.shape
-    I = twoI // 2
+    E, nin, _ = wgu.shape
+    I = _inter(wgu, act)
     k = ids.shape[1]
     experts = np.arange(E, dtype=np.int32) if experts is None else _c(experts, np.int32)
-    dwgu = np.empty((experts.size, twoI, H), np.uint16)
+    dwgu = np.empty((experts.size, nin, H), np.uint16)
     dwd = np.empty((experts.size, H, I), np.uint16)
     rc = _load().oracle_backward_dw(x.ctypes.data, dy.ctypes.data, wgu.ctypes.data, wd.ctypes.data,
                                     ids.ctypes.data, w.ctypes.data, T, H, I, E, k, experts.ctypes.data,

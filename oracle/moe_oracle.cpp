@@ -27,6 +27,8 @@
 //     activations bounded SwiGLU (with an activation clamp), SwiGLU-OAI and
 //     GeGLU, plus ReGLU; the pages name them without formulas, so each is
 //     written out below in its plainest published form (see act_forward).
+//     ReLU² is the one non-gated form: its experts hold two weights (up
+//     and down, LightMoE README, "MoE inference"), h = max(a, 0)^2.
 // Readings where the pages are silent (tie order, gate/up row order,
 // rounding points, softmax over the selected k) are spelled out at each
 // function.  Arithmetic is float (fp32) with bf16 inputs widened exactly;
@@ -74,14 +76,20 @@ inline float silu(float a) { return a / (1.0f + std::exp(-a)); }
 //   2 SwiGLU-OAI      h = gc sigmoid(a gc) (uc + 1),  a = 1.702, same clamps with c the limit
 //   3 GeGLU           h = gelu(g) u,  gelu(g) = g/2 (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3)))
 //   4 ReGLU           h = max(g, 0) u
+//   5 ReLU²           h = r r,  r = max(g, 0)   (not gated: there is no u, see gated())
 // A clamp passes the gradient where its input lies inside the closed interval and blocks it
 // outside.  SwiGLU keeps its own operation order (silu, then the product) everywhere below.
-constexpr int kActSwiGLU = 0, kActBounded = 1, kActOAI = 2, kActGeGLU = 3, kActReGLU = 4;
+constexpr int kActSwiGLU = 0, kActBounded = 1, kActOAI = 2, kActGeGLU = 3, kActReGLU = 4, kActReLU2 = 5;
 constexpr float kOaiAlpha = 1.702f;
 constexpr float kGeluK0 = 0.7978845608028654f;  // sqrt(2 / pi)
 constexpr float kGeluK1 = 0.044715f;
 
 inline float sigmoid(float a) { return 1.0f / (1.0f + std::exp(-a)); }
+
+// Gated activations read two projections of x (rows [0, I) and [I, 2I) of the expert's first
+// weight, [2I, H]); ReLU² reads one (its up weight, [I, H]).
+inline bool gated(int act) { return act != kActReLU2; }
+inline int first_rows(int act, int I) { return gated(act) ? 2 * I : I; }
 
 inline float act_forward(int act, float c, float g, float u) {
   switch (act) {
@@ -99,6 +107,10 @@ inline float act_forward(int act, float c, float g, float u) {
     }
     case kActReGLU:
       return std::max(g, 0.0f) * u;
+    case kActReLU2: {
+      const float r = std::max(g, 0.0f);
+      return r * r;
+    }
     default:
       return silu(g) * u;
   }
@@ -131,6 +143,10 @@ inline void act_partials(int act, float c, float g, float u, float* dhdg, float*
     case kActReGLU:
       *dhdg = (g > 0.0f) ? u : 0.0f;
       *dhdu = std::max(g, 0.0f);
+      return;
+    case kActReLU2:
+      *dhdg = 2.0f * std::max(g, 0.0f);
+      *dhdu = 0.0f;
       return;
     default:
       return;
@@ -175,17 +191,18 @@ inline bool ranks_before(float a, int ia, float b, int ib) {
 //   u[n] = sum_h x[h] * Wgu[I + n, h]              (rows [I, 2I) are the up)
 //   hq[n] = bf16( act(g[n], u[n]) )                 (rounded: h is stored bf16; SwiGLU:
 //                                                   silu(g[n]) * u[n])
-// Sums in float, h ascending.
+// Sums in float, h ascending.  ReLU²: Wgu is the up weight [I, H], g[n] = sum_h x[h] * Wup[n, h],
+// u[n] = 0.
 void gate_up_row(const uint16_t* xrow, const uint16_t* wgu_e, int H, int I, float* g, float* u,
                  float* hq, int act = kActSwiGLU, float clamp = 0.0f) {
   for (int n = 0; n < I; ++n) {
     const uint16_t* wg = wgu_e + static_cast<size_t>(n) * H;
-    const uint16_t* wu = wgu_e + static_cast<size_t>(I + n) * H;
+    const uint16_t* wu = gated(act) ? wgu_e + static_cast<size_t>(I + n) * H : nullptr;
     float ag = 0.0f, au = 0.0f;
     for (int h = 0; h < H; ++h) {
       float xv = bf16_to_float(xrow[h]);
       ag += xv * bf16_to_float(wg[h]);
-      au += xv * bf16_to_float(wu[h]);
+      if (wu) au += xv * bf16_to_float(wu[h]);
     }
     g[n] = ag;
     u[n] = au;
@@ -210,7 +227,8 @@ void down_row(const float* hq, const uint16_t* wd_e, int H, int I, float* o) {
 //   s      = 1 / (1 + exp(-g[n]))
 //   dg[n]  = ((dh[n] * u[n]) * s) * (1 + g[n] * (1 - s))  d/dg of silu(g)*u
 //   du[n]  = dh[n] * silu(g[n])                           d/du of silu(g)*u
-// (other activations: dg[n] = dh[n] * dh/dg, du[n] = dh[n] * dh/du from act_partials)
+// (other activations: dg[n] = dh[n] * dh/dg, du[n] = dh[n] * dh/du from act_partials;
+//  ReLU²: dg[n] = dh[n] * 2 max(g[n], 0), du[n] = 0)
 // g and u are the unrounded float values (recomputed, as LigerCute's
 // backward recomputes activations: LigerCute README, "Backward pass").
 float swiglu_row_backward(const uint16_t* dyrow, const uint16_t* wd_e, int H, int I, float wj,
@@ -337,11 +355,11 @@ int oracle_dispatch(const int32_t* ids, const float* w, const uint16_t* x, int T
 // LightMoE README, "Grouped GEMM" (out[sum M_e, N] = a[rows_e] @ b[e].T with
 // b: [num_experts, N, K]) and "MoE inference" (gate/up projection, gated
 // activation, down projection, routing-weight application).  act / clamp
-// choose the gated activation (act_forward).  For row r of expert e (found
-// from m_indptr):
+// choose the activation (act_forward); wgu is [E, 2I, H], or the up weight
+// [E, I, H] for ReLU².  For row r of expert e (found from m_indptr):
 //   g, u, hq as in gate_up_row;  o = down_row(hq)
 //   h_out[i, n]  = bf16(hq[n])                           (optional)
-//   gu_out[i, :] = [g | u] as float, 2I values            (optional)
+//   gu_out[i, :] = [g | u] as float, 2I values (ReLU²: g, I values)  (optional)
 //   y_out[i, c]  = bf16( w_perm[r] * o[c] )               (optional)
 // The weight is applied to the down projection's float result before the
 // single bf16 rounding of y.
@@ -349,7 +367,7 @@ int oracle_grouped_swiglu_rows(const uint16_t* x_perm, const int32_t* m_indptr, 
                                const uint16_t* wd, const float* w_perm, int R, int H, int I, int E,
                                const int32_t* rows, int nrows, uint16_t* h_out, float* gu_out,
                                uint16_t* y_out, int act, float clamp, int threads) {
-  if (R < 0 || H < 1 || I < 1 || E < 1 || nrows < 0 || act < 0 || act > kActReGLU) return ORACLE_BAD_ARG;
+  if (R < 0 || H < 1 || I < 1 || E < 1 || nrows < 0 || act < 0 || act > kActReLU2) return ORACLE_BAD_ARG;
   for (int i = 0; i < nrows; ++i) {
     if (rows[i] < 0 || rows[i] >= R || expert_of_row(m_indptr, E, rows[i]) < 0) return ORACLE_BAD_ARG;
   }
@@ -357,15 +375,16 @@ int oracle_grouped_swiglu_rows(const uint16_t* x_perm, const int32_t* m_indptr, 
     int r = rows[i];
     int e = expert_of_row(m_indptr, E, r);
     std::vector<float> g(I), u(I), hq(I), o(H);
-    const uint16_t* wgu_e = wgu + static_cast<size_t>(e) * 2 * I * H;
+    const int nin = first_rows(act, I);
+    const uint16_t* wgu_e = wgu + static_cast<size_t>(e) * nin * H;
     const uint16_t* wd_e = wd + static_cast<size_t>(e) * H * I;
     gate_up_row(x_perm + static_cast<size_t>(r) * H, wgu_e, H, I, g.data(), u.data(), hq.data(), act, clamp);
     if (h_out)
       for (int n = 0; n < I; ++n) h_out[static_cast<size_t>(i) * I + n] = float_to_bf16(hq[n]);
     if (gu_out)
       for (int n = 0; n < I; ++n) {
-        gu_out[static_cast<size_t>(i) * 2 * I + n] = g[n];
-        gu_out[static_cast<size_t>(i) * 2 * I + I + n] = u[n];
+        gu_out[static_cast<size_t>(i) * nin + n] = g[n];
+        if (gated(act)) gu_out[static_cast<size_t>(i) * nin + I + n] = u[n];
       }
     if (y_out) {
       down_row(hq.data(), wd_e, H, I, o.data());
@@ -409,7 +428,7 @@ int oracle_combine(const uint16_t* y_perm, const int32_t* slot_to_row, int T, in
 int oracle_forward_tokens(const uint16_t* x, const uint16_t* wgu, const uint16_t* wd,
                           const int32_t* ids, const float* w, int T, int H, int I, int E, int k,
                           const int32_t* toks, int ntok, uint16_t* y_out, int act, float clamp, int threads) {
-  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || ntok < 0 || act < 0 || act > kActReGLU) return ORACLE_BAD_ARG;
+  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || ntok < 0 || act < 0 || act > kActReLU2) return ORACLE_BAD_ARG;
   for (int i = 0; i < ntok; ++i) {
     if (toks[i] < 0 || toks[i] >= T) return ORACLE_BAD_ARG;
     for (int j = 0; j < k; ++j) {
@@ -423,8 +442,8 @@ int oracle_forward_tokens(const uint16_t* x, const uint16_t* wgu, const uint16_t
     for (int j = 0; j < k; ++j) {
       int e = ids[static_cast<size_t>(t) * k + j];
       float wj = w[static_cast<size_t>(t) * k + j];
-      gate_up_row(x + static_cast<size_t>(t) * H, wgu + static_cast<size_t>(e) * 2 * I * H, H, I, g.data(),
-                  u.data(), hq.data(), act, clamp);
+      gate_up_row(x + static_cast<size_t>(t) * H, wgu + static_cast<size_t>(e) * first_rows(act, I) * H, H, I,
+                  g.data(), u.data(), hq.data(), act, clamp);
       down_row(hq.data(), wd + static_cast<size_t>(e) * H * I, H, I, o.data());
       for (int c = 0; c < H; ++c) acc[c] += round_to_bf16(wj * o[c]);
     }
@@ -441,7 +460,8 @@ int oracle_forward_tokens(const uint16_t* x, const uint16_t* wgu, const uint16_t
 // differentiable_probs).  For token t, with loss L = <dY, Y>:
 //   per j: (gamma_j, dg_j, du_j) = swiglu_row_backward(...)
 //   dX[t, h] = bf16( sum_j sum_n ( dg_j[n]*Wgu[e_j, n, h] + du_j[n]*Wgu[e_j, I+n, h] ) )
-//              (float; j ascending, then n ascending, gate term then up term)
+//              (float; j ascending, then n ascending, gate term then up term;
+//               ReLU²: the gate term alone, Wgu the up weight)
 //   S = sum_i w_i * gamma_i                    (i ascending)
 //   d_logits[t, ids_j] = w_j * (gamma_j - S);  every other entry is exactly 0
 // gamma_j = dL/dw_j; the last line is the softmax Jacobian restricted to the
@@ -450,7 +470,7 @@ int oracle_backward_tokens(const uint16_t* x, const uint16_t* dy, const uint16_t
                            const int32_t* ids, const float* w, int T, int H, int I, int E, int k,
                            const int32_t* toks, int ntok, uint16_t* dx_out, float* dlogits_out, int act,
                            float clamp, int threads) {
-  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || ntok < 0 || act < 0 || act > kActReGLU) return ORACLE_BAD_ARG;
+  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || ntok < 0 || act < 0 || act > kActReLU2) return ORACLE_BAD_ARG;
   for (int i = 0; i < ntok; ++i) {
     if (toks[i] < 0 || toks[i] >= T) return ORACLE_BAD_ARG;
     for (int j = 0; j < k; ++j) {
@@ -464,17 +484,17 @@ int oracle_backward_tokens(const uint16_t* x, const uint16_t* dy, const uint16_t
     for (int j = 0; j < k; ++j) {
       int e = ids[static_cast<size_t>(t) * k + j];
       float wj = w[static_cast<size_t>(t) * k + j];
-      const uint16_t* wgu_e = wgu + static_cast<size_t>(e) * 2 * I * H;
+      const uint16_t* wgu_e = wgu + static_cast<size_t>(e) * first_rows(act, I) * H;
       gate_up_row(x + static_cast<size_t>(t) * H, wgu_e, H, I, g.data(), u.data(), hq.data(), act, clamp);
       gam[j] = swiglu_row_backward(dy + static_cast<size_t>(t) * H, wd + static_cast<size_t>(e) * H * I, H, I,
                                    wj, g.data(), u.data(), hq.data(), dHu.data(), dg.data(), du.data(), act,
                                    clamp);
       for (int n = 0; n < I; ++n) {
         const uint16_t* wg = wgu_e + static_cast<size_t>(n) * H;
-        const uint16_t* wu = wgu_e + static_cast<size_t>(I + n) * H;
+        const uint16_t* wu = gated(act) ? wgu_e + static_cast<size_t>(I + n) * H : nullptr;
         for (int h = 0; h < H; ++h) {
           acc[h] += dg[n] * bf16_to_float(wg[h]);
-          acc[h] += du[n] * bf16_to_float(wu[h]);
+          if (wu) acc[h] += du[n] * bf16_to_float(wu[h]);
         }
       }
     }
@@ -501,14 +521,15 @@ int oracle_backward_tokens(const uint16_t* x, const uint16_t* dy, const uint16_t
 // weight-gradient kernels).  For expert e, over its routed rows (t, j) with
 // t ascending:
 //   dW_gu[e, n, h]   = bf16( sum dg[n] * x[t, h] )        n < I
-//   dW_gu[e, I+n, h] = bf16( sum du[n] * x[t, h] )
+//   dW_gu[e, I+n, h] = bf16( sum du[n] * x[t, h] )          (gated activations only: ReLU²'s
+//                                                          dW_up is [E, I, H])
 //   dW_d[e, c, n]    = bf16( sum (w_j * dY[t, c]) * hq[n] )
 // float sums in row order.  An expert with no rows gets exact zeros.
 int oracle_backward_dw(const uint16_t* x, const uint16_t* dy, const uint16_t* wgu, const uint16_t* wd,
                        const int32_t* ids, const float* w, int T, int H, int I, int E, int k,
                        const int32_t* experts, int nexp, uint16_t* dwgu_out, uint16_t* dwd_out, int act,
                        float clamp, int threads) {
-  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || nexp < 0 || act < 0 || act > kActReGLU) return ORACLE_BAD_ARG;
+  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || nexp < 0 || act < 0 || act > kActReLU2) return ORACLE_BAD_ARG;
   for (int i = 0; i < nexp; ++i)
     if (experts[i] < 0 || experts[i] >= E) return ORACLE_BAD_ARG;
   for (long long s = 0; s < static_cast<long long>(T) * k; ++s)
@@ -516,8 +537,9 @@ int oracle_backward_dw(const uint16_t* x, const uint16_t* dy, const uint16_t* wg
   parallel_for(nexp, threads, [&](int i) {
     int e = experts[i];
     std::vector<float> g(I), u(I), hq(I), dHu(I), dg(I), du(I);
-    std::vector<float> agu(static_cast<size_t>(2) * I * H, 0.0f), ad(static_cast<size_t>(H) * I, 0.0f);
-    const uint16_t* wgu_e = wgu + static_cast<size_t>(e) * 2 * I * H;
+    const int nin = first_rows(act, I);
+    std::vector<float> agu(static_cast<size_t>(nin) * H, 0.0f), ad(static_cast<size_t>(H) * I, 0.0f);
+    const uint16_t* wgu_e = wgu + static_cast<size_t>(e) * nin * H;
     const uint16_t* wd_e = wd + static_cast<size_t>(e) * H * I;
     for (int t = 0; t < T; ++t) {
       for (int j = 0; j < k; ++j) {
@@ -530,11 +552,11 @@ int oracle_backward_dw(const uint16_t* x, const uint16_t* dy, const uint16_t* wg
                             du.data(), act, clamp);
         for (int n = 0; n < I; ++n) {
           float* rg = agu.data() + static_cast<size_t>(n) * H;
-          float* ru = agu.data() + static_cast<size_t>(I + n) * H;
+          float* ru = gated(act) ? agu.data() + static_cast<size_t>(I + n) * H : nullptr;
           for (int h = 0; h < H; ++h) {
             float xv = bf16_to_float(xr[h]);
             rg[h] += dg[n] * xv;
-            ru[h] += du[n] * xv;
+            if (ru) ru[h] += du[n] * xv;
           }
         }
         for (int c = 0; c < H; ++c) {
@@ -545,7 +567,7 @@ int oracle_backward_dw(const uint16_t* x, const uint16_t* dy, const uint16_t* wg
       }
     }
     if (dwgu_out) {
-      uint16_t* o = dwgu_out + static_cast<size_t>(i) * 2 * I * H;
+      uint16_t* o = dwgu_out + static_cast<size_t>(i) * nin * H;
       for (size_t q = 0; q < agu.size(); ++q) o[q] = float_to_bf16(agu[q]);
     }
     if (dwd_out) {

@@ -94,7 +94,8 @@ def gated_act_torch(g, u, act="swiglu", clamp=0.0):
 
 
 def dense_layer_fp64(x_bits, wgu_bits, wd_bits, logits, sel, requires_grad=False, act="swiglu", clamp=0.0):
-    """fp64 dense evaluation of the routed SwiGLU layer.
+    """fp64 dense evaluation of the routed SwiGLU layer (or another activation: gated_act_torch;
+    relu2 takes the up weight [E, I, H] as wgu and h = relu(x Wup^T)^2).
 
     Y[t, c] = sum_e G[t, e] * sum_n silu(g[t,e,n]) * u[t,e,n] * Wd[e, c, n]
     with g = x Wgu[e, :I]^T, u = x Wgu[e, I:]^T and G = softmax over the
@@ -106,12 +107,15 @@ def dense_layer_fp64(x_bits, wgu_bits, wd_bits, logits, sel, requires_grad=False
     wd = torch.tensor(bf16_to_f64(wd_bits), requires_grad=requires_grad)
     lg = torch.tensor(np.asarray(logits, dtype=np.float64), requires_grad=requires_grad)
     T, E = lg.shape
-    I = wgu.shape[1] // 2
+    I = wgu.shape[1] // 2 if act != "relu2" else wgu.shape[1]
     mask = torch.zeros((T, E), dtype=torch.bool)
     mask[torch.arange(T)[:, None], torch.tensor(sel, dtype=torch.long)] = True
     G = torch.softmax(lg.masked_fill(~mask, float("-inf")), dim=1)
-    gu = torch.einsum("th,enh->ten", x, wgu)
-    a = gated_act_torch(gu[..., :I], gu[..., I:], act, clamp)
+    if act == "relu2":  # not gated: wgu is the up weight [E, I, H], h = relu(x Wup^T)^2
+        a = torch.relu(torch.einsum("th,enh->ten", x, wgu)) ** 2
+    else:
+        gu = torch.einsum("th,enh->ten", x, wgu)
+        a = gated_act_torch(gu[..., :I], gu[..., I:], act, clamp)
     o = torch.einsum("ten,ecn->tec", a, wd)
     Y = torch.einsum("te,tec->tc", G, o)
     return Y, dict(x=x, wgu=wgu, wd=wd, logits=lg, G=G)

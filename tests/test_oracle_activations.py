@@ -1,10 +1,12 @@
-"""Pins for the oracle's gated-activation variants (bounded SwiGLU, SwiGLU-OAI, GeGLU, ReGLU), CPU only.
+"""Pins for the oracle's activation variants (bounded SwiGLU, SwiGLU-OAI, GeGLU, ReGLU, ReLU²), CPU only.
 
 LightMoE README, "Compatibility" and "Highlights" name the activations; their formulas are the
 plainest published forms (written out in tests/helpers.py gated_act_torch, independently of the
 oracle's C++).  Expected values come from that fp64 torch form (dense over all experts, autograd for
 the gradients) and from closed-form values at chosen points; the clamp values here are small so that
-the clamp branches are exercised by the synthetic N(0, 1) pre-activations.
+the clamp branches are exercised by the synthetic N(0, 1) pre-activations.  ReLU² experts hold two
+weights (LightMoE README, "MoE inference"); its up weight [E, I, H] is the gate half of the
+synthetic W_gu.
 """
 import math
 
@@ -19,19 +21,21 @@ from tests.helpers import bf16_to_f64, dense_layer_fp64, rel_errors, rel_errors_
 ORACLE_MAX_REL = 1.5e-2
 ORACLE_MEAN_REL = 3e-3
 
-VARIANTS = [("swiglu_bounded", 0.75), ("swiglu_oai", 1.0), ("geglu", 0.0), ("reglu", 0.0)]
+VARIANTS = [("swiglu_bounded", 0.75), ("swiglu_oai", 1.0), ("geglu", 0.0), ("reglu", 0.0), ("relu2", 0.0)]
 RAGGED = synthetic.Workload("ragged_T50_H64_I64_E5_k3", 50, 64, 64, 5, 3)
 
 
-def _case(wl):
+def _case(wl, act="swiglu"):
     inp = synthetic.make_inputs(wl)
+    if act == "relu2":  # the two-weight form: the up weight is the gate half of W_gu
+        inp["wgu"] = np.ascontiguousarray(inp["wgu"][:, : wl.I])
     ids, w = oracle.route_topk(inp["logits"], wl.k)
     return inp, ids, w
 
 
 @pytest.mark.parametrize("act,clamp", VARIANTS)
 def test_forward_matches_fp64_dense(act, clamp):
-    inp, ids, w = _case(RAGGED)
+    inp, ids, w = _case(RAGGED, act)
     Y = oracle.forward_tokens(inp["x"], inp["wgu"], inp["wd"], ids, w, act=act, clamp=clamp)
     Yd, _ = dense_layer_fp64(inp["x"], inp["wgu"], inp["wd"], inp["logits"], ids, act=act, clamp=clamp)
     mx, mn = rel_errors(bf16_to_f64(Y), Yd.numpy())
@@ -40,7 +44,7 @@ def test_forward_matches_fp64_dense(act, clamp):
 
 @pytest.mark.parametrize("act,clamp", VARIANTS)
 def test_backward_matches_fp64_autograd(act, clamp):
-    inp, ids, w = _case(RAGGED)
+    inp, ids, w = _case(RAGGED, act)
     dX, dl = oracle.backward_tokens(inp["x"], inp["dy"], inp["wgu"], inp["wd"], ids, w, act=act, clamp=clamp)
     dwgu, dwd = oracle.backward_dw(inp["x"], inp["dy"], inp["wgu"], inp["wd"], ids, w, act=act, clamp=clamp)
     Yd, leaves = dense_layer_fp64(inp["x"], inp["wgu"], inp["wd"], inp["logits"], ids, requires_grad=True,
@@ -56,7 +60,7 @@ def test_backward_matches_fp64_autograd(act, clamp):
 
 @pytest.mark.parametrize("act,clamp", VARIANTS)
 def test_grouped_rows_agree_with_per_token_forward(act, clamp):
-    inp, ids, w = _case(RAGGED)
+    inp, ids, w = _case(RAGGED, act)
     d = oracle.dispatch(ids, w, inp["x"], RAGGED.E)
     rows = np.arange(RAGGED.R, dtype=np.int32)
     _, _, y = oracle.grouped_swiglu_rows(d["x_perm"], d["m_indptr"], inp["wgu"], inp["wd"], d["w_perm"], rows,
@@ -66,16 +70,18 @@ def test_grouped_rows_agree_with_per_token_forward(act, clamp):
     np.testing.assert_array_equal(Yc, Yt)
 
 
-def _one_hot_layer(g_vals, u_vals):
+def _one_hot_layer(g_vals, u_vals, gated=True):
     """One token, one expert, k = 1: x = e_0, W_gu[:, 0] = (g, u), W_d = identity.  Then
-    g, u are exactly the given (bf16) values and Y[n] = bf16(act(g[n], u[n]))."""
+    g, u are exactly the given (bf16) values and Y[n] = bf16(act(g[n], u[n])).  Not gated:
+    W_up[:, 0] = g and Y[n] = bf16(act(g[n]))."""
     I = len(g_vals)
     H = I
     x = np.zeros((1, H), np.float32)
     x[0, 0] = 1.0
-    wgu = np.zeros((1, 2 * I, H), np.float32)
+    wgu = np.zeros((1, 2 * I if gated else I, H), np.float32)
     wgu[0, :I, 0] = g_vals
-    wgu[0, I:, 0] = u_vals
+    if gated:
+        wgu[0, I:, 0] = u_vals
     wd = np.eye(H, I, dtype=np.float32)[None]
     bits = synthetic.f32_to_bf16_bits
     return bits(x), bits(wgu), bits(wd), np.zeros((1, 1), np.int32), np.ones((1, 1), np.float32)
@@ -102,12 +108,15 @@ CLOSED_FORM = [
     ("geglu", 0.0, -2.0, 3.0, _gelu_tanh(-2.0) * 3.0),
     ("reglu", 0.0, -2.0, 5.0, 0.0),
     ("reglu", 0.0, 3.0, 2.0, 6.0),
+    ("relu2", 0.0, 3.0, 0.0, 9.0),
+    ("relu2", 0.0, -2.0, 0.0, 0.0),
+    ("relu2", 0.0, 0.75, 0.0, 0.5625),
 ]
 
 
 @pytest.mark.parametrize("act,clamp,g,u,h", CLOSED_FORM)
 def test_closed_form_values(act, clamp, g, u, h):
-    x, wgu, wd, ids, w = _one_hot_layer([g], [u])
+    x, wgu, wd, ids, w = _one_hot_layer([g], [u], gated=act != "relu2")
     Y = oracle.forward_tokens(x, wgu, wd, ids, w, act=act, clamp=clamp)
     got = float(bf16_to_f64(Y)[0, 0])
     # float evaluation then one bf16 rounding: within one bf16 ulp of the exact value
@@ -125,3 +134,17 @@ def test_unknown_activation_is_rejected():
     inp, ids, w = _case(RAGGED)
     with pytest.raises(ValueError):
         oracle.forward_tokens(inp["x"], inp["wgu"], inp["wd"], ids, w, act="relu3")
+
+
+def test_relu2_gradient_closed_form():
+    """One token, one expert, k = 1, W_d = identity, dY = e_0: dX[0] = 2 relu(g) W_up[0, 0] and
+    dW_up[0, 0] = 2 relu(g) x[0] = 2 relu(g) (x = e_0), both exact in bf16 for these values."""
+    for g, dxv in ((3.0, 6.0 * 3.0), (-2.0, 0.0), (0.5, 1.0 * 0.5)):
+        x, wup, wd, ids, w = _one_hot_layer([g], [0.0], gated=False)
+        dy = synthetic.f32_to_bf16_bits(np.array([[1.0]], np.float32))
+        dX, dl = oracle.backward_tokens(x, dy, wup, wd, ids, w, act="relu2")
+        dwup, dwd = oracle.backward_dw(x, dy, wup, wd, ids, w, act="relu2")
+        assert float(bf16_to_f64(dX)[0, 0]) == dxv
+        assert dwup.shape == (1, 1, 1) and float(bf16_to_f64(dwup)[0, 0, 0]) == 2.0 * max(g, 0.0)
+        assert float(bf16_to_f64(dwd)[0, 0, 0]) == max(g, 0.0) ** 2
+        assert dl[0, 0] == 0.0  # k = 1

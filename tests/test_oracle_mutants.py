@@ -24,7 +24,7 @@ MUTANTS = {
                                  "for (int j = 0; j < k; ++j) {\n      ex[j] = std::exp(l[order[j]] - m);\n      if (j) s += ex[j];"),
     "dispatch_not_stable": ("for (long long s = 0; s < R; ++s) {\n    int e = ids[s];",
                             "for (long long s = R - 1; s >= 0; --s) {\n    int e = ids[s];"),
-    "gate_up_rows_swapped": ("const uint16_t* wg = wgu_e + static_cast<size_t>(n) * H;\n    const uint16_t* wu = wgu_e + static_cast<size_t>(I + n) * H;",
+    "gate_up_rows_swapped": ("const uint16_t* wg = wgu_e + static_cast<size_t>(n) * H;\n    const uint16_t* wu = gated(act) ? wgu_e + static_cast<size_t>(I + n) * H : nullptr;",
                              "const uint16_t* wu = wgu_e + static_cast<size_t>(n) * H;\n    const uint16_t* wg = wgu_e + static_cast<size_t>(I + n) * H;"),
     "silu_sign": ("inline float silu(float a) { return a / (1.0f + std::exp(-a)); }",
                   "inline float silu(float a) { return a / (1.0f + std::exp(a)); }"),
@@ -34,7 +34,7 @@ MUTANTS = {
     "grouped_weight_dropped": ("float_to_bf16(w_perm[r] * o[c]);", "float_to_bf16(o[c]);"),
     "swiglu_grad_sign": ("dg[n] = ((dh * u[n]) * s) * (1.0f + g[n] * (1.0f - s));",
                          "dg[n] = ((dh * u[n]) * s) * (1.0f - g[n] * (1.0f - s));"),
-    "dx_up_term_dropped": ("          acc[h] += du[n] * bf16_to_float(wu[h]);\n", ""),
+    "dx_up_term_dropped": ("          if (wu) acc[h] += du[n] * bf16_to_float(wu[h]);\n", ""),
     "router_grad_sign": ("dl[ids[static_cast<size_t>(t) * k + j]] = wj * (gam[j] - S);",
                          "dl[ids[static_cast<size_t>(t) * k + j]] = wj * (gam[j] + S);"),
     "router_grad_unweighted_gamma": ("for (int j = 0; j < k; ++j) S += w[static_cast<size_t>(t) * k + j] * gam[j];",
@@ -76,6 +76,9 @@ ACT_MUTANTS = {
     "geglu_grad_second_term_dropped": ("const float dgelu = 0.5f * (1.0f + t) + 0.5f * g * (1.0f - t * t) * kGeluK0 * (1.0f + 3.0f * kGeluK1 * g * g);",
                                        "const float dgelu = 0.5f * (1.0f + t);"),
     "reglu_grad_not_gated": ("*dhdg = (g > 0.0f) ? u : 0.0f;", "*dhdg = u;"),
+    "relu2_not_squared": ("      return r * r;\n", "      return r;\n"),
+    "relu2_grad_halved": ("*dhdg = 2.0f * std::max(g, 0.0f);", "*dhdg = std::max(g, 0.0f);"),
+    "relu2_grad_not_gated": ("*dhdg = 2.0f * std::max(g, 0.0f);", "*dhdg = 2.0f * g;"),
 }
 
 
