@@ -56,8 +56,9 @@ def parse_args():
     ap.add_argument("--inputs", choices=["x_perm", "gather"], default="x_perm",
                     help="expert GEMM inputs: expert-major copies (x_perm, dy_perm) read as dense tiles, or the "
                     "memory-lean path that gathers x and dY rows by token inside the GEMMs")
-    ap.add_argument("--act", choices=["swiglu", "swiglu_bounded", "swiglu_oai", "geglu", "reglu"],
-                    default="swiglu", help="gated activation of the expert MLP (x_perm inputs only for the others)")
+    ap.add_argument("--act", choices=["swiglu", "swiglu_bounded", "swiglu_oai", "geglu", "reglu", "relu2"],
+                    default="swiglu", help="activation of the expert MLP (x_perm inputs only for the others; relu2 "
+                    "runs two-weight experts whose up weight is the gate half of the synthetic W_gu)")
     ap.add_argument("--act-clamp", type=float, default=7.0, help="clamp of swiglu_bounded / limit of swiglu_oai")
     args = ap.parse_args()
     if args.act != "swiglu" and args.inputs == "gather":
@@ -78,40 +79,47 @@ def load_peaks() -> dict:
 
 
 # ---------------------------------------------------------------- algorithmic work
-def step_flops(wl) -> dict:
+def step_flops(wl, gated: bool = True) -> dict:
+    """Gated experts: gate/up 4 + down 2 forward; dH 2 + dX 4 + dW_gu 4 + dW_d 2 backward (x R H I).
+    Two-weight (relu2) experts: up 2 + down 2; dH 2 + dX 2 + dW_up 2 + dW_d 2."""
     rhi = wl.R * wl.H * wl.I
-    return dict(fwd=6 * rhi, bwd=12 * rhi, total=18 * rhi)
+    fwd, bwd = (6, 12) if gated else (4, 8)
+    return dict(fwd=fwd * rhi, bwd=bwd * rhi, total=(fwd + bwd) * rhi)
 
 
-def gemm_bytes(wl, name: str, experts_used: int) -> int:
+def gemm_bytes(wl, name: str, experts_used: int, gated: bool = True) -> int:
     """Minimum DRAM bytes of one grouped-GEMM launch: every operand read once and every output
     written once, at its algorithmic precision (bf16 activations and weights, the fp32 SwiGLU
     derivative factors the forward saves; the hi/lo second halves of the weight-gradient
     operands are an implementation choice and are not counted).  Weights count only for
-    experts that received rows."""
+    experts that received rows.  nin = rows of the first weight per expert (2I gated, I relu2)."""
     H, I, E, R = wl.H, wl.I, wl.E, wl.R
-    w_gu = experts_used * 2 * I * H * 2
+    nin = 2 * I if gated else I
+    w_gu = experts_used * nin * H * 2
     w_d = experts_used * H * I * 2
     act_h, act_x = R * H * 2, R * I * 2  # [R, H] and [R, I] bf16
-    factors = R * 2 * I * 4
+    dgu = R * nin * 2
+    factors = R * nin * 4
+    up = act_h + w_gu + act_x + factors  # x_perm, W_gu -> h, factors
     return {
-        "gemm_gate_up_swiglu": act_h + w_gu + act_x + factors,    # x_perm, W_gu -> h, factors
+        "gemm_gate_up_swiglu": up, "gemm_gate_up_glu": up, "gemm_up_relu2": up,
         "gemm_down_scale": act_x + w_d + act_h,                   # h, W_d -> y_perm
-        "gemm_bwd_dh": act_h + w_d + factors + act_x + 2 * act_x + act_x,  # dY rows, W_d, factors, h -> dgu, w h
-        "gemm_bwd_dx": 2 * act_x + w_gu + act_h,                  # dgu, W_gu -> dx_perm
-        "gemm_bwd_dw_gate_up": 2 * act_x + act_h + E * 2 * I * H * 2,  # dgu, x_perm -> dW_gate_up (all experts)
+        "gemm_bwd_dh": act_h + w_d + factors + act_x + dgu + act_x,  # dY rows, W_d, factors, h -> dgu, w h
+        "gemm_bwd_dx": dgu + w_gu + act_h,                        # dgu, W_gu -> dx_perm
+        "gemm_bwd_dw_gate_up": dgu + act_h + E * nin * H * 2,     # dgu, x_perm -> dW_gate_up (all experts)
         "gemm_bwd_dw_down": act_h + act_x + E * H * I * 2,         # dY rows, w h -> dW_down (all experts)
-    }["gemm_gate_up_swiglu" if name == "gemm_gate_up_glu" else name]
+    }[name]
 
 
-def kernel_work(wl, name: str):
+def kernel_work(wl, name: str, gated: bool = True):
     """(kind, algorithmic amount per launch): kind 'flop' for GEMMs, 'byte' for the rest."""
     T, H, I, E, k, R = wl.T, wl.H, wl.I, wl.E, wl.k, wl.R
     rhi = R * H * I
     nunits = math.ceil(R / 256)
-    gemm = {"gemm_gate_up_swiglu": 4 * rhi, "gemm_gate_up_glu": 4 * rhi, "gemm_down_scale": 2 * rhi,
-            "gemm_bwd_dh": 2 * rhi,
-            "gemm_bwd_dx": 4 * rhi, "gemm_bwd_dw_gate_up": 4 * rhi, "gemm_bwd_dw_down": 2 * rhi}
+    g = 2 if gated else 1  # rows of the first weight per expert, in units of I
+    gemm = {"gemm_gate_up_swiglu": 4 * rhi, "gemm_gate_up_glu": 4 * rhi, "gemm_up_relu2": 2 * rhi,
+            "gemm_down_scale": 2 * rhi, "gemm_bwd_dh": 2 * rhi,
+            "gemm_bwd_dx": 2 * g * rhi, "gemm_bwd_dw_gate_up": 2 * g * rhi, "gemm_bwd_dw_down": 2 * rhi}
     if name in gemm:
         return "flop", gemm[name]
     nbytes = {
@@ -199,12 +207,13 @@ def oracle_sample(wl, inp, ids, w, n_tokens: int, experts, act=("swiglu", 0.0)) 
     kw = dict(act=act[0], clamp=act[1])
     oracle.forward_tokens(inp["x"], inp["wgu"], inp["wd"], ids, w, toks=toks, **kw)
     oracle.backward_tokens(inp["x"], inp["dy"], inp["wgu"], inp["wd"], ids, w, toks=toks, **kw)
-    flop = 12 * n_tokens * wl.k * wl.H * wl.I  # fwd (6) + dH (2) + dX (4) per routed row
+    g = 1 if act[0] == "relu2" else 2  # rows of the first weight per expert, in units of I
+    flop = (2 * g + 2 + 2 + 2 * g) * n_tokens * wl.k * wl.H * wl.I  # fwd + dH + dX per routed row
     if len(experts):
         oracle.backward_dw(inp["x"], inp["dy"], inp["wgu"], inp["wd"], ids, w,
                            experts=np.asarray(experts, dtype=np.int32), **kw)
         rows = np.bincount(ids.ravel(), minlength=wl.E)[np.asarray(experts)].sum()
-        flop += 6 * int(rows) * wl.H * wl.I
+        flop += (2 * g + 2) * int(rows) * wl.H * wl.I
     return float(flop)
 
 
@@ -240,6 +249,8 @@ def run_reference(args, rank, world):
 
     wl = synthetic.workload(args.workload)
     inp = synthetic.make_inputs(wl, seed=args.seed)
+    if args.act == "relu2":  # two-weight experts: the up weight is the gate half of W_gu
+        inp["wgu"] = np.ascontiguousarray(inp["wgu"][:, : wl.I])
     ids, w = oracle.route_topk(inp["logits"], wl.k)
     total_steps = args.warmup + args.steps
     per_step = max(0.05, min(5.0, 150.0 / max(total_steps, 1)))
@@ -288,6 +299,10 @@ def run_ours(args, rank, world, local_rank):
     wl = synthetic.workload(args.workload)
     T, H, I, E, k, R = wl.T, wl.H, wl.I, wl.E, wl.k, wl.R
     inp = synthetic.make_inputs(wl, seed=args.seed)
+    gated = args.act != "relu2"
+    if not gated:  # two-weight experts: the up weight W_up [E, I, H] is the gate half of W_gu
+        inp["wgu"] = np.ascontiguousarray(inp["wgu"][:, :I])
+    nin = 2 * I if gated else I  # rows of the first weight per expert
 
     def to_dev(a):
         a = np.ascontiguousarray(a)
@@ -305,9 +320,9 @@ def run_ours(args, rank, world, local_rank):
     gather = args.inputs == "gather"
     if not gather:
         dbuf["x_perm"] = e(R, H)
-    fbuf = dict(h_perm=e(R, I), gu_perm=e(R, 2 * I, dt=f32), y_perm=e(R, H))
+    fbuf = dict(h_perm=e(R, I), gu_perm=e(R, nin, dt=f32), y_perm=e(R, H))
     Y = e(T, H)
-    bbuf = dict(dx=e(T, H), dw_gate_up=e(E, 2 * I, H), dw_down=e(E, H, I), d_logits=e(T, E, dt=f32))
+    bbuf = dict(dx=e(T, H), dw_gate_up=e(E, nin, H), dw_down=e(E, H, I), d_logits=e(T, E, dt=f32))
     ws_d = e(moe.workspace_bytes("dispatch", T=T, E=E, k=k), dt=torch.uint8)
     ws_f = e(moe.workspace_bytes("grouped_swiglu_fwd", R=R, H=H, I=I, E=E), dt=torch.uint8)
     ws_b = e(moe.workspace_bytes("bwd_dx_dw", T=T, H=H, I=I, E=E, k=k, saved_gu=True, gather=gather), dt=torch.uint8)
@@ -334,10 +349,14 @@ def run_ours(args, rank, world, local_rank):
         out = dict(bbuf)
         if dx_out is not None:
             out.update(dx=dx_out, d_logits=dl_out)
-        # the saved derivative factors make the backward the same for every activation
-        bwd = moe.bwd_dx_dw_gather if gather else moe.bwd_dx_dw
-        bwd(dyy, xx if gather else dbuf["x_perm"], fbuf["h_perm"], fbuf["gu_perm"], ids, w, dbuf["m_indptr"],
-            dbuf["row_to_slot"], dbuf["slot_to_row"], dbuf["w_perm"], wgu, wd, out=out, workspace=ws_b)
+        # the saved derivative factors make the backward the same for every gated activation;
+        # two-weight experts (relu2) have their own operand shapes
+        args_b = (dyy, xx if gather else dbuf["x_perm"], fbuf["h_perm"], fbuf["gu_perm"], ids, w, dbuf["m_indptr"],
+                  dbuf["row_to_slot"], dbuf["slot_to_row"], dbuf["w_perm"], wgu, wd)
+        if not gated:
+            moe.bwd_dx_dw_glu(*args_b, args.act, args.act_clamp, out=out, workspace=ws_b)
+        else:
+            (moe.bwd_dx_dw_gather if gather else moe.bwd_dx_dw)(*args_b, out=out, workspace=ws_b)
 
     def step():
         forward(logits, x)
@@ -421,7 +440,7 @@ def run_ours(args, rank, world, local_rank):
     if flags:
         raise RuntimeError(f"device error flags {flags:#x} in the timed region")
 
-    fl = step_flops(wl)
+    fl = step_flops(wl, gated)
     ms_per_step = elapsed_ms / args.steps
     value = world * args.steps * fl["total"] / (elapsed_ms * 1e-3) / 1e12
     tokens_per_s = world * args.steps * T / (elapsed_ms * 1e-3)
@@ -460,19 +479,19 @@ def run_ours(args, rank, world, local_rank):
     # peaks (the dense bf16 rate sustained inside a long step, over the copy bandwidth)
     ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     for name, (n, tot) in sorted(stats.items(), key=lambda kv: -kv[1][1]):
-        kind, amount = kernel_work(wl, name)
+        kind, amount = kernel_work(wl, name, gated)
         avg_s = tot / n * 1e-3
         rate = amount / avg_s if avg_s > 0 else 0.0
         kernels[name] = {"launches": n, "avg_us": round(1e3 * tot / n, 2), "share": round(tot / total_kernel_ms, 4),
                          ("tflops" if kind == "flop" else "gbs"): round(rate / (1e12 if kind == "flop" else 1e9), 1)}
         if kind == "flop":
-            nbytes = gemm_bytes(wl, name, experts_used)
+            nbytes = gemm_bytes(wl, name, experts_used, gated)
             kernels[name]["gbs"] = round(nbytes / avg_s / 1e9, 1) if avg_s > 0 else 0.0
             kernels[name]["flop_per_byte"] = round(amount / nbytes, 1)
     dom = max(stats.items(), key=lambda kv: kv[1][1])[0]
-    kind, amount = kernel_work(wl, dom)
+    kind, amount = kernel_work(wl, dom, gated)
     dom_avg_s = stats[dom][1] / stats[dom][0] * 1e-3
-    if kind == "flop" and amount / gemm_bytes(wl, dom, experts_used) >= ridge:
+    if kind == "flop" and amount / gemm_bytes(wl, dom, experts_used, gated) >= ridge:
         achieved = amount / dom_avg_s / 1e12
         peak = peaks["bf16_tflops_sustained"]
         roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
@@ -480,7 +499,7 @@ def run_ours(args, rank, world, local_rank):
                     "algorithmic_per_launch": amount,
                     "peak_kind": f"bf16 sustained ({peaks['source']}): timed inside a long step"}
     elif kind == "flop":
-        nbytes = gemm_bytes(wl, dom, experts_used)
+        nbytes = gemm_bytes(wl, dom, experts_used, gated)
         achieved = nbytes / dom_avg_s / 1e9
         roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,

@@ -63,16 +63,20 @@ typedef enum {
   LIGER_MOE_ERR_DEVICE = -6              /* returned by liger_moe_device_error when a flag is set */
 } liger_moe_status;
 
-/* Gated activations of the expert MLP, h = act(g, u) with g, u the fp32 gate and up
- * projections.  LightMoE README, "Compatibility" and "Highlights" name the variants; their
- * formulas are the plainest published forms.  A clamp passes the gradient on its closed
- * interval and blocks it outside. */
+/* Activations of the expert MLP, h = act(g, u) with g, u the fp32 gate and up projections.
+ * LightMoE README, "Compatibility" and "Highlights" name the variants; their formulas are the
+ * plainest published forms.  A clamp passes the gradient on its closed interval and blocks it
+ * outside.  LIGER_MOE_ACT_RELU2 is the one non-gated form: its experts hold two weights
+ * (LightMoE README, "MoE inference"), the up weight W_up [E, I, H] taking the place of
+ * w_gate_up, h = max(a, 0)^2 with a = x W_up^T; its saved factor is dh/da, gu_perm [R, I],
+ * and dw_gate_up receives dW_up [E, I, H]. */
 enum liger_moe_activation {
   LIGER_MOE_ACT_SWIGLU = 0,         /* silu(g) u                                             */
   LIGER_MOE_ACT_SWIGLU_BOUNDED = 1, /* silu(min(g, c)) clamp(u, -c, c)          (c = clamp)  */
   LIGER_MOE_ACT_SWIGLU_OAI = 2,     /* gc sigmoid(1.702 gc) (clamp(u, -c, c) + 1), gc = min(g, c) */
   LIGER_MOE_ACT_GEGLU = 3,          /* gelu(g) u, gelu(g) = g/2 (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))) */
-  LIGER_MOE_ACT_REGLU = 4           /* max(g, 0) u                                           */
+  LIGER_MOE_ACT_REGLU = 4,          /* max(g, 0) u                                           */
+  LIGER_MOE_ACT_RELU2 = 5           /* max(a, 0)^2 of one up projection (two-weight experts) */
 };
 
 /* Bits of the device error flag. */
@@ -168,10 +172,12 @@ int liger_moe_grouped_swiglu_fwd(const void* x_perm, const int32_t* m_indptr, co
                                  size_t* workspace_bytes, void* stream);
 
 /*
- * The expert MLP with another gated activation (enum liger_moe_activation) in place of
- * SwiGLU; everything else as liger_moe_grouped_swiglu_fwd.  gu_perm receives that
- * activation's derivative factors [dh/dg | dh/du], so liger_moe_bwd_dx_dw applies to the
- * result unchanged when gu_perm is saved.
+ * The expert MLP with another activation (enum liger_moe_activation) in place of SwiGLU;
+ * everything else as liger_moe_grouped_swiglu_fwd.  gu_perm receives that activation's
+ * derivative factors [dh/dg | dh/du], so for a gated activation liger_moe_bwd_dx_dw applies
+ * to the result unchanged when gu_perm is saved.  LIGER_MOE_ACT_RELU2: w_gate_up is the up
+ * weight W_up [E, I, H] and gu_perm [R, I] receives dh/da (its backward is
+ * liger_moe_bwd_dx_dw_glu with LIGER_MOE_ACT_RELU2).
  *   activation  LIGER_MOE_ACT_*; anything else is LIGER_MOE_ERR_INVALID_ARG.
  *   clamp       c of the bounded SwiGLU and the limit of SwiGLU-OAI: finite and > 0 for those
  *               two (else LIGER_MOE_ERR_INVALID_ARG); ignored by the others.
@@ -246,11 +252,13 @@ int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const void* h_perm, 
                         size_t* workspace_bytes, void* stream);
 
 /*
- * liger_moe_bwd_dx_dw for a layer whose forward used another gated activation
- * (liger_moe_grouped_glu_fwd): the activation and clamp matter only when gu_perm is NULL,
- * where the derivative factors are recomputed; with saved factors the result equals
- * liger_moe_bwd_dx_dw.  Arguments, outputs, limits and workspace otherwise as
- * liger_moe_bwd_dx_dw; activation and clamp are checked as in liger_moe_grouped_glu_fwd.
+ * liger_moe_bwd_dx_dw for a layer whose forward used another activation
+ * (liger_moe_grouped_glu_fwd).  For a gated activation, the activation and clamp matter only
+ * when gu_perm is NULL, where the derivative factors are recomputed; with saved factors the
+ * result equals liger_moe_bwd_dx_dw.  LIGER_MOE_ACT_RELU2 (two-weight experts): w_gate_up is
+ * W_up [E, I, H], gu_perm (saved dh/da) [R, I] or NULL, dw_gate_up receives dW_up [E, I, H].
+ * Arguments, outputs, limits and workspace otherwise as liger_moe_bwd_dx_dw; activation and
+ * clamp are checked as in liger_moe_grouped_glu_fwd.
  */
 int liger_moe_bwd_dx_dw_glu(const void* dy, const void* x_perm, const void* h_perm, const float* gu_perm,
                             const int32_t* topk_ids, const float* topk_w, const int32_t* m_indptr,

@@ -28,8 +28,8 @@ OK = 0
 STATUS = {0: "OK", -1: "INVALID_ARG", -2: "MISALIGNED", -3: "CAPACITY", -4: "UNSUPPORTED_DEVICE", -5: "LAUNCH",
           -6: "DEVICE"}
 DEVERR = {0x1: "BAD_EXPERT_ID", 0x2: "BAD_ROW", 0x4: "BAD_INDPTR", 0x8: "WAIT_TIMEOUT"}
-# enum liger_moe_activation: gated activations of the expert MLP
-ACTIVATIONS = {"swiglu": 0, "swiglu_bounded": 1, "swiglu_oai": 2, "geglu": 3, "reglu": 4}
+# enum liger_moe_activation: activations of the expert MLP (relu2: two-weight, non-gated experts)
+ACTIVATIONS = {"swiglu": 0, "swiglu_bounded": 1, "swiglu_oai": 2, "geglu": 3, "reglu": 4, "relu2": 5}
 
 
 class LigerMoEError(RuntimeError):
@@ -194,17 +194,17 @@ def dispatch(topk_ids, topk_w, x, num_experts, *, out=None, workspace=None, stre
     return o
 
 
-def _fwd_args(R, H, w_gate_up, w_down, m_indptr, w_perm, save_gu, out, workspace, dev):
+def _fwd_args(R, H, w_gate_up, w_down, m_indptr, w_perm, save_gu, out, workspace, dev, gated=True):
     _need(w_gate_up, "w_gate_up", torch.bfloat16)
-    E, two_i, _ = w_gate_up.shape
-    I = two_i // 2
-    _need(w_gate_up, "w_gate_up", torch.bfloat16, (E, 2 * I, H))
+    E, nin, _ = w_gate_up.shape  # gated: [E, 2I, H]; relu2: the up weight [E, I, H]
+    I = nin // 2 if gated else nin
+    _need(w_gate_up, "w_gate_up", torch.bfloat16, (E, 2 * I if gated else I, H))
     _need(w_down, "w_down", torch.bfloat16, (E, H, I))
     _need(m_indptr, "m_indptr", torch.int32, (E + 1,))
     _need(w_perm, "w_perm", torch.float32, (R,))
     out = dict(out or {})
     h = _out(out.get("h_perm"), "h_perm", torch.bfloat16, (R, I), dev)
-    gu = _out(out.get("gu_perm"), "gu_perm", torch.float32, (R, 2 * I), dev) if save_gu else None
+    gu = _out(out.get("gu_perm"), "gu_perm", torch.float32, (R, 2 * I if gated else I), dev) if save_gu else None
     y = _out(out.get("y_perm"), "y_perm", torch.bfloat16, (R, H), dev)
     ws = _workspace(workspace, workspace_bytes("grouped_swiglu_fwd", R=R, H=H, I=I, E=E), dev)
     return E, I, h, gu, y, ws
@@ -232,15 +232,17 @@ def _act_id(activation: str) -> int:
 
 def grouped_glu_fwd(x_perm, m_indptr, w_gate_up, w_down, w_perm, activation="swiglu", clamp=0.0, *, save_gu=True,
                     out=None, workspace=None, stream=None):
-    """The expert MLP with a chosen gated activation (ACTIVATIONS); returns (h_perm, gu_perm, y_perm).
+    """The expert MLP with a chosen activation (ACTIVATIONS); returns (h_perm, gu_perm, y_perm).
 
     gu_perm holds that activation's derivative factors [dh/dg | dh/du]; clamp is the bound of
-    swiglu_bounded and the limit of swiglu_oai.
+    swiglu_bounded and the limit of swiglu_oai.  relu2 (two-weight experts): w_gate_up is the
+    up weight [E, I, H] and gu_perm [R, I] holds dh/da.
     """
     lib = load_library()
     _need(x_perm, "x_perm", torch.bfloat16)
     R, H = x_perm.shape
-    E, I, h, gu, y, ws = _fwd_args(R, H, w_gate_up, w_down, m_indptr, w_perm, save_gu, out, workspace, x_perm.device)
+    E, I, h, gu, y, ws = _fwd_args(R, H, w_gate_up, w_down, m_indptr, w_perm, save_gu, out, workspace, x_perm.device,
+                                   gated=activation != "relu2")
     n = ctypes.c_size_t(ws.numel())
     _check("liger_moe_grouped_glu_fwd", lib.liger_moe_grouped_glu_fwd(
         _ptr(x_perm), _ptr(m_indptr), _ptr(w_gate_up), _ptr(w_down), _ptr(w_perm), R, H, I, E, _act_id(activation),
@@ -286,23 +288,25 @@ def _bwd(fn, dy, x_src, x_name, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row
     T, H = dy.shape
     _need(topk_ids, "topk_ids", torch.int32)
     k = topk_ids.shape[1]
-    E, two_i, _ = w_gate_up.shape
-    I = two_i // 2
+    E, nin, _ = w_gate_up.shape  # gated: [E, 2I, H]; relu2: the up weight [E, I, H]
+    gated = act is None or act[0] != "relu2"
+    I = nin // 2 if gated else nin
+    nin = 2 * I if gated else I
     R = T * k
     x_shape = (T, H) if x_name == "x" else (R, H)
     for t, n, dt, sh in ((x_src, x_name, torch.bfloat16, x_shape), (h_perm, "h_perm", torch.bfloat16, (R, I)),
                          (topk_w, "topk_w", torch.float32, (T, k)), (m_indptr, "m_indptr", torch.int32, (E + 1,)),
                          (row_to_slot, "row_to_slot", torch.int32, (R,)),
                          (slot_to_row, "slot_to_row", torch.int32, (R,)), (w_perm, "w_perm", torch.float32, (R,)),
-                         (w_gate_up, "w_gate_up", torch.bfloat16, (E, 2 * I, H)),
+                         (w_gate_up, "w_gate_up", torch.bfloat16, (E, nin, H)),
                          (w_down, "w_down", torch.bfloat16, (E, H, I))):
         _need(t, n, dt, sh)
     if gu_perm is not None:
-        _need(gu_perm, "gu_perm", torch.float32, (R, 2 * I))
+        _need(gu_perm, "gu_perm", torch.float32, (R, nin))
     dev = dy.device
     out = dict(out or {})
     dx = _out(out.get("dx"), "dx", torch.bfloat16, (T, H), dev)
-    dwgu = _out(out.get("dw_gate_up"), "dw_gate_up", torch.bfloat16, (E, 2 * I, H), dev)
+    dwgu = _out(out.get("dw_gate_up"), "dw_gate_up", torch.bfloat16, (E, nin, H), dev)
     dwd = _out(out.get("dw_down"), "dw_down", torch.bfloat16, (E, H, I), dev)
     dl = _out(out.get("d_logits"), "d_logits", torch.float32, (T, E), dev)
     ws = _workspace(workspace, workspace_bytes("bwd_dx_dw", T=T, H=H, I=I, E=E, k=k, saved_gu=gu_perm is not None,
@@ -325,8 +329,9 @@ def bwd_dx_dw(dy, x_perm, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_sl
 
 def bwd_dx_dw_glu(dy, x_perm, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_slot, slot_to_row, w_perm,
                   w_gate_up, w_down, activation="swiglu", clamp=0.0, *, out=None, workspace=None, stream=None):
-    """bwd_dx_dw for a forward with another gated activation (needed when gu_perm is None: the
-    derivative factors are recomputed with that activation)."""
+    """bwd_dx_dw for a forward with another activation (needed when gu_perm is None: the
+    derivative factors are recomputed with that activation; always for relu2, whose w_gate_up is
+    the up weight [E, I, H], gu_perm [R, I] and dw_gate_up [E, I, H])."""
     return _bwd("liger_moe_bwd_dx_dw_glu", dy, x_perm, "x_perm", h_perm, gu_perm, topk_ids, topk_w, m_indptr,
                 row_to_slot, slot_to_row, w_perm, w_gate_up, w_down, out, workspace, stream, act=(activation, clamp))
 

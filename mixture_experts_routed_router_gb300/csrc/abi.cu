@@ -48,7 +48,7 @@ int check_topk(long long T, int E, int k) {
 
 // activation id and clamp (enum liger_moe_activation)
 int check_activation(int act, float clamp) {
-  if (act < LIGER_MOE_ACT_SWIGLU || act > LIGER_MOE_ACT_REGLU) return LIGER_MOE_ERR_INVALID_ARG;
+  if (act < LIGER_MOE_ACT_SWIGLU || act > LIGER_MOE_ACT_RELU2) return LIGER_MOE_ERR_INVALID_ARG;
   if ((act == LIGER_MOE_ACT_SWIGLU_BOUNDED || act == LIGER_MOE_ACT_SWIGLU_OAI) && !(clamp > 0.f && clamp < 3.0e38f))
     return LIGER_MOE_ERR_INVALID_ARG;
   return LIGER_MOE_OK;
@@ -417,6 +417,7 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
   a.H = H;
   a.I = I;
   a.E = E;
+  a.nin = act == LIGER_MOE_ACT_RELU2 ? I : 2 * I;  // ReLU²: one up weight, one factor, da [.., I]
 
   if (R > 0) {
     if (int rc = launch_tile_schedule(m_indptr, E, R, tile_prefix, pad_indptr, dev, s)) return rc;

@@ -81,10 +81,13 @@ struct Layout {
 enum class Sched : int { RowsM = 0, RowsK = 1 };
 // SwiGLU: the gate/up GEMM with SwiGLU; GLU: the same with the activation chosen at run time
 // (Params::act), kept apart so that the default SwiGLU kernel carries none of the variants' code.
-enum class Epi : int { SwiGLU = 0, ScaleRows = 1, DH = 2, Store = 3, GLU = 4 };
+// ReLU2: the up GEMM of a two-weight (non-gated) expert, h = max(a, 0)^2.  DH1: the dH epilogue
+// of such an expert (one derivative factor, one output instead of [dg | du]).
+enum class Epi : int { SwiGLU = 0, ScaleRows = 1, DH = 2, Store = 3, GLU = 4, ReLU2 = 5, DH1 = 6 };
 constexpr bool gate_up_epi(Epi e) { return e == Epi::SwiGLU || e == Epi::GLU; }
+constexpr bool dh_epi(Epi e) { return e == Epi::DH || e == Epi::DH1; }
 template <Epi EP, int SPLIT>
-using LayoutOf = Layout<EP == Epi::DH ? 1 : 0, SPLIT>;
+using LayoutOf = Layout<dh_epi(EP) ? 1 : 0, SPLIT>;
 
 struct Params {
   const int32_t* m_indptr;     // [E+1]
@@ -103,7 +106,7 @@ struct Params {
   uint16_t* out;
   long long ld_out;
   long long out_expert_stride;
-  uint16_t* out2;         // DH: dgu [2R, 2I] (hi rows, then lo rows)
+  uint16_t* out2;         // DH: dgu [2R, 2I] (hi rows, then lo rows); DH1: da [2R, I]
   float* gu_out;          // SwiGLU: derivative factors [a | b] fp32 [R, 2I] (nullable)
   int act;                // SwiGLU epilogue: gated activation (LIGER_MOE_ACT_*)
   float act_clamp;        // its clamp (bounded SwiGLU) or limit (SwiGLU-OAI)
@@ -372,7 +375,40 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
       }
       if (p.out != nullptr) emit_row(mode, row_ok, tmC0, st, lane, hw, col, y, p.out + r * p.ld_out + col);
     }
-  } else if constexpr (EP == Epi::DH) {
+  } else if constexpr (EP == Epi::ReLU2) {
+    // acc = a = x W_up[e]^T (the expert's one projection); h = r^2 with r = max(a, 0), and the
+    // backward's derivative factor dh/da = 2 r in fp32 ([R, I]).  This warp's output columns:
+    // [128 colhalf, 128 colhalf + 128) of the tile's BN.
+    if (mode == Rows::None) return;
+    const long long r = tl.m0 + row_local;
+    const int y = tl.m0 + sub * 32;
+#pragma unroll 1
+    for (int q = 2 * colhalf; q < 2 * colhalf + 2; ++q) {
+      const int col = tl.nt * BN + q * 64;
+      if (col >= p.I) break;
+      uint32_t hw[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float a[32];
+        tmem_ld32(t_row + q * 64 + half * 32, a);
+        tmem_ld_wait();
+        uint32_t fw[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float rr = fmaxf(a[i], 0.0f);
+          fw[i] = __float_as_uint(2.0f * rr);
+          a[i] = rr * rr;
+        }
+        if (p.gu_out != nullptr) {
+          const int xg = col + half * 32;
+          emit_row(mode, row_ok, tmC1, st, lane, fw, xg, y, p.gu_out + r * p.I + xg);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) hw[half * 16 + i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
+      }
+      if (p.out != nullptr) emit_row(mode, row_ok, tmC0, st, lane, hw, col, y, p.out + r * p.ld_out + col);
+    }
+  } else if constexpr (dh_epi(EP)) {
     // acc = dHu = dY[token] W_d[e] for this row; d = w_r * dHu in fp32.  The saved forward
     // state gives the SwiGLU derivative factors a = dh/dg, b = dh/du (fp32) and h (bf16):
     //   dg = d a,  du = d b,  <d, h> (router-gradient partial),  w_r h (the dW_down operand).
@@ -386,10 +422,13 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
     // Input rows are routed rows r; outputs go to padded rows ro (their expert's padded range).
     // In an expert's last tile the lanes past its rows, up to the next multiple of 16, write
     // zero rows (all inside the slice that holds the expert's last row, since 16 divides 32).
+    // DH1 (two-weight experts, h = max(a, 0)^2): one factor a = dh/da per element ([R, I]) and one
+    // gradient da = d a, written as hi/lo into [2R, I]; four output boxes per 16 columns.
+    constexpr bool kGated = EP == Epi::DH;
     const long long r = tl.m0 + row_local;
     const long long ro = tl.am0 + row_local;
     const bool pad_row = !row_ok && row_local < ((tl.rows + 15) & ~15);
-    const long long two_i = 2LL * p.I;
+    const long long two_i = (kGated ? 2LL : 1LL) * p.I;  // row length of the factors and of dgu
     const int y = tl.am0 + sub * 32;
     const int n0 = tl.nt * BN;
     const int ncols = min(BN, p.I - n0);  // a positive multiple of 64
@@ -402,7 +441,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
     auto load_ops = [&](int n, float (&a)[16], float (&b)[16], float (&h)[16]) {
       if (row_ok) {
         load16_f32(arow + n, a);
-        load16_f32(arow + p.I + n, b);
+        if constexpr (kGated) load16_f32(arow + p.I + n, b);
         load16_bf16(hrow + n, h);
       }
     };
@@ -420,11 +459,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
           const float d = wr * dh[q];
           part += d * h[q];
           v[0][e2] = d * a[q];
-          v[1][e2] = d * b[q];
+          v[1][e2] = kGated ? d * b[q] : 0.f;
           v[2][e2] = wr * h[q];
         }
 #pragma unroll
         for (int f = 0; f < 3; ++f) {
+          if (!kGated && f == 1) continue;
           const uint32_t hi = pack_bf16x2(v[f][0], v[f][1]);
           o[2 * f][i / 2] = hi;
           o[2 * f + 1][i / 2] = pack_bf16x2(v[f][0] - bf16_lo(hi), v[f][1] - bf16_hi(hi));
@@ -438,6 +478,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
         const uint32_t sw = (lane >> 2) & 1;  // 32-byte swizzle: chunk ^= (row >> 2) & 1
 #pragma unroll
         for (int f = 0; f < 6; ++f) {
+          if (!kGated && (f == 2 || f == 3)) continue;
           const uint32_t row_addr = base + f * kDhBoxBytes + lane * 32;
           st_shared_v4(row_addr + ((0 ^ sw) << 4), make_uint4(o[f][0], o[f][1], o[f][2], o[f][3]));
           st_shared_v4(row_addr + ((1 ^ sw) << 4), make_uint4(o[f][4], o[f][5], o[f][6], o[f][7]));
@@ -448,8 +489,10 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
           const int yl = y + static_cast<int>(p.lo_rows);
           tma_store_2d(tmC0, base + 0 * kDhBoxBytes, n, y);
           tma_store_2d(tmC0, base + 1 * kDhBoxBytes, n, yl);
-          tma_store_2d(tmC0, base + 2 * kDhBoxBytes, p.I + n, y);
-          tma_store_2d(tmC0, base + 3 * kDhBoxBytes, p.I + n, yl);
+          if constexpr (kGated) {
+            tma_store_2d(tmC0, base + 2 * kDhBoxBytes, p.I + n, y);
+            tma_store_2d(tmC0, base + 3 * kDhBoxBytes, p.I + n, yl);
+          }
           tma_store_2d(tmC1, base + 4 * kDhBoxBytes, n, y);
           tma_store_2d(tmC1, base + 5 * kDhBoxBytes, n, yl);
           bulk_commit_group();
@@ -466,6 +509,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
                             p.out2 + rl * two_i + p.I + n, p.hw_out + ro * p.I + n, p.hw_out + rl * p.I + n};
 #pragma unroll
         for (int f = 0; f < 6; ++f) {
+          if (!kGated && (f == 2 || f == 3)) continue;
           reinterpret_cast<uint4*>(dst[f])[0] = make_uint4(o[f][0], o[f][1], o[f][2], o[f][3]);
           reinterpret_cast<uint4*>(dst[f])[1] = make_uint4(o[f][4], o[f][5], o[f][6], o[f][7]);
         }
@@ -531,7 +575,8 @@ __device__ __forceinline__ void store_zero_tile(const Tile& tl, int sub, int col
 template <Sched S, Epi EP>
 __device__ __forceinline__ void prefetch_epilogue_operands(int t, int total, int row_local, int colhalf,
                                                            const Params& p) {
-  if constexpr (EP == Epi::DH) {
+  if constexpr (dh_epi(EP)) {
+    constexpr int kFactors = EP == Epi::DH ? 2 : 1;  // [a | b] or a alone per row
     if (t >= total) return;
     const Tile tl = decode_tile<S>(t, p);
     if (row_local >= tl.rows) return;
@@ -539,8 +584,8 @@ __device__ __forceinline__ void prefetch_epilogue_operands(int t, int total, int
     const int n0 = tl.nt * BN + colhalf * (BN / 2);
     const int ncols = min(BN / 2, p.I - n0);
     if (ncols <= 0) return;
-    prefetch_l2_bulk(p.gu_in + r * 2LL * p.I + n0, ncols * 4);
-    prefetch_l2_bulk(p.gu_in + r * 2LL * p.I + p.I + n0, ncols * 4);
+    prefetch_l2_bulk(p.gu_in + r * kFactors * p.I + n0, ncols * 4);
+    if constexpr (kFactors == 2) prefetch_l2_bulk(p.gu_in + r * 2LL * p.I + p.I + n0, ncols * 4);
     prefetch_l2_bulk(p.h_in + r * p.I + n0, ncols * 2);
   }
 }
@@ -1177,8 +1222,35 @@ int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, int32_t* t
 
 int gdot_tiles(int I) { return 2 * cdiv(I, BN); }
 
+// Up GEMM of a two-weight expert (ReLU²): a = x W_up[e]^T over N = I columns in full BN tiles,
+// h = max(a, 0)^2 and the factor dh/da (fp32 [R, I]).
+int launch_up_relu2(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
+  if (a.x != nullptr) return LIGER_MOE_ERR_INVALID_ARG;  // reads x_perm
+  CUtensorMap ta, tb;
+  if (make_tmap(&ta, a.x_perm, a.H, a.R, BK, BM) || make_tmap(&tb, a.w_gate_up, a.H, 1ULL * a.I * a.E, BK, BN))
+    return LIGER_MOE_ERR_LAUNCH;
+  Params p = base_params(a.m_indptr, a.tile_prefix, a.E, dev.err_flag);
+  p.n_tiles = cdiv(a.I, BN);
+  p.num_kb = a.H / BK;
+  p.b_rows_per_expert = a.I;
+  p.N_out = a.I;
+  p.I = a.I;
+  p.out = a.h_perm;
+  p.ld_out = a.I;
+  p.gu_out = a.gu_perm;
+  CUtensorMap tc0, tc1;  // h (bf16) and dh/da (fp32); an absent output reuses the other's map
+  if (a.h_perm != nullptr && make_out_bf16(&tc0, a.h_perm, a.I, a.R)) return LIGER_MOE_ERR_LAUNCH;
+  if (a.gu_perm != nullptr && make_out_f32(&tc1, a.gu_perm, a.I, a.R)) return LIGER_MOE_ERR_LAUNCH;
+  if (a.h_perm == nullptr) tc0 = tc1;
+  if (a.gu_perm == nullptr) tc1 = tc0;
+  if (a.h_perm == nullptr && a.gu_perm == nullptr) return LIGER_MOE_OK;
+  return launch_gemm<Sched::RowsM, Epi::ReLU2, false, false>(ta, tb, tc0, tc1, p, rows_m_tiles(a.R, a.E, p.n_tiles),
+                                                              dev, s, "gemm_up_relu2");
+}
+
 int launch_gate_up(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   if (a.R == 0) return LIGER_MOE_OK;
+  if (a.act == LIGER_MOE_ACT_RELU2) return launch_up_relu2(a, dev, s);
   const bool gather = a.x != nullptr;  // A rows gathered from x [T, H]; else read from x_perm [R, H]
   CUtensorMap ta, tb;
   if ((gather ? make_gather_map(&ta, a.x, a.H, a.T) : make_tmap(&ta, a.x_perm, a.H, a.R, BK, BM)) ||
@@ -1261,11 +1333,15 @@ int launch_bwd_dh(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.hw_out = a.hw_perm;
   p.row_scale = a.w_perm;
   p.gdot = a.gdot;
-  CUtensorMap tc0, tc1;  // dgu [2R, 2I] and hw [2R, I]: hi rows then lo rows
-  if (make_out_bf16_narrow(&tc0, a.dgu, 2ULL * a.I, 2ULL * a.R_pad) ||
+  CUtensorMap tc0, tc1;  // dgu [2R, nin] and hw [2R, I]: hi rows then lo rows
+  if (make_out_bf16_narrow(&tc0, a.dgu, static_cast<uint64_t>(a.nin), 2ULL * a.R_pad) ||
       make_out_bf16_narrow(&tc1, a.hw_perm, a.I, 2ULL * a.R_pad))
     return LIGER_MOE_ERR_LAUNCH;
   const long long tiles = rows_m_tiles(a.R, a.E, p.n_tiles);
+  if (a.nin == a.I) {  // two-weight experts (ReLU²): one factor, one gradient
+    if (gather) return LIGER_MOE_ERR_INVALID_ARG;
+    return launch_gemm<Sched::RowsM, Epi::DH1, false, true>(ta, tb, tc0, tc1, p, tiles, dev, s, "gemm_bwd_dh");
+  }
   if (gather)
     return launch_gemm<Sched::RowsM, Epi::DH, false, true, 0, Gather::A>(ta, tb, tc0, tc1, p, tiles, dev, s,
                                                                         "gemm_bwd_dh");
@@ -1275,15 +1351,15 @@ int launch_bwd_dh(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
 int launch_bwd_dx(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   if (a.R == 0) return LIGER_MOE_OK;
   CUtensorMap ta, tb;
-  if (make_tmap(&ta, a.dgu, 2ULL * a.I, a.R_pad, BK, BM) ||  // hi rows of dgu, padded row space
-      make_tmap(&tb, a.w_gate_up, a.H, 2ULL * a.I * a.E, 64, BK))
+  if (make_tmap(&ta, a.dgu, static_cast<uint64_t>(a.nin), a.R_pad, BK, BM) ||  // hi rows of dgu, padded row space
+      make_tmap(&tb, a.w_gate_up, a.H, 1ULL * a.nin * a.E, 64, BK))
     return LIGER_MOE_ERR_LAUNCH;
   Params p = base_params(a.m_indptr, a.tile_prefix, a.E, dev.err_flag);
   p.pad_indptr = a.pad_indptr;
   p.pad_a = 1;  // A = dgu hi rows in the padded row space
   p.n_tiles = cdiv(a.H, BN);
-  p.num_kb = 2 * a.I / BK;
-  p.b_rows_per_expert = 2 * a.I;
+  p.num_kb = a.nin / BK;
+  p.b_rows_per_expert = a.nin;
   p.N_out = a.H;
   p.I = a.I;
   p.out = a.dx_perm;
@@ -1295,7 +1371,7 @@ int launch_bwd_dx(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
 }
 
 int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
-  // dW_gu[e] = dgu_e^T x_e  ([2I, H]),  dW_d[e] = dY_e^T (w h)_e  ([H, I]); K = rows of e.
+  // dW_gu[e] = dgu_e^T x_e  ([nin, H]),  dW_d[e] = dY_e^T (w h)_e  ([H, I]); K = rows of e.
   // The token-row operands x_e and dY_e are read as dense tiles of x_perm / dy_perm [R, H], or
   // gathered by token from x / dY [T, H] where those copies are absent.  With no rows at all
   // (R = 0) every expert's gradient is zero: the kernel still runs to write the zeros, over
@@ -1309,7 +1385,8 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   // R + r of dgu [2R, 2I]) and one B tile; two MMAs per K step.
   const uint64_t prows = empty ? 1 : static_cast<uint64_t>(a.R_pad);
   p.pad_indptr = a.pad_indptr;
-  if (make_tmap(&ta, empty ? a.dw_gate_up : a.dgu, 2ULL * a.I, 2 * prows, 64, BK)) return LIGER_MOE_ERR_LAUNCH;
+  const uint64_t nin = static_cast<uint64_t>(a.nin);
+  if (make_tmap(&ta, empty ? a.dw_gate_up : a.dgu, nin, 2 * prows, 64, BK)) return LIGER_MOE_ERR_LAUNCH;
   if (gather_x) {
     set_gather(p, a.row_to_slot, a.R, a.k);
     if (empty ? make_gather_map(&tb, a.dw_gate_up, a.H, 1) : make_gather_map(&tb, a.x, a.H, a.T))
@@ -1317,18 +1394,18 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   } else if (make_tmap(&tb, a.x_perm, a.H, rows, 64, BK)) {
     return LIGER_MOE_ERR_LAUNCH;
   }
-  p.m_tiles = cdiv(2LL * a.I, BM);
+  p.m_tiles = cdiv(a.nin, BM);
   p.n_tiles = cdiv(a.H, BN);
   p.a_split_rows = static_cast<int>(a.R_pad);
   p.b_split_rows = 0;
   p.pad_a = 1;  // dgu rows: padded row space (zero rows past each expert)
   p.pad_b = 0;
-  p.M_out = 2 * a.I;
+  p.M_out = a.nin;
   p.N_out = a.H;
   p.out = a.dw_gate_up;
   p.ld_out = a.H;
-  p.out_expert_stride = 2LL * a.I * a.H;
-  if (make_out_bf16_3d(&tc0, a.dw_gate_up, a.H, 2ULL * a.I, a.E)) return LIGER_MOE_ERR_LAUNCH;
+  p.out_expert_stride = static_cast<long long>(a.nin) * a.H;
+  if (make_out_bf16_3d(&tc0, a.dw_gate_up, a.H, nin, a.E)) return LIGER_MOE_ERR_LAUNCH;
   // CTA pairs over neighbouring M blocks share the x tile (multicast) when the M blocks pair up
   const long long tiles_gu = static_cast<long long>(a.E) * p.m_tiles * p.n_tiles;
   int rc;

@@ -91,7 +91,7 @@ struct BwdGemmArgs {
   const int32_t* row_to_slot;  // [R]; token of row r = row_to_slot[r] / k
   int T, k;
   const uint16_t* h_perm;
-  const float* gu;       // [R, 2I] fp32 [dh/dg | dh/du] (saved or recomputed)
+  const float* gu;       // [R, nin] fp32 [dh/dg | dh/du] (saved or recomputed); ReLU²: dh/da
   const float* w_perm;   // [R]
   // Weight-gradient operands in the padded row space: expert e's rows start at pad_indptr[e]
   // and are followed by zero rows up to a multiple of 16; R_pad (>= pad_indptr[E]) is the
@@ -106,6 +106,9 @@ struct BwdGemmArgs {
   uint16_t* dw_down;     // [E, H, I]
   long long R;
   int H, I, E;
+  // rows of the first weight per expert: 2I (gated: W_gu, factors [dh/dg | dh/du], dgu [.., 2I],
+  // dW_gu [E, 2I, H]) or I (ReLU²: W_up, one factor dh/da, da [.., I], dW_up [E, I, H])
+  int nin = 0;
 };
 int gdot_tiles(int I);
 int launch_bwd_dh(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s);

@@ -153,10 +153,10 @@ def test_glu_entry_points_validate_the_activation(lib):
     assert lib.liger_moe_grouped_swiglu_fwd(D, D, D, D, D, 1024, 256, 128, 8, D, None, D, None, ctypes.byref(n),
                                             None) == OK
     assert n.value == q  # same workspace for every activation
-    for act, clamp in ((3, 0.0), (4, 0.0), (1, 7.0), (2, 7.0)):
+    for act, clamp in ((3, 0.0), (4, 0.0), (1, 7.0), (2, 7.0), (5, 0.0)):
         assert fwd(act, clamp) == OK
     # unknown ids; bounded variants need a finite positive clamp
-    for act, clamp in ((-1, 0.0), (5, 0.0), (1, 0.0), (2, -1.0), (1, float("inf")), (2, float("nan"))):
+    for act, clamp in ((-1, 0.0), (6, 0.0), (1, 0.0), (2, -1.0), (1, float("inf")), (2, float("nan"))):
         assert fwd(act, clamp) == INVALID, (act, clamp)
     g = lib.liger_moe_bwd_dx_dw_glu
     # (dy, x_perm, h, gu, ids, w, indptr, r2s, s2r, w_perm, w_gu, w_d, T, H, I, E, k, act, clamp, dx, dwgu, dwd,

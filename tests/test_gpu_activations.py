@@ -1,4 +1,5 @@
-"""GPU parity of the gated-activation variants (bounded SwiGLU, SwiGLU-OAI, GeGLU, ReGLU) against the oracle.
+"""GPU parity of the activation variants (bounded SwiGLU, SwiGLU-OAI, GeGLU, ReGLU, and the two-weight
+ReLU² experts) against the oracle.
 
 LightMoE README, "Compatibility" / "Highlights" name the variants.  The CUDA path runs them through
 liger_moe_grouped_glu_fwd (the gate/up epilogue computes h and the fp32 derivative factors
@@ -134,3 +135,72 @@ def test_glu_entry_with_swiglu_is_the_swiglu_path_bitwise():
     d = a["d"]
     h, gu, y = moe.grouped_swiglu_fwd(d["x_perm"], d["m_indptr"], a["wgu"], a["wd"], d["w_perm"])
     assert torch.equal(a["h"], h) and torch.equal(a["gu"], gu) and torch.equal(a["y_perm"], y)
+
+
+# ------------------------------------------------------------------ ReLU² (two-weight experts)
+# LightMoE README, "MoE inference": ReLU² experts hold an up and a down weight, no gate.  The up
+# weight W_up [E, I, H] takes the place of W_gate_up; here it is the gate half of the synthetic
+# W_gu (same N(0, 1/sqrt(H)) init).  gu_perm [R, I] holds dh/da = 2 max(a, 0).
+
+
+def _relu2_inputs(wl):
+    inp = synthetic.make_inputs(wl)
+    inp["wgu"] = np.ascontiguousarray(inp["wgu"][:, : wl.I])
+    return inp
+
+
+@pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
+def test_relu2_forward_parity(wl):
+    inp = _relu2_inputs(wl)
+    g = _forward(wl, inp, "relu2", 0.0)
+    assert moe.device_error() == 0
+    assert tuple(g["gu"].shape) == (wl.R, wl.I)
+    ids, w = oracle.route_topk(inp["logits"], wl.k)
+    ref = oracle.dispatch(ids, w, inp["x"], wl.E)
+    rows = np.arange(wl.R, dtype=np.int32)
+    h, a, y = oracle.grouped_swiglu_rows(ref["x_perm"], ref["m_indptr"], inp["wgu"], inp["wd"],
+                                         to_host(g["d"]["w_perm"]), rows, act="relu2")
+    assert_close(bf16_to_f64(to_host(g["h"])), bf16_to_f64(h), "h_perm[relu2]")
+    # dh/da = 2 max(a, 0) at the oracle's fp32 a; elements within rounding of a = 0 may take either side
+    a64 = a.astype(np.float64)
+    keep = np.abs(a64) > 1e-3 * np.abs(a64).max()
+    assert keep.mean() > 0.99
+    got_f, ref_f = to_host(g["gu"]).astype(np.float64), 2.0 * np.maximum(a64, 0.0)
+    assert_close(got_f[keep], ref_f[keep], "gu_perm[relu2]", max_rel=1e-3, mean_rel=1e-4)
+    assert np.all(got_f[keep & (a64 < 0)] == 0)
+    assert 0.3 < (a64 < 0).mean() < 0.7  # both branches of the ReLU are exercised
+    assert_close(bf16_to_f64(to_host(g["y_perm"])), bf16_to_f64(y), "y_perm[relu2]")
+    Y = oracle.forward_tokens(inp["x"], inp["wgu"], inp["wd"], ids, w, act="relu2")
+    assert_close(bf16_to_f64(to_host(g["Y"])), bf16_to_f64(Y), "Y[relu2]")
+
+
+@pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
+@pytest.mark.parametrize("save_gu", [True, False], ids=["saved_gu", "recomputed_gu"])
+def test_relu2_backward_parity(wl, save_gu):
+    inp = _relu2_inputs(wl)
+    g = _forward(wl, inp, "relu2", 0.0, save_gu=save_gu)
+    d = g["d"]
+    dx, dwup, dwd, dl = moe.bwd_dx_dw_glu(to_dev(inp["dy"]), d["x_perm"], g["h"], g["gu"], g["ids"], g["w"],
+                                          d["m_indptr"], d["row_to_slot"], d["slot_to_row"], d["w_perm"], g["wgu"],
+                                          g["wd"], "relu2")
+    assert moe.device_error() == 0
+    assert tuple(dwup.shape) == (wl.E, wl.I, wl.H)
+    ids, w = oracle.route_topk(inp["logits"], wl.k)
+    rdx, rdl = oracle.backward_tokens(inp["x"], inp["dy"], inp["wgu"], inp["wd"], ids, w, act="relu2")
+    rdwup, rdwd = oracle.backward_dw(inp["x"], inp["dy"], inp["wgu"], inp["wd"], ids, w, act="relu2")
+    assert_close(bf16_to_f64(to_host(dx)), bf16_to_f64(rdx), "dX[relu2]")
+    dl_h = to_host(dl)
+    assert_close(dl_h, rdl, "d_logits[relu2]")
+    assert np.all(dl_h[rdl == 0] == 0)
+    assert_close(bf16_to_f64(to_host(dwup)), bf16_to_f64(rdwup), "dW_up[relu2]", per_expert=True)
+    assert_close(bf16_to_f64(to_host(dwd)), bf16_to_f64(rdwd), "dW_down[relu2]", per_expert=True)
+
+
+def test_relu2_rejects_a_gated_weight_shape():
+    """The binding checks W_up's shape against I from W_down: a [E, 2I, H] weight is refused for relu2."""
+    wl = CASES[0]
+    inp = synthetic.make_inputs(wl)
+    ids, w = moe.route_topk(to_dev(inp["logits"]), wl.k)
+    d = moe.dispatch(ids, w, to_dev(inp["x"]), wl.E)
+    with pytest.raises(ValueError):
+        moe.grouped_glu_fwd(d["x_perm"], d["m_indptr"], to_dev(inp["wgu"]), to_dev(inp["wd"]), d["w_perm"], "relu2")
