@@ -56,9 +56,11 @@ def open_library(path: str):
     lib.oracle_forward_tokens.argtypes = [P, P, P, P, P, I, I, I, I, I, P, I, P, I, F, I]
     lib.oracle_backward_tokens.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, I, P, P, I, F, I]
     lib.oracle_backward_dw.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, I, P, P, I, F, I]
+    lib.oracle_router_logits.argtypes = [P, P, P, I, I, I, P, I]
+    lib.oracle_router_backward.argtypes = [P, P, P, P, I, I, I, P, I, P, P, I, P, P, I]
     for f in (lib.oracle_route_topk, lib.oracle_dispatch, lib.oracle_grouped_swiglu_rows,
               lib.oracle_combine, lib.oracle_forward_tokens, lib.oracle_backward_tokens,
-              lib.oracle_backward_dw):
+              lib.oracle_backward_dw, lib.oracle_router_logits, lib.oracle_router_backward):
         f.restype = ctypes.c_int
     return lib
 
@@ -247,3 +249,43 @@ def backward_dw(x, dy, wgu, wd, ids, w, experts=None, threads=None, act="swiglu"
                                     threads or default_threads())
     _check(rc, "backward_dw")
     return dwgu, dwd
+
+
+def router_logits(x, wr, bias=None, threads=None):
+    """Router projection logits = x Wr^T + bias (float32 [T, E]); bias float32 [E] or None."""
+    x, wr = _c(x, np.uint16), _c(wr, np.uint16)
+    T, H = x.shape
+    E = wr.shape[0]
+    if wr.shape != (E, H):
+        raise ValueError("wr must be [E, H]")
+    b = None if bias is None else _c(bias, np.float32)
+    out = np.empty((T, E), np.float32)
+    rc = _load().oracle_router_logits(x.ctypes.data, wr.ctypes.data, _ptr(b), T, H, E, out.ctypes.data,
+                                      threads or default_threads())
+    _check(rc, "router_logits")
+    return out
+
+
+def router_backward(d_logits, x, wr, dx_in=None, toks=None, experts=None, threads=None):
+    """(dX bf16 [n, H] = bf16(dx_in + d_logits Wr) for the listed tokens, dWr bf16 [m, H] and
+    dbias float32 [m] for the listed experts); d_logits float32 [T, E] is used densely."""
+    dl = _c(d_logits, np.float32)
+    x, wr = _c(x, np.uint16), _c(wr, np.uint16)
+    T, H = x.shape
+    E = wr.shape[0]
+    if dl.shape != (T, E) or wr.shape != (E, H):
+        raise ValueError("d_logits must be [T, E] and wr [E, H]")
+    base = None if dx_in is None else _c(dx_in, np.uint16)
+    if base is not None and base.shape != (T, H):
+        raise ValueError("dx_in must be [T, H]")
+    toks = np.arange(T, dtype=np.int32) if toks is None else _c(toks, np.int32)
+    experts = np.arange(E, dtype=np.int32) if experts is None else _c(experts, np.int32)
+    dx = np.empty((toks.size, H), np.uint16)
+    dwr = np.empty((experts.size, H), np.uint16)
+    db = np.empty(experts.size, np.float32)
+    rc = _load().oracle_router_backward(dl.ctypes.data, x.ctypes.data, wr.ctypes.data, _ptr(base), T, H, E,
+                                        toks.ctypes.data, toks.size, dx.ctypes.data, experts.ctypes.data,
+                                        experts.size, dwr.ctypes.data, db.ctypes.data,
+                                        threads or default_threads())
+    _check(rc, "router_backward")
+    return dx, dwr, db

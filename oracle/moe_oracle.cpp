@@ -29,6 +29,11 @@
 //     written out below in its plainest published form (see act_forward).
 //     ReLU² is the one non-gated form: its experts hold two weights (up
 //     and down, LightMoE README, "MoE inference"), h = max(a, 0)^2.
+//   * The router projection that produces the logits, and its backward
+//     (oracle_router_logits, oracle_router_backward).  LightMoE README, "MoE
+//     training", leaves the routing policy to the host framework; its
+//     plainest form is one linear layer, logits = x Wr^T + b, whose input
+//     gradient adds to the layer's dX.
 // Readings where the pages are silent (tie order, gate/up row order,
 // rounding points, softmax over the selected k) are spelled out at each
 // function.  Arithmetic is float (fp32) with bf16 inputs widened exactly;
@@ -575,6 +580,77 @@ int oracle_backward_dw(const uint16_t* x, const uint16_t* dy, const uint16_t* wg
       for (size_t q = 0; q < ad.size(); ++q) o[q] = float_to_bf16(ad[q]);
     }
   });
+  return ORACLE_OK;
+}
+
+
+// ---------------------------------------------------------------------------
+// Router projection (the linear layer in front of route_topk; LightMoE README,
+// "MoE training": routing policy belongs to the host framework, whose
+// plainest router is one bias-optional linear layer).
+//   logits[t, e] = ( sum_h x[t, h] * Wr[e, h] ) + bias[e]
+// float, h ascending, the bias added once after the sum (bias may be NULL).
+int oracle_router_logits(const uint16_t* x, const uint16_t* wr, const float* bias, int T, int H, int E,
+                         float* logits, int threads) {
+  if (T < 0 || H < 1 || E < 1) return ORACLE_BAD_ARG;
+  parallel_for(T, threads, [&](int t) {
+    const uint16_t* xr = x + static_cast<size_t>(t) * H;
+    for (int e = 0; e < E; ++e) {
+      const uint16_t* we = wr + static_cast<size_t>(e) * H;
+      float acc = 0.0f;
+      for (int h = 0; h < H; ++h) acc += bf16_to_float(xr[h]) * bf16_to_float(we[h]);
+      logits[static_cast<size_t>(t) * E + e] = bias ? acc + bias[e] : acc;
+    }
+  });
+  return ORACLE_OK;
+}
+
+// Backward of the router projection for an upstream gradient d_logits [T, E]
+// (dense: every entry is used).  With L the layer loss:
+//   dX[t, h]  = bf16( float(dx_in[t, h]) + sum_e d_logits[t, e] * Wr[e, h] )
+//               (the router's input gradient added to the layer's dX, dx_in;
+//                the sum over e ascending is formed first; dx_in may be NULL = 0)
+//   dWr[e, h] = bf16( sum_t d_logits[t, e] * x[t, h] )      t ascending
+//   dbias[e]  = sum_t d_logits[t, e]                          t ascending
+// for the listed tokens (dx_out [ntok, H]) and experts (dwr_out [nexp, H],
+// dbias_out [nexp]); any output may be NULL.
+int oracle_router_backward(const float* dlogits, const uint16_t* x, const uint16_t* wr, const uint16_t* dx_in,
+                           int T, int H, int E, const int32_t* toks, int ntok, uint16_t* dx_out,
+                           const int32_t* experts, int nexp, uint16_t* dwr_out, float* dbias_out, int threads) {
+  if (T < 0 || H < 1 || E < 1 || ntok < 0 || nexp < 0) return ORACLE_BAD_ARG;
+  for (int i = 0; i < ntok; ++i)
+    if (toks[i] < 0 || toks[i] >= T) return ORACLE_BAD_ARG;
+  for (int i = 0; i < nexp; ++i)
+    if (experts[i] < 0 || experts[i] >= E) return ORACLE_BAD_ARG;
+  if (dx_out)
+    parallel_for(ntok, threads, [&](int i) {
+      const int t = toks[i];
+      std::vector<float> acc(H, 0.0f);
+      const float* dl = dlogits + static_cast<size_t>(t) * E;
+      for (int e = 0; e < E; ++e) {
+        const uint16_t* we = wr + static_cast<size_t>(e) * H;
+        for (int h = 0; h < H; ++h) acc[h] += dl[e] * bf16_to_float(we[h]);
+      }
+      for (int h = 0; h < H; ++h) {
+        const float base = dx_in ? bf16_to_float(dx_in[static_cast<size_t>(t) * H + h]) : 0.0f;
+        dx_out[static_cast<size_t>(i) * H + h] = float_to_bf16(base + acc[h]);
+      }
+    });
+  if (dwr_out || dbias_out)
+    parallel_for(nexp, threads, [&](int i) {
+      const int e = experts[i];
+      std::vector<float> acc(H, 0.0f);
+      float db = 0.0f;
+      for (int t = 0; t < T; ++t) {
+        const float d = dlogits[static_cast<size_t>(t) * E + e];
+        const uint16_t* xr = x + static_cast<size_t>(t) * H;
+        for (int h = 0; h < H; ++h) acc[h] += d * bf16_to_float(xr[h]);
+        db += d;
+      }
+      if (dwr_out)
+        for (int h = 0; h < H; ++h) dwr_out[static_cast<size_t>(i) * H + h] = float_to_bf16(acc[h]);
+      if (dbias_out) dbias_out[i] = db;
+    });
   return ORACLE_OK;
 }
 

@@ -146,15 +146,20 @@ def zipf_bias(E: int, s: float, seed: int) -> np.ndarray:
 
 
 def make_inputs(w: Workload, seed: int = 0, want=("x", "logits", "wgu", "wd", "dy")) -> dict:
-    """All inputs of one workload as numpy arrays (bf16 as uint16 bits)."""
+    """All inputs of one workload as numpy arrays (bf16 as uint16 bits).  ``"wr"`` in ``want``
+    adds the router weight ``wr`` and bias ``bias`` (float32 [E], or None without a Zipf skew)."""
     out: dict = {}
     need_x = "x" in want or "logits" in want
     if need_x:
         out["x"] = normal_bf16((w.T, w.H), seed, STREAM_X, 1.0)
-    if "logits" in want:
+    if "logits" in want or "wr" in want:
         wr = normal_bf16((w.E, w.H), seed, STREAM_WR, w.router_std)
         bias = zipf_bias(w.E, w.zipf_s, seed) if w.zipf_s is not None else None
-        out["logits"] = router_logits(out["x"], wr, bias)
+        if "logits" in want:
+            out["logits"] = router_logits(out["x"], wr, bias)
+        if "wr" in want:  # the router weight and (Zipf workload) bias themselves, as inputs
+            out["wr"] = wr
+            out["bias"] = None if bias is None else bias.astype(np.float32)
     if "wgu" in want:
         out["wgu"] = normal_bf16((w.E, 2 * w.I, w.H), seed, STREAM_WGU, 1.0 / math.sqrt(w.H))
     if "wd" in want:

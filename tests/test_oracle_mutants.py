@@ -2,7 +2,7 @@
 
 Each case plants one mistake in a temporary copy of the oracle source (never
 in the real one), compiles it on the CPU, and runs the pin battery of
-test_oracle_route / _dispatch / _layer against it: at least one pin must fail.
+test_oracle_route / _dispatch / _layer / _activations / _router against it: at least one pin must fail.
 """
 import os
 import shutil
@@ -14,6 +14,7 @@ from tests import test_oracle_activations as P_A
 from tests import test_oracle_dispatch as P_D
 from tests import test_oracle_layer as P_L
 from tests import test_oracle_route as P_R
+from tests import test_oracle_router as P_RP
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.cpp")
 
@@ -93,6 +94,34 @@ def _act_battery():
 def test_battery_passes_on_the_real_oracle():
     _battery()
     _act_battery()
+    _router_battery()
+
+
+# Mistakes in the router projection and its backward, caught by the router pins.
+ROUTER_MUTANTS = {
+    "router_bias_dropped": ("logits[static_cast<size_t>(t) * E + e] = bias ? acc + bias[e] : acc;",
+                            "logits[static_cast<size_t>(t) * E + e] = acc;"),
+    "router_logits_sum_short": ("for (int h = 0; h < H; ++h) acc += bf16_to_float(xr[h]) * bf16_to_float(we[h]);",
+                                "for (int h = 0; h < H - 1; ++h) acc += bf16_to_float(xr[h]) * bf16_to_float(we[h]);"),
+    "router_dx_in_dropped": ("const float base = dx_in ? bf16_to_float(dx_in[static_cast<size_t>(t) * H + h]) : 0.0f;",
+                             "const float base = 0.0f;"),
+    "router_dx_weight_transposed": ("for (int h = 0; h < H; ++h) acc[h] += dl[e] * bf16_to_float(we[h]);",
+                                    "for (int h = 0; h < H; ++h) acc[h] += dl[e] * bf16_to_float(wr[static_cast<size_t>(h) * E + e]);"),
+    "router_dwr_wrong_operand": ("for (int h = 0; h < H; ++h) acc[h] += d * bf16_to_float(xr[h]);",
+                                 "for (int h = 0; h < H; ++h) acc[h] += d * bf16_to_float(wr[static_cast<size_t>(e) * H + h]);"),
+    "router_dbias_sign": ("        db += d;\n", "        db -= d;\n"),
+}
+
+
+def _router_battery():
+    for shape in P_RP.SHAPES:
+        P_RP.test_logits_match_fp64_within_summation_bound(*shape, True)
+        P_RP.test_backward_matches_fp64_autograd_dense(*shape, True)
+    P_RP.test_logits_equal_the_input_recipe_sum()
+    P_RP.test_closed_form_values()
+    for wl in P_RP.LAYERS:
+        P_RP.test_layer_with_router_matches_fp64_autograd(wl)
+    P_RP.test_top1_routing_gives_no_router_gradient()
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
@@ -120,4 +149,18 @@ def test_planted_activation_mistake_is_caught(name, tmp_path):
     with oracle.using(lib):
         with pytest.raises((AssertionError, ValueError)):
             _act_battery()
+    shutil.rmtree(tmp_path, ignore_errors=True)
+
+
+@pytest.mark.parametrize("name", sorted(ROUTER_MUTANTS))
+def test_planted_router_mistake_is_caught(name, tmp_path):
+    before, after = ROUTER_MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(before) == 1, f"mutation anchor for {name} not found exactly once"
+    path = tmp_path / "mutant.cpp"
+    path.write_text(src.replace(before, after))
+    lib = oracle.open_library(oracle.compile_source(str(path), str(tmp_path / "libmutant.so")))
+    with oracle.using(lib):
+        with pytest.raises((AssertionError, ValueError)):
+            _router_battery()
     shutil.rmtree(tmp_path, ignore_errors=True)
