@@ -60,6 +60,9 @@ def parse_args():
                     default="swiglu", help="activation of the expert MLP (x_perm inputs only for the others; relu2 "
                     "runs two-weight experts whose up weight is the gate half of the synthetic W_gu)")
     ap.add_argument("--act-clamp", type=float, default=7.0, help="clamp of swiglu_bounded / limit of swiglu_oai")
+    ap.add_argument("--router", action="store_true", help="start the step from x: the router projection "
+                    "logits = x Wr^T (+ bias) runs on the GPU, and its backward adds the router's dX and gives "
+                    "dWr, dbias (default: the logits are the layer's input)")
     args = ap.parse_args()
     if args.act != "swiglu" and args.inputs == "gather":
         ap.error("--act other than swiglu runs on x_perm inputs")
@@ -79,12 +82,18 @@ def load_peaks() -> dict:
 
 
 # ---------------------------------------------------------------- algorithmic work
-def step_flops(wl, gated: bool = True) -> dict:
+def step_flops(wl, gated: bool = True, router: bool = False) -> dict:
     """Gated experts: gate/up 4 + down 2 forward; dH 2 + dX 4 + dW_gu 4 + dW_d 2 backward (x R H I).
-    Two-weight (relu2) experts: up 2 + down 2; dH 2 + dX 2 + dW_up 2 + dW_d 2."""
+    Two-weight (relu2) experts: up 2 + down 2; dH 2 + dX 2 + dW_up 2 + dW_d 2.
+    With the router projection: 2 T H E forward (x Wr^T); 4 R H backward (its dX and dWr, each one
+    multiply-add per selected (token, expert) pair and column: d_logits vanish off the top-k)."""
     rhi = wl.R * wl.H * wl.I
     fwd, bwd = (6, 12) if gated else (4, 8)
-    return dict(fwd=fwd * rhi, bwd=bwd * rhi, total=(fwd + bwd) * rhi)
+    fwd, bwd = fwd * rhi, bwd * rhi
+    if router:
+        fwd += 2 * wl.T * wl.H * wl.E
+        bwd += 4 * wl.R * wl.H
+    return dict(fwd=fwd, bwd=bwd, total=fwd + bwd)
 
 
 def gemm_bytes(wl, name: str, experts_used: int, gated: bool = True) -> int:
@@ -108,6 +117,7 @@ def gemm_bytes(wl, name: str, experts_used: int, gated: bool = True) -> int:
         "gemm_bwd_dx": dgu + w_gu + act_h,                        # dgu, W_gu -> dx_perm
         "gemm_bwd_dw_gate_up": dgu + act_h + E * nin * H * 2,     # dgu, x_perm -> dW_gate_up (all experts)
         "gemm_bwd_dw_down": act_h + act_x + E * H * I * 2,         # dY rows, w h -> dW_down (all experts)
+        "gemm_router_logits": wl.T * H * 2 + E * H * 2 + wl.T * E * 4,  # x, Wr -> logits (fp32)
     }[name]
 
 
@@ -119,7 +129,8 @@ def kernel_work(wl, name: str, gated: bool = True):
     g = 2 if gated else 1  # rows of the first weight per expert, in units of I
     gemm = {"gemm_gate_up_swiglu": 4 * rhi, "gemm_gate_up_glu": 4 * rhi, "gemm_up_relu2": 2 * rhi,
             "gemm_down_scale": 2 * rhi, "gemm_bwd_dh": 2 * rhi,
-            "gemm_bwd_dx": 2 * g * rhi, "gemm_bwd_dw_gate_up": 2 * g * rhi, "gemm_bwd_dw_down": 2 * rhi}
+            "gemm_bwd_dx": 2 * g * rhi, "gemm_bwd_dw_gate_up": 2 * g * rhi, "gemm_bwd_dw_down": 2 * rhi,
+            "gemm_router_logits": 2 * T * H * E}
     if name in gemm:
         return "flop", gemm[name]
     nbytes = {
@@ -132,6 +143,8 @@ def kernel_work(wl, name: str, gated: bool = True):
         "combine": R * H * 2 + T * H * 2 + R * 4,
         "router_grad": T * E * 4 + R * (4 * math.ceil(I / 256) + 12),
         "tile_schedule": (E + 1) * 8,
+        "router_dx": 2 * T * H * 2 + E * H * 2 + T * k * 8,        # dX read + written, Wr, ids + d_logits
+        "router_dw": T * H * 2 + E * H * 2 + R * 8 + E * 8,         # x, dWr, row_to_slot + d_logits, m_indptr
     }
     return "byte", nbytes.get(name, 0)
 
@@ -197,18 +210,24 @@ def gpu_index_for(local_rank: int) -> str:
 
 
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
-def oracle_sample(wl, inp, ids, w, n_tokens: int, experts, act=("swiglu", 0.0)) -> float:
-    """Runs the oracle's fwd + bwd on n_tokens tokens and dW on `experts`; returns algorithmic flop."""
+def oracle_sample(wl, inp, ids, w, n_tokens: int, experts, act=("swiglu", 0.0), router=False) -> float:
+    """Runs the oracle's fwd + bwd on n_tokens tokens and dW on `experts` (with `router`, also the
+    router projection of those tokens and its backward); returns algorithmic flop."""
     import numpy as np
 
     import oracle
 
     toks = np.arange(n_tokens, dtype=np.int32)
     kw = dict(act=act[0], clamp=act[1])
+    if router:
+        oracle.router_logits(inp["x"][:n_tokens], inp["wr"], inp["bias"])
     oracle.forward_tokens(inp["x"], inp["wgu"], inp["wd"], ids, w, toks=toks, **kw)
-    oracle.backward_tokens(inp["x"], inp["dy"], inp["wgu"], inp["wd"], ids, w, toks=toks, **kw)
+    dx, dl = oracle.backward_tokens(inp["x"], inp["dy"], inp["wgu"], inp["wd"], ids, w, toks=toks, **kw)
     g = 1 if act[0] == "relu2" else 2  # rows of the first weight per expert, in units of I
     flop = (2 * g + 2 + 2 + 2 * g) * n_tokens * wl.k * wl.H * wl.I  # fwd + dH + dX per routed row
+    if router:
+        oracle.router_backward(dl, inp["x"][:n_tokens], inp["wr"], dx)
+        flop += 2 * n_tokens * wl.H * wl.E + 4 * n_tokens * wl.k * wl.H
     if len(experts):
         oracle.backward_dw(inp["x"], inp["dy"], inp["wgu"], inp["wd"], ids, w,
                            experts=np.asarray(experts, dtype=np.int32), **kw)
@@ -217,7 +236,7 @@ def oracle_sample(wl, inp, ids, w, n_tokens: int, experts, act=("swiglu", 0.0)) 
     return float(flop)
 
 
-def size_oracle_sample(wl, inp, ids, w, seconds: float, act=("swiglu", 0.0)):
+def size_oracle_sample(wl, inp, ids, w, seconds: float, act=("swiglu", 0.0), router=False):
     """Tokens / experts for a sample of about `seconds` of oracle work (one calibration call)."""
     import numpy as np
 
@@ -225,7 +244,7 @@ def size_oracle_sample(wl, inp, ids, w, seconds: float, act=("swiglu", 0.0)):
 
     n_cal = min(wl.T, 2 * oracle.default_threads())  # enough tokens to engage every thread
     t0 = time.perf_counter()
-    oracle_sample(wl, inp, ids, w, n_cal, [], act)
+    oracle_sample(wl, inp, ids, w, n_cal, [], act, router)
     per_tok = max((time.perf_counter() - t0) / n_cal, 1e-6)
     n_tok = int(max(1, min(wl.T, seconds * 0.7 / per_tok)))
     # dW runs one expert per thread: up to `threads` mid-size experts whose largest row count
@@ -248,13 +267,13 @@ def run_reference(args, rank, world):
     import synthetic
 
     wl = synthetic.workload(args.workload)
-    inp = synthetic.make_inputs(wl, seed=args.seed)
+    inp = synthetic.make_inputs(wl, seed=args.seed, want=("x", "logits", "wgu", "wd", "dy", "wr"))
     if args.act == "relu2":  # two-weight experts: the up weight is the gate half of W_gu
         inp["wgu"] = np.ascontiguousarray(inp["wgu"][:, : wl.I])
     ids, w = oracle.route_topk(inp["logits"], wl.k)
     total_steps = args.warmup + args.steps
     per_step = max(0.05, min(5.0, 150.0 / max(total_steps, 1)))
-    n_tok, _ = size_oracle_sample(wl, inp, ids, w, per_step, (args.act, args.act_clamp))
+    n_tok, _ = size_oracle_sample(wl, inp, ids, w, per_step, (args.act, args.act_clamp), args.router)
     counts = np.bincount(ids.ravel(), minlength=wl.E)
     nonempty = [int(e) for e in np.nonzero(counts)[0]]
     flops = []
@@ -262,14 +281,15 @@ def run_reference(args, rank, world):
     for i in range(total_steps):
         experts = [nonempty[i % len(nonempty)]] if nonempty else []
         t0 = time.perf_counter()
-        f = oracle_sample(wl, inp, ids, w, n_tok, experts, (args.act, args.act_clamp))
+        f = oracle_sample(wl, inp, ids, w, n_tok, experts, (args.act, args.act_clamp), args.router)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             flops.append(f)
             times.append(dt)
     value = sum(flops) / sum(times) / 1e12
     cores = oracle.default_threads()
-    sample = (f"{n_tok} of {wl.T} tokens (forward + dX + d_logits) and one expert's dW per step, "
+    sample = (f"{n_tok} of {wl.T} tokens (forward + dX + d_logits"
+              f"{', router projection and its backward' if args.router else ''}) and one expert's dW per step, "
               f"oracle threads={cores}")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
@@ -298,7 +318,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     wl = synthetic.workload(args.workload)
     T, H, I, E, k, R = wl.T, wl.H, wl.I, wl.E, wl.k, wl.R
-    inp = synthetic.make_inputs(wl, seed=args.seed)
+    inp = synthetic.make_inputs(wl, seed=args.seed, want=("x", "logits", "wgu", "wd", "dy", "wr"))
     gated = args.act != "relu2"
     if not gated:  # two-weight experts: the up weight W_up [E, I, H] is the gate half of W_gu
         inp["wgu"] = np.ascontiguousarray(inp["wgu"][:, :I])
@@ -326,12 +346,19 @@ def run_ours(args, rank, world, local_rank):
     ws_d = e(moe.workspace_bytes("dispatch", T=T, E=E, k=k), dt=torch.uint8)
     ws_f = e(moe.workspace_bytes("grouped_swiglu_fwd", R=R, H=H, I=I, E=E), dt=torch.uint8)
     ws_b = e(moe.workspace_bytes("bwd_dx_dw", T=T, H=H, I=I, E=E, k=k, saved_gu=True, gather=gather), dt=torch.uint8)
+    # --router: the router projection (weights resident like the experts'); with it the step's input
+    # is x alone and the logits buffer is an output of the step
+    wr = to_dev(inp["wr"]) if args.router else None
+    rbias = to_dev(inp["bias"]) if args.router and inp["bias"] is not None else None
+    rbuf = dict(dw_router=e(E, H), d_bias=e(E, dt=f32)) if args.router else None
 
     # --inputs x_perm (default): the dispatch writes the expert-major copy x_perm (and the backward
     # its dy_perm), which the GEMMs read as dense TMA tiles.  --inputs gather: the layer on
     # token-major x and dY, the expert GEMMs copying their rows by token, so no expert-major copy
     # exists (less memory, slower).
     def forward(lg, xx, y_out=None):
+        if args.router:
+            moe.router_logits(xx, wr, rbias, out=lg)
         moe.route_topk(lg, k, topk_ids=ids, topk_w=w)
         moe.dispatch(ids, w, None if gather else xx, E, out=dbuf, workspace=ws_d)
         if gather:
@@ -357,6 +384,9 @@ def run_ours(args, rank, world, local_rank):
             moe.bwd_dx_dw_glu(*args_b, args.act, args.act_clamp, out=out, workspace=ws_b)
         else:
             (moe.bwd_dx_dw_gather if gather else moe.bwd_dx_dw)(*args_b, out=out, workspace=ws_b)
+        if args.router:  # adds the router's input gradient to dX; dWr, dbias
+            moe.router_bwd(out["d_logits"], ids, dbuf["m_indptr"], dbuf["row_to_slot"], xx, wr, out["dx"],
+                           dw_router=rbuf["dw_router"], d_bias=rbuf["d_bias"])
 
     def step():
         forward(logits, x)
@@ -440,7 +470,7 @@ def run_ours(args, rank, world, local_rank):
     if flags:
         raise RuntimeError(f"device error flags {flags:#x} in the timed region")
 
-    fl = step_flops(wl, gated)
+    fl = step_flops(wl, gated, args.router)
     ms_per_step = elapsed_ms / args.steps
     value = world * args.steps * fl["total"] / (elapsed_ms * 1e-3) / 1e12
     tokens_per_s = world * args.steps * T / (elapsed_ms * 1e-3)
@@ -526,6 +556,8 @@ def run_ours(args, rank, world, local_rank):
         h_x = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
         h_dy = torch.from_numpy(inp["dy"].view(np.int16)).view(torch.bfloat16).pin_memory()
         d_in = [(torch.empty_like(logits), torch.empty_like(x), torch.empty_like(dy)) for _ in range(2)]
+        # uploads per step: (logits,) x, dY -- with --router the logits buffer is written on the device
+        up = (lambda b_: list(zip(d_in[b_], (h_logits, h_x, h_dy)))[1 if args.router else 0:])
         d_out = [(e(T, H), e(T, H), e(T, E, dt=f32)) for _ in range(2)]
         h_out = [(torch.empty((T, H), dtype=bf).pin_memory(), torch.empty((T, H), dtype=bf).pin_memory(),
                   torch.empty((T, E), dtype=f32).pin_memory()) for _ in range(2)]
@@ -542,7 +574,7 @@ def run_ours(args, rank, world, local_rank):
             copy_s.wait_event(start)
             with torch.cuda.stream(copy_s):
                 for b_ in range(min(2, nsteps)):
-                    for dst, src in zip(d_in[b_], (h_logits, h_x, h_dy)):
+                    for dst, src in up(b_):
                         dst.copy_(src, non_blocking=True)
                     uploaded[b_].record(copy_s)
             for i in range(nsteps):
@@ -561,7 +593,7 @@ def run_ours(args, rank, world, local_rank):
                         dst.copy_(src, non_blocking=True)
                     downloaded[b_].record(copy_s)
                     if i + 2 < nsteps:  # next inputs into this buffer once step i has consumed it
-                        for dst, src in zip(d_in[b_], (h_logits, h_x, h_dy)):
+                        for dst, src in up(b_):
                             dst.copy_(src, non_blocking=True)
                         uploaded[b_].record(copy_s)
             cur.wait_stream(copy_s)
@@ -591,7 +623,7 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         barrier()
         e2e_ms = max_over_ranks(ev4.elapsed_time(ev5))
-        h2d = T * E * 4 + 2 * T * H * 2
+        h2d = (0 if args.router else T * E * 4) + 2 * T * H * 2
         d2h = 2 * T * H * 2 + T * E * 4
         e2e = {"value": round(world * ne * fl["total"] / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / ne, 4),
@@ -605,14 +637,15 @@ def run_ours(args, rank, world, local_rank):
         import oracle
 
         ids_h, w_h = oracle.route_topk(inp["logits"], k)
-        n_tok, experts = size_oracle_sample(wl, inp, ids_h, w_h, args.cpu_seconds, (args.act, args.act_clamp))
+        n_tok, experts = size_oracle_sample(wl, inp, ids_h, w_h, args.cpu_seconds, (args.act, args.act_clamp),
+                                            args.router)
         t0 = time.perf_counter()
-        f = oracle_sample(wl, inp, ids_h, w_h, n_tok, experts, (args.act, args.act_clamp))
+        f = oracle_sample(wl, inp, ids_h, w_h, n_tok, experts, (args.act, args.act_clamp), args.router)
         dt = time.perf_counter() - t0
         cpu = {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.default_threads(),
                "kind": "oracle",
-               "sample": f"forward + dX + d_logits of tokens 0..{n_tok - 1} of {T}, dW of {len(experts)} experts "
-                         f"({dt:.1f} s wall)"}
+               "sample": f"forward + dX + d_logits{' + router projection and its backward' if args.router else ''} "
+                         f"of tokens 0..{n_tok - 1} of {T}, dW of {len(experts)} experts ({dt:.1f} s wall)"}
 
     launches = len(records)
     if rank == 0:
@@ -622,6 +655,8 @@ def run_ours(args, rank, world, local_rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict(wl.as_dict(), **{"pass": "forward+backward", "parallelism": f"replicas x{world}",
                                            "expert_inputs": args.inputs, "activation": args.act,
+                                           "router": "x Wr^T (+ bias) and its backward on the GPU" if args.router
+                                           else "logits are the layer's input",
                                            "l2": f"inputs larger than L2: {(wgu.numel() + wd.numel()) * 2 / 1e9:.2f} GB "
                                                  f"of weights + activations streamed per step (L2 129 MB)"}),
             "tokens_per_s": round(tokens_per_s, 1),

@@ -27,7 +27,8 @@
  *     Every call only enqueues work on `stream`: it never synchronises, never
  *     allocates device memory and never frees anything.
  *   - The caller owns every buffer.  Outputs are overwritten, never
- *     accumulated into.  Buffers of one call must not overlap unless stated.
+ *     accumulated into (one stated exception: liger_moe_router_bwd adds to dx).
+ *     Buffers of one call must not overlap unless stated.
  *   - bf16 buffers must be 16-byte aligned; H and I must be multiples of 64.
  *   - Limits: 1 <= E <= 1024; 1 <= k <= min(E, 32); T >= 0;
  *     T*k, E*2I and E*H below 2^31.  T = 0 is valid and launches nothing.
@@ -283,6 +284,48 @@ int liger_moe_bwd_dx_dw_gather(const void* dy, const void* x, const void* h_perm
                                const void* w_gate_up, const void* w_down, int T, int H, int I, int E, int k,
                                void* dx, void* dw_gate_up, void* dw_down, float* d_logits, void* workspace,
                                size_t* workspace_bytes, void* stream);
+
+/*
+ * Router projection in front of liger_moe_route_topk: one bias-optional linear layer,
+ *   logits[t, e] = sum_h x[t, h] * w_router[e, h] + bias[e]      (fp32 accumulation).
+ * The pages leave the router to the host framework (LightMoE README, "MoE training": routing
+ * policy is the framework's responsibility); this is its plainest form.  Runs as one dense
+ * tcgen05 GEMM (M = T, N = E, K = H); the summation order differs from a sequential sum, so
+ * the logits agree with a plain fp32 loop to rounding, not bit for bit.
+ *   x         [T, H] bf16, input.
+ *   w_router  [E, H] bf16, input.
+ *   bias      [E] float32, input, or NULL (no bias); any 4-byte alignment.
+ *   logits    [T, E] float32, output (16-byte aligned).
+ * No workspace.  Limits: H a multiple of 64; 1 <= E <= 1024.
+ */
+int liger_moe_router_logits(const void* x, const void* w_router, const float* bias, int T, int H, int E,
+                            float* logits, void* stream);
+
+/*
+ * Backward of the router projection for the layer's own logit gradient (the d_logits that
+ * liger_moe_bwd_dx_dw writes).  Those are zero off each token's top-k selection, so only the
+ * selected entries are read:
+ *   dx[t, :]         = bf16( dx[t, :] + sum_j d_logits[t, id_j] * w_router[id_j, :] )
+ *                      (j = 0..k-1 in slot order, fp32; dx is INPUT AND OUTPUT: the router's
+ *                      input gradient is added to the layer's dX in place -- pass zeros for
+ *                      the router term alone.  This is the one accumulating output of the ABI.)
+ *   dw_router[e, :]  = bf16( sum over expert e's routed rows (token order) of
+ *                      d_logits[t, e] * x[t, :] )        (overwritten; zero for an empty expert)
+ *   d_bias[e]        = sum over the same rows of d_logits[t, e]   (float32, overwritten), or NULL.
+ * Both sums accumulate in fp32 from the exact bf16 inputs, in a fixed order (results are
+ * identical from run to run).
+ *   d_logits     [T, E] float32, input; entries off the selection are not read (they must be
+ *                zero for the result to be the full gradient).
+ *   topk_ids     [T, k] int32, input (liger_moe_route_topk); an id outside [0, E) sets
+ *                LIGER_MOE_DEVERR_BAD_EXPERT_ID and leaves that token's dx unchanged.
+ *   m_indptr     [E+1], row_to_slot [R] int32, inputs: liger_moe_dispatch of the same routing.
+ *   x            [T, H] bf16, input (the router's input).
+ *   w_router     [E, H] bf16, input.
+ * No workspace.  Limits as liger_moe_route_topk and H a multiple of 64.
+ */
+int liger_moe_router_bwd(const float* d_logits, const int32_t* topk_ids, const int32_t* m_indptr,
+                         const int32_t* row_to_slot, const void* x, const void* w_router, int T, int H, int E, int k,
+                         void* dx, void* dw_router, float* d_bias, void* stream);
 
 /*
  * Synchronises `stream`, then returns LIGER_MOE_OK and *flags = 0 when no

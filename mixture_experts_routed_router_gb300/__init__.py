@@ -18,7 +18,8 @@ import torch
 from . import build as _build
 
 __all__ = ["route_topk", "dispatch", "grouped_swiglu_fwd", "grouped_swiglu_fwd_gather", "grouped_glu_fwd",
-           "combine", "bwd_dx_dw", "bwd_dx_dw_gather", "bwd_dx_dw_glu", "ACTIVATIONS", "device_error",
+           "combine", "bwd_dx_dw", "bwd_dx_dw_gather", "bwd_dx_dw_glu", "router_logits", "router_bwd", "ACTIVATIONS",
+           "device_error",
            "workspace_bytes", "trace_enable", "trace_records", "LigerMoEError", "library_path", "load_library"]
 
 _lock = threading.Lock()
@@ -64,6 +65,8 @@ def load_library(build_if_missing: bool = True):
         lib.liger_moe_grouped_glu_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P, P, P, P, S, P]
         lib.liger_moe_bwd_dx_dw_glu.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P,
                                                 P, S, P]
+        lib.liger_moe_router_logits.argtypes = [P, P, P, I, I, I, P, P]
+        lib.liger_moe_router_bwd.argtypes = [P, P, P, P, P, P, I, I, I, I, P, P, P, P]
         lib.liger_moe_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
         lib.liger_moe_trace_enable.argtypes = [I]
         lib.liger_moe_trace_get.argtypes = [I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)]
@@ -73,7 +76,7 @@ def load_library(build_if_missing: bool = True):
         for f in (lib.liger_moe_route_topk, lib.liger_moe_dispatch, lib.liger_moe_grouped_swiglu_fwd,
                   lib.liger_moe_grouped_swiglu_fwd_gather, lib.liger_moe_combine, lib.liger_moe_bwd_dx_dw,
                   lib.liger_moe_bwd_dx_dw_gather, lib.liger_moe_grouped_glu_fwd, lib.liger_moe_bwd_dx_dw_glu,
-                  lib.liger_moe_device_error,
+                  lib.liger_moe_router_logits, lib.liger_moe_router_bwd, lib.liger_moe_device_error,
                   lib.liger_moe_abi_version, lib.liger_moe_trace_enable, lib.liger_moe_trace_count,
                   lib.liger_moe_trace_get):
             f.restype = ctypes.c_int
@@ -123,6 +126,48 @@ def _workspace(ws, nbytes, device):
     if ws.numel() < nbytes:
         raise ValueError(f"workspace has {ws.numel()} bytes, {nbytes} needed")
     return ws
+
+
+def router_logits(x, w_router, bias=None, *, out=None, stream=None):
+    """Router projection logits = x w_router^T (+ bias): float32 [T, E] from x bf16 [T, H],
+    w_router bf16 [E, H] and bias float32 [E] or None."""
+    lib = load_library()
+    _need(x, "x", torch.bfloat16)
+    T, H = x.shape
+    _need(w_router, "w_router", torch.bfloat16)
+    E = w_router.shape[0]
+    _need(w_router, "w_router", torch.bfloat16, (E, H))
+    if bias is not None:
+        _need(bias, "bias", torch.float32, (E,))
+    out = _out(out, "logits", torch.float32, (T, E), x.device)
+    _check("liger_moe_router_logits", lib.liger_moe_router_logits(_ptr(x), _ptr(w_router), _ptr(bias), T, H, E,
+                                                                  _ptr(out), _stream(stream)))
+    return out
+
+
+def router_bwd(d_logits, topk_ids, m_indptr, row_to_slot, x, w_router, dx, *, dw_router=None, d_bias=None,
+               want_bias=True, stream=None):
+    """Backward of the router projection for the layer's d_logits (zero off the top-k).
+
+    Adds the router's input gradient to dx (bf16 [T, H], updated in place) and returns
+    (dw_router bf16 [E, H], d_bias float32 [E] or None when want_bias is False)."""
+    lib = load_library()
+    _need(d_logits, "d_logits", torch.float32)
+    T, E = d_logits.shape
+    _need(topk_ids, "topk_ids", torch.int32)
+    k = topk_ids.shape[1]
+    _need(x, "x", torch.bfloat16)
+    H = x.shape[1]
+    for t, n, dt, sh in ((topk_ids, "topk_ids", torch.int32, (T, k)), (m_indptr, "m_indptr", torch.int32, (E + 1,)),
+                         (row_to_slot, "row_to_slot", torch.int32, (T * k,)), (x, "x", torch.bfloat16, (T, H)),
+                         (w_router, "w_router", torch.bfloat16, (E, H)), (dx, "dx", torch.bfloat16, (T, H))):
+        _need(t, n, dt, sh)
+    dw_router = _out(dw_router, "dw_router", torch.bfloat16, (E, H), x.device)
+    d_bias = _out(d_bias, "d_bias", torch.float32, (E,), x.device) if want_bias else None
+    _check("liger_moe_router_bwd", lib.liger_moe_router_bwd(
+        _ptr(d_logits), _ptr(topk_ids), _ptr(m_indptr), _ptr(row_to_slot), _ptr(x), _ptr(w_router), T, H, E, k,
+        _ptr(dx), _ptr(dw_router), _ptr(d_bias), _stream(stream)))
+    return dw_router, d_bias
 
 
 def route_topk(logits, k, *, topk_ids=None, topk_w=None, stream=None):

@@ -494,6 +494,37 @@ LIGER_MOE_API int liger_moe_bwd_dx_dw_gather(const void* dy, const void* x, cons
                         workspace_bytes, stream);
 }
 
+LIGER_MOE_API int liger_moe_router_logits(const void* x, const void* w_router, const float* bias, int T, int H,
+                                          int E, float* logits, void* stream) {
+  if (T < 0 || H < 1 || E < 1) return LIGER_MOE_ERR_INVALID_ARG;
+  if (E > kMaxExperts || 1LL * T * E > kIndexLimit * 4LL) return LIGER_MOE_ERR_CAPACITY;
+  if (H % 64 != 0) return LIGER_MOE_ERR_MISALIGNED;
+  if (w_router == nullptr || (T > 0 && (x == nullptr || logits == nullptr))) return LIGER_MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(logits)) return LIGER_MOE_ERR_MISALIGNED;
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  return launch_router_logits(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(w_router), bias, T, H,
+                              E, logits, dev, static_cast<cudaStream_t>(stream));
+}
+
+LIGER_MOE_API int liger_moe_router_bwd(const float* d_logits, const int32_t* topk_ids, const int32_t* m_indptr,
+                                       const int32_t* row_to_slot, const void* x, const void* w_router, int T, int H,
+                                       int E, int k, void* dx, void* dw_router, float* d_bias, void* stream) {
+  if (int rc = check_topk(T, E, k)) return rc;
+  if (H < 1) return LIGER_MOE_ERR_INVALID_ARG;
+  if (H % 64 != 0) return LIGER_MOE_ERR_MISALIGNED;
+  if (m_indptr == nullptr || w_router == nullptr || dw_router == nullptr) return LIGER_MOE_ERR_INVALID_ARG;
+  if (T > 0 && (d_logits == nullptr || topk_ids == nullptr || row_to_slot == nullptr || x == nullptr ||
+                dx == nullptr))
+    return LIGER_MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(dx)) return LIGER_MOE_ERR_MISALIGNED;
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  return launch_router_bwd(d_logits, topk_ids, m_indptr, row_to_slot, static_cast<const uint16_t*>(x),
+                           static_cast<const uint16_t*>(w_router), T, H, E, k, static_cast<uint16_t*>(dx),
+                           static_cast<uint16_t*>(dw_router), d_bias, dev, static_cast<cudaStream_t>(stream));
+}
+
 LIGER_MOE_API int liger_moe_trace_enable(int on) {
   std::lock_guard<std::mutex> lock(g_trace_mu);
   for (const TraceRecord& r : g_trace) {

@@ -78,12 +78,14 @@ struct Layout {
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
 };
 
-enum class Sched : int { RowsM = 0, RowsK = 1 };
+// Dense: one plain GEMM over p.R rows (no experts): the router projection.
+enum class Sched : int { RowsM = 0, RowsK = 1, Dense = 2 };
 // SwiGLU: the gate/up GEMM with SwiGLU; GLU: the same with the activation chosen at run time
 // (Params::act), kept apart so that the default SwiGLU kernel carries none of the variants' code.
 // ReLU2: the up GEMM of a two-weight (non-gated) expert, h = max(a, 0)^2.  DH1: the dH epilogue
-// of such an expert (one derivative factor, one output instead of [dg | du]).
-enum class Epi : int { SwiGLU = 0, ScaleRows = 1, DH = 2, Store = 3, GLU = 4, ReLU2 = 5, DH1 = 6 };
+// of such an expert (one derivative factor, one output instead of [dg | du]).  Logits: fp32
+// output plus a per-column bias (the router projection).
+enum class Epi : int { SwiGLU = 0, ScaleRows = 1, DH = 2, Store = 3, GLU = 4, ReLU2 = 5, DH1 = 6, Logits = 7 };
 constexpr bool gate_up_epi(Epi e) { return e == Epi::SwiGLU || e == Epi::GLU; }
 constexpr bool dh_epi(Epi e) { return e == Epi::DH || e == Epi::DH1; }
 template <Epi EP, int SPLIT>
@@ -125,6 +127,11 @@ struct Params {
   int pad_a, pad_b;           // A / B rows are padded rows (RowsM: A only)
   const int32_t* row_slot;  // gathered operand: row_to_slot [R]; token of row r = row_slot[r] / topk
   int topk;
+  // Logits: fp32 output [R, N_out] (row stride ld_out), optional bias [N_out]; out_tma: 32-column
+  // chunks leave through TMA boxes (N_out a multiple of 32), else by masked direct stores
+  float* out_f32;
+  const float* col_bias;
+  int out_tma;
   int* err;
 };
 
@@ -160,6 +167,16 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p) {
     tl.rows = min(BM, end - tl.m0);
     tl.row0 = 0;
     tl.am0 = p.pad_indptr != nullptr ? __ldg(p.pad_indptr + lo) + (tl.m0 - start) : tl.m0;
+    tl.prow0 = 0;
+    tl.kb_count = p.num_kb;
+  } else if constexpr (S == Sched::Dense) {
+    const int mt = t / p.n_tiles;
+    tl.nt = t - mt * p.n_tiles;
+    tl.e = 0;
+    tl.m0 = mt * BM;
+    tl.rows = static_cast<int>(min(static_cast<long long>(BM), p.R - tl.m0));
+    tl.row0 = 0;
+    tl.am0 = tl.m0;
     tl.prow0 = 0;
     tl.kb_count = p.num_kb;
   } else {
@@ -407,6 +424,40 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
         for (int i = 0; i < 16; ++i) hw[half * 16 + i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
       }
       if (p.out != nullptr) emit_row(mode, row_ok, tmC0, st, lane, hw, col, y, p.out + r * p.ld_out + col);
+    }
+  } else if constexpr (EP == Epi::Logits) {
+    // acc = x[r] Wr^T over this tile's columns; out = acc + bias (fp32).  This warp's columns:
+    // [128 colhalf, 128 colhalf + 128) of the tile, in chunks of 32.  Chunks that lie wholly
+    // inside N_out leave as 32 x 32 fp32 boxes (or 32-float row stores in a partial slice);
+    // a chunk that crosses N_out, or any chunk when the row stride is not a multiple of 32,
+    // is stored element by element.
+    if (mode == Rows::None) return;
+    const long long r = tl.m0 + row_local;
+    const int y = tl.m0 + sub * 32;
+#pragma unroll 1
+    for (int q = 4 * colhalf; q < 4 * colhalf + 4; ++q) {
+      const int col = tl.nt * BN + q * 32;
+      if (col >= p.N_out) break;
+      const int ncol = min(32, p.N_out - col);
+      float v[32];
+      tmem_ld32(t_row + q * 32, v);
+      tmem_ld_wait();
+      if (p.col_bias != nullptr) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < ncol) v[i] += __ldg(p.col_bias + col + i);
+      }
+      if (p.out_tma && ncol == 32) {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
+        emit_row(mode, row_ok, tmC0, st, lane, w, col, y, p.out_f32 + r * p.ld_out + col);
+      } else if (row_ok) {
+        float* dst = p.out_f32 + r * p.ld_out + col;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < ncol) dst[i] = v[i];
+      }
     }
   } else if constexpr (dh_epi(EP)) {
     // acc = dHu = dY[token] W_d[e] for this row; d = w_r * dHu in fp32.  The saved forward
@@ -753,6 +804,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int total;
   if constexpr (S == Sched::RowsM)
     total = __ldg(p.tile_prefix + p.E) * p.n_tiles;
+  else if constexpr (S == Sched::Dense)
+    total = static_cast<int>((p.R + BM - 1) / BM) * p.n_tiles;
   else
     total = p.E * p.m_tiles * p.n_tiles;
 
@@ -1285,6 +1338,32 @@ int launch_gate_up(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) 
                                                                               "gemm_gate_up_swiglu");
   return launch_gemm<Sched::RowsM, Epi::SwiGLU, false, false>(ta, tb, tc0, tc1, p, tiles, dev, s,
                                                                "gemm_gate_up_swiglu");
+}
+
+// Router projection logits[T, E] = x[T, H] Wr[E, H]^T (+ bias[E]), fp32: one dense GEMM over T
+// rows, N = E in 256-column tiles (Wr rows past E read as zeros), K = H.
+int launch_router_logits(const uint16_t* x, const uint16_t* w_router, const float* bias, int T, int H, int E,
+                         float* logits, const DeviceInfo& dev, cudaStream_t s) {
+  if (T == 0) return LIGER_MOE_OK;
+  CUtensorMap ta, tb, tc;
+  if (make_tmap(&ta, x, H, T, BK, BM) || make_tmap(&tb, w_router, H, E, BK, BN)) return LIGER_MOE_ERR_LAUNCH;
+  Params p = base_params(nullptr, nullptr, 1, dev.err_flag);
+  p.R = T;
+  p.n_tiles = cdiv(E, BN);
+  p.num_kb = H / BK;
+  p.b_rows_per_expert = 0;
+  p.N_out = E;
+  p.ld_out = E;
+  p.out_f32 = logits;
+  p.col_bias = bias;
+  p.out_tma = (E % 32 == 0) ? 1 : 0;  // the fp32 output map needs rows of whole 128-byte boxes
+  if (p.out_tma) {
+    if (make_out_f32(&tc, logits, E, T)) return LIGER_MOE_ERR_LAUNCH;
+  } else {
+    tc = ta;  // never used for stores
+  }
+  const long long tiles = static_cast<long long>(cdiv(T, BM)) * p.n_tiles;
+  return launch_gemm<Sched::Dense, Epi::Logits, false, false>(ta, tb, tc, tc, p, tiles, dev, s, "gemm_router_logits");
 }
 
 int launch_down(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {

@@ -49,7 +49,17 @@ int launch_router_grad(const float* gdot, int gdot_tiles, const int32_t* ids, co
                        const int32_t* slot_to_row, int T, int E, int k, float* d_logits, const DeviceInfo& dev,
                        cudaStream_t s);
 
+// Router projection backward (router.cu): dx[t] = bf16(dx[t] + sum_j d_logits[t, id_j] Wr[id_j]),
+// dw_router[e] = bf16(sum over e's rows of d_logits[t, e] x[t]), d_bias[e] (nullable).
+int launch_router_bwd(const float* d_logits, const int32_t* topk_ids, const int32_t* m_indptr,
+                      const int32_t* row_to_slot, const uint16_t* x, const uint16_t* w_router, int T, int H, int E,
+                      int k, uint16_t* dx, uint16_t* dw_router, float* d_bias, const DeviceInfo& dev,
+                      cudaStream_t s);
+
 // ---- grouped GEMMs (grouped_gemm.cu)
+// Router projection logits[T, E] = x Wr^T (+ bias), fp32, as one dense tcgen05 GEMM.
+int launch_router_logits(const uint16_t* x, const uint16_t* w_router, const float* bias, int T, int H, int E,
+                         float* logits, const DeviceInfo& dev, cudaStream_t s);
 // Tile schedule: tile_prefix[e] = sum over e' < e of ceil(rows_e' / 128); [E] = total.
 size_t schedule_bytes(int E);
 // With pad_indptr != NULL it also receives the padded row prefix (row counts rounded up to 16).

@@ -29,7 +29,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for f in ("liger_moe_route_topk", "liger_moe_dispatch", "liger_moe_grouped_swiglu_fwd", "liger_moe_combine",
               "liger_moe_bwd_dx_dw", "liger_moe_grouped_swiglu_fwd_gather", "liger_moe_bwd_dx_dw_gather",
-              "liger_moe_grouped_glu_fwd", "liger_moe_bwd_dx_dw_glu"):
+              "liger_moe_grouped_glu_fwd", "liger_moe_bwd_dx_dw_glu", "liger_moe_router_logits",
+              "liger_moe_router_bwd"):
         assert f in names
 
 
@@ -187,3 +188,25 @@ def test_calls_fail_loudly_without_a_device(lib):
     assert lib.liger_moe_route_topk(D, 4, 8, 2, D, D, None) == UNSUPPORTED
     with pytest.raises(RuntimeError):  # LigerMoEError or torch's "no CUDA" error: never a silent result
         moe.device_error()
+
+
+def test_router_entry_points_validate_before_launch(lib):
+    f = lib.liger_moe_router_logits
+    # (x, w_router, bias, T, H, E, logits, stream)
+    assert f(D, D, None, -1, 256, 8, D, None) == INVALID
+    assert f(D, D, None, 4, 256, 0, D, None) == INVALID
+    assert f(D, D, None, 4, 256, 2048, D, None) == CAPACITY    # E above the limit
+    assert f(D, D, None, 4, 200, 8, D, None) == MISALIGNED     # H not a multiple of 64
+    assert f(None, D, None, 4, 256, 8, D, None) == INVALID
+    assert f(D, None, None, 4, 256, 8, D, None) == INVALID
+    assert f(D, D, None, 4, 256, 8, ctypes.c_void_p(260), None) == MISALIGNED
+    g = lib.liger_moe_router_bwd
+    # (d_logits, ids, m_indptr, row_to_slot, x, w_router, T, H, E, k, dx, dw_router, d_bias, stream)
+    assert g(D, D, D, D, D, D, 4, 256, 8, 9, D, D, None, None) == INVALID       # k > E
+    assert g(D, D, D, D, D, D, 4, 256, 8, 0, D, D, None, None) == INVALID       # k < 1
+    assert g(D, D, D, D, D, D, 4, 256, 2048, 2, D, D, None, None) == CAPACITY
+    assert g(D, D, D, D, D, D, 4, 192 + 8, 8, 2, D, D, None, None) == MISALIGNED
+    assert g(D, D, None, D, D, D, 4, 256, 8, 2, D, D, None, None) == INVALID    # m_indptr
+    assert g(D, D, D, D, D, D, 4, 256, 8, 2, None, D, None, None) == INVALID    # dx
+    assert g(D, D, D, D, D, D, 4, 256, 8, 2, D, None, None, None) == INVALID    # dw_router
+    assert g(D, D, D, D, ctypes.c_void_p(264), D, 4, 256, 8, 2, D, D, None, None) == MISALIGNED
