@@ -273,40 +273,76 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
 //   y[t, :] = bf16( sum_{j=0..k-1} y_perm[slot_to_row[t*k + j], :] )  (fp32, j ascending)
 // One warp per token; lane j fetches the row index of slot j once.
 // ============================================================================
+// Work item = (token, segment of kCombineSeg 16-byte chunks); one warp per item, so that a small
+// batch (decode) still spreads over many warps.  Each lane owns two chunks of the segment and
+// reads the k rows four at a time: eight independent 16-byte loads in flight.  The sum over j
+// still runs in j order for every element.
+constexpr int kCombineLaneChunks = 2;
+constexpr int kCombineSeg = 32 * kCombineLaneChunks;  // 16-byte chunks (512 columns) per item
+
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y_perm,
                                                       const int32_t* __restrict__ slot_to_row, int T, int H, int k,
                                                       long long R, uint16_t* __restrict__ y, int* err) {
   const int lane = threadIdx.x & 31;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   const int chunks = H >> 3;
-  for (long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+  const int nseg = (chunks + kCombineSeg - 1) / kCombineSeg;
+  const long long items = static_cast<long long>(T) * nseg;
+  for (long long it = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; it < items;
+       it += nwarps) {
+    const long long t = it / nseg;
+    const int seg = static_cast<int>(it - t * nseg);
     int my_row = (lane < k) ? __ldg(slot_to_row + t * k + lane) : 0;
     const bool bad = static_cast<unsigned long long>(my_row) >= static_cast<unsigned long long>(R);
     if (__any_sync(kFull, bad)) {
-      if (lane == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_ROW);
+      if (lane == 0 && seg == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_ROW);
       continue;
     }
-    for (int c = lane; c < chunks; c += 32) {
-      float acc[8];
+    const int c0 = seg * kCombineSeg + lane;  // this lane's chunks: c0, c0 + 32
+    float acc[kCombineLaneChunks][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      for (int j = 0; j < k; ++j) {
-        const int r = __shfl_sync(kFull, my_row, j);
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(y_perm + static_cast<size_t>(r) * H) + c);
-        acc[0] += bf16_lo(v.x);
-        acc[1] += bf16_hi(v.x);
-        acc[2] += bf16_lo(v.y);
-        acc[3] += bf16_hi(v.y);
-        acc[4] += bf16_lo(v.z);
-        acc[5] += bf16_hi(v.z);
-        acc[6] += bf16_lo(v.w);
-        acc[7] += bf16_hi(v.w);
+    for (int q = 0; q < kCombineLaneChunks; ++q)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[q][i] = 0.f;
+    for (int j0 = 0; j0 < k; j0 += 4) {
+      uint4 v[4][kCombineLaneChunks];
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int r = __shfl_sync(kFull, my_row, (j0 + jj) & 31);
+        if (j0 + jj < k) {
+          const uint4* src = reinterpret_cast<const uint4*>(y_perm + static_cast<size_t>(r) * H);
+#pragma unroll
+          for (int q = 0; q < kCombineLaneChunks; ++q)
+            if (c0 + 32 * q < chunks) v[jj][q] = __ldg(src + c0 + 32 * q);
+        }
       }
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        if (j0 + jj >= k) break;
+#pragma unroll
+        for (int q = 0; q < kCombineLaneChunks; ++q) {
+          if (c0 + 32 * q >= chunks) continue;
+          const uint4 u = v[jj][q];
+          acc[q][0] += bf16_lo(u.x);
+          acc[q][1] += bf16_hi(u.x);
+          acc[q][2] += bf16_lo(u.y);
+          acc[q][3] += bf16_hi(u.y);
+          acc[q][4] += bf16_lo(u.z);
+          acc[q][5] += bf16_hi(u.z);
+          acc[q][6] += bf16_lo(u.w);
+          acc[q][7] += bf16_hi(u.w);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kCombineLaneChunks; ++q) {
+      const int c = c0 + 32 * q;
+      if (c >= chunks) continue;
       uint4 o;
-      o.x = pack_bf16x2(acc[0], acc[1]);
-      o.y = pack_bf16x2(acc[2], acc[3]);
-      o.z = pack_bf16x2(acc[4], acc[5]);
-      o.w = pack_bf16x2(acc[6], acc[7]);
+      o.x = pack_bf16x2(acc[q][0], acc[q][1]);
+      o.y = pack_bf16x2(acc[q][2], acc[q][3]);
+      o.z = pack_bf16x2(acc[q][4], acc[q][5]);
+      o.w = pack_bf16x2(acc[q][6], acc[q][7]);
       reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * H)[c] = o;
     }
   }
@@ -437,8 +473,9 @@ int launch_combine(const uint16_t* y_perm, const int32_t* slot_to_row, int T, in
   if (T == 0) return LIGER_MOE_OK;
   {
     KernelScope trace("combine", s);
-    combine_kernel<<<grid_for_warps(T, 8, dev), 256, 0, s>>>(y_perm, slot_to_row, T, H, k,
-                                                             static_cast<long long>(T) * k, y, dev.err_flag);
+    const long long items = static_cast<long long>(T) * ((H / 8 + kCombineSeg - 1) / kCombineSeg);
+    combine_kernel<<<grid_for_warps(items, 8, dev), 256, 0, s>>>(y_perm, slot_to_row, T, H, k,
+                                                                 static_cast<long long>(T) * k, y, dev.err_flag);
   }
   return check_launch("combine");
 }
