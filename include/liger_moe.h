@@ -336,6 +336,17 @@ int liger_moe_router_bwd(const float* d_logits, const int32_t* topk_ids, const i
 int liger_moe_device_error(void* stream, int* flags);
 
 /*
+ * Failure-detection self-test (diagnostics).  Launches one kernel in which a thread waits,
+ * through the bounded wait that every grouped-GEMM pipeline wait uses, on an mbarrier phase
+ * that nothing completes.  After limit_us microseconds the wait gives up and the kernel sets
+ * LIGER_MOE_DEVERR_WAIT_TIMEOUT in the device error flag, as a stalled GEMM role would; the
+ * context stays usable.  Read the result with liger_moe_device_error().  The GEMMs' own limit
+ * is 2 s per wait.
+ *   limit_us  1 .. 1000000 (else LIGER_MOE_ERR_INVALID_ARG).
+ */
+int liger_moe_selftest_wait_timeout(int limit_us, void* stream);
+
+/*
  * Kernel trace (diagnostics; off by default).  While enabled, every kernel
  * this library launches is bracketed by two CUDA events recorded on the
  * launch stream, giving its device-side duration without a profiler.

@@ -20,7 +20,7 @@ from . import build as _build
 __all__ = ["route_topk", "dispatch", "grouped_swiglu_fwd", "grouped_swiglu_fwd_gather", "grouped_glu_fwd",
            "combine", "bwd_dx_dw", "bwd_dx_dw_gather", "bwd_dx_dw_glu", "router_logits", "router_bwd", "ACTIVATIONS",
            "device_error",
-           "workspace_bytes", "trace_enable", "trace_records", "LigerMoEError", "library_path", "load_library"]
+           "selftest_wait_timeout", "workspace_bytes", "trace_enable", "trace_records", "LigerMoEError", "library_path", "load_library"]
 
 _lock = threading.Lock()
 _lib = None
@@ -68,6 +68,7 @@ def load_library(build_if_missing: bool = True):
         lib.liger_moe_router_logits.argtypes = [P, P, P, I, I, I, P, P]
         lib.liger_moe_router_bwd.argtypes = [P, P, P, P, P, P, I, I, I, I, P, P, P, P]
         lib.liger_moe_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
+        lib.liger_moe_selftest_wait_timeout.argtypes = [I, P]
         lib.liger_moe_trace_enable.argtypes = [I]
         lib.liger_moe_trace_get.argtypes = [I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)]
         lib.liger_moe_last_cuda_error.restype = ctypes.c_char_p
@@ -77,6 +78,7 @@ def load_library(build_if_missing: bool = True):
                   lib.liger_moe_grouped_swiglu_fwd_gather, lib.liger_moe_combine, lib.liger_moe_bwd_dx_dw,
                   lib.liger_moe_bwd_dx_dw_gather, lib.liger_moe_grouped_glu_fwd, lib.liger_moe_bwd_dx_dw_glu,
                   lib.liger_moe_router_logits, lib.liger_moe_router_bwd, lib.liger_moe_device_error,
+                  lib.liger_moe_selftest_wait_timeout,
                   lib.liger_moe_abi_version, lib.liger_moe_trace_enable, lib.liger_moe_trace_count,
                   lib.liger_moe_trace_get):
             f.restype = ctypes.c_int
@@ -386,6 +388,13 @@ def bwd_dx_dw_gather(dy, x, h_perm, gu_perm, topk_ids, topk_w, m_indptr, row_to_
     """The backward on token-major x [T,H] (no x_perm); same outputs as bwd_dx_dw."""
     return _bwd("liger_moe_bwd_dx_dw_gather", dy, x, "x", h_perm, gu_perm, topk_ids, topk_w, m_indptr,
                 row_to_slot, slot_to_row, w_perm, w_gate_up, w_down, out, workspace, stream)
+
+
+def selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Runs the bounded-wait self-test: a wait that nothing completes gives up after limit_us and
+    sets the WAIT_TIMEOUT bit, which device_error() then returns."""
+    lib = load_library()
+    _check("liger_moe_selftest_wait_timeout", lib.liger_moe_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def device_error(stream=None) -> int:

@@ -525,6 +525,13 @@ LIGER_MOE_API int liger_moe_router_bwd(const float* d_logits, const int32_t* top
                            static_cast<uint16_t*>(dw_router), d_bias, dev, static_cast<cudaStream_t>(stream));
 }
 
+LIGER_MOE_API int liger_moe_selftest_wait_timeout(int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return LIGER_MOE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  return launch_bounded_wait_selftest(static_cast<uint64_t>(limit_us) * 1000ull, dev, static_cast<cudaStream_t>(stream));
+}
+
 LIGER_MOE_API int liger_moe_trace_enable(int on) {
   std::lock_guard<std::mutex> lock(g_trace_mu);
   for (const TraceRecord& r : g_trace) {

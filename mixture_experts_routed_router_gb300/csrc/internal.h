@@ -56,6 +56,9 @@ int launch_router_bwd(const float* d_logits, const int32_t* topk_ids, const int3
                       int k, uint16_t* dx, uint16_t* dw_router, float* d_bias, const DeviceInfo& dev,
                       cudaStream_t s);
 
+// Failure-detection self-test (selftest.cu): a bounded wait on a phase nothing completes.
+int launch_bounded_wait_selftest(uint64_t limit_ns, const DeviceInfo& dev, cudaStream_t s);
+
 // ---- grouped GEMMs (grouped_gemm.cu)
 // Router projection logits[T, E] = x Wr^T (+ bias), fp32, as one dense tcgen05 GEMM.
 int launch_router_logits(const uint16_t* x, const uint16_t* w_router, const float* bias, int T, int H, int E,

@@ -58,16 +58,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // one tile's worth of work (microseconds to milliseconds).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-// Bounded wait: returns false if the phase did not complete within
-// kWaitLimitNs or *abort became non-zero (another role gave up).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort) {
+// Bounded wait: returns false if the phase did not complete within limit_ns
+// (kWaitLimitNs unless given) or *abort became non-zero (another role gave up).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 127u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
     }
   }
 }

@@ -11,9 +11,9 @@
 // accumulation and no bf16 rounding of d_logits.  Entries of d_logits off the selection are
 // not read.
 //
-// router_dx_kernel: one warp per token, 16-byte vectors of H (like the combine).
-// router_dw_kernel: one CTA per (expert, 256-column block); its 16 warps split each pass of the
-// expert's rows into 16 contiguous ranges (rows in token order), then the partial sums are added
+// router_dx_kernel: one warp per (token, 512-column segment), 16-byte vectors (like the combine).
+// router_dw_kernel: one CTA per (expert, 256-column block); its 8 warps split each pass of the
+// expert's rows into 8 contiguous ranges (rows in token order), then the partial sums are added
 // in warp order, so the result does not depend on timing.
 #include <cuda_runtime.h>
 
@@ -26,7 +26,7 @@ namespace lmoe {
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr int kDwWarps = 16;
+constexpr int kDwWarps = 8;
 constexpr int kDwCols = 256;  // columns per CTA: 32 lanes x 8
 
 __device__ __forceinline__ void fma8(float (&acc)[8], float d, const uint4& v) {
@@ -40,9 +40,12 @@ __device__ __forceinline__ void fma8(float (&acc)[8], float d, const uint4& v) {
   acc[7] += d * bf16_hi(v.w);
 }
 
-// Four 8-column chunks per lane at a time (columns lane*8 + 256*i), the k rows of Wr two at a
-// time: eight independent 16-byte loads in flight per lane.
-constexpr int kDxChunks = 4;
+// Work item = (token, segment of 64 16-byte chunks = 512 columns), one warp per item, as in the
+// combine: a small batch still spreads over many warps.  Each lane owns two chunks; the k rows of
+// Wr are read four at a time (eight independent 16-byte loads in flight), and the lane's dX chunks
+// are loaded before them.
+constexpr int kDxLaneChunks = 2;
+constexpr int kDxSeg = 32 * kDxLaneChunks;
 
 __global__ void __launch_bounds__(256) router_dx_kernel(const float* __restrict__ d_logits,
                                                         const int32_t* __restrict__ ids,
@@ -51,7 +54,12 @@ __global__ void __launch_bounds__(256) router_dx_kernel(const float* __restrict_
   const int lane = threadIdx.x & 31;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   const int chunks = H >> 3;  // 16-byte chunks of a row
-  for (long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+  const int nseg = (chunks + kDxSeg - 1) / kDxSeg;
+  const long long items = static_cast<long long>(T) * nseg;
+  for (long long it = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; it < items;
+       it += nwarps) {
+    const long long t = it / nseg;
+    const int seg = static_cast<int>(it - t * nseg);
     int id = 0;
     float d = 0.f;
     bool bad = false;
@@ -61,57 +69,58 @@ __global__ void __launch_bounds__(256) router_dx_kernel(const float* __restrict_
       if (!bad) d = __ldg(d_logits + t * E + id);
     }
     if (__any_sync(kFull, bad)) {
-      if (lane == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_EXPERT_ID);
+      if (lane == 0 && seg == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_EXPERT_ID);
       continue;
     }
     uint4* row = reinterpret_cast<uint4*>(dx + static_cast<size_t>(t) * H);
-    for (int c0 = lane; c0 < chunks; c0 += 32 * kDxChunks) {
-      float acc[kDxChunks][8];
+    const int c0 = seg * kDxSeg + lane;  // this lane's chunks: c0, c0 + 32
+    uint4 base[kDxLaneChunks];
 #pragma unroll
-      for (int q = 0; q < kDxChunks; ++q)
+    for (int q = 0; q < kDxLaneChunks; ++q)
+      if (c0 + 32 * q < chunks) base[q] = __ldcs(row + c0 + 32 * q);  // read once, overwritten below
+    float acc[kDxLaneChunks][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[q][i] = 0.f;
-      for (int j = 0; j < k; j += 2) {
-        const bool two = j + 1 < k;
-        const int e0 = __shfl_sync(kFull, id, j), e1 = __shfl_sync(kFull, id, two ? j + 1 : j);
-        const float d0 = __shfl_sync(kFull, d, j), d1 = two ? __shfl_sync(kFull, d, j + 1) : 0.f;
-        const uint4* w0 = reinterpret_cast<const uint4*>(w_router + static_cast<size_t>(e0) * H);
-        const uint4* w1 = reinterpret_cast<const uint4*>(w_router + static_cast<size_t>(e1) * H);
-        uint4 v0[kDxChunks], v1[kDxChunks];
+    for (int q = 0; q < kDxLaneChunks; ++q)
 #pragma unroll
-        for (int q = 0; q < kDxChunks; ++q) {
-          const int c = c0 + 32 * q;
-          if (c < chunks) {
-            v0[q] = __ldg(w0 + c);
-            v1[q] = __ldg(w1 + c);
-          }
-        }
+      for (int i = 0; i < 8; ++i) acc[q][i] = 0.f;
+    for (int j0 = 0; j0 < k; j0 += 4) {
+      uint4 v[4][kDxLaneChunks];
+      float dj[4];
 #pragma unroll
-        for (int q = 0; q < kDxChunks; ++q) {
-          if (c0 + 32 * q < chunks) {
-            fma8(acc[q], d0, v0[q]);
-            if (two) fma8(acc[q], d1, v1[q]);
-          }
+      for (int jj = 0; jj < 4; ++jj) {
+        const int e = __shfl_sync(kFull, id, (j0 + jj) & 31);
+        dj[jj] = __shfl_sync(kFull, d, (j0 + jj) & 31);
+        if (j0 + jj < k) {
+          const uint4* w = reinterpret_cast<const uint4*>(w_router + static_cast<size_t>(e) * H);
+#pragma unroll
+          for (int q = 0; q < kDxLaneChunks; ++q)
+            if (c0 + 32 * q < chunks) v[jj][q] = __ldg(w + c0 + 32 * q);
         }
       }
 #pragma unroll
-      for (int q = 0; q < kDxChunks; ++q) {
-        const int c = c0 + 32 * q;
-        if (c >= chunks) break;
-        const uint4 b = __ldcs(row + c);  // read once, then overwritten in place
-        uint4 o;
-        o.x = pack_bf16x2(bf16_lo(b.x) + acc[q][0], bf16_hi(b.x) + acc[q][1]);
-        o.y = pack_bf16x2(bf16_lo(b.y) + acc[q][2], bf16_hi(b.y) + acc[q][3]);
-        o.z = pack_bf16x2(bf16_lo(b.z) + acc[q][4], bf16_hi(b.z) + acc[q][5]);
-        o.w = pack_bf16x2(bf16_lo(b.w) + acc[q][6], bf16_hi(b.w) + acc[q][7]);
-        row[c] = o;
+      for (int jj = 0; jj < 4; ++jj) {
+        if (j0 + jj >= k) break;
+#pragma unroll
+        for (int q = 0; q < kDxLaneChunks; ++q)
+          if (c0 + 32 * q < chunks) fma8(acc[q], dj[jj], v[jj][q]);
       }
+    }
+#pragma unroll
+    for (int q = 0; q < kDxLaneChunks; ++q) {
+      const int c = c0 + 32 * q;
+      if (c >= chunks) continue;
+      const uint4 b = base[q];
+      uint4 o;
+      o.x = pack_bf16x2(bf16_lo(b.x) + acc[q][0], bf16_hi(b.x) + acc[q][1]);
+      o.y = pack_bf16x2(bf16_lo(b.y) + acc[q][2], bf16_hi(b.y) + acc[q][3]);
+      o.z = pack_bf16x2(bf16_lo(b.z) + acc[q][4], bf16_hi(b.z) + acc[q][5]);
+      o.w = pack_bf16x2(bf16_lo(b.w) + acc[q][6], bf16_hi(b.w) + acc[q][7]);
+      row[c] = o;
     }
   }
 }
 
-
-// grid (E, ceil(H / 256)), block 16 warps.  m_indptr / row_to_slot: the dispatch of the same
+// grid (E, ceil(H / 256)), block kDwWarps warps.  m_indptr / row_to_slot: the dispatch of the same
 // routing (expert e's rows in token order); the token of row r is row_to_slot[r] / k.  The
 // expert's rows are taken in passes of up to kDwStage: the whole CTA first stages their tokens
 // and d_logits entries in shared memory (every load independent), then each warp streams the x
@@ -179,7 +188,7 @@ __global__ void __launch_bounds__(kDwWarps * 32) router_dw_kernel(const float* _
   for (int q = 0; q < 8; ++q) part[warp][lane * 8 + q] = acc[q];
   if (lane == 0) part_b[warp] = db;
   __syncthreads();
-  // thread c adds column c of the 16 partials in warp order
+  // thread c adds column c of the kDwWarps partials in warp order
   for (int c = threadIdx.x; c < kDwCols; c += blockDim.x) {
     const int gc = blockIdx.y * kDwCols + c;
     if (gc >= H) continue;
@@ -213,8 +222,9 @@ int launch_router_bwd(const float* d_logits, const int32_t* topk_ids, const int3
   if (T > 0) {
     {
       KernelScope trace("router_dx", s);
-      router_dx_kernel<<<grid_warps(T, 8, dev), 256, 0, s>>>(d_logits, topk_ids, w_router, T, H, E, k, dx,
-                                                            dev.err_flag);
+      const long long items = static_cast<long long>(T) * ((H / 8 + kDxSeg - 1) / kDxSeg);
+      router_dx_kernel<<<grid_warps(items, 8, dev), 256, 0, s>>>(d_logits, topk_ids, w_router, T, H, E, k, dx,
+                                                                dev.err_flag);
     }
     if (int rc = check_launch("router_dx")) return rc;
   }

@@ -210,3 +210,8 @@ def test_router_entry_points_validate_before_launch(lib):
     assert g(D, D, D, D, D, D, 4, 256, 8, 2, None, D, None, None) == INVALID    # dx
     assert g(D, D, D, D, D, D, 4, 256, 8, 2, D, None, None, None) == INVALID    # dw_router
     assert g(D, D, D, D, ctypes.c_void_p(264), D, 4, 256, 8, 2, D, D, None, None) == MISALIGNED
+
+
+def test_selftest_limit_is_validated(lib):
+    for bad in (0, -5, 1000001):
+        assert lib.liger_moe_selftest_wait_timeout(bad, None) == INVALID
