@@ -258,7 +258,7 @@ int grouped_swiglu_fwd_impl(const void* x_perm, const void* x, const int32_t* ro
   if (!aligned16(a_src) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(h_perm) ||
       !aligned16(gu_perm) || !aligned16(y_perm))
     return LIGER_MOE_ERR_MISALIGNED;
-  const size_t need = schedule_bytes(E);
+  const size_t need = 2 * schedule_bytes(E);  // tile prefixes of 128-row tiles and of 256-row pair tiles
   if (workspace == nullptr) {
     *workspace_bytes = need;
     return LIGER_MOE_OK;
@@ -269,8 +269,10 @@ int grouped_swiglu_fwd_impl(const void* x_perm, const void* x, const int32_t* ro
   if (int rc = current_device(&dev)) return rc;
   if (R == 0) return LIGER_MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int32_t* tile_prefix = static_cast<int32_t*>(workspace);
-  if (int rc = launch_tile_schedule(m_indptr, E, R, tile_prefix, nullptr, dev, s)) return rc;
+  uint8_t* cur = static_cast<uint8_t*>(workspace);
+  int32_t* tile_prefix = carve<int32_t>(cur, schedule_bytes(E));
+  int32_t* pair_prefix = carve<int32_t>(cur, schedule_bytes(E));
+  if (int rc = launch_tile_schedule(m_indptr, E, R, tile_prefix, nullptr, dev, s, pair_prefix)) return rc;
   FwdGemmArgs a{};
   a.x_perm = static_cast<const uint16_t*>(x_perm);
   a.x = static_cast<const uint16_t*>(x);
@@ -279,6 +281,7 @@ int grouped_swiglu_fwd_impl(const void* x_perm, const void* x, const int32_t* ro
   a.k = k;
   a.m_indptr = m_indptr;
   a.tile_prefix = tile_prefix;
+  a.pair_prefix = pair_prefix;
   a.w_gate_up = static_cast<const uint16_t*>(w_gate_up);
   a.w_down = static_cast<const uint16_t*>(w_down);
   a.w_perm = w_perm;

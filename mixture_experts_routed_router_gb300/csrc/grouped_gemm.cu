@@ -62,14 +62,15 @@ constexpr int kDhSetBytes = 6 * kDhBoxBytes;    // six output boxes per 16 colum
 //   SPLIT = 0: one A and one B tile per stage (48 KB), 4 stages;
 //   SPLIT = 1: A as two bf16 parts (hi, lo) + B (64 KB), 3 stages: two MMAs per K step share B;
 //   SPLIT = 2: A + B as two parts (80 KB), 2 stages: two MMAs per K step share A.
+//   PAIR: a CTA of a 2-SM pair holds its 128 rows of A and half of B's rows (32 KB), 6 stages.
 // Epilogue staging per warp: one 4 KB box, or for the dH kernel one set of six 1 KB boxes
 // (3 operand stages there: its MMAs are a small part of its time).
-template <int kDh, int SPLIT>
+template <int kDh, int SPLIT, int PAIR = 0>
 struct Layout {
   static constexpr int kABytes = A_BYTES * (SPLIT == 1 ? 2 : 1);
-  static constexpr int kBBytes = B_BYTES * (SPLIT == 2 ? 2 : 1);
+  static constexpr int kBBytes = B_BYTES * (SPLIT == 2 ? 2 : 1) / (PAIR ? 2 : 1);
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = kDh ? 3 : (SPLIT == 0 ? 4 : (SPLIT == 1 ? 3 : 2));
+  static constexpr int kStages = PAIR ? (kDh ? 4 : 6) : (kDh ? 3 : (SPLIT == 0 ? 4 : (SPLIT == 1 ? 3 : 2)));
   static constexpr int kStgWarpBytes = kDh ? kDhSetBytes : STG_PER_WARP * STG_BYTES;
   static constexpr int kStgOffset = kStages * kStageBytes;
   static constexpr int kBarOffset = kStgOffset + kEpiWarps * kStgWarpBytes;
@@ -88,8 +89,8 @@ enum class Sched : int { RowsM = 0, RowsK = 1, Dense = 2 };
 enum class Epi : int { SwiGLU = 0, ScaleRows = 1, DH = 2, Store = 3, GLU = 4, ReLU2 = 5, DH1 = 6, Logits = 7 };
 constexpr bool gate_up_epi(Epi e) { return e == Epi::SwiGLU || e == Epi::GLU; }
 constexpr bool dh_epi(Epi e) { return e == Epi::DH || e == Epi::DH1; }
-template <Epi EP, int SPLIT>
-using LayoutOf = Layout<dh_epi(EP) ? 1 : 0, SPLIT>;
+template <Epi EP, int SPLIT, int PAIR = 0>
+using LayoutOf = Layout<dh_epi(EP) ? 1 : 0, SPLIT, PAIR>;
 
 struct Params {
   const int32_t* m_indptr;     // [E+1]
@@ -194,6 +195,32 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p) {
     tl.prow0 = p.pad_indptr != nullptr ? __ldg(p.pad_indptr + tl.e) : tl.row0;
     tl.kb_count = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
   }
+  return tl;
+}
+
+// RowsM tile of a 2-SM pair: tile_prefix counts 256-row blocks per expert; CTA `rank` of the
+// pair owns rows [m0, m0 + 128) of the block (none when the expert ends before them).
+__device__ __forceinline__ Tile decode_tile_pair(int t, const Params& p, uint32_t rank) {
+  Tile tl;
+  const int mt = t / p.n_tiles;
+  tl.nt = t - mt * p.n_tiles;
+  int lo = 0, hi = p.E;  // tile_prefix[lo] <= mt < tile_prefix[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(p.tile_prefix + mid) <= mt)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  tl.e = lo;
+  const int end = __ldg(p.m_indptr + lo + 1);
+  const int start = __ldg(p.m_indptr + lo);
+  tl.m0 = start + (mt - __ldg(p.tile_prefix + lo)) * (2 * BM) + static_cast<int>(rank) * BM;
+  tl.rows = max(0, min(BM, end - tl.m0));
+  tl.row0 = 0;
+  tl.am0 = tl.m0;
+  tl.prow0 = 0;
+  tl.kb_count = p.num_kb;
   return tl;
 }
 
@@ -704,6 +731,28 @@ __device__ __forceinline__ void load_stage_tiled(const CUtensorMap* tmA, const C
   }
 }
 
+// Loads of one stage in a 2-SM pair (RowsM, K-major A): this CTA's 128 rows of A and its half of
+// B's 256 rows, both completing on the even CTA's full barrier (`bar`, a shared::cluster
+// address), which expects the bytes of both CTAs.  Gate/up tiles put the gate rows in the even
+// CTA and the up rows in the odd one, so the accumulator columns stay [g | u].
+template <Epi EP, bool B_MN>
+__device__ __forceinline__ void load_stage_pair(const CUtensorMap* tmA, const CUtensorMap* tmB, const Params& p,
+                                                const Tile& tl, int kb, uint32_t sa, uint32_t sb, uint32_t bar,
+                                                uint32_t rank) {
+  tma_load_2d_pair(sa, tmA, bar, kb * BK, tl.m0);  // A box: 128 rows (past R: zero fill)
+  if constexpr (!B_MN) {
+    const int r = gate_up_epi(EP) ? tl.e * p.b_rows_per_expert + tl.nt * (BN / 2) + (rank ? p.b_split : 0)
+                                  : tl.e * p.b_rows_per_expert + tl.nt * BN + static_cast<int>(rank) * (BN / 2);
+    tma_load_2d_pair(sb, tmB, bar, kb * BK, r);  // B box: 128 rows
+  } else {
+    const int krow = tl.e * p.b_rows_per_expert + kb * BK;
+#pragma unroll
+    for (int i = 0; i < BN / 128; ++i)  // this CTA's two 64-column boxes of the tile's N columns
+      tma_load_2d_pair(sb + i * MN_BOX_BYTES, tmB, bar, tl.nt * BN + static_cast<int>(rank) * (BN / 2) + 64 * i,
+                       krow);
+  }
+}
+
 // Tokens of the four rows a producer lane gathers for (tile, K block): RowsM, rows 4 lane ..
 // 4 lane + 3 of the tile; RowsK, rows 4 (lane & 15) .. + 3 of the K block.  Rows outside the
 // tile or expert take token 0 (their products are discarded, or their shared-memory rows are
@@ -737,18 +786,34 @@ __device__ __forceinline__ void gather_tokens(const Tile& tl, int kb, int lane, 
 // tile count must be a multiple of CL, so that the CTAs of a cluster walk the same number of
 // tiles and K blocks in lockstep.  A stage is refilled only after every CTA of the cluster has
 // consumed it (each MMA warp's commit arrives on the empty barrier of all of them).
-template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT, Gather G, int CL>
+// PAIR (with CL = 2): the two CTAs of a cluster work on one 256-row tile with 2-SM MMAs
+// (cta_group::2): both load their halves, the even CTA's MMA warp issues every MMA and commits to
+// both CTAs' barriers, and both CTAs' epilogues release the accumulator to the even CTA.
+template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT, Gather G, int CL, int PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
                         const Params p) {
-  using L = LayoutOf<EP, SPLIT>;
+  using L = LayoutOf<EP, SPLIT, PAIR>;
+  constexpr bool kPair = PAIR != 0;
+  static_assert(!kPair || (CL == 2 && S == Sched::RowsM && G == Gather::None && !A_MN && SPLIT == 0),
+                "2-SM pairs: RowsM tiles with K-major A, one operand part, no gather");
   constexpr int STAGES = L::kStages;
   constexpr int STAGE_BYTES = L::kStageBytes;
   constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CL) - 1u);
   static_assert(CL == 1 || G == Gather::None, "clusters share tiled operands only");
   static_assert(CL == 1 || (S == Sched::RowsM ? !A_MN : B_MN), "shared operand: K-major A (RowsM), MN-major B (RowsK)");
   const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
+  const bool leader = !kPair || rank == 0;  // the CTA that issues the MMAs
+  // pairs walk the tiles together: tile t of cluster c is t = c, c + clusters, ...
+  const int tile0 = kPair ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+  const int tstride = kPair ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
+  auto decode = [&](int t) -> Tile {
+    if constexpr (kPair)
+      return decode_tile_pair(t, p, rank);
+    else
+      return decode_tile<S>(t, p);
+  };
   static_assert(SPLIT == 0 || (S == Sched::RowsK && A_MN && B_MN), "hi/lo operands only in the dW GEMMs");
   static_assert(G == Gather::None || (S == Sched::RowsM ? (G == Gather::A && !A_MN)
                                                          : (G == Gather::A ? (A_MN && SPLIT != 1)
@@ -773,11 +838,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, CL);  // one release per CTA of the cluster
+      mbar_init(empty0 + 8 * s, kPair ? 1 : CL);  // one release per CTA of the cluster (pair: the even CTA's)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, kEpiWarps);
+      mbar_init(tempty0 + 8 * a, kPair ? 2 * kEpiWarps : kEpiWarps);  // pair: both CTAs' epilogue warps
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -790,8 +855,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmC1);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
   if constexpr (CL > 1)
@@ -816,8 +886,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         bool failed = false;
-        for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
-          const Tile tl = decode_tile<S>(t, p);
+        for (int t = tile0; t < total && !failed; t += tstride) {
+          const Tile tl = decode(t);
           for (int kb = 0; kb < tl.kb_count; ++kb) {
             if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
               raise_abort(p.err, abort_flag);
@@ -826,9 +896,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint32_t sa = sbase + stage * STAGE_BYTES;
             const uint32_t fb = full0 + 8 * stage;
-            mbar_arrive_expect_tx(fb, STAGE_BYTES);
-            load_stage_tiled<S, EP, A_MN, B_MN, SPLIT, true, true, CL>(&tmA, &tmB, p, tl, kb, sa, sa + L::kABytes, fb,
-                                                                      rank);
+            if constexpr (kPair) {
+              // the even CTA's full barrier counts both CTAs' bytes of this stage
+              if (leader) mbar_arrive_expect_tx(fb, 2 * STAGE_BYTES);
+              load_stage_pair<EP, B_MN>(&tmA, &tmB, p, tl, kb, sa, sa + L::kABytes, mapa_shared(fb, 0), rank);
+            } else {
+              mbar_arrive_expect_tx(fb, STAGE_BYTES);
+              load_stage_tiled<S, EP, A_MN, B_MN, SPLIT, true, true, CL>(&tmA, &tmB, p, tl, kb, sa, sa + L::kABytes,
+                                                                        fb, rank);
+            }
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -921,17 +997,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    // pair: M = 256 across the two CTAs (the odd CTA's MMA warp issues nothing)
+    constexpr uint32_t idesc = idesc_bf16_f32(kPair ? 2 * BM : BM, BN, A_MN, B_MN);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool failed = false;
-    for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
-      const Tile tl = decode_tile<S>(t, p);
+    for (int t = tile0; leader && t < total && !failed; t += tstride) {
+      const Tile tl = decode(t);
       if (tl.kb_count == 0) continue;
-      // every lane waits (so every lane acquires the phase); the outcome is made warp-uniform
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag))) {
+      // every lane waits (so every lane acquires the phase); the outcome is made warp-uniform.
+      // Pair: the accumulator is free once both CTAs' epilogues have read it (cluster scope).
+      const bool freed = kPair ? mbar_wait_cluster(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag)
+                               : mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, freed)) {
         raise_abort(p.err, abort_flag);
         break;
       }
@@ -963,13 +1043,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      : smem_desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc_sw128(sb + kk * 2048, MN_BOX_BYTES, 1024)
                                      : smem_desc_sw128(sb + kk * 32, 16, 1024);
-            umma_bf16_f32(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            if constexpr (kPair)
+              umma_bf16_f32_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            else
+              umma_bf16_f32(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
             if constexpr (SPLIT == 1)  // lo part of A against the same B
               umma_bf16_f32(d_tmem, smem_desc_sw128(sa + A_BYTES + kk * 2048, MN_BOX_BYTES, 1024), bd, idesc, 1u);
             if constexpr (SPLIT == 2)  // the same A against the lo part of B
               umma_bf16_f32(d_tmem, ad, smem_desc_sw128(sb + B_BYTES + kk * 2048, MN_BOX_BYTES, 1024), idesc, 1u);
           }
-          if constexpr (CL > 1)
+          if constexpr (kPair)
+            umma_commit_pair_mc(empty0 + 8 * stage, kClusterMask);  // both CTAs' stage is free
+          else if constexpr (CL > 1)
             umma_commit_mc(empty0 + 8 * stage, kClusterMask);
           else
             umma_commit(empty0 + 8 * stage);
@@ -981,14 +1066,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (failed) break;
-      if (lane == 0) umma_commit(tfull0 + 8 * acc);
+      if (lane == 0) {
+        if constexpr (kPair)
+          umma_commit_pair_mc(tfull0 + 8 * acc, kClusterMask);  // both CTAs' accumulators are ready
+        else
+          umma_commit(tfull0 + 8 * acc);
+      }
       __syncwarp();
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
     // every MMA issued by this CTA has completed before TMEM is released
-    if (lane == 0) {
-      umma_commit(drain);
+    if (lane == 0 && leader) {
+      if constexpr (kPair)
+        umma_commit_pair(drain);
+      else
+        umma_commit(drain);
       const int never = 0;
       mbar_wait(drain, 0, &never);
     }
@@ -1002,8 +1095,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     Stager st{sbase + L::kStgOffset + static_cast<uint32_t>(ew * L::kStgWarpBytes), 0};
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = decode_tile<S>(t, p);
+    for (int t = tile0; t < total; t += tstride) {
+      const Tile tl = decode(t);
       // the tile's epilogue operands (DH) start moving into L2 now, a tile's MMA time ahead of use
       // when the MMAs lead, and at least ahead of the later column chunks when the epilogue does
       prefetch_epilogue_operands<S, EP>(t, total, row_local, colhalf, p);
@@ -1020,7 +1113,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       epilogue_tile<S, EP>(t_row, tl, sub, colhalf, lane, p, &tmC0, &tmC1, st);
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      if (lane == 0) {
+        if constexpr (kPair)
+          mbar_arrive_cluster(mapa_shared(tempty0 + 8 * acc, 0));  // the even CTA issues the next MMAs
+        else
+          mbar_arrive(tempty0 + 8 * acc);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -1031,8 +1129,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (kPair) {
+    // neither CTA of the pair leaves while the other may still arrive on its barriers, and the
+    // odd CTA's TMEM (written by the even CTA's MMAs) is released by both together
+    cluster_sync();
+  }
   tc_fence_after_sync();
-  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == 1) {
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
+  }
 }
 
 // ============================================================================
@@ -1070,30 +1178,35 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* s_warp, int
 
 __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __restrict__ m_indptr, int E,
                                                              long long R, int32_t* __restrict__ tile_prefix,
-                                                             int32_t* __restrict__ pad_indptr, int* err) {
+                                                             int32_t* __restrict__ pad_indptr,
+                                                             int32_t* __restrict__ pair_prefix, int* err) {
   __shared__ int s_warp[32];
   __shared__ int s_bad;
-  __shared__ int s_total[2];
+  __shared__ int s_total[3];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) s_bad = (m_indptr[0] != 0 || static_cast<long long>(m_indptr[E]) != R) ? 1 : 0;
   __syncthreads();
-  int tiles = 0, padded = 0;
+  int tiles = 0, padded = 0, pairs = 0;
   if (tid < E) {
     const int a = m_indptr[tid], b = m_indptr[tid + 1];
     if (b < a) atomicOr(&s_bad, 1);
     tiles = (b > a) ? (b - a + BM - 1) / BM : 0;
     padded = (b > a) ? ((b - a + 15) & ~15) : 0;
+    pairs = (b > a) ? (b - a + 2 * BM - 1) / (2 * BM) : 0;
   }
   const int t_excl = block_exclusive_scan_1024(tiles, s_warp, lane, warp, &s_total[0]);
   const int p_excl = pad_indptr != nullptr ? block_exclusive_scan_1024(padded, s_warp, lane, warp, &s_total[1]) : 0;
+  const int q_excl = pair_prefix != nullptr ? block_exclusive_scan_1024(pairs, s_warp, lane, warp, &s_total[2]) : 0;
   const bool bad = s_bad != 0;
   if (tid < E) {
     tile_prefix[tid] = bad ? 0 : t_excl;
     if (pad_indptr != nullptr) pad_indptr[tid] = bad ? 0 : p_excl;
+    if (pair_prefix != nullptr) pair_prefix[tid] = bad ? 0 : q_excl;
   }
   if (tid == 0) {
     tile_prefix[E] = bad ? 0 : s_total[0];
     if (pad_indptr != nullptr) pad_indptr[E] = bad ? 0 : s_total[1];
+    if (pair_prefix != nullptr) pair_prefix[E] = bad ? 0 : s_total[2];
   }
   if (bad && tid == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_INDPTR);
 }
@@ -1173,12 +1286,13 @@ int make_out_bf16_3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t ro
 // Launches one grouped GEMM.  `tiles` is the number of tiles the persistent grid walks (for
 // RowsM an upper bound: the device schedule decides); the grid is at most one CTA per SM.
 // With CL > 1 the grid is made of clusters of CL CTAs (tiles must be a multiple of CL), as
-// many as can be resident at once.
-template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT = 0, Gather G = Gather::None, int CL = 1>
+// many as can be resident at once.  PAIR: `tiles` counts 256-row pair tiles, one per cluster.
+template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT = 0, Gather G = Gather::None, int CL = 1,
+          int PAIR = 0>
 int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc0, const CUtensorMap& tc1,
                 const Params& p, long long tiles, const DeviceInfo& dev, cudaStream_t s, const char* name) {
-  auto kern = grouped_gemm_kernel<S, EP, A_MN, B_MN, SPLIT, G, CL>;
-  constexpr int kSmem = LayoutOf<EP, SPLIT>::kSmemBytes;
+  auto kern = grouped_gemm_kernel<S, EP, A_MN, B_MN, SPLIT, G, CL, PAIR>;
+  constexpr int kSmem = LayoutOf<EP, SPLIT, PAIR>::kSmemBytes;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters = 0;
@@ -1210,7 +1324,7 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
     KernelScope trace(name, s);
     kern<<<grid, kThreads, kSmem, s>>>(ta, tb, tc0, tc1, p);
   } else {
-    const long long groups = tiles / CL;
+    const long long groups = PAIR ? tiles : tiles / CL;  // pair: one tile per cluster
     const int clusters = static_cast<int>(groups < max_clusters ? groups : max_clusters);
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr{};
@@ -1257,6 +1371,14 @@ void set_gather(Params& p, const int32_t* row_to_slot, long long R, int k) {
 
 // Upper bound on the RowsM tile count: sum over experts of ceil(rows_e / BM) N tiles.
 long long rows_m_tiles(long long R, int E, int n_tiles) { return ((R + BM - 1) / BM + E) * n_tiles; }
+// the same bound for 256-row pair tiles
+long long pair_m_tiles(long long R, int E, int n_tiles) { return ((R + 2 * BM - 1) / (2 * BM) + E) * n_tiles; }
+
+// The forward GEMMs run as 2-SM pairs when experts hold at least 512 rows on average.  A pair
+// tile spans 256 rows of one expert, so below that the rows wasted in each expert's last tile
+// (up to 255 instead of 127) cost more than the pairs gain (measured on GB300: about even at
+// 512 rows per expert, slower at 256).
+bool use_pairs(const FwdGemmArgs& a) { return a.pair_prefix != nullptr && a.R >= 512LL * a.E; }
 
 int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -1265,10 +1387,10 @@ int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 size_t schedule_bytes(int E) { return align_up(sizeof(int32_t) * (E + 1), 256); }
 
 int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, int32_t* tile_prefix, int32_t* pad_indptr,
-                         const DeviceInfo& dev, cudaStream_t s) {
+                         const DeviceInfo& dev, cudaStream_t s, int32_t* pair_prefix) {
   {
     KernelScope trace("tile_schedule", s);
-    tile_schedule_kernel<<<1, 1024, 0, s>>>(m_indptr, E, R, tile_prefix, pad_indptr, dev.err_flag);
+    tile_schedule_kernel<<<1, 1024, 0, s>>>(m_indptr, E, R, tile_prefix, pad_indptr, pair_prefix, dev.err_flag);
   }
   return check_launch("tile_schedule");
 }
@@ -1329,6 +1451,12 @@ int launch_gate_up(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) 
   if (a.gu_perm == nullptr) tc1 = tc0;
   if (a.h_perm == nullptr && a.gu_perm == nullptr) return LIGER_MOE_OK;
   const long long tiles = rows_m_tiles(a.R, a.E, p.n_tiles);
+  if (use_pairs(a) && !gather && a.act == LIGER_MOE_ACT_SWIGLU) {
+    // 2-SM pairs over 256-row blocks: the even CTA loads the gate rows of B, the odd one the up rows
+    p.tile_prefix = a.pair_prefix;
+    return launch_gemm<Sched::RowsM, Epi::SwiGLU, false, false, 0, Gather::None, 2, 1>(
+        ta, tb, tc0, tc1, p, pair_m_tiles(a.R, a.E, p.n_tiles), dev, s, "gemm_gate_up_swiglu");
+  }
   if (a.act != LIGER_MOE_ACT_SWIGLU) {  // the other gated activations read x_perm
     if (gather) return LIGER_MOE_ERR_INVALID_ARG;
     return launch_gemm<Sched::RowsM, Epi::GLU, false, false>(ta, tb, tc0, tc1, p, tiles, dev, s, "gemm_gate_up_glu");
@@ -1369,7 +1497,9 @@ int launch_router_logits(const uint16_t* x, const uint16_t* w_router, const floa
 int launch_down(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   if (a.R == 0) return LIGER_MOE_OK;
   CUtensorMap ta, tb;
-  if (make_tmap(&ta, a.h_perm, a.I, a.R, BK, BM) || make_tmap(&tb, a.w_down, a.I, 1ULL * a.H * a.E, BK, BN))
+  const bool pair = use_pairs(a);  // 2-SM pairs: each CTA loads 128 of a tile's 256 B rows
+  if (make_tmap(&ta, a.h_perm, a.I, a.R, BK, BM) ||
+      make_tmap(&tb, a.w_down, a.I, 1ULL * a.H * a.E, BK, pair ? BN / 2 : BN))
     return LIGER_MOE_ERR_LAUNCH;
   Params p = base_params(a.m_indptr, a.tile_prefix, a.E, dev.err_flag);
   p.n_tiles = cdiv(a.H, BN);
@@ -1382,6 +1512,11 @@ int launch_down(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.row_scale = a.w_perm;
   CUtensorMap tc0;
   if (make_out_bf16(&tc0, a.y_perm, a.H, a.R)) return LIGER_MOE_ERR_LAUNCH;
+  if (pair) {
+    p.tile_prefix = a.pair_prefix;
+    return launch_gemm<Sched::RowsM, Epi::ScaleRows, false, false, 0, Gather::None, 2, 1>(
+        ta, tb, tc0, tc0, p, pair_m_tiles(a.R, a.E, p.n_tiles), dev, s, "gemm_down_scale");
+  }
   return launch_gemm<Sched::RowsM, Epi::ScaleRows, false, false>(ta, tb, tc0, tc0, p,
                                                                   rows_m_tiles(a.R, a.E, p.n_tiles), dev, s,
                                                                   "gemm_down_scale");

@@ -65,9 +65,10 @@ int launch_router_logits(const uint16_t* x, const uint16_t* w_router, const floa
                          float* logits, const DeviceInfo& dev, cudaStream_t s);
 // Tile schedule: tile_prefix[e] = sum over e' < e of ceil(rows_e' / 128); [E] = total.
 size_t schedule_bytes(int E);
-// With pad_indptr != NULL it also receives the padded row prefix (row counts rounded up to 16).
+// With pad_indptr != NULL it also receives the padded row prefix (row counts rounded up to 16);
+// with pair_prefix != NULL the prefix of 256-row blocks (the 2-SM pair GEMMs' tiles).
 int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, int32_t* tile_prefix, int32_t* pad_indptr,
-                         const DeviceInfo& dev, cudaStream_t s);
+                         const DeviceInfo& dev, cudaStream_t s, int32_t* pair_prefix = nullptr);
 
 struct FwdGemmArgs {
   const uint16_t* x_perm;       // [R, H]; used when x is NULL
@@ -76,6 +77,7 @@ struct FwdGemmArgs {
   int T, k;                     // (gather only)
   const int32_t* m_indptr;
   const int32_t* tile_prefix;
+  const int32_t* pair_prefix = nullptr;  // 256-row block prefix: the pair GEMMs run when set
   const uint16_t* w_gate_up;
   const uint16_t* w_down;
   const float* w_perm;
@@ -95,6 +97,7 @@ int launch_down(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s);
 struct BwdGemmArgs {
   const int32_t* m_indptr;
   const int32_t* tile_prefix;
+  const int32_t* pair_prefix = nullptr;  // 256-row block prefix: the pair GEMMs run when set
   const uint16_t* w_gate_up;
   const uint16_t* w_down;
   const uint16_t* x_perm;   // [R, H]; used when x is NULL

@@ -63,6 +63,15 @@ def assert_close(got, ref, name, max_rel=MAX_REL_TOL, mean_rel=MEAN_REL_TOL, per
     return mx, mn
 
 
+def off_selection(ids: np.ndarray, E: int) -> np.ndarray:
+    """[T, E] mask, True where expert e is not among token t's selected ids (where d_logits must
+    be exactly zero).  Taken from the routing itself: a selected entry may be zero too."""
+    ids = np.asarray(ids, dtype=np.int64)
+    mask = np.ones((ids.shape[0], E), dtype=bool)
+    np.put_along_axis(mask, ids, False, axis=1)
+    return mask
+
+
 def topk_bruteforce(logits: np.ndarray, k: int) -> np.ndarray:
     """Selected experts per token: full sort by (logit descending, id ascending)."""
     T, E = logits.shape
