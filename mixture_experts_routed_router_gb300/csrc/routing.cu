@@ -35,6 +35,14 @@ __device__ __forceinline__ uint64_t route_key(float v, int e) {
   return (static_cast<uint64_t>(ord) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(e));
 }
 
+// The logit back from a key: the order map above is one-to-one on non-NaN floats (with -0.0
+// folded into +0.0); a NaN comes back as a NaN.
+__device__ __forceinline__ float key_value(uint64_t key) {
+  const uint32_t ord = static_cast<uint32_t>(key >> 32);
+  if (ord == 0u) return __uint_as_float(0x7FFFFFFFu);
+  return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
+}
+
 __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
   uint32_t lo = __shfl_xor_sync(kFull, static_cast<uint32_t>(v), m);
   uint32_t hi = __shfl_xor_sync(kFull, static_cast<uint32_t>(v >> 32), m);
@@ -70,7 +78,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     // array stays in registers)
 #pragma unroll
     for (int i = 0; i < EPL; ++i) key[i] = (key[i] == best) ? 0ull : key[i];
-    const float v = __ldg(row + id);
+    const float v = key_value(best);  // the winner's logit, without another load
     if (j == 0) top = v;
     if (lane == j) {
       my_val = v;
