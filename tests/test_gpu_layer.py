@@ -25,6 +25,7 @@ CASES = [
     # at least 512 rows per expert: the forward GEMMs run as 2-SM pairs over 256-row tiles
     W("pairs_T2048_H256_I128_E8_k2", 2048, 256, 128, 8, 2),
     W("pairs_zipf_T2048_H320_I192_E4_k2", 2048, 320, 192, 4, 2, zipf_s=1.2, router_std=0.3),  # ragged, skewed
+    W("limits_T64_H128_I64_E1024_k32", 64, 128, 64, 1024, 32, router_std=0.3),  # the largest E and k
 ]
 
 
