@@ -62,7 +62,8 @@ constexpr int kDhSetBytes = 6 * kDhBoxBytes;    // six output boxes per 16 colum
 //   SPLIT = 0: one A and one B tile per stage (48 KB), 4 stages;
 //   SPLIT = 1: A as two bf16 parts (hi, lo) + B (64 KB), 3 stages: two MMAs per K step share B;
 //   SPLIT = 2: A + B as two parts (80 KB), 2 stages: two MMAs per K step share A.
-//   PAIR: a CTA of a 2-SM pair holds its 128 rows of A and half of B's rows (32 KB), 6 stages.
+//   PAIR: a CTA of a 2-SM pair holds its 128 rows (RowsM) or columns (RowsK) of A and half of B's
+//         256 rows or columns: 32 KB and 6 stages, or 48 KB and 4 stages with hi/lo parts.
 // Epilogue staging per warp: one 4 KB box, or for the dH kernel one set of six 1 KB boxes
 // (3 operand stages there: its MMAs are a small part of its time).
 template <int kDh, int SPLIT, int PAIR = 0>
@@ -70,7 +71,8 @@ struct Layout {
   static constexpr int kABytes = A_BYTES * (SPLIT == 1 ? 2 : 1);
   static constexpr int kBBytes = B_BYTES * (SPLIT == 2 ? 2 : 1) / (PAIR ? 2 : 1);
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = PAIR ? (kDh ? 4 : 6) : (kDh ? 3 : (SPLIT == 0 ? 4 : (SPLIT == 1 ? 3 : 2)));
+  static constexpr int kStages =
+      PAIR ? (kDh ? 4 : (SPLIT == 0 ? 6 : 4)) : (kDh ? 3 : (SPLIT == 0 ? 4 : (SPLIT == 1 ? 3 : 2)));
   static constexpr int kStgWarpBytes = kDh ? kDhSetBytes : STG_PER_WARP * STG_BYTES;
   static constexpr int kStgOffset = kStages * kStageBytes;
   static constexpr int kBarOffset = kStgOffset + kEpiWarps * kStgWarpBytes;
@@ -198,10 +200,29 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p) {
   return tl;
 }
 
-// RowsM tile of a 2-SM pair: tile_prefix counts 256-row blocks per expert; CTA `rank` of the
-// pair owns rows [m0, m0 + 128) of the block (none when the expert ends before them).
+// Tile of a 2-SM pair.  RowsM: tile_prefix counts 256-row blocks per expert; CTA `rank` of the
+// pair owns rows [m0, m0 + 128) of the block (none when the expert ends before them).  RowsK:
+// CTA `rank` owns output rows [m0, m0 + 128) of the expert's weight gradient.
+template <Sched S>
 __device__ __forceinline__ Tile decode_tile_pair(int t, const Params& p, uint32_t rank) {
   Tile tl;
+  if constexpr (S == Sched::RowsK) {
+    // weight gradients: the pair covers M blocks 2 mp and 2 mp + 1 of the expert's output; pair
+    // blocks fastest, so neighbouring pairs share the expert and the N block
+    const int mpt = p.m_tiles / 2;
+    const int per_e = mpt * p.n_tiles;
+    tl.e = t / per_e;
+    const int r = t - tl.e * per_e;
+    tl.nt = r / mpt;
+    const int mp = r - tl.nt * mpt;
+    tl.m0 = mp * (2 * BM) + static_cast<int>(rank) * BM;
+    tl.row0 = __ldg(p.m_indptr + tl.e);
+    tl.rows = __ldg(p.m_indptr + tl.e + 1) - tl.row0;
+    tl.am0 = tl.m0;
+    tl.prow0 = p.pad_indptr != nullptr ? __ldg(p.pad_indptr + tl.e) : tl.row0;
+    tl.kb_count = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
+    return tl;
+  }
   const int mt = t / p.n_tiles;
   tl.nt = t - mt * p.n_tiles;
   int lo = 0, hi = p.E;  // tile_prefix[lo] <= mt < tile_prefix[hi]
@@ -735,10 +756,30 @@ __device__ __forceinline__ void load_stage_tiled(const CUtensorMap* tmA, const C
 // B's 256 rows, both completing on the even CTA's full barrier (`bar`, a shared::cluster
 // address), which expects the bytes of both CTAs.  Gate/up tiles put the gate rows in the even
 // CTA and the up rows in the odd one, so the accumulator columns stay [g | u].
-template <Epi EP, bool B_MN>
+template <Sched S, Epi EP, bool B_MN, int SPLIT>
 __device__ __forceinline__ void load_stage_pair(const CUtensorMap* tmA, const CUtensorMap* tmB, const Params& p,
                                                 const Tile& tl, int kb, uint32_t sa, uint32_t sb, uint32_t bar,
                                                 uint32_t rank) {
+  if constexpr (S == Sched::RowsK) {
+    // weight gradients, both operands MN-major with the expert's rows as K: this CTA's 128 M
+    // columns of A (two 64-column boxes, hi and lo parts for SPLIT 1) and its 128 of the N
+    // block's 256 columns of B (hi and lo parts for SPLIT 2)
+    const int krow_a = (p.pad_a ? tl.prow0 : tl.row0) + kb * BK;
+    const int krow_b = (p.pad_b ? tl.prow0 : tl.row0) + kb * BK;
+#pragma unroll
+    for (int part = 0; part < (SPLIT == 1 ? 2 : 1); ++part)
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        tma_load_2d_pair(sa + part * A_BYTES + i * MN_BOX_BYTES, tmA, bar, tl.m0 + 64 * i,
+                         krow_a + part * p.a_split_rows);
+#pragma unroll
+    for (int part = 0; part < (SPLIT == 2 ? 2 : 1); ++part)
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        tma_load_2d_pair(sb + part * (B_BYTES / 2) + i * MN_BOX_BYTES, tmB, bar,
+                         tl.nt * BN + static_cast<int>(rank) * (BN / 2) + 64 * i, krow_b + part * p.b_split_rows);
+    return;
+  }
   tma_load_2d_pair(sa, tmA, bar, kb * BK, tl.m0);  // A box: 128 rows (past R: zero fill)
   if constexpr (!B_MN) {
     const int r = gate_up_epi(EP) ? tl.e * p.b_rows_per_expert + tl.nt * (BN / 2) + (rank ? p.b_split : 0)
@@ -796,8 +837,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const Params p) {
   using L = LayoutOf<EP, SPLIT, PAIR>;
   constexpr bool kPair = PAIR != 0;
-  static_assert(!kPair || (CL == 2 && S == Sched::RowsM && G == Gather::None && !A_MN && SPLIT == 0),
-                "2-SM pairs: RowsM tiles with K-major A, one operand part, no gather");
+  static_assert(!kPair || (CL == 2 && G == Gather::None &&
+                            ((S == Sched::RowsM && !A_MN && SPLIT == 0) || (S == Sched::RowsK && A_MN && B_MN))),
+                "2-SM pairs: RowsM tiles with K-major A and one operand part, or RowsK tiles, no gather");
   constexpr int STAGES = L::kStages;
   constexpr int STAGE_BYTES = L::kStageBytes;
   constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CL) - 1u);
@@ -810,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tstride = kPair ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
   auto decode = [&](int t) -> Tile {
     if constexpr (kPair)
-      return decode_tile_pair(t, p, rank);
+      return decode_tile_pair<S>(t, p, rank);
     else
       return decode_tile<S>(t, p);
   };
@@ -877,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   else if constexpr (S == Sched::Dense)
     total = static_cast<int>((p.R + BM - 1) / BM) * p.n_tiles;
   else
-    total = p.E * p.m_tiles * p.n_tiles;
+    total = p.E * (kPair ? p.m_tiles / 2 : p.m_tiles) * p.n_tiles;  // pair: M blocks two at a time
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -899,7 +941,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (kPair) {
               // the even CTA's full barrier counts both CTAs' bytes of this stage
               if (leader) mbar_arrive_expect_tx(fb, 2 * STAGE_BYTES);
-              load_stage_pair<EP, B_MN>(&tmA, &tmB, p, tl, kb, sa, sa + L::kABytes, mapa_shared(fb, 0), rank);
+              load_stage_pair<S, EP, B_MN, SPLIT>(&tmA, &tmB, p, tl, kb, sa, sa + L::kABytes, mapa_shared(fb, 0),
+                                                  rank);
             } else {
               mbar_arrive_expect_tx(fb, STAGE_BYTES);
               load_stage_tiled<S, EP, A_MN, B_MN, SPLIT, true, true, CL>(&tmA, &tmB, p, tl, kb, sa, sa + L::kABytes,
@@ -1047,10 +1090,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               umma_bf16_f32_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
             else
               umma_bf16_f32(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-            if constexpr (SPLIT == 1)  // lo part of A against the same B
-              umma_bf16_f32(d_tmem, smem_desc_sw128(sa + A_BYTES + kk * 2048, MN_BOX_BYTES, 1024), bd, idesc, 1u);
-            if constexpr (SPLIT == 2)  // the same A against the lo part of B
-              umma_bf16_f32(d_tmem, ad, smem_desc_sw128(sb + B_BYTES + kk * 2048, MN_BOX_BYTES, 1024), idesc, 1u);
+            if constexpr (SPLIT == 1) {  // lo part of A against the same B
+              const uint64_t lo = smem_desc_sw128(sa + A_BYTES + kk * 2048, MN_BOX_BYTES, 1024);
+              if constexpr (kPair)
+                umma_bf16_f32_pair(d_tmem, lo, bd, idesc, 1u);
+              else
+                umma_bf16_f32(d_tmem, lo, bd, idesc, 1u);
+            }
+            if constexpr (SPLIT == 2) {  // the same A against the lo part of B (half of it per CTA in a pair)
+              const uint64_t lo = smem_desc_sw128(sb + L::kBBytes / 2 + kk * 2048, MN_BOX_BYTES, 1024);
+              if constexpr (kPair)
+                umma_bf16_f32_pair(d_tmem, ad, lo, idesc, 1u);
+              else
+                umma_bf16_f32(d_tmem, ad, lo, idesc, 1u);
+            }
           }
           if constexpr (kPair)
             umma_commit_pair_mc(empty0 + 8 * stage, kClusterMask);  // both CTAs' stage is free
@@ -1620,15 +1673,15 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.ld_out = a.H;
   p.out_expert_stride = static_cast<long long>(a.nin) * a.H;
   if (make_out_bf16_3d(&tc0, a.dw_gate_up, a.H, nin, a.E)) return LIGER_MOE_ERR_LAUNCH;
-  // CTA pairs over neighbouring M blocks share the x tile (multicast) when the M blocks pair up
+  // CTA pairs over neighbouring M blocks when the M blocks pair up
   const long long tiles_gu = static_cast<long long>(a.E) * p.m_tiles * p.n_tiles;
   int rc;
   if (gather_x)
     rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::B>(ta, tb, tc0, tc0, p, tiles_gu, dev, s,
                                                                          "gemm_bwd_dw_gate_up");
-  else if (p.m_tiles % 2 == 0)
-    rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::None, 2>(ta, tb, tc0, tc0, p, tiles_gu, dev, s,
-                                                                               "gemm_bwd_dw_gate_up");
+  else if (p.m_tiles % 2 == 0)  // 2-SM pairs over neighbouring M blocks, each CTA holding half of the x tile
+    rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::None, 2, 1>(ta, tb, tc0, tc0, p, tiles_gu / 2,
+                                                                                  dev, s, "gemm_bwd_dw_gate_up");
   else
     rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1>(ta, tb, tc0, tc0, p, tiles_gu, dev, s,
                                                               "gemm_bwd_dw_gate_up");
@@ -1656,14 +1709,14 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.ld_out = a.I;
   p.out_expert_stride = 1LL * a.H * a.I;
   if (make_out_bf16_3d(&tc0, a.dw_down, a.I, a.H, a.E)) return LIGER_MOE_ERR_LAUNCH;
-  // CTA pairs over neighbouring M blocks share the two parts of the w h tile (multicast)
+  // CTA pairs over neighbouring M blocks (2-SM MMAs) when the M blocks pair up
   const long long tiles_d = static_cast<long long>(a.E) * p.m_tiles * p.n_tiles;
   if (gather_dy)
     return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::A>(ta, tb, tc0, tc0, p, tiles_d, dev, s,
                                                                            "gemm_bwd_dw_down");
-  if (p.m_tiles % 2 == 0)
-    return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::None, 2>(ta, tb, tc0, tc0, p, tiles_d, dev, s,
-                                                                                 "gemm_bwd_dw_down");
+  if (p.m_tiles % 2 == 0)  // 2-SM pairs over neighbouring M blocks, each CTA holding half of the w h tile
+    return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::None, 2, 1>(ta, tb, tc0, tc0, p, tiles_d / 2,
+                                                                                    dev, s, "gemm_bwd_dw_down");
   return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2>(ta, tb, tc0, tc0, p, tiles_d, dev, s, "gemm_bwd_dw_down");
 }
 
