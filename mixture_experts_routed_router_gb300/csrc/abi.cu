@@ -168,7 +168,7 @@ long long padded_rows(long long R, int E) { return R + 15LL * E; }
 
 size_t bwd_workspace_bytes(long long R, int H, int I, int E, bool recompute_gu, bool gather) {
   const long long Rp = padded_rows(R, E);
-  size_t b = 2 * schedule_bytes(E);                                   // tile prefix, padded row prefix
+  size_t b = 3 * schedule_bytes(E);  // tile prefix, padded row prefix, 256-row pair block prefix
   if (!gather) b += align_up(static_cast<size_t>(R) * H * 2, 256);  // dy_perm
   b += align_up(static_cast<size_t>(Rp) * 2 * I * 2 * 2, 256);        // dgu (hi, lo), padded rows
   b += align_up(static_cast<size_t>(R) * H * 2, 256);                 // dx_perm
@@ -386,6 +386,7 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
   const long long Rp = padded_rows(R, E);
   int32_t* tile_prefix = carve<int32_t>(cur, schedule_bytes(E));
   int32_t* pad_indptr = carve<int32_t>(cur, schedule_bytes(E));
+  int32_t* pair_prefix = carve<int32_t>(cur, schedule_bytes(E));
   uint16_t* dy_perm = gather ? nullptr : carve<uint16_t>(cur, static_cast<size_t>(R) * H * 2);
   uint16_t* dgu = carve<uint16_t>(cur, static_cast<size_t>(Rp) * 2 * I * 2 * 2);
   uint16_t* dx_perm = carve<uint16_t>(cur, static_cast<size_t>(R) * H * 2);
@@ -396,6 +397,7 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
   BwdGemmArgs a{};
   a.m_indptr = m_indptr;
   a.tile_prefix = tile_prefix;
+  a.pair_prefix = pair_prefix;
   a.w_gate_up = static_cast<const uint16_t*>(w_gate_up);
   a.w_down = static_cast<const uint16_t*>(w_down);
   a.x_perm = static_cast<const uint16_t*>(x_perm);
@@ -423,7 +425,7 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
   a.nin = act == LIGER_MOE_ACT_RELU2 ? I : 2 * I;  // ReLU²: one up weight, one factor, da [.., I]
 
   if (R > 0) {
-    if (int rc = launch_tile_schedule(m_indptr, E, R, tile_prefix, pad_indptr, dev, s)) return rc;
+    if (int rc = launch_tile_schedule(m_indptr, E, R, tile_prefix, pad_indptr, dev, s, pair_prefix)) return rc;
     if (!gather) {  // dy_perm[r] = dY[token of r]: the dH and dW_down GEMMs read it as dense tiles
       if (int rc = launch_gather_rows(static_cast<const uint16_t*>(dy), row_to_slot, nullptr, R, H, k, dy_perm, dev, s))
         return rc;

@@ -239,7 +239,7 @@ __device__ __forceinline__ Tile decode_tile_pair(int t, const Params& p, uint32_
   tl.m0 = start + (mt - __ldg(p.tile_prefix + lo)) * (2 * BM) + static_cast<int>(rank) * BM;
   tl.rows = max(0, min(BM, end - tl.m0));
   tl.row0 = 0;
-  tl.am0 = tl.m0;
+  tl.am0 = p.pad_indptr != nullptr ? __ldg(p.pad_indptr + lo) + (tl.m0 - start) : tl.m0;
   tl.prow0 = 0;
   tl.kb_count = p.num_kb;
   return tl;
@@ -672,12 +672,10 @@ __device__ __forceinline__ void store_zero_tile(const Tile& tl, int sub, int col
 // earlier proved too early: in the epilogue-bound dH kernel a tile takes tens of microseconds,
 // and the prefetched lines were evicted before use.
 template <Sched S, Epi EP>
-__device__ __forceinline__ void prefetch_epilogue_operands(int t, int total, int row_local, int colhalf,
+__device__ __forceinline__ void prefetch_epilogue_operands(const Tile& tl, int row_local, int colhalf,
                                                            const Params& p) {
   if constexpr (dh_epi(EP)) {
     constexpr int kFactors = EP == Epi::DH ? 2 : 1;  // [a | b] or a alone per row
-    if (t >= total) return;
-    const Tile tl = decode_tile<S>(t, p);
     if (row_local >= tl.rows) return;
     const long long r = tl.m0 + row_local;
     const int n0 = tl.nt * BN + colhalf * (BN / 2);
@@ -780,7 +778,7 @@ __device__ __forceinline__ void load_stage_pair(const CUtensorMap* tmA, const CU
                          tl.nt * BN + static_cast<int>(rank) * (BN / 2) + 64 * i, krow_b + part * p.b_split_rows);
     return;
   }
-  tma_load_2d_pair(sa, tmA, bar, kb * BK, tl.m0);  // A box: 128 rows (past R: zero fill)
+  tma_load_2d_pair(sa, tmA, bar, kb * BK, p.pad_a ? tl.am0 : tl.m0);  // A box: 128 rows (past the end: zeros)
   if constexpr (!B_MN) {
     const int r = gate_up_epi(EP) ? tl.e * p.b_rows_per_expert + tl.nt * (BN / 2) + (rank ? p.b_split : 0)
                                   : tl.e * p.b_rows_per_expert + tl.nt * BN + static_cast<int>(rank) * (BN / 2);
@@ -1152,7 +1150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile tl = decode(t);
       // the tile's epilogue operands (DH) start moving into L2 now, a tile's MMA time ahead of use
       // when the MMAs lead, and at least ahead of the later column chunks when the epilogue does
-      prefetch_epilogue_operands<S, EP>(t, total, row_local, colhalf, p);
+      prefetch_epilogue_operands<S, EP>(tl, row_local, colhalf, p);
       if (tl.kb_count == 0) {
         if constexpr (S == Sched::RowsK) store_zero_tile(tl, sub, colhalf, lane, p, &tmC0, st);
         continue;
@@ -1432,6 +1430,10 @@ long long pair_m_tiles(long long R, int E, int n_tiles) { return ((R + 2 * BM - 
 // (up to 255 instead of 127) cost more than the pairs gain (measured on GB300: about even at
 // 512 rows per expert, slower at 256).
 bool use_pairs(const FwdGemmArgs& a) { return a.pair_prefix != nullptr && a.R >= 512LL * a.E; }
+// The same rule for the backward's dX GEMM (gated experts, expert-major dY rows).
+bool use_pairs(const BwdGemmArgs& a) {
+  return a.pair_prefix != nullptr && a.R >= 512LL * a.E && a.dy_perm != nullptr && a.nin == 2 * a.I;
+}
 
 int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -1612,6 +1614,8 @@ int launch_bwd_dh(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   if (gather)
     return launch_gemm<Sched::RowsM, Epi::DH, false, true, 0, Gather::A>(ta, tb, tc0, tc1, p, tiles, dev, s,
                                                                         "gemm_bwd_dh");
+  // dH stays one CTA per tile at every load: its epilogue, not its operand pipeline, bounds it, and
+  // 2-SM pairs measured 5 % slower at 512 rows per expert (their 256-row tiles waste rows)
   return launch_gemm<Sched::RowsM, Epi::DH, false, true>(ta, tb, tc0, tc1, p, tiles, dev, s, "gemm_bwd_dh");
 }
 
@@ -1633,6 +1637,11 @@ int launch_bwd_dx(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.ld_out = a.H;
   CUtensorMap tc0;
   if (make_out_bf16(&tc0, a.dx_perm, a.H, a.R)) return LIGER_MOE_ERR_LAUNCH;
+  if (use_pairs(a)) {  // 2-SM pairs over 256-row blocks: each CTA loads half of the W_gu columns
+    p.tile_prefix = a.pair_prefix;
+    return launch_gemm<Sched::RowsM, Epi::Store, false, true, 0, Gather::None, 2, 1>(
+        ta, tb, tc0, tc0, p, pair_m_tiles(a.R, a.E, p.n_tiles), dev, s, "gemm_bwd_dx");
+  }
   return launch_gemm<Sched::RowsM, Epi::Store, false, true>(ta, tb, tc0, tc0, p, rows_m_tiles(a.R, a.E, p.n_tiles),
                                                              dev, s, "gemm_bwd_dx");
 }
