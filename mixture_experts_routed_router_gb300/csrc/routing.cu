@@ -17,36 +17,23 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 // Router: top-k + renormalised softmax.  LightMoE README, "MoE inference"
 // (top_k_ids distinct per token, top_k_weights float32) and "MoE training"
 // (differentiable_probs).  One warp per token; lane i holds experts
-// i, i+32, ... as 64-bit keys
-//    key = (order-preserving bits of the logit) << 32 | (0xFFFFFFFF - id)
-// so the warp-wide maximum is the largest logit, ties to the smallest id.
-// NaN maps to the lowest order value; -0.0 is treated as +0.0.  A selected
-// expert's key is set to 0, below every valid key.
+// i, i+32, ... as the order-preserving bits of their logits (NaN lowest,
+// -0.0 as +0.0).  Each round takes the warp-wide maximum of those bits with one
+// reduction, then the smallest expert id among the lanes that hold it with a
+// second: the largest logit wins, ties go to the smallest id.
 // ============================================================================
-__device__ __forceinline__ uint64_t route_key(float v, int e) {
+__device__ __forceinline__ uint32_t route_ord(float v) {
   uint32_t u = __float_as_uint(v);
-  uint32_t ord;
-  if ((u & 0x7FFFFFFFu) > 0x7F800000u) {
-    ord = 0u;
-  } else {
-    if (u == 0x80000000u) u = 0u;
-    ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  }
-  return (static_cast<uint64_t>(ord) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(e));
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0u;  // NaN: below every number
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// The logit back from a key: the order map above is one-to-one on non-NaN floats (with -0.0
+// The logit back from its order bits: the map above is one-to-one on non-NaN floats (with -0.0
 // folded into +0.0); a NaN comes back as a NaN.
-__device__ __forceinline__ float key_value(uint64_t key) {
-  const uint32_t ord = static_cast<uint32_t>(key >> 32);
+__device__ __forceinline__ float ord_value(uint32_t ord) {
   if (ord == 0u) return __uint_as_float(0x7FFFFFFFu);
   return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
-}
-
-__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
-  uint32_t lo = __shfl_xor_sync(kFull, static_cast<uint32_t>(v), m);
-  uint32_t hi = __shfl_xor_sync(kFull, static_cast<uint32_t>(v >> 32), m);
-  return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
 template <int EPL>
@@ -56,29 +43,40 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   const long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
   const float* row = logits + t * E;
-  uint64_t key[EPL];
+  // order bits + 1 of the lane's experts; 0 = no expert there, or already selected
+  uint32_t ord1[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = i * 32 + lane;
-    key[i] = (e < E) ? route_key(__ldg(row + e), e) : 0ull;
+    ord1[i] = (e < E) ? route_ord(__ldg(row + e)) + 1u : 0u;  // +inf gives 0xFF800001: no overflow
   }
+  // the lane's best: largest value, then smallest slot i (= smallest id within the lane)
+  uint32_t bv = 0u;
+  int bi = 0;
+  auto lane_best = [&]() {
+    bv = 0u;
+    bi = 0;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (ord1[i] > bv) {
+        bv = ord1[i];
+        bi = i;
+      }
+  };
+  lane_best();
   float my_val = 0.f, top = 0.f;
   int my_id = 0;
   for (int j = 0; j < k; ++j) {
-    uint64_t best = key[0];
+    const uint32_t m = __reduce_max_sync(kFull, bv);
+    const uint32_t cand = (bv == m) ? static_cast<uint32_t>(bi * 32 + lane) : 0xFFFFFFFFu;
+    const int id = static_cast<int>(__reduce_min_sync(kFull, cand));
+    if ((id & 31) == lane) {  // the winner's lane takes it out and finds its next best
 #pragma unroll
-    for (int i = 1; i < EPL; ++i) best = key[i] > best ? key[i] : best;
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) {
-      const uint64_t o = shfl_xor_u64(best, m);
-      best = o > best ? o : best;
+      for (int i = 0; i < EPL; ++i)
+        if (i == (id >> 5)) ord1[i] = 0u;
+      lane_best();
     }
-    const int id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best));
-    // clear the winner's key in place (compare against the key itself so the
-    // array stays in registers)
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) key[i] = (key[i] == best) ? 0ull : key[i];
-    const float v = key_value(best);  // the winner's logit, without another load
+    const float v = ord_value(m - 1u);  // the winner's logit, without another load
     if (j == 0) top = v;
     if (lane == j) {
       my_val = v;
