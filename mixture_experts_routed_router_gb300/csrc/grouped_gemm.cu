@@ -1682,15 +1682,22 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.ld_out = a.H;
   p.out_expert_stride = static_cast<long long>(a.nin) * a.H;
   if (make_out_bf16_3d(&tc0, a.dw_gate_up, a.H, nin, a.E)) return LIGER_MOE_ERR_LAUNCH;
-  // CTA pairs over neighbouring M blocks when the M blocks pair up
+  // CTA pairs over neighbouring M blocks when the M blocks pair up: 2-SM MMAs (each CTA holding half
+  // of the x tile) when experts hold at least 192 rows on average, else two CTAs that share the x
+  // tile by multicast.  With few rows per expert the tiles are mostly gradient writes, and a 2-SM
+  // pair ties the two CTAs' epilogues to each other (measured on GB300: slower at 4 and 160 rows
+  // per expert, faster at 256 and 512).
   const long long tiles_gu = static_cast<long long>(a.E) * p.m_tiles * p.n_tiles;
   int rc;
   if (gather_x)
     rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::B>(ta, tb, tc0, tc0, p, tiles_gu, dev, s,
                                                                          "gemm_bwd_dw_gate_up");
-  else if (p.m_tiles % 2 == 0)  // 2-SM pairs over neighbouring M blocks, each CTA holding half of the x tile
+  else if (p.m_tiles % 2 == 0 && a.R >= 192LL * a.E)
     rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::None, 2, 1>(ta, tb, tc0, tc0, p, tiles_gu / 2,
                                                                                   dev, s, "gemm_bwd_dw_gate_up");
+  else if (p.m_tiles % 2 == 0)
+    rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::None, 2>(ta, tb, tc0, tc0, p, tiles_gu, dev, s,
+                                                                               "gemm_bwd_dw_gate_up");
   else
     rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1>(ta, tb, tc0, tc0, p, tiles_gu, dev, s,
                                                               "gemm_bwd_dw_gate_up");
@@ -1718,14 +1725,19 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.ld_out = a.I;
   p.out_expert_stride = 1LL * a.H * a.I;
   if (make_out_bf16_3d(&tc0, a.dw_down, a.I, a.H, a.E)) return LIGER_MOE_ERR_LAUNCH;
-  // CTA pairs over neighbouring M blocks (2-SM MMAs) when the M blocks pair up
+  // CTA pairs over neighbouring M blocks when the M blocks pair up: 2-SM MMAs (each CTA holding half
+  // of the w h tile, 4 stages instead of 2) from 128 rows per expert on average, else two CTAs that
+  // share the w h tile by multicast (measured: slower as pairs at 4 rows per expert, faster at 160)
   const long long tiles_d = static_cast<long long>(a.E) * p.m_tiles * p.n_tiles;
   if (gather_dy)
     return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::A>(ta, tb, tc0, tc0, p, tiles_d, dev, s,
                                                                            "gemm_bwd_dw_down");
-  if (p.m_tiles % 2 == 0)  // 2-SM pairs over neighbouring M blocks, each CTA holding half of the w h tile
+  if (p.m_tiles % 2 == 0 && a.R >= 128LL * a.E)
     return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::None, 2, 1>(ta, tb, tc0, tc0, p, tiles_d / 2,
                                                                                     dev, s, "gemm_bwd_dw_down");
+  if (p.m_tiles % 2 == 0)
+    return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::None, 2>(ta, tb, tc0, tc0, p, tiles_d, dev, s,
+                                                                                 "gemm_bwd_dw_down");
   return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2>(ta, tb, tc0, tc0, p, tiles_d, dev, s, "gemm_bwd_dw_down");
 }
 
