@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -118,6 +119,14 @@ KernelScope::~KernelScope() {
 
 void set_cuda_error(cudaError_t e, const char* where) {
   std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("LIGER_MOE_PDL");
+    return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
+  }();
+  return on;
 }
 
 int check_launch(const char* where) {

@@ -910,6 +910,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  // barriers, TMEM and descriptors are ready: from here on the kernel reads what earlier kernels wrote
+  griddep_wait();
+  griddep_launch_dependents();
 
   int total;
   if constexpr (S == Sched::RowsM)
@@ -1234,6 +1237,8 @@ __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __re
   __shared__ int s_warp[32];
   __shared__ int s_bad;
   __shared__ int s_total[3];
+  griddep_wait();
+  griddep_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) s_bad = (m_indptr[0] != 0 || static_cast<long long>(m_indptr[E]) != R) ? 1 : 0;
   __syncthreads();
@@ -1370,32 +1375,16 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
     return LIGER_MOE_ERR_LAUNCH;
   }
   if (tiles < 1) return LIGER_MOE_OK;
+  int grid;
   if constexpr (CL == 1) {
-    const int grid = static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
-    KernelScope trace(name, s);
-    kern<<<grid, kThreads, kSmem, s>>>(ta, tb, tc0, tc1, p);
+    grid = static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
   } else {
     const long long groups = PAIR ? tiles : tiles / CL;  // pair: one tile per cluster
-    const int clusters = static_cast<int>(groups < max_clusters ? groups : max_clusters);
-    cudaLaunchConfig_t cfg{};
-    cudaLaunchAttribute attr{};
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = CL;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmem;
-    cfg.stream = s;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    KernelScope trace(name, s);
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc0, tc1, p);
-    if (e != cudaSuccess) {
-      set_cuda_error(e, name);
-      return LIGER_MOE_ERR_LAUNCH;
-    }
+    grid = static_cast<int>(groups < max_clusters ? groups : max_clusters) * CL;
   }
+  KernelScope trace(name, s);
+  if (launch_kernel(kern, dim3(grid), dim3(kThreads), kSmem, s, name, CL, ta, tb, tc0, tc1, p) != cudaSuccess)
+    return LIGER_MOE_ERR_LAUNCH;
   return check_launch(name);
 }
 
@@ -1445,7 +1434,9 @@ int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, int32_t* t
                          const DeviceInfo& dev, cudaStream_t s, int32_t* pair_prefix) {
   {
     KernelScope trace("tile_schedule", s);
-    tile_schedule_kernel<<<1, 1024, 0, s>>>(m_indptr, E, R, tile_prefix, pad_indptr, pair_prefix, dev.err_flag);
+    if (launch_kernel(tile_schedule_kernel, dim3(1), dim3(1024), 0, s, "tile_schedule", 1, m_indptr, E, R,
+                      tile_prefix, pad_indptr, pair_prefix, dev.err_flag) != cudaSuccess)
+      return LIGER_MOE_ERR_LAUNCH;
   }
   return check_launch("tile_schedule");
 }

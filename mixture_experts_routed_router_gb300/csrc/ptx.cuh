@@ -29,6 +29,18 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 
 // Makes mbarrier initialisation visible to the async proxy (TMA, tcgen05).
+// Programmatic dependent launch (optional, see pdl_enabled).  A kernel launched with programmatic
+// stream serialization may start while the kernel before it on the stream is still running:
+// `griddep_wait` blocks until that kernel has completed and its memory operations are visible (it
+// returns at once for a kernel launched without the attribute).  Every kernel of the library calls it before its first
+// global memory access, so each one sees all earlier work on the stream complete.
+// `griddep_launch_dependents` lets the next kernel on the stream be scheduled; the library calls
+// it right after the wait, so at most one kernel ahead is ever resident and waiting.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

@@ -51,6 +51,8 @@ __global__ void __launch_bounds__(256) router_dx_kernel(const float* __restrict_
                                                         const int32_t* __restrict__ ids,
                                                         const uint16_t* __restrict__ w_router, int T, int H, int E,
                                                         int k, uint16_t* __restrict__ dx, int* err) {
+  griddep_wait();  // earlier kernels on the stream are complete
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   const int chunks = H >> 3;  // 16-byte chunks of a row
@@ -134,6 +136,8 @@ __global__ void __launch_bounds__(kDwWarps * 32) router_dw_kernel(const float* _
                                                                   const uint16_t* __restrict__ x, int H, int E,
                                                                   int k, long long R, uint16_t* __restrict__ dw,
                                                                   float* __restrict__ d_bias, int* err) {
+  griddep_wait();  // earlier kernels on the stream are complete
+  griddep_launch_dependents();
   __shared__ float part[kDwWarps][kDwCols];
   __shared__ float part_b[kDwWarps];
   __shared__ int s_tok[kDwStage];
@@ -223,8 +227,8 @@ int launch_router_bwd(const float* d_logits, const int32_t* topk_ids, const int3
     {
       KernelScope trace("router_dx", s);
       const long long items = static_cast<long long>(T) * ((H / 8 + kDxSeg - 1) / kDxSeg);
-      router_dx_kernel<<<grid_warps(items, 8, dev), 256, 0, s>>>(d_logits, topk_ids, w_router, T, H, E, k, dx,
-                                                                dev.err_flag);
+      launch_kernel(router_dx_kernel, dim3(grid_warps(items, 8, dev)), dim3(256), 0, s, "router_dx", 1, d_logits,
+                    topk_ids, w_router, T, H, E, k, dx, dev.err_flag);
     }
     if (int rc = check_launch("router_dx")) return rc;
   }
@@ -232,8 +236,8 @@ int launch_router_bwd(const float* d_logits, const int32_t* topk_ids, const int3
     // every expert's block is written, zero for an expert with no rows
     KernelScope trace("router_dw", s);
     const dim3 grid(static_cast<unsigned>(E), static_cast<unsigned>((H + kDwCols - 1) / kDwCols));
-    router_dw_kernel<<<grid, kDwWarps * 32, 0, s>>>(d_logits, m_indptr, row_to_slot, x, H, E, k, R, dw_router,
-                                                     d_bias, dev.err_flag);
+    launch_kernel(router_dw_kernel, dim3(grid), dim3(kDwWarps * 32), 0, s, "router_dw", 1, d_logits, m_indptr,
+                  row_to_slot, x, H, E, k, R, dw_router, d_bias, dev.err_flag);
   }
   return check_launch("router_dw");
 }

@@ -39,6 +39,8 @@ __device__ __forceinline__ float ord_value(uint32_t ord) {
 template <int EPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                          int32_t* __restrict__ ids, float* __restrict__ w) {
+  griddep_wait();  // earlier kernels on the stream are complete
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
@@ -110,6 +112,8 @@ constexpr int kWarpsPerBlock = 8;
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) dispatch_hist_kernel(const int32_t* __restrict__ ids,
                                                                            long long R, int E, int nunits,
                                                                            int32_t* __restrict__ hist, int* err) {
+  griddep_wait();  // earlier kernels on the stream are complete
+  griddep_launch_dependents();
   extern __shared__ int s_hist[];
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.x * kWarpsPerBlock + wib;
@@ -137,6 +141,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) dispatch_hist_kernel(cons
 // One warp per expert: exclusive scan of hist[e][*] in place, counts[e] = total.
 __global__ void __launch_bounds__(256) dispatch_scan_kernel(int32_t* __restrict__ hist, int nunits, int E,
                                                             int32_t* __restrict__ counts) {
+  griddep_wait();  // earlier kernels on the stream are complete
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int e = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (e >= E) return;
@@ -195,6 +201,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) dispatch_scatter_kernel(
     const int32_t* __restrict__ ids, const float* __restrict__ w, long long R, int E, int nunits,
     const int32_t* __restrict__ base, const int32_t* __restrict__ counts, int32_t* __restrict__ m_indptr,
     int32_t* __restrict__ row_to_slot, int32_t* __restrict__ slot_to_row, float* __restrict__ w_perm) {
+  griddep_wait();  // earlier kernels on the stream are complete
+  griddep_launch_dependents();
   extern __shared__ int smem[];
   int* s_off = smem;                       // [E + 1]
   int* s_warp = s_off + (E + 1);           // [32]
@@ -239,6 +247,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
                                                           const int32_t* __restrict__ row_to_slot,
                                                           const float* __restrict__ scale, long long R, int H, int k,
                                                           uint16_t* __restrict__ dst, int* err) {
+  griddep_wait();  // earlier kernels on the stream are complete
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   const int chunks = H >> 3;
@@ -289,6 +299,8 @@ constexpr int kCombineSeg = 32 * kCombineLaneChunks;  // 16-byte chunks (512 col
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y_perm,
                                                       const int32_t* __restrict__ slot_to_row, int T, int H, int k,
                                                       long long R, uint16_t* __restrict__ y, int* err) {
+  griddep_wait();  // earlier kernels on the stream are complete
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   const int chunks = H >> 3;
@@ -367,6 +379,8 @@ __global__ void __launch_bounds__(256) router_grad_kernel(const float* __restric
                                                           const int32_t* __restrict__ slot_to_row, int T, int E,
                                                           int k, long long R, float* __restrict__ d_logits,
                                                           int* err) {
+  griddep_wait();  // earlier kernels on the stream are complete
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   for (long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
@@ -411,17 +425,17 @@ int launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, fl
   const int epl = (E + 31) / 32;
   KernelScope trace("route_topk", s);
   if (epl <= 1)
-    route_topk_kernel<1><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+    launch_kernel(route_topk_kernel<1>, dim3(blocks), dim3(256), 0, s, "route_topk", 1, logits, T, E, k, ids, w);
   else if (epl <= 2)
-    route_topk_kernel<2><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+    launch_kernel(route_topk_kernel<2>, dim3(blocks), dim3(256), 0, s, "route_topk", 1, logits, T, E, k, ids, w);
   else if (epl <= 4)
-    route_topk_kernel<4><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+    launch_kernel(route_topk_kernel<4>, dim3(blocks), dim3(256), 0, s, "route_topk", 1, logits, T, E, k, ids, w);
   else if (epl <= 8)
-    route_topk_kernel<8><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+    launch_kernel(route_topk_kernel<8>, dim3(blocks), dim3(256), 0, s, "route_topk", 1, logits, T, E, k, ids, w);
   else if (epl <= 16)
-    route_topk_kernel<16><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+    launch_kernel(route_topk_kernel<16>, dim3(blocks), dim3(256), 0, s, "route_topk", 1, logits, T, E, k, ids, w);
   else
-    route_topk_kernel<32><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+    launch_kernel(route_topk_kernel<32>, dim3(blocks), dim3(256), 0, s, "route_topk", 1, logits, T, E, k, ids, w);
   return check_launch("route_topk");
 }
 
@@ -440,13 +454,14 @@ int launch_dispatch(const int32_t* ids, const float* w, const uint16_t* x, int T
   if (nunits > 0) {
     {
       KernelScope trace("dispatch_hist", s);
-      dispatch_hist_kernel<<<blocks, kWarpsPerBlock * 32, kWarpsPerBlock * E * sizeof(int), s>>>(
-          ids, R, E, nunits, hist, dev.err_flag);
+      launch_kernel(dispatch_hist_kernel, dim3(blocks), dim3(kWarpsPerBlock * 32), kWarpsPerBlock * E * sizeof(int), s,
+                    "dispatch_hist", 1, ids, R, E, nunits, hist, dev.err_flag);
     }
     if (int rc = check_launch("dispatch_hist")) return rc;
     {
       KernelScope trace("dispatch_scan", s);
-      dispatch_scan_kernel<<<(E * 32 + 255) / 256, 256, 0, s>>>(hist, nunits, E, counts);
+      launch_kernel(dispatch_scan_kernel, dim3((E * 32 + 255) / 256), dim3(256), 0, s, "dispatch_scan", 1, hist,
+                    nunits, E, counts);
     }
     if (int rc = check_launch("dispatch_scan")) return rc;
   } else {
@@ -455,8 +470,9 @@ int launch_dispatch(const int32_t* ids, const float* w, const uint16_t* x, int T
   const size_t smem = (E + 1 + 32 + kWarpsPerBlock * E) * sizeof(int);
   {
     KernelScope trace("dispatch_scatter", s);
-    dispatch_scatter_kernel<<<blocks > 0 ? blocks : 1, kWarpsPerBlock * 32, smem, s>>>(
-        ids, w, R, E, nunits, hist, counts, m_indptr, row_to_slot, slot_to_row, w_perm);
+    launch_kernel(dispatch_scatter_kernel, dim3(blocks > 0 ? blocks : 1), dim3(kWarpsPerBlock * 32), smem, s,
+                  "dispatch_scatter", 1, ids, w, R, E, nunits, hist, counts, m_indptr, row_to_slot, slot_to_row,
+                  w_perm);
   }
   if (int rc = check_launch("dispatch_scatter")) return rc;
   if (x_perm != nullptr && R > 0) return launch_gather_rows(x, row_to_slot, nullptr, R, H, k, x_perm, dev, s);
@@ -468,8 +484,8 @@ int launch_gather_rows(const uint16_t* src, const int32_t* row_to_slot, const fl
   if (R == 0) return LIGER_MOE_OK;
   {
     KernelScope trace(scale == nullptr ? "gather_rows" : "gather_rows_scaled", s);
-    gather_rows_kernel<<<grid_for_warps(R, 8, dev), 256, 0, s>>>(src, row_to_slot, scale, R, H, k, dst,
-                                                                 dev.err_flag);
+    launch_kernel(gather_rows_kernel, dim3(grid_for_warps(R, 8, dev)), dim3(256), 0, s, "gather_rows", 1, src,
+                  row_to_slot, scale, R, H, k, dst, dev.err_flag);
   }
   return check_launch("gather_rows");
 }
@@ -480,8 +496,8 @@ int launch_combine(const uint16_t* y_perm, const int32_t* slot_to_row, int T, in
   {
     KernelScope trace("combine", s);
     const long long items = static_cast<long long>(T) * ((H / 8 + kCombineSeg - 1) / kCombineSeg);
-    combine_kernel<<<grid_for_warps(items, 8, dev), 256, 0, s>>>(y_perm, slot_to_row, T, H, k,
-                                                                 static_cast<long long>(T) * k, y, dev.err_flag);
+    launch_kernel(combine_kernel, dim3(grid_for_warps(items, 8, dev)), dim3(256), 0, s, "combine", 1, y_perm,
+                  slot_to_row, T, H, k, static_cast<long long>(T) * k, y, dev.err_flag);
   }
   return check_launch("combine");
 }
@@ -492,9 +508,8 @@ int launch_router_grad(const float* gdot, int gdot_tiles_, const int32_t* ids, c
   if (T == 0) return LIGER_MOE_OK;
   {
     KernelScope trace("router_grad", s);
-    router_grad_kernel<<<grid_for_warps(T, 8, dev), 256, 0, s>>>(gdot, gdot_tiles_, ids, w, slot_to_row, T, E, k,
-                                                                 static_cast<long long>(T) * k, d_logits,
-                                                                 dev.err_flag);
+    launch_kernel(router_grad_kernel, dim3(grid_for_warps(T, 8, dev)), dim3(256), 0, s, "router_grad", 1, gdot,
+                  gdot_tiles_, ids, w, slot_to_row, T, E, k, static_cast<long long>(T) * k, d_logits, dev.err_flag);
   }
   return check_launch("router_grad");
 }

@@ -17,6 +17,8 @@ namespace lmoe {
 namespace {
 
 __global__ void bounded_wait_selftest_kernel(uint64_t limit_ns, int* err) {
+  griddep_wait();  // earlier kernels on the stream are complete
+  griddep_launch_dependents();
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bar), 1);  // one arrival completes phase 0; none is ever made
@@ -34,7 +36,8 @@ __global__ void bounded_wait_selftest_kernel(uint64_t limit_ns, int* err) {
 int launch_bounded_wait_selftest(uint64_t limit_ns, const DeviceInfo& dev, cudaStream_t s) {
   {
     KernelScope trace("bounded_wait_selftest", s);
-    bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns, dev.err_flag);
+    launch_kernel(bounded_wait_selftest_kernel, dim3(1), dim3(32), 0, s, "bounded_wait_selftest", 1, limit_ns,
+                  dev.err_flag);
   }
   return check_launch("bounded_wait_selftest");
 }
