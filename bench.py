@@ -13,6 +13,8 @@ with the workload's shapes (no dataset).  The printed JSON line carries:
                 step's inputs and device->host copies of its outputs inside the timed loop
 * cpu_baseline  the CPU oracle on a bounded sample of the same workload
 * clocks        SM clock / throttle reasons sampled with nvidia-smi during the timed loop
+* inference_forward  the forward alone without saved derivative factors (nothing kept for a
+                backward): ms, TFLOP/s, and each expert GEMM's TFLOP/s against the bf16 peaks
 
 ``--impl reference`` times the CPU oracle itself on the host cores (the only
 reference implementation of this method that exists here).
@@ -356,20 +358,21 @@ def run_ours(args, rank, world, local_rank):
     # its dy_perm), which the GEMMs read as dense TMA tiles.  --inputs gather: the layer on
     # token-major x and dY, the expert GEMMs copying their rows by token, so no expert-major copy
     # exists (less memory, slower).
-    def forward(lg, xx, y_out=None):
+    # save=False: an inference forward, which keeps no derivative factors for a backward
+    def forward(lg, xx, y_out=None, save=True):
         if args.router:
             moe.router_logits(xx, wr, rbias, out=lg)
         moe.route_topk(lg, k, topk_ids=ids, topk_w=w)
         moe.dispatch(ids, w, None if gather else xx, E, out=dbuf, workspace=ws_d)
         if gather:
             moe.grouped_swiglu_fwd_gather(xx, dbuf["row_to_slot"], k, dbuf["m_indptr"], wgu, wd, dbuf["w_perm"],
-                                          out=fbuf, workspace=ws_f)
+                                          save_gu=save, out=fbuf, workspace=ws_f)
         elif args.act != "swiglu":
             moe.grouped_glu_fwd(dbuf["x_perm"], dbuf["m_indptr"], wgu, wd, dbuf["w_perm"], args.act, args.act_clamp,
-                                out=fbuf, workspace=ws_f)
+                                save_gu=save, out=fbuf, workspace=ws_f)
         else:
-            moe.grouped_swiglu_fwd(dbuf["x_perm"], dbuf["m_indptr"], wgu, wd, dbuf["w_perm"], out=fbuf,
-                                   workspace=ws_f)
+            moe.grouped_swiglu_fwd(dbuf["x_perm"], dbuf["m_indptr"], wgu, wd, dbuf["w_perm"], save_gu=save,
+                                   out=fbuf, workspace=ws_f)
         moe.combine(fbuf["y_perm"], dbuf["slot_to_row"], T, k, out=Y if y_out is None else y_out)
 
     def backward(dyy, xx, dx_out=None, dl_out=None):
@@ -496,6 +499,42 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     fwd_ms = ev2.elapsed_time(ev3) / nf
 
+    # inference forward (no derivative factors saved), timed the same way; a traced replay of
+    # the same launches gives each expert GEMM's rate
+    gi, ti = None, None
+    if graph is not None:
+        gi = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gi):
+            for _ in range(nf):
+                forward(logits, x, save=False)
+        moe.trace_enable(True)  # stays on until the records are read (turning it off clears them)
+        ti = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ti):
+            for _ in range(nf):
+                forward(logits, x, save=False)
+        gi.replay()
+        ti.replay()
+    torch.cuda.synchronize()
+    ev8, ev9 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev8.record(stream)
+    if gi is not None:
+        gi.replay()
+    else:
+        for _ in range(nf):
+            forward(logits, x, save=False)
+    ev9.record(stream)
+    torch.cuda.synchronize()
+    inf_ms = ev8.elapsed_time(ev9) / nf
+    if ti is not None:
+        ti.replay()
+    else:
+        moe.trace_enable(True)
+        for _ in range(nf):
+            forward(logits, x, save=False)
+    torch.cuda.synchronize()
+    inf_records = moe.trace_records()
+    moe.trace_enable(False)
+
     # ---------------- per-kernel statistics from the trace of the timed region
     peaks = load_peaks()
     stats = {}
@@ -544,6 +583,25 @@ def run_ours(args, rank, world, local_rank):
     traffic = load_traffic(wl.name, dom)
     if traffic is not None:
         roofline["traffic"] = traffic
+
+    inf_stats = {}
+    for name, ms in inf_records:
+        s_ = inf_stats.setdefault(name, [0, 0.0])
+        s_[0] += 1
+        s_[1] += ms
+    inf_gemms = {}
+    for name, (n, tot) in sorted(inf_stats.items(), key=lambda kv: -kv[1][1]):
+        kind, amount = kernel_work(wl, name, gated)
+        if kind != "flop" or tot <= 0:
+            continue
+        tf = amount / (tot / n * 1e-3) / 1e12
+        inf_gemms[name] = {"avg_us": round(1e3 * tot / n, 2), "tflops": round(tf, 1),
+                           "frac_of_bf16_burst": round(tf / peaks["bf16_tflops"], 4),
+                           "frac_of_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 4)}
+    inference = {"ms_per_step": round(inf_ms, 4), "tflops": round(world * fl["fwd"] / (inf_ms * 1e-3) / 1e12, 2),
+                 "tokens_per_s": round(world * T / (inf_ms * 1e-3), 1),
+                 "saved_state": "none: the forward keeps no derivative factors for a backward",
+                 "gemms": inf_gemms}
 
     # ---------------- end to end: host buffers, copies inside the timed loop
     # Every step uploads its inputs (logits, x, dY) from pinned host memory and downloads its
@@ -664,6 +722,7 @@ def run_ours(args, rank, world, local_rank):
             "fwd_tflops": round(fl["fwd"] / (fwd_ms * 1e-3) / 1e12, 2),
             "bwd_tflops": round(fl["bwd"] / ((ms_per_step - fwd_ms) * 1e-3) / 1e12, 2),
             "pct_of_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
+            "inference_forward": inference,
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clock_info, "launch": graph_note,
             "traced_ms_per_step": None if trace_ms is None else round(trace_ms, 4),
