@@ -353,6 +353,40 @@ LIGER_MOE_API int liger_moe_combine(const void* y_perm, const int32_t* slot_to_r
 
 namespace {
 
+// A second stream of the calling thread on one device, with a fork and a join event, for work
+// that may run beside the caller's stream.  Created on first use, never while the caller's
+// stream is being captured (it is then retried on a later call); nullptr when unavailable, in
+// which case the caller runs everything in order on its own stream.  Per thread, so that two
+// threads capturing graphs never share it.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr;
+  cudaEvent_t join = nullptr;
+  bool failed = false;
+};
+
+SideStream* side_stream(int device, cudaStream_t caller) {
+  thread_local SideStream per_device[kMaxDevices];
+  if (device < 0 || device >= kMaxDevices) return nullptr;
+  SideStream& ss = per_device[device];
+  if (ss.stream != nullptr) return &ss;
+  if (ss.failed) return nullptr;
+  cudaStreamCaptureStatus status = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(caller, &status) != cudaSuccess || status != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();  // a refused query is not a launch error of this call
+    return nullptr;
+  }
+  if (cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    ss.failed = true;
+    ss.stream = nullptr;
+    return nullptr;
+  }
+  return &ss;
+}
+
 // Backward of the layer.  With x_perm: dY is copied to expert-major order (dy_perm, in the
 // workspace) and both are read as dense tiles.  With x (x_perm NULL): x and dY rows are
 // gathered by token inside the GEMMs and no expert-major copy is made.
@@ -462,6 +496,29 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
     }
     if (int rc = launch_bwd_dh(a, dev, s)) return rc;
     if (int rc = launch_bwd_dx(a, dev, s)) return rc;
+    // The weight-gradient GEMMs, the per-token sum of dX_perm and d_logits all depend only on
+    // what is done by now.  The two small kernels go to a side stream, where their CTAs share
+    // the SMs (and the spare bandwidth) with the GEMMs' one CTA per SM; the GEMMs are enqueued
+    // first so that they take their SMs first.  Measured on GB300: 1.864 -> 1.844 ms per layer
+    // step at T=8192, H=2048, I=512, E=256, k=8 (in order, or with the side work first: 1.869).
+    if (SideStream* side = side_stream(dev.device, s)) {
+      if (cudaEventRecord(side->fork, s) != cudaSuccess) {
+        set_cuda_error(cudaGetLastError(), "cudaEventRecord");
+        return LIGER_MOE_ERR_LAUNCH;
+      }
+      int rc = launch_bwd_dw(a, dev, s);
+      cudaStreamWaitEvent(side->stream, side->fork, 0);
+      if (rc == LIGER_MOE_OK)
+        rc = launch_combine(dx_perm, slot_to_row, T, H, k, static_cast<uint16_t*>(dx), dev, side->stream);
+      if (rc == LIGER_MOE_OK)
+        rc = launch_router_grad(gdot, gdot_tiles(I), topk_ids, topk_w, slot_to_row, T, E, k, d_logits, dev,
+                                side->stream);
+      // joined on every path, so that a capture of the caller's stream stays well formed
+      cudaEventRecord(side->join, side->stream);
+      cudaStreamWaitEvent(s, side->join, 0);
+      if (rc == LIGER_MOE_OK) rc = check_launch("side stream join");
+      return rc;
+    }
     if (int rc = launch_combine(dx_perm, slot_to_row, T, H, k, static_cast<uint16_t*>(dx), dev, s)) return rc;
   }
   if (int rc = launch_bwd_dw(a, dev, s)) return rc;
