@@ -25,7 +25,11 @@
  *     bf16 tensors are passed as void* (IEEE bfloat16 bit patterns).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
  *     Every call only enqueues work on `stream`: it never synchronises, never
- *     allocates device memory and never frees anything.
+ *     allocates device memory and never frees anything.  The backward entry
+ *     points run two of their small kernels on a library-owned stream of the
+ *     calling thread, forked from `stream` and joined back into it with
+ *     events: to the caller (and to a graph capture of `stream`) all of the
+ *     call's work is ordered on `stream`.
  *   - The caller owns every buffer.  Outputs are overwritten, never
  *     accumulated into (one stated exception: liger_moe_router_bwd adds to dx).
  *     Buffers of one call must not overlap unless stated.
