@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
           o.z = pack_bf16x2(f * bf16_lo(o.z), f * bf16_hi(o.z));
           o.w = pack_bf16x2(f * bf16_lo(o.w), f * bf16_hi(o.w));
         }
-        b[c0 + 32 * j] = o;
+        __stcs(b + c0 + 32 * j, o);  // evict-first: the GEMMs read the copy only after the whole gather
       }
     }
   }
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
           const uint4* src = reinterpret_cast<const uint4*>(y_perm + static_cast<size_t>(r) * H);
 #pragma unroll
           for (int q = 0; q < kCombineLaneChunks; ++q)
-            if (c0 + 32 * q < chunks) v[jj][q] = __ldg(src + c0 + 32 * q);
+            if (c0 + 32 * q < chunks) v[jj][q] = __ldcs(src + c0 + 32 * q);  // each row is read once
         }
       }
 #pragma unroll
