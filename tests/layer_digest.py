@@ -1,5 +1,6 @@
 """Runs one routed MoE layer step (forward and backward) on cuda:0 and prints the SHA-256 of
-every output, as launched one call at a time and as replayed from a captured CUDA graph.
+every output, as launched one call at a time and as replayed from a captured CUDA graph (or, with
+"capture_first", only the latter, captured before any other call).
 
 Used by tests/test_gpu_pdl.py as a child process: the library reads its launch mode
 (programmatic dependent launch with LIGER_MOE_PDL=1, else plain stream order) once per
@@ -39,6 +40,9 @@ def _digest(t: torch.Tensor) -> str:
 
 def main() -> None:
     wl = synthetic.workload(sys.argv[1])
+    # "capture_first": the process's first library calls are made inside the graph capture (the
+    # backward then finds no side stream and runs in order on the captured stream)
+    capture_first = len(sys.argv) > 2 and sys.argv[2] == "capture_first"
     inp = synthetic.make_inputs(wl)
     logits, x, dy = _dev(inp["logits"]), _dev(inp["x"]), _dev(inp["dy"])
     wgu, wd = _dev(inp["wgu"]), _dev(inp["wd"])
@@ -53,11 +57,13 @@ def main() -> None:
         return dict(ids=ids, w=w, m_indptr=d["m_indptr"], row_to_slot=d["row_to_slot"], x_perm=d["x_perm"], h=h,
                     gu=gu, Y=Y, dx=dx, dw_gate_up=dwgu, dw_down=dwd, d_logits=dl)
 
-    eager = step()
-    torch.cuda.synchronize()
-    out = {"eager": {k: _digest(v) for k, v in eager.items()}}
-    step()  # warm the allocator before capture
-    torch.cuda.synchronize()
+    out = {}
+    if not capture_first:
+        eager = step()
+        torch.cuda.synchronize()
+        out["eager"] = {k: _digest(v) for k, v in eager.items()}
+        step()  # warm the allocator before capture
+        torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         captured = step()

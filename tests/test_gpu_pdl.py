@@ -22,12 +22,12 @@ WORKLOADS = [
 ]
 
 
-def _digests(workload: str, pdl: bool) -> dict:
+def _digests(workload: str, pdl: bool, *extra: str) -> dict:
     env = dict(os.environ)
     env.pop("LIGER_MOE_PDL", None)
     if pdl:
         env["LIGER_MOE_PDL"] = "1"
-    r = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "layer_digest.py"), workload], env=env,
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "layer_digest.py"), workload, *extra], env=env,
                        capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
     return json.loads(r.stdout.strip().splitlines()[-1])
@@ -40,3 +40,11 @@ def test_outputs_do_not_depend_on_launch_mode(workload):
         assert run["device_error"] == 0
         assert run["graph"] == run["eager"], "graph replay differs from call-by-call launches"
     assert on["eager"] == off["eager"], "programmatic dependent launch changed an output"
+
+
+def test_first_call_inside_a_capture_matches():
+    """No side stream exists yet when the first backward is captured: it runs in order, same bytes."""
+    workload = WORKLOADS[0]
+    first = _digests(workload, False, "capture_first")
+    assert first["device_error"] == 0
+    assert first["graph"] == _digests(workload, False)["eager"]
