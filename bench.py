@@ -304,6 +304,31 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- ranks
+# N GPUs run N independent replicas of the layer step (the path has no exchange step on one
+# GPU's data).  The ranks meet only around the timed region: a barrier on both sides, the
+# slowest rank's time, and the whole-job rate from it.
+def rank_barrier(dist) -> None:
+    if dist is not None:
+        dist.barrier()
+
+
+def rank_max(v: float, dist, device) -> float:
+    """The largest `v` over all ranks (`device`: where the reduction tensor lives for the backend)."""
+    if dist is None:
+        return v
+    import torch
+
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, units_per_rank: float, slowest_ms: float) -> float:
+    """Units per second of the whole job: every rank processed `units_per_rank` within `slowest_ms`."""
+    return world * units_per_rank / (slowest_ms * 1e-3)
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local_rank):
     import numpy as np
@@ -396,15 +421,10 @@ def run_ours(args, rank, world, local_rank):
         backward(dy, x)
 
     def barrier():
-        if dist is not None:
-            dist.barrier()
+        rank_barrier(dist)
 
     def max_over_ranks(v: float) -> float:
-        if dist is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return rank_max(v, dist, dev)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -475,8 +495,8 @@ def run_ours(args, rank, world, local_rank):
 
     fl = step_flops(wl, gated, args.router)
     ms_per_step = elapsed_ms / args.steps
-    value = world * args.steps * fl["total"] / (elapsed_ms * 1e-3) / 1e12
-    tokens_per_s = world * args.steps * T / (elapsed_ms * 1e-3)
+    value = whole_job_rate(world, args.steps * fl["total"], elapsed_ms) / 1e12
+    tokens_per_s = whole_job_rate(world, args.steps * T, elapsed_ms)
 
     # forward-only timing (same buffers, launched the same way), for the fwd / bwd split
     ev2, ev3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -497,7 +517,7 @@ def run_ours(args, rank, world, local_rank):
             forward(logits, x)
     ev3.record(stream)
     torch.cuda.synchronize()
-    fwd_ms = ev2.elapsed_time(ev3) / nf
+    fwd_ms = max_over_ranks(ev2.elapsed_time(ev3)) / nf
 
     # inference forward (no derivative factors saved), timed the same way; a traced replay of
     # the same launches gives each expert GEMM's rate
@@ -524,7 +544,7 @@ def run_ours(args, rank, world, local_rank):
             forward(logits, x, save=False)
     ev9.record(stream)
     torch.cuda.synchronize()
-    inf_ms = ev8.elapsed_time(ev9) / nf
+    inf_ms = max_over_ranks(ev8.elapsed_time(ev9)) / nf
     if ti is not None:
         ti.replay()
     else:
@@ -598,8 +618,8 @@ def run_ours(args, rank, world, local_rank):
         inf_gemms[name] = {"avg_us": round(1e3 * tot / n, 2), "tflops": round(tf, 1),
                            "frac_of_bf16_burst": round(tf / peaks["bf16_tflops"], 4),
                            "frac_of_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 4)}
-    inference = {"ms_per_step": round(inf_ms, 4), "tflops": round(world * fl["fwd"] / (inf_ms * 1e-3) / 1e12, 2),
-                 "tokens_per_s": round(world * T / (inf_ms * 1e-3), 1),
+    inference = {"ms_per_step": round(inf_ms, 4), "tflops": round(whole_job_rate(world, fl["fwd"], inf_ms) / 1e12, 2),
+                 "tokens_per_s": round(whole_job_rate(world, T, inf_ms), 1),
                  "saved_state": "none: the forward keeps no derivative factors for a backward",
                  "gemms": inf_gemms}
 
@@ -683,7 +703,7 @@ def run_ours(args, rank, world, local_rank):
         e2e_ms = max_over_ranks(ev4.elapsed_time(ev5))
         h2d = (0 if args.router else T * E * 4) + 2 * T * H * 2
         d2h = 2 * T * H * 2 + T * E * 4
-        e2e = {"value": round(world * ne * fl["total"] / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        e2e = {"value": round(whole_job_rate(world, ne * fl["total"], e2e_ms) / 1e12, 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / ne, 4),
                "weights": "resident on the device; dW stays on the device",
                "copies": "double-buffered on a copy stream, overlapped with the neighbouring steps' compute",
@@ -719,8 +739,8 @@ def run_ours(args, rank, world, local_rank):
                                                  f"of weights + activations streamed per step (L2 129 MB)"}),
             "tokens_per_s": round(tokens_per_s, 1),
             "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(ms_per_step - fwd_ms, 4),
-            "fwd_tflops": round(fl["fwd"] / (fwd_ms * 1e-3) / 1e12, 2),
-            "bwd_tflops": round(fl["bwd"] / ((ms_per_step - fwd_ms) * 1e-3) / 1e12, 2),
+            "fwd_tflops": round(whole_job_rate(world, fl["fwd"], fwd_ms) / 1e12, 2),
+            "bwd_tflops": round(whole_job_rate(world, fl["bwd"], ms_per_step - fwd_ms) / 1e12, 2),
             "pct_of_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
             "inference_forward": inference,
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,

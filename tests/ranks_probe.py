@@ -1,0 +1,35 @@
+"""One rank of a CPU run of bench.py's multi-rank host logic, launched by torch.distributed.run.
+
+Joins a gloo process group from the launcher's environment, reports a per-rank time of
+10 * (rank + 1) ms, and prints (as one JSON line per rank) what bench.py's helpers make of it:
+the slowest rank's time and the whole-job rate for 1000 units per rank.
+"""
+from __future__ import annotations
+
+import json
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import torch.distributed as dist  # noqa: E402
+
+import bench  # noqa: E402
+
+
+def main() -> None:
+    dist.init_process_group("gloo")
+    try:
+        rank, world = dist.get_rank(), dist.get_world_size()
+        bench.rank_barrier(dist)
+        slowest = bench.rank_max(10.0 * (rank + 1), dist, "cpu")
+        rate = bench.whole_job_rate(world, 1000.0, slowest)
+        bench.rank_barrier(dist)
+        print(json.dumps({"rank": rank, "world": world, "slowest_ms": slowest, "rate": rate}), flush=True)
+    finally:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
