@@ -48,7 +48,7 @@ def rel_errors_per_expert(got, ref) -> tuple[float, float]:
 
     Expert gradients differ in scale by the square root of their row counts
     (strongly so under skewed routing), so one tensor-wide rms floor would
-    judge a heavy expert's near-zero entries against a light expert's scale.
+    measure a heavy expert's near-zero entries against a light expert's scale.
     mean_rel stays tensor-wide.
     """
     g = np.asarray(got, dtype=np.float64)
