@@ -108,6 +108,8 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 // ============================================================================
 constexpr int kUnit = 256;
 constexpr int kWarpsPerBlock = 8;
+constexpr int kGroups = kUnit / 32;  // 32-slot groups of a unit (one per lane round)
+constexpr int kNoSlot = -1;          // register placeholder past the last slot
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) dispatch_hist_kernel(const int32_t* __restrict__ ids,
                                                                            long long R, int E, int nunits,
@@ -122,16 +124,22 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) dispatch_hist_kernel(cons
   __syncwarp();
   if (unit >= nunits) return;
   const long long s0 = static_cast<long long>(unit) * kUnit;
+  // all of the unit's ids are loaded first, so their latencies overlap
+  int ev[kGroups];
+#pragma unroll
+  for (int g = 0; g < kGroups; ++g) {
+    const long long s = s0 + g * 32 + lane;
+    ev[g] = (s < R) ? __ldg(ids + s) : kNoSlot;
+  }
   int bad = 0;
-  for (int i = lane; i < kUnit; i += 32) {
-    const long long s = s0 + i;
-    if (s < R) {
-      const int e = __ldg(ids + s);
-      if (static_cast<unsigned>(e) < static_cast<unsigned>(E))
-        atomicAdd(&h[e], 1);
-      else
-        bad = 1;
-    }
+#pragma unroll
+  for (int g = 0; g < kGroups; ++g) {
+    if (s0 + g * 32 + lane >= R) continue;  // past the last slot
+    const int e = ev[g];
+    if (static_cast<unsigned>(e) < static_cast<unsigned>(E))
+      atomicAdd(&h[e], 1);
+    else
+      bad = 1;
   }
   if (__any_sync(kFull, bad) && lane == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_EXPERT_ID);
   __syncwarp();
@@ -217,10 +225,21 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) dispatch_scatter_kernel(
   for (int e = lane; e < E; e += 32) cnt[e] = s_off[e] + __ldg(base + static_cast<size_t>(e) * nunits + unit);
   __syncwarp();
   const long long s0 = static_cast<long long>(unit) * kUnit;
-  for (int g = 0; g < kUnit; g += 32) {
-    const long long s = s0 + g + lane;
-    int e = (s < R) ? __ldg(ids + s) : -1;
-    const bool ok = static_cast<unsigned>(e) < static_cast<unsigned>(E);
+  // the unit's ids and weights are loaded first, so their latencies overlap; the rounds below
+  // then only wait on shared memory
+  int ev[kGroups];
+  float wv[kGroups];
+#pragma unroll
+  for (int g = 0; g < kGroups; ++g) {
+    const long long s = s0 + g * 32 + lane;
+    ev[g] = (s < R) ? __ldg(ids + s) : kNoSlot;
+    wv[g] = (w_perm != nullptr && s < R) ? __ldg(w + s) : 0.f;
+  }
+#pragma unroll
+  for (int g = 0; g < kGroups; ++g) {
+    const long long s = s0 + g * 32 + lane;
+    int e = ev[g];
+    const bool ok = s < R && static_cast<unsigned>(e) < static_cast<unsigned>(E);
     if (!ok) e = E + lane;  // unique per lane: never matches a real expert
     const unsigned peers = __match_any_sync(kFull, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
@@ -234,7 +253,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) dispatch_scatter_kernel(
       const int r = pos + rank;
       slot_to_row[s] = r;
       row_to_slot[r] = static_cast<int32_t>(s);
-      if (w_perm) w_perm[r] = __ldg(w + s);
+      if (w_perm) w_perm[r] = wv[g];
     }
   }
 }
