@@ -376,14 +376,21 @@ SideStream* side_stream(int device, cudaStream_t caller) {
     cudaGetLastError();  // a refused query is not a launch error of this call
     return nullptr;
   }
-  if (cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  if (cudaStreamCreateWithFlags(&stream, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+    if (join != nullptr) cudaEventDestroy(join);
+    if (fork != nullptr) cudaEventDestroy(fork);
+    if (stream != nullptr) cudaStreamDestroy(stream);
     cudaGetLastError();
     ss.failed = true;
-    ss.stream = nullptr;
     return nullptr;
   }
+  ss.stream = stream;
+  ss.fork = fork;
+  ss.join = join;
   return &ss;
 }
 
