@@ -5,28 +5,32 @@
 // b laid out [num_experts, N, K]; LigerCute README, "LigerMoE design":
 // persistent warp-specialised TMA / MMA pipeline):
 //   warp 0      TMA producer: one elected lane streams A and B tiles into a
-//               shared-memory ring of 2-4 stages (128-byte swizzle), mbarrier-tracked.
+//               shared-memory ring of 2-6 stages (128-byte swizzle), mbarrier-tracked.
 //               In the memory-lean variant an operand whose rows are token rows picked
 //               by the routing (x or dY in expert-major order) is instead gathered by
 //               the whole warp with TMA gather4 (four rows per copy) straight from the
 //               token-major tensor, so no permuted copy of it is ever written.
 //   warp 1      MMA issuer: allocates 512 TMEM columns, one elected lane issues
-//               tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32) and commits
-//               stage releases and accumulator-ready events to mbarriers
-//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (each warp owns one
-//               32-lane TMEM quadrant = 32 rows), fused math, bf16 stores
+//               tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32; M=256 across a
+//               2-SM CTA pair) and commits stage releases and accumulator-ready events
+//               to mbarriers
+//   warps 2..9  epilogue: tcgen05.ld of the fp32 accumulator, fused math, TMA bulk
+//               stores.  Two warps per 32-lane TMEM quadrant (the quadrant's 32 rows),
+//               each owning half of the tile's columns.
 // The two 128x256 fp32 accumulators in TMEM are double-buffered, so the
 // epilogue of tile i overlaps the MMAs of tile i+1.
 //
-// Two schedules:
+// Schedules:
 //   RowsM  rows of an expert are the GEMM's M (forward gate/up and down,
 //          backward dH and dX): tiles (expert, 128-row block, N block), K fixed.
 //          The per-expert M-tile prefix is built on the device from m_indptr.
 //   RowsK  rows of an expert are the GEMM's K (weight gradients): tiles
 //          (expert, M block, N block), K = rows of that expert, walked in row
-//          order by one CTA (deterministic, no split-K atomics).  The last
-//          K block's rows that belong to the next expert are zeroed in shared
-//          memory before the MMA reads them.
+//          order by one CTA (deterministic, no split-K atomics).  The operand the
+//          dH epilogue writes (dgu, w h) sits in a padded row space: each expert's
+//          rows are followed by zero rows up to a multiple of 16, so the last
+//          16-row K step adds nothing from the next expert's rows of the other operand.
+//   Dense  one plain GEMM over R rows (the router projection).
 // Epilogues: SwiGLU (h = silu(g)*u, optional fp32 derivative factors), ScaleRows
 // (y = w_r * acc), DH (SwiGLU backward from the saved factors, hi/lo operands for
 // the weight gradients, per-row partial <dh, h> for the router gradient), Store.
@@ -183,8 +187,8 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p) {
     tl.prow0 = 0;
     tl.kb_count = p.num_kb;
   } else {
-    // M blocks fastest: consecutive tiles (the CTAs of a cluster) share the expert and the N
-    // block, so they read the same B tile
+    // M blocks fastest: neighbouring tiles share the expert and the N block, so they read the
+    // same B tile (through L2)
     const int per_e = p.m_tiles * p.n_tiles;
     tl.e = t / per_e;
     const int r = t - tl.e * per_e;
@@ -694,24 +698,13 @@ __device__ __forceinline__ void prefetch_epilogue_operands(const Tile& tl, int r
 enum class Gather : int { None = 0, A = 1, B = 2 };
 
 // Tiled loads of one stage for the operands that are not gathered (lane 0 of the producer).
-// In a cluster of CL > 1 CTAs one operand is shared: RowsM tiles of a cluster have the same
-// M block (A shared; each CTA loads BM / CL of its rows, tensor map box BM / CL rows high),
-// RowsK tiles the same expert and N block (B shared; each CTA loads every CL-th 64-column
-// box); the shared part is multicast to every CTA of the cluster, at the same offsets.
-template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT, bool kLoadA, bool kLoadB, int CL = 1>
+// Every box lands in this CTA's own shared memory and completes on its own full barrier.
+template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT, bool kLoadA, bool kLoadB>
 __device__ __forceinline__ void load_stage_tiled(const CUtensorMap* tmA, const CUtensorMap* tmB, const Params& p,
-                                                 const Tile& tl, int kb, uint32_t sa, uint32_t sb, uint32_t fb,
-                                                 uint32_t rank = 0) {
-  constexpr uint16_t kMask = static_cast<uint16_t>((1u << CL) - 1u);
+                                                 const Tile& tl, int kb, uint32_t sa, uint32_t sb, uint32_t fb) {
   if constexpr (kLoadA) {
     if constexpr (!A_MN) {  // RowsM: the tile's rows, in the padded row space when A is a padded operand
-      const int arow = p.pad_a ? tl.am0 : tl.m0;
-      if constexpr (S == Sched::RowsM && CL > 1) {
-        constexpr int kRows = BM / CL;
-        tma_load_2d_mc(sa + rank * kRows * 128, tmA, fb, kb * BK, arow + static_cast<int>(rank) * kRows, kMask);
-      } else {
-        tma_load_2d(sa, tmA, fb, kb * BK, arow);
-      }
+      tma_load_2d(sa, tmA, fb, kb * BK, p.pad_a ? tl.am0 : tl.m0);
     } else {
       const int krow = (p.pad_a ? tl.prow0 : tl.row0) + kb * BK;
 #pragma unroll
@@ -737,15 +730,9 @@ __device__ __forceinline__ void load_stage_tiled(const CUtensorMap* tmA, const C
 #pragma unroll
       for (int part = 0; part < (SPLIT == 2 ? 2 : 1); ++part)
 #pragma unroll
-        for (int i = 0; i < BN / 64; ++i) {
-          const uint32_t dst = sb + part * B_BYTES + i * MN_BOX_BYTES;
-          if constexpr (S == Sched::RowsK && CL > 1) {
-            if (i % CL == static_cast<int>(rank))
-              tma_load_2d_mc(dst, tmB, fb, tl.nt * BN + 64 * i, krow + part * p.b_split_rows, kMask);
-          } else {
-            tma_load_2d(dst, tmB, fb, tl.nt * BN + 64 * i, krow + part * p.b_split_rows);
-          }
-        }
+        for (int i = 0; i < BN / 64; ++i)
+          tma_load_2d(sb + part * B_BYTES + i * MN_BOX_BYTES, tmB, fb, tl.nt * BN + 64 * i,
+                      krow + part * p.b_split_rows);
     }
   }
 }
@@ -821,13 +808,10 @@ __device__ __forceinline__ void gather_tokens(const Tile& tl, int kb, int lane, 
   }
 }
 
-// CL: CTAs per cluster (1, 2 or 4) sharing one operand by multicast (load_stage_tiled); the
-// tile count must be a multiple of CL, so that the CTAs of a cluster walk the same number of
-// tiles and K blocks in lockstep.  A stage is refilled only after every CTA of the cluster has
-// consumed it (each MMA warp's commit arrives on the empty barrier of all of them).
-// PAIR (with CL = 2): the two CTAs of a cluster work on one 256-row tile with 2-SM MMAs
-// (cta_group::2): both load their halves, the even CTA's MMA warp issues every MMA and commits to
-// both CTAs' barriers, and both CTAs' epilogues release the accumulator to the even CTA.
+// PAIR (launched as clusters of two CTAs): the two CTAs work on one 256-row tile with 2-SM MMAs
+// (cta_group::2): each loads its own halves of the operands into its own shared memory, the even
+// CTA's MMA warp issues every MMA and commits to both CTAs' barriers, and both CTAs' epilogues
+// release the accumulator to the even CTA.  Without PAIR every CTA works alone (CL = 1).
 template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT, Gather G, int CL, int PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -835,14 +819,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const Params p) {
   using L = LayoutOf<EP, SPLIT, PAIR>;
   constexpr bool kPair = PAIR != 0;
+  static_assert(CL == (kPair ? 2 : 1), "clusters exist only as the 2-SM pairs");
   static_assert(!kPair || (CL == 2 && G == Gather::None &&
                             ((S == Sched::RowsM && !A_MN && SPLIT == 0) || (S == Sched::RowsK && A_MN && B_MN))),
                 "2-SM pairs: RowsM tiles with K-major A and one operand part, or RowsK tiles, no gather");
   constexpr int STAGES = L::kStages;
   constexpr int STAGE_BYTES = L::kStageBytes;
   constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CL) - 1u);
-  static_assert(CL == 1 || G == Gather::None, "clusters share tiled operands only");
-  static_assert(CL == 1 || (S == Sched::RowsM ? !A_MN : B_MN), "shared operand: K-major A (RowsM), MN-major B (RowsK)");
   const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
   const bool leader = !kPair || rank == 0;  // the CTA that issues the MMAs
   // pairs walk the tiles together: tile t of cluster c is t = c, c + clusters, ...
@@ -878,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, kPair ? 1 : CL);  // one release per CTA of the cluster (pair: the even CTA's)
+      mbar_init(empty0 + 8 * s, 1);  // released by this CTA's MMA commit (pair: the even CTA's)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -905,7 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before_sync();
   if constexpr (CL > 1)
-    cluster_sync();  // every CTA's barriers exist before any multicast load or release reaches them
+    cluster_sync();  // both CTAs' barriers exist before a pair load or commit reaches them
   else
     __syncthreads();
   tc_fence_after_sync();
@@ -946,8 +929,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                   rank);
             } else {
               mbar_arrive_expect_tx(fb, STAGE_BYTES);
-              load_stage_tiled<S, EP, A_MN, B_MN, SPLIT, true, true, CL>(&tmA, &tmB, p, tl, kb, sa, sa + L::kABytes,
-                                                                        fb, rank);
+              load_stage_tiled<S, EP, A_MN, B_MN, SPLIT, true, true>(&tmA, &tmB, p, tl, kb, sa, sa + L::kABytes, fb);
             }
             if (++stage == STAGES) {
               stage = 0;
@@ -955,9 +937,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if constexpr (CL > 1) {
-          // every CTA of the cluster has released the last fill of each stage: no release from a
-          // peer is still on its way to this CTA's barriers when it exits
+        if constexpr (kPair) {
+          // the even CTA has released the last fill of each stage: no release from the peer is
+          // still on its way to this CTA's barriers when it exits
           for (int i = 0; i < STAGES && !failed; ++i) {
             if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
               raise_abort(p.err, abort_flag);
@@ -1108,8 +1090,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if constexpr (kPair)
             umma_commit_pair_mc(empty0 + 8 * stage, kClusterMask);  // both CTAs' stage is free
-          else if constexpr (CL > 1)
-            umma_commit_mc(empty0 + 8 * stage, kClusterMask);
           else
             umma_commit(empty0 + 8 * stage);
         }
@@ -1341,8 +1321,8 @@ int make_out_bf16_3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t ro
 
 // Launches one grouped GEMM.  `tiles` is the number of tiles the persistent grid walks (for
 // RowsM an upper bound: the device schedule decides); the grid is at most one CTA per SM.
-// With CL > 1 the grid is made of clusters of CL CTAs (tiles must be a multiple of CL), as
-// many as can be resident at once.  PAIR: `tiles` counts 256-row pair tiles, one per cluster.
+// PAIR (CL = 2): the grid is made of CTA pairs, as many as can be resident at once, and `tiles`
+// counts 256-row (RowsM) or 256-column (RowsK) pair tiles, one per pair.
 template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT = 0, Gather G = Gather::None, int CL = 1,
           int PAIR = 0>
 int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc0, const CUtensorMap& tc1,
@@ -1673,11 +1653,9 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.ld_out = a.H;
   p.out_expert_stride = static_cast<long long>(a.nin) * a.H;
   if (make_out_bf16_3d(&tc0, a.dw_gate_up, a.H, nin, a.E)) return LIGER_MOE_ERR_LAUNCH;
-  // CTA pairs over neighbouring M blocks when the M blocks pair up: 2-SM MMAs (each CTA holding half
-  // of the x tile) when experts hold at least 192 rows on average, else two CTAs that share the x
-  // tile by multicast.  With few rows per expert the tiles are mostly gradient writes, and a 2-SM
-  // pair ties the two CTAs' epilogues to each other (measured on GB300: slower at 4 and 160 rows
-  // per expert, faster at 256 and 512).
+  // CTA pairs over neighbouring M blocks (2-SM MMAs, each CTA holding half of the x tile) when the M
+  // blocks pair up and experts hold at least 192 rows on average.  With few rows per expert the tiles
+  // are mostly gradient writes, and a 2-SM pair ties the two CTAs' epilogues to each other.
   const long long tiles_gu = static_cast<long long>(a.E) * p.m_tiles * p.n_tiles;
   int rc;
   if (gather_x)
@@ -1686,9 +1664,6 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   else if (p.m_tiles % 2 == 0 && a.R >= 192LL * a.E)
     rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::None, 2, 1>(ta, tb, tc0, tc0, p, tiles_gu / 2,
                                                                                   dev, s, "gemm_bwd_dw_gate_up");
-  else if (p.m_tiles % 2 == 0)
-    rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::None, 2>(ta, tb, tc0, tc0, p, tiles_gu, dev, s,
-                                                                               "gemm_bwd_dw_gate_up");
   else
     rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1>(ta, tb, tc0, tc0, p, tiles_gu, dev, s,
                                                               "gemm_bwd_dw_gate_up");
@@ -1717,8 +1692,7 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.out_expert_stride = 1LL * a.H * a.I;
   if (make_out_bf16_3d(&tc0, a.dw_down, a.I, a.H, a.E)) return LIGER_MOE_ERR_LAUNCH;
   // CTA pairs over neighbouring M blocks when the M blocks pair up: 2-SM MMAs (each CTA holding half
-  // of the w h tile, 4 stages instead of 2) from 128 rows per expert on average, else two CTAs that
-  // share the w h tile by multicast (measured: slower as pairs at 4 rows per expert, faster at 160)
+  // of the w h tile, 4 stages instead of 2) from 128 rows per expert on average
   const long long tiles_d = static_cast<long long>(a.E) * p.m_tiles * p.n_tiles;
   if (gather_dy)
     return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::A>(ta, tb, tc0, tc0, p, tiles_d, dev, s,
@@ -1726,9 +1700,6 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   if (p.m_tiles % 2 == 0 && a.R >= 128LL * a.E)
     return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::None, 2, 1>(ta, tb, tc0, tc0, p, tiles_d / 2,
                                                                                     dev, s, "gemm_bwd_dw_down");
-  if (p.m_tiles % 2 == 0)
-    return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::None, 2>(ta, tb, tc0, tc0, p, tiles_d, dev, s,
-                                                                                 "gemm_bwd_dw_down");
   return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2>(ta, tb, tc0, tc0, p, tiles_d, dev, s, "gemm_bwd_dw_down");
 }
 

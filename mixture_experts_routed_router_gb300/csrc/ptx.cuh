@@ -99,18 +99,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
-// The same load delivered to every CTA of the cluster named in `mask` (bit i = CTA rank i):
-// the box lands at offset `dst` of each one's shared memory and completes on the mbarrier at
-// offset `bar` of each one.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, uint32_t bar, int x, int y,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(mask)
-      : "memory");
-}
-
 // Row gather: four rows (y0..y3) of one column window starting at x, from a 2D tensor map
 // whose box is one row high; they land as four consecutive box rows at `dst` (the map's
 // swizzle applies by shared-memory address, as for a 4-row box).  Completion on `bar`.
@@ -198,14 +186,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
 }
-// The same arrival on the mbarrier at offset `bar` of every CTA of the cluster in `mask`.
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   bar),
-               "h"(mask)
-               : "memory");
-}
-
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
