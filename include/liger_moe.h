@@ -143,7 +143,8 @@ int liger_moe_dispatch(const int32_t* topk_ids, const float* topk_w, const void*
  * the workspace: its scratch is a fixed 1 MiB array inside this library,
  * present in the memory of every GPU that loads the library until the
  * process exits.  It allocates nothing and frees nothing.
- *   Limit: ceil(T*k / 256) * E * 4 + 512 <= 1 MiB (e.g. T*k <= 131072 at E = 512);
+ *   Limit: ceil(T*k / 256) * E * 4 <= 1 MiB (T*k <= 131072 at E = 512,
+ *   T*k <= 65536 at E = 1024);
  *   larger sizes return LIGER_MOE_ERR_CAPACITY before anything is launched.
  *   The first call on each device looks up the array's device address; make
  *   that first call before any stream capture.
@@ -337,10 +338,14 @@ int liger_moe_router_bwd(const float* d_logits, const int32_t* topk_ids, const i
                          void* dx, void* dw_router, float* d_bias, void* stream);
 
 /*
- * Synchronises `stream`, then returns LIGER_MOE_OK and *flags = 0 when no
- * device error was recorded on the current device since the last call, or
- * LIGER_MOE_ERR_DEVICE with *flags = the LIGER_MOE_DEVERR_* bits.  The flag
- * is cleared.  Returns LIGER_MOE_ERR_LAUNCH if the synchronisation failed.
+ * Takes the device error flag of the current device after the work already
+ * enqueued on `stream`, then synchronises `stream`.  Returns LIGER_MOE_OK and
+ * *flags = 0 when no device error was recorded since the last call, or
+ * LIGER_MOE_ERR_DEVICE with *flags = the LIGER_MOE_DEVERR_* bits.  The flag is
+ * read and cleared in one atomic exchange on the device: a bit that a kernel
+ * on another stream sets at the same time is reported now or by the next
+ * call, never lost.  Returns LIGER_MOE_ERR_LAUNCH if the launch, the copy or
+ * the synchronisation failed.
  */
 int liger_moe_device_error(void* stream, int* flags);
 

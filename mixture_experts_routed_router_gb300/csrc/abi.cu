@@ -21,6 +21,14 @@ namespace lmoe {
 namespace {
 thread_local char g_last_error[256] = "";
 __device__ int g_device_error = 0;  // device-side error word, one per device
+__device__ int g_device_error_taken = 0;  // what the last read-and-clear took out of it
+
+// Reads and clears the error word in one atomic exchange, so that a bit a kernel on another
+// stream sets at the same moment is either taken now or left for the next read, never lost.
+__global__ void take_device_error_kernel() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  g_device_error_taken = atomicExch(&g_device_error, 0);
+}
 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
@@ -29,21 +37,12 @@ bool g_dev_known[kMaxDevices] = {};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-constexpr long long kIndexLimit = 2147483647LL;  // int32 row / slot indices and TMA coordinates
-
 // Shape checks shared by the expert entry points.
 int check_shapes(long long R, int H, int I, int E) {
   if (R < 0 || E < 1 || H < 1 || I < 1) return LIGER_MOE_ERR_INVALID_ARG;
   if (E > kMaxExperts) return LIGER_MOE_ERR_CAPACITY;
   if (H % 64 != 0 || I % 64 != 0) return LIGER_MOE_ERR_MISALIGNED;
   if (R > kIndexLimit || 2LL * I * E > kIndexLimit || 1LL * H * E > kIndexLimit) return LIGER_MOE_ERR_CAPACITY;
-  return LIGER_MOE_OK;
-}
-
-int check_topk(long long T, int E, int k) {
-  if (T < 0 || E < 1 || k < 1 || k > E) return LIGER_MOE_ERR_INVALID_ARG;
-  if (E > kMaxExperts || k > kMaxTopK) return LIGER_MOE_ERR_CAPACITY;
-  if (T * k > kIndexLimit) return LIGER_MOE_ERR_CAPACITY;
   return LIGER_MOE_OK;
 }
 
@@ -63,6 +62,13 @@ T* carve(uint8_t*& cursor, size_t bytes) {
 }
 
 }  // namespace
+
+int check_topk(long long T, int E, int k) {
+  if (T < 0 || E < 1 || k < 1 || k > E) return LIGER_MOE_ERR_INVALID_ARG;
+  if (E > kMaxExperts || k > kMaxTopK) return LIGER_MOE_ERR_CAPACITY;
+  if (T * k > kIndexLimit) return LIGER_MOE_ERR_CAPACITY;
+  return LIGER_MOE_OK;
+}
 
 // ---------------------------------------------------------------- kernel trace
 namespace {
@@ -645,15 +651,13 @@ LIGER_MOE_API int liger_moe_device_error(void* stream, int* flags) {
   if (flags == nullptr) return LIGER_MOE_ERR_INVALID_ARG;
   DeviceInfo dev;
   if (int rc = current_device(&dev)) return rc;
-  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) {
-    set_cuda_error(e, "cudaStreamSynchronize");
-    return LIGER_MOE_ERR_LAUNCH;
-  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* taken = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&taken, g_device_error_taken);
+  if (e == cudaSuccess) e = launch_kernel(take_device_error_kernel, dim3(1), dim3(1), 0, s, "take_device_error", 1);
   int v = 0;
-  e = cudaMemcpy(&v, dev.err_flag, sizeof(int), cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess && v != 0) e = cudaMemset(dev.err_flag, 0, sizeof(int));
-  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&v, taken, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) {
     set_cuda_error(e, "reading the device error flag");
     return LIGER_MOE_ERR_LAUNCH;

@@ -28,7 +28,8 @@ namespace lmoe {
 namespace {
 
 // 1 MiB: histograms of ceil(T*k / 256) slot chunks x E experts, int32 each,
-// e.g. T*k up to 131072 with E = 512, or up to 65536 with E = 1024.
+// so T*k up to 131072 with E = 512, or up to 65536 with E = 1024.  The array
+// is 256-byte aligned, which is all the dispatch kernels ask of their scratch.
 constexpr size_t kDispatchScratchBytes = size_t(1) << 20;
 
 static __device__ __align__(256) int32_t g_dispatch_scratch[kDispatchScratchBytes / sizeof(int32_t)];
@@ -64,8 +65,7 @@ LIGER_MOE_API int liger_moe_dispatch_noalloc(const int32_t* topk_ids, const floa
                                              int H, int E, int k, int32_t* counts, int32_t* m_indptr,
                                              int32_t* row_to_slot, int32_t* slot_to_row, float* w_perm,
                                              void* x_perm, void* stream) {
-  if (T < 0 || E < 1 || k < 1 || k > E) return LIGER_MOE_ERR_INVALID_ARG;
-  if (E > kMaxExperts || k > kMaxTopK || static_cast<long long>(T) * k > 2147483647LL) return LIGER_MOE_ERR_CAPACITY;
+  if (int rc = check_topk(T, E, k)) return rc;
   const long long R = static_cast<long long>(T) * k;
   if (counts == nullptr || m_indptr == nullptr) return LIGER_MOE_ERR_INVALID_ARG;
   if (R > 0 && (topk_ids == nullptr || row_to_slot == nullptr || slot_to_row == nullptr))
@@ -76,11 +76,8 @@ LIGER_MOE_API int liger_moe_dispatch_noalloc(const int32_t* topk_ids, const floa
     if (H < 64 || H % 64 != 0 || (reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(x_perm) & 15u))
       return LIGER_MOE_ERR_MISALIGNED;
   }
-  // the stated limit: ceil(T*k / 256) * E * 4 + 512 <= 1 MiB (covers the histogram and its alignment)
-  const long long chunks = (R + 255) / 256;
-  if (chunks * E * 4 + 512 > static_cast<long long>(kDispatchScratchBytes) ||
-      dispatch_workspace_bytes(R, E) > kDispatchScratchBytes)
-    return LIGER_MOE_ERR_CAPACITY;
+  // the stated limit: the histograms, ceil(T*k / 256) * E * 4 bytes, fit in the array
+  if (dispatch_scratch_bytes(R, E) > kDispatchScratchBytes) return LIGER_MOE_ERR_CAPACITY;
   DeviceInfo dev;
   if (int rc = current_device(&dev)) return rc;
   void* scratch = nullptr;

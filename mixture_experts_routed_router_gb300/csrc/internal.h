@@ -13,6 +13,10 @@ namespace lmoe {
 
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
+constexpr long long kIndexLimit = 2147483647LL;  // int32 row / slot indices and TMA coordinates
+
+// Validates T, E and k of an entry point that takes top-k routing (a liger_moe_status).
+int check_topk(long long T, int E, int k);
 
 // Records a CUDA error message for liger_moe_last_cuda_error().
 void set_cuda_error(cudaError_t e, const char* where);
@@ -31,7 +35,9 @@ int current_device(DeviceInfo* info);
 // ---- launchers (each enqueues on `s`; return a liger_moe_status)
 int launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s);
 
-// Dispatch workspace bytes for R slots and E experts.
+// Bytes of scratch the dispatch kernels use for R slots and E experts (per-chunk histograms),
+// and the workspace size the dispatch entry point asks for (that, plus alignment slack).
+size_t dispatch_scratch_bytes(long long R, int E);
 size_t dispatch_workspace_bytes(long long R, int E);
 int launch_dispatch(const int32_t* ids, const float* w, const uint16_t* x, int T, int H, int E, int k,
                     int32_t* counts, int32_t* m_indptr, int32_t* row_to_slot, int32_t* slot_to_row, float* w_perm,

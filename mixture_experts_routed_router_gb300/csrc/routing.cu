@@ -458,10 +458,12 @@ int launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, fl
   return check_launch("route_topk");
 }
 
-size_t dispatch_workspace_bytes(long long R, int E) {
+size_t dispatch_scratch_bytes(long long R, int E) {
   const long long nunits = (R + kUnit - 1) / kUnit;
-  return align_up(static_cast<size_t>(nunits) * E * sizeof(int32_t), 256) + 256;
+  return static_cast<size_t>(nunits) * E * sizeof(int32_t);
 }
+
+size_t dispatch_workspace_bytes(long long R, int E) { return align_up(dispatch_scratch_bytes(R, E), 256) + 256; }
 
 int launch_dispatch(const int32_t* ids, const float* w, const uint16_t* x, int T, int H, int E, int k,
                     int32_t* counts, int32_t* m_indptr, int32_t* row_to_slot, int32_t* slot_to_row, float* w_perm,
