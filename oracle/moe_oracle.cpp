@@ -539,47 +539,101 @@ int oracle_backward_dw(const uint16_t* x, const uint16_t* dy, const uint16_t* wg
     if (experts[i] < 0 || experts[i] >= E) return ORACLE_BAD_ARG;
   for (long long s = 0; s < static_cast<long long>(T) * k; ++s)
     if (ids[s] < 0 || ids[s] >= E) return ORACLE_BAD_ID;
-  parallel_for(nexp, threads, [&](int i) {
-    int e = experts[i];
-    std::vector<float> g(I), u(I), hq(I), dHu(I), dg(I), du(I);
-    const int nin = first_rows(act, I);
-    std::vector<float> agu(static_cast<size_t>(nin) * H, 0.0f), ad(static_cast<size_t>(H) * I, 0.0f);
-    const uint16_t* wgu_e = wgu + static_cast<size_t>(e) * nin * H;
-    const uint16_t* wd_e = wd + static_cast<size_t>(e) * H * I;
-    for (int t = 0; t < T; ++t) {
-      for (int j = 0; j < k; ++j) {
-        if (ids[static_cast<size_t>(t) * k + j] != e) continue;
-        float wj = w[static_cast<size_t>(t) * k + j];
-        const uint16_t* xr = x + static_cast<size_t>(t) * H;
-        const uint16_t* dyr = dy + static_cast<size_t>(t) * H;
-        gate_up_row(xr, wgu_e, H, I, g.data(), u.data(), hq.data(), act, clamp);
-        swiglu_row_backward(dyr, wd_e, H, I, wj, g.data(), u.data(), hq.data(), dHu.data(), dg.data(),
-                            du.data(), act, clamp);
-        for (int n = 0; n < I; ++n) {
-          float* rg = agu.data() + static_cast<size_t>(n) * H;
-          float* ru = gated(act) ? agu.data() + static_cast<size_t>(I + n) * H : nullptr;
-          for (int h = 0; h < H; ++h) {
-            float xv = bf16_to_float(xr[h]);
-            rg[h] += dg[n] * xv;
-            if (ru) ru[h] += du[n] * xv;
+  // Two passes with the same arithmetic as one loop per expert: (1) each routed row's dg, du
+  // and hq (independent rows, so they run in parallel); (2) each block of output rows sums
+  // its products over the expert's rows in row order.  Experts are taken in groups whose
+  // per-row vectors fit a bounded buffer.
+  const int nin = first_rows(act, I);
+  const long long R = static_cast<long long>(T) * k;
+  struct Row {
+    int t;
+    float wj;
+  };
+  std::vector<std::vector<Row>> rows_of(nexp);
+  for (int i = 0; i < nexp; ++i)
+    for (long long s = 0; s < R; ++s)  // t ascending, j ascending within t
+      if (ids[s] == experts[i]) rows_of[i].push_back(Row{static_cast<int>(s / k), w[s]});
+  const size_t cap_rows = std::max<size_t>(1, (size_t(256) << 20) / (3 * sizeof(float) * static_cast<size_t>(I)));
+  constexpr int kBlk = 32;  // output rows per unit of the second pass
+  for (int i0 = 0; i0 < nexp;) {
+    int i1 = i0;
+    std::vector<size_t> first{0};  // row offset of each expert of the group in the buffers
+    while (i1 < nexp && (i1 == i0 || first.back() + rows_of[i1].size() <= cap_rows)) {
+      first.push_back(first.back() + rows_of[i1].size());
+      ++i1;
+    }
+    const size_t nrows = first.back();
+    std::vector<int> owner(nrows);
+    for (int i = i0; i < i1; ++i)
+      for (size_t q = first[i - i0]; q < first[i - i0 + 1]; ++q) owner[q] = i;
+    std::vector<float> dgv(nrows * I), duv(nrows * I), hqv(nrows * I);
+    parallel_for(static_cast<int>(nrows), threads, [&](int q) {
+      const int i = owner[q];
+      const int e = experts[i];
+      const Row& rw = rows_of[i][q - first[i - i0]];
+      std::vector<float> g(I), u(I), dHu(I);
+      gate_up_row(x + static_cast<size_t>(rw.t) * H, wgu + static_cast<size_t>(e) * nin * H, H, I, g.data(), u.data(),
+                  hqv.data() + static_cast<size_t>(q) * I, act, clamp);
+      swiglu_row_backward(dy + static_cast<size_t>(rw.t) * H, wd + static_cast<size_t>(e) * H * I, H, I, rw.wj,
+                          g.data(), u.data(), hqv.data() + static_cast<size_t>(q) * I, dHu.data(),
+                          dgv.data() + static_cast<size_t>(q) * I, duv.data() + static_cast<size_t>(q) * I, act, clamp);
+    });
+    // units: per expert of the group, I / kBlk blocks of gate(/up) rows n, then H / kBlk blocks of rows c
+    const int ublk_gu = (I + kBlk - 1) / kBlk, ublk_d = (H + kBlk - 1) / kBlk;
+    const int per_e = ublk_gu + ublk_d;
+    parallel_for((i1 - i0) * per_e, threads, [&](int unit) {
+      const int i = i0 + unit / per_e;
+      const int b = unit % per_e;
+      const std::vector<Row>& rws = rows_of[i];
+      const size_t q0 = first[i - i0];
+      if (b < ublk_gu) {
+        const int n0 = b * kBlk, n1 = std::min(I, n0 + kBlk);
+        std::vector<float> agu(static_cast<size_t>(n1 - n0) * H * 2, 0.0f);  // gate rows, then up rows
+        for (size_t r = 0; r < rws.size(); ++r) {
+          const float* dg = dgv.data() + (q0 + r) * I;
+          const float* du = duv.data() + (q0 + r) * I;
+          const uint16_t* xr = x + static_cast<size_t>(rws[r].t) * H;
+          for (int n = n0; n < n1; ++n) {
+            float* rg = agu.data() + static_cast<size_t>(n - n0) * H;
+            float* ru = gated(act) ? agu.data() + static_cast<size_t>(n1 - n0 + n - n0) * H : nullptr;
+            for (int h = 0; h < H; ++h) {
+              float xv = bf16_to_float(xr[h]);
+              rg[h] += dg[n] * xv;
+              if (ru) ru[h] += du[n] * xv;
+            }
           }
         }
-        for (int c = 0; c < H; ++c) {
-          float wdy = wj * bf16_to_float(dyr[c]);
-          float* rd = ad.data() + static_cast<size_t>(c) * I;
-          for (int n = 0; n < I; ++n) rd[n] += wdy * hq[n];
+        if (dwgu_out) {
+          uint16_t* o = dwgu_out + static_cast<size_t>(i) * nin * H;
+          for (int n = n0; n < n1; ++n) {
+            for (int h = 0; h < H; ++h) {
+              o[static_cast<size_t>(n) * H + h] = float_to_bf16(agu[static_cast<size_t>(n - n0) * H + h]);
+              if (gated(act))
+                o[static_cast<size_t>(I + n) * H + h] = float_to_bf16(agu[static_cast<size_t>(n1 - n0 + n - n0) * H + h]);
+            }
+          }
+        }
+      } else {
+        const int c0 = (b - ublk_gu) * kBlk, c1 = std::min(H, c0 + kBlk);
+        std::vector<float> ad(static_cast<size_t>(c1 - c0) * I, 0.0f);
+        for (size_t r = 0; r < rws.size(); ++r) {
+          const float wj = rws[r].wj;
+          const float* hq = hqv.data() + (q0 + r) * I;
+          const uint16_t* dyr = dy + static_cast<size_t>(rws[r].t) * H;
+          for (int c = c0; c < c1; ++c) {
+            float wdy = wj * bf16_to_float(dyr[c]);
+            float* rd = ad.data() + static_cast<size_t>(c - c0) * I;
+            for (int n = 0; n < I; ++n) rd[n] += wdy * hq[n];
+          }
+        }
+        if (dwd_out) {
+          uint16_t* o = dwd_out + static_cast<size_t>(i) * H * I + static_cast<size_t>(c0) * I;
+          for (size_t q = 0; q < ad.size(); ++q) o[q] = float_to_bf16(ad[q]);
         }
       }
-    }
-    if (dwgu_out) {
-      uint16_t* o = dwgu_out + static_cast<size_t>(i) * nin * H;
-      for (size_t q = 0; q < agu.size(); ++q) o[q] = float_to_bf16(agu[q]);
-    }
-    if (dwd_out) {
-      uint16_t* o = dwd_out + static_cast<size_t>(i) * H * I;
-      for (size_t q = 0; q < ad.size(); ++q) o[q] = float_to_bf16(ad[q]);
-    }
-  });
+    });
+    i0 = i1;
+  }
   return ORACLE_OK;
 }
 

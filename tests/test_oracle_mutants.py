@@ -41,8 +41,8 @@ MUTANTS = {
     "router_grad_unweighted_gamma": ("for (int j = 0; j < k; ++j) S += w[static_cast<size_t>(t) * k + j] * gam[j];",
                                      "for (int j = 0; j < k; ++j) S += gam[j];"),
     "dwd_weight_dropped": ("float wdy = wj * bf16_to_float(dyr[c]);", "float wdy = bf16_to_float(dyr[c]);"),
-    "dwgu_wrong_input_row": ("float xv = bf16_to_float(xr[h]);\n            rg[h]",
-                             "float xv = bf16_to_float(dyr[h]);\n            rg[h]"),
+    "dwgu_wrong_input_row": ("const uint16_t* xr = x + static_cast<size_t>(rws[r].t) * H;",
+                             "const uint16_t* xr = dy + static_cast<size_t>(rws[r].t) * H;"),
     "dhu_reads_gate_weights": ("const uint16_t* wr = wd_e + static_cast<size_t>(c) * I;\n    for (int n = 0; n < I; ++n) dHu[n]",
                                "const uint16_t* wr = wd_e + static_cast<size_t>(c) * I + 1;\n    for (int n = 0; n < I - 1; ++n) dHu[n]"),
 }
