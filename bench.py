@@ -15,6 +15,12 @@ with the workload's shapes (no dataset).  The printed JSON line carries:
 * clocks        SM clock / throttle reasons sampled with nvidia-smi during the timed loop
 * inference_forward  the forward alone without saved derivative factors (nothing kept for a
                 backward): ms, TFLOP/s, and each expert GEMM's TFLOP/s against the bf16 peaks
+* sustained     the same step graph replayed back to back for at least a second, with the
+                median SM clock of that window (the power cap settles in over such a run)
+* train_shape_forward  the training shape (H=2048, I=768, E=128, top-8, 8192 tokens), the one
+                shape whose forward expert GEMMs are tensor-bound: each GEMM's TFLOP/s in its
+                training step and in an inference forward, against the burst and sustained
+                bf16 peaks, with the clocks sampled over those replays
 
 ``--impl reference`` times the CPU oracle itself on the host cores (the only
 reference implementation of this method that exists here).
@@ -38,7 +44,10 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer fwd/bwd TFLOP/s and tokens/s on 1 GB300; % of BF16 tensor-core peak"
-DEFAULT_WORKLOAD = "fwd_T8192_H2048_I512_E256_k8"
+# The largest single-GPU workload: the 4096/1024/512-expert top-10 model shape with Zipf(1.2)-skewed
+# expert load.  The training shape's forward GEMMs get their own record (train_shape_forward).
+DEFAULT_WORKLOAD = "fwd_zipf_T8192_H4096_I1024_E512_k10"
+TRAIN_SHAPE = "train_T8192_H2048_I768_E128_k8"
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -52,6 +61,7 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-train-shape", action="store_true", help="leave out the training shape's forward-GEMM record")
     ap.add_argument("--no-graph", action="store_true", help="launch the timed steps one by one instead of "
                     "replaying them as one captured CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work of the oracle baseline sample")
@@ -330,6 +340,193 @@ def whole_job_rate(world: int, units_per_rank: float, slowest_ms: float) -> floa
 
 
 # ---------------------------------------------------------------- our arm
+class Layer:
+    """Device buffers and the layer calls of one workload (forward, backward, one step)."""
+
+    def __init__(self, args, wl, dev, inp, act="swiglu", inputs="x_perm", router=False):
+        import numpy as np
+        import torch
+
+        import mixture_experts_routed_router_gb300 as moe
+
+        self.wl, self.dev = wl, dev
+        T, H, I, E, k, R = wl.T, wl.H, wl.I, wl.E, wl.k, wl.R
+        self.gated = gated = act != "relu2"
+        if not gated:  # two-weight experts: the up weight W_up [E, I, H] is the gate half of W_gu
+            inp["wgu"] = np.ascontiguousarray(inp["wgu"][:, :I])
+        nin = 2 * I if gated else I  # rows of the first weight per expert
+
+        def to_dev(a):
+            a = np.ascontiguousarray(a)
+            if a.dtype == np.uint16:
+                return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+            return torch.from_numpy(a).to(dev)
+
+        self.logits, self.x, self.dy = to_dev(inp["logits"]), to_dev(inp["x"]), to_dev(inp["dy"])
+        wgu, wd = to_dev(inp["wgu"]), to_dev(inp["wd"])
+        self.weight_bytes = (wgu.numel() + wd.numel()) * 2
+        bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+        e = lambda *s, dt=bf: torch.empty(s, dtype=dt, device=dev)
+        self.empty = e
+        ids, w = e(T, k, dt=i32), e(T, k, dt=f32)
+        dbuf = dict(counts=e(E, dt=i32), m_indptr=e(E + 1, dt=i32), row_to_slot=e(R, dt=i32),
+                    slot_to_row=e(R, dt=i32), w_perm=e(R, dt=f32))
+        gather = inputs == "gather"
+        if not gather:
+            dbuf["x_perm"] = e(R, H)
+        fbuf = dict(h_perm=e(R, I), gu_perm=e(R, nin, dt=f32), y_perm=e(R, H))
+        self.Y = Y = e(T, H)
+        bbuf = dict(dx=e(T, H), dw_gate_up=e(E, nin, H), dw_down=e(E, H, I), d_logits=e(T, E, dt=f32))
+        ws_d = e(moe.workspace_bytes("dispatch", T=T, E=E, k=k), dt=torch.uint8)
+        ws_f = e(moe.workspace_bytes("grouped_swiglu_fwd", R=R, H=H, I=I, E=E), dt=torch.uint8)
+        ws_b = e(moe.workspace_bytes("bwd_dx_dw", T=T, H=H, I=I, E=E, k=k, saved_gu=True, gather=gather),
+                 dt=torch.uint8)
+        self.dbuf = dbuf
+        # router: the router projection (weights resident like the experts'); with it the step's input
+        # is x alone and the logits buffer is an output of the step
+        wr = to_dev(inp["wr"]) if router else None
+        rbias = to_dev(inp["bias"]) if router and inp["bias"] is not None else None
+        rbuf = dict(dw_router=e(E, H), d_bias=e(E, dt=f32)) if router else None
+
+        # inputs x_perm (default): the dispatch writes the expert-major copy x_perm (and the backward
+        # its dy_perm), which the GEMMs read as dense TMA tiles.  inputs gather: the layer on
+        # token-major x and dY, the expert GEMMs copying their rows by token, so no expert-major copy
+        # exists (less memory, slower).
+        # save=False: an inference forward, which keeps no derivative factors for a backward
+        def forward(lg, xx, y_out=None, save=True):
+            if router:
+                moe.router_logits(xx, wr, rbias, out=lg)
+            moe.route_topk(lg, k, topk_ids=ids, topk_w=w)
+            moe.dispatch(ids, w, None if gather else xx, E, out=dbuf, workspace=ws_d)
+            if gather:
+                moe.grouped_swiglu_fwd_gather(xx, dbuf["row_to_slot"], k, dbuf["m_indptr"], wgu, wd, dbuf["w_perm"],
+                                              save_gu=save, out=fbuf, workspace=ws_f)
+            elif act != "swiglu":
+                moe.grouped_glu_fwd(dbuf["x_perm"], dbuf["m_indptr"], wgu, wd, dbuf["w_perm"], act, args.act_clamp,
+                                    save_gu=save, out=fbuf, workspace=ws_f)
+            else:
+                moe.grouped_swiglu_fwd(dbuf["x_perm"], dbuf["m_indptr"], wgu, wd, dbuf["w_perm"], save_gu=save,
+                                       out=fbuf, workspace=ws_f)
+            moe.combine(fbuf["y_perm"], dbuf["slot_to_row"], T, k, out=Y if y_out is None else y_out)
+
+        def backward(dyy, xx, dx_out=None, dl_out=None):
+            out = dict(bbuf)
+            if dx_out is not None:
+                out.update(dx=dx_out, d_logits=dl_out)
+            # the saved derivative factors make the backward the same for every gated activation;
+            # two-weight experts (relu2) have their own operand shapes
+            args_b = (dyy, xx if gather else dbuf["x_perm"], fbuf["h_perm"], fbuf["gu_perm"], ids, w,
+                      dbuf["m_indptr"], dbuf["row_to_slot"], dbuf["slot_to_row"], dbuf["w_perm"], wgu, wd)
+            if not gated:
+                moe.bwd_dx_dw_glu(*args_b, act, args.act_clamp, out=out, workspace=ws_b)
+            else:
+                (moe.bwd_dx_dw_gather if gather else moe.bwd_dx_dw)(*args_b, out=out, workspace=ws_b)
+            if router:  # adds the router's input gradient to dX; dWr, dbias
+                moe.router_bwd(out["d_logits"], ids, dbuf["m_indptr"], dbuf["row_to_slot"], xx, wr, out["dx"],
+                               dw_router=rbuf["dw_router"], d_bias=rbuf["d_bias"])
+
+        self.forward, self.backward = forward, backward
+
+    def step(self):
+        self.forward(self.logits, self.x)
+        self.backward(self.dy, self.x)
+
+
+def capture(fn, n):
+    """One CUDA graph of n calls of fn (the library's calls only enqueue work on the current stream)."""
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(n):
+            fn()
+    return g
+
+
+def gemm_rates(wl, records, peaks, gated=True) -> dict:
+    """Each grouped GEMM's mean duration and TFLOP/s in a trace, against the burst and sustained bf16 peaks."""
+    stats = {}
+    for name, ms in records:
+        s_ = stats.setdefault(name, [0, 0.0])
+        s_[0] += 1
+        s_[1] += ms
+    out = {}
+    for name, (n, tot) in sorted(stats.items(), key=lambda kv: -kv[1][1]):
+        kind, amount = kernel_work(wl, name, gated)
+        if kind != "flop" or tot <= 0:
+            continue
+        tf = amount / (tot / n * 1e-3) / 1e12
+        out[name] = {"avg_us": round(1e3 * tot / n, 2), "tflops": round(tf, 1),
+                     "frac_of_bf16_burst": round(tf / peaks["bf16_tflops"], 4),
+                     "frac_of_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 4)}
+    return out
+
+
+def train_shape_forward(args, dev, local_rank, peaks, max_over_ranks, world) -> dict:
+    """The training shape's forward expert GEMMs, in its training step and in an inference forward.
+
+    Each GEMM's rate comes from the library's per-launch trace of a replayed graph (the step's,
+    then the inference forward's); the clocks are sampled over both replays."""
+    import torch
+
+    import mixture_experts_routed_router_gb300 as moe
+    import synthetic
+
+    wl = synthetic.workload(TRAIN_SHAPE)
+    inp = synthetic.make_inputs(wl, seed=args.seed, want=("x", "logits", "wgu", "wd", "dy"))
+    L = Layer(args, wl, dev, inp)
+    for _ in range(3):
+        L.step()
+    torch.cuda.synchronize()
+    n_step, n_fwd = 40, 100
+    # The trace logs a record per launch when the graphs are captured; each replay re-times the
+    # records' events, so the records read after the last replay hold that replay's durations.
+    moe.trace_enable(True)  # stays on until the records are read (turning it off clears them)
+    g_step = capture(L.step, n_step)
+    n_step_records = moe.load_library().liger_moe_trace_count()  # records of the step graph (not yet timed)
+    g_inf = capture(lambda: L.forward(L.logits, L.x, save=False), n_fwd)
+    g_step.replay()  # first replays upload the graphs; untimed
+    g_inf.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(gpu_index_for(local_rank))
+    clocks.start()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    stream = torch.cuda.current_stream()
+    ev[0].record(stream)
+    g_step.replay()
+    ev[1].record(stream)
+    ev[2].record(stream)
+    g_inf.replay()
+    ev[3].record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    records = moe.trace_records()
+    step_records, inf_records = records[:n_step_records], records[n_step_records:]
+    moe.trace_enable(False)
+    flags = moe.device_error()
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x} in the training-shape record")
+    fl = step_flops(wl)
+    step_ms = max_over_ranks(ev[0].elapsed_time(ev[1])) / n_step  # traced replays: a few % slower
+    inf_ms = max_over_ranks(ev[2].elapsed_time(ev[3])) / n_fwd
+    rec = {"workload": wl.name, "config": wl.as_dict(),
+           "training_step": {"ms_per_step_traced": round(step_ms, 4),
+                             "tflops": round(whole_job_rate(world, fl["total"], step_ms) / 1e12, 2),
+                             "gemms": {k_: v for k_, v in gemm_rates(wl, step_records, peaks).items()
+                                       if k_ in ("gemm_gate_up_swiglu", "gemm_down_scale")}},
+           "inference_forward": {"ms_traced": round(inf_ms, 4),
+                                 "tflops": round(whole_job_rate(world, fl["fwd"], inf_ms) / 1e12, 2),
+                                 "gemms": gemm_rates(wl, inf_records, peaks)},
+           "peaks": {"bf16_burst_tflops": peaks["bf16_tflops"], "bf16_sustained_tflops": peaks["bf16_tflops_sustained"],
+                     "source": peaks["source"]},
+           "clocks": clock_info,
+           "timing": f"library trace of a replayed graph: {n_step} training steps, then {n_fwd} inference forwards"}
+    del L, g_step, g_inf
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -346,79 +543,12 @@ def run_ours(args, rank, world, local_rank):
     wl = synthetic.workload(args.workload)
     T, H, I, E, k, R = wl.T, wl.H, wl.I, wl.E, wl.k, wl.R
     inp = synthetic.make_inputs(wl, seed=args.seed, want=("x", "logits", "wgu", "wd", "dy", "wr"))
-    gated = args.act != "relu2"
-    if not gated:  # two-weight experts: the up weight W_up [E, I, H] is the gate half of W_gu
-        inp["wgu"] = np.ascontiguousarray(inp["wgu"][:, :I])
-    nin = 2 * I if gated else I  # rows of the first weight per expert
-
-    def to_dev(a):
-        a = np.ascontiguousarray(a)
-        if a.dtype == np.uint16:
-            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
-        return torch.from_numpy(a).to(dev)
-
-    logits, x, dy = to_dev(inp["logits"]), to_dev(inp["x"]), to_dev(inp["dy"])
-    wgu, wd = to_dev(inp["wgu"]), to_dev(inp["wd"])
-    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
-    e = lambda *s, dt=bf: torch.empty(s, dtype=dt, device=dev)
-    ids, w = e(T, k, dt=i32), e(T, k, dt=f32)
-    dbuf = dict(counts=e(E, dt=i32), m_indptr=e(E + 1, dt=i32), row_to_slot=e(R, dt=i32), slot_to_row=e(R, dt=i32),
-                w_perm=e(R, dt=f32))
-    gather = args.inputs == "gather"
-    if not gather:
-        dbuf["x_perm"] = e(R, H)
-    fbuf = dict(h_perm=e(R, I), gu_perm=e(R, nin, dt=f32), y_perm=e(R, H))
-    Y = e(T, H)
-    bbuf = dict(dx=e(T, H), dw_gate_up=e(E, nin, H), dw_down=e(E, H, I), d_logits=e(T, E, dt=f32))
-    ws_d = e(moe.workspace_bytes("dispatch", T=T, E=E, k=k), dt=torch.uint8)
-    ws_f = e(moe.workspace_bytes("grouped_swiglu_fwd", R=R, H=H, I=I, E=E), dt=torch.uint8)
-    ws_b = e(moe.workspace_bytes("bwd_dx_dw", T=T, H=H, I=I, E=E, k=k, saved_gu=True, gather=gather), dt=torch.uint8)
-    # --router: the router projection (weights resident like the experts'); with it the step's input
-    # is x alone and the logits buffer is an output of the step
-    wr = to_dev(inp["wr"]) if args.router else None
-    rbias = to_dev(inp["bias"]) if args.router and inp["bias"] is not None else None
-    rbuf = dict(dw_router=e(E, H), d_bias=e(E, dt=f32)) if args.router else None
-
-    # --inputs x_perm (default): the dispatch writes the expert-major copy x_perm (and the backward
-    # its dy_perm), which the GEMMs read as dense TMA tiles.  --inputs gather: the layer on
-    # token-major x and dY, the expert GEMMs copying their rows by token, so no expert-major copy
-    # exists (less memory, slower).
-    # save=False: an inference forward, which keeps no derivative factors for a backward
-    def forward(lg, xx, y_out=None, save=True):
-        if args.router:
-            moe.router_logits(xx, wr, rbias, out=lg)
-        moe.route_topk(lg, k, topk_ids=ids, topk_w=w)
-        moe.dispatch(ids, w, None if gather else xx, E, out=dbuf, workspace=ws_d)
-        if gather:
-            moe.grouped_swiglu_fwd_gather(xx, dbuf["row_to_slot"], k, dbuf["m_indptr"], wgu, wd, dbuf["w_perm"],
-                                          save_gu=save, out=fbuf, workspace=ws_f)
-        elif args.act != "swiglu":
-            moe.grouped_glu_fwd(dbuf["x_perm"], dbuf["m_indptr"], wgu, wd, dbuf["w_perm"], args.act, args.act_clamp,
-                                save_gu=save, out=fbuf, workspace=ws_f)
-        else:
-            moe.grouped_swiglu_fwd(dbuf["x_perm"], dbuf["m_indptr"], wgu, wd, dbuf["w_perm"], save_gu=save,
-                                   out=fbuf, workspace=ws_f)
-        moe.combine(fbuf["y_perm"], dbuf["slot_to_row"], T, k, out=Y if y_out is None else y_out)
-
-    def backward(dyy, xx, dx_out=None, dl_out=None):
-        out = dict(bbuf)
-        if dx_out is not None:
-            out.update(dx=dx_out, d_logits=dl_out)
-        # the saved derivative factors make the backward the same for every gated activation;
-        # two-weight experts (relu2) have their own operand shapes
-        args_b = (dyy, xx if gather else dbuf["x_perm"], fbuf["h_perm"], fbuf["gu_perm"], ids, w, dbuf["m_indptr"],
-                  dbuf["row_to_slot"], dbuf["slot_to_row"], dbuf["w_perm"], wgu, wd)
-        if not gated:
-            moe.bwd_dx_dw_glu(*args_b, args.act, args.act_clamp, out=out, workspace=ws_b)
-        else:
-            (moe.bwd_dx_dw_gather if gather else moe.bwd_dx_dw)(*args_b, out=out, workspace=ws_b)
-        if args.router:  # adds the router's input gradient to dX; dWr, dbias
-            moe.router_bwd(out["d_logits"], ids, dbuf["m_indptr"], dbuf["row_to_slot"], xx, wr, out["dx"],
-                           dw_router=rbuf["dw_router"], d_bias=rbuf["d_bias"])
-
-    def step():
-        forward(logits, x)
-        backward(dy, x)
+    L = Layer(args, wl, dev, inp, act=args.act, inputs=args.inputs, router=args.router)
+    gated = L.gated
+    logits, x, dy, Y, dbuf = L.logits, L.x, L.dy, L.Y, L.dbuf
+    forward, backward, step = L.forward, L.backward, L.step
+    e = L.empty
+    bf, f32 = torch.bfloat16, torch.float32
 
     def barrier():
         rank_barrier(dist)
@@ -497,6 +627,32 @@ def run_ours(args, rank, world, local_rank):
     ms_per_step = elapsed_ms / args.steps
     value = whole_job_rate(world, args.steps * fl["total"], elapsed_ms) / 1e12
     tokens_per_s = whole_job_rate(world, args.steps * T, elapsed_ms)
+
+    # ---------------- sustained: the same untraced step graph replayed back to back for at least
+    # a second (the timed region above can be shorter than the time the power cap takes to settle)
+    sustained = None
+    if graph is not None:
+        n_rep = max(1, math.ceil(1200.0 / max(elapsed_ms, 1e-3)))
+        sclocks = ClockSampler(gpu_index_for(local_rank))
+        sclocks.start()
+        barrier()
+        torch.cuda.synchronize()
+        ev10, ev11 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev10.record(stream)
+        for _ in range(n_rep):
+            graph.replay()
+        ev11.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        sc = sclocks.stop()
+        s_ms = max_over_ranks(ev10.elapsed_time(ev11))
+        sustained = {"seconds": round(s_ms / 1e3, 3), "steps": n_rep * args.steps,
+                     "ms_per_step": round(s_ms / (n_rep * args.steps), 4),
+                     "value": round(whole_job_rate(world, n_rep * args.steps * fl["total"], s_ms) / 1e12, 2),
+                     "unit": "TFLOP/s", "sm_mhz_median": sc["sm_mhz"], "clocks": sc}
+        flags = moe.device_error()
+        if flags:
+            raise RuntimeError(f"device error flags {flags:#x} in the sustained replay")
 
     # forward-only timing (same buffers, launched the same way), for the fwd / bwd split
     ev2, ev3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -604,20 +760,7 @@ def run_ours(args, rank, world, local_rank):
     if traffic is not None:
         roofline["traffic"] = traffic
 
-    inf_stats = {}
-    for name, ms in inf_records:
-        s_ = inf_stats.setdefault(name, [0, 0.0])
-        s_[0] += 1
-        s_[1] += ms
-    inf_gemms = {}
-    for name, (n, tot) in sorted(inf_stats.items(), key=lambda kv: -kv[1][1]):
-        kind, amount = kernel_work(wl, name, gated)
-        if kind != "flop" or tot <= 0:
-            continue
-        tf = amount / (tot / n * 1e-3) / 1e12
-        inf_gemms[name] = {"avg_us": round(1e3 * tot / n, 2), "tflops": round(tf, 1),
-                           "frac_of_bf16_burst": round(tf / peaks["bf16_tflops"], 4),
-                           "frac_of_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 4)}
+    inf_gemms = gemm_rates(wl, inf_records, peaks, gated)
     inference = {"ms_per_step": round(inf_ms, 4), "tflops": round(whole_job_rate(world, fl["fwd"], inf_ms) / 1e12, 2),
                  "tokens_per_s": round(whole_job_rate(world, T, inf_ms), 1),
                  "saved_state": "none: the forward keeps no derivative factors for a backward",
@@ -709,6 +852,11 @@ def run_ours(args, rank, world, local_rank):
                "copies": "double-buffered on a copy stream, overlapped with the neighbouring steps' compute",
                "graph": g2 is not None}
 
+    # ---------------- the training shape's forward GEMMs (tensor-bound there), own buffers
+    tsf = None
+    if not args.no_train_shape:
+        tsf = train_shape_forward(args, dev, local_rank, peaks, max_over_ranks, world)
+
     # ---------------- CPU oracle baseline (rank 0, one GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -735,14 +883,14 @@ def run_ours(args, rank, world, local_rank):
                                            "expert_inputs": args.inputs, "activation": args.act,
                                            "router": "x Wr^T (+ bias) and its backward on the GPU" if args.router
                                            else "logits are the layer's input",
-                                           "l2": f"inputs larger than L2: {(wgu.numel() + wd.numel()) * 2 / 1e9:.2f} GB "
+                                           "l2": f"inputs larger than L2: {L.weight_bytes / 1e9:.2f} GB "
                                                  f"of weights + activations streamed per step (L2 129 MB)"}),
             "tokens_per_s": round(tokens_per_s, 1),
             "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(ms_per_step - fwd_ms, 4),
             "fwd_tflops": round(whole_job_rate(world, fl["fwd"], fwd_ms) / 1e12, 2),
             "bwd_tflops": round(whole_job_rate(world, fl["bwd"], ms_per_step - fwd_ms) / 1e12, 2),
             "pct_of_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
-            "inference_forward": inference,
+            "inference_forward": inference, "sustained": sustained, "train_shape_forward": tsf,
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clock_info, "launch": graph_note,
             "traced_ms_per_step": None if trace_ms is None else round(trace_ms, 4),

@@ -87,8 +87,13 @@ def test_traffic_is_reported_only_for_the_kernel_source_it_was_taken_on(monkeypa
     assert bench.load_traffic("no_such_workload", "gemm_bwd_dw_gate_up") is None
 
 
-def test_defaults_are_one_gpu_and_the_bench_workload(monkeypatch):
+def test_defaults_are_one_gpu_and_the_largest_workload(monkeypatch):
+    """The default line is the largest single-GPU workload (the most flops per step of the five)."""
     monkeypatch.setattr(sys, "argv", ["bench.py"])
     a = bench.parse_args()
-    assert (a.gpus, a.impl, a.workload, a.inputs, a.act) == (1, "ours", BENCH.name, "x_perm", "swiglu")
-    assert a.warmup >= 3 and a.steps >= 1 and not a.router
+    largest = max(synthetic.WORKLOADS.values(), key=lambda w: bench.step_flops(w)["total"])
+    assert (a.gpus, a.impl, a.workload, a.inputs, a.act) == (1, "ours", largest.name, "x_perm", "swiglu")
+    assert largest.name == "fwd_zipf_T8192_H4096_I1024_E512_k10"
+    assert a.warmup >= 3 and a.steps >= 1 and not a.router and not a.no_train_shape
+    assert synthetic.workload(bench.TRAIN_SHAPE).as_dict() == dict(workload=bench.TRAIN_SHAPE, T=8192, H=2048, I=768,
+                                                                   E=128, k=8)
