@@ -183,7 +183,8 @@ long long padded_rows(long long R, int E) { return R + 15LL * E; }
 
 size_t bwd_workspace_bytes(long long R, int H, int I, int E, bool recompute_gu, bool gather) {
   const long long Rp = padded_rows(R, E);
-  size_t b = 3 * schedule_bytes(E);  // tile prefix, padded row prefix, 256-row pair block prefix
+  // tile prefix, padded row prefix, 256-row pair block prefix, expert order, claim counters
+  size_t b = 4 * schedule_bytes(E) + kClaimBytes;
   if (!gather) b += align_up(static_cast<size_t>(R) * H * 2, 256);  // dy_perm
   b += align_up(static_cast<size_t>(Rp) * 2 * I * 2 * 2, 256);        // dgu (hi, lo), padded rows
   b += align_up(static_cast<size_t>(R) * H * 2, 256);                 // dx_perm
@@ -285,9 +286,12 @@ int grouped_swiglu_fwd_impl(const void* x_perm, const void* x, const int32_t* ro
   if (R == 0) return LIGER_MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* cur = static_cast<uint8_t*>(workspace);
-  int32_t* tile_prefix = carve<int32_t>(cur, schedule_bytes(E));
-  int32_t* pair_prefix = carve<int32_t>(cur, schedule_bytes(E));
-  if (int rc = launch_tile_schedule(m_indptr, E, R, tile_prefix, nullptr, dev, s, pair_prefix)) return rc;
+  ScheduleBufs sb;
+  sb.tile_prefix = carve<int32_t>(cur, schedule_bytes(E));
+  sb.pair_prefix = carve<int32_t>(cur, schedule_bytes(E));
+  if (int rc = launch_tile_schedule(m_indptr, E, R, sb, dev, s)) return rc;
+  int32_t* tile_prefix = sb.tile_prefix;
+  int32_t* pair_prefix = sb.pair_prefix;
   FwdGemmArgs a{};
   a.x_perm = static_cast<const uint16_t*>(x_perm);
   a.x = static_cast<const uint16_t*>(x);
@@ -440,9 +444,15 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
 
   uint8_t* cur = static_cast<uint8_t*>(workspace);
   const long long Rp = padded_rows(R, E);
-  int32_t* tile_prefix = carve<int32_t>(cur, schedule_bytes(E));
-  int32_t* pad_indptr = carve<int32_t>(cur, schedule_bytes(E));
-  int32_t* pair_prefix = carve<int32_t>(cur, schedule_bytes(E));
+  ScheduleBufs sb;
+  sb.tile_prefix = carve<int32_t>(cur, schedule_bytes(E));
+  sb.pad_indptr = carve<int32_t>(cur, schedule_bytes(E));
+  sb.pair_prefix = carve<int32_t>(cur, schedule_bytes(E));
+  sb.order = carve<int32_t>(cur, schedule_bytes(E));
+  sb.claims = carve<int>(cur, kClaimBytes);
+  int32_t* tile_prefix = sb.tile_prefix;
+  int32_t* pad_indptr = sb.pad_indptr;
+  int32_t* pair_prefix = sb.pair_prefix;
   uint16_t* dy_perm = gather ? nullptr : carve<uint16_t>(cur, static_cast<size_t>(R) * H * 2);
   uint16_t* dgu = carve<uint16_t>(cur, static_cast<size_t>(Rp) * 2 * I * 2 * 2);
   uint16_t* dx_perm = carve<uint16_t>(cur, static_cast<size_t>(R) * H * 2);
@@ -454,6 +464,8 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
   a.m_indptr = m_indptr;
   a.tile_prefix = tile_prefix;
   a.pair_prefix = pair_prefix;
+  a.sched_order = sb.order;
+  a.claims = sb.claims;
   a.w_gate_up = static_cast<const uint16_t*>(w_gate_up);
   a.w_down = static_cast<const uint16_t*>(w_down);
   a.x_perm = static_cast<const uint16_t*>(x_perm);
@@ -481,7 +493,7 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
   a.nin = act == LIGER_MOE_ACT_RELU2 ? I : 2 * I;  // ReLU²: one up weight, one factor, da [.., I]
 
   if (R > 0) {
-    if (int rc = launch_tile_schedule(m_indptr, E, R, tile_prefix, pad_indptr, dev, s, pair_prefix)) return rc;
+    if (int rc = launch_tile_schedule(m_indptr, E, R, sb, dev, s)) return rc;
     if (!gather) {  // dy_perm[r] = dY[token of r]: the dH and dW_down GEMMs read it as dense tiles
       if (int rc = launch_gather_rows(static_cast<const uint16_t*>(dy), row_to_slot, nullptr, R, H, k, dy_perm, dev, s))
         return rc;

@@ -58,7 +58,13 @@ constexpr uint32_t kTmemCols = 2 * BN;
 // feeds TMA bulk stores, so output rows leave the SM as whole lines.
 constexpr int STG_BYTES = 32 * 128;
 constexpr int STG_PER_WARP = 1;
-constexpr int kBarrierBytes = 256;
+constexpr int kBarrierBytes = 768;  // barriers, the tile ring, and (at kZeroOffset) a zero row for zero tiles
+constexpr int kZeroOffset = 512;
+constexpr int kZeroBytes = 256;     // one warp row of a zero tile: BN / 2 bf16 columns
+// Dynamic tile order: slots of the ring that passes claimed tiles from the producer to the other
+// warps, and the index of its first barrier in the barrier area (after the pipeline barriers).
+constexpr int kSchedSlots = 8;
+constexpr int kSchedBarIndex = 24;
 constexpr int kDhBoxBytes = 32 * 32;            // dH epilogue: 32 rows x 16 bf16 columns
 constexpr int kDhSetBytes = 6 * kDhBoxBytes;    // six output boxes per 16 columns
 
@@ -134,6 +140,13 @@ struct Params {
   int pad_a, pad_b;           // A / B rows are padded rows (RowsM: A only)
   const int32_t* row_slot;  // gathered operand: row_to_slot [R]; token of row r = row_slot[r] / topk
   int topk;
+  // Dynamic tile order of the weight-gradient GEMMs (claims != NULL): when the schedule found the
+  // load skewed (*sched_skewed != 0), the tiles are queued expert by expert with the experts
+  // sorted by rows, most first (sched_order), and each CTA's producer claims the next position
+  // through one counter (zeroed by the schedule kernel).  Otherwise the static order.
+  const int32_t* sched_order;   // [E]
+  const int* sched_skewed;
+  int* claims;
   // Logits: fp32 output [R, N_out] (row stride ld_out), optional bias [N_out]; out_tma: 32-column
   // chunks leave through TMA boxes (N_out a multiple of 32), else by masked direct stores
   float* out_f32;
@@ -153,30 +166,62 @@ struct Tile {
   int kb_count;  // K blocks
 };
 
-template <Sched S>
-__device__ __forceinline__ Tile decode_tile(int t, const Params& p) {
+// RowsM tile of expert e: its local M tile lm (128 rows) and N tile nt.
+__device__ __forceinline__ Tile rows_m_tile(int e, int lm, int nt, const Params& p) {
   Tile tl;
+  tl.e = e;
+  tl.nt = nt;
+  const int end = __ldg(p.m_indptr + e + 1);
+  const int start = __ldg(p.m_indptr + e);
+  tl.m0 = start + lm * BM;
+  tl.rows = min(BM, end - tl.m0);
+  tl.row0 = 0;
+  tl.am0 = p.pad_indptr != nullptr ? __ldg(p.pad_indptr + e) + (tl.m0 - start) : tl.m0;
+  tl.prow0 = 0;
+  tl.kb_count = p.num_kb;
+  return tl;
+}
+
+// RowsK tile r (of m_tiles * n_tiles) of expert e, M blocks fastest: neighbouring tiles share the
+// expert and the N block, so they read the same B tile (through L2).
+__device__ __forceinline__ Tile rows_k_tile(int e, int r, const Params& p) {
+  Tile tl;
+  tl.e = e;
+  tl.nt = r / p.m_tiles;
+  const int mt = r - tl.nt * p.m_tiles;
+  tl.m0 = mt * BM;
+  tl.row0 = __ldg(p.m_indptr + e);
+  tl.rows = __ldg(p.m_indptr + e + 1) - tl.row0;
+  tl.am0 = tl.m0;
+  tl.prow0 = p.pad_indptr != nullptr ? __ldg(p.pad_indptr + e) : tl.row0;
+  tl.kb_count = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
+  return tl;
+}
+
+// Largest i in [0, n) with prefix[i] <= v (prefix non-decreasing, prefix[0] = 0 <= v).
+__device__ __forceinline__ int prefix_search(const int32_t* prefix, int n, int v) {
+  int lo = 0, hi = n;  // prefix[lo] <= v < prefix[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(prefix + mid) <= v)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+// Tile t of the launch, experts in id order; RowsK in the dynamic order (dyn): t is a queue
+// position and the experts are taken in the sorted order.
+template <Sched S>
+__device__ __forceinline__ Tile decode_tile(int t, const Params& p, bool dyn = false) {
   if constexpr (S == Sched::RowsM) {
     const int mt = t / p.n_tiles;
-    tl.nt = t - mt * p.n_tiles;
-    int lo = 0, hi = p.E;  // tile_prefix[lo] <= mt < tile_prefix[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldg(p.tile_prefix + mid) <= mt)
-        lo = mid;
-      else
-        hi = mid;
-    }
-    tl.e = lo;
-    const int end = __ldg(p.m_indptr + lo + 1);
-    const int start = __ldg(p.m_indptr + lo);
-    tl.m0 = start + (mt - __ldg(p.tile_prefix + lo)) * BM;
-    tl.rows = min(BM, end - tl.m0);
-    tl.row0 = 0;
-    tl.am0 = p.pad_indptr != nullptr ? __ldg(p.pad_indptr + lo) + (tl.m0 - start) : tl.m0;
-    tl.prow0 = 0;
-    tl.kb_count = p.num_kb;
+    const int nt = t - mt * p.n_tiles;
+    const int i = prefix_search(p.tile_prefix, p.E, mt);
+    return rows_m_tile(i, mt - __ldg(p.tile_prefix + i), nt, p);
   } else if constexpr (S == Sched::Dense) {
+    Tile tl;
     const int mt = t / p.n_tiles;
     tl.nt = t - mt * p.n_tiles;
     tl.e = 0;
@@ -186,23 +231,20 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p) {
     tl.am0 = tl.m0;
     tl.prow0 = 0;
     tl.kb_count = p.num_kb;
+    return tl;
   } else {
-    // M blocks fastest: neighbouring tiles share the expert and the N block, so they read the
-    // same B tile (through L2)
     const int per_e = p.m_tiles * p.n_tiles;
-    tl.e = t / per_e;
-    const int r = t - tl.e * per_e;
-    tl.nt = r / p.m_tiles;
-    const int mt = r - tl.nt * p.m_tiles;
-    tl.m0 = mt * BM;
-    tl.row0 = __ldg(p.m_indptr + tl.e);
-    tl.rows = __ldg(p.m_indptr + tl.e + 1) - tl.row0;
-    tl.am0 = tl.m0;
-    tl.prow0 = p.pad_indptr != nullptr ? __ldg(p.pad_indptr + tl.e) : tl.row0;
-    tl.kb_count = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
+    const int i = t / per_e;
+    const int e = dyn ? __ldg(p.sched_order + i) : i;
+    return rows_k_tile(e, t - i * per_e, p);
   }
-  return tl;
 }
+
+// The next queue position of a dynamic order: one atomic on the launch's counter; -1 once the
+// queue is empty.  claim_issue and claim_position are split so that the atomic's latency passes
+// while the producer loads the current tile.
+__device__ __forceinline__ int claim_issue(const Params& p) { return atomicAdd(p.claims, 1); }
+__device__ __forceinline__ int claim_position(int claimed, int total) { return claimed < total ? claimed : -1; }
 
 // Tile of a 2-SM pair.  RowsM: tile_prefix counts 256-row blocks per expert; CTA `rank` of the
 // pair owns rows [m0, m0 + 128) of the block (none when the expert ends before them).  RowsK:
@@ -658,16 +700,18 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
   }
 }
 
-// RowsK tile of an expert with no rows: the gradient block is exactly zero.
+// RowsK tile of an expert with no rows: the gradient block is exactly zero.  Each lane copies its
+// output row's part of the tile (128 columns, 256 bytes) from a zero row in shared memory that no
+// one ever writes again, so zero tiles need no staging and no wait between them.
 __device__ __forceinline__ void store_zero_tile(const Tile& tl, int sub, int colhalf, int lane, const Params& p,
-                                                const CUtensorMap* tmC0, Stager& st) {
-  uint32_t w[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) w[i] = 0u;
-  for (int q = 2 * colhalf; q < 2 * colhalf + 2; ++q) {
-    const int col = tl.nt * BN + q * 64;
-    if (col >= p.N_out) break;
-    emit_box<3>(tmC0, st, lane, w, col, tl.m0 + sub * 32, tl.e);
+                                                uint32_t zero_row) {
+  const int row = tl.m0 + sub * 32 + lane;
+  const int c0 = tl.nt * BN + colhalf * (BN / 2);
+  const int n = min(BN / 2, p.N_out - c0);  // a multiple of 64 (N_out is)
+  if (row < p.M_out && n > 0) {
+    bulk_store_s2g(p.out + tl.e * p.out_expert_stride + static_cast<long long>(row) * p.ld_out + c0, zero_row,
+                   static_cast<uint32_t>(n) * 2u);
+    bulk_commit_group();
   }
 }
 
@@ -831,11 +875,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   // pairs walk the tiles together: tile t of cluster c is t = c, c + clusters, ...
   const int tile0 = kPair ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
   const int tstride = kPair ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
+  // dynamic order: weight gradients of one-CTA tiles with tiled operands, when the load is skewed
+  // (every role reads the same flag, written by the schedule kernel before this launch)
+  bool dyn = false;
   auto decode = [&](int t) -> Tile {
     if constexpr (kPair)
       return decode_tile_pair<S>(t, p, rank);
     else
-      return decode_tile<S>(t, p);
+      return decode_tile<S>(t, p, dyn);
   };
   static_assert(SPLIT == 0 || (S == Sched::RowsK && A_MN && B_MN), "hi/lo operands only in the dW GEMMs");
   static_assert(G == Gather::None || (S == Sched::RowsM ? (G == Gather::A && !A_MN)
@@ -849,6 +896,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + L::kBarOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // dynamic tile order: a ring of claimed tile positions from the producer to the MMA and epilogue
+  // warps (full: written; empty: read by all of them)
+  static_assert(2 * 6 + 5 + 1 <= kSchedBarIndex && (kSchedBarIndex + 2 * kSchedSlots) * 8 + 4 * kSchedSlots <= kBarrierBytes,
+                "barrier area layout");
+  volatile int* sched_ring = reinterpret_cast<volatile int*>(bars + kSchedBarIndex + 2 * kSchedSlots);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -857,6 +909,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tfull0 = smem_u32(bars + 2 * STAGES);
   const uint32_t tempty0 = smem_u32(bars + 2 * STAGES + 2);
   const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
+  const uint32_t sfull0 = smem_u32(bars + kSchedBarIndex);
+  const uint32_t sempty0 = smem_u32(bars + kSchedBarIndex + kSchedSlots);
+  const uint32_t zero_row = smem_u32(base_ptr + L::kBarOffset + kZeroOffset);  // kZeroBytes of zeros
+  static_assert(kSchedBarIndex * 8 + 2 * kSchedSlots * 8 + 4 * kSchedSlots <= kZeroOffset &&
+                    kZeroOffset + kZeroBytes <= kBarrierBytes,
+                "barrier area: barriers, tile ring, zero row");
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -868,8 +926,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty0 + 8 * a, kPair ? 2 * kEpiWarps : kEpiWarps);  // pair: both CTAs' epilogue warps
     }
     mbar_init(drain, 1);
+    for (int q = 0; q < kSchedSlots; ++q) {
+      mbar_init(sfull0 + 8 * q, 1);
+      mbar_init(sempty0 + 8 * q, 1 + kEpiWarps);  // the MMA warp and every epilogue warp
+    }
     *abort_flag = 0;
     fence_mbar_init();
+  }
+  if (threadIdx.x < kZeroBytes / 16) {  // the zero row that zero tiles copy out (async proxy reads it)
+    st_shared_v4(zero_row + 16 * threadIdx.x, make_uint4(0u, 0u, 0u, 0u));
+    fence_proxy_async_smem();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
@@ -896,6 +962,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // barriers, TMEM and descriptors are ready: from here on the kernel reads what earlier kernels wrote
   griddep_wait();
   griddep_launch_dependents();
+  if constexpr (S == Sched::RowsK && !kPair && G == Gather::None)
+    dyn = p.claims != nullptr && __ldg(p.sched_skewed) != 0;
 
   int total;
   if constexpr (S == Sched::RowsM)
@@ -905,6 +973,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   else
     total = p.E * (kPair ? p.m_tiles / 2 : p.m_tiles) * p.n_tiles;  // pair: M blocks two at a time
 
+  // The next tile of the MMA warp or an epilogue warp: the static sequence tile0, tile0 + tstride,
+  // ..., or the next entry of the producer's ring (dynamic order).  false: the wait gave up.
+  // (slot, sphase: this warp's position in the ring; the producer writes through its own copy.)
+  int slot = 0;
+  uint32_t sphase = 0;
+  auto next_tile = [&](int& t, bool first) -> bool {
+    if (!dyn) {
+      t = first ? tile0 : t + tstride;
+      return true;
+    }
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(sfull0 + 8 * slot, sphase, abort_flag))) return false;
+    t = sched_ring[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sempty0 + 8 * slot);
+    if (++slot == kSchedSlots) {
+      slot = 0;
+      sphase ^= 1u;
+    }
+    return true;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if constexpr (G == Gather::None) {
@@ -912,7 +1001,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         bool failed = false;
-        for (int t = tile0; t < total && !failed; t += tstride) {
+        // dynamic order: every claim is published to the ring (-1 last) before its loads
+        int t = dyn ? claim_position(claim_issue(p), total) : tile0;
+        for (;;) {
+          if (dyn) {
+            if (!mbar_wait(sempty0 + 8 * slot, sphase ^ 1u, abort_flag)) {
+              raise_abort(p.err, abort_flag);
+              failed = true;
+              break;
+            }
+            sched_ring[slot] = t;
+            mbar_arrive(sfull0 + 8 * slot);
+            if (++slot == kSchedSlots) {
+              slot = 0;
+              sphase ^= 1u;
+            }
+          }
+          if (t < 0 || t >= total) break;
+          const int next_claim = dyn ? claim_issue(p) : 0;
           const Tile tl = decode(t);
           for (int kb = 0; kb < tl.kb_count; ++kb) {
             if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
@@ -936,6 +1042,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               phase ^= 1u;
             }
           }
+          if (failed) break;
+          t = dyn ? claim_position(next_claim, total) : t + tstride;
         }
         if constexpr (kPair) {
           // the even CTA has released the last fill of each stage: no release from the peer is
@@ -1030,7 +1138,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool failed = false;
-    for (int t = tile0; leader && t < total && !failed; t += tstride) {
+    int t = 0;
+    for (bool first = true; leader && !failed; first = false) {
+      if (!next_tile(t, first)) {
+        raise_abort(p.err, abort_flag);
+        break;
+      }
+      if (t < 0 || t >= total) break;
       const Tile tl = decode(t);
       if (tl.kb_count == 0) continue;
       // every lane waits (so every lane acquires the phase); the outcome is made warp-uniform.
@@ -1129,13 +1243,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     Stager st{sbase + L::kStgOffset + static_cast<uint32_t>(ew * L::kStgWarpBytes), 0};
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = tile0; t < total; t += tstride) {
+    int t = 0;
+    for (bool first = true;; first = false) {
+      if (!next_tile(t, first)) {
+        raise_abort(p.err, abort_flag);
+        break;
+      }
+      if (t < 0 || t >= total) break;
       const Tile tl = decode(t);
       // the tile's epilogue operands (DH) start moving into L2 now, a tile's MMA time ahead of use
       // when the MMAs lead, and at least ahead of the later column chunks when the epilogue does
       prefetch_epilogue_operands<S, EP>(tl, row_local, colhalf, p);
       if (tl.kb_count == 0) {
-        if constexpr (S == Sched::RowsK) store_zero_tile(tl, sub, colhalf, lane, p, &tmC0, st);
+        if constexpr (S == Sched::RowsK) store_zero_tile(tl, sub, colhalf, lane, p, zero_row);
         continue;
       }
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag))) {
@@ -1156,8 +1276,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
-    // outputs are in global memory (and the staging buffers free) before the CTA exits
-    if (lane == 0) bulk_wait_group<0>();
+    // outputs are in global memory (and the staging buffers free) before the CTA exits; every lane
+    // waits for its own bulk copies (zero tiles)
+    bulk_wait_group<0>();
     __syncwarp();
   }
 
@@ -1213,24 +1334,35 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* s_warp, int
 __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __restrict__ m_indptr, int E,
                                                              long long R, int32_t* __restrict__ tile_prefix,
                                                              int32_t* __restrict__ pad_indptr,
-                                                             int32_t* __restrict__ pair_prefix, int* err) {
+                                                             int32_t* __restrict__ pair_prefix,
+                                                             int32_t* __restrict__ order, int* __restrict__ claims,
+                                                             int* err) {
   __shared__ int s_warp[32];
   __shared__ int s_bad;
+  __shared__ int s_max;
   __shared__ int s_total[3];
+  __shared__ int s_rows[1024];
   griddep_wait();
   griddep_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) s_bad = (m_indptr[0] != 0 || static_cast<long long>(m_indptr[E]) != R) ? 1 : 0;
+  if (tid == 0) {
+    s_bad = (m_indptr[0] != 0 || static_cast<long long>(m_indptr[E]) != R) ? 1 : 0;
+    s_max = 0;
+  }
+  if (claims != nullptr && tid < kClaimSlots) claims[tid] = 0;
   __syncthreads();
-  int tiles = 0, padded = 0, pairs = 0;
+  int rows = 0;
   if (tid < E) {
     const int a = m_indptr[tid], b = m_indptr[tid + 1];
     if (b < a) atomicOr(&s_bad, 1);
-    tiles = (b > a) ? (b - a + BM - 1) / BM : 0;
-    padded = (b > a) ? ((b - a + 15) & ~15) : 0;
-    pairs = (b > a) ? (b - a + 2 * BM - 1) / (2 * BM) : 0;
+    rows = max(b - a, 0);
+    atomicMax(&s_max, rows);
   }
-  const int t_excl = block_exclusive_scan_1024(tiles, s_warp, lane, warp, &s_total[0]);
+  s_rows[tid] = rows;
+  const int tiles = (rows + BM - 1) / BM;
+  const int padded = (rows + 15) & ~15;
+  const int pairs = (rows + 2 * BM - 1) / (2 * BM);
+  const int t_excl = block_exclusive_scan_1024(tiles, s_warp, lane, warp, &s_total[0]);  // (syncs s_rows too)
   const int p_excl = pad_indptr != nullptr ? block_exclusive_scan_1024(padded, s_warp, lane, warp, &s_total[1]) : 0;
   const int q_excl = pair_prefix != nullptr ? block_exclusive_scan_1024(pairs, s_warp, lane, warp, &s_total[2]) : 0;
   const bool bad = s_bad != 0;
@@ -1243,6 +1375,23 @@ __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __re
     tile_prefix[E] = bad ? 0 : s_total[0];
     if (pad_indptr != nullptr) pad_indptr[E] = bad ? 0 : s_total[1];
     if (pair_prefix != nullptr) pair_prefix[E] = bad ? 0 : s_total[2];
+  }
+  if (order != nullptr) {
+    // experts by rows, most first; equal rows in id order (the rank of expert tid)
+    if (tid < E) {
+      int rank = 0;
+      for (int e = 0; e < E; ++e) {
+        const int r = s_rows[e];
+        rank += (r > rows || (r == rows && e < tid)) ? 1 : 0;
+      }
+      order[rank] = tid;
+    }
+    // skewed load: the largest expert holds at least 512 rows and 4x the mean (the weight-gradient
+    // GEMMs then take their tiles in that order, heaviest first)
+    if (tid == 0 && claims != nullptr) {
+      const long long mean = (R + E - 1) / E;
+      claims[kClaimSlots] = (!bad && s_max >= 512 && s_max >= 4 * mean) ? 1 : 0;
+    }
   }
   if (bad && tid == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_INDPTR);
 }
@@ -1377,6 +1526,15 @@ Params base_params(const int32_t* m_indptr, const int32_t* tile_prefix, int E, i
   return p;
 }
 
+// Weight gradients in the dynamic order when the schedule finds the load skewed (claim counter
+// `slot` of the schedule's counters; the flag follows the counters).
+void set_dynamic(Params& p, const int32_t* order, int* claims, int slot) {
+  if (order == nullptr || claims == nullptr) return;
+  p.sched_order = order;
+  p.claims = claims + slot;
+  p.sched_skewed = claims + kClaimSlots;
+}
+
 // Token-major bf16 matrix [rows, cols] as a gather source: box 64 columns x 1 row.
 int make_gather_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows) {
   return make_tmap(m, ptr, cols, rows, 64, 1);
@@ -1410,12 +1568,12 @@ int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
 size_t schedule_bytes(int E) { return align_up(sizeof(int32_t) * (E + 1), 256); }
 
-int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, int32_t* tile_prefix, int32_t* pad_indptr,
-                         const DeviceInfo& dev, cudaStream_t s, int32_t* pair_prefix) {
+int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, const ScheduleBufs& b, const DeviceInfo& dev,
+                         cudaStream_t s) {
   {
     KernelScope trace("tile_schedule", s);
     if (launch_kernel(tile_schedule_kernel, dim3(1), dim3(1024), 0, s, "tile_schedule", 1, m_indptr, E, R,
-                      tile_prefix, pad_indptr, pair_prefix, dev.err_flag) != cudaSuccess)
+                      b.tile_prefix, b.pad_indptr, b.pair_prefix, b.order, b.claims, dev.err_flag) != cudaSuccess)
       return LIGER_MOE_ERR_LAUNCH;
   }
   return check_launch("tile_schedule");
@@ -1647,6 +1805,7 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.b_split_rows = 0;
   p.pad_a = 1;  // dgu rows: padded row space (zero rows past each expert)
   p.pad_b = 0;
+  if (!empty) set_dynamic(p, a.sched_order, a.claims, kClaimDwGateUp);  // R = 0: no schedule
   p.M_out = a.nin;
   p.N_out = a.H;
   p.out = a.dw_gate_up;
@@ -1685,6 +1844,7 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.b_split_rows = static_cast<int>(a.R_pad);
   p.pad_a = 0;
   p.pad_b = 1;  // w h rows: padded row space
+  if (!empty) set_dynamic(p, a.sched_order, a.claims, kClaimDwDown);
   p.M_out = a.H;
   p.N_out = a.I;
   p.out = a.dw_down;

@@ -70,12 +70,27 @@ int launch_bounded_wait_selftest(uint64_t limit_ns, const DeviceInfo& dev, cudaS
 // Router projection logits[T, E] = x Wr^T (+ bias), fp32, as one dense tcgen05 GEMM.
 int launch_router_logits(const uint16_t* x, const uint16_t* w_router, const float* bias, int T, int H, int E,
                          float* logits, const DeviceInfo& dev, cudaStream_t s);
-// Tile schedule: tile_prefix[e] = sum over e' < e of ceil(rows_e' / 128); [E] = total.
-size_t schedule_bytes(int E);
-// With pad_indptr != NULL it also receives the padded row prefix (row counts rounded up to 16);
-// with pair_prefix != NULL the prefix of 256-row blocks (the 2-SM pair GEMMs' tiles).
-int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, int32_t* tile_prefix, int32_t* pad_indptr,
-                         const DeviceInfo& dev, cudaStream_t s, int32_t* pair_prefix = nullptr);
+// The device-built schedule of one layer call, carved from the caller's workspace:
+//   tile_prefix[e]   sum over e' < e of ceil(rows_e' / 128) ([E] = total M tiles)
+//   pad_indptr[e]    the padded row prefix (row counts rounded up to 16), or nullptr
+//   pair_prefix[e]   the prefix of 256-row blocks (the 2-SM pair GEMMs' tiles), or nullptr
+//   order[i]         experts by rows, most first, equal rows in id order, or nullptr
+//   claims           kClaimSlots claim counters, zeroed by the schedule kernel (one per GEMM launch
+//                    that may take its tiles in that order), then the skew flag; or nullptr
+struct ScheduleBufs {
+  int32_t* tile_prefix = nullptr;
+  int32_t* pad_indptr = nullptr;
+  int32_t* pair_prefix = nullptr;
+  int32_t* order = nullptr;
+  int* claims = nullptr;
+};
+constexpr int kClaimSlots = 8;
+// Claim counters of the launches that may use the dynamic order: the weight-gradient GEMMs.
+enum ClaimSlot : int { kClaimDwGateUp = 0, kClaimDwDown = 1 };
+size_t schedule_bytes(int E);                  // one [E+1] int32 array, 256-byte aligned
+constexpr size_t kClaimBytes = 256;            // kClaimSlots counters and the skew flag, 256-byte aligned
+int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, const ScheduleBufs& b, const DeviceInfo& dev,
+                         cudaStream_t s);
 
 struct FwdGemmArgs {
   const uint16_t* x_perm;       // [R, H]; used when x is NULL
@@ -105,6 +120,8 @@ struct BwdGemmArgs {
   const int32_t* m_indptr;
   const int32_t* tile_prefix;
   const int32_t* pair_prefix = nullptr;  // 256-row block prefix: the pair GEMMs run when set
+  const int32_t* sched_order = nullptr;   // experts by rows (the weight gradients' dynamic order)
+  int* claims = nullptr;                  // the schedule's claim counters and skew flag
   const uint16_t* w_gate_up;
   const uint16_t* w_down;
   const uint16_t* x_perm;   // [R, H]; used when x is NULL

@@ -124,6 +124,13 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int
                "r"(src), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// Plain bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from shared to
+// global memory (bulk-group completion).
+__device__ __forceinline__ void bulk_store_s2g(void* gdst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
+               "r"(src), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N committed bulk groups of this thread still read shared memory.
 template <int N>
