@@ -105,7 +105,7 @@ cudaEvent_t trace_event() {
 }  // namespace
 
 KernelScope::KernelScope(const char* name, cudaStream_t s) : name_(name), stream_(s) {
-  if (!g_trace_on.load(std::memory_order_relaxed)) return;
+  if (name == nullptr || !g_trace_on.load(std::memory_order_relaxed)) return;  // nullptr: not traced
   std::lock_guard<std::mutex> lock(g_trace_mu);
   start_ = trace_event();
   if (start_ != nullptr) trace_record(start_, stream_);
@@ -183,8 +183,9 @@ long long padded_rows(long long R, int E) { return R + 15LL * E; }
 
 size_t bwd_workspace_bytes(long long R, int H, int I, int E, bool recompute_gu, bool gather) {
   const long long Rp = padded_rows(R, E);
-  // tile prefix, padded row prefix, 256-row pair block prefix, expert order, claim counters
-  size_t b = 4 * schedule_bytes(E) + kClaimBytes;
+  // tile prefix, padded row prefix, 256-row pair block prefix, light tile and heavy pair prefixes,
+  // expert order, claim counters
+  size_t b = 6 * schedule_bytes(E) + kClaimBytes;
   if (!gather) b += align_up(static_cast<size_t>(R) * H * 2, 256);  // dy_perm
   b += align_up(static_cast<size_t>(Rp) * 2 * I * 2 * 2, 256);        // dgu (hi, lo), padded rows
   b += align_up(static_cast<size_t>(R) * H * 2, 256);                 // dx_perm
@@ -274,7 +275,8 @@ int grouped_swiglu_fwd_impl(const void* x_perm, const void* x, const int32_t* ro
   if (!aligned16(a_src) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(h_perm) ||
       !aligned16(gu_perm) || !aligned16(y_perm))
     return LIGER_MOE_ERR_MISALIGNED;
-  const size_t need = 2 * schedule_bytes(E);  // tile prefixes of 128-row tiles and of 256-row pair tiles
+  // tile prefixes of 128-row tiles and of 256-row pair tiles, and the two of the heavy / light split
+  const size_t need = 4 * schedule_bytes(E);
   if (workspace == nullptr) {
     *workspace_bytes = need;
     return LIGER_MOE_OK;
@@ -289,6 +291,12 @@ int grouped_swiglu_fwd_impl(const void* x_perm, const void* x, const int32_t* ro
   ScheduleBufs sb;
   sb.tile_prefix = carve<int32_t>(cur, schedule_bytes(E));
   sb.pair_prefix = carve<int32_t>(cur, schedule_bytes(E));
+  int32_t* light = carve<int32_t>(cur, schedule_bytes(E));
+  int32_t* heavy = carve<int32_t>(cur, schedule_bytes(E));
+  if (split_schedule(R, E)) {  // the heavy / light split may run: the schedule builds its prefixes
+    sb.light_prefix = light;
+    sb.heavy_pair_prefix = heavy;
+  }
   if (int rc = launch_tile_schedule(m_indptr, E, R, sb, dev, s)) return rc;
   int32_t* tile_prefix = sb.tile_prefix;
   int32_t* pair_prefix = sb.pair_prefix;
@@ -301,6 +309,8 @@ int grouped_swiglu_fwd_impl(const void* x_perm, const void* x, const int32_t* ro
   a.m_indptr = m_indptr;
   a.tile_prefix = tile_prefix;
   a.pair_prefix = pair_prefix;
+  a.light_prefix = sb.light_prefix;
+  a.heavy_pair_prefix = sb.heavy_pair_prefix;
   a.w_gate_up = static_cast<const uint16_t*>(w_gate_up);
   a.w_down = static_cast<const uint16_t*>(w_down);
   a.w_perm = w_perm;
@@ -448,6 +458,12 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
   sb.tile_prefix = carve<int32_t>(cur, schedule_bytes(E));
   sb.pad_indptr = carve<int32_t>(cur, schedule_bytes(E));
   sb.pair_prefix = carve<int32_t>(cur, schedule_bytes(E));
+  int32_t* light = carve<int32_t>(cur, schedule_bytes(E));
+  int32_t* heavy = carve<int32_t>(cur, schedule_bytes(E));
+  if (split_schedule(R, E)) {
+    sb.light_prefix = light;
+    sb.heavy_pair_prefix = heavy;
+  }
   sb.order = carve<int32_t>(cur, schedule_bytes(E));
   sb.claims = carve<int>(cur, kClaimBytes);
   int32_t* tile_prefix = sb.tile_prefix;
@@ -464,6 +480,8 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
   a.m_indptr = m_indptr;
   a.tile_prefix = tile_prefix;
   a.pair_prefix = pair_prefix;
+  a.light_prefix = sb.light_prefix;
+  a.heavy_pair_prefix = sb.heavy_pair_prefix;
   a.sched_order = sb.order;
   a.claims = sb.claims;
   a.w_gate_up = static_cast<const uint16_t*>(w_gate_up);

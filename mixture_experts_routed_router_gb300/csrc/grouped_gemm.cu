@@ -61,6 +61,10 @@ constexpr int STG_PER_WARP = 1;
 constexpr int kBarrierBytes = 768;  // barriers, the tile ring, and (at kZeroOffset) a zero row for zero tiles
 constexpr int kZeroOffset = 512;
 constexpr int kZeroBytes = 256;     // one warp row of a zero tile: BN / 2 bf16 columns
+// Per-expert 2-SM pair thresholds (rows of one expert): the forward and dX GEMMs (256-row pair tiles)
+// and the two weight-gradient GEMMs.  An expert with fewer rows runs one CTA per tile.
+constexpr int kPairRowsM = 512, kPairRowsDwGu = 192, kPairRowsDwD = 128;  // dW_gate_up: on the mean rows
+
 // Dynamic tile order: slots of the ring that passes claimed tiles from the producer to the other
 // warps, and the index of its first barrier in the barrier area (after the pipeline barriers).
 constexpr int kSchedSlots = 8;
@@ -147,6 +151,11 @@ struct Params {
   const int32_t* sched_order;   // [E]
   const int* sched_skewed;
   int* claims;
+  // Heavy / light split of dW_down (split_part != 0): the experts of the sorted
+  // order are split at *split_heavy (the count with at least the pair threshold's rows); part 1
+  // takes the first *split_heavy of them (2-SM pairs), part 2 the rest (one CTA per tile).
+  const int* split_heavy;
+  int split_part;
   // Logits: fp32 output [R, N_out] (row stride ld_out), optional bias [N_out]; out_tma: 32-column
   // chunks leave through TMA boxes (N_out a multiple of 32), else by masked direct stores
   float* out_f32;
@@ -235,7 +244,9 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, bool dyn = f
   } else {
     const int per_e = p.m_tiles * p.n_tiles;
     const int i = t / per_e;
-    const int e = dyn ? __ldg(p.sched_order + i) : i;
+    // the sorted order from the split's first expert (dynamic order or a heavy / light part)
+    const int base = p.split_part == 2 ? __ldg(p.split_heavy) : 0;
+    const int e = (dyn || p.split_part != 0) ? __ldg(p.sched_order + base + i) : i;
     return rows_k_tile(e, t - i * per_e, p);
   }
 }
@@ -257,8 +268,9 @@ __device__ __forceinline__ Tile decode_tile_pair(int t, const Params& p, uint32_
     // blocks fastest, so neighbouring pairs share the expert and the N block
     const int mpt = p.m_tiles / 2;
     const int per_e = mpt * p.n_tiles;
-    tl.e = t / per_e;
-    const int r = t - tl.e * per_e;
+    const int i = t / per_e;
+    tl.e = p.split_part != 0 ? __ldg(p.sched_order + i) : i;  // the heavy part: the first sorted experts
+    const int r = t - i * per_e;
     tl.nt = r / mpt;
     const int mp = r - tl.nt * mpt;
     tl.m0 = mp * (2 * BM) + static_cast<int>(rank) * BM;
@@ -971,7 +983,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   else if constexpr (S == Sched::Dense)
     total = static_cast<int>((p.R + BM - 1) / BM) * p.n_tiles;
   else
-    total = p.E * (kPair ? p.m_tiles / 2 : p.m_tiles) * p.n_tiles;  // pair: M blocks two at a time
+    total = (p.split_part == 0 ? p.E : (p.split_part == 1 ? __ldg(p.split_heavy) : p.E - __ldg(p.split_heavy))) *
+            (kPair ? p.m_tiles / 2 : p.m_tiles) * p.n_tiles;  // experts of the part x tiles (pair: M blocks two at a time)
 
   // The next tile of the MMA warp or an epilogue warp: the static sequence tile0, tile0 + tstride,
   // ..., or the next entry of the producer's ring (dynamic order).  false: the wait gave up.
@@ -1332,15 +1345,12 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* s_warp, int
 }
 
 __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __restrict__ m_indptr, int E,
-                                                             long long R, int32_t* __restrict__ tile_prefix,
-                                                             int32_t* __restrict__ pad_indptr,
-                                                             int32_t* __restrict__ pair_prefix,
-                                                             int32_t* __restrict__ order, int* __restrict__ claims,
-                                                             int* err) {
+                                                             long long R, ScheduleBufs sb, int* err) {
   __shared__ int s_warp[32];
   __shared__ int s_bad;
   __shared__ int s_max;
-  __shared__ int s_total[3];
+  __shared__ int s_heavy;
+  __shared__ int s_total[5];
   __shared__ int s_rows[1024];
   griddep_wait();
   griddep_launch_dependents();
@@ -1348,8 +1358,9 @@ __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __re
   if (tid == 0) {
     s_bad = (m_indptr[0] != 0 || static_cast<long long>(m_indptr[E]) != R) ? 1 : 0;
     s_max = 0;
+    s_heavy = 0;
   }
-  if (claims != nullptr && tid < kClaimSlots) claims[tid] = 0;
+  if (sb.claims != nullptr && tid < kClaimSlots) sb.claims[tid] = 0;
   __syncthreads();
   int rows = 0;
   if (tid < E) {
@@ -1357,26 +1368,41 @@ __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __re
     if (b < a) atomicOr(&s_bad, 1);
     rows = max(b - a, 0);
     atomicMax(&s_max, rows);
+    if (rows >= kPairRowsDwD) atomicAdd(&s_heavy, 1);
   }
   s_rows[tid] = rows;
+  const bool heavy_m = rows >= kPairRowsM;
   const int tiles = (rows + BM - 1) / BM;
   const int padded = (rows + 15) & ~15;
   const int pairs = (rows + 2 * BM - 1) / (2 * BM);
   const int t_excl = block_exclusive_scan_1024(tiles, s_warp, lane, warp, &s_total[0]);  // (syncs s_rows too)
-  const int p_excl = pad_indptr != nullptr ? block_exclusive_scan_1024(padded, s_warp, lane, warp, &s_total[1]) : 0;
-  const int q_excl = pair_prefix != nullptr ? block_exclusive_scan_1024(pairs, s_warp, lane, warp, &s_total[2]) : 0;
+  const int p_excl = sb.pad_indptr != nullptr ? block_exclusive_scan_1024(padded, s_warp, lane, warp, &s_total[1]) : 0;
+  const int q_excl = sb.pair_prefix != nullptr ? block_exclusive_scan_1024(pairs, s_warp, lane, warp, &s_total[2]) : 0;
+  int l_excl = 0, h_excl = 0;
+  if (sb.light_prefix != nullptr) {
+    l_excl = block_exclusive_scan_1024(heavy_m ? 0 : tiles, s_warp, lane, warp, &s_total[3]);
+    h_excl = block_exclusive_scan_1024(heavy_m ? pairs : 0, s_warp, lane, warp, &s_total[4]);
+  }
   const bool bad = s_bad != 0;
   if (tid < E) {
-    tile_prefix[tid] = bad ? 0 : t_excl;
-    if (pad_indptr != nullptr) pad_indptr[tid] = bad ? 0 : p_excl;
-    if (pair_prefix != nullptr) pair_prefix[tid] = bad ? 0 : q_excl;
+    sb.tile_prefix[tid] = bad ? 0 : t_excl;
+    if (sb.pad_indptr != nullptr) sb.pad_indptr[tid] = bad ? 0 : p_excl;
+    if (sb.pair_prefix != nullptr) sb.pair_prefix[tid] = bad ? 0 : q_excl;
+    if (sb.light_prefix != nullptr) {
+      sb.light_prefix[tid] = bad ? 0 : l_excl;
+      sb.heavy_pair_prefix[tid] = bad ? 0 : h_excl;
+    }
   }
   if (tid == 0) {
-    tile_prefix[E] = bad ? 0 : s_total[0];
-    if (pad_indptr != nullptr) pad_indptr[E] = bad ? 0 : s_total[1];
-    if (pair_prefix != nullptr) pair_prefix[E] = bad ? 0 : s_total[2];
+    sb.tile_prefix[E] = bad ? 0 : s_total[0];
+    if (sb.pad_indptr != nullptr) sb.pad_indptr[E] = bad ? 0 : s_total[1];
+    if (sb.pair_prefix != nullptr) sb.pair_prefix[E] = bad ? 0 : s_total[2];
+    if (sb.light_prefix != nullptr) {
+      sb.light_prefix[E] = bad ? 0 : s_total[3];
+      sb.heavy_pair_prefix[E] = bad ? 0 : s_total[4];
+    }
   }
-  if (order != nullptr) {
+  if (sb.order != nullptr) {
     // experts by rows, most first; equal rows in id order (the rank of expert tid)
     if (tid < E) {
       int rank = 0;
@@ -1384,13 +1410,15 @@ __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __re
         const int r = s_rows[e];
         rank += (r > rows || (r == rows && e < tid)) ? 1 : 0;
       }
-      order[rank] = tid;
+      sb.order[rank] = tid;
     }
-    // skewed load: the largest expert holds at least 512 rows and 4x the mean (the weight-gradient
-    // GEMMs then take their tiles in that order, heaviest first)
-    if (tid == 0 && claims != nullptr) {
+    if (tid == 0 && sb.claims != nullptr) {
+      // skewed load: the largest expert holds at least 512 rows and 4x the mean (the one-CTA
+      // weight-gradient tiles are then claimed heaviest first)
       const long long mean = (R + E - 1) / E;
-      claims[kClaimSlots] = (!bad && s_max >= 512 && s_max >= 4 * mean) ? 1 : 0;
+      sb.claims[kClaimSlots] = (!bad && s_max >= 512 && s_max >= 4 * mean) ? 1 : 0;
+      // the experts at the head of that order with enough rows for the 2-SM pair dW_down
+      sb.claims[kClaimSlots + 1] = bad ? 0 : s_heavy;
     }
   }
   if (bad && tid == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_INDPTR);
@@ -1475,7 +1503,8 @@ int make_out_bf16_3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t ro
 template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT = 0, Gather G = Gather::None, int CL = 1,
           int PAIR = 0>
 int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc0, const CUtensorMap& tc1,
-                const Params& p, long long tiles, const DeviceInfo& dev, cudaStream_t s, const char* name) {
+                const Params& p, long long tiles, const DeviceInfo& dev, cudaStream_t s, const char* name,
+                bool traced = true) {
   auto kern = grouped_gemm_kernel<S, EP, A_MN, B_MN, SPLIT, G, CL, PAIR>;
   constexpr int kSmem = LayoutOf<EP, SPLIT, PAIR>::kSmemBytes;
   static std::once_flag once;
@@ -1511,7 +1540,7 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
     const long long groups = PAIR ? tiles : tiles / CL;  // pair: one tile per cluster
     grid = static_cast<int>(groups < max_clusters ? groups : max_clusters) * CL;
   }
-  KernelScope trace(name, s);
+  KernelScope trace(traced ? name : nullptr, s);  // untraced: one scope of the caller spans both parts of a split
   if (launch_kernel(kern, dim3(grid), dim3(kThreads), kSmem, s, name, CL, ta, tb, tc0, tc1, p) != cudaSuccess)
     return LIGER_MOE_ERR_LAUNCH;
   return check_launch(name);
@@ -1562,6 +1591,33 @@ bool use_pairs(const BwdGemmArgs& a) {
   return a.pair_prefix != nullptr && a.R >= 512LL * a.E && a.dy_perm != nullptr && a.nin == 2 * a.I;
 }
 
+// Heavy / light split: the experts with at least the pair threshold's rows run as 2-SM pairs and the
+// others one CTA per tile, in two launches over the schedule's filtered prefixes (forward and dX
+// GEMMs) or the two parts of the sorted expert order (dW_down).  Pairs halve the operand tiles each
+// SM streams through L2 for a heavy expert's rows; a light expert's rows would leave most of a
+// 256-row pair tile empty.  Taken for skewed batches: experts average fewer than kSplitMeanRows rows
+// (with more, every expert runs as pairs or a uniform load gains nothing from a second launch),
+// and the batch is large enough for one expert to reach the threshold (R rows in all, T per expert
+// at most).  Measured on GB300 (Zipf 4096/1024 workload, 160 rows per expert on average):
+// dW_down 1587-1608 -> 1397-1418 us, down 840-846 -> 809-816, dX 1545-1559 -> 1529-1545; on
+// uniform loads an empty second launch cost 3-10 us per GEMM.
+constexpr long long kSplitMeanRows = 192;
+constexpr long long kSplitMinRows = 8 * kPairRowsM;  // forward: R rows in the batch (T is not known)
+}  // namespace
+
+bool split_schedule(long long R, int E) { return R >= kSplitMinRows && R < kSplitMeanRows * E; }
+
+namespace {
+
+bool use_split(const FwdGemmArgs& a) {
+  return a.light_prefix != nullptr && !use_pairs(a) && a.x == nullptr && a.R >= kSplitMinRows &&
+         a.R < kSplitMeanRows * a.E;
+}
+bool use_split(const BwdGemmArgs& a) {
+  return a.light_prefix != nullptr && !use_pairs(a) && a.T >= kPairRowsM && a.dy_perm != nullptr &&
+         a.nin == 2 * a.I && a.R < kSplitMeanRows * a.E;
+}
+
 int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
 }  // namespace
@@ -1572,8 +1628,8 @@ int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, const Sche
                          cudaStream_t s) {
   {
     KernelScope trace("tile_schedule", s);
-    if (launch_kernel(tile_schedule_kernel, dim3(1), dim3(1024), 0, s, "tile_schedule", 1, m_indptr, E, R,
-                      b.tile_prefix, b.pad_indptr, b.pair_prefix, b.order, b.claims, dev.err_flag) != cudaSuccess)
+    if (launch_kernel(tile_schedule_kernel, dim3(1), dim3(1024), 0, s, "tile_schedule", 1, m_indptr, E, R, b,
+                      dev.err_flag) != cudaSuccess)
       return LIGER_MOE_ERR_LAUNCH;
   }
   return check_launch("tile_schedule");
@@ -1641,6 +1697,17 @@ int launch_gate_up(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) 
     return launch_gemm<Sched::RowsM, Epi::SwiGLU, false, false, 0, Gather::None, 2, 1>(
         ta, tb, tc0, tc1, p, pair_m_tiles(a.R, a.E, p.n_tiles), dev, s, "gemm_gate_up_swiglu");
   }
+  if (use_split(a) && a.act == LIGER_MOE_ACT_SWIGLU) {  // heavy experts as pairs, then the light ones
+    KernelScope trace("gemm_gate_up_swiglu", s);
+    Params ph = p;
+    ph.tile_prefix = a.heavy_pair_prefix;
+    if (int rc = launch_gemm<Sched::RowsM, Epi::SwiGLU, false, false, 0, Gather::None, 2, 1>(
+            ta, tb, tc0, tc1, ph, pair_m_tiles(a.R, a.E, p.n_tiles), dev, s, "gemm_gate_up_swiglu", false))
+      return rc;
+    p.tile_prefix = a.light_prefix;
+    return launch_gemm<Sched::RowsM, Epi::SwiGLU, false, false>(ta, tb, tc0, tc1, p, tiles, dev, s,
+                                                                 "gemm_gate_up_swiglu", false);
+  }
   if (a.act != LIGER_MOE_ACT_SWIGLU) {  // the other gated activations read x_perm
     if (gather) return LIGER_MOE_ERR_INVALID_ARG;
     return launch_gemm<Sched::RowsM, Epi::GLU, false, false>(ta, tb, tc0, tc1, p, tiles, dev, s, "gemm_gate_up_glu");
@@ -1680,10 +1747,12 @@ int launch_router_logits(const uint16_t* x, const uint16_t* w_router, const floa
 
 int launch_down(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   if (a.R == 0) return LIGER_MOE_OK;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tb_half;
   const bool pair = use_pairs(a);  // 2-SM pairs: each CTA loads 128 of a tile's 256 B rows
+  const bool split = use_split(a);  // pairs for the heavy experts only
   if (make_tmap(&ta, a.h_perm, a.I, a.R, BK, BM) ||
-      make_tmap(&tb, a.w_down, a.I, 1ULL * a.H * a.E, BK, pair ? BN / 2 : BN))
+      make_tmap(&tb, a.w_down, a.I, 1ULL * a.H * a.E, BK, pair ? BN / 2 : BN) ||
+      (split && make_tmap(&tb_half, a.w_down, a.I, 1ULL * a.H * a.E, BK, BN / 2)))
     return LIGER_MOE_ERR_LAUNCH;
   Params p = base_params(a.m_indptr, a.tile_prefix, a.E, dev.err_flag);
   p.n_tiles = cdiv(a.H, BN);
@@ -1700,6 +1769,18 @@ int launch_down(const FwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
     p.tile_prefix = a.pair_prefix;
     return launch_gemm<Sched::RowsM, Epi::ScaleRows, false, false, 0, Gather::None, 2, 1>(
         ta, tb, tc0, tc0, p, pair_m_tiles(a.R, a.E, p.n_tiles), dev, s, "gemm_down_scale");
+  }
+  if (split) {  // heavy experts as pairs, then the light ones
+    KernelScope trace("gemm_down_scale", s);
+    Params ph = p;
+    ph.tile_prefix = a.heavy_pair_prefix;
+    if (int rc = launch_gemm<Sched::RowsM, Epi::ScaleRows, false, false, 0, Gather::None, 2, 1>(
+            ta, tb_half, tc0, tc0, ph, pair_m_tiles(a.R, a.E, p.n_tiles), dev, s, "gemm_down_scale", false))
+      return rc;
+    p.tile_prefix = a.light_prefix;
+    return launch_gemm<Sched::RowsM, Epi::ScaleRows, false, false>(ta, tb, tc0, tc0, p,
+                                                                    rows_m_tiles(a.R, a.E, p.n_tiles), dev, s,
+                                                                    "gemm_down_scale", false);
   }
   return launch_gemm<Sched::RowsM, Epi::ScaleRows, false, false>(ta, tb, tc0, tc0, p,
                                                                   rows_m_tiles(a.R, a.E, p.n_tiles), dev, s,
@@ -1771,6 +1852,17 @@ int launch_bwd_dx(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
     return launch_gemm<Sched::RowsM, Epi::Store, false, true, 0, Gather::None, 2, 1>(
         ta, tb, tc0, tc0, p, pair_m_tiles(a.R, a.E, p.n_tiles), dev, s, "gemm_bwd_dx");
   }
+  if (use_split(a)) {  // heavy experts as pairs, then the light ones
+    KernelScope trace("gemm_bwd_dx", s);
+    Params ph = p;
+    ph.tile_prefix = a.heavy_pair_prefix;
+    if (int rc = launch_gemm<Sched::RowsM, Epi::Store, false, true, 0, Gather::None, 2, 1>(
+            ta, tb, tc0, tc0, ph, pair_m_tiles(a.R, a.E, p.n_tiles), dev, s, "gemm_bwd_dx", false))
+      return rc;
+    p.tile_prefix = a.light_prefix;
+    return launch_gemm<Sched::RowsM, Epi::Store, false, true>(ta, tb, tc0, tc0, p, rows_m_tiles(a.R, a.E, p.n_tiles),
+                                                               dev, s, "gemm_bwd_dx", false);
+  }
   return launch_gemm<Sched::RowsM, Epi::Store, false, true>(ta, tb, tc0, tc0, p, rows_m_tiles(a.R, a.E, p.n_tiles),
                                                              dev, s, "gemm_bwd_dx");
 }
@@ -1813,14 +1905,17 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.out_expert_stride = static_cast<long long>(a.nin) * a.H;
   if (make_out_bf16_3d(&tc0, a.dw_gate_up, a.H, nin, a.E)) return LIGER_MOE_ERR_LAUNCH;
   // CTA pairs over neighbouring M blocks (2-SM MMAs, each CTA holding half of the x tile) when the M
-  // blocks pair up and experts hold at least 192 rows on average.  With few rows per expert the tiles
-  // are mostly gradient writes, and a 2-SM pair ties the two CTAs' epilogues to each other.
+  // blocks pair up and experts hold at least kPairRowsDwGu rows on average; below that every CTA
+  // works alone on its tile (with few rows per expert the tiles are mostly gradient writes, and a
+  // 2-SM pair ties the two CTAs' epilogues to each other).  A heavy / light split measured slower
+  // here than one-CTA tiles in the heavy-first dynamic order (2687-2719 against 2647-2688 us on the
+  // Zipf 4096/1024 workload).
   const long long tiles_gu = static_cast<long long>(a.E) * p.m_tiles * p.n_tiles;
   int rc;
   if (gather_x)
     rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::B>(ta, tb, tc0, tc0, p, tiles_gu, dev, s,
                                                                          "gemm_bwd_dw_gate_up");
-  else if (p.m_tiles % 2 == 0 && a.R >= 192LL * a.E)
+  else if (p.m_tiles % 2 == 0 && a.R >= kPairRowsDwGu * a.E)
     rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::None, 2, 1>(ta, tb, tc0, tc0, p, tiles_gu / 2,
                                                                                   dev, s, "gemm_bwd_dw_gate_up");
   else
@@ -1851,15 +1946,31 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.ld_out = a.I;
   p.out_expert_stride = 1LL * a.H * a.I;
   if (make_out_bf16_3d(&tc0, a.dw_down, a.I, a.H, a.E)) return LIGER_MOE_ERR_LAUNCH;
-  // CTA pairs over neighbouring M blocks when the M blocks pair up: 2-SM MMAs (each CTA holding half
-  // of the w h tile, 4 stages instead of 2) from 128 rows per expert on average
+  // CTA pairs over neighbouring M blocks (2-SM MMAs, each CTA holding half of the w h tile, 4 stages
+  // instead of 2): for every expert when they hold at least kSplitMeanRows rows on average; for the
+  // experts with at least kPairRowsDwD rows (the head of the sorted order) when fewer, the others one
+  // CTA per tile (the heavy / light split); one CTA per tile for all when no expert can reach it
   const long long tiles_d = static_cast<long long>(a.E) * p.m_tiles * p.n_tiles;
   if (gather_dy)
     return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::A>(ta, tb, tc0, tc0, p, tiles_d, dev, s,
                                                                            "gemm_bwd_dw_down");
-  if (p.m_tiles % 2 == 0 && a.R >= 128LL * a.E)
+  if (p.m_tiles % 2 == 0 && a.R >= kSplitMeanRows * a.E)
     return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::None, 2, 1>(ta, tb, tc0, tc0, p, tiles_d / 2,
                                                                                     dev, s, "gemm_bwd_dw_down");
+  if (p.m_tiles % 2 == 0 && a.T >= kPairRowsDwD) {
+    KernelScope trace("gemm_bwd_dw_down", s);
+    Params ph = p;
+    ph.split_part = 1;
+    ph.split_heavy = a.claims + kClaimSlots + 1;
+    if (int rc2 = launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::None, 2, 1>(
+            ta, tb, tc0, tc0, ph, tiles_d / 2, dev, s, "gemm_bwd_dw_down", false))
+      return rc2;
+    Params pl = p;
+    pl.split_part = 2;
+    pl.split_heavy = ph.split_heavy;
+    return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2>(ta, tb, tc0, tc0, pl, tiles_d, dev, s,
+                                                                "gemm_bwd_dw_down", false);
+  }
   return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2>(ta, tb, tc0, tc0, p, tiles_d, dev, s, "gemm_bwd_dw_down");
 }
 

@@ -74,13 +74,19 @@ int launch_router_logits(const uint16_t* x, const uint16_t* w_router, const floa
 //   tile_prefix[e]   sum over e' < e of ceil(rows_e' / 128) ([E] = total M tiles)
 //   pad_indptr[e]    the padded row prefix (row counts rounded up to 16), or nullptr
 //   pair_prefix[e]   the prefix of 256-row blocks (the 2-SM pair GEMMs' tiles), or nullptr
+//   light_prefix[e], heavy_pair_prefix[e]   (both or neither) the 128-row tile prefix counting only
+//                    experts below the forward / dX pair threshold, and the 256-row block prefix
+//                    counting only those at or above it (the heavy / light split of those GEMMs)
 //   order[i]         experts by rows, most first, equal rows in id order, or nullptr
 //   claims           kClaimSlots claim counters, zeroed by the schedule kernel (one per GEMM launch
-//                    that may take its tiles in that order), then the skew flag; or nullptr
+//                    that may take its tiles in that order), then the skew flag and the count of
+//                    experts at or above the dW_down pair threshold; or nullptr
 struct ScheduleBufs {
   int32_t* tile_prefix = nullptr;
   int32_t* pad_indptr = nullptr;
   int32_t* pair_prefix = nullptr;
+  int32_t* light_prefix = nullptr;
+  int32_t* heavy_pair_prefix = nullptr;
   int32_t* order = nullptr;
   int* claims = nullptr;
 };
@@ -91,6 +97,9 @@ size_t schedule_bytes(int E);                  // one [E+1] int32 array, 256-byt
 constexpr size_t kClaimBytes = 256;            // kClaimSlots counters and the skew flag, 256-byte aligned
 int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, const ScheduleBufs& b, const DeviceInfo& dev,
                          cudaStream_t s);
+// True when R routed rows over E experts may take the heavy / light split of the forward and dX
+// GEMMs (then the schedule needs light_prefix and heavy_pair_prefix).
+bool split_schedule(long long R, int E);
 
 struct FwdGemmArgs {
   const uint16_t* x_perm;       // [R, H]; used when x is NULL
@@ -100,6 +109,10 @@ struct FwdGemmArgs {
   const int32_t* m_indptr;
   const int32_t* tile_prefix;
   const int32_t* pair_prefix = nullptr;  // 256-row block prefix: the pair GEMMs run when set
+  // heavy / light split (both set): 2-SM pairs over the experts with many rows, one CTA per tile
+  // over the others (ScheduleBufs)
+  const int32_t* light_prefix = nullptr;
+  const int32_t* heavy_pair_prefix = nullptr;
   const uint16_t* w_gate_up;
   const uint16_t* w_down;
   const float* w_perm;
@@ -120,8 +133,10 @@ struct BwdGemmArgs {
   const int32_t* m_indptr;
   const int32_t* tile_prefix;
   const int32_t* pair_prefix = nullptr;  // 256-row block prefix: the pair GEMMs run when set
-  const int32_t* sched_order = nullptr;   // experts by rows (the weight gradients' dynamic order)
-  int* claims = nullptr;                  // the schedule's claim counters and skew flag
+  const int32_t* light_prefix = nullptr;  // heavy / light split of the dX GEMM (ScheduleBufs)
+  const int32_t* heavy_pair_prefix = nullptr;
+  const int32_t* sched_order = nullptr;   // experts by rows (the weight gradients' dynamic order and split)
+  int* claims = nullptr;                  // the schedule's claim counters, skew flag and heavy counts
   const uint16_t* w_gate_up;
   const uint16_t* w_down;
   const uint16_t* x_perm;   // [R, H]; used when x is NULL
@@ -196,7 +211,8 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 }
 
 // Kernel trace (off by default): while enabled, each launch made inside a
-// KernelScope is bracketed by two CUDA events recorded on its stream.
+// KernelScope is bracketed by two CUDA events recorded on its stream (a scope named
+// nullptr records nothing).
 class KernelScope {
  public:
   KernelScope(const char* name, cudaStream_t s);
