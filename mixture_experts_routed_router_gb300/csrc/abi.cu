@@ -184,8 +184,8 @@ long long padded_rows(long long R, int E) { return R + 15LL * E; }
 size_t bwd_workspace_bytes(long long R, int H, int I, int E, bool recompute_gu, bool gather) {
   const long long Rp = padded_rows(R, E);
   // tile prefix, padded row prefix, 256-row pair block prefix, light tile and heavy pair prefixes,
-  // expert order, claim counters
-  size_t b = 6 * schedule_bytes(E) + kClaimBytes;
+  // expert order and its [E][4] table, claim counters
+  size_t b = 10 * schedule_bytes(E) + kClaimBytes;
   if (!gather) b += align_up(static_cast<size_t>(R) * H * 2, 256);  // dy_perm
   b += align_up(static_cast<size_t>(Rp) * 2 * I * 2 * 2, 256);        // dgu (hi, lo), padded rows
   b += align_up(static_cast<size_t>(R) * H * 2, 256);                 // dx_perm
@@ -465,6 +465,7 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
     sb.heavy_pair_prefix = heavy;
   }
   sb.order = carve<int32_t>(cur, schedule_bytes(E));
+  sb.order_info = carve<int32_t>(cur, 4 * schedule_bytes(E));
   sb.claims = carve<int>(cur, kClaimBytes);
   int32_t* tile_prefix = sb.tile_prefix;
   int32_t* pad_indptr = sb.pad_indptr;
@@ -483,6 +484,7 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
   a.light_prefix = sb.light_prefix;
   a.heavy_pair_prefix = sb.heavy_pair_prefix;
   a.sched_order = sb.order;
+  a.sched_info = sb.order_info;
   a.claims = sb.claims;
   a.w_gate_up = static_cast<const uint16_t*>(w_gate_up);
   a.w_down = static_cast<const uint16_t*>(w_down);

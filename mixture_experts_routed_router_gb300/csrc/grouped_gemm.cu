@@ -58,17 +58,19 @@ constexpr uint32_t kTmemCols = 2 * BN;
 // feeds TMA bulk stores, so output rows leave the SM as whole lines.
 constexpr int STG_BYTES = 32 * 128;
 constexpr int STG_PER_WARP = 1;
-constexpr int kBarrierBytes = 768;  // barriers, the tile ring, and (at kZeroOffset) a zero row for zero tiles
-constexpr int kZeroOffset = 512;
+constexpr int kBarrierBytes = 1024;  // barriers, the tile ring, and (at kZeroOffset) a zero row for zero tiles
+constexpr int kZeroOffset = 768;
 constexpr int kZeroBytes = 256;     // one warp row of a zero tile: BN / 2 bf16 columns
 // Per-expert 2-SM pair thresholds (rows of one expert): the forward and dX GEMMs (256-row pair tiles)
 // and the two weight-gradient GEMMs.  An expert with fewer rows runs one CTA per tile.
 constexpr int kPairRowsM = 512, kPairRowsDwGu = 192, kPairRowsDwD = 128;  // dW_gate_up: on the mean rows
 
-// Dynamic tile order: slots of the ring that passes claimed tiles from the producer to the other
-// warps, and the index of its first barrier in the barrier area (after the pipeline barriers).
+// The tile ring: slots of the ring that passes decoded tiles from the producer to the MMA and
+// epilogue warps (kRingInts ints each), and the index of its first barrier in the barrier area
+// (after the pipeline barriers).
 constexpr int kSchedSlots = 8;
 constexpr int kSchedBarIndex = 24;
+constexpr int kRingInts = 10;
 constexpr int kDhBoxBytes = 32 * 32;            // dH epilogue: 32 rows x 16 bf16 columns
 constexpr int kDhSetBytes = 6 * kDhBoxBytes;    // six output boxes per 16 columns
 
@@ -146,9 +148,11 @@ struct Params {
   int topk;
   // Dynamic tile order of the weight-gradient GEMMs (claims != NULL): when the schedule found the
   // load skewed (*sched_skewed != 0), the tiles are queued expert by expert with the experts
-  // sorted by rows, most first (sched_order), and each CTA's producer claims the next position
-  // through one counter (zeroed by the schedule kernel).  Otherwise the static order.
+  // sorted by rows, most first (sched_order, and sched_info for each sorted expert), and each CTA's
+  // producer claims the next positions through one counter (zeroed by the schedule kernel).
+  // Otherwise the static order.
   const int32_t* sched_order;   // [E]
+  const int32_t* sched_info;    // [E][4]: expert, first row, rows, first padded row of each sorted expert
   const int* sched_skewed;
   int* claims;
   // Heavy / light split of dW_down (split_part != 0): the experts of the sorted
@@ -207,6 +211,21 @@ __device__ __forceinline__ Tile rows_k_tile(int e, int r, const Params& p) {
   return tl;
 }
 
+// The same tile from the schedule's table entry of its expert (id, first row, rows, first padded
+// row): one 16-byte load instead of the order and then the expert's row offsets.
+__device__ __forceinline__ Tile rows_k_tile_info(int4 q, int r, const Params& p) {
+  Tile tl;
+  tl.e = q.x;
+  tl.nt = r / p.m_tiles;
+  tl.m0 = (r - tl.nt * p.m_tiles) * BM;
+  tl.row0 = q.y;
+  tl.rows = q.z;
+  tl.am0 = tl.m0;
+  tl.prow0 = q.w;
+  tl.kb_count = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
+  return tl;
+}
+
 // Largest i in [0, n) with prefix[i] <= v (prefix non-decreasing, prefix[0] = 0 <= v).
 __device__ __forceinline__ int prefix_search(const int32_t* prefix, int n, int v) {
   int lo = 0, hi = n;  // prefix[lo] <= v < prefix[hi]
@@ -220,10 +239,11 @@ __device__ __forceinline__ int prefix_search(const int32_t* prefix, int n, int v
   return lo;
 }
 
-// Tile t of the launch, experts in id order; RowsK in the dynamic order (dyn): t is a queue
-// position and the experts are taken in the sorted order.
+// Tile t of the launch in the static order, experts in id order (RowsK parts of a heavy / light
+// split: in the sorted order).  The dynamic order decodes its tiles from the schedule's table
+// (rows_k_tile_info).
 template <Sched S>
-__device__ __forceinline__ Tile decode_tile(int t, const Params& p, bool dyn = false) {
+__device__ __forceinline__ Tile decode_tile(int t, const Params& p) {
   if constexpr (S == Sched::RowsM) {
     const int mt = t / p.n_tiles;
     const int nt = t - mt * p.n_tiles;
@@ -246,16 +266,10 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, bool dyn = f
     const int i = t / per_e;
     // the sorted order from the split's first expert (dynamic order or a heavy / light part)
     const int base = p.split_part == 2 ? __ldg(p.split_heavy) : 0;
-    const int e = (dyn || p.split_part != 0) ? __ldg(p.sched_order + base + i) : i;
+    const int e = p.split_part != 0 ? __ldg(p.sched_order + base + i) : i;
     return rows_k_tile(e, t - i * per_e, p);
   }
 }
-
-// The next queue position of a dynamic order: one atomic on the launch's counter; -1 once the
-// queue is empty.  claim_issue and claim_position are split so that the atomic's latency passes
-// while the producer loads the current tile.
-__device__ __forceinline__ int claim_issue(const Params& p) { return atomicAdd(p.claims, 1); }
-__device__ __forceinline__ int claim_position(int claimed, int total) { return claimed < total ? claimed : -1; }
 
 // Tile of a 2-SM pair.  RowsM: tile_prefix counts 256-row blocks per expert; CTA `rank` of the
 // pair owns rows [m0, m0 + 128) of the block (none when the expert ends before them).  RowsK:
@@ -894,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (kPair)
       return decode_tile_pair<S>(t, p, rank);
     else
-      return decode_tile<S>(t, p, dyn);
+      return decode_tile<S>(t, p);
   };
   static_assert(SPLIT == 0 || (S == Sched::RowsK && A_MN && B_MN), "hi/lo operands only in the dW GEMMs");
   static_assert(G == Gather::None || (S == Sched::RowsM ? (G == Gather::A && !A_MN)
@@ -908,9 +922,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + L::kBarOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  // dynamic tile order: a ring of claimed tile positions from the producer to the MMA and epilogue
-  // warps (full: written; empty: read by all of them)
-  static_assert(2 * 6 + 5 + 1 <= kSchedBarIndex && (kSchedBarIndex + 2 * kSchedSlots) * 8 + 4 * kSchedSlots <= kBarrierBytes,
+  // the tile ring (dynamic order): decoded tiles from the producer to the MMA and epilogue warps
+  // (full: written; empty: read by all of them), so that only the producer reads the schedule from
+  // global memory
+  static_assert(2 * 6 + 5 + 1 <= kSchedBarIndex &&
+                    (kSchedBarIndex + 2 * kSchedSlots) * 8 + 4 * kRingInts * kSchedSlots <= kBarrierBytes,
                 "barrier area layout");
   volatile int* sched_ring = reinterpret_cast<volatile int*>(bars + kSchedBarIndex + 2 * kSchedSlots);
 
@@ -924,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sfull0 = smem_u32(bars + kSchedBarIndex);
   const uint32_t sempty0 = smem_u32(bars + kSchedBarIndex + kSchedSlots);
   const uint32_t zero_row = smem_u32(base_ptr + L::kBarOffset + kZeroOffset);  // kZeroBytes of zeros
-  static_assert(kSchedBarIndex * 8 + 2 * kSchedSlots * 8 + 4 * kSchedSlots <= kZeroOffset &&
+  static_assert(kSchedBarIndex * 8 + 2 * kSchedSlots * 8 + 4 * kRingInts * kSchedSlots <= kZeroOffset &&
                     kZeroOffset + kZeroBytes <= kBarrierBytes,
                 "barrier area: barriers, tile ring, zero row");
 
@@ -940,7 +956,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     for (int q = 0; q < kSchedSlots; ++q) {
       mbar_init(sfull0 + 8 * q, 1);
-      mbar_init(sempty0 + 8 * q, 1 + kEpiWarps);  // the MMA warp and every epilogue warp
+      mbar_init(sempty0 + 8 * q, (leader ? 1 : 0) + kEpiWarps);  // the MMA warp (if it issues) and every epilogue warp
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -986,25 +1002,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     total = (p.split_part == 0 ? p.E : (p.split_part == 1 ? __ldg(p.split_heavy) : p.E - __ldg(p.split_heavy))) *
             (kPair ? p.m_tiles / 2 : p.m_tiles) * p.n_tiles;  // experts of the part x tiles (pair: M blocks two at a time)
 
-  // The next tile of the MMA warp or an epilogue warp: the static sequence tile0, tile0 + tstride,
-  // ..., or the next entry of the producer's ring (dynamic order).  false: the wait gave up.
-  // (slot, sphase: this warp's position in the ring; the producer writes through its own copy.)
+  // The tile sequence of the MMA warp and the epilogue warps: the tile at queue position t (t < 0 or
+  // past the launch's tiles ends it) and its accumulator.  In the static order every warp walks
+  // tile0, tile0 + tstride, ... and decodes the tiles itself, the accumulators alternating over
+  // tiles with K blocks; in the dynamic order the producer decodes every tile and passes it, with
+  // its accumulator, through the ring.  (slot, sphase: this warp's position in the ring; the
+  // producer writes through its own copy.)  false: a wait gave up.
   int slot = 0;
   uint32_t sphase = 0;
-  auto next_tile = [&](int& t, bool first) -> bool {
-    if (!dyn) {
+  int acc_walk = 1;
+  auto next_tile = [&](int& t, Tile& tl, int& acc, bool first) -> bool {
+    if (G != Gather::None || !dyn) {
       t = first ? tile0 : t + tstride;
+      if (t < total) {
+        tl = decode(t);
+        if (tl.kb_count > 0) acc_walk ^= 1;
+        acc = acc_walk;
+      }
+      return true;
+    } else {
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(sfull0 + 8 * slot, sphase, abort_flag))) return false;
+      const volatile int* r = sched_ring + kRingInts * slot;
+      t = r[0];
+      acc = r[1];
+      tl.e = r[2];
+      tl.m0 = r[3];
+      tl.rows = r[4];
+      tl.nt = r[5];
+      tl.row0 = r[6];
+      tl.am0 = r[7];
+      tl.prow0 = r[8];
+      tl.kb_count = r[9];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sempty0 + 8 * slot);
+      if (++slot == kSchedSlots) {
+        slot = 0;
+        sphase ^= 1u;
+      }
       return true;
     }
-    if (!__all_sync(0xFFFFFFFFu, mbar_wait(sfull0 + 8 * slot, sphase, abort_flag))) return false;
-    t = sched_ring[slot];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sempty0 + 8 * slot);
-    if (++slot == kSchedSlots) {
-      slot = 0;
-      sphase ^= 1u;
-    }
-    return true;
   };
 
   if (warp == 0) {
@@ -1014,31 +1050,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         bool failed = false;
-        // dynamic order: every claim is published to the ring (-1 last) before its loads
-        int t = dyn ? claim_position(claim_issue(p), total) : tile0;
-        for (;;) {
-          if (dyn) {
-            if (!mbar_wait(sempty0 + 8 * slot, sphase ^ 1u, abort_flag)) {
-              raise_abort(p.err, abort_flag);
-              failed = true;
-              break;
-            }
-            sched_ring[slot] = t;
-            mbar_arrive(sfull0 + 8 * slot);
-            if (++slot == kSchedSlots) {
-              slot = 0;
-              sphase ^= 1u;
-            }
-          }
-          if (t < 0 || t >= total) break;
-          const int next_claim = dyn ? claim_issue(p) : 0;
-          const Tile tl = decode(t);
+        // the K blocks of a tile into the stage ring, in order.  false: a wait gave up.
+        auto load_tile = [&](const Tile& tl) -> bool {
           for (int kb = 0; kb < tl.kb_count; ++kb) {
-            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
-              raise_abort(p.err, abort_flag);
-              failed = true;
-              break;
-            }
+            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) return false;
             const uint32_t sa = sbase + stage * STAGE_BYTES;
             const uint32_t fb = full0 + 8 * stage;
             if constexpr (kPair) {
@@ -1055,9 +1070,73 @@ __global__ void __launch_bounds__(kThreads, 1)
               phase ^= 1u;
             }
           }
-          if (failed) break;
-          t = dyn ? claim_position(next_claim, total) : t + tstride;
+          return true;
+        };
+        // a tile's position, accumulator and decoded fields into the ring (before its loads)
+        auto publish = [&](int t, const Tile& tl, int acc) -> bool {
+          if (!mbar_wait(sempty0 + 8 * slot, sphase ^ 1u, abort_flag)) return false;
+          volatile int* r = sched_ring + kRingInts * slot;
+          r[0] = t;
+          r[1] = acc;
+          r[2] = tl.e;
+          r[3] = tl.m0;
+          r[4] = tl.rows;
+          r[5] = tl.nt;
+          r[6] = tl.row0;
+          r[7] = tl.am0;
+          r[8] = tl.prow0;
+          r[9] = tl.kb_count;
+          mbar_arrive(sfull0 + 8 * slot);
+          if (++slot == kSchedSlots) {
+            slot = 0;
+            sphase ^= 1u;
+          }
+          return true;
+        };
+        if (!dyn) {
+          for (int t = tile0; t < total; t += tstride) {
+            const Tile tl = decode(t);
+            if (!load_tile(tl)) {
+              failed = true;
+              break;
+            }
+          }
+        } else {
+          // Dynamic order: the queue positions (experts sorted by rows, most first, their tiles
+          // expert by expert) are claimed through one counter, two claims ahead, and the next
+          // tile's table entry is loaded one tile ahead, so that the atomics' and the loads'
+          // latency passes during the loads of earlier tiles.  A claimed position is always
+          // processed by its claimer.  Every tile is published to the ring before its loads, the
+          // accumulators alternating over tiles with K blocks; a -1 position ends the sequence.
+          const int per_e = p.m_tiles * p.n_tiles;
+          const int4* info = reinterpret_cast<const int4*>(p.sched_info) + (p.split_part == 2 ? __ldg(p.split_heavy) : 0);
+          auto claim = [&]() -> int {
+            const int c = atomicAdd(p.claims, 1);
+            return c < total ? c : -1;
+          };
+          auto info_of = [&](int t) -> int4 { return t >= 0 ? __ldg(info + t / per_e) : make_int4(0, 0, 0, 0); };
+          int next = claim();
+          int next2 = claim();
+          int4 next_info = info_of(next);
+          int acc = 1;
+          for (;;) {
+            const int t = next;
+            Tile tl{};
+            if (t >= 0) {
+              tl = rows_k_tile_info(next_info, t - (t / per_e) * per_e, p);
+              next = next2;
+              next2 = claim();
+              next_info = info_of(next);
+              if (tl.kb_count > 0) acc ^= 1;
+            }
+            if (!publish(t, tl, acc) || (t >= 0 && !load_tile(tl))) {
+              failed = true;
+              break;
+            }
+            if (t < 0) break;
+          }
         }
+        if (failed) raise_abort(p.err, abort_flag);
         if constexpr (kPair) {
           // the even CTA has released the last fill of each stage: no release from the peer is
           // still on its way to this CTA's barriers when it exits
@@ -1148,22 +1227,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc = idesc_bf16_f32(kPair ? 2 * BM : BM, BN, A_MN, B_MN);
     int stage = 0;
     uint32_t phase = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
+    uint32_t acc_phase = 0;  // bit a: the phase of accumulator a
     bool failed = false;
-    int t = 0;
+    int t = 0, acc = 0;
+    Tile tl{};
     for (bool first = true; leader && !failed; first = false) {
-      if (!next_tile(t, first)) {
+      if (!next_tile(t, tl, acc, first)) {
         raise_abort(p.err, abort_flag);
         break;
       }
       if (t < 0 || t >= total) break;
-      const Tile tl = decode(t);
       if (tl.kb_count == 0) continue;
       // every lane waits (so every lane acquires the phase); the outcome is made warp-uniform.
       // Pair: the accumulator is free once both CTAs' epilogues have read it (cluster scope).
-      const bool freed = kPair ? mbar_wait_cluster(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag)
-                               : mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag);
+      const uint32_t par = ((acc_phase >> acc) & 1u) ^ 1u;
+      const bool freed = kPair ? mbar_wait_cluster(tempty0 + 8 * acc, par, abort_flag)
+                               : mbar_wait(tempty0 + 8 * acc, par, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, freed)) {
         raise_abort(p.err, abort_flag);
         break;
@@ -1234,8 +1313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(tfull0 + 8 * acc);
       }
       __syncwarp();
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      acc_phase ^= 1u << acc;
     }
     // every MMA issued by this CTA has completed before TMEM is released
     if (lane == 0 && leader) {
@@ -1254,16 +1332,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int colhalf = ew >> 2;   // which half of the tile's columns
     const int row_local = sub * 32 + lane;
     Stager st{sbase + L::kStgOffset + static_cast<uint32_t>(ew * L::kStgWarpBytes), 0};
-    int acc = 0;
     uint32_t acc_phase = 0;
-    int t = 0;
+    int t = 0, acc = 0;
+    Tile tl{};
     for (bool first = true;; first = false) {
-      if (!next_tile(t, first)) {
+      if (!next_tile(t, tl, acc, first)) {
         raise_abort(p.err, abort_flag);
         break;
       }
       if (t < 0 || t >= total) break;
-      const Tile tl = decode(t);
       // the tile's epilogue operands (DH) start moving into L2 now, a tile's MMA time ahead of use
       // when the MMAs lead, and at least ahead of the later column chunks when the epilogue does
       prefetch_epilogue_operands<S, EP>(tl, row_local, colhalf, p);
@@ -1271,7 +1348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (S == Sched::RowsK) store_zero_tile(tl, sub, colhalf, lane, p, zero_row);
         continue;
       }
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag))) {
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull0 + 8 * acc, (acc_phase >> acc) & 1u, abort_flag))) {
         raise_abort(p.err, abort_flag);
         break;
       }
@@ -1286,8 +1363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           mbar_arrive(tempty0 + 8 * acc);
       }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      acc_phase ^= 1u << acc;
     }
     // outputs are in global memory (and the staging buffers free) before the CTA exits; every lane
     // waits for its own bulk copies (zero tiles)
@@ -1411,6 +1487,15 @@ __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __re
         rank += (r > rows || (r == rows && e < tid)) ? 1 : 0;
       }
       sb.order[rank] = tid;
+      if (sb.order_info != nullptr) {
+        const int a0 = bad ? 0 : m_indptr[tid];
+        int4 q;
+        q.x = tid;
+        q.y = a0;
+        q.z = bad ? 0 : rows;
+        q.w = sb.pad_indptr != nullptr ? (bad ? 0 : p_excl) : a0;
+        reinterpret_cast<int4*>(sb.order_info)[rank] = q;
+      }
     }
     if (tid == 0 && sb.claims != nullptr) {
       // skewed load: the largest expert holds at least 512 rows and 4x the mean (the one-CTA
@@ -1556,10 +1641,11 @@ Params base_params(const int32_t* m_indptr, const int32_t* tile_prefix, int E, i
 }
 
 // Weight gradients in the dynamic order when the schedule finds the load skewed (claim counter
-// `slot` of the schedule's counters; the flag follows the counters).
-void set_dynamic(Params& p, const int32_t* order, int* claims, int slot) {
-  if (order == nullptr || claims == nullptr) return;
+// `slot` of the schedule's counters; the skew flag follows the counters).
+void set_dynamic(Params& p, const int32_t* order, const int32_t* info, int* claims, int slot) {
+  if (order == nullptr || info == nullptr || claims == nullptr) return;
   p.sched_order = order;
+  p.sched_info = info;
   p.claims = claims + slot;
   p.sched_skewed = claims + kClaimSlots;
 }
@@ -1824,8 +1910,10 @@ int launch_bwd_dh(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   if (gather)
     return launch_gemm<Sched::RowsM, Epi::DH, false, true, 0, Gather::A>(ta, tb, tc0, tc1, p, tiles, dev, s,
                                                                         "gemm_bwd_dh");
-  // dH stays one CTA per tile at every load: its epilogue, not its operand pipeline, bounds it, and
-  // 2-SM pairs measured 5 % slower at 512 rows per expert (their 256-row tiles waste rows)
+  // dH stays one CTA per tile at every load: its epilogue, not its operand pipeline, bounds it.
+  // 2-SM pairs measured 5 % slower at 512 rows per expert (their 256-row tiles waste rows), and
+  // pairs for the heavy experts of a skewed batch (the split of the forward and dX GEMMs) changed
+  // nothing (1161-1165 against 1163-1172 us on the Zipf 4096/1024 workload)
   return launch_gemm<Sched::RowsM, Epi::DH, false, true>(ta, tb, tc0, tc1, p, tiles, dev, s, "gemm_bwd_dh");
 }
 
@@ -1897,7 +1985,7 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.b_split_rows = 0;
   p.pad_a = 1;  // dgu rows: padded row space (zero rows past each expert)
   p.pad_b = 0;
-  if (!empty) set_dynamic(p, a.sched_order, a.claims, kClaimDwGateUp);  // R = 0: no schedule
+  if (!empty) set_dynamic(p, a.sched_order, a.sched_info, a.claims, kClaimDwGateUp);  // R = 0: no schedule
   p.M_out = a.nin;
   p.N_out = a.H;
   p.out = a.dw_gate_up;
@@ -1939,7 +2027,7 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.b_split_rows = static_cast<int>(a.R_pad);
   p.pad_a = 0;
   p.pad_b = 1;  // w h rows: padded row space
-  if (!empty) set_dynamic(p, a.sched_order, a.claims, kClaimDwDown);
+  if (!empty) set_dynamic(p, a.sched_order, a.sched_info, a.claims, kClaimDwDown);
   p.M_out = a.H;
   p.N_out = a.I;
   p.out = a.dw_down;

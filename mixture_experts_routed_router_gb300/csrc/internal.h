@@ -78,6 +78,8 @@ int launch_router_logits(const uint16_t* x, const uint16_t* w_router, const floa
 //                    experts below the forward / dX pair threshold, and the 256-row block prefix
 //                    counting only those at or above it (the heavy / light split of those GEMMs)
 //   order[i]         experts by rows, most first, equal rows in id order, or nullptr
+//   order_info[4i..] the expert at order[i], its first row, its rows and its first padded row (the
+//                    first row when there is no padded row prefix); with order, or nullptr
 //   claims           kClaimSlots claim counters, zeroed by the schedule kernel (one per GEMM launch
 //                    that may take its tiles in that order), then the skew flag and the count of
 //                    experts at or above the dW_down pair threshold; or nullptr
@@ -88,6 +90,7 @@ struct ScheduleBufs {
   int32_t* light_prefix = nullptr;
   int32_t* heavy_pair_prefix = nullptr;
   int32_t* order = nullptr;
+  int32_t* order_info = nullptr;
   int* claims = nullptr;
 };
 constexpr int kClaimSlots = 8;
@@ -136,6 +139,7 @@ struct BwdGemmArgs {
   const int32_t* light_prefix = nullptr;  // heavy / light split of the dX GEMM (ScheduleBufs)
   const int32_t* heavy_pair_prefix = nullptr;
   const int32_t* sched_order = nullptr;   // experts by rows (the weight gradients' dynamic order and split)
+  const int32_t* sched_info = nullptr;    // [E][4]: each sorted expert's id, first row, rows, first padded row
   int* claims = nullptr;                  // the schedule's claim counters, skew flag and heavy counts
   const uint16_t* w_gate_up;
   const uint16_t* w_down;

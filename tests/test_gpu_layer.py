@@ -26,6 +26,9 @@ CASES = [
     W("pairs_T2048_H256_I128_E8_k2", 2048, 256, 128, 8, 2),
     W("pairs_zipf_T2048_H320_I192_E4_k2", 2048, 320, 192, 4, 2, zipf_s=1.2, router_std=0.3),  # ragged, skewed
     W("limits_T64_H128_I64_E1024_k32", 64, 128, 64, 1024, 32, router_std=0.3),  # the largest E and k
+    # fewer than 192 rows per expert on average, a few experts with 512 or more: the heavy experts run
+    # as 2-SM pairs and the rest one CTA per tile (two launches per GEMM); ragged N tails, empty experts
+    W("split_zipf_T1024_H320_I192_E64_k8", 1024, 320, 192, 64, 8, zipf_s=1.2, router_std=0.05),
 ]
 
 
