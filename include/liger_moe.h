@@ -363,18 +363,24 @@ int liger_moe_selftest_wait_timeout(int limit_us, void* stream);
 /*
  * Kernel trace (diagnostics; off by default).  While enabled, every kernel
  * this library launches is bracketed by two CUDA events recorded on the
- * launch stream, giving its device-side duration without a profiler.
- *   liger_moe_trace_enable(on)   turns tracing on or off and clears the log
- *   liger_moe_trace_count()      number of launches logged
- *   liger_moe_trace_get(i, ...)  kernel name (static string) and duration in ms
- *                                of launch i; waits for that launch to finish
- * Host-side cost: two event records per launch while enabled.  The records
+ * launch stream, giving its device-side duration without a profiler.  One
+ * logged interval is one kernel, or both launches of a GEMM that runs its
+ * heavy and light experts as two launches.
+ *   liger_moe_trace_enable(on)       turns tracing on or off and clears the log
+ *   liger_moe_trace_count()          number of intervals logged
+ *   liger_moe_trace_get(i, ...)      kernel name (static string) and duration in
+ *                                    ms of interval i; waits for it to finish
+ *   liger_moe_trace_launches(i, n)   number of kernel launches in interval i
+ * Host-side cost: two event records per interval while enabled.  The records
  * are "external", so a trace taken while the stream is captured into a CUDA
  * graph times every replay of the captured launches (the last replay wins).
+ * Errors: LIGER_MOE_ERR_INVALID_ARG for an index outside the log or a NULL
+ * output pointer.
  */
 int liger_moe_trace_enable(int on);
 int liger_moe_trace_count(void);
 int liger_moe_trace_get(int i, const char** name, float* ms);
+int liger_moe_trace_launches(int i, int* launches);
 
 /* Text of the last CUDA error seen by this library in this thread ("" if none). */
 const char* liger_moe_last_cuda_error(void);

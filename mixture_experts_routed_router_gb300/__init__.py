@@ -71,6 +71,7 @@ def load_library(build_if_missing: bool = True):
         lib.liger_moe_selftest_wait_timeout.argtypes = [I, P]
         lib.liger_moe_trace_enable.argtypes = [I]
         lib.liger_moe_trace_get.argtypes = [I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)]
+        lib.liger_moe_trace_launches.argtypes = [I, ctypes.POINTER(ctypes.c_int)]
         lib.liger_moe_last_cuda_error.restype = ctypes.c_char_p
         lib.liger_moe_status_string.restype = ctypes.c_char_p
         lib.liger_moe_status_string.argtypes = [I]
@@ -80,7 +81,7 @@ def load_library(build_if_missing: bool = True):
                   lib.liger_moe_router_logits, lib.liger_moe_router_bwd, lib.liger_moe_device_error,
                   lib.liger_moe_selftest_wait_timeout,
                   lib.liger_moe_abi_version, lib.liger_moe_trace_enable, lib.liger_moe_trace_count,
-                  lib.liger_moe_trace_get):
+                  lib.liger_moe_trace_get, lib.liger_moe_trace_launches):
             f.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -410,6 +411,17 @@ def device_error(stream=None) -> int:
 def trace_enable(on: bool = True) -> None:
     """Turns the library's per-kernel CUDA-event trace on or off (clears the log)."""
     _check("liger_moe_trace_enable", load_library().liger_moe_trace_enable(1 if on else 0))
+
+
+def trace_launch_counts() -> list[int]:
+    """Kernel launches of every logged interval (one, or two for a GEMM split in two launches)."""
+    lib = load_library()
+    out = []
+    n = ctypes.c_int()
+    for i in range(lib.liger_moe_trace_count()):
+        _check("liger_moe_trace_launches", lib.liger_moe_trace_launches(i, ctypes.byref(n)))
+        out.append(int(n.value))
+    return out
 
 
 def trace_records() -> list[tuple[str, float]]:

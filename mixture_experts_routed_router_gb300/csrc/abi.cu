@@ -75,6 +75,7 @@ namespace {
 struct TraceRecord {
   const char* name;
   cudaEvent_t start, stop;
+  int launches;  // kernels launched inside the interval
 };
 std::atomic<int> g_trace_on{0};
 std::mutex g_trace_mu;
@@ -109,6 +110,7 @@ KernelScope::KernelScope(const char* name, cudaStream_t s) : name_(name), stream
   std::lock_guard<std::mutex> lock(g_trace_mu);
   start_ = trace_event();
   if (start_ != nullptr) trace_record(start_, stream_);
+  launches0_ = t_kernel_launches;
 }
 
 KernelScope::~KernelScope() {
@@ -120,7 +122,7 @@ KernelScope::~KernelScope() {
     return;
   }
   trace_record(stop, stream_);
-  g_trace.push_back(TraceRecord{name_, start_, stop});
+  g_trace.push_back(TraceRecord{name_, start_, stop, static_cast<int>(t_kernel_launches - launches0_)});
 }
 
 void set_cuda_error(cudaError_t e, const char* where) {
@@ -676,6 +678,13 @@ LIGER_MOE_API int liger_moe_trace_get(int i, const char** name, float* ms) {
     set_cuda_error(e, "trace event");
     return LIGER_MOE_ERR_LAUNCH;
   }
+  return LIGER_MOE_OK;
+}
+
+LIGER_MOE_API int liger_moe_trace_launches(int i, int* launches) {
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  if (i < 0 || i >= static_cast<int>(g_trace.size()) || launches == nullptr) return LIGER_MOE_ERR_INVALID_ARG;
+  *launches = g_trace[i].launches;
   return LIGER_MOE_OK;
 }
 

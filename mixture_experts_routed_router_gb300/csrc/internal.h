@@ -185,6 +185,9 @@ bool pdl_enabled();
 
 // Launches `kern` on `s` with programmatic stream serialization (when enabled) and, for
 // cluster > 1, that cluster size; records and returns the launch error.
+// Kernels launched by this thread (the trace's per-interval launch counts).
+inline thread_local unsigned long long t_kernel_launches = 0;
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                           const char* name, int cluster, Args&&... args) {
@@ -211,12 +214,13 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
   cfg.numAttrs = n;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
   if (e != cudaSuccess) set_cuda_error(e, name);
+  ++t_kernel_launches;
   return e;
 }
 
-// Kernel trace (off by default): while enabled, each launch made inside a
-// KernelScope is bracketed by two CUDA events recorded on its stream (a scope named
-// nullptr records nothing).
+// Kernel trace (off by default): while enabled, each KernelScope brackets the launches made
+// inside it with two CUDA events recorded on its stream and counts them (a scope named nullptr
+// records nothing; traced scopes do not nest).
 class KernelScope {
  public:
   KernelScope(const char* name, cudaStream_t s);
@@ -228,6 +232,7 @@ class KernelScope {
   const char* name_;
   cudaStream_t stream_;
   cudaEvent_t start_ = nullptr;
+  unsigned long long launches0_ = 0;
 };
 
 }  // namespace lmoe
