@@ -258,6 +258,93 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) dispatch_scatter_kernel(
   }
 }
 
+// The three steps in one block for small batches: one warp per unit, kSmallUnits units at most
+// (R <= 8192 slots) and at most kSmallExperts experts, so that every unit's histogram fits in
+// shared memory.  The units, their order and the ranks inside a unit are those of the three
+// kernels above, so the outputs are identical; two launches fewer matter when a whole layer
+// step takes tens of microseconds.
+constexpr int kSmallUnits = 32;
+constexpr int kSmallExperts = 256;
+
+__global__ void __launch_bounds__(kSmallUnits * 32) dispatch_small_kernel(
+    const int32_t* __restrict__ ids, const float* __restrict__ w, long long R, int E, int nunits,
+    int32_t* __restrict__ counts, int32_t* __restrict__ m_indptr, int32_t* __restrict__ row_to_slot,
+    int32_t* __restrict__ slot_to_row, float* __restrict__ w_perm, int* err) {
+  griddep_wait();  // earlier kernels on the stream are complete
+  griddep_launch_dependents();
+  __shared__ int s_hist[kSmallUnits * kSmallExperts];  // [unit][e]: counts, then the unit's base
+  __shared__ int s_cnt[kSmallExperts];
+  __shared__ int s_off[kSmallExperts + 1];
+  __shared__ int s_warp[32];
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = wib;
+  int* h = s_hist + wib * E;
+  for (int e = lane; e < E; e += 32) h[e] = 0;
+  __syncwarp();
+  const long long s0 = static_cast<long long>(unit) * kUnit;
+  int ev[kGroups];
+  float wv[kGroups];
+#pragma unroll
+  for (int g = 0; g < kGroups; ++g) {
+    const long long s = s0 + g * 32 + lane;
+    const bool in = unit < nunits && s < R;
+    ev[g] = in ? __ldg(ids + s) : kNoSlot;
+    wv[g] = (in && w_perm != nullptr) ? __ldg(w + s) : 0.f;
+  }
+  // 1. the unit's histogram
+  int bad = 0;
+#pragma unroll
+  for (int g = 0; g < kGroups; ++g) {
+    if (unit >= nunits || s0 + g * 32 + lane >= R) continue;
+    const int e = ev[g];
+    if (static_cast<unsigned>(e) < static_cast<unsigned>(E))
+      atomicAdd(&h[e], 1);
+    else
+      bad = 1;
+  }
+  if (__any_sync(kFull, bad) && lane == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_EXPERT_ID);
+  __syncthreads();
+  // 2. per expert, the exclusive scan over units in place, and the expert's count
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int u = 0; u < nunits; ++u) {
+      const int v = s_hist[u * E + e];
+      s_hist[u * E + e] = run;
+      run += v;
+    }
+    s_cnt[e] = run;
+    counts[e] = run;
+  }
+  __syncthreads();
+  block_exclusive_scan(s_cnt, E, s_off, s_warp);
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) m_indptr[e] = s_off[e];
+  if (unit >= nunits) return;
+  // 3. the unit's slots in order, as the scatter kernel
+  for (int e = lane; e < E; e += 32) h[e] += s_off[e];
+  __syncwarp();
+#pragma unroll
+  for (int g = 0; g < kGroups; ++g) {
+    const long long s = s0 + g * 32 + lane;
+    int e = ev[g];
+    const bool ok = s < R && static_cast<unsigned>(e) < static_cast<unsigned>(E);
+    if (!ok) e = E + lane;  // unique per lane: never matches a real expert
+    const unsigned peers = __match_any_sync(kFull, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int leader = __ffs(peers) - 1;
+    int pos = 0;
+    if (ok) pos = h[e];
+    __syncwarp();
+    if (ok && lane == leader) h[e] = pos + __popc(peers);
+    __syncwarp();
+    if (ok) {
+      const int r = pos + rank;
+      slot_to_row[s] = r;
+      row_to_slot[r] = static_cast<int32_t>(s);
+      if (w_perm) w_perm[r] = wv[g];
+    }
+  }
+}
+
 // ============================================================================
 // Row gather: dst[r] = src[row_to_slot[r] / k] (optionally scaled by scale[r]
 // in fp32 and rounded to bf16).  One warp per row, 16-byte vectors.
@@ -472,6 +559,16 @@ int launch_dispatch(const int32_t* ids, const float* w, const uint16_t* x, int T
   const int nunits = static_cast<int>((R + kUnit - 1) / kUnit);
   int32_t* hist = static_cast<int32_t*>(workspace);
   const int blocks = (nunits + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  if (nunits > 0 && nunits <= kSmallUnits && E <= kSmallExperts) {  // one launch instead of three
+    {
+      KernelScope trace("dispatch_small", s);
+      launch_kernel(dispatch_small_kernel, dim3(1), dim3(kSmallUnits * 32), 0, s, "dispatch_small", 1, ids, w, R, E,
+                    nunits, counts, m_indptr, row_to_slot, slot_to_row, w_perm, dev.err_flag);
+    }
+    if (int rc = check_launch("dispatch_small")) return rc;
+    if (x_perm != nullptr) return launch_gather_rows(x, row_to_slot, nullptr, R, H, k, x_perm, dev, s);
+    return LIGER_MOE_OK;
+  }
   if (nunits > 0) {
     {
       KernelScope trace("dispatch_hist", s);
