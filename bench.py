@@ -152,7 +152,6 @@ def kernel_work(wl, name: str, gated: bool = True):
         "dispatch_scatter": R * 4 * 5 + nunits * E * 4,
         "dispatch_small": R * 4 * 5 + (2 * E + 1) * 4,  # ids, w read; both maps, w_perm written; counts, m_indptr
         "gather_rows": T * H * 2 + R * H * 2 + R * 4,
-        "gather_rows_scaled": T * H * 2 + R * H * 2 + R * 8,
         "combine": R * H * 2 + T * H * 2 + R * 4,
         "router_grad": T * E * 4 + R * (4 * math.ceil(I / 256) + 12),
         "tile_schedule": (E + 1) * 8,

@@ -517,7 +517,7 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
   if (R > 0) {
     if (int rc = launch_tile_schedule(m_indptr, E, R, sb, dev, s)) return rc;
     if (!gather) {  // dy_perm[r] = dY[token of r]: the dH and dW_down GEMMs read it as dense tiles
-      if (int rc = launch_gather_rows(static_cast<const uint16_t*>(dy), row_to_slot, nullptr, R, H, k, dy_perm, dev, s))
+      if (int rc = launch_scatter_rows(static_cast<const uint16_t*>(dy), slot_to_row, T, H, k, dy_perm, dev, s))
         return rc;
     }
     if (recompute) {

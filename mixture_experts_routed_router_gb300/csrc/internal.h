@@ -43,9 +43,10 @@ int launch_dispatch(const int32_t* ids, const float* w, const uint16_t* x, int T
                     int32_t* counts, int32_t* m_indptr, int32_t* row_to_slot, int32_t* slot_to_row, float* w_perm,
                     uint16_t* x_perm, void* workspace, const DeviceInfo& dev, cudaStream_t s);
 
-// dst[r, :] = src[row_to_slot[r] / k, :] (times scale[r] in fp32 when scale != NULL).
-int launch_gather_rows(const uint16_t* src, const int32_t* row_to_slot, const float* scale, long long R, int H,
-                       int k, uint16_t* dst, const DeviceInfo& dev, cudaStream_t s);
+// The expert-major row copy dst[r, :] = src[row_to_slot[r] / k, :], written by token:
+// dst[slot_to_row[t*k + j], :] = src[t, :] for j < k (each token row read once).
+int launch_scatter_rows(const uint16_t* src, const int32_t* slot_to_row, int T, int H, int k, uint16_t* dst,
+                        const DeviceInfo& dev, cudaStream_t s);
 
 // y[t, :] = bf16(sum_j y_perm[slot_to_row[t*k+j], :]).
 int launch_combine(const uint16_t* y_perm, const int32_t* slot_to_row, int T, int H, int k, uint16_t* y,
