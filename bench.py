@@ -133,8 +133,11 @@ def gemm_bytes(wl, name: str, experts_used: int, gated: bool = True) -> int:
     }[name]
 
 
-def kernel_work(wl, name: str, gated: bool = True):
-    """(kind, algorithmic amount per launch): kind 'flop' for GEMMs, 'byte' for the rest."""
+def kernel_work(wl, name: str, gated: bool = True, f16_rows: int = 0):
+    """(kind, algorithmic amount per launch): kind 'flop' for GEMMs, 'byte' for the rest.  f16_rows:
+    routed rows of the experts that take the backward's fp16 weight-gradient pass (at least 384 rows
+    each; 0: none), whose dY and x rows the row copy also writes as fp16, after the largest |dY|, |x|
+    are read."""
     T, H, I, E, k, R = wl.T, wl.H, wl.I, wl.E, wl.k, wl.R
     rhi = R * H * I
     nunits = math.ceil(R / 256)
@@ -152,6 +155,10 @@ def kernel_work(wl, name: str, gated: bool = True):
         "dispatch_scatter": R * 4 * 5 + nunits * E * 4,
         "dispatch_small": R * 4 * 5 + (2 * E + 1) * 4,  # ids, w read; both maps, w_perm written; counts, m_indptr
         "gather_rows": T * H * 2 + R * H * 2 + R * 4,
+        # dY (and, for the fp16 copies, one x row per token) read; dy_perm (and dy16, x16) written
+        "gather_rows_f16": (2 * T * H * 2 + R * H * 2 + 2 * f16_rows * H * 2 + R * 4) if f16_rows
+                           else (T * H * 2 + R * H * 2 + R * 4),
+        "f16_prep": (2 * T * H * 2 + T * 4) if f16_rows else 0,
         "combine": R * H * 2 + T * H * 2 + R * 4,
         "router_grad": T * E * 4 + R * (4 * math.ceil(I / 256) + 12),
         "tile_schedule": (E + 1) * 8,
@@ -563,6 +570,10 @@ def run_ours(args, rank, world, local_rank):
     if flags:
         raise RuntimeError(f"device error flags {flags:#x} during warm-up")
     experts_used = int((dbuf["counts"] > 0).sum().item())  # experts whose weights the GEMMs read
+    # rows of the experts that take the backward's fp16 weight-gradient pass (the library's rule: gated
+    # experts, expert-major inputs, R >= 4096, experts with at least 384 rows)
+    counts_h = dbuf["counts"].cpu()
+    f16_rows = int(counts_h[counts_h >= 384].sum().item()) if gated and args.inputs != "gather" and wl.R >= 4096 else 0
 
     # ---------------- timed region: K steps, CUDA events on the launching stream
     # The K steps are captured once as a CUDA graph (the library's calls only enqueue work on
@@ -725,7 +736,7 @@ def run_ours(args, rank, world, local_rank):
     # peaks (the dense bf16 rate sustained inside a long step, over the copy bandwidth)
     ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     for name, (n, tot) in sorted(stats.items(), key=lambda kv: -kv[1][1]):
-        kind, amount = kernel_work(wl, name, gated)
+        kind, amount = kernel_work(wl, name, gated, f16_rows)
         avg_s = tot / n * 1e-3
         rate = amount / avg_s if avg_s > 0 else 0.0
         kernels[name] = {"launches": n, "avg_us": round(1e3 * tot / n, 2), "share": round(tot / total_kernel_ms, 4),
@@ -735,7 +746,7 @@ def run_ours(args, rank, world, local_rank):
             kernels[name]["gbs"] = round(nbytes / avg_s / 1e9, 1) if avg_s > 0 else 0.0
             kernels[name]["flop_per_byte"] = round(amount / nbytes, 1)
     dom = max(stats.items(), key=lambda kv: kv[1][1])[0]
-    kind, amount = kernel_work(wl, dom, gated)
+    kind, amount = kernel_work(wl, dom, gated, f16_rows)
     dom_avg_s = stats[dom][1] / stats[dom][0] * 1e-3
     if kind == "flop" and amount / gemm_bytes(wl, dom, experts_used, gated) >= ridge:
         achieved = amount / dom_avg_s / 1e12

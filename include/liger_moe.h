@@ -252,8 +252,17 @@ int liger_moe_combine(const void* y_perm, const int32_t* slot_to_row, int T, int
  * weight is applied in fp32 to the dH accumulator.  The weight-gradient GEMMs
  * take their non-input operand (dgu for dW_gate_up, w * h for dW_down) as two
  * bf16 parts, hi + lo, so that operand carries about 16 significant bits.
+ * Experts with at least 384 rows (when R >= 4096 and the experts are gated)
+ * take one fp16 pass instead (liger_moe_set_dw_fp16): x and dY rows as
+ * fp16(v 2^s) with s set by the tensor's largest magnitude (exact), dgu and
+ * w * h as fp16 (11 significant bits) with power-of-two scales derived from
+ * it, and the result scaled back exactly.  An expert whose scaled dgu or
+ * w * h would leave the fp16 window (overflow, or a largest magnitude too
+ * small for full precision) takes the two-part path instead, so every input
+ * gets one of the two precisions.
  * Limit: T*k < 2^30.  Workspace: about R*(2H + 6I)*2 bytes, plus R*2I*4 more
- * when gu_perm is NULL.
+ * when gu_perm is NULL, plus R*2H*2 for the fp16 copies when R >= 4096 and
+ * the experts are gated.
  */
 int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const void* h_perm, const float* gu_perm,
                         const int32_t* topk_ids, const float* topk_w, const int32_t* m_indptr,
@@ -348,6 +357,16 @@ int liger_moe_router_bwd(const float* d_logits, const int32_t* topk_ids, const i
  * the synchronisation failed.
  */
 int liger_moe_device_error(void* stream, int* flags);
+
+/*
+ * Precision of the weight-gradient operands of the heavy experts in
+ * liger_moe_bwd_dx_dw and liger_moe_bwd_dx_dw_glu (process-wide; default 1):
+ *   1  experts with at least 384 rows use the single fp16 pass described there
+ *      (half the tensor-core work of the two-part path);
+ *   0  every expert uses the bf16 hi + lo parts (about 16 significant bits).
+ * The workspace size does not depend on it.  Anything else is LIGER_MOE_ERR_INVALID_ARG.
+ */
+int liger_moe_set_dw_fp16(int on);
 
 /*
  * Failure-detection self-test (diagnostics).  Launches one kernel in which a thread waits,

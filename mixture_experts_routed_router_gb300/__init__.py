@@ -20,7 +20,7 @@ from . import build as _build
 __all__ = ["route_topk", "dispatch", "grouped_swiglu_fwd", "grouped_swiglu_fwd_gather", "grouped_glu_fwd",
            "combine", "bwd_dx_dw", "bwd_dx_dw_gather", "bwd_dx_dw_glu", "router_logits", "router_bwd", "ACTIVATIONS",
            "device_error",
-           "selftest_wait_timeout", "workspace_bytes", "trace_enable", "trace_records", "LigerMoEError", "library_path", "load_library"]
+           "selftest_wait_timeout", "workspace_bytes", "set_dw_fp16", "trace_enable", "trace_records", "LigerMoEError", "library_path", "load_library"]
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +70,7 @@ def load_library(build_if_missing: bool = True):
         lib.liger_moe_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
         lib.liger_moe_selftest_wait_timeout.argtypes = [I, P]
         lib.liger_moe_trace_enable.argtypes = [I]
+        lib.liger_moe_set_dw_fp16.argtypes = [I]
         lib.liger_moe_trace_get.argtypes = [I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)]
         lib.liger_moe_trace_launches.argtypes = [I, ctypes.POINTER(ctypes.c_int)]
         lib.liger_moe_last_cuda_error.restype = ctypes.c_char_p
@@ -81,7 +82,7 @@ def load_library(build_if_missing: bool = True):
                   lib.liger_moe_router_logits, lib.liger_moe_router_bwd, lib.liger_moe_device_error,
                   lib.liger_moe_selftest_wait_timeout,
                   lib.liger_moe_abi_version, lib.liger_moe_trace_enable, lib.liger_moe_trace_count,
-                  lib.liger_moe_trace_get, lib.liger_moe_trace_launches):
+                  lib.liger_moe_trace_get, lib.liger_moe_trace_launches, lib.liger_moe_set_dw_fp16):
             f.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -406,6 +407,11 @@ def device_error(stream=None) -> int:
     if rc not in (OK, -6):
         _check("liger_moe_device_error", rc)
     return flags.value
+
+
+def set_dw_fp16(on: bool = True) -> None:
+    """Heavy experts' weight gradients in one fp16 pass (True, the default) or as bf16 hi + lo parts."""
+    _check("liger_moe_set_dw_fp16", load_library().liger_moe_set_dw_fp16(1 if on else 0))
 
 
 def trace_enable(on: bool = True) -> None:

@@ -183,7 +183,11 @@ namespace {
 // Rows of each half of the padded weight-gradient operands: every expert's rows rounded up to 16.
 long long padded_rows(long long R, int E) { return R + 15LL * E; }
 
-size_t bwd_workspace_bytes(long long R, int H, int I, int E, bool recompute_gu, bool gather) {
+// The backward may use fp16 weight-gradient operands (f16 rows, expert-major inputs, gated experts):
+// the workspace then holds the fp16 words and the fp16 copies of the x and dY rows.
+bool bwd_f16_possible(long long R, bool gated, bool gather) { return gated && !gather && R >= kF16MinR; }
+
+size_t bwd_workspace_bytes(long long R, int H, int I, int E, bool recompute_gu, bool gather, bool f16) {
   const long long Rp = padded_rows(R, E);
   // tile prefix, padded row prefix, 256-row pair block prefix, light tile and heavy pair prefixes,
   // expert order and its [E][4] table, claim counters
@@ -194,8 +198,11 @@ size_t bwd_workspace_bytes(long long R, int H, int I, int E, bool recompute_gu, 
   b += align_up(static_cast<size_t>(Rp) * I * 2 * 2, 256);            // hw_perm (hi, lo), padded rows
   b += align_up(static_cast<size_t>(R) * gdot_tiles(I) * 4, 256);     // gdot
   if (recompute_gu) b += align_up(static_cast<size_t>(R) * 2 * I * 4, 256);
+  if (f16) b += f16_words_bytes(E) + 2 * align_up(static_cast<size_t>(R) * H * 2, 256);  // words, x16, dy16
   return b;
 }
+
+std::atomic<int> g_dw_fp16{1};
 
 }  // namespace
 }  // namespace lmoe
@@ -443,7 +450,8 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
     return LIGER_MOE_ERR_MISALIGNED;
   const bool recompute = (gu_perm == nullptr);
   const bool gather = (x != nullptr);  // token-major inputs: x and dY rows gathered inside the GEMMs
-  const size_t need = bwd_workspace_bytes(R, H, I, E, recompute, gather);
+  const bool f16_ws = bwd_f16_possible(R, act != LIGER_MOE_ACT_RELU2, gather);
+  const size_t need = bwd_workspace_bytes(R, H, I, E, recompute, gather, f16_ws);
   if (workspace == nullptr) {
     *workspace_bytes = need;
     return LIGER_MOE_OK;
@@ -478,6 +486,11 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
   uint16_t* hw_perm = carve<uint16_t>(cur, static_cast<size_t>(Rp) * I * 2 * 2);
   float* gdot = carve<float>(cur, static_cast<size_t>(R) * gdot_tiles(I) * 4);
   float* gu_ws = recompute ? carve<float>(cur, static_cast<size_t>(R) * 2 * I * 4) : nullptr;
+  unsigned* f16_words = f16_ws ? carve<unsigned>(cur, f16_words_bytes(E)) : nullptr;
+  uint16_t* x16 = f16_ws ? carve<uint16_t>(cur, static_cast<size_t>(R) * H * 2) : nullptr;
+  uint16_t* dy16 = f16_ws ? carve<uint16_t>(cur, static_cast<size_t>(R) * H * 2) : nullptr;
+  const bool f16 = f16_ws && g_dw_fp16.load() != 0;
+  if (f16) sb.f16_words = f16_words;  // zeroed (and the any-heavy word set) by the schedule kernel
 
   BwdGemmArgs a{};
   a.m_indptr = m_indptr;
@@ -513,10 +526,24 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
   a.I = I;
   a.E = E;
   a.nin = act == LIGER_MOE_ACT_RELU2 ? I : 2 * I;  // ReLU²: one up weight, one factor, da [.., I]
+  if (f16) {
+    a.x16 = x16;
+    a.dy16 = dy16;
+    a.f16_words = f16_words;
+    a.f16_rows = kF16Rows;
+  }
 
   if (R > 0) {
     if (int rc = launch_tile_schedule(m_indptr, E, R, sb, dev, s)) return rc;
-    if (!gather) {  // dy_perm[r] = dY[token of r]: the dH and dW_down GEMMs read it as dense tiles
+    if (f16) {
+      // the largest |dY| and |x|, then dy_perm with the fp16 copies of the dY and x rows
+      if (int rc = launch_f16_prep(static_cast<const uint16_t*>(dy), a.x_perm, slot_to_row, T, H, k, f16_words, dev,
+                                   s))
+        return rc;
+      if (int rc = launch_scatter_rows_f16(static_cast<const uint16_t*>(dy), a.x_perm, slot_to_row, T, H, k, m_indptr,
+                                           E, dy_perm, dy16, x16, f16_words, dev, s))
+        return rc;
+    } else if (!gather) {  // dy_perm[r] = dY[token of r]: the dH and dW_down GEMMs read it as dense tiles
       if (int rc = launch_scatter_rows(static_cast<const uint16_t*>(dy), slot_to_row, T, H, k, dy_perm, dev, s))
         return rc;
     }
@@ -648,6 +675,12 @@ LIGER_MOE_API int liger_moe_selftest_wait_timeout(int limit_us, void* stream) {
   DeviceInfo dev;
   if (int rc = current_device(&dev)) return rc;
   return launch_bounded_wait_selftest(static_cast<uint64_t>(limit_us) * 1000ull, dev, static_cast<cudaStream_t>(stream));
+}
+
+LIGER_MOE_API int liger_moe_set_dw_fp16(int on) {
+  if (on != 0 && on != 1) return LIGER_MOE_ERR_INVALID_ARG;
+  g_dw_fp16.store(on);
+  return LIGER_MOE_OK;
 }
 
 LIGER_MOE_API int liger_moe_trace_enable(int on) {

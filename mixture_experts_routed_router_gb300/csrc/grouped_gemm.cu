@@ -70,7 +70,7 @@ constexpr int kPairRowsM = 512, kPairRowsDwGu = 192, kPairRowsDwD = 128;  // dW_
 // (after the pipeline barriers).
 constexpr int kSchedSlots = 8;
 constexpr int kSchedBarIndex = 24;
-constexpr int kRingInts = 10;
+constexpr int kRingInts = 11;
 constexpr int kDhBoxBytes = 32 * 32;            // dH epilogue: 32 rows x 16 bf16 columns
 constexpr int kDhSetBytes = 6 * kDhBoxBytes;    // six output boxes per 16 columns
 
@@ -165,6 +165,18 @@ struct Params {
   float* out_f32;
   const float* col_bias;
   int out_tma;
+  // fp16 weight-gradient operands (f16_role != 0), for the experts with at least f16_rows rows;
+  // f16_words: the backward's words (kF16MaxX, kF16MaxDy, kF16Any, per-expert range maxima).
+  //   DH, role 1: those experts' tiles write fp16(dgu 2^sg) and fp16(w h 2^sh) into the lo rows
+  //     (and no hi rows of w h), and the largest magnitudes into the range words;
+  //   DH, role 2 (refill): only those experts whose fp16 parts are unusable (f16_usable), with
+  //     hi / lo parts;
+  //   RowsK, role 3 (dW_gate_up) / 4 (dW_down): the tiles of experts with usable fp16 parts take
+  //     one fp16 MMA per K step, the lo rows of the padded operand against the fp16 token rows
+  //     (tensor map tmF), and scale the result back by the inverse powers of two.
+  int f16_role;
+  int f16_rows;
+  unsigned* f16_words;
   int* err;
 };
 
@@ -177,7 +189,32 @@ struct Tile {
   int am0;       // RowsM: first row of the tile in the padded row space (= m0 without padding)
   int prow0;     // RowsK: first padded row of the expert (= row0 without padding)
   int kb_count;  // K blocks
+  int f16;       // RowsK: one fp16 MMA per K step; DH: write the fp16 parts
 };
+
+// Expert e's fp16 weight-gradient operands are usable: both token-row scales exist and both of
+// its fp16 parts (written by the dH epilogue) lie within their window.
+__device__ __forceinline__ bool f16_usable(int e, const Params& p) {
+  int s;
+  return p.f16_words[kF16Any] != 0u && f16_scale_exp(p.f16_words[kF16MaxX], s) &&
+         f16_scale_exp(p.f16_words[kF16MaxDy], s) && f16_in_range(p.f16_words[kF16Range + e]) &&
+         f16_in_range(p.f16_words[kF16Range + p.E + e]);
+}
+
+// fp16 tile of a weight-gradient GEMM: an expert with f16_rows rows and usable fp16 parts.
+__device__ __forceinline__ int f16_tile_k(int e, int rows, const Params& p) {
+  return (p.f16_role >= 3 && rows >= p.f16_rows && f16_usable(e, p)) ? 1 : 0;
+}
+
+// The factor that undoes the fp16 operands' scales in a weight gradient: 2^-(s_x + s_g) for
+// dW_gate_up (x 2^s_x against dgu 2^s_g, s_g = s_dY + kF16DguShift), 2^-(s_dY + kF16HwShift) for
+// dW_down.  Exact: a power of two.
+__device__ __forceinline__ float f16_unscale(const Params& p) {
+  int sx = 0, sd = 0;
+  f16_scale_exp(p.f16_words[kF16MaxX], sx);
+  f16_scale_exp(p.f16_words[kF16MaxDy], sd);
+  return p.f16_role == 3 ? f16_pow2(-(sx + sd + kF16DguShift)) : f16_pow2(-(sd + kF16HwShift));
+}
 
 // RowsM tile of expert e: its local M tile lm (128 rows) and N tile nt.
 __device__ __forceinline__ Tile rows_m_tile(int e, int lm, int nt, const Params& p) {
@@ -192,6 +229,14 @@ __device__ __forceinline__ Tile rows_m_tile(int e, int lm, int nt, const Params&
   tl.am0 = p.pad_indptr != nullptr ? __ldg(p.pad_indptr + e) + (tl.m0 - start) : tl.m0;
   tl.prow0 = 0;
   tl.kb_count = p.num_kb;
+  tl.f16 = 0;
+  if (p.f16_role != 0) {  // the dH passes
+    const bool heavy = end - start >= p.f16_rows;
+    if (p.f16_role == 1)
+      tl.f16 = heavy ? 1 : 0;
+    else if (!heavy || f16_usable(e, p))
+      tl.kb_count = 0;  // refill: only the experts whose fp16 parts are unusable
+  }
   return tl;
 }
 
@@ -208,6 +253,7 @@ __device__ __forceinline__ Tile rows_k_tile(int e, int r, const Params& p) {
   tl.am0 = tl.m0;
   tl.prow0 = p.pad_indptr != nullptr ? __ldg(p.pad_indptr + e) : tl.row0;
   tl.kb_count = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
+  tl.f16 = f16_tile_k(e, tl.rows, p);
   return tl;
 }
 
@@ -223,6 +269,7 @@ __device__ __forceinline__ Tile rows_k_tile_info(int4 q, int r, const Params& p)
   tl.am0 = tl.m0;
   tl.prow0 = q.w;
   tl.kb_count = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
+  tl.f16 = f16_tile_k(tl.e, tl.rows, p);
   return tl;
 }
 
@@ -260,6 +307,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p) {
     tl.am0 = tl.m0;
     tl.prow0 = 0;
     tl.kb_count = p.num_kb;
+    tl.f16 = 0;
     return tl;
   } else {
     const int per_e = p.m_tiles * p.n_tiles;
@@ -293,6 +341,7 @@ __device__ __forceinline__ Tile decode_tile_pair(int t, const Params& p, uint32_
     tl.am0 = tl.m0;
     tl.prow0 = p.pad_indptr != nullptr ? __ldg(p.pad_indptr + tl.e) : tl.row0;
     tl.kb_count = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
+    tl.f16 = f16_tile_k(tl.e, tl.rows, p);
     return tl;
   }
   const int mt = t / p.n_tiles;
@@ -314,6 +363,7 @@ __device__ __forceinline__ Tile decode_tile_pair(int t, const Params& p, uint32_
   tl.am0 = p.pad_indptr != nullptr ? __ldg(p.pad_indptr + lo) + (tl.m0 - start) : tl.m0;
   tl.prow0 = 0;
   tl.kb_count = p.num_kb;
+  tl.f16 = 0;
   return tl;
 }
 
@@ -595,7 +645,19 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
     // zero rows (all inside the slice that holds the expert's last row, since 16 divides 32).
     // DH1 (two-weight experts, h = max(a, 0)^2): one factor a = dh/da per element ([R, I]) and one
     // gradient da = d a, written as hi/lo into [2R, I]; four output boxes per 16 columns.
+    // fp16 tiles (tl.f16, experts with many rows): the lo rows receive fp16(dg 2^sg), fp16(du 2^sg)
+    // and fp16(w h 2^sh) instead, the hi rows of w h are not written (five boxes per 16 columns),
+    // and the largest scaled magnitudes go to the expert's range words.
     constexpr bool kGated = EP == Epi::DH;
+    const bool f16 = kGated && tl.f16 != 0;
+    float sg = 1.f;
+    if (f16) {
+      int sd = 0;
+      f16_scale_exp(p.f16_words[kF16MaxDy], sd);
+      sg = f16_pow2(sd + kF16DguShift);
+    }
+    const float sh = f16_pow2(kF16HwShift);
+    float mg = 0.f, mh = 0.f;  // largest |scaled dgu| and |scaled w h| of this thread's row
     const long long r = tl.m0 + row_local;
     const long long ro = tl.am0 + row_local;
     const bool pad_row = !row_ok && row_local < ((tl.rows + 15) & ~15);
@@ -638,7 +700,18 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
           if (!kGated && f == 1) continue;
           const uint32_t hi = pack_bf16x2(v[f][0], v[f][1]);
           o[2 * f][i / 2] = hi;
-          o[2 * f + 1][i / 2] = pack_bf16x2(v[f][0] - bf16_lo(hi), v[f][1] - bf16_hi(hi));
+          if (f16) {
+            const float sc = f == 2 ? sh : sg;
+            const float x0 = v[f][0] * sc, x1 = v[f][1] * sc;
+            o[2 * f + 1][i / 2] = pack_f16x2(x0, x1);
+            const float m = row_ok ? fmaxf(fabsf(x0), fabsf(x1)) : 0.f;
+            if (f == 2)
+              mh = fmaxf(mh, m);
+            else
+              mg = fmaxf(mg, m);
+          } else {
+            o[2 * f + 1][i / 2] = pack_bf16x2(v[f][0] - bf16_lo(hi), v[f][1] - bf16_hi(hi));
+          }
         }
       }
       const int n = n0 + c;
@@ -649,7 +722,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
         const uint32_t sw = (lane >> 2) & 1;  // 32-byte swizzle: chunk ^= (row >> 2) & 1
 #pragma unroll
         for (int f = 0; f < 6; ++f) {
-          if (!kGated && (f == 2 || f == 3)) continue;
+          if ((!kGated && (f == 2 || f == 3)) || (f16 && f == 4)) continue;
           const uint32_t row_addr = base + f * kDhBoxBytes + lane * 32;
           st_shared_v4(row_addr + ((0 ^ sw) << 4), make_uint4(o[f][0], o[f][1], o[f][2], o[f][3]));
           st_shared_v4(row_addr + ((1 ^ sw) << 4), make_uint4(o[f][4], o[f][5], o[f][6], o[f][7]));
@@ -664,7 +737,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
             tma_store_2d(tmC0, base + 2 * kDhBoxBytes, p.I + n, y);
             tma_store_2d(tmC0, base + 3 * kDhBoxBytes, p.I + n, yl);
           }
-          tma_store_2d(tmC1, base + 4 * kDhBoxBytes, n, y);
+          if (!f16) tma_store_2d(tmC1, base + 4 * kDhBoxBytes, n, y);
           tma_store_2d(tmC1, base + 5 * kDhBoxBytes, n, yl);
           bulk_commit_group();
         }
@@ -680,7 +753,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
                             p.out2 + rl * two_i + p.I + n, p.hw_out + ro * p.I + n, p.hw_out + rl * p.I + n};
 #pragma unroll
         for (int f = 0; f < 6; ++f) {
-          if (!kGated && (f == 2 || f == 3)) continue;
+          if ((!kGated && (f == 2 || f == 3)) || (f16 && f == 4)) continue;
           reinterpret_cast<uint4*>(dst[f])[0] = make_uint4(o[f][0], o[f][1], o[f][2], o[f][3]);
           reinterpret_cast<uint4*>(dst[f])[1] = make_uint4(o[f][4], o[f][5], o[f][6], o[f][7]);
         }
@@ -698,10 +771,21 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
       }
     }
     if (row_ok) p.gdot[r * (2LL * p.n_tiles) + 2 * tl.nt + colhalf] = part;
+    if (f16 && mode != Rows::None) {
+      // non-negative floats order as their bits
+      const unsigned bg = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(mg));
+      const unsigned bh = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(mh));
+      if (lane == 0) {
+        atomicMax(p.f16_words + kF16Range + tl.e, bg);
+        atomicMax(p.f16_words + kF16Range + p.E + tl.e, bh);
+      }
+    }
   } else {  // ScaleRows, Store: this warp's columns [128 colhalf, 128 colhalf + 128)
     if (mode == Rows::None) return;
     float sc = 1.f;
     if constexpr (EP == Epi::ScaleRows) sc = row_ok ? __ldg(p.row_scale + tl.m0 + row_local) : 0.f;
+    if constexpr (S == Sched::RowsK)
+      if (tl.f16) sc = f16_unscale(p);  // fp16 operands: undo their scales
 #pragma unroll 1
     for (int q = 2 * colhalf; q < 2 * colhalf + 2; ++q) {
       const int col = tl.nt * BN + q * 64;
@@ -768,21 +852,29 @@ __device__ __forceinline__ void prefetch_epilogue_operands(const Tile& tl, int r
 enum class Gather : int { None = 0, A = 1, B = 2 };
 
 // Tiled loads of one stage for the operands that are not gathered (lane 0 of the producer).
-// Every box lands in this CTA's own shared memory and completes on its own full barrier.
+// Every box lands in this CTA's own shared memory and completes on its own full barrier.  An fp16
+// weight-gradient tile (tl.f16) loads one part of each operand: the lo rows of the padded operand
+// (its fp16 part) into the first part's place, and the other operand from tmF (its fp16 copy).
 template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT, bool kLoadA, bool kLoadB>
-__device__ __forceinline__ void load_stage_tiled(const CUtensorMap* tmA, const CUtensorMap* tmB, const Params& p,
-                                                 const Tile& tl, int kb, uint32_t sa, uint32_t sb, uint32_t fb) {
+__device__ __forceinline__ void load_stage_tiled(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmF,
+                                                 const Params& p, const Tile& tl, int kb, uint32_t sa, uint32_t sb,
+                                                 uint32_t fb) {
+  const bool f16 = SPLIT != 0 && tl.f16 != 0;
   if constexpr (kLoadA) {
     if constexpr (!A_MN) {  // RowsM: the tile's rows, in the padded row space when A is a padded operand
       tma_load_2d(sa, tmA, fb, kb * BK, p.pad_a ? tl.am0 : tl.m0);
     } else {
       const int krow = (p.pad_a ? tl.prow0 : tl.row0) + kb * BK;
+      const CUtensorMap* src = (f16 && SPLIT == 2) ? tmF : tmA;
+      const int off = (f16 && SPLIT == 1) ? p.a_split_rows : 0;
 #pragma unroll
-      for (int part = 0; part < (SPLIT == 1 ? 2 : 1); ++part)
+      for (int part = 0; part < (SPLIT == 1 ? 2 : 1); ++part) {
+        if (part > 0 && f16) break;
 #pragma unroll
         for (int i = 0; i < BM / 64; ++i)
-          tma_load_2d(sa + part * A_BYTES + i * MN_BOX_BYTES, tmA, fb, tl.m0 + 64 * i,
-                      krow + part * p.a_split_rows);
+          tma_load_2d(sa + part * A_BYTES + i * MN_BOX_BYTES, src, fb, tl.m0 + 64 * i,
+                      krow + part * p.a_split_rows + off);
+      }
     }
   }
   if constexpr (kLoadB) {
@@ -797,12 +889,16 @@ __device__ __forceinline__ void load_stage_tiled(const CUtensorMap* tmA, const C
     } else {
       const int krow = (S == Sched::RowsM) ? tl.e * p.b_rows_per_expert + kb * BK
                                            : (p.pad_b ? tl.prow0 : tl.row0) + kb * BK;
+      const CUtensorMap* src = (f16 && SPLIT == 1) ? tmF : tmB;
+      const int off = (f16 && SPLIT == 2) ? p.b_split_rows : 0;
 #pragma unroll
-      for (int part = 0; part < (SPLIT == 2 ? 2 : 1); ++part)
+      for (int part = 0; part < (SPLIT == 2 ? 2 : 1); ++part) {
+        if (part > 0 && f16) break;
 #pragma unroll
         for (int i = 0; i < BN / 64; ++i)
-          tma_load_2d(sb + part * B_BYTES + i * MN_BOX_BYTES, tmB, fb, tl.nt * BN + 64 * i,
-                      krow + part * p.b_split_rows);
+          tma_load_2d(sb + part * B_BYTES + i * MN_BOX_BYTES, src, fb, tl.nt * BN + 64 * i,
+                      krow + part * p.b_split_rows + off);
+      }
     }
   }
 }
@@ -812,27 +908,35 @@ __device__ __forceinline__ void load_stage_tiled(const CUtensorMap* tmA, const C
 // address), which expects the bytes of both CTAs.  Gate/up tiles put the gate rows in the even
 // CTA and the up rows in the odd one, so the accumulator columns stay [g | u].
 template <Sched S, Epi EP, bool B_MN, int SPLIT>
-__device__ __forceinline__ void load_stage_pair(const CUtensorMap* tmA, const CUtensorMap* tmB, const Params& p,
-                                                const Tile& tl, int kb, uint32_t sa, uint32_t sb, uint32_t bar,
-                                                uint32_t rank) {
+__device__ __forceinline__ void load_stage_pair(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmF,
+                                                const Params& p, const Tile& tl, int kb, uint32_t sa, uint32_t sb,
+                                                uint32_t bar, uint32_t rank) {
   if constexpr (S == Sched::RowsK) {
     // weight gradients, both operands MN-major with the expert's rows as K: this CTA's 128 M
     // columns of A (two 64-column boxes, hi and lo parts for SPLIT 1) and its 128 of the N
-    // block's 256 columns of B (hi and lo parts for SPLIT 2)
-    const int krow_a = (p.pad_a ? tl.prow0 : tl.row0) + kb * BK;
-    const int krow_b = (p.pad_b ? tl.prow0 : tl.row0) + kb * BK;
+    // block's 256 columns of B (hi and lo parts for SPLIT 2).  fp16 tiles: one part of each, as
+    // in load_stage_tiled.
+    const bool f16 = SPLIT != 0 && tl.f16 != 0;
+    const int krow_a = (p.pad_a ? tl.prow0 : tl.row0) + kb * BK + ((f16 && SPLIT == 1) ? p.a_split_rows : 0);
+    const int krow_b = (p.pad_b ? tl.prow0 : tl.row0) + kb * BK + ((f16 && SPLIT == 2) ? p.b_split_rows : 0);
+    const CUtensorMap* src_a = (f16 && SPLIT == 2) ? tmF : tmA;
+    const CUtensorMap* src_b = (f16 && SPLIT == 1) ? tmF : tmB;
 #pragma unroll
-    for (int part = 0; part < (SPLIT == 1 ? 2 : 1); ++part)
+    for (int part = 0; part < (SPLIT == 1 ? 2 : 1); ++part) {
+      if (part > 0 && f16) break;
 #pragma unroll
       for (int i = 0; i < 2; ++i)
-        tma_load_2d_pair(sa + part * A_BYTES + i * MN_BOX_BYTES, tmA, bar, tl.m0 + 64 * i,
+        tma_load_2d_pair(sa + part * A_BYTES + i * MN_BOX_BYTES, src_a, bar, tl.m0 + 64 * i,
                          krow_a + part * p.a_split_rows);
+    }
 #pragma unroll
-    for (int part = 0; part < (SPLIT == 2 ? 2 : 1); ++part)
+    for (int part = 0; part < (SPLIT == 2 ? 2 : 1); ++part) {
+      if (part > 0 && f16) break;
 #pragma unroll
       for (int i = 0; i < 2; ++i)
-        tma_load_2d_pair(sb + part * (B_BYTES / 2) + i * MN_BOX_BYTES, tmB, bar,
+        tma_load_2d_pair(sb + part * (B_BYTES / 2) + i * MN_BOX_BYTES, src_b, bar,
                          tl.nt * BN + static_cast<int>(rank) * (BN / 2) + 64 * i, krow_b + part * p.b_split_rows);
+    }
     return;
   }
   tma_load_2d_pair(sa, tmA, bar, kb * BK, p.pad_a ? tl.am0 : tl.m0);  // A box: 128 rows (past the end: zeros)
@@ -886,7 +990,7 @@ template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT, Gather G, int CL, in
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
-                        const Params p) {
+                        const __grid_constant__ CUtensorMap tmF, const Params p) {
   using L = LayoutOf<EP, SPLIT, PAIR>;
   constexpr bool kPair = PAIR != 0;
   static_assert(CL == (kPair ? 2 : 1), "clusters exist only as the 2-SM pairs");
@@ -895,6 +999,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 "2-SM pairs: RowsM tiles with K-major A and one operand part, or RowsK tiles, no gather");
   constexpr int STAGES = L::kStages;
   constexpr int STAGE_BYTES = L::kStageBytes;
+  // bytes of a stage's lo part, which an fp16 weight-gradient tile does not load
+  constexpr int LO_BYTES = SPLIT == 1 ? A_BYTES : (SPLIT == 2 ? L::kBBytes / 2 : 0);
   constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CL) - 1u);
   const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
   const bool leader = !kPair || rank == 0;  // the CTA that issues the MMAs
@@ -915,6 +1021,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                          : (G == Gather::A ? (A_MN && SPLIT != 1)
                                                                            : (B_MN && SPLIT != 2))),
                 "RowsM gathers a K-major A; RowsK gathers an MN-major operand held as one part");
+  if (p.f16_role == 2) {
+    // dH refill: leave at once (before any set-up) when no expert with f16 rows has unusable fp16
+    // parts, which is the usual case; the range words are the previous kernel's output
+    griddep_wait();
+    bool need = false;
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x)
+      need = need || (__ldg(p.m_indptr + e + 1) - __ldg(p.m_indptr + e) >= p.f16_rows && !f16_usable(e, p));
+    if (!__syncthreads_or(need ? 1 : 0)) return;
+  }
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -970,6 +1085,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC0);
     tma_prefetch_desc(&tmC1);
+    if (p.f16_role >= 3) tma_prefetch_desc(&tmF);
   }
   if (warp == 1) {
     if constexpr (kPair) {
@@ -1033,6 +1149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tl.am0 = r[7];
       tl.prow0 = r[8];
       tl.kb_count = r[9];
+      tl.f16 = r[10];
       __syncwarp();
       if (lane == 0) mbar_arrive(sempty0 + 8 * slot);
       if (++slot == kSchedSlots) {
@@ -1056,14 +1173,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) return false;
             const uint32_t sa = sbase + stage * STAGE_BYTES;
             const uint32_t fb = full0 + 8 * stage;
+            const int bytes = (SPLIT != 0 && tl.f16) ? STAGE_BYTES - LO_BYTES : STAGE_BYTES;
             if constexpr (kPair) {
               // the even CTA's full barrier counts both CTAs' bytes of this stage
-              if (leader) mbar_arrive_expect_tx(fb, 2 * STAGE_BYTES);
-              load_stage_pair<S, EP, B_MN, SPLIT>(&tmA, &tmB, p, tl, kb, sa, sa + L::kABytes, mapa_shared(fb, 0),
-                                                  rank);
+              if (leader) mbar_arrive_expect_tx(fb, 2 * bytes);
+              load_stage_pair<S, EP, B_MN, SPLIT>(&tmA, &tmB, &tmF, p, tl, kb, sa, sa + L::kABytes,
+                                                  mapa_shared(fb, 0), rank);
             } else {
-              mbar_arrive_expect_tx(fb, STAGE_BYTES);
-              load_stage_tiled<S, EP, A_MN, B_MN, SPLIT, true, true>(&tmA, &tmB, p, tl, kb, sa, sa + L::kABytes, fb);
+              mbar_arrive_expect_tx(fb, bytes);
+              load_stage_tiled<S, EP, A_MN, B_MN, SPLIT, true, true>(&tmA, &tmB, &tmF, p, tl, kb, sa,
+                                                                     sa + L::kABytes, fb);
             }
             if (++stage == STAGES) {
               stage = 0;
@@ -1086,6 +1205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           r[7] = tl.am0;
           r[8] = tl.prow0;
           r[9] = tl.kb_count;
+          r[10] = tl.f16;
           mbar_arrive(sfull0 + 8 * slot);
           if (++slot == kSchedSlots) {
             slot = 0;
@@ -1195,7 +1315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t fb = full0 + 8 * stage;
         if (lane == 0) {
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          load_stage_tiled<S, EP, A_MN, B_MN, SPLIT, !kGA, kGA>(&tmA, &tmB, p, ct, ckb, sa, sb, fb);
+          load_stage_tiled<S, EP, A_MN, B_MN, SPLIT, !kGA, kGA>(&tmA, &tmB, &tmF, p, ct, ckb, sa, sb, fb);
         }
         __syncwarp();
         if constexpr (S == Sched::RowsM) {
@@ -1225,6 +1345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     // pair: M = 256 across the two CTAs (the odd CTA's MMA warp issues nothing)
     constexpr uint32_t idesc = idesc_bf16_f32(kPair ? 2 * BM : BM, BN, A_MN, B_MN);
+    constexpr uint32_t idesc16 = idesc_f16_f32(kPair ? 2 * BM : BM, BN, A_MN, B_MN);
     int stage = 0;
     uint32_t phase = 0;
     uint32_t acc_phase = 0;  // bit a: the phase of accumulator a
@@ -1249,6 +1370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after_sync();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      const bool f16 = SPLIT != 0 && tl.f16 != 0;  // one fp16 MMA per K step
+      const uint32_t id = f16 ? idesc16 : idesc;
       for (int kb = 0; kb < tl.kb_count; ++kb) {
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * stage, phase, abort_flag))) {
           raise_abort(p.err, abort_flag);
@@ -1276,9 +1399,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = B_MN ? smem_desc_sw128(sb + kk * 2048, MN_BOX_BYTES, 1024)
                                      : smem_desc_sw128(sb + kk * 32, 16, 1024);
             if constexpr (kPair)
-              umma_bf16_f32_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              umma_bf16_f32_pair(d_tmem, ad, bd, id, (kb | kk) != 0 ? 1u : 0u);
             else
-              umma_bf16_f32(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              umma_bf16_f32(d_tmem, ad, bd, id, (kb | kk) != 0 ? 1u : 0u);
+            if (f16) continue;
             if constexpr (SPLIT == 1) {  // lo part of A against the same B
               const uint64_t lo = smem_desc_sw128(sa + A_BYTES + kk * 2048, MN_BOX_BYTES, 1024);
               if constexpr (kPair)
@@ -1341,13 +1465,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       if (t < 0 || t >= total) break;
-      // the tile's epilogue operands (DH) start moving into L2 now, a tile's MMA time ahead of use
-      // when the MMAs lead, and at least ahead of the later column chunks when the epilogue does
-      prefetch_epilogue_operands<S, EP>(tl, row_local, colhalf, p);
       if (tl.kb_count == 0) {
         if constexpr (S == Sched::RowsK) store_zero_tile(tl, sub, colhalf, lane, p, zero_row);
         continue;
       }
+      // the tile's epilogue operands (DH) start moving into L2 now, a tile's MMA time ahead of use
+      // when the MMAs lead, and at least ahead of the later column chunks when the epilogue does
+      prefetch_epilogue_operands<S, EP>(tl, row_local, colhalf, p);
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull0 + 8 * acc, (acc_phase >> acc) & 1u, abort_flag))) {
         raise_abort(p.err, abort_flag);
         break;
@@ -1460,6 +1584,10 @@ __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __re
     h_excl = block_exclusive_scan_1024(heavy_m ? pairs : 0, s_warp, lane, warp, &s_total[4]);
   }
   const bool bad = s_bad != 0;
+  if (sb.f16_words != nullptr) {  // s_max is final here (the scans synchronise)
+    for (int i = tid; i < kF16Range + 2 * E; i += blockDim.x)
+      sb.f16_words[i] = (i == kF16Any && !bad && s_max >= kF16Rows) ? 1u : 0u;
+  }
   if (tid < E) {
     sb.tile_prefix[tid] = bad ? 0 : t_excl;
     if (sb.pad_indptr != nullptr) sb.pad_indptr[tid] = bad ? 0 : p_excl;
@@ -1589,7 +1717,7 @@ template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT = 0, Gather G = Gathe
           int PAIR = 0>
 int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc0, const CUtensorMap& tc1,
                 const Params& p, long long tiles, const DeviceInfo& dev, cudaStream_t s, const char* name,
-                bool traced = true) {
+                bool traced = true, const CUtensorMap* tf = nullptr) {
   auto kern = grouped_gemm_kernel<S, EP, A_MN, B_MN, SPLIT, G, CL, PAIR>;
   constexpr int kSmem = LayoutOf<EP, SPLIT, PAIR>::kSmemBytes;
   static std::once_flag once;
@@ -1626,7 +1754,8 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
     grid = static_cast<int>(groups < max_clusters ? groups : max_clusters) * CL;
   }
   KernelScope trace(traced ? name : nullptr, s);  // untraced: one scope of the caller spans both parts of a split
-  if (launch_kernel(kern, dim3(grid), dim3(kThreads), kSmem, s, name, CL, ta, tb, tc0, tc1, p) != cudaSuccess)
+  if (launch_kernel(kern, dim3(grid), dim3(kThreads), kSmem, s, name, CL, ta, tb, tc0, tc1, tf != nullptr ? *tf : ta,
+                    p) != cudaSuccess)
     return LIGER_MOE_ERR_LAUNCH;
   return check_launch(name);
 }
@@ -1914,7 +2043,18 @@ int launch_bwd_dh(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   // 2-SM pairs measured 5 % slower at 512 rows per expert (their 256-row tiles waste rows), and
   // pairs for the heavy experts of a skewed batch (the split of the forward and dX GEMMs) changed
   // nothing (1161-1165 against 1163-1172 us on the Zipf 4096/1024 workload)
-  return launch_gemm<Sched::RowsM, Epi::DH, false, true>(ta, tb, tc0, tc1, p, tiles, dev, s, "gemm_bwd_dh");
+  if (a.f16_words == nullptr)
+    return launch_gemm<Sched::RowsM, Epi::DH, false, true>(ta, tb, tc0, tc1, p, tiles, dev, s, "gemm_bwd_dh");
+  // fp16 weight-gradient operands: the experts with f16_rows rows write fp16 parts; then the
+  // refill pass writes hi / lo parts for those of them whose fp16 parts are unusable (usually none:
+  // its CTAs walk the tile order and leave)
+  p.f16_rows = a.f16_rows;
+  p.f16_words = a.f16_words;
+  p.f16_role = 1;
+  if (int rc = launch_gemm<Sched::RowsM, Epi::DH, false, true>(ta, tb, tc0, tc1, p, tiles, dev, s, "gemm_bwd_dh"))
+    return rc;
+  p.f16_role = 2;
+  return launch_gemm<Sched::RowsM, Epi::DH, false, true>(ta, tb, tc0, tc1, p, tiles, dev, s, "gemm_bwd_dh_refill");
 }
 
 int launch_bwd_dx(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
@@ -1992,6 +2132,16 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.ld_out = a.H;
   p.out_expert_stride = static_cast<long long>(a.nin) * a.H;
   if (make_out_bf16_3d(&tc0, a.dw_gate_up, a.H, nin, a.E)) return LIGER_MOE_ERR_LAUNCH;
+  // fp16 operands (experts with f16_rows rows): the lo rows of dgu hold fp16(dgu 2^sg), x16 the x rows
+  CUtensorMap tf;
+  const CUtensorMap* tfp = nullptr;
+  if (a.f16_words != nullptr && !gather_x && !empty) {
+    if (make_tmap(&tf, a.x16, a.H, rows, 64, BK)) return LIGER_MOE_ERR_LAUNCH;
+    tfp = &tf;
+    p.f16_role = 3;
+    p.f16_rows = a.f16_rows;
+    p.f16_words = a.f16_words;
+  }
   // CTA pairs over neighbouring M blocks (2-SM MMAs, each CTA holding half of the x tile) when the M
   // blocks pair up and experts hold at least kPairRowsDwGu rows on average; below that every CTA
   // works alone on its tile (with few rows per expert the tiles are mostly gradient writes, and a
@@ -2004,12 +2154,13 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
     rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::B>(ta, tb, tc0, tc0, p, tiles_gu, dev, s,
                                                                          "gemm_bwd_dw_gate_up");
   else if (p.m_tiles % 2 == 0 && a.R >= kPairRowsDwGu * a.E)
-    rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::None, 2, 1>(ta, tb, tc0, tc0, p, tiles_gu / 2,
-                                                                                  dev, s, "gemm_bwd_dw_gate_up");
+    rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::None, 2, 1>(
+        ta, tb, tc0, tc0, p, tiles_gu / 2, dev, s, "gemm_bwd_dw_gate_up", true, tfp);
   else
     rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1>(ta, tb, tc0, tc0, p, tiles_gu, dev, s,
-                                                              "gemm_bwd_dw_gate_up");
+                                                              "gemm_bwd_dw_gate_up", true, tfp);
   if (rc) return rc;
+  p.f16_role = 0;
   // dW_d[e] = dY_e^T hw_hi_e + dY_e^T hw_lo_e: each stage holds one A tile (dY rows gathered by
   // token) and both parts of B (rows r and R + r of hw [2R, I]); two MMAs per K step.
   const bool gather_dy = a.dy_perm == nullptr || empty;
@@ -2034,6 +2185,15 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.ld_out = a.I;
   p.out_expert_stride = 1LL * a.H * a.I;
   if (make_out_bf16_3d(&tc0, a.dw_down, a.I, a.H, a.E)) return LIGER_MOE_ERR_LAUNCH;
+  // fp16 operands: the lo rows of hw hold fp16(w h 2^sh), dy16 the dY rows
+  tfp = nullptr;
+  if (a.f16_words != nullptr && !gather_dy) {
+    if (make_tmap(&tf, a.dy16, a.H, rows, 64, BK)) return LIGER_MOE_ERR_LAUNCH;
+    tfp = &tf;
+    p.f16_role = 4;
+    p.f16_rows = a.f16_rows;
+    p.f16_words = a.f16_words;
+  }
   // CTA pairs over neighbouring M blocks (2-SM MMAs, each CTA holding half of the w h tile, 4 stages
   // instead of 2): for every expert when they hold at least kSplitMeanRows rows on average; for the
   // experts with at least kPairRowsDwD rows (the head of the sorted order) when fewer, the others one
@@ -2043,23 +2203,24 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
     return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::A>(ta, tb, tc0, tc0, p, tiles_d, dev, s,
                                                                            "gemm_bwd_dw_down");
   if (p.m_tiles % 2 == 0 && a.R >= kSplitMeanRows * a.E)
-    return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::None, 2, 1>(ta, tb, tc0, tc0, p, tiles_d / 2,
-                                                                                    dev, s, "gemm_bwd_dw_down");
+    return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::None, 2, 1>(
+        ta, tb, tc0, tc0, p, tiles_d / 2, dev, s, "gemm_bwd_dw_down", true, tfp);
   if (p.m_tiles % 2 == 0 && a.T >= kPairRowsDwD) {
     KernelScope trace("gemm_bwd_dw_down", s);
     Params ph = p;
     ph.split_part = 1;
     ph.split_heavy = a.claims + kClaimSlots + 1;
     if (int rc2 = launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::None, 2, 1>(
-            ta, tb, tc0, tc0, ph, tiles_d / 2, dev, s, "gemm_bwd_dw_down", false))
+            ta, tb, tc0, tc0, ph, tiles_d / 2, dev, s, "gemm_bwd_dw_down", false, tfp))
       return rc2;
     Params pl = p;
     pl.split_part = 2;
     pl.split_heavy = ph.split_heavy;
     return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2>(ta, tb, tc0, tc0, pl, tiles_d, dev, s,
-                                                                "gemm_bwd_dw_down", false);
+                                                                "gemm_bwd_dw_down", false, tfp);
   }
-  return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2>(ta, tb, tc0, tc0, p, tiles_d, dev, s, "gemm_bwd_dw_down");
+  return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2>(ta, tb, tc0, tc0, p, tiles_d, dev, s, "gemm_bwd_dw_down",
+                                                              true, tfp);
 }
 
 }  // namespace lmoe

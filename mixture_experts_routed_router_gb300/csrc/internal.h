@@ -48,6 +48,55 @@ int launch_dispatch(const int32_t* ids, const float* w, const uint16_t* x, int T
 int launch_scatter_rows(const uint16_t* src, const int32_t* slot_to_row, int T, int H, int k, uint16_t* dst,
                         const DeviceInfo& dev, cudaStream_t s);
 
+// ---------------------------------------------------------------- fp16 weight-gradient operands
+// Experts with at least f16 rows (kF16Rows) take their weight gradients in one fp16 MMA per K step
+// instead of two bf16 ones (the hi and lo parts): x and dY rows as fp16(v 2^s) with s from the
+// tensor's largest magnitude, and the dH epilogue's dgu and w h as fp16 with fixed offsets from
+// those scales.  An expert whose fp16 parts fall outside their window (f16_in_range) falls back
+// to the hi / lo parts, which a second dH pass then writes.  Words in the backward's workspace:
+//   [kF16MaxX]  largest |x| (float bits),  [kF16MaxDy] largest |dY|,  [kF16Any] 1 when some
+//   expert has at least f16 rows,  [kF16Range + e] / [kF16Range + E + e] largest |scaled dgu| /
+//   |scaled w h| of expert e (float bits; atomicMax of the dH epilogue).
+constexpr int kF16Rows = 384;
+constexpr long long kF16MinR = 4096;  // routed rows below which the backward never takes the fp16 pass
+constexpr int kF16MaxX = 0, kF16MaxDy = 1, kF16Any = 2, kF16Range = 4;
+constexpr int kF16DguShift = -6;  // dgu scaled by 2^(s_dY - 6)
+constexpr int kF16HwShift = 4;    // w h scaled by 2^4
+inline size_t f16_words_bytes(int E) { return ((static_cast<size_t>(kF16Range) + 2 * E) * 4 + 255) / 256 * 256; }
+// The largest |dY| and |x| (x read as x_perm[slot_to_row[t k]]) into words zeroed, and [kF16Any]
+// set, by the schedule kernel (ScheduleBufs::f16_words).
+int launch_f16_prep(const uint16_t* dy, const uint16_t* x_perm, const int32_t* slot_to_row, int T, int H, int k,
+                    unsigned* words, const DeviceInfo& dev, cudaStream_t s);
+// The backward's row copies in one launch: dy_perm[r, :] = dY[token of r, :] (bf16) with dy16[r, :]
+// = fp16(dY[token of r, :] 2^s_dY), and x16[r, :] = fp16(x_perm[r, :] 2^s_x) (x_perm read once per
+// token); the fp16 copies only when words[kF16Any] is set and the scales exist, and only for the rows
+// the fp16 weight-gradient tiles read (experts with kF16Rows rows and the 15 rows after each).
+int launch_scatter_rows_f16(const uint16_t* dy, const uint16_t* x_perm, const int32_t* slot_to_row, int T, int H,
+                            int k, const int32_t* m_indptr, int E, uint16_t* dy_perm, uint16_t* dy16, uint16_t* x16,
+                            const unsigned* words, const DeviceInfo& dev, cudaStream_t s);
+
+#ifdef __CUDACC__
+// 2^s as a float (s in [-126, 127]).
+__device__ __forceinline__ float f16_pow2(int s) { return __uint_as_float(static_cast<unsigned>(127 + s) << 23); }
+// The scale exponent s of a tensor whose largest magnitude has the float bits m: m 2^s in
+// [2^14, 2^15), so every value within 2^28 of m keeps its full precision in fp16.  false when m is
+// not finite or outside [2^-40, 2^41) (the fp16 operands are then not used); m = 0 gives s = 0.
+__device__ __forceinline__ bool f16_scale_exp(unsigned m, int& s) {
+  s = 0;
+  if (m == 0u) return true;
+  const int ex = static_cast<int>(m >> 23) - 127;  // m >= 0: no sign bit
+  if (ex < -40 || ex > 40) return false;
+  s = 14 - ex;
+  return true;
+}
+// The window of an fp16 part's largest scaled magnitude: below 65504 (no overflow) and at least
+// 2^-6, so that values down to 2^-8 of it are normal fp16 numbers.
+__device__ __forceinline__ bool f16_in_range(unsigned m) {
+  const float f = __uint_as_float(m);
+  return f >= 0.015625f && f < 65504.f;
+}
+#endif
+
 // y[t, :] = bf16(sum_j y_perm[slot_to_row[t*k+j], :]).
 int launch_combine(const uint16_t* y_perm, const int32_t* slot_to_row, int T, int H, int k, uint16_t* y,
                    const DeviceInfo& dev, cudaStream_t s);
@@ -93,6 +142,9 @@ struct ScheduleBufs {
   int32_t* order = nullptr;
   int32_t* order_info = nullptr;
   int* claims = nullptr;
+  // the backward's fp16 operand words (kF16Range + 2E of them), or NULL: zeroed, and [kF16Any] set
+  // when some expert has at least kF16Rows rows
+  unsigned* f16_words = nullptr;
 };
 constexpr int kClaimSlots = 8;
 // Claim counters of the launches that may use the dynamic order: the weight-gradient GEMMs.
@@ -160,6 +212,13 @@ struct BwdGemmArgs {
   long long R_pad;
   uint16_t* hw_perm;     // [2 R_pad, I]: hi rows bf16(w h), then lo rows bf16(w h - hi)
   uint16_t* dgu;         // [2 R_pad, 2I]: hi rows bf16(dgu), then lo rows bf16(dgu - hi)
+  // fp16 weight-gradient operands (f16_words != NULL): x16 / dy16 [R, H] fp16 copies of x_perm and
+  // dy_perm; an expert with at least f16_rows rows gets fp16(dgu 2^sg) and fp16(w h 2^sh) in the
+  // lo rows of dgu and hw_perm instead of lo parts (the hi rows stay bf16 for the dX GEMM).
+  const uint16_t* x16 = nullptr;
+  const uint16_t* dy16 = nullptr;
+  unsigned* f16_words = nullptr;
+  int f16_rows = 0;
   uint16_t* dx_perm;     // [R, H]
   float* gdot;           // [R, ceil(I / 256)]
   uint16_t* dw_gate_up;  // [E, 2I, H]

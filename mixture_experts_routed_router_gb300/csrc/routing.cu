@@ -394,6 +394,159 @@ __global__ void __launch_bounds__(256) scatter_rows_kernel(const uint16_t* __res
 }
 
 // ============================================================================
+// fp16 operands of the weight gradients (experts with many rows): the largest |dY| and |x| of the
+// step, then fp16 copies of the token rows scaled by a power of two from them.
+// ============================================================================
+// |v| of the eight bf16 values of a 16-byte chunk, as the largest bf16 magnitude bits.
+__device__ __forceinline__ unsigned absmax_bf16x8(const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  unsigned m = 0u;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+  return m;
+}
+
+// Largest |dY| and |x| (token t's x row read as x_perm[slot_to_row[t k]]) into words[kF16MaxDy],
+// words[kF16MaxX] (float bits; a bf16 NaN gives NaN bits, which disable the fp16 operands).  The
+// words were zeroed by the schedule kernel, which also set words[kF16Any]; without an expert of
+// f16 rows nothing is done.  Work item = (token, segment), as in the row copy.
+__global__ void __launch_bounds__(256) f16_prep_kernel(const uint16_t* __restrict__ dy,
+                                                       const uint16_t* __restrict__ x_perm,
+                                                       const int32_t* __restrict__ slot_to_row, int T, int H, int k,
+                                                       long long R, unsigned* words, int* err) {
+  __shared__ unsigned s_max[2];
+  griddep_wait();
+  griddep_launch_dependents();
+  if (words[kF16Any] == 0u) return;
+  if (threadIdx.x < 2) s_max[threadIdx.x] = 0u;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const int chunks = H >> 3;
+  const int nseg = (chunks + kScatterSeg - 1) / kScatterSeg;
+  const long long items = static_cast<long long>(T) * nseg;
+  unsigned md = 0u, mx = 0u;
+  for (long long it = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; it < items;
+       it += nwarps) {
+    const long long t = it / nseg;
+    const int seg = static_cast<int>(it - t * nseg);
+    const int row = __ldg(slot_to_row + t * k);
+    if (static_cast<unsigned long long>(row) >= static_cast<unsigned long long>(R)) {
+      if (lane == 0 && seg == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_ROW);
+      continue;
+    }
+    const int c0 = seg * kScatterSeg + lane;
+    const uint4* a = reinterpret_cast<const uint4*>(dy + static_cast<size_t>(t) * H);
+    const uint4* b = reinterpret_cast<const uint4*>(x_perm + static_cast<size_t>(row) * H);
+#pragma unroll
+    for (int q = 0; q < kScatterLaneChunks; ++q)
+      if (c0 + 32 * q < chunks) {
+        md = max(md, absmax_bf16x8(__ldg(a + c0 + 32 * q)));
+        mx = max(mx, absmax_bf16x8(__ldg(b + c0 + 32 * q)));
+      }
+  }
+  md = __reduce_max_sync(kFull, md);
+  mx = __reduce_max_sync(kFull, mx);
+  if (lane == 0) {
+    atomicMax(&s_max[0], md);
+    atomicMax(&s_max[1], mx);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    atomicMax(words + kF16MaxDy, s_max[0] << 16);  // bf16 magnitude bits -> float bits
+    atomicMax(words + kF16MaxX, s_max[1] << 16);
+  }
+}
+
+// Two row copies in one launch (blockIdx.y picks the job): dst16[slot_to_row[t k + j], :] =
+// fp16(row_t 2^s) for j < k, and the plain bf16 copy into dst when dst is set; row_t = src[t, :]
+// or, with src_rows, src_rows[slot_to_row[t k], :].  The fp16 copy is written only when
+// words[kF16Any] is set and words[max_word] gives a scale (f16_scale_exp), and only for the rows
+// the fp16 weight-gradient tiles read: those of experts with at least f16_rows rows, and the 15
+// rows after each of them (the last 16-row K step of such an expert reaches up to 15 rows into the
+// next experts; its padded operand is zero there, so those rows must hold finite values).
+// Scaling by a power of two is exact.
+struct RowCopyF16 {
+  const uint16_t* src;
+  const uint16_t* src_rows;
+  uint16_t* dst;
+  uint16_t* dst16;
+  int max_word;
+};
+
+// Expert holding row r: the largest e with m_indptr[e] <= r (empty experts repeat a value).
+__device__ __forceinline__ int expert_of_row(const int32_t* __restrict__ m_indptr, int E, int r) {
+  int lo = 0, hi = E;  // m_indptr[lo] <= r < m_indptr[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(m_indptr + mid) <= r)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(256) scatter_rows_f16_kernel(RowCopyF16 j0, RowCopyF16 j1,
+                                                               const int32_t* __restrict__ slot_to_row, int T, int H,
+                                                               int k, long long R, const int32_t* __restrict__ m_indptr,
+                                                               int E, int f16_rows, const unsigned* words, int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const RowCopyF16 job = blockIdx.y == 0 ? j0 : j1;
+  int sexp = 0;
+  const bool f16 = job.dst16 != nullptr && words[kF16Any] != 0u && f16_scale_exp(words[job.max_word], sexp);
+  if (!f16 && job.dst == nullptr) return;
+  const float sc = f16_pow2(sexp);
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const int chunks = H >> 3;
+  const int nseg = (chunks + kScatterSeg - 1) / kScatterSeg;
+  const long long items = static_cast<long long>(T) * nseg;
+  for (long long it = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; it < items;
+       it += nwarps) {
+    const long long t = it / nseg;
+    const int seg = static_cast<int>(it - t * nseg);
+    const int my_row = (lane < k) ? __ldg(slot_to_row + t * k + lane) : 0;
+    const bool bad = lane < k && static_cast<unsigned long long>(my_row) >= static_cast<unsigned long long>(R);
+    if (__any_sync(kFull, bad)) {
+      if (lane == 0 && seg == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_ROW);
+      continue;
+    }
+    const int c0 = seg * kScatterSeg + lane;
+    const int first = __shfl_sync(kFull, my_row, 0);
+    bool need = false;  // lane j < k: row my_row is read by an fp16 tile
+    if (f16 && lane < k) {
+      const auto heavy = [&](int e) { return __ldg(m_indptr + e + 1) - __ldg(m_indptr + e) >= f16_rows; };
+      need = heavy(expert_of_row(m_indptr, E, my_row)) ||
+             (my_row >= 15 && heavy(expert_of_row(m_indptr, E, my_row - 15)));
+    }
+    const unsigned need_mask = __ballot_sync(kFull, need);
+    const uint4* a = reinterpret_cast<const uint4*>(
+        job.src_rows != nullptr ? job.src_rows + static_cast<size_t>(first) * H : job.src + static_cast<size_t>(t) * H);
+    uint4 v[kScatterLaneChunks], h[kScatterLaneChunks];
+#pragma unroll
+    for (int q = 0; q < kScatterLaneChunks; ++q)
+      if (c0 + 32 * q < chunks) {
+        v[q] = __ldg(a + c0 + 32 * q);
+        uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = pack_f16x2(bf16_lo(w[i]) * sc, bf16_hi(w[i]) * sc);
+        h[q] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    for (int j = 0; j < k; ++j) {
+      const size_t r = static_cast<size_t>(__shfl_sync(kFull, my_row, j & 31));
+#pragma unroll
+      for (int q = 0; q < kScatterLaneChunks; ++q)
+        if (c0 + 32 * q < chunks) {
+          if (job.dst != nullptr) __stcs(reinterpret_cast<uint4*>(job.dst + r * H) + c0 + 32 * q, v[q]);
+          if ((need_mask >> j) & 1u) __stcs(reinterpret_cast<uint4*>(job.dst16 + r * H) + c0 + 32 * q, h[q]);
+        }
+    }
+  }
+}
+
+// ============================================================================
 // Combine.  LigerCute README, "Forward pass" (final local combine);
 // LightMoE README, "Highlights" (deterministic combine).
 //   y[t, :] = bf16( sum_{j=0..k-1} y_perm[slot_to_row[t*k + j], :] )  (fp32, j ascending)
@@ -611,6 +764,34 @@ int launch_scatter_rows(const uint16_t* src, const int32_t* slot_to_row, int T, 
                   slot_to_row, T, H, k, static_cast<long long>(T) * k, dst, dev.err_flag);
   }
   return check_launch("gather_rows");
+}
+
+int launch_f16_prep(const uint16_t* dy, const uint16_t* x_perm, const int32_t* slot_to_row, int T, int H, int k,
+                    unsigned* words, const DeviceInfo& dev, cudaStream_t s) {
+  if (T == 0) return LIGER_MOE_OK;
+  {
+    KernelScope trace("f16_prep", s);
+    const long long items = static_cast<long long>(T) * ((H / 8 + kScatterSeg - 1) / kScatterSeg);
+    launch_kernel(f16_prep_kernel, dim3(grid_for_warps(items, 8, dev)), dim3(256), 0, s, "f16_prep", 1, dy, x_perm,
+                  slot_to_row, T, H, k, static_cast<long long>(T) * k, words, dev.err_flag);
+  }
+  return check_launch("f16_prep");
+}
+
+int launch_scatter_rows_f16(const uint16_t* dy, const uint16_t* x_perm, const int32_t* slot_to_row, int T, int H,
+                            int k, const int32_t* m_indptr, int E, uint16_t* dy_perm, uint16_t* dy16, uint16_t* x16,
+                            const unsigned* words, const DeviceInfo& dev, cudaStream_t s) {
+  if (T == 0) return LIGER_MOE_OK;
+  const RowCopyF16 j0{dy, nullptr, dy_perm, dy16, kF16MaxDy};
+  const RowCopyF16 j1{nullptr, x_perm, nullptr, x16, kF16MaxX};
+  {
+    KernelScope trace("gather_rows_f16", s);
+    const long long items = static_cast<long long>(T) * ((H / 8 + kScatterSeg - 1) / kScatterSeg);
+    launch_kernel(scatter_rows_f16_kernel, dim3(grid_for_warps(items, 8, dev), 2), dim3(256), 0, s,
+                  "gather_rows_f16", 1, j0, j1, slot_to_row, T, H, k, static_cast<long long>(T) * k, m_indptr, E,
+                  kF16Rows, words, dev.err_flag);
+  }
+  return check_launch("gather_rows_f16");
 }
 
 int launch_combine(const uint16_t* y_perm, const int32_t* slot_to_row, int T, int H, int k, uint16_t* y,

@@ -1,6 +1,21 @@
-"""Moving test inputs between numpy (bf16 as uint16 bits) and CUDA tensors."""
+"""Moving test inputs between numpy (bf16 as uint16 bits) and CUDA tensors; the library's
+process-wide weight-gradient precision switch as a context manager."""
+import contextlib
+
 import numpy as np
 import torch
+
+import mixture_experts_routed_router_gb300 as moe
+
+
+@contextlib.contextmanager
+def dw_fp16(on: bool):
+    """Heavy experts' weight gradients in one fp16 pass (on) or as bf16 hi + lo parts, restoring the default."""
+    moe.set_dw_fp16(on)
+    try:
+        yield
+    finally:
+        moe.set_dw_fp16(True)
 
 
 def to_dev(a: np.ndarray, dtype=None) -> torch.Tensor:
