@@ -155,11 +155,13 @@ struct Params {
   const int32_t* sched_info;    // [E][4]: expert, first row, rows, first padded row of each sorted expert
   const int* sched_skewed;
   int* claims;
-  // Heavy / light split of dW_down (split_part != 0): the experts of the sorted
-  // order are split at *split_heavy (the count with at least the pair threshold's rows); part 1
-  // takes the first *split_heavy of them (2-SM pairs), part 2 the rest (one CTA per tile).
-  const int* split_heavy;
-  int split_part;
+  // Weight gradients in parts (parted != 0): this launch takes the experts at positions
+  // [*part_begin, *part_end) of the sorted order (NULL: 0 / E), counts the schedule kernel wrote
+  // (experts with at least the fp16 or the pair threshold's rows, which lead the order); else
+  // every expert, in id order (static) or sorted (dynamic).
+  int parted;
+  const int* part_begin;
+  const int* part_end;
   // Logits: fp32 output [R, N_out] (row stride ld_out), optional bias [N_out]; out_tma: 32-column
   // chunks leave through TMA boxes (N_out a multiple of 32), else by masked direct stores
   float* out_f32;
@@ -171,11 +173,14 @@ struct Params {
   //     (and no hi rows of w h), and the largest magnitudes into the range words;
   //   DH, role 2 (refill): only those experts whose fp16 parts are unusable (f16_usable), with
   //     hi / lo parts;
-  //   RowsK, role 3 (dW_gate_up) / 4 (dW_down): the tiles of experts with usable fp16 parts take
-  //     one fp16 MMA per K step, the lo rows of the padded operand against the fp16 token rows
-  //     (tensor map tmF), and scale the result back by the inverse powers of two.
+  //   RowsK, role 3 (dW_gate_up) / 4 (dW_down), in the launch of those experts (f16_part, one
+  //     operand part per stage): an expert with usable fp16 parts takes one fp16 MMA per K step,
+  //     the lo rows of the padded operand against the fp16 token rows (tensor map tmF), and
+  //     scales the result back by the inverse powers of two; an expert without takes its hi and lo
+  //     parts as two passes over its K blocks (bf16).
   int f16_role;
   int f16_rows;
+  int f16_part;
   unsigned* f16_words;
   int* err;
 };
@@ -201,9 +206,28 @@ __device__ __forceinline__ bool f16_usable(int e, const Params& p) {
          f16_in_range(p.f16_words[kF16Range + p.E + e]);
 }
 
-// fp16 tile of a weight-gradient GEMM: an expert with f16_rows rows and usable fp16 parts.
-__device__ __forceinline__ int f16_tile_k(int e, int rows, const Params& p) {
-  return (p.f16_role >= 3 && rows >= p.f16_rows && f16_usable(e, p)) ? 1 : 0;
+// K blocks and precision of a weight-gradient tile of expert tl.e with tl.rows rows: in the fp16
+// experts' launch, one fp16 pass (usable parts) or the hi and lo parts as two passes over the K
+// blocks; elsewhere the template's own operand parts.
+__device__ __forceinline__ void rows_k_finish(Tile& tl, const Params& p) {
+  tl.kb_count = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
+  tl.f16 = 0;
+  if (p.f16_part) {
+    tl.f16 = f16_usable(tl.e, p) ? 1 : 0;
+    if (!tl.f16) tl.kb_count *= 2;
+  }
+}
+
+// The experts of a parted launch: positions [part_lo, part_hi) of the sorted order.
+__device__ __forceinline__ int part_lo(const Params& p) { return p.part_begin != nullptr ? __ldg(p.part_begin) : 0; }
+__device__ __forceinline__ int part_hi(const Params& p) { return p.part_end != nullptr ? __ldg(p.part_end) : p.E; }
+// Expert of position i of a launch's static order: the sorted order inside a part that leaves some
+// experts out, else the id order (a part holding every expert keeps it: measured faster for the
+// uniform loads, where the sorted order only shuffles equal experts).
+__device__ __forceinline__ int static_expert(int i, const Params& p) {
+  if (!p.parted) return i;
+  const int lo = part_lo(p);
+  return (lo == 0 && part_hi(p) == p.E) ? i : __ldg(p.sched_order + lo + i);
 }
 
 // The factor that undoes the fp16 operands' scales in a weight gradient: 2^-(s_x + s_g) for
@@ -252,8 +276,7 @@ __device__ __forceinline__ Tile rows_k_tile(int e, int r, const Params& p) {
   tl.rows = __ldg(p.m_indptr + e + 1) - tl.row0;
   tl.am0 = tl.m0;
   tl.prow0 = p.pad_indptr != nullptr ? __ldg(p.pad_indptr + e) : tl.row0;
-  tl.kb_count = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
-  tl.f16 = f16_tile_k(e, tl.rows, p);
+  rows_k_finish(tl, p);
   return tl;
 }
 
@@ -268,8 +291,7 @@ __device__ __forceinline__ Tile rows_k_tile_info(int4 q, int r, const Params& p)
   tl.rows = q.z;
   tl.am0 = tl.m0;
   tl.prow0 = q.w;
-  tl.kb_count = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
-  tl.f16 = f16_tile_k(tl.e, tl.rows, p);
+  rows_k_finish(tl, p);
   return tl;
 }
 
@@ -312,10 +334,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p) {
   } else {
     const int per_e = p.m_tiles * p.n_tiles;
     const int i = t / per_e;
-    // the sorted order from the split's first expert (dynamic order or a heavy / light part)
-    const int base = p.split_part == 2 ? __ldg(p.split_heavy) : 0;
-    const int e = p.split_part != 0 ? __ldg(p.sched_order + base + i) : i;
-    return rows_k_tile(e, t - i * per_e, p);
+    return rows_k_tile(static_expert(i, p), t - i * per_e, p);
   }
 }
 
@@ -331,7 +350,7 @@ __device__ __forceinline__ Tile decode_tile_pair(int t, const Params& p, uint32_
     const int mpt = p.m_tiles / 2;
     const int per_e = mpt * p.n_tiles;
     const int i = t / per_e;
-    tl.e = p.split_part != 0 ? __ldg(p.sched_order + i) : i;  // the heavy part: the first sorted experts
+    tl.e = static_expert(i, p);
     const int r = t - i * per_e;
     tl.nt = r / mpt;
     const int mp = r - tl.nt * mpt;
@@ -340,8 +359,7 @@ __device__ __forceinline__ Tile decode_tile_pair(int t, const Params& p, uint32_
     tl.rows = __ldg(p.m_indptr + tl.e + 1) - tl.row0;
     tl.am0 = tl.m0;
     tl.prow0 = p.pad_indptr != nullptr ? __ldg(p.pad_indptr + tl.e) : tl.row0;
-    tl.kb_count = tl.rows > 0 ? (tl.rows + BK - 1) / BK : 0;
-    tl.f16 = f16_tile_k(tl.e, tl.rows, p);
+    rows_k_finish(tl, p);
     return tl;
   }
   const int mt = t / p.n_tiles;
@@ -851,30 +869,53 @@ __device__ __forceinline__ void prefetch_epilogue_operands(const Tile& tl, int r
 // M), RowsK an MN-major operand (rows = K).
 enum class Gather : int { None = 0, A = 1, B = 2 };
 
+// Where K block kb of a weight-gradient tile comes from.  In the fp16 experts' launch (f16_part,
+// one operand part per stage): an fp16 tile reads the lo rows of the padded operand (its fp16 part,
+// row offset a_split_rows for dW_gate_up's A, b_split_rows for dW_down's B) and the other operand
+// from tmF (the fp16 token rows); a two-pass tile reads K block kbe = kb of the hi rows, then
+// kbe = kb - n of the lo rows, against the bf16 token rows.  Elsewhere: block kb, tmA and tmB.
+struct KbSource {
+  int kbe;           // K block within the expert's rows
+  int off_a, off_b;  // row offsets of A and B
+  bool a_f16, b_f16; // A / B from tmF
+};
+__device__ __forceinline__ KbSource kb_source(const Tile& tl, int kb, const Params& p) {
+  KbSource q{kb, 0, 0, false, false};
+  if (!p.f16_part) return q;
+  const bool gu = p.f16_role == 3;  // the padded operand: A (dW_gate_up) or B (dW_down)
+  bool lo = tl.f16 != 0;
+  if (!lo) {
+    const int n = tl.kb_count / 2;
+    lo = kb >= n;
+    if (lo) q.kbe = kb - n;
+  } else if (gu) {
+    q.b_f16 = true;
+  } else {
+    q.a_f16 = true;
+  }
+  if (lo) (gu ? q.off_a : q.off_b) = gu ? p.a_split_rows : p.b_split_rows;
+  return q;
+}
+
 // Tiled loads of one stage for the operands that are not gathered (lane 0 of the producer).
-// Every box lands in this CTA's own shared memory and completes on its own full barrier.  An fp16
-// weight-gradient tile (tl.f16) loads one part of each operand: the lo rows of the padded operand
-// (its fp16 part) into the first part's place, and the other operand from tmF (its fp16 copy).
+// Every box lands in this CTA's own shared memory and completes on its own full barrier.
 template <Sched S, Epi EP, bool A_MN, bool B_MN, int SPLIT, bool kLoadA, bool kLoadB>
 __device__ __forceinline__ void load_stage_tiled(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmF,
                                                  const Params& p, const Tile& tl, int kb, uint32_t sa, uint32_t sb,
                                                  uint32_t fb) {
-  const bool f16 = SPLIT != 0 && tl.f16 != 0;
+  const KbSource q = S == Sched::RowsK ? kb_source(tl, kb, p) : KbSource{kb, 0, 0, false, false};
   if constexpr (kLoadA) {
     if constexpr (!A_MN) {  // RowsM: the tile's rows, in the padded row space when A is a padded operand
       tma_load_2d(sa, tmA, fb, kb * BK, p.pad_a ? tl.am0 : tl.m0);
     } else {
-      const int krow = (p.pad_a ? tl.prow0 : tl.row0) + kb * BK;
-      const CUtensorMap* src = (f16 && SPLIT == 2) ? tmF : tmA;
-      const int off = (f16 && SPLIT == 1) ? p.a_split_rows : 0;
+      const int krow = (p.pad_a ? tl.prow0 : tl.row0) + q.kbe * BK + q.off_a;
+      const CUtensorMap* src = q.a_f16 ? tmF : tmA;
 #pragma unroll
-      for (int part = 0; part < (SPLIT == 1 ? 2 : 1); ++part) {
-        if (part > 0 && f16) break;
+      for (int part = 0; part < (SPLIT == 1 ? 2 : 1); ++part)
 #pragma unroll
         for (int i = 0; i < BM / 64; ++i)
           tma_load_2d(sa + part * A_BYTES + i * MN_BOX_BYTES, src, fb, tl.m0 + 64 * i,
-                      krow + part * p.a_split_rows + off);
-      }
+                      krow + part * p.a_split_rows);
     }
   }
   if constexpr (kLoadB) {
@@ -888,17 +929,14 @@ __device__ __forceinline__ void load_stage_tiled(const CUtensorMap* tmA, const C
       }
     } else {
       const int krow = (S == Sched::RowsM) ? tl.e * p.b_rows_per_expert + kb * BK
-                                           : (p.pad_b ? tl.prow0 : tl.row0) + kb * BK;
-      const CUtensorMap* src = (f16 && SPLIT == 1) ? tmF : tmB;
-      const int off = (f16 && SPLIT == 2) ? p.b_split_rows : 0;
+                                           : (p.pad_b ? tl.prow0 : tl.row0) + q.kbe * BK + q.off_b;
+      const CUtensorMap* src = q.b_f16 ? tmF : tmB;
 #pragma unroll
-      for (int part = 0; part < (SPLIT == 2 ? 2 : 1); ++part) {
-        if (part > 0 && f16) break;
+      for (int part = 0; part < (SPLIT == 2 ? 2 : 1); ++part)
 #pragma unroll
         for (int i = 0; i < BN / 64; ++i)
           tma_load_2d(sb + part * B_BYTES + i * MN_BOX_BYTES, src, fb, tl.nt * BN + 64 * i,
-                      krow + part * p.b_split_rows + off);
-      }
+                      krow + part * p.b_split_rows);
     }
   }
 }
@@ -914,29 +952,25 @@ __device__ __forceinline__ void load_stage_pair(const CUtensorMap* tmA, const CU
   if constexpr (S == Sched::RowsK) {
     // weight gradients, both operands MN-major with the expert's rows as K: this CTA's 128 M
     // columns of A (two 64-column boxes, hi and lo parts for SPLIT 1) and its 128 of the N
-    // block's 256 columns of B (hi and lo parts for SPLIT 2).  fp16 tiles: one part of each, as
-    // in load_stage_tiled.
-    const bool f16 = SPLIT != 0 && tl.f16 != 0;
-    const int krow_a = (p.pad_a ? tl.prow0 : tl.row0) + kb * BK + ((f16 && SPLIT == 1) ? p.a_split_rows : 0);
-    const int krow_b = (p.pad_b ? tl.prow0 : tl.row0) + kb * BK + ((f16 && SPLIT == 2) ? p.b_split_rows : 0);
-    const CUtensorMap* src_a = (f16 && SPLIT == 2) ? tmF : tmA;
-    const CUtensorMap* src_b = (f16 && SPLIT == 1) ? tmF : tmB;
+    // block's 256 columns of B (hi and lo parts for SPLIT 2).  The fp16 experts' launch: as
+    // kb_source says.
+    const KbSource q = kb_source(tl, kb, p);
+    const int krow_a = (p.pad_a ? tl.prow0 : tl.row0) + q.kbe * BK + q.off_a;
+    const int krow_b = (p.pad_b ? tl.prow0 : tl.row0) + q.kbe * BK + q.off_b;
+    const CUtensorMap* src_a = q.a_f16 ? tmF : tmA;
+    const CUtensorMap* src_b = q.b_f16 ? tmF : tmB;
 #pragma unroll
-    for (int part = 0; part < (SPLIT == 1 ? 2 : 1); ++part) {
-      if (part > 0 && f16) break;
+    for (int part = 0; part < (SPLIT == 1 ? 2 : 1); ++part)
 #pragma unroll
       for (int i = 0; i < 2; ++i)
         tma_load_2d_pair(sa + part * A_BYTES + i * MN_BOX_BYTES, src_a, bar, tl.m0 + 64 * i,
                          krow_a + part * p.a_split_rows);
-    }
 #pragma unroll
-    for (int part = 0; part < (SPLIT == 2 ? 2 : 1); ++part) {
-      if (part > 0 && f16) break;
+    for (int part = 0; part < (SPLIT == 2 ? 2 : 1); ++part)
 #pragma unroll
       for (int i = 0; i < 2; ++i)
         tma_load_2d_pair(sb + part * (B_BYTES / 2) + i * MN_BOX_BYTES, src_b, bar,
                          tl.nt * BN + static_cast<int>(rank) * (BN / 2) + 64 * i, krow_b + part * p.b_split_rows);
-    }
     return;
   }
   tma_load_2d_pair(sa, tmA, bar, kb * BK, p.pad_a ? tl.am0 : tl.m0);  // A box: 128 rows (past the end: zeros)
@@ -999,8 +1033,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 "2-SM pairs: RowsM tiles with K-major A and one operand part, or RowsK tiles, no gather");
   constexpr int STAGES = L::kStages;
   constexpr int STAGE_BYTES = L::kStageBytes;
-  // bytes of a stage's lo part, which an fp16 weight-gradient tile does not load
-  constexpr int LO_BYTES = SPLIT == 1 ? A_BYTES : (SPLIT == 2 ? L::kBBytes / 2 : 0);
   constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CL) - 1u);
   const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
   const bool leader = !kPair || rank == 0;  // the CTA that issues the MMAs
@@ -1115,8 +1147,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   else if constexpr (S == Sched::Dense)
     total = static_cast<int>((p.R + BM - 1) / BM) * p.n_tiles;
   else
-    total = (p.split_part == 0 ? p.E : (p.split_part == 1 ? __ldg(p.split_heavy) : p.E - __ldg(p.split_heavy))) *
-            (kPair ? p.m_tiles / 2 : p.m_tiles) * p.n_tiles;  // experts of the part x tiles (pair: M blocks two at a time)
+    total = (p.parted ? part_hi(p) - part_lo(p) : p.E) * (kPair ? p.m_tiles / 2 : p.m_tiles) *
+            p.n_tiles;  // experts of the part x tiles (pair: M blocks two at a time)
 
   // The tile sequence of the MMA warp and the epilogue warps: the tile at queue position t (t < 0 or
   // past the launch's tiles ends it) and its accumulator.  In the static order every warp walks
@@ -1173,14 +1205,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) return false;
             const uint32_t sa = sbase + stage * STAGE_BYTES;
             const uint32_t fb = full0 + 8 * stage;
-            const int bytes = (SPLIT != 0 && tl.f16) ? STAGE_BYTES - LO_BYTES : STAGE_BYTES;
             if constexpr (kPair) {
               // the even CTA's full barrier counts both CTAs' bytes of this stage
-              if (leader) mbar_arrive_expect_tx(fb, 2 * bytes);
+              if (leader) mbar_arrive_expect_tx(fb, 2 * STAGE_BYTES);
               load_stage_pair<S, EP, B_MN, SPLIT>(&tmA, &tmB, &tmF, p, tl, kb, sa, sa + L::kABytes,
                                                   mapa_shared(fb, 0), rank);
             } else {
-              mbar_arrive_expect_tx(fb, bytes);
+              mbar_arrive_expect_tx(fb, STAGE_BYTES);
               load_stage_tiled<S, EP, A_MN, B_MN, SPLIT, true, true>(&tmA, &tmB, &tmF, p, tl, kb, sa,
                                                                      sa + L::kABytes, fb);
             }
@@ -1229,7 +1260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // processed by its claimer.  Every tile is published to the ring before its loads, the
           // accumulators alternating over tiles with K blocks; a -1 position ends the sequence.
           const int per_e = p.m_tiles * p.n_tiles;
-          const int4* info = reinterpret_cast<const int4*>(p.sched_info) + (p.split_part == 2 ? __ldg(p.split_heavy) : 0);
+          const int4* info = reinterpret_cast<const int4*>(p.sched_info) + (p.parted ? part_lo(p) : 0);
           auto claim = [&]() -> int {
             const int c = atomicAdd(p.claims, 1);
             return c < total ? c : -1;
@@ -1370,8 +1401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after_sync();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-      const bool f16 = SPLIT != 0 && tl.f16 != 0;  // one fp16 MMA per K step
-      const uint32_t id = f16 ? idesc16 : idesc;
+      // fp16 operands: a weight-gradient tile of the fp16 experts' launch (in the dH GEMM the flag
+      // marks the tiles that write fp16 parts; its operands are bf16)
+      const uint32_t id = (S == Sched::RowsK && tl.f16) ? idesc16 : idesc;
       for (int kb = 0; kb < tl.kb_count; ++kb) {
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * stage, phase, abort_flag))) {
           raise_abort(p.err, abort_flag);
@@ -1387,7 +1419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // so the other operand's rows there (the next expert's) add nothing.
         int ksteps = BK / 16;
         if constexpr (S == Sched::RowsK) {
-          const int valid = tl.rows - kb * BK;
+          const int valid = tl.rows - kb_source(tl, kb, p).kbe * BK;
           if (valid < BK) ksteps = (valid + 15) / 16;
         }
         if (lane == 0) {
@@ -1402,7 +1434,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               umma_bf16_f32_pair(d_tmem, ad, bd, id, (kb | kk) != 0 ? 1u : 0u);
             else
               umma_bf16_f32(d_tmem, ad, bd, id, (kb | kk) != 0 ? 1u : 0u);
-            if (f16) continue;
             if constexpr (SPLIT == 1) {  // lo part of A against the same B
               const uint64_t lo = smem_desc_sw128(sa + A_BYTES + kk * 2048, MN_BOX_BYTES, 1024);
               if constexpr (kPair)
@@ -1550,6 +1581,7 @@ __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __re
   __shared__ int s_bad;
   __shared__ int s_max;
   __shared__ int s_heavy;
+  __shared__ int s_f16;
   __shared__ int s_total[5];
   __shared__ int s_rows[1024];
   griddep_wait();
@@ -1559,6 +1591,7 @@ __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __re
     s_bad = (m_indptr[0] != 0 || static_cast<long long>(m_indptr[E]) != R) ? 1 : 0;
     s_max = 0;
     s_heavy = 0;
+    s_f16 = 0;
   }
   if (sb.claims != nullptr && tid < kClaimSlots) sb.claims[tid] = 0;
   __syncthreads();
@@ -1569,6 +1602,7 @@ __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __re
     rows = max(b - a, 0);
     atomicMax(&s_max, rows);
     if (rows >= kPairRowsDwD) atomicAdd(&s_heavy, 1);
+    if (rows >= kF16Rows) atomicAdd(&s_f16, 1);
   }
   s_rows[tid] = rows;
   const bool heavy_m = rows >= kPairRowsM;
@@ -1632,6 +1666,8 @@ __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __re
       sb.claims[kClaimSlots] = (!bad && s_max >= 512 && s_max >= 4 * mean) ? 1 : 0;
       // the experts at the head of that order with enough rows for the 2-SM pair dW_down
       sb.claims[kClaimSlots + 1] = bad ? 0 : s_heavy;
+      // and those with enough rows for the fp16 weight-gradient pass (kF16Rows >= kPairRowsDwD)
+      sb.claims[kClaimSlots + 2] = bad ? 0 : s_f16;
     }
   }
   if (bad && tid == 0) atomicOr(err, LIGER_MOE_DEVERR_BAD_INDPTR);
@@ -2132,16 +2168,32 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.ld_out = a.H;
   p.out_expert_stride = static_cast<long long>(a.nin) * a.H;
   if (make_out_bf16_3d(&tc0, a.dw_gate_up, a.H, nin, a.E)) return LIGER_MOE_ERR_LAUNCH;
-  // fp16 operands (experts with f16_rows rows): the lo rows of dgu hold fp16(dgu 2^sg), x16 the x rows
+  // The fp16 pass (f16): the experts with at least kF16Rows rows lead the sorted order; their
+  // count is *f16_count.  They run in a launch of their own with one operand part per stage (more
+  // stages in flight), taking one fp16 MMA per K step (lo rows of dgu: fp16(dgu 2^sg); x16: the x
+  // rows), or their hi / lo parts as two passes where their fp16 parts are unusable.  The two
+  // launches are one traced interval.  The fp16 launch goes first when the experts average
+  // kF16Rows rows (then it holds most of the work); else after the two-part launch of the other
+  // experts, so that an empty fp16 launch cannot hand the SMs to the side stream's kernels before
+  // the GEMM takes them.  Measured, ms per step (fp16 first / last / no fp16 pass): training shape
+  // 2.04-2.05 / 2.09-2.10 / 2.19-2.22; 2048/512 workload (no expert of kF16Rows) 1.909 / 1.900 /
+  // 1.885-1.891; Zipf 4096/1024 the same either way.
+  const bool f16 = a.f16_words != nullptr && !gather_x && !empty;
+  const bool f16_first = a.R >= static_cast<long long>(kF16Rows) * a.E;
+  const int* f16_count = a.claims + kClaimSlots + 2;
+  const int* pair_count = a.claims + kClaimSlots + 1;
+  static_assert(kF16Rows >= kPairRowsDwD, "the fp16 experts lead the pair experts of dW_down");
   CUtensorMap tf;
-  const CUtensorMap* tfp = nullptr;
-  if (a.f16_words != nullptr && !gather_x && !empty) {
-    if (make_tmap(&tf, a.x16, a.H, rows, 64, BK)) return LIGER_MOE_ERR_LAUNCH;
-    tfp = &tf;
-    p.f16_role = 3;
-    p.f16_rows = a.f16_rows;
-    p.f16_words = a.f16_words;
-  }
+  auto f16_params = [&](Params& pf, int role, int slot) {
+    pf.parted = 1;
+    pf.part_begin = nullptr;
+    pf.part_end = f16_count;
+    pf.f16_role = role;
+    pf.f16_part = 1;
+    pf.f16_rows = a.f16_rows;
+    pf.f16_words = a.f16_words;
+    set_dynamic(pf, a.sched_order, a.sched_info, a.claims, slot);
+  };
   // CTA pairs over neighbouring M blocks (2-SM MMAs, each CTA holding half of the x tile) when the M
   // blocks pair up and experts hold at least kPairRowsDwGu rows on average; below that every CTA
   // works alone on its tile (with few rows per expert the tiles are mostly gradient writes, and a
@@ -2149,18 +2201,40 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   // here than one-CTA tiles in the heavy-first dynamic order (2687-2719 against 2647-2688 us on the
   // Zipf 4096/1024 workload).
   const long long tiles_gu = static_cast<long long>(a.E) * p.m_tiles * p.n_tiles;
-  int rc;
-  if (gather_x)
-    rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::B>(ta, tb, tc0, tc0, p, tiles_gu, dev, s,
-                                                                         "gemm_bwd_dw_gate_up");
-  else if (p.m_tiles % 2 == 0 && a.R >= kPairRowsDwGu * a.E)
-    rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::None, 2, 1>(
-        ta, tb, tc0, tc0, p, tiles_gu / 2, dev, s, "gemm_bwd_dw_gate_up", true, tfp);
-  else
-    rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1>(ta, tb, tc0, tc0, p, tiles_gu, dev, s,
-                                                              "gemm_bwd_dw_gate_up", true, tfp);
-  if (rc) return rc;
-  p.f16_role = 0;
+  const bool pairs_gu = p.m_tiles % 2 == 0 && a.R >= kPairRowsDwGu * a.E;
+  {
+    KernelScope trace("gemm_bwd_dw_gate_up", s);
+    if (gather_x) {
+      if (int rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::B>(ta, tb, tc0, tc0, p, tiles_gu, dev,
+                                                                                 s, "gemm_bwd_dw_gate_up", false))
+        return rc;
+    } else {
+      Params pr = p;  // the experts of the two-part launch
+      if (f16) {
+        pr.parted = 1;
+        pr.part_begin = f16_count;
+      }
+      auto two_part = [&]() {
+        return pairs_gu ? launch_gemm<Sched::RowsK, Epi::Store, true, true, 1, Gather::None, 2, 1>(
+                              ta, tb, tc0, tc0, pr, tiles_gu / 2, dev, s, "gemm_bwd_dw_gate_up", false)
+                        : launch_gemm<Sched::RowsK, Epi::Store, true, true, 1>(ta, tb, tc0, tc0, pr, tiles_gu, dev, s,
+                                                                               "gemm_bwd_dw_gate_up", false);
+      };
+      auto fp16_part = [&]() {
+        if (make_tmap(&tf, a.x16, a.H, rows, 64, BK)) return static_cast<int>(LIGER_MOE_ERR_LAUNCH);
+        Params pf = p;
+        f16_params(pf, 3, kClaimDwGateUpF16);
+        return pairs_gu ? launch_gemm<Sched::RowsK, Epi::Store, true, true, 0, Gather::None, 2, 1>(
+                              ta, tb, tc0, tc0, pf, tiles_gu / 2, dev, s, "gemm_bwd_dw_gate_up", false, &tf)
+                        : launch_gemm<Sched::RowsK, Epi::Store, true, true, 0>(ta, tb, tc0, tc0, pf, tiles_gu, dev, s,
+                                                                               "gemm_bwd_dw_gate_up", false, &tf);
+      };
+      int rc = (f16 && f16_first) ? fp16_part() : LIGER_MOE_OK;
+      if (rc == LIGER_MOE_OK) rc = two_part();
+      if (rc == LIGER_MOE_OK && f16 && !f16_first) rc = fp16_part();
+      if (rc) return rc;
+    }
+  }
   // dW_d[e] = dY_e^T hw_hi_e + dY_e^T hw_lo_e: each stage holds one A tile (dY rows gathered by
   // token) and both parts of B (rows r and R + r of hw [2R, I]); two MMAs per K step.
   const bool gather_dy = a.dy_perm == nullptr || empty;
@@ -2185,42 +2259,58 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   p.ld_out = a.I;
   p.out_expert_stride = 1LL * a.H * a.I;
   if (make_out_bf16_3d(&tc0, a.dw_down, a.I, a.H, a.E)) return LIGER_MOE_ERR_LAUNCH;
-  // fp16 operands: the lo rows of hw hold fp16(w h 2^sh), dy16 the dY rows
-  tfp = nullptr;
-  if (a.f16_words != nullptr && !gather_dy) {
-    if (make_tmap(&tf, a.dy16, a.H, rows, 64, BK)) return LIGER_MOE_ERR_LAUNCH;
-    tfp = &tf;
-    p.f16_role = 4;
-    p.f16_rows = a.f16_rows;
-    p.f16_words = a.f16_words;
-  }
   // CTA pairs over neighbouring M blocks (2-SM MMAs, each CTA holding half of the w h tile, 4 stages
   // instead of 2): for every expert when they hold at least kSplitMeanRows rows on average; for the
   // experts with at least kPairRowsDwD rows (the head of the sorted order) when fewer, the others one
-  // CTA per tile (the heavy / light split); one CTA per tile for all when no expert can reach it
+  // CTA per tile (the heavy / light split); one CTA per tile for all when no expert can reach it.
+  // With the fp16 pass its experts (fp16(w h 2^sh) in the lo rows of hw; dy16: the dY rows) run
+  // last, as pairs where the pair experts do.
   const long long tiles_d = static_cast<long long>(a.E) * p.m_tiles * p.n_tiles;
+  const bool pairs_all = p.m_tiles % 2 == 0 && a.R >= kSplitMeanRows * a.E;
+  const bool split = !pairs_all && p.m_tiles % 2 == 0 && a.T >= kPairRowsDwD;
+  KernelScope trace("gemm_bwd_dw_down", s);
   if (gather_dy)
     return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::A>(ta, tb, tc0, tc0, p, tiles_d, dev, s,
-                                                                           "gemm_bwd_dw_down");
-  if (p.m_tiles % 2 == 0 && a.R >= kSplitMeanRows * a.E)
-    return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::None, 2, 1>(
-        ta, tb, tc0, tc0, p, tiles_d / 2, dev, s, "gemm_bwd_dw_down", true, tfp);
-  if (p.m_tiles % 2 == 0 && a.T >= kPairRowsDwD) {
-    KernelScope trace("gemm_bwd_dw_down", s);
-    Params ph = p;
-    ph.split_part = 1;
-    ph.split_heavy = a.claims + kClaimSlots + 1;
-    if (int rc2 = launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::None, 2, 1>(
-            ta, tb, tc0, tc0, ph, tiles_d / 2, dev, s, "gemm_bwd_dw_down", false, tfp))
-      return rc2;
-    Params pl = p;
-    pl.split_part = 2;
-    pl.split_heavy = ph.split_heavy;
-    return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2>(ta, tb, tc0, tc0, pl, tiles_d, dev, s,
-                                                                "gemm_bwd_dw_down", false, tfp);
+                                                                           "gemm_bwd_dw_down", false);
+  const bool f16_d = f16 && !gather_dy;
+  Params pr = p;
+  if (f16_d) {  // the two-part launches start after the fp16 experts
+    pr.parted = 1;
+    pr.part_begin = f16_count;
   }
-  return launch_gemm<Sched::RowsK, Epi::Store, true, true, 2>(ta, tb, tc0, tc0, p, tiles_d, dev, s, "gemm_bwd_dw_down",
-                                                              true, tfp);
+  auto fp16_part = [&]() {
+    if (make_tmap(&tf, a.dy16, a.H, rows, 64, BK)) return static_cast<int>(LIGER_MOE_ERR_LAUNCH);
+    Params pf = p;
+    f16_params(pf, 4, kClaimDwDownF16);
+    return (pairs_all || split) ? launch_gemm<Sched::RowsK, Epi::Store, true, true, 0, Gather::None, 2, 1>(
+                                      ta, tb, tc0, tc0, pf, tiles_d / 2, dev, s, "gemm_bwd_dw_down", false, &tf)
+                                : launch_gemm<Sched::RowsK, Epi::Store, true, true, 0>(ta, tb, tc0, tc0, pf, tiles_d,
+                                                                                       dev, s, "gemm_bwd_dw_down", false,
+                                                                                       &tf);
+  };
+  int rc = (f16_d && f16_first) ? fp16_part() : LIGER_MOE_OK;
+  if (rc != LIGER_MOE_OK) return rc;
+  if (pairs_all) {
+    rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::None, 2, 1>(ta, tb, tc0, tc0, pr, tiles_d / 2,
+                                                                                  dev, s, "gemm_bwd_dw_down", false);
+  } else if (split) {
+    Params ph = pr;  // [begin, pair_count): pairs; [pair_count, E): one CTA per tile
+    ph.parted = 1;
+    ph.part_end = pair_count;
+    rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 2, Gather::None, 2, 1>(ta, tb, tc0, tc0, ph, tiles_d / 2,
+                                                                                  dev, s, "gemm_bwd_dw_down", false);
+    Params pl = p;
+    pl.parted = 1;
+    pl.part_begin = pair_count;
+    if (rc == LIGER_MOE_OK)
+      rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 2>(ta, tb, tc0, tc0, pl, tiles_d, dev, s,
+                                                                "gemm_bwd_dw_down", false);
+  } else {
+    rc = launch_gemm<Sched::RowsK, Epi::Store, true, true, 2>(ta, tb, tc0, tc0, pr, tiles_d, dev, s,
+                                                              "gemm_bwd_dw_down", false);
+  }
+  if (rc == LIGER_MOE_OK && f16_d && !f16_first) rc = fp16_part();
+  return rc;
 }
 
 }  // namespace lmoe

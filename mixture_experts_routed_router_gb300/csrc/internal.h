@@ -131,8 +131,9 @@ int launch_router_logits(const uint16_t* x, const uint16_t* w_router, const floa
 //   order_info[4i..] the expert at order[i], its first row, its rows and its first padded row (the
 //                    first row when there is no padded row prefix); with order, or nullptr
 //   claims           kClaimSlots claim counters, zeroed by the schedule kernel (one per GEMM launch
-//                    that may take its tiles in that order), then the skew flag and the count of
-//                    experts at or above the dW_down pair threshold; or nullptr
+//                    that may take its tiles in that order), then the skew flag, the count of
+//                    experts at or above the dW_down pair threshold and the count at or above
+//                    kF16Rows (the fp16 weight-gradient experts); or nullptr
 struct ScheduleBufs {
   int32_t* tile_prefix = nullptr;
   int32_t* pad_indptr = nullptr;
@@ -148,7 +149,7 @@ struct ScheduleBufs {
 };
 constexpr int kClaimSlots = 8;
 // Claim counters of the launches that may use the dynamic order: the weight-gradient GEMMs.
-enum ClaimSlot : int { kClaimDwGateUp = 0, kClaimDwDown = 1 };
+enum ClaimSlot : int { kClaimDwGateUp = 0, kClaimDwDown = 1, kClaimDwGateUpF16 = 2, kClaimDwDownF16 = 3 };
 size_t schedule_bytes(int E);                  // one [E+1] int32 array, 256-byte aligned
 constexpr size_t kClaimBytes = 256;            // kClaimSlots counters and the skew flag, 256-byte aligned
 int launch_tile_schedule(const int32_t* m_indptr, int E, long long R, const ScheduleBufs& b, const DeviceInfo& dev,

@@ -9,8 +9,11 @@ expert:
 - the fp16 pass is taken exactly by the heavy experts: their gradients differ from the hi / lo
   run, while dX, d_logits and the light experts' gradients are bit-identical;
 - an expert whose scaled dgu leaves the fp16 window (here: its W_down scaled by 2^40, so its dgu
-  overflows) falls back to the hi / lo parts, bit-identical to the hi / lo run, while the other
-  heavy experts keep the fp16 pass;
+  overflows) falls back to the hi / lo parts: it matches the oracle (its fp16 parts, infinite,
+  could not) and the hi / lo run in all but a few elements (the same products in fp32, the hi and
+  lo parts summed as two passes over its rows instead of interleaved, so a rounding of the bf16
+  result rarely flips), while the other heavy experts keep the fp16 pass (11-bit dgu: about one
+  element in ten rounds differently);
 - the pass is deterministic.
 """
 import numpy as np
@@ -55,6 +58,11 @@ def _differs(a, b, experts):
     return [bool((a[e] != b[e]).any()) for e in experts]
 
 
+def _flipped(a, b):
+    """Fraction of elements whose bf16 bits differ."""
+    return float(np.mean(a != b))
+
+
 def test_heavy_experts_take_the_fp16_pass_and_match_the_oracle():
     inp = synthetic.make_inputs(WL)
     args, counts = _layer(inp)
@@ -93,10 +101,9 @@ def test_an_expert_outside_the_fp16_window_falls_back_to_hi_lo():
     assert moe.device_error() == 0
     _oracle_check(inp, f16, wd_host=to_host(wd))
     others = [e for e in heavy if e != big]
-    a, b = to_host(f16[1]), to_host(hilo[1])
-    assert not _differs(a, b, [big])[0], "the overflowing expert kept the fp16 pass"
-    assert all(_differs(a, b, others)), "the other heavy experts lost the fp16 pass"
-    a, b = to_host(f16[2]), to_host(hilo[2])
-    assert not _differs(a, b, [big])[0]
+    for i in (1, 2):
+        a, b = to_host(f16[i]), to_host(hilo[i])
+        assert _flipped(a[big], b[big]) < 0.01, "the overflowing expert kept the fp16 pass"
+        assert min(_flipped(a[e], b[e]) for e in others) > 0.01, "another heavy expert lost the fp16 pass"
     for name, i in (("dX", 0), ("d_logits", 3)):
         assert torch.equal(f16[i], hilo[i]), name
