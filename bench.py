@@ -893,6 +893,9 @@ def run_ours(args, rank, world, local_rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict(wl.as_dict(), **{"pass": "forward+backward", "parallelism": f"replicas x{world}",
                                            "expert_inputs": args.inputs, "activation": args.act,
+                                           "dw_operands": (f"fp16 (scaled by powers of two) for the {f16_rows} routed "
+                                                           "rows of experts with 384+ rows; bf16 hi + lo for the rest"
+                                                           if f16_rows else "bf16 hi + lo"),
                                            "router": "x Wr^T (+ bias) and its backward on the GPU" if args.router
                                            else "logits are the layer's input",
                                            "l2": f"inputs larger than L2: {L.weight_bytes / 1e9:.2f} GB "

@@ -9,8 +9,8 @@ expert:
 - the fp16 pass is taken exactly by the heavy experts: their gradients differ from the hi / lo
   run, while dX, d_logits and the light experts' gradients are bit-identical;
 - an expert whose scaled dgu leaves the fp16 window (here: its W_down scaled by 2^40, so its dgu
-  overflows) falls back to the hi / lo parts: it matches the oracle (its fp16 parts, infinite,
-  could not) and the hi / lo run in all but a few elements (the same products in fp32, the hi and
+  overflows, or by 2^-40, so its dgu would be subnormal) falls back to the hi / lo parts: it matches
+  the oracle and the hi / lo run in all but a few elements (the same products in fp32, the hi and
   lo parts summed as two passes over its rows instead of interleaved, so a rounding of the bf16
   result rarely flips), while the other heavy experts keep the fp16 pass (11-bit dgu: about one
   element in ten rounds differently);
@@ -86,14 +86,17 @@ def test_heavy_experts_take_the_fp16_pass_and_match_the_oracle():
         assert torch.equal(u, v)
 
 
-def test_an_expert_outside_the_fp16_window_falls_back_to_hi_lo():
+@pytest.mark.parametrize("scale", [2.0 ** 40, 2.0 ** -40], ids=["overflow", "too_small"])
+def test_an_expert_outside_the_fp16_window_falls_back_to_hi_lo(scale):
     inp = synthetic.make_inputs(WL)
     _, counts = _layer(inp)
     heavy = np.nonzero(counts >= HEAVY_ROWS)[0]
     assert len(heavy) >= 2, counts
     big = int(np.argmax(counts))
     wd = to_dev(inp["wd"])
-    wd[big] *= 2.0 ** 40  # exact in bf16; the expert's dgu grows by 2^40 and overflows fp16
+    # exact in bf16: the expert's dgu scales with its W_down, and its largest scaled fp16 magnitude
+    # leaves the window (overflow above 65504, or below 2^-6 where values would lose precision)
+    wd[big] *= scale
     args, _ = _layer(inp, wd=wd)
     f16 = moe.bwd_dx_dw(*args)
     with dw_fp16(False):
