@@ -46,11 +46,13 @@
  *     an internal pipeline wait that ran past its time limit) set a flag that
  *     liger_moe_device_error() returns; outputs of that call are unspecified.
  *   - Only devices of compute capability 10.3 (sm_103) are supported.
- *   - Launch mode: kernels run in plain stream order.  With the environment
- *     variable LIGER_MOE_PDL set to a non-empty value other than "0" (read
- *     once per process) they are launched with programmatic dependent launch:
- *     each kernel may start while the one before it on the stream finishes,
- *     and waits for it before touching memory.  Results are identical.
+ *   - Launch mode: a call with fewer than 4096 routed rows (T*k) launches its
+ *     kernels with programmatic dependent launch: each kernel may start while
+ *     the one before it on the stream finishes, and waits for it before
+ *     touching memory.  Larger calls run in plain stream order.  The
+ *     environment variable LIGER_MOE_PDL (read once per process) overrides
+ *     this: "0" never, any other non-empty value always.  Results are
+ *     identical in every mode.
  */
 #ifndef LIGER_MOE_H_
 #define LIGER_MOE_H_

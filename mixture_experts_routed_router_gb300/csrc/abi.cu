@@ -130,11 +130,12 @@ void set_cuda_error(cudaError_t e, const char* where) {
 }
 
 bool pdl_enabled() {
-  static const bool on = [] {
+  static const int mode = [] {  // 0 never, 1 always, 2 small calls
     const char* v = std::getenv("LIGER_MOE_PDL");
-    return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
+    if (v == nullptr || v[0] == '\0') return 2;
+    return std::strcmp(v, "0") == 0 ? 0 : 1;
   }();
-  return on;
+  return mode == 1 || (mode == 2 && t_pdl_small);
 }
 
 int check_launch(const char* where) {
@@ -230,6 +231,7 @@ LIGER_MOE_API int liger_moe_route_topk(const float* logits, int T, int E, int k,
                                        void* stream) {
   if (int rc = check_topk(T, E, k)) return rc;
   if (T > 0 && (logits == nullptr || topk_ids == nullptr || topk_w == nullptr)) return LIGER_MOE_ERR_INVALID_ARG;
+  PdlScope pdl(static_cast<long long>(T) * k);
   DeviceInfo dev;
   if (int rc = current_device(&dev)) return rc;
   if (T == 0) return LIGER_MOE_OK;
@@ -257,6 +259,7 @@ LIGER_MOE_API int liger_moe_dispatch(const int32_t* topk_ids, const float* topk_
   }
   if (*workspace_bytes < need) return LIGER_MOE_ERR_CAPACITY;
   if (!aligned16(workspace)) return LIGER_MOE_ERR_MISALIGNED;
+  PdlScope pdl(R);
   DeviceInfo dev;
   if (int rc = current_device(&dev)) return rc;
   return launch_dispatch(topk_ids, topk_w, static_cast<const uint16_t*>(x), T, H, E, k, counts, m_indptr, row_to_slot,
@@ -292,6 +295,7 @@ int grouped_swiglu_fwd_impl(const void* x_perm, const void* x, const int32_t* ro
   }
   if (*workspace_bytes < need) return LIGER_MOE_ERR_CAPACITY;
   if (!aligned16(workspace)) return LIGER_MOE_ERR_MISALIGNED;
+  PdlScope pdl(R);
   DeviceInfo dev;
   if (int rc = current_device(&dev)) return rc;
   if (R == 0) return LIGER_MOE_OK;
@@ -374,6 +378,7 @@ LIGER_MOE_API int liger_moe_combine(const void* y_perm, const int32_t* slot_to_r
   if (H % 64 != 0) return LIGER_MOE_ERR_MISALIGNED;
   if (T > 0 && (y_perm == nullptr || slot_to_row == nullptr || y == nullptr)) return LIGER_MOE_ERR_INVALID_ARG;
   if (!aligned16(y_perm) || !aligned16(y)) return LIGER_MOE_ERR_MISALIGNED;
+  PdlScope pdl(static_cast<long long>(T) * k);
   DeviceInfo dev;
   if (int rc = current_device(&dev)) return rc;
   return launch_combine(static_cast<const uint16_t*>(y_perm), slot_to_row, T, H, k, static_cast<uint16_t*>(y), dev,
@@ -458,6 +463,7 @@ int bwd_dx_dw_impl(const void* dy, const void* x_perm, const void* x, const void
   }
   if (*workspace_bytes < need) return LIGER_MOE_ERR_CAPACITY;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LIGER_MOE_ERR_MISALIGNED;
+  PdlScope pdl(R);
   DeviceInfo dev;
   if (int rc = current_device(&dev)) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -646,6 +652,7 @@ LIGER_MOE_API int liger_moe_router_logits(const void* x, const void* w_router, c
   if (H % 64 != 0) return LIGER_MOE_ERR_MISALIGNED;
   if (w_router == nullptr || (T > 0 && (x == nullptr || logits == nullptr))) return LIGER_MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(logits)) return LIGER_MOE_ERR_MISALIGNED;
+  PdlScope pdl(T);
   DeviceInfo dev;
   if (int rc = current_device(&dev)) return rc;
   return launch_router_logits(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(w_router), bias, T, H,
@@ -663,6 +670,7 @@ LIGER_MOE_API int liger_moe_router_bwd(const float* d_logits, const int32_t* top
                 dx == nullptr))
     return LIGER_MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(dx)) return LIGER_MOE_ERR_MISALIGNED;
+  PdlScope pdl(static_cast<long long>(T) * k);
   DeviceInfo dev;
   if (int rc = current_device(&dev)) return rc;
   return launch_router_bwd(d_logits, topk_ids, m_indptr, row_to_slot, static_cast<const uint16_t*>(x),

@@ -78,6 +78,7 @@ LIGER_MOE_API int liger_moe_dispatch_noalloc(const int32_t* topk_ids, const floa
   }
   // the stated limit: the histograms, ceil(T*k / 256) * E * 4 bytes, fit in the array
   if (dispatch_scratch_bytes(R, E) > kDispatchScratchBytes) return LIGER_MOE_ERR_CAPACITY;
+  PdlScope pdl(R);
   DeviceInfo dev;
   if (int rc = current_device(&dev)) return rc;
   void* scratch = nullptr;

@@ -237,12 +237,23 @@ int launch_bwd_dw(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// True when LIGER_MOE_PDL is set to a non-empty value other than "0" (read once): kernels are then
-// launched with programmatic stream serialization, so each one's launch and prologue overlap the
-// end of the kernel before it (every kernel waits on its predecessor before touching memory).
-// Off by default: on GB300 it shortened a launch-bound step (256 tokens) by about 7 % but
-// lengthened a 65536-row step by 1.5-4 %, wherever the GEMMs signalled their dependents.
-bool pdl_enabled();
+// Programmatic dependent launch: kernels launched with programmatic stream serialization, so each
+// one's launch and prologue overlap the end of the kernel before it (every kernel waits on its
+// predecessor before touching memory).  LIGER_MOE_PDL (read once): "0" never, any other non-empty
+// value always, unset or empty for the calls with fewer than kPdlMaxRows routed rows only.  On
+// GB300 it shortened a launch-bound step (256 tokens) by about 7 % but lengthened a 65536-row step
+// by 1.5-4 %, wherever the GEMMs signalled their dependents.
+constexpr long long kPdlMaxRows = 4096;
+inline thread_local bool t_pdl_small = false;  // this thread is inside a call below kPdlMaxRows rows
+// Marks the launches of one entry-point call as small (rows < kPdlMaxRows) or not.
+struct PdlScope {
+  bool prev;
+  explicit PdlScope(long long rows) : prev(t_pdl_small) { t_pdl_small = rows < kPdlMaxRows; }
+  ~PdlScope() { t_pdl_small = prev; }
+  PdlScope(const PdlScope&) = delete;
+  PdlScope& operator=(const PdlScope&) = delete;
+};
+bool pdl_enabled();  // for a launch made now by this thread
 
 // Launches `kern` on `s` with programmatic stream serialization (when enabled) and, for
 // cluster > 1, that cluster size; records and returns the launch error.

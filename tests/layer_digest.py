@@ -3,8 +3,8 @@ every output, as launched one call at a time and as replayed from a captured CUD
 "capture_first", only the latter, captured before any other call).
 
 Used by tests/test_gpu_pdl.py as a child process: the library reads its launch mode
-(programmatic dependent launch with LIGER_MOE_PDL=1, else plain stream order) once per
-process, so each mode gets its own process.  Every kernel sums in a fixed order, so the digests must not depend on
+(LIGER_MOE_PDL=1: programmatic dependent launch; =0: plain stream order; unset: programmatic
+launch for the calls below 4096 routed rows) once per process, so each mode gets its own process.  Every kernel sums in a fixed order, so the digests must not depend on
 the launch mode or on graph replay.
 """
 from __future__ import annotations
