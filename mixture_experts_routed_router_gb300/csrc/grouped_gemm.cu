@@ -11,9 +11,9 @@
 //               the whole warp with TMA gather4 (four rows per copy) straight from the
 //               token-major tensor, so no permuted copy of it is ever written.
 //   warp 1      MMA issuer: allocates 512 TMEM columns, one elected lane issues
-//               tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32; M=256 across a
-//               2-SM CTA pair) and commits stage releases and accumulator-ready events
-//               to mbarriers
+//               tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32, or fp16 x fp16 in
+//               the weight gradients' fp16 launch; M=256 across a 2-SM CTA pair) and
+//               commits stage releases and accumulator-ready events to mbarriers
 //   warps 2..9  epilogue: tcgen05.ld of the fp32 accumulator, fused math, TMA bulk
 //               stores.  Two warps per 32-lane TMEM quadrant (the quadrant's 32 rows),
 //               each owning half of the tile's columns.
@@ -30,10 +30,14 @@
 //          dH epilogue writes (dgu, w h) sits in a padded row space: each expert's
 //          rows are followed by zero rows up to a multiple of 16, so the last
 //          16-row K step adds nothing from the next expert's rows of the other operand.
+//          A launch may take one part of the experts, a range of their sorted order
+//          (the experts of the fp16 pass, the 2-SM pair experts of dW_down).
 //   Dense  one plain GEMM over R rows (the router projection).
 // Epilogues: SwiGLU (h = silu(g)*u, optional fp32 derivative factors), ScaleRows
 // (y = w_r * acc), DH (SwiGLU backward from the saved factors, hi/lo operands for
-// the weight gradients, per-row partial <dh, h> for the router gradient), Store.
+// the weight gradients or, for experts with many rows, fp16 ones, per-row partial
+// <dh, h> for the router gradient), Store (the weight gradients: scaled back from
+// the fp16 operands' powers of two where they were used).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -75,7 +79,8 @@ constexpr int kDhBoxBytes = 32 * 32;            // dH epilogue: 32 rows x 16 bf1
 constexpr int kDhSetBytes = 6 * kDhBoxBytes;    // six output boxes per 16 columns
 
 // Shared memory of one CTA: operand stages | epilogue staging | barriers.
-//   SPLIT = 0: one A and one B tile per stage (48 KB), 4 stages;
+//   SPLIT = 0: one A and one B tile per stage (48 KB), 4 stages (also the weight gradients'
+//              fp16 launch, whose tiles take one part of each operand);
 //   SPLIT = 1: A as two bf16 parts (hi, lo) + B (64 KB), 3 stages: two MMAs per K step share B;
 //   SPLIT = 2: A + B as two parts (80 KB), 2 stages: two MMAs per K step share A.
 //   PAIR: a CTA of a 2-SM pair holds its 128 rows (RowsM) or columns (RowsK) of A and half of B's
