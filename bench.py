@@ -571,9 +571,9 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device error flags {flags:#x} during warm-up")
     experts_used = int((dbuf["counts"] > 0).sum().item())  # experts whose weights the GEMMs read
     # rows of the experts that take the backward's fp16 weight-gradient pass (the library's rule: gated
-    # experts, expert-major inputs, R >= 4096, experts with at least 384 rows)
+    # experts, expert-major inputs, R >= 32768, experts with at least 384 rows)
     counts_h = dbuf["counts"].cpu()
-    f16_rows = int(counts_h[counts_h >= 384].sum().item()) if gated and args.inputs != "gather" and wl.R >= 4096 else 0
+    f16_rows = int(counts_h[counts_h >= 384].sum().item()) if gated and args.inputs != "gather" and wl.R >= 32768 else 0
 
     # ---------------- timed region: K steps, CUDA events on the launching stream
     # The K steps are captured once as a CUDA graph (the library's calls only enqueue work on

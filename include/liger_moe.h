@@ -254,7 +254,7 @@ int liger_moe_combine(const void* y_perm, const int32_t* slot_to_row, int T, int
  * weight is applied in fp32 to the dH accumulator.  The weight-gradient GEMMs
  * take their non-input operand (dgu for dW_gate_up, w * h for dW_down) as two
  * bf16 parts, hi + lo, so that operand carries about 16 significant bits.
- * Experts with at least 384 rows (when R >= 4096 and the experts are gated)
+ * Experts with at least 384 rows (when R >= 32768 and the experts are gated)
  * take one fp16 pass instead (liger_moe_set_dw_fp16): x and dY rows as
  * fp16(v 2^s) with s set by the tensor's largest magnitude (exact), dgu and
  * w * h as fp16 (11 significant bits) with power-of-two scales derived from
@@ -263,7 +263,7 @@ int liger_moe_combine(const void* y_perm, const int32_t* slot_to_row, int T, int
  * small for full precision) takes the two-part path instead, so every input
  * gets one of the two precisions.
  * Limit: T*k < 2^30.  Workspace: about R*(2H + 6I)*2 bytes, plus R*2I*4 more
- * when gu_perm is NULL, plus R*2H*2 for the fp16 copies when R >= 4096 and
+ * when gu_perm is NULL, plus R*2H*2 for the fp16 copies when R >= 32768 and
  * the experts are gated.
  */
 int liger_moe_bwd_dx_dw(const void* dy, const void* x_perm, const void* h_perm, const float* gu_perm,

@@ -1067,6 +1067,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       need = need || (__ldg(p.m_indptr + e + 1) - __ldg(p.m_indptr + e) >= p.f16_rows && !f16_usable(e, p));
     if (!__syncthreads_or(need ? 1 : 0)) return;
   }
+  if (p.parted) {
+    // an empty part of the experts (e.g. no expert reaches the fp16 pass's rows): leave before any
+    // set-up; every CTA of a pair reads the same counts, so both leave
+    griddep_wait();
+    if (part_hi(p) <= part_lo(p)) return;
+  }
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;

@@ -58,7 +58,10 @@ int launch_scatter_rows(const uint16_t* src, const int32_t* slot_to_row, int T, 
 //   expert has at least f16 rows,  [kF16Range + e] / [kF16Range + E + e] largest |scaled dgu| /
 //   |scaled w h| of expert e (float bits; atomicMax of the dH epilogue).
 constexpr int kF16Rows = 384;
-constexpr long long kF16MinR = 4096;  // routed rows below which the backward never takes the fp16 pass
+// Routed rows below which the backward never takes the fp16 pass: at fewer rows its fixed costs (four
+// launches, which leave at once when no expert reaches kF16Rows) were measured at 1.3 % of a step
+// (8192 and 16384 rows, 64-128 per expert) and even a skewed batch has few heavy rows to gain on.
+constexpr long long kF16MinR = 32768;
 constexpr int kF16MaxX = 0, kF16MaxDy = 1, kF16Any = 2, kF16Range = 4;
 constexpr int kF16DguShift = -6;  // dgu scaled by 2^(s_dY - 6)
 constexpr int kF16HwShift = 4;    // w h scaled by 2^4

@@ -108,13 +108,13 @@ def test_bwd_workspace_grows_when_recomputing(lib):
     assert g >= R * (2 * H + 12 * I) and a - g >= R * H * 2
 
 
-def test_bwd_workspace_holds_the_fp16_copies_from_4096_rows(lib):
-    """From R = 4096 routed rows the x_perm backward may take the fp16 weight-gradient pass: its
+def test_bwd_workspace_holds_the_fp16_copies_from_32768_rows(lib):
+    """From R = 32768 routed rows the x_perm backward may take the fp16 weight-gradient pass: its
     workspace then holds fp16 copies of the x and dY rows; the gathered backward never does."""
     q = lambda T, gather=False: moe.workspace_bytes("bwd_dx_dw", T=T, H=256, I=128, E=8, k=2, gather=gather)
-    small, big = q(2047), q(2048)  # R = 4094, 4096
-    assert big - small >= 2 * 4096 * 256 * 2  # x16 and dy16 [R, H] fp16 on top
-    assert q(2048, gather=True) - q(2047, gather=True) < 64 * 1024  # two more rows and alignment only
+    small, big = q(16383), q(16384)  # R = 32766, 32768
+    assert big - small >= 2 * 32768 * 256 * 2  # x16 and dy16 [R, H] fp16 on top
+    assert q(16384, gather=True) - q(16383, gather=True) < 64 * 1024  # two more rows and alignment only
 
 
 def test_dw_fp16_switch_validates(lib):

@@ -1,6 +1,6 @@
 """The single fp16 pass of the heavy experts' weight gradients (liger_moe_set_dw_fp16).
 
-Experts with at least 384 rows (batches of R >= 4096 routed rows, gated experts, expert-major
+Experts with at least 384 rows (batches of R >= 32768 routed rows, gated experts, expert-major
 inputs) take dW_gate_up and dW_down in one fp16 MMA per K step: the x and dY rows scaled by powers
 of two from their largest magnitudes (exact), dgu and w h rounded to fp16 (11 significant bits)
 instead of split into bf16 hi + lo parts.  Checked here, on a skewed batch with both kinds of
@@ -28,7 +28,7 @@ from tests.helpers import assert_close, bf16_to_f64
 
 pytestmark = pytest.mark.gpu
 
-WL = synthetic.Workload("split_zipf_T1024_H320_I192_E64_k8", 1024, 320, 192, 64, 8, zipf_s=1.2, router_std=0.05)
+WL = synthetic.Workload("f16_zipf_T4096_H320_I192_E64_k8", 4096, 320, 192, 64, 8, zipf_s=1.2, router_std=0.05)
 HEAVY_ROWS = 384
 
 
