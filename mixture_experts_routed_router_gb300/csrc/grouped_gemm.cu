@@ -109,9 +109,12 @@ enum class Sched : int { RowsM = 0, RowsK = 1, Dense = 2 };
 // ReLU2: the up GEMM of a two-weight (non-gated) expert, h = max(a, 0)^2.  DH1: the dH epilogue
 // of such an expert (one derivative factor, one output instead of [dg | du]).  Logits: fp32
 // output plus a per-column bias (the router projection).
-enum class Epi : int { SwiGLU = 0, ScaleRows = 1, DH = 2, Store = 3, GLU = 4, ReLU2 = 5, DH1 = 6, Logits = 7 };
+// DH16: the DH epilogue that writes fp16 parts for the experts with many rows (the first dH pass of a
+// backward with the fp16 weight-gradient pass), kept apart so that the plain DH kernel carries none of
+// that code (with it, DH measured 7 % slower where no expert takes the pass).
+enum class Epi : int { SwiGLU = 0, ScaleRows = 1, DH = 2, Store = 3, GLU = 4, ReLU2 = 5, DH1 = 6, Logits = 7, DH16 = 8 };
 constexpr bool gate_up_epi(Epi e) { return e == Epi::SwiGLU || e == Epi::GLU; }
-constexpr bool dh_epi(Epi e) { return e == Epi::DH || e == Epi::DH1; }
+constexpr bool dh_epi(Epi e) { return e == Epi::DH || e == Epi::DH1 || e == Epi::DH16; }
 template <Epi EP, int SPLIT, int PAIR = 0>
 using LayoutOf = Layout<dh_epi(EP) ? 1 : 0, SPLIT, PAIR>;
 
@@ -174,10 +177,11 @@ struct Params {
   int out_tma;
   // fp16 weight-gradient operands (f16_role != 0), for the experts with at least f16_rows rows;
   // f16_words: the backward's words (kF16MaxX, kF16MaxDy, kF16Any, per-expert range maxima).
-  //   DH, role 1: those experts' tiles write fp16(dgu 2^sg) and fp16(w h 2^sh) into the lo rows
-  //     (and no hi rows of w h), and the largest magnitudes into the range words;
-  //   DH, role 2 (refill): only those experts whose fp16 parts are unusable (f16_usable), with
-  //     hi / lo parts;
+  //   DH16, role 1: those experts' tiles write fp16(dgu 2^sg) and fp16(w h 2^sh) into the lo rows
+  //     (and no hi rows of w h), and the largest magnitudes into the range words; the launch leaves
+  //     at once when no expert has f16_rows rows;
+  //   DH, role 2: then only those experts whose fp16 parts are unusable (f16_usable), with hi / lo
+  //     parts (the refill); or, when no expert has f16_rows rows, the whole dH GEMM;
   //   RowsK, role 3 (dW_gate_up) / 4 (dW_down), in the launch of those experts (f16_part, one
   //     operand part per stage): an expert with usable fp16 parts takes one fp16 MMA per K step,
   //     the lo rows of the padded operand against the fp16 token rows (tensor map tmF), and
@@ -263,7 +267,7 @@ __device__ __forceinline__ Tile rows_m_tile(int e, int lm, int nt, const Params&
     const bool heavy = end - start >= p.f16_rows;
     if (p.f16_role == 1)
       tl.f16 = heavy ? 1 : 0;
-    else if (!heavy || f16_usable(e, p))
+    else if (p.f16_words[kF16Any] != 0u && (!heavy || f16_usable(e, p)))
       tl.kb_count = 0;  // refill: only the experts whose fp16 parts are unusable
   }
   return tl;
@@ -671,8 +675,8 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, const Tile& tl, in
     // fp16 tiles (tl.f16, experts with many rows): the lo rows receive fp16(dg 2^sg), fp16(du 2^sg)
     // and fp16(w h 2^sh) instead, the hi rows of w h are not written (five boxes per 16 columns),
     // and the largest scaled magnitudes go to the expert's range words.
-    constexpr bool kGated = EP == Epi::DH;
-    const bool f16 = kGated && tl.f16 != 0;
+    constexpr bool kGated = EP != Epi::DH1;
+    const bool f16 = EP == Epi::DH16 && tl.f16 != 0;
     float sg = 1.f;
     if (f16) {
       int sd = 0;
@@ -856,7 +860,7 @@ template <Sched S, Epi EP>
 __device__ __forceinline__ void prefetch_epilogue_operands(const Tile& tl, int row_local, int colhalf,
                                                            const Params& p) {
   if constexpr (dh_epi(EP)) {
-    constexpr int kFactors = EP == Epi::DH ? 2 : 1;  // [a | b] or a alone per row
+    constexpr int kFactors = EP != Epi::DH1 ? 2 : 1;  // [a | b] or a alone per row
     if (row_local >= tl.rows) return;
     const long long r = tl.m0 + row_local;
     const int n0 = tl.nt * BN + colhalf * (BN / 2);
@@ -1058,7 +1062,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                          : (G == Gather::A ? (A_MN && SPLIT != 1)
                                                                            : (B_MN && SPLIT != 2))),
                 "RowsM gathers a K-major A; RowsK gathers an MN-major operand held as one part");
-  if (p.f16_role == 2) {
+  if (p.f16_role == 1) {
+    // the fp16 dH pass: leave at once when no expert has f16 rows (the next launch is then the whole dH)
+    griddep_wait();
+    if (p.f16_words[kF16Any] == 0u) return;
+  }
+  if (p.f16_role == 2 && p.f16_words[kF16Any] != 0u) {
     // dH refill: leave at once (before any set-up) when no expert with f16 rows has unusable fp16
     // parts, which is the usual case; the range words are the previous kernel's output
     griddep_wait();
@@ -2092,16 +2101,20 @@ int launch_bwd_dh(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   // nothing (1161-1165 against 1163-1172 us on the Zipf 4096/1024 workload)
   if (a.f16_words == nullptr)
     return launch_gemm<Sched::RowsM, Epi::DH, false, true>(ta, tb, tc0, tc1, p, tiles, dev, s, "gemm_bwd_dh");
-  // fp16 weight-gradient operands: the experts with f16_rows rows write fp16 parts; then the
-  // refill pass writes hi / lo parts for those of them whose fp16 parts are unusable (usually none:
-  // its CTAs walk the tile order and leave)
+  // fp16 weight-gradient operands: when some expert has f16_rows rows (a device flag), the fp16 pass
+  // writes their fp16 parts and the hi / lo parts of the rest; the second launch then rewrites hi /
+  // lo parts for those whose fp16 parts are unusable (usually none: it leaves at once).  When no
+  // expert has them the first launch leaves at once and the second is the plain dH GEMM, whose
+  // kernel carries none of the fp16 code (with it, dH measured 7-9 % slower).  One traced interval.
+  KernelScope trace("gemm_bwd_dh", s);
   p.f16_rows = a.f16_rows;
   p.f16_words = a.f16_words;
   p.f16_role = 1;
-  if (int rc = launch_gemm<Sched::RowsM, Epi::DH, false, true>(ta, tb, tc0, tc1, p, tiles, dev, s, "gemm_bwd_dh"))
+  if (int rc = launch_gemm<Sched::RowsM, Epi::DH16, false, true>(ta, tb, tc0, tc1, p, tiles, dev, s, "gemm_bwd_dh",
+                                                                 false))
     return rc;
   p.f16_role = 2;
-  return launch_gemm<Sched::RowsM, Epi::DH, false, true>(ta, tb, tc0, tc1, p, tiles, dev, s, "gemm_bwd_dh_refill");
+  return launch_gemm<Sched::RowsM, Epi::DH, false, true>(ta, tb, tc0, tc1, p, tiles, dev, s, "gemm_bwd_dh", false);
 }
 
 int launch_bwd_dx(const BwdGemmArgs& a, const DeviceInfo& dev, cudaStream_t s) {

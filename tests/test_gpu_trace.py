@@ -2,8 +2,9 @@
 
 A GEMM that takes the heavy / light split (heavy experts as 2-SM pairs in one launch, the rest
 one CTA per tile in a second) is one traced interval holding two kernel launches, and so is a
-weight-gradient GEMM whose experts with many rows take the fp16 pass in a launch of their own;
-every other interval holds one.  A skewed batch of 8192 routed rows splits the forward GEMMs and
+weight-gradient GEMM whose experts with many rows take the fp16 pass in a launch of their own, and
+the dH GEMM of such a backward (its fp16 pass, then the refill or, with no such expert, the plain
+dH); every other interval holds one.  A skewed batch of 8192 routed rows splits the forward GEMMs and
 dX; a skewed batch of 32768 rows runs both weight-gradient GEMMs in an fp16 and a hi / lo launch;
 a small batch whose weight-gradient blocks pair up splits dW_down.  The bench's launch count is
 the sum.
@@ -33,7 +34,7 @@ def _step(wl, inp):
     (synthetic.Workload("split_zipf_T1024_H320_I192_E64_k8", 1024, 320, 192, 64, 8, zipf_s=1.2, router_std=0.05),
      {"gemm_gate_up_swiglu", "gemm_down_scale", "gemm_bwd_dx"}),
     (synthetic.Workload("f16_zipf_T4096_H320_I192_E64_k8", 4096, 320, 192, 64, 8, zipf_s=1.2, router_std=0.05),
-     {"gemm_bwd_dw_gate_up", "gemm_bwd_dw_down"}),
+     {"gemm_bwd_dh", "gemm_bwd_dw_gate_up", "gemm_bwd_dw_down"}),
     (synthetic.Workload("tiny_T256_H256_I128_E8_k2", 256, 256, 128, 8, 2), {"gemm_bwd_dw_down"}),
 ], ids=["skewed", "fp16", "small"])
 def test_trace_intervals_count_their_launches(wl, split):
