@@ -133,6 +133,15 @@ def gemm_bytes(wl, name: str, experts_used: int, gated: bool = True) -> int:
     }[name]
 
 
+def f16_pass_rows(counts, R: int, gated: bool, expert_major: bool) -> int:
+    """Routed rows of the experts that take the backward's fp16 weight-gradient pass, by the
+    library's rule: gated experts, expert-major inputs, a batch of at least 32768 routed rows, and
+    experts with at least 384 rows each.  0 when the pass does not apply."""
+    if not (gated and expert_major and R >= 32768):
+        return 0
+    return sum(int(c) for c in counts if c >= 384)
+
+
 def kernel_work(wl, name: str, gated: bool = True, f16_rows: int = 0):
     """(kind, algorithmic amount per launch): kind 'flop' for GEMMs, 'byte' for the rest.  f16_rows:
     routed rows of the experts that take the backward's fp16 weight-gradient pass (at least 384 rows
@@ -570,10 +579,7 @@ def run_ours(args, rank, world, local_rank):
     if flags:
         raise RuntimeError(f"device error flags {flags:#x} during warm-up")
     experts_used = int((dbuf["counts"] > 0).sum().item())  # experts whose weights the GEMMs read
-    # rows of the experts that take the backward's fp16 weight-gradient pass (the library's rule: gated
-    # experts, expert-major inputs, R >= 32768, experts with at least 384 rows)
-    counts_h = dbuf["counts"].cpu()
-    f16_rows = int(counts_h[counts_h >= 384].sum().item()) if gated and args.inputs != "gather" and wl.R >= 32768 else 0
+    f16_rows = f16_pass_rows(dbuf["counts"].cpu().tolist(), wl.R, gated, args.inputs != "gather")
 
     # ---------------- timed region: K steps, CUDA events on the launching stream
     # The K steps are captured once as a CUDA graph (the library's calls only enqueue work on

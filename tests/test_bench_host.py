@@ -97,3 +97,24 @@ def test_defaults_are_one_gpu_and_the_largest_workload(monkeypatch):
     assert a.warmup >= 3 and a.steps >= 1 and not a.router and not a.no_train_shape
     assert synthetic.workload(bench.TRAIN_SHAPE).as_dict() == dict(workload=bench.TRAIN_SHAPE, T=8192, H=2048, I=768,
                                                                    E=128, k=8)
+
+
+def test_fp16_pass_rows_follow_the_library_rule():
+    counts = [383, 384, 1000, 0, 5]
+    assert bench.f16_pass_rows(counts, 32768, True, True) == 1384
+    assert bench.f16_pass_rows(counts, 32767, True, True) == 0   # batch below 32768 routed rows
+    assert bench.f16_pass_rows(counts, 65536, False, True) == 0  # two-weight experts
+    assert bench.f16_pass_rows(counts, 65536, True, False) == 0  # token-major (gathered) inputs
+
+
+def test_fp16_row_copy_bytes():
+    wl = synthetic.workload("fwd_zipf_T8192_H4096_I1024_E512_k10")
+    T, H, R = wl.T, wl.H, wl.R
+    plain = bench.kernel_work(wl, "gather_rows")[1]
+    assert bench.kernel_work(wl, "gather_rows_f16", f16_rows=0)[1] == plain
+    assert bench.kernel_work(wl, "f16_prep", f16_rows=0)[1] == 0
+    f16_rows = 40000
+    # on top of the plain dY copy: one x row per token read, fp16 dY and x rows written for the heavy experts
+    extra = bench.kernel_work(wl, "gather_rows_f16", f16_rows=f16_rows)[1] - plain
+    assert extra == T * H * 2 + 2 * f16_rows * H * 2
+    assert bench.kernel_work(wl, "f16_prep", f16_rows=f16_rows)[1] >= 2 * T * H * 2  # |x| and |dY| maxima read
